@@ -1,0 +1,495 @@
+"""Pins of the fp64 oracle against facts fixed outside it.
+
+Each test checks the oracle against something other than itself: values the
+MX specification prints (E2M1 table, E8M0 definition), library conversions
+(numpy float16, torch bfloat16), brute force on tiny inputs, closed forms, and
+special cases that reduce to library routines (numpy matmul, scipy expit).
+They are chosen so that a plausible slip (swapped nibbles, transposed weight,
+swapped gate/up, wrong slot weight, a dropped bias) fails at least one.
+"""
+import itertools
+import math
+from fractions import Fraction
+from types import SimpleNamespace
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import expit, softmax
+
+import oracle
+from oracle import FMT_INT4, FMT_MXFP4
+
+import os
+
+
+def _load_e2m1_table():
+    """OCP MX v1.0 FP4 (E2M1) values by encoding, from tests/golden/e2m1_table.txt"""
+    path = os.path.join(os.path.dirname(__file__), "golden", "e2m1_table.txt")
+    vals = {}
+    for line in open(path):
+        if line.strip() and not line.startswith("#"):
+            c, v = line.split()
+            vals[int(c)] = float(v)
+    return [vals[c] for c in range(16)]
+
+
+E2M1_TABLE = _load_e2m1_table()
+
+
+def test_e2m1_table():
+    for code, v in enumerate(E2M1_TABLE):
+        got = oracle.e2m1(code)
+        assert got == v and math.copysign(1, got) == math.copysign(1, v), code
+
+
+def test_e8m0_values():
+    assert oracle.e8m0(127) == 1.0
+    assert oracle.e8m0(128) == 2.0
+    assert oracle.e8m0(126) == 0.5
+    assert oracle.e8m0(117) == 1.0 / 1024
+    assert oracle.e8m0(124) == 0.125
+    assert oracle.e8m0(0) == float.fromhex("0x1p-127")
+    assert oracle.e8m0(254) == float.fromhex("0x1p127")
+    assert math.isnan(oracle.e8m0(255))
+    for e in range(254):
+        assert oracle.e8m0(e + 1) == 2 * oracle.e8m0(e)
+
+
+def _pack(codes):
+    """pack a list of 4-bit codes, element 2b in the low nibble of byte b"""
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[0::2] | (c[1::2] << 4)).astype(np.uint8)
+
+
+def test_dequant_all_code_scale_pairs():
+    # brute force over every (code, E8M0) pair: one 32-wide row per scale byte
+    codes = np.array([c % 16 for c in range(32)], dtype=np.uint8)
+    N = 255
+    packed = np.tile(_pack(codes), (N, 1))
+    scales = np.arange(N, dtype=np.uint8).reshape(N, 1)
+    W = oracle.dequant(FMT_MXFP4, packed, scales, N, 32)
+    for e in range(N):
+        for k in range(32):
+            assert W[e, k] == E2M1_TABLE[k % 16] * 2.0 ** (e - 127)
+
+
+def test_dequant_hand_block_and_nibble_order():
+    # byte 0x21: element 0 = code 1 (0.5), element 1 = code 2 (1.0)
+    packed = np.full((1, 16), 0x21, dtype=np.uint8)
+    W = oracle.dequant(FMT_MXFP4, packed, np.array([[127]], np.uint8), 1, 32)
+    assert list(W[0, :4]) == [0.5, 1.0, 0.5, 1.0]
+    # two blocks with different scales: the scale index follows k // 32
+    packed = np.full((1, 32), 0x77, dtype=np.uint8)     # all +6
+    W = oracle.dequant(FMT_MXFP4, packed, np.array([[126, 129]], np.uint8), 1, 64)
+    assert np.all(W[0, :32] == 3.0) and np.all(W[0, 32:] == 24.0)
+    # rows: row n uses scales row n
+    packed = np.full((2, 16), 0x22, dtype=np.uint8)     # all +1
+    W = oracle.dequant(FMT_MXFP4, packed, np.array([[127], [130]], np.uint8), 2, 32)
+    assert np.all(W[0] == 1.0) and np.all(W[1] == 8.0)
+
+
+def test_fp16_all_bit_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.fp16(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_bf16_all_bit_patterns():
+    bits = np.arange(65536, dtype=np.int32).astype(np.int16)
+    ref = torch.from_numpy(bits).view(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.bf16_array(bits.view(np.uint16))
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_to_bf16_matches_torch_on_fp32():
+    rng = np.random.default_rng(5)
+    v = np.concatenate([rng.standard_normal(20000).astype(np.float32),
+                        (rng.standard_normal(2000) * 1e-38).astype(np.float32),
+                        rng.uniform(-3.3e38, 3.3e38, 2000).astype(np.float32),
+                        np.array([0.0, -0.0, 1.0, 1.00390625, 1.01171875], np.float32)])
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.to_bf16_array(v.astype(np.float64))
+    assert np.array_equal(got, ref)
+
+
+def _nearest_bf16_bruteforce(x: float) -> int:
+    """nearest bf16 to an fp64 value by exact comparison of the two neighbours"""
+    f32 = np.float32(x)   # not used for the answer, only to find the binade
+    cands = set()
+    b = int(torch.tensor([float(f32)], dtype=torch.float32).to(torch.bfloat16)
+            .view(torch.int16).item()) & 0xFFFF
+    for d in range(-2, 3):
+        c = (b + d) & 0xFFFF
+        if (c & 0x7F80) != 0x7F80:
+            cands.add(c)
+    X = Fraction(x)
+    best = None
+    for c in sorted(cands):
+        v = Fraction(oracle.bf16(c))
+        if (c >> 15) != (0 if x >= 0 else 1) and v != 0:
+            continue
+        d = abs(v - X)
+        if best is None or d < best[0] or (d == best[0] and (c & 1) == 0):
+            best = (d, c)
+    return best[1]
+
+
+def test_to_bf16_fp64_ties_and_bruteforce():
+    # exact ties between two bf16 neighbours go to the even fraction
+    assert oracle.to_bf16(1.0 + 2.0 ** -8) == 0x3F80         # 1.0 (even) wins
+    assert oracle.to_bf16(1.0 + 3 * 2.0 ** -8) == 0x3F82     # 1+2^-6 (even) wins
+    assert oracle.to_bf16(1.0 + 2.0 ** -8 + 2.0 ** -40) == 0x3F81   # just above the tie
+    assert oracle.to_bf16(2.0 ** 128) == 0x7F80
+    assert oracle.to_bf16(-(2.0 ** -140)) == 0x8000          # underflows to -0
+    assert oracle.to_bf16(2.0 ** -133) == 0x0001             # smallest subnormal
+    rng = np.random.default_rng(7)
+    for x in rng.standard_normal(300) * np.exp(rng.uniform(-20, 20, 300)):
+        assert oracle.to_bf16(float(x)) == _nearest_bf16_bruteforce(float(x)), x
+
+
+def test_int4_decode_special_codes():
+    s = np.float16(0.0234).view(np.uint16)
+    sv = float(np.float16(0.0234))
+    codes = _pack([8, 0, 15, 9] * 16)                      # 64 elements, one group
+    W = oracle.dequant(FMT_INT4, codes.reshape(1, -1), np.array([[s]], np.uint16), 1, 64, 64)
+    assert W[0, 0] == 0.0 and W[0, 1] == -8 * sv and W[0, 2] == 7 * sv and W[0, 3] == sv
+    # group index follows k // 64
+    codes = _pack([15] * 128).reshape(1, -1)
+    sc = np.array([[np.float16(1.0).view(np.uint16), np.float16(-0.5).view(np.uint16)]])
+    W = oracle.dequant(FMT_INT4, codes, sc, 1, 128, 64)
+    assert np.all(W[0, :64] == 7.0) and np.all(W[0, 64:] == -3.5)
+
+
+# ---------------------------------------------------------------- router
+
+def test_route_bruteforce_subsets():
+    rng = np.random.default_rng(11)
+    for E, k in [(4, 2), (6, 3), (8, 2), (5, 5), (7, 1)]:
+        logits = rng.standard_normal((20, E)).astype(np.float32)
+        idx, w = oracle.route(logits, k)
+        for m in range(20):
+            best = max(itertools.combinations(range(E), k),
+                       key=lambda S: sum(float(logits[m, e]) for e in S))
+            assert sorted(idx[m]) == sorted(best)
+            vals = logits[m, idx[m]]
+            assert np.all(np.diff(vals) <= 0)             # descending selection order
+            ref = softmax(vals.astype(np.float64))
+            assert np.allclose(w[m], ref, rtol=1e-14, atol=0)
+            assert abs(w[m].sum() - 1.0) < 1e-15
+
+
+def test_route_ties_and_nan():
+    logits = np.zeros((1, 8), np.float32)
+    idx, w = oracle.route(logits, 3)
+    assert list(idx[0]) == [0, 1, 2] and np.allclose(w[0], 1 / 3)
+    logits = np.array([[1.0, 2.0, 2.0, -1.0, 2.0]], np.float32)
+    idx, _ = oracle.route(logits, 2)
+    assert list(idx[0]) == [1, 2]
+    logits = np.array([[np.nan, 0.5, -3.0, np.nan]], np.float32)
+    idx, w = oracle.route(logits, 2)
+    assert list(idx[0]) == [1, 2]
+    assert abs(w[0, 0] - expit(3.5)) < 1e-15
+
+
+def test_route_permutation_invariance():
+    rng = np.random.default_rng(3)
+    logits = rng.standard_normal((10, 32)).astype(np.float32)
+    perm = rng.permutation(32)
+    idx, w = oracle.route(logits, 4)
+    idx2, w2 = oracle.route(logits[:, perm], 4)
+    assert np.array_equal(perm[idx2], idx)
+    assert np.array_equal(w2, w)
+
+
+# ---------------------------------------------------------------- layer
+
+def _rand_layer(rng, H, I, E, fmt=FMT_MXFP4, group=32, bias=True, e_lo=119, e_hi=123):
+    bs = 32 if fmt == FMT_MXFP4 else group
+
+    def scales(n):
+        if fmt == FMT_MXFP4:
+            return rng.integers(e_lo, e_hi + 1, n, dtype=np.uint8)
+        return np.abs(rng.normal(0, 0.05, n)).astype(np.float16).view(np.uint16)
+
+    t = SimpleNamespace(
+        gu_codes=rng.integers(0, 256, (E, 2 * I, H // 2), dtype=np.uint8),
+        gu_scales=scales(E * 2 * I * (H // bs)).reshape(E, 2 * I, H // bs),
+        gu_bias=(torch.randn(E, 2 * I, generator=torch.Generator().manual_seed(int(rng.integers(1 << 30))))
+                 .to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16) if bias else None),
+        dn_codes=rng.integers(0, 256, (E, H, I // 2), dtype=np.uint8),
+        dn_scales=scales(E * H * (I // bs)).reshape(E, H, I // bs),
+        dn_bias=(torch.randn(E, H, generator=torch.Generator().manual_seed(int(rng.integers(1 << 30))))
+                 .to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16) if bias else None),
+    )
+    return t
+
+
+def _bf16_bits(v):
+    return torch.from_numpy(np.asarray(v, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _bf16_val(bits):
+    return torch.from_numpy(np.asarray(bits, np.uint16).view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+
+
+def _dense_expert(t, e, fmt, H, I, group, xv):
+    """one expert's MLP with numpy matmul on oracle-dequantised (pinned) matrices"""
+    Wgu = oracle.dequant(fmt, t.gu_codes[e], t.gu_scales[e], 2 * I, H, group)
+    Wd = oracle.dequant(fmt, t.dn_codes[e], t.dn_scales[e], H, I, group)
+    bgu = _bf16_val(t.gu_bias[e]) if t.gu_bias is not None else 0.0
+    bd = _bf16_val(t.dn_bias[e]) if t.dn_bias is not None else 0.0
+    a = Wgu @ xv + bgu
+    g, u = a[:I], a[I:]
+    h = g * expit(g) * u
+    return Wd @ h + bd
+
+
+@pytest.mark.parametrize("fmt,group", [(FMT_MXFP4, 32), (FMT_INT4, 64)])
+def test_layer_one_hot_equals_dense_mlp(fmt, group):
+    rng = np.random.default_rng(21)
+    H, I, E = 128, 192, 4                                   # non-square: catches transposes
+    t = _rand_layer(rng, H, I, E, fmt, group)
+    x = _bf16_bits(rng.standard_normal((3, H)))
+    r = _bf16_bits(rng.standard_normal((3, H)))
+    logits = rng.standard_normal((3, E)).astype(np.float32)
+    out, idx, w = oracle.layer(fmt, H, I, E, 1, t, x, logits, r, group=group)
+    assert np.all(w == 1.0)
+    for m in range(3):
+        e = int(np.argmax(logits[m]))
+        assert idx[m, 0] == e
+        ref = _bf16_val(r[m]) + _dense_expert(t, e, fmt, H, I, group, _bf16_val(x[m]))
+        assert np.allclose(out[m], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def test_layer_is_weighted_sum_of_single_experts():
+    rng = np.random.default_rng(22)
+    H, I, E, k = 64, 96, 6, 3
+    t = _rand_layer(rng, H, I, E)
+    x = _bf16_bits(rng.standard_normal((2, H)))
+    r = _bf16_bits(rng.standard_normal((2, H)))
+    logits = rng.standard_normal((2, E)).astype(np.float32)
+    out, idx, w = oracle.layer(FMT_MXFP4, H, I, E, k, t, x, logits, r)
+    for m in range(2):
+        acc = _bf16_val(r[m]).copy()
+        for s in range(k):
+            acc += w[m, s] * _dense_expert(t, idx[m, s], FMT_MXFP4, H, I, 32, _bf16_val(x[m]))
+        assert np.allclose(out[m], acc, rtol=1e-12, atol=1e-12 * np.abs(acc).max())
+
+
+def test_layer_down_scale_exponent_plus_one_doubles_exactly():
+    rng = np.random.default_rng(23)
+    H, I, E, k = 64, 64, 4, 2
+    t = _rand_layer(rng, H, I, E)
+    t.dn_bias = None
+    x = _bf16_bits(rng.standard_normal((2, H)))
+    logits = rng.standard_normal((2, E)).astype(np.float32)
+    out1, _, _ = oracle.layer(FMT_MXFP4, H, I, E, k, t, x, logits, None)
+    t.dn_scales = (t.dn_scales + 1).astype(np.uint8)
+    out2, _, _ = oracle.layer(FMT_MXFP4, H, I, E, k, t, x, logits, None)
+    assert np.array_equal(out2, 2 * out1)
+
+
+def test_layer_zero_codes_closed_form():
+    rng = np.random.default_rng(24)
+    H, I, E, k = 64, 32, 4, 2
+    t = _rand_layer(rng, H, I, E)
+    t.gu_codes[:] = 0
+    t.dn_codes[:] = 0
+    x = _bf16_bits(rng.standard_normal((1, H)))
+    r = _bf16_bits(rng.standard_normal((1, H)))
+    logits = rng.standard_normal((1, E)).astype(np.float32)
+    out, idx, w = oracle.layer(FMT_MXFP4, H, I, E, k, t, x, logits, r)
+    ref = _bf16_val(r[0]) + sum(w[0, s] * _bf16_val(t.dn_bias[idx[0, s]]) for s in range(k))
+    assert np.allclose(out[0], ref, rtol=1e-15, atol=0)
+
+
+def test_layer_gate_up_orientation():
+    # gate rows constant (codes 0, bias c) -> h = silu(c) * (W_up x + b_up)
+    rng = np.random.default_rng(25)
+    H, I, E = 64, 32, 2
+    t = _rand_layer(rng, H, I, E)
+    t.gu_codes[:, :I, :] = 0
+    c = 1.25
+    t.gu_bias[:, :I] = _bf16_bits(np.full(I, c))
+    x = _bf16_bits(rng.standard_normal((1, H)))
+    logits = np.array([[1.0, 0.0]], np.float32)
+    out, _, _ = oracle.layer(FMT_MXFP4, H, I, E, 1, t, x, logits, None)
+    Wu = oracle.dequant(FMT_MXFP4, t.gu_codes[0, I:], t.gu_scales[0, I:], I, H)
+    Wd = oracle.dequant(FMT_MXFP4, t.dn_codes[0], t.dn_scales[0], H, I)
+    up = Wu @ _bf16_val(x[0]) + _bf16_val(t.gu_bias[0, I:])
+    ref = Wd @ (c * expit(c) * up) + _bf16_val(t.dn_bias[0])
+    assert np.allclose(out[0], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+# ---------------------------------------------------------------- stack
+
+def test_stack_zero_layers_and_zero_weights():
+    rng = np.random.default_rng(31)
+    H, I, E, k = 64, 32, 4, 2
+    r0 = _bf16_bits(rng.standard_normal((2, H)))
+    t = _rand_layer(rng, H, I, E)
+    t.gu_codes[:] = 0
+    t.dn_codes[:] = 0
+    t.gu_bias[:] = 0
+    t.dn_bias[:] = 0
+    logits = rng.standard_normal((3, 2, E)).astype(np.float32)
+    assert np.array_equal(oracle.stack(FMT_MXFP4, H, I, E, k, [t] * 3, logits, r0), r0)
+    assert np.array_equal(oracle.stack(FMT_MXFP4, H, I, E, k, [], logits[:0], r0), r0)
+
+
+def test_stack_bias_only_closed_form():
+    # with zero codes and zero gate bias, h = 0 and each layer adds sum_s w_s b_d
+    rng = np.random.default_rng(32)
+    H, I, E, k = 64, 32, 4, 2
+    t = _rand_layer(rng, H, I, E)
+    t.gu_codes[:] = 0
+    t.dn_codes[:] = 0
+    t.gu_bias[:] = 0
+    r = _bf16_bits(rng.standard_normal((1, H)))
+    logits = rng.standard_normal((2, 1, E)).astype(np.float32)
+    got = oracle.stack(FMT_MXFP4, H, I, E, k, [t, t], logits, r)
+    ref = r.copy()
+    for l in range(2):
+        idx, w = oracle.route(logits[l], k)
+        add = sum(w[0, s] * _bf16_val(t.dn_bias[idx[0, s]]) for s in range(k))
+        ref = np.array([oracle.to_bf16(v) for v in _bf16_val(ref[0]) + add], np.uint16)[None]
+    assert np.array_equal(got, ref)
+
+
+def test_stack_composes_layer_by_layer():
+    rng = np.random.default_rng(33)
+    H, I, E, k = 64, 32, 4, 2
+    ts = [_rand_layer(rng, H, I, E) for _ in range(3)]
+    r = _bf16_bits(rng.standard_normal((2, H)))
+    logits = rng.standard_normal((3, 2, E)).astype(np.float32)
+    whole = oracle.stack(FMT_MXFP4, H, I, E, k, ts, logits, r)
+    step = r
+    for l in range(3):
+        step = oracle.stack(FMT_MXFP4, H, I, E, k, [ts[l]], logits[l:l + 1], step)
+    assert np.array_equal(whole, step)
+
+
+def test_stack_one_layer_matches_layer_on_normalised_input():
+    # r1 = bf16(r0 + MoE(x0)); x0 is bf16 of r0 scaled by a positive per-token
+    # factor, which the layer call receives as its x; the residual add and
+    # rounding then have to agree with the layer oracle plus to_bf16.
+    rng = np.random.default_rng(34)
+    H, I, E, k = 64, 32, 4, 2
+    t = _rand_layer(rng, H, I, E)
+    r0 = _bf16_bits(rng.standard_normal((1, H)) * 3.0)
+    logits = rng.standard_normal((1, 1, E)).astype(np.float32)
+    got = oracle.stack(FMT_MXFP4, H, I, E, k, [t], logits, r0)
+    rv = _bf16_val(r0[0])
+    x0 = _bf16_bits(rv / np.sqrt(np.mean(rv * rv) + 1e-6))
+    out, _, _ = oracle.layer(FMT_MXFP4, H, I, E, k, t, x0, logits[0], r0)
+    ref = np.array([oracle.to_bf16(v) for v in out[0]], np.uint16)
+    assert np.array_equal(got[0], ref)
+
+
+# ---------------------------------------------------------------- MX quantiser
+
+GRID = np.array(sorted(set(abs(v) for v in E2M1_TABLE)))
+
+
+def test_mx_quantize_scale_examples():
+    for amax, byte in [(1.0, 125), (6.0, 127), (0.75, 124), (7.99, 127), (8.0, 128), (2.0 ** -130, 0)]:
+        v = np.zeros(32)
+        v[5] = amax
+        _, s = oracle.mx_quantize(v)
+        assert s[0] == byte, (amax, s[0])
+    _, s = oracle.mx_quantize(np.zeros(32))
+    assert s[0] == 0
+
+
+def test_mx_quantize_grid_roundtrip_is_identity():
+    rng = np.random.default_rng(41)
+    for X in [-10, -3, 0, 5]:
+        codes = rng.integers(0, 16, 32)
+        codes[0] = 7                                    # amax = 6 * 2^X sets the exponent
+        v = np.array([E2M1_TABLE[c] for c in codes]) * 2.0 ** X
+        qc, qs = oracle.mx_quantize(v)
+        assert qs[0] == X + 127
+        dq = oracle.dequant(FMT_MXFP4, qc.reshape(1, -1), qs.reshape(1, 1), 1, 32)[0]
+        assert np.array_equal(dq, v)
+
+
+def test_mx_quantize_nearest_even_bruteforce():
+    rng = np.random.default_rng(42)
+    v = rng.standard_normal((200, 32)) * np.exp(rng.uniform(-5, 5, (200, 1)))
+    v[0, :8] = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 4.0]   # exact ties at X = 0
+    v[0, 8] = -4.0
+    for row in v:
+        qc, qs = oracle.mx_quantize(row)
+        X = int(qs[0]) - 127
+        assert X == math.floor(math.log2(np.abs(row).max())) - 2
+        dq = oracle.dequant(FMT_MXFP4, qc.reshape(1, -1), qs.reshape(1, 1), 1, 32)[0]
+        for val, got in zip(row, dq):
+            a = abs(val) / 2.0 ** X
+            d = np.abs(GRID - a)
+            cand = np.flatnonzero(d == d.min())
+            # ties: the even mantissa (grid index even <=> mantissa bit 0)
+            pick = cand[0] if len(cand) == 1 else [c for c in cand if c % 2 == 0][0]
+            want = math.copysign(GRID[pick] * 2.0 ** X, val)
+            assert got == want, (val, got, want)
+    # element values at amax saturate to 6 * 2^X
+    row = np.zeros(32)
+    row[3] = 7.5
+    qc, qs = oracle.mx_quantize(row)
+    assert qs[0] == 127 and (qc[1] >> 4) == 7
+
+
+def test_batched_layer_closed_form_through_quantised_h():
+    # gate rows constant 100 (silu(100) == 100 in fp64) so h = 100 * up;
+    # up rows constant too (codes 0) so h = 100 * b_up independent of x.
+    rng = np.random.default_rng(43)
+    H, I, E, k = 64, 64, 3, 2
+    t = _rand_layer(rng, H, I, E, e_lo=120, e_hi=126)
+    t.gu_codes[:] = 0
+    t.gu_bias[:, :I] = _bf16_bits(np.full(I, 100.0))
+    x = _bf16_bits(rng.standard_normal((2, H)))
+    r = _bf16_bits(rng.standard_normal((2, H)))
+    logits = rng.standard_normal((2, E)).astype(np.float32)
+    out, hc, hs = oracle.layer_batched(H, I, E, k, t, x, logits, r, want_h=True)
+    idx, w = oracle.route(logits, k)
+    for m in range(2):
+        acc = _bf16_val(r[m]).copy()
+        for s in range(k):
+            e = idx[m, s]
+            h = 100.0 * _bf16_val(t.gu_bias[e, I:])
+            qc, qs = oracle.mx_quantize(h)
+            assert np.array_equal(qc, hc[m, s]) and np.array_equal(qs, hs[m, s])
+            hq = oracle.dequant(FMT_MXFP4, qc.reshape(1, -1), qs.reshape(1, -1), 1, I)[0]
+            Wd = oracle.dequant(FMT_MXFP4, t.dn_codes[e], t.dn_scales[e], H, I)
+            acc += w[m, s] * (Wd @ hq + _bf16_val(t.dn_bias[e]))
+        assert np.allclose(out[m], acc, rtol=1e-12, atol=1e-12 * np.abs(acc).max())
+
+
+def test_batched_equals_decode_when_x_on_grid_and_h_given():
+    # x already on the MX grid: the batched gate_up stage sees x unchanged.
+    # Feeding h_q through h_codes_in then fixes the down stage; compare with a
+    # dense numpy evaluation on the same quantised h.
+    rng = np.random.default_rng(44)
+    H, I, E, k = 64, 64, 3, 1
+    t = _rand_layer(rng, H, I, E)
+    codes = rng.integers(0, 16, H)
+    xv = np.array([E2M1_TABLE[c] for c in codes]) * 0.25
+    x = _bf16_bits(xv)[None]
+    logits = rng.standard_normal((1, E)).astype(np.float32)
+    hcodes = rng.integers(0, 256, (1, k, I // 2), dtype=np.uint8)
+    hscales = rng.integers(120, 125, (1, k, I // 32), dtype=np.uint8)
+    out = oracle.layer_batched(H, I, E, k, t, x, logits, None, h_codes_in=hcodes, h_scales_in=hscales)
+    e = int(np.argmax(logits[0]))
+    hq = oracle.dequant(FMT_MXFP4, hcodes[0], hscales[0], 1, I)[0]
+    Wd = oracle.dequant(FMT_MXFP4, t.dn_codes[e], t.dn_scales[e], H, I)
+    ref = Wd @ hq + _bf16_val(t.dn_bias[e])
+    assert np.allclose(out[0], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    # and the decode oracle with the same x differs from it only through h
+    out_dec, _, _ = oracle.layer(FMT_MXFP4, H, I, E, k, t, x, logits, None)
+    assert out_dec.shape == out.shape
