@@ -1,0 +1,535 @@
+// moe_api.cu -- the C ABI declared in include/moe.h: handle, argument checks,
+// resident weight arena, workspace, launch of the decode kernels and the
+// cached CUDA graph of the expert stack.
+//
+// All tables the kernels need are fixed at moe_create / moe_load_experts; a
+// forward call does no host-side work that depends on the routing (the pages'
+// lesson: per-token host setup once cost 10.65 ms of a 36.95 ms token,
+// "Amortizing the per-token host-sync setup tax ...", section 3), and it
+// allocates nothing (the grow-only buffer cache that reallocated on every
+// count change, TinyTitan tracker D114).
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/moe.h"
+#include "moe_internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what)
+{
+    return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct StackGraph {
+    int M = 0, k = 0;
+    const void* resid = nullptr;
+    const void* logits = nullptr;
+    cudaGraphExec_t exec = nullptr;
+};
+
+}  // namespace
+
+struct moe_handle {
+    moe_config cfg{};
+    int device = 0;
+    int num_sms = 0;
+    // per-layer tensor sizes in bytes (one layer, all experts)
+    size_t gu_codes_b = 0, gu_scales_b = 0, gu_bias_b = 0;
+    size_t dn_codes_b = 0, dn_scales_b = 0, dn_bias_b = 0;
+    size_t layer_stride = 0;
+    size_t off_gu_scales = 0, off_gu_bias = 0, off_dn_codes = 0, off_dn_scales = 0, off_dn_bias = 0;
+    int sbh = 0, sbi = 0;
+    uint8_t* arena = nullptr;
+    std::vector<char> loaded;
+    // workspace
+    float* h = nullptr;
+    float* ypart = nullptr;
+    unsigned int* tile_count = nullptr;
+    int* stats = nullptr;   // distinct experts per layer of the last call
+    int* status = nullptr;
+    // staging for moe_forward_host
+    uint16_t* st_x = nullptr;
+    uint16_t* st_out = nullptr;
+    float* st_logits = nullptr;
+    // stack graphs
+    cudaStream_t capture_stream = nullptr;
+    std::vector<StackGraph> graphs;
+    int last_layers = 0;       // layers touched by the last forward call
+    int last_first_layer = 0;
+    int last_launches = 0;
+};
+
+namespace {
+
+int check_cfg(const moe_config* c)
+{
+    if (!c)
+        return fail(MOE_ERR_INVALID_ARG, "moe_create: cfg is NULL");
+    if (c->hidden <= 0 || c->hidden % 32 || c->hidden > moe::kMaxK)
+        return fail(MOE_ERR_INVALID_ARG, "hidden=%d must be a positive multiple of 32, <= %d",
+                    c->hidden, moe::kMaxK);
+    if (c->intermediate <= 0 || c->intermediate % 32 || c->intermediate > moe::kMaxK)
+        return fail(MOE_ERR_INVALID_ARG, "intermediate=%d must be a positive multiple of 32, <= %d",
+                    c->intermediate, moe::kMaxK);
+    if (c->num_experts < 1 || c->num_experts > moe::kMaxExperts)
+        return fail(MOE_ERR_INVALID_ARG, "num_experts=%d must be in 1..%d", c->num_experts,
+                    moe::kMaxExperts);
+    if (c->num_layers < 1)
+        return fail(MOE_ERR_INVALID_ARG, "num_layers=%d must be >= 1", c->num_layers);
+    if (c->max_tokens < 1 || c->max_tokens > moe::kMaxTokens)
+        return fail(MOE_ERR_INVALID_ARG, "max_tokens=%d must be in 1..%d", c->max_tokens,
+                    moe::kMaxTokens);
+    if (c->max_top_k < 1 || c->max_top_k > moe::kMaxTopK || c->max_top_k > c->num_experts)
+        return fail(MOE_ERR_INVALID_ARG, "max_top_k=%d must be in 1..min(num_experts, %d)",
+                    c->max_top_k, moe::kMaxTopK);
+    if (c->format == MOE_FMT_MXFP4) {
+        if (c->group != 32)
+            return fail(MOE_ERR_INVALID_ARG, "MXFP4 needs group == 32 (got %d)", c->group);
+    } else if (c->format == MOE_FMT_INT4) {
+        if (c->group < 32 || c->group % 32 || c->hidden % c->group || c->intermediate % c->group)
+            return fail(MOE_ERR_INVALID_ARG,
+                        "int4 group=%d must be a multiple of 32 dividing hidden and intermediate",
+                        c->group);
+    } else {
+        return fail(MOE_ERR_INVALID_ARG, "format=%d is neither MOE_FMT_MXFP4 nor MOE_FMT_INT4",
+                    c->format);
+    }
+    if (c->has_bias != 0 && c->has_bias != 1)
+        return fail(MOE_ERR_INVALID_ARG, "has_bias must be 0 or 1");
+    return MOE_OK;
+}
+
+void free_handle(moe_handle* h)
+{
+    if (!h)
+        return;
+    for (auto& g : h->graphs)
+        if (g.exec)
+            cudaGraphExecDestroy(g.exec);
+    if (h->capture_stream)
+        cudaStreamDestroy(h->capture_stream);
+    cudaFree(h->arena);
+    cudaFree(h->h);
+    cudaFree(h->ypart);
+    cudaFree(h->tile_count);
+    cudaFree(h->stats);
+    cudaFree(h->status);
+    cudaFree(h->st_x);
+    cudaFree(h->st_out);
+    cudaFree(h->st_logits);
+    delete h;
+}
+
+template <typename T>
+int dev_alloc(T** p, size_t bytes, const char* what)
+{
+    cudaError_t e = cudaMalloc((void**)p, bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *p = nullptr;
+        return fail(MOE_ERR_OOM, "cudaMalloc(%zu bytes) for %s failed: %s", bytes, what,
+                    cudaGetErrorString(e));
+    }
+    return MOE_OK;
+}
+
+moe::LayerParams layer_params(const moe_handle* h, int layer)
+{
+    const moe_config& c = h->cfg;
+    const uint8_t* base = h->arena + (size_t)layer * h->layer_stride;
+    moe::LayerParams p{};
+    p.gu_codes = base;
+    p.gu_scales = base + h->off_gu_scales;
+    p.gu_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(base + h->off_gu_bias) : nullptr;
+    p.dn_codes = base + h->off_dn_codes;
+    p.dn_scales = base + h->off_dn_scales;
+    p.dn_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(base + h->off_dn_bias) : nullptr;
+    p.h = h->h;
+    p.ypart = h->ypart;
+    p.tile_count = h->tile_count;
+    p.nu_out = h->stats + layer;
+    p.H = c.hidden;
+    p.I = c.intermediate;
+    p.E = c.num_experts;
+    p.kmax = c.max_top_k;
+    p.group = c.group;
+    p.sbh = h->sbh;
+    p.sbi = h->sbi;
+    return p;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb)
+{
+    auto pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + nb && pb < pa + na;
+}
+
+int check_forward_args(const moe_handle* h, int M, int top_k)
+{
+    if (!h)
+        return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
+    if (M < 1 || M > h->cfg.max_tokens)
+        return fail(MOE_ERR_INVALID_ARG, "M=%d must be in 1..max_tokens=%d", M, h->cfg.max_tokens);
+    if (top_k < 1 || top_k > h->cfg.max_top_k)
+        return fail(MOE_ERR_INVALID_ARG, "top_k=%d must be in 1..max_top_k=%d", top_k,
+                    h->cfg.max_top_k);
+    return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_last_error(void) { return g_err; }
+
+int moe_create(const moe_config* cfg, moe_handle** out)
+{
+    if (!out)
+        return fail(MOE_ERR_INVALID_ARG, "moe_create: out is NULL");
+    *out = nullptr;
+    int rc = check_cfg(cfg);
+    if (rc != MOE_OK)
+        return rc;
+    moe_handle* h = new (std::nothrow) moe_handle();
+    if (!h)
+        return fail(MOE_ERR_OOM, "host allocation failed");
+    h->cfg = *cfg;
+    const moe_config& c = h->cfg;
+    const size_t H = c.hidden, I = c.intermediate, E = c.num_experts;
+    h->sbh = c.format == MOE_FMT_MXFP4 ? (int)(H / 32) : (int)(2 * H / c.group);
+    h->sbi = c.format == MOE_FMT_MXFP4 ? (int)(I / 32) : (int)(2 * I / c.group);
+    h->gu_codes_b = E * 2 * I * H / 2;
+    h->gu_scales_b = E * 2 * I * h->sbh;
+    h->gu_bias_b = c.has_bias ? E * 2 * I * 2 : 0;
+    h->dn_codes_b = E * H * I / 2;
+    h->dn_scales_b = E * H * h->sbi;
+    h->dn_bias_b = c.has_bias ? E * H * 2 : 0;
+    size_t off = align_up(h->gu_codes_b, 256);
+    h->off_gu_scales = off;
+    off = align_up(off + h->gu_scales_b, 256);
+    h->off_gu_bias = off;
+    off = align_up(off + h->gu_bias_b, 256);
+    h->off_dn_codes = off;
+    off = align_up(off + h->dn_codes_b, 256);
+    h->off_dn_scales = off;
+    off = align_up(off + h->dn_scales_b, 256);
+    h->off_dn_bias = off;
+    off = align_up(off + h->dn_bias_b, 256);
+    h->layer_stride = off;
+
+    cudaError_t e = cudaGetDevice(&h->device);
+    if (e != cudaSuccess) {
+        free_handle(h);
+        return cuda_fail(e, "cudaGetDevice");
+    }
+    e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+    if (e != cudaSuccess) {
+        free_handle(h);
+        return cuda_fail(e, "cudaDeviceGetAttribute");
+    }
+    const size_t Mx = c.max_tokens, Kx = c.max_top_k;
+    if ((rc = dev_alloc(&h->arena, h->layer_stride * c.num_layers, "expert weights")) ||
+        (rc = dev_alloc(&h->h, Mx * Kx * I * sizeof(float), "h workspace")) ||
+        (rc = dev_alloc(&h->ypart, Mx * Kx * H * sizeof(float), "y workspace")) ||
+        (rc = dev_alloc(&h->tile_count, (H / moe::kRowsPerItem) * sizeof(unsigned), "tile counters")) ||
+        (rc = dev_alloc(&h->stats, c.num_layers * sizeof(int), "stats")) ||
+        (rc = dev_alloc(&h->status, sizeof(int), "status")) ||
+        (rc = dev_alloc(&h->st_x, Mx * H * 2, "staging x")) ||
+        (rc = dev_alloc(&h->st_out, Mx * H * 2, "staging out")) ||
+        (rc = dev_alloc(&h->st_logits, Mx * E * sizeof(float), "staging logits"))) {
+        free_handle(h);
+        return rc;
+    }
+    if ((e = cudaMemset(h->tile_count, 0, (H / moe::kRowsPerItem) * sizeof(unsigned))) != cudaSuccess ||
+        (e = cudaMemset(h->stats, 0, c.num_layers * sizeof(int))) != cudaSuccess ||
+        (e = cudaMemset(h->status, 0, sizeof(int))) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&h->capture_stream, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaDeviceSynchronize()) != cudaSuccess) {
+        free_handle(h);
+        return cuda_fail(e, "moe_create setup");
+    }
+    h->loaded.assign(c.num_layers, 0);
+    *out = h;
+    g_err[0] = 0;
+    return MOE_OK;
+}
+
+void moe_destroy(moe_handle* h)
+{
+    if (!h)
+        return;
+    cudaDeviceSynchronize();
+    free_handle(h);
+}
+
+long long moe_expert_bytes(const moe_handle* h)
+{
+    if (!h)
+        return 0;
+    const size_t E = h->cfg.num_experts;
+    return (long long)((h->gu_codes_b + h->gu_scales_b + h->gu_bias_b + h->dn_codes_b +
+                        h->dn_scales_b + h->dn_bias_b) / E);
+}
+
+int moe_last_launches(const moe_handle* h) { return h ? h->last_launches : 0; }
+
+int moe_load_experts(moe_handle* h, int layer, const void* gu_codes, const void* gu_scales,
+                     const void* gu_bias, const void* dn_codes, const void* dn_scales,
+                     const void* dn_bias, void* stream)
+{
+    if (!h)
+        return fail(MOE_ERR_INVALID_ARG, "moe_load_experts: handle is NULL");
+    if (layer < 0 || layer >= h->cfg.num_layers)
+        return fail(MOE_ERR_INVALID_ARG, "layer=%d out of range 0..%d", layer, h->cfg.num_layers - 1);
+    if (!gu_codes || !gu_scales || !dn_codes || !dn_scales)
+        return fail(MOE_ERR_INVALID_ARG, "moe_load_experts: codes and scales must not be NULL");
+    if (h->cfg.has_bias && (!gu_bias || !dn_bias))
+        return fail(MOE_ERR_INVALID_ARG, "moe_load_experts: has_bias=1 but a bias pointer is NULL");
+    cudaStream_t s = (cudaStream_t)stream;
+    uint8_t* base = h->arena + (size_t)layer * h->layer_stride;
+    struct {
+        void* dst;
+        const void* src;
+        size_t n;
+    } cp[6] = {{base, gu_codes, h->gu_codes_b},
+               {base + h->off_gu_scales, gu_scales, h->gu_scales_b},
+               {base + h->off_gu_bias, gu_bias, h->gu_bias_b},
+               {base + h->off_dn_codes, dn_codes, h->dn_codes_b},
+               {base + h->off_dn_scales, dn_scales, h->dn_scales_b},
+               {base + h->off_dn_bias, dn_bias, h->dn_bias_b}};
+    for (auto& c : cp) {
+        if (c.n == 0)
+            continue;
+        cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyDefault, s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "moe_load_experts copy");
+    }
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "moe_load_experts sync");
+    h->loaded[layer] = 1;
+    return MOE_OK;
+}
+
+int moe_forward(moe_handle* h, int layer, const void* x_bf16, const float* router_logits, int M,
+                int top_k, void* out_bf16, void* stream)
+{
+    int rc = check_forward_args(h, M, top_k);
+    if (rc != MOE_OK)
+        return rc;
+    if (layer < 0 || layer >= h->cfg.num_layers)
+        return fail(MOE_ERR_INVALID_ARG, "layer=%d out of range 0..%d", layer, h->cfg.num_layers - 1);
+    if (!x_bf16 || !router_logits || !out_bf16)
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward: x, logits and out must not be NULL");
+    if (!aligned16(x_bf16) || !aligned16(out_bf16) || !aligned16(router_logits))
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward: x, logits and out must be 16-byte aligned");
+    const size_t nb = (size_t)M * h->cfg.hidden * 2;
+    if (overlaps(x_bf16, nb, out_bf16, nb))
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward: x overlaps out");
+    if (!h->loaded[layer])
+        return fail(MOE_ERR_NOT_LOADED, "moe_forward: layer %d has no experts loaded", layer);
+    moe::LayerParams p = layer_params(h, layer);
+    p.logits = router_logits;
+    p.x = static_cast<const uint16_t*>(x_bf16);
+    p.resid = static_cast<uint16_t*>(out_bf16);
+    p.M = M;
+    p.k = top_k;
+    cudaError_t e = moe::launch_layer(p, h->cfg.format, h->num_sms, (cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "moe_forward launch");
+    h->last_layers = 1;
+    h->last_first_layer = layer;
+    h->last_launches = 2;
+    return MOE_OK;
+}
+
+int moe_forward_host(moe_handle* h, int layer, const void* x_bf16, const float* router_logits,
+                     int M, int top_k, void* out_bf16, void* stream)
+{
+    int rc = check_forward_args(h, M, top_k);
+    if (rc != MOE_OK)
+        return rc;
+    if (!x_bf16 || !router_logits || !out_bf16)
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_host: x, logits and out must not be NULL");
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t nb = (size_t)M * h->cfg.hidden * 2, nl = (size_t)M * h->cfg.num_experts * 4;
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(h->st_x, x_bf16, nb, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(h->st_logits, router_logits, nl, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(h->st_out, out_bf16, nb, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(e, "moe_forward_host upload");
+    rc = moe_forward(h, layer, h->st_x, h->st_logits, M, top_k, h->st_out, stream);
+    if (rc != MOE_OK)
+        return rc;
+    if ((e = cudaMemcpyAsync(out_bf16, h->st_out, nb, cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
+        (e = cudaStreamSynchronize(s)) != cudaSuccess)
+        return cuda_fail(e, "moe_forward_host download");
+    return MOE_OK;
+}
+
+int moe_forward_stack(moe_handle* h, void* resid_bf16, const float* router_logits, int M, int top_k,
+                      void* stream)
+{
+    int rc = check_forward_args(h, M, top_k);
+    if (rc != MOE_OK)
+        return rc;
+    if (!resid_bf16 || !router_logits)
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_stack: resid and logits must not be NULL");
+    if (!aligned16(resid_bf16) || !aligned16(router_logits))
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_stack: resid and logits must be 16-byte aligned");
+    const int L = h->cfg.num_layers;
+    for (int l = 0; l < L; ++l)
+        if (!h->loaded[l])
+            return fail(MOE_ERR_NOT_LOADED, "moe_forward_stack: layer %d has no experts loaded", l);
+    StackGraph* g = nullptr;
+    for (auto& c : h->graphs)
+        if (c.M == M && c.k == top_k && c.resid == resid_bf16 && c.logits == router_logits)
+            g = &c;
+    if (!g) {
+        // capture the 2L launches once for this (M, top_k, buffers)
+        cudaStream_t cs = h->capture_stream;
+        cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "moe_forward_stack capture begin");
+        cudaError_t le = cudaSuccess;
+        for (int l = 0; l < L && le == cudaSuccess; ++l) {
+            moe::LayerParams p = layer_params(h, l);
+            p.logits = router_logits + (size_t)l * M * h->cfg.num_experts;
+            p.x = nullptr;
+            p.resid = static_cast<uint16_t*>(resid_bf16);
+            p.M = M;
+            p.k = top_k;
+            le = moe::launch_layer(p, h->cfg.format, h->num_sms, cs);
+        }
+        cudaGraph_t graph = nullptr;
+        e = cudaStreamEndCapture(cs, &graph);
+        if (le != cudaSuccess || e != cudaSuccess) {
+            if (graph)
+                cudaGraphDestroy(graph);
+            return cuda_fail(le != cudaSuccess ? le : e, "moe_forward_stack capture");
+        }
+        cudaGraphExec_t exec = nullptr;
+        e = cudaGraphInstantiate(&exec, graph, 0);
+        cudaGraphDestroy(graph);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "moe_forward_stack instantiate");
+        if (h->graphs.size() >= 8) {
+            cudaGraphExecDestroy(h->graphs.front().exec);
+            h->graphs.erase(h->graphs.begin());
+        }
+        StackGraph ng;
+        ng.M = M;
+        ng.k = top_k;
+        ng.resid = resid_bf16;
+        ng.logits = router_logits;
+        ng.exec = exec;
+        h->graphs.push_back(ng);
+        g = &h->graphs.back();
+    }
+    cudaError_t e = cudaGraphLaunch(g->exec, (cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "moe_forward_stack launch");
+    h->last_layers = L;
+    h->last_first_layer = 0;
+    h->last_launches = 2 * L;
+    return MOE_OK;
+}
+
+int moe_get_status(moe_handle* h, void* stream)
+{
+    if (!h)
+        return fail(MOE_ERR_INVALID_ARG, "moe_get_status: handle is NULL");
+    cudaStream_t s = (cudaStream_t)stream;
+    int st = 0;
+    cudaError_t e;
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess ||
+        (e = cudaMemcpy(&st, h->status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess ||
+        (e = cudaMemset(h->status, 0, sizeof(int))) != cudaSuccess)
+        return cuda_fail(e, "moe_get_status");
+    return st;
+}
+
+int moe_last_bytes(moe_handle* h, void* stream, long long* bytes)
+{
+    if (!h || !bytes)
+        return fail(MOE_ERR_INVALID_ARG, "moe_last_bytes: NULL argument");
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "moe_last_bytes sync");
+    std::vector<int> nu(h->last_layers > 0 ? h->last_layers : 1, 0);
+    if (h->last_layers > 0) {
+        e = cudaMemcpy(nu.data(), h->stats + h->last_first_layer, h->last_layers * sizeof(int),
+                       cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "moe_last_bytes read");
+    }
+    long long total = 0;
+    for (int l = 0; l < h->last_layers; ++l)
+        total += (long long)nu[l] * moe_expert_bytes(h);
+    *bytes = total;
+    return MOE_OK;
+}
+
+int moe_debug_dequant(moe_handle* h, int layer, int expert, int proj, float* out_dev, void* stream)
+{
+    if (!h || !out_dev)
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_dequant: NULL argument");
+    const moe_config& c = h->cfg;
+    if (layer < 0 || layer >= c.num_layers || expert < 0 || expert >= c.num_experts ||
+        (proj != 0 && proj != 1))
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_dequant: layer/expert/proj out of range");
+    if (!h->loaded[layer])
+        return fail(MOE_ERR_NOT_LOADED, "moe_debug_dequant: layer %d has no experts loaded", layer);
+    moe::LayerParams p = layer_params(h, layer);
+    const int N = proj == 0 ? 2 * c.intermediate : c.hidden;
+    const int K = proj == 0 ? c.hidden : c.intermediate;
+    const int sb = proj == 0 ? h->sbh : h->sbi;
+    const uint8_t* codes = (proj == 0 ? p.gu_codes : p.dn_codes) + (size_t)expert * N * (K / 2);
+    const uint8_t* scales = (proj == 0 ? p.gu_scales : p.dn_scales) + (size_t)expert * N * sb;
+    cudaError_t e = moe::launch_dequant(c.format, codes, scales, N, K, c.group, out_dev,
+                                        (cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "moe_debug_dequant launch");
+    return MOE_OK;
+}
+
+int moe_debug_route(moe_handle* h, const float* logits, int M, int top_k, int* idx, float* w,
+                    void* stream)
+{
+    if (!h || !logits || !idx || !w)
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_route: NULL argument");
+    if (M < 1 || M > 65536)
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_route: M=%d must be in 1..65536", M);
+    if (top_k < 1 || top_k > h->cfg.max_top_k)
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_route: top_k=%d must be in 1..%d", top_k,
+                    h->cfg.max_top_k);
+    cudaError_t e = moe::launch_route(logits, M, h->cfg.num_experts, top_k, idx, w,
+                                      (cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "moe_debug_route launch");
+    return MOE_OK;
+}
+
+}  // extern "C"

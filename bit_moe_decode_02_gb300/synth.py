@@ -140,15 +140,31 @@ def expert_tensors(shape: Shape, layer: int, expert: int):
     return gu_codes, gu_scales, gu_bias, dn_codes, dn_scales, dn_bias
 
 
-def layer_tensors(shape: Shape, layer: int = 0) -> LayerTensors:
-    parts = [expert_tensors(shape, layer, e) for e in range(shape.experts)]
+def layer_tensors(shape: Shape, layer: int = 0, experts=None) -> LayerTensors:
+    """All E experts of one layer; with ``experts`` given, only those are drawn
+    and the others are left zero (for a caller that reads only those)."""
+    if experts is None:
+        parts = [expert_tensors(shape, layer, e) for e in range(shape.experts)]
 
-    def stackp(i):
-        if parts[0][i] is None:
-            return None
-        return np.stack([p[i] for p in parts])
+        def stackp(i):
+            if parts[0][i] is None:
+                return None
+            return np.stack([p[i] for p in parts])
 
-    return LayerTensors(*[stackp(i) for i in range(6)])
+        return LayerTensors(*[stackp(i) for i in range(6)])
+    H, I, E = shape.hidden, shape.intermediate, shape.experts
+    sd = shape.scale_dtype
+    t = LayerTensors(
+        np.zeros((E, 2 * I, H // 2), np.uint8), np.zeros((E, 2 * I, shape.scales_per_row(H)), sd),
+        np.zeros((E, 2 * I), np.uint16) if shape.has_bias else None,
+        np.zeros((E, H, I // 2), np.uint8), np.zeros((E, H, shape.scales_per_row(I)), sd),
+        np.zeros((E, H), np.uint16) if shape.has_bias else None)
+    names = ("gu_codes", "gu_scales", "gu_bias", "dn_codes", "dn_scales", "dn_bias")
+    for e in sorted(set(int(v) for v in experts)):
+        for name, part in zip(names, expert_tensors(shape, layer, e)):
+            if part is not None:
+                getattr(t, name)[e] = part
+    return t
 
 
 def step_inputs(shape: Shape, step: int, M: int | None = None, layers: int | None = None):

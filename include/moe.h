@@ -1,0 +1,170 @@
+/*
+ * moe.h -- C ABI of libmoe: the routed-expert block of a fine-grained
+ * sparse-MoE decode step with 4-bit packed expert weights, on one GB300
+ * (sm_103a).
+ *
+ * What one forward computes, per token m of a batch of M:
+ *   1. router: the top_k experts with the largest logits (ties: lower expert
+ *      index first; NaN orders as -inf) and a softmax over those top_k logits
+ *      only ("Sovereign gpt-oss-20B (MXFP4) on Apple Silicon", section 3:
+ *      top-4 routing of 32 experts; GPU top-k on the serving path in
+ *      "Amortizing the per-token host-sync setup tax ...", section 3);
+ *   2. per selected expert e: a = W_gu[e] x + b_gu[e] with W_gu dequantised
+ *      on chip (gate rows [0, I), up rows [I, 2I)); h = silu(gate) * up with
+ *      silu(g) = g / (1 + exp(-g)); y = W_d[e] h + b_d[e] (the "4 sequential
+ *      experts x 2 small-block GEMVs" of the gpt-oss page, section 3);
+ *   3. out[m] = r[m] + sum_s w[m][s] * y_{m,s}   (routing-weighted sum into
+ *      the residual), rounded to bfloat16 (nearest even).
+ *
+ * Weight formats ("MXFP4 reader", gpt-oss page section 3; packed int4 with
+ * on-chip dequantisation, "Single-stream int4 decode of a 30B MoE", sections
+ * 1 and 6).  All matrices are row-major [N_out][K]; two 4-bit codes per byte,
+ * the low nibble holding the even element:
+ *   MOE_FMT_MXFP4: OCP MX v1.0 MXFP4 -- FP4 E2M1 codes, one E8M0 scale byte
+ *                  (value 2^(s-127), 0xFF = NaN) per 32 consecutive elements
+ *                  along K.  Scales u8 [N][K/32].
+ *   MOE_FMT_INT4 : symmetric int4, W = (code - 8) * s, one fp16 scale per
+ *                  `group` consecutive elements along K.  Scales fp16
+ *                  [N][K/group].
+ *
+ * Precision: x, r and out are bfloat16; routing weights, gate_up outputs, h
+ * and down outputs are fp32 and never rounded to 16 bits; dot products are
+ * accumulated in fp32.  Denormal scales are kept (no flush to zero).
+ *
+ * Conventions:
+ *   - Every call returns a moe_status (0 = MOE_OK).  Arguments are checked
+ *     before anything is enqueued: a call that fails validation enqueues no
+ *     work and leaves all buffers untouched.  moe_last_error() gives a
+ *     message for the calling thread's last failure.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *     Forward calls are asynchronous on it.
+ *   - Device pointers are plain CUDA device addresses (e.g. from a PyTorch
+ *     tensor's data_ptr()); they are borrowed for the duration of the work
+ *     enqueued by the call and never freed by the library.
+ *   - A handle owns all the device memory it uses: the resident weights of
+ *     every layer, a fixed workspace sized at moe_create, and a status word.
+ *     No forward call allocates.
+ *   - A handle is not thread-safe: use it from one host thread and one stream
+ *     at a time.  Distinct handles are independent.
+ *   - Failures detected on the device (a bounded wait that gave up, an index
+ *     out of range) set the handle's status word; read it with
+ *     moe_get_status().  Device code never traps.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_handle moe_handle;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1,    /* bad pointer, size, layer, M or top_k   */
+    MOE_ERR_UNSUPPORTED = -2,    /* a shape or format this build does not run */
+    MOE_ERR_OOM = -3,            /* device allocation failed in moe_create */
+    MOE_ERR_CUDA = -4,           /* a CUDA runtime call failed             */
+    MOE_ERR_NOT_LOADED = -5,     /* forward on a layer whose experts were never loaded */
+    MOE_ERR_DEVICE_TIMEOUT = -6, /* a device-side bounded wait gave up     */
+    MOE_ERR_DEVICE_FAULT = -7    /* a device-side bounds check fired       */
+} moe_status;
+
+typedef enum { MOE_FMT_MXFP4 = 1, MOE_FMT_INT4 = 2 } moe_format;
+
+typedef struct {
+    int hidden;        /* H: model width, the K of gate_up and the N of down   */
+    int intermediate;  /* I: expert width; gate_up has 2I rows                 */
+    int num_experts;   /* E experts per layer                                  */
+    int num_layers;    /* L layers held resident                               */
+    int max_tokens;    /* largest M any forward will be given (1..4 decode)    */
+    int max_top_k;     /* largest top_k any forward will be given (<= E)       */
+    int format;        /* moe_format                                           */
+    int group;         /* elements per scale along K: 32 (MXFP4) or e.g. 64 (int4) */
+    int has_bias;      /* 1: bf16 biases b_gu [E][2I] and b_d [E][H] are loaded */
+} moe_config;
+
+/* Validate cfg and create a handle on the current CUDA device.  Allocates
+ * the resident weight arena for all L layers plus a fixed workspace.
+ * Requirements: H and I multiples of 32 and at most 4096; E in 1..256;
+ * max_top_k in 1..min(E, 16); max_tokens in 1..4; MXFP4 needs group == 32;
+ * int4 needs group a multiple of 32 dividing both H and I.
+ * On success *out receives the handle; on failure *out is set to NULL. */
+int moe_create(const moe_config* cfg, moe_handle** out);
+
+/* Copy one layer's experts into the handle.  Each pointer may be host or
+ * device memory (any address the CUDA runtime can copy from); the caller keeps
+ * ownership and may free or reuse its buffers once the call returns (the call
+ * synchronises `stream`).  Layouts (E experts, caller order):
+ *   gu_codes  u8 [E][2I][H/2]   gu_scales u8 [E][2I][H/32] | fp16 [E][2I][H/group]
+ *   gu_bias bf16 [E][2I]        (NULL allowed only when has_bias == 0)
+ *   dn_codes  u8 [E][H][I/2]    dn_scales u8 [E][H][I/32]  | fp16 [E][H][I/group]
+ *   dn_bias bf16 [E][H]         (NULL allowed only when has_bias == 0)
+ * A layer may be reloaded; the new weights replace the old ones. */
+int moe_load_experts(moe_handle* h, int layer,
+                     const void* gu_codes, const void* gu_scales, const void* gu_bias,
+                     const void* dn_codes, const void* dn_scales, const void* dn_bias,
+                     void* stream);
+
+/* One decode layer.  x bf16 [M][H] (the layer input, already normalised),
+ * router_logits fp32 [M][E], out bf16 [M][H]: the residual r on entry and
+ * r + MoE(x) on return.  1 <= M <= max_tokens, 1 <= top_k <= max_top_k.
+ * x must not overlap out (checked).  All three are device pointers. */
+int moe_forward(moe_handle* h, int layer, const void* x_bf16, const float* router_logits,
+                int M, int top_k, void* out_bf16, void* stream);
+
+/* The same layer with host buffers: copies x, logits and the residual to the
+ * handle's device workspace, runs moe_forward on `stream`, copies the result
+ * back into out_bf16 and synchronises the stream before returning. */
+int moe_forward_host(moe_handle* h, int layer, const void* x_bf16, const float* router_logits,
+                     int M, int top_k, void* out_bf16, void* stream);
+
+/* The whole L-layer expert stack for one decode step.  For l = 0..L-1:
+ *   x_l = bf16(r_l / sqrt(mean(r_l^2) + 1e-6))   (weightless RMSNorm, per token)
+ *   r_{l+1} = bf16(r_l + MoE_l(x_l))
+ * resid bf16 [M][H] holds r_0 on entry and r_L on return; logits fp32
+ * [L][M][E].  Layer l+1 reads its logits only after layer l's output is
+ * complete.  Device pointers.  Launched as a cached CUDA graph per (M, top_k). */
+int moe_forward_stack(moe_handle* h, void* resid_bf16, const float* router_logits,
+                      int M, int top_k, void* stream);
+
+/* Synchronise `stream` and return (and clear) the handle's device status:
+ * MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_FAULT. */
+int moe_get_status(moe_handle* h, void* stream);
+
+/* Debug: decode one stored expert projection to fp32, exactly (each element
+ * is e2m1 * 2^(s-127) or (q - 8) * fp16 scale, rounded to fp32 once).
+ * proj 0 = gate_up ([2I][H], caller row order), 1 = down ([H][I]).
+ * out_dev fp32 device buffer of N*K elements. */
+int moe_debug_dequant(moe_handle* h, int layer, int expert, int proj, float* out_dev,
+                      void* stream);
+
+/* Debug: the router alone.  logits fp32 [M][E] device; idx int32 [M][top_k]
+ * and w fp32 [M][top_k] device outputs, selection order (largest first).
+ * M up to 65536 here. */
+int moe_debug_route(moe_handle* h, const float* logits, int M, int top_k, int* idx, float* w,
+                    void* stream);
+
+/* Algorithmic expert bytes moved by the last forward call on this handle:
+ * codes + scales + biases of the distinct experts selected in each layer,
+ * counted once per layer.  Synchronises `stream`.  Returns MOE_OK and
+ * writes *bytes, or an error. */
+int moe_last_bytes(moe_handle* h, void* stream, long long* bytes);
+
+/* Bytes of one expert (codes + scales + biases) for this handle's config. */
+long long moe_expert_bytes(const moe_handle* h);
+
+/* Number of kernel launches the last forward call enqueued (for the caller's
+ * launch accounting; a graph replay counts the kernels inside it). */
+int moe_last_launches(const moe_handle* h);
+
+/* Message for the calling thread's most recent failure ("" if none). */
+const char* moe_last_error(void);
+
+/* Release a handle and all device memory it owns.  NULL is a no-op. */
+void moe_destroy(moe_handle* h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

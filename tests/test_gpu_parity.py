@@ -1,0 +1,300 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Bars: bit-exact for dequantised weights and expert selection; routing weights
+within 1e-6; layer outputs within 2e-3 of the output's max-norm plus the bf16
+output rounding (see moe_testlib.assert_parity).
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle
+from bit_moe_decode_02_gb300 import synth
+from moe_testlib import (assert_parity, bf16_bits_to_f64, create_handle, dev_to_bits, load_layer,
+                         oracle_layer, sparse_layer, to_dev_bf16)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_moe_decode_02_gb300 import build_ext
+    build_ext.build()
+    import bit_moe_decode_02_gb300 as m
+    return m
+
+
+def _run_layer(moe, h, layer, x, r, logits, k):
+    xd = to_dev_bf16(x)
+    out = to_dev_bf16(r)
+    ld = torch.from_numpy(np.ascontiguousarray(logits, np.float32)).cuda()
+    moe.moe_forward(h, layer, xd, ld, x.shape[0], k, out)
+    torch.cuda.synchronize()
+    assert moe.moe_get_status(h) == 0
+    return bf16_bits_to_f64(dev_to_bits(out))
+
+
+# ------------------------------------------------------------------ dequant
+
+def test_dequant_bitexact_mxfp4_every_code_and_scale(moe):
+    # gate_up rows n use scale byte n % 256 in every block and codes cycling
+    # through all 16 values, so every (code, E8M0) pair appears.
+    H, I, E = 64, 256, 2
+    shp = synth.Shape("dequant", H, I, E, 1, e8m0_lo=0, e8m0_hi=254)
+    t = synth.layer_tensors(shp)
+    codes = np.array([(j + n) % 16 for n in range(2 * I) for j in range(H)], np.uint8).reshape(2 * I, H)
+    t.gu_codes[0] = codes[:, 0::2] | (codes[:, 1::2] << 4)
+    t.gu_scales[0] = (np.arange(2 * I) % 256).astype(np.uint8)[:, None]
+    h = create_handle(shp, max_top_k=1)
+    try:
+        load_layer(h, 0, t)
+        for e, proj, N, K in [(0, 0, 2 * I, H), (1, 0, 2 * I, H), (0, 1, H, I), (1, 1, H, I)]:
+            out = torch.empty(N * K, dtype=torch.float32, device="cuda")
+            moe.moe_debug_dequant(h, 0, e, proj, out)
+            got = out.cpu().numpy().reshape(N, K)
+            c, s = (t.gu_codes[e], t.gu_scales[e]) if proj == 0 else (t.dn_codes[e], t.dn_scales[e])
+            ref = oracle.dequant(oracle.FMT_MXFP4, c, s, N, K).astype(np.float32)
+            assert np.array_equal(np.isnan(got), np.isnan(ref))
+            ok = ~np.isnan(ref)
+            assert np.array_equal(got[ok].view(np.uint32), ref[ok].view(np.uint32)), (e, proj)
+    finally:
+        moe.moe_destroy(h)
+
+
+def test_dequant_bitexact_int4(moe):
+    H, I, E = 128, 64, 3
+    shp = synth.Shape("dequant int4", H, I, E, 1, fmt=synth.FMT_INT4, group=64, has_bias=False)
+    t = synth.layer_tensors(shp)
+    rng = np.random.default_rng(9)
+    # fp16 scales over the whole range: subnormal, negative, zero, large
+    special = np.array([0x0001, 0x03FF, 0x0400, 0x8001, 0x0000, 0x8000, 0x7BFF, 0xFBFF, 0x3C00],
+                       np.uint16)
+    t.gu_scales[0].ravel()[:special.size] = special
+    t.dn_scales[1] = rng.integers(0, 0x7C00, t.dn_scales[1].shape).astype(np.uint16)
+    h = create_handle(shp, max_top_k=1)
+    try:
+        load_layer(h, 0, t)
+        for e in range(E):
+            for proj, N, K in [(0, 2 * I, H), (1, H, I)]:
+                out = torch.empty(N * K, dtype=torch.float32, device="cuda")
+                moe.moe_debug_dequant(h, 0, e, proj, out)
+                got = out.cpu().numpy().reshape(N, K)
+                c, s = (t.gu_codes[e], t.gu_scales[e]) if proj == 0 else (t.dn_codes[e], t.dn_scales[e])
+                ref = oracle.dequant(oracle.FMT_INT4, c, s, N, K, 64).astype(np.float32)
+                assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), (e, proj)
+    finally:
+        moe.moe_destroy(h)
+
+
+# ------------------------------------------------------------------ router
+
+@pytest.mark.parametrize("E,k", [(8, 2), (32, 4), (128, 8), (256, 16), (5, 5), (32, 1)])
+def test_route_matches_oracle(moe, E, k):
+    rng = np.random.default_rng(E * 100 + k)
+    M = 777
+    logits = rng.standard_normal((M, E)).astype(np.float32)
+    logits[:100] = np.round(logits[:100] * 2) / 2          # many ties
+    logits[100, :] = 0.0                                    # all tied
+    logits[101, ::3] = np.nan
+    shp = synth.Shape("route", 64, 64, E, k)
+    h = create_handle(shp, max_top_k=k)
+    try:
+        ld = torch.from_numpy(logits).cuda()
+        idx = torch.empty((M, k), dtype=torch.int32, device="cuda")
+        w = torch.empty((M, k), dtype=torch.float32, device="cuda")
+        moe.moe_debug_route(h, ld, M, k, idx, w)
+        ridx, rw = oracle.route(logits, k)
+        assert np.array_equal(idx.cpu().numpy(), ridx)
+        gw = w.cpu().numpy().astype(np.float64)
+        assert np.abs(gw - rw).max() <= 1e-6
+        assert np.abs(gw.sum(1) - 1).max() <= 1e-6
+    finally:
+        moe.moe_destroy(h)
+
+
+# ------------------------------------------------------------------ one layer
+
+SMALL = [
+    synth.TINY,
+    synth.Shape("ragged H=160 I=96 E=5 top-3", 160, 96, 5, 3, e8m0_lo=118, e8m0_hi=124,
+                bias_sigma=0.5, seed=11),
+    synth.Shape("int4 H=128 I=64 E=6 top-2", 128, 64, 6, 2, fmt=synth.FMT_INT4, group=64,
+                has_bias=False, seed=12),
+    synth.Shape("int4 biased H=192 I=320 E=7 top-4", 192, 320, 7, 4, fmt=synth.FMT_INT4, group=32,
+                has_bias=True, bias_sigma=0.1, seed=13),
+    synth.Shape("all experts H=64 I=64 E=4 top-4", 64, 64, 4, 4, seed=14),
+    synth.Shape("one-hot H=256 I=512 E=8 top-1", 256, 512, 8, 1, seed=15),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: s.name)
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+def test_layer_parity_small(moe, shape, M):
+    t = synth.layer_tensors(shape)
+    h = create_handle(shape)
+    try:
+        load_layer(h, 0, t)
+        for step in range(2):
+            x, r, logits = synth.step_inputs(shape, step, M=M, layers=1)
+            got = _run_layer(moe, h, 0, x, r, logits[0], shape.top_k)
+            ref, _, _ = oracle_layer(shape, t, x, logits[0], r)
+            assert_parity(got, ref, what=f"{shape.name} M={M} step={step}")
+    finally:
+        moe.moe_destroy(h)
+
+
+def test_layer_topk_ties_and_nan_logits(moe):
+    shape = synth.TINY
+    t = synth.layer_tensors(shape)
+    h = create_handle(shape)
+    try:
+        load_layer(h, 0, t)
+        x, r, _ = synth.step_inputs(shape, 0, M=3, layers=1)
+        logits = np.zeros((3, shape.experts), np.float32)
+        logits[1, [2, 5]] = 1.0
+        logits[2, :] = np.nan
+        logits[2, 6] = 0.25
+        got = _run_layer(moe, h, 0, x, r, logits, shape.top_k)
+        ref, idx, _ = oracle_layer(shape, t, x, logits, r)
+        assert list(idx[0]) == [0, 1] and list(idx[1]) == [2, 5] and list(idx[2]) == [6, 0]
+        assert_parity(got, ref, what="ties/NaN")
+    finally:
+        moe.moe_destroy(h)
+
+
+@pytest.mark.parametrize("shape", [synth.GPTOSS_LAYER,
+                                   synth.Shape("int4 layer H=2048 I=768 E=128 top-8", 2048, 768,
+                                               128, 8, fmt=synth.FMT_INT4, group=64,
+                                               has_bias=False, seed=3)],
+                         ids=lambda s: s.name)
+@pytest.mark.parametrize("M", [1, 4])
+def test_layer_parity_full_size(moe, shape, M):
+    t = synth.layer_tensors(shape)
+    h = create_handle(shape)
+    try:
+        load_layer(h, 0, t)
+        for step in range(2):
+            x, r, logits = synth.step_inputs(shape, step, M=M, layers=1)
+            got = _run_layer(moe, h, 0, x, r, logits[0], shape.top_k)
+            ref, idx, _ = oracle_layer(shape, t, x, logits[0], r)
+            assert_parity(got, ref, what=f"{shape.name} M={M}")
+        # the expert bytes of the last call: distinct selected experts x bytes per expert
+        nu = len(set(idx.ravel().tolist()))
+        assert moe.moe_expert_bytes(h) == shape.expert_bytes()
+        assert moe.moe_last_bytes(h) == nu * shape.expert_bytes()
+    finally:
+        moe.moe_destroy(h)
+
+
+def test_forward_host_equals_forward_and_is_deterministic(moe):
+    shape = synth.GPTOSS_LAYER
+    t = synth.layer_tensors(shape)
+    h = create_handle(shape)
+    try:
+        load_layer(h, 0, t)
+        x, r, logits = synth.step_inputs(shape, 5, M=2, layers=1)
+        a = dev_to_bits(torch.from_numpy(r.view(np.int16)).cuda())
+        outs = []
+        for _ in range(3):
+            xd, od = to_dev_bf16(x), to_dev_bf16(r)
+            ld = torch.from_numpy(logits[0]).cuda()
+            moe.moe_forward(h, 0, xd, ld, 2, shape.top_k, od)
+            outs.append(dev_to_bits(od))
+        assert all(np.array_equal(outs[0], o) for o in outs[1:])
+        host_out = r.copy()
+        moe.moe_forward_host(h, 0, x, np.ascontiguousarray(logits[0]), 2, shape.top_k, host_out)
+        assert np.array_equal(host_out, outs[0])
+        assert not np.array_equal(a, outs[0])
+    finally:
+        moe.moe_destroy(h)
+
+
+def test_forward_argument_errors(moe):
+    shape = synth.TINY
+    h = create_handle(shape, max_tokens=2)
+    try:
+        x, r, logits = synth.step_inputs(shape, 0, M=2, layers=1)
+        xd, od = to_dev_bf16(x), to_dev_bf16(r)
+        ld = torch.from_numpy(logits[0]).cuda()
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_forward(h, 0, xd, ld, 2, shape.top_k, od)
+        assert ei.value.status == moe.MOE_ERR_NOT_LOADED
+        load_layer(h, 0, synth.layer_tensors(shape))
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_forward(h, 0, xd, ld, 3, shape.top_k, od)
+        assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_forward(h, 0, xd, ld, 2, shape.top_k, xd)
+        assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_forward(h, 1, xd, ld, 2, shape.top_k, od)
+        assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+        before = dev_to_bits(od)
+        with pytest.raises(moe.MoeError):
+            moe.moe_forward(h, 0, xd, ld, 2, shape.top_k + 1, od)
+        torch.cuda.synchronize()
+        assert np.array_equal(before, dev_to_bits(od))     # nothing was enqueued
+    finally:
+        moe.moe_destroy(h)
+
+
+# ------------------------------------------------------------------ stack
+
+def _run_stack(moe, h, r, logits, k):
+    rd = to_dev_bf16(r)
+    ld = torch.from_numpy(np.ascontiguousarray(logits, np.float32)).cuda()
+    moe.moe_forward_stack(h, rd, ld, r.shape[0], k)
+    torch.cuda.synchronize()
+    assert moe.moe_get_status(h) == 0
+    return dev_to_bits(rd)
+
+
+@pytest.mark.parametrize("shape,L", [
+    (synth.Shape("tiny stack L=4", 256, 256, 8, 2, layers=4, bias_sigma=0.02, seed=21), 4),
+    (synth.Shape("int4 stack L=3", 128, 64, 6, 2, fmt=synth.FMT_INT4, group=64, has_bias=False,
+                 layers=3, seed=22), 3)], ids=lambda v: getattr(v, "name", str(v)))
+@pytest.mark.parametrize("M", [1, 3])
+def test_stack_parity_small(moe, shape, L, M):
+    layers = [synth.layer_tensors(shape, l) for l in range(L)]
+    h = create_handle(shape, layers=L)
+    try:
+        for l, t in enumerate(layers):
+            load_layer(h, l, t)
+        for step in range(2):
+            _, r, logits = synth.step_inputs(shape, step, M=M)
+            got = _run_stack(moe, h, r, logits, shape.top_k)
+            ref = oracle.stack(shape.fmt, shape.hidden, shape.intermediate, shape.experts,
+                               shape.top_k, layers, logits, r, group=shape.group,
+                               nthreads=oracle.max_threads())
+            assert_parity(bf16_bits_to_f64(got), bf16_bits_to_f64(ref), ulps=1.0,
+                          what=f"{shape.name} M={M}")
+    finally:
+        moe.moe_destroy(h)
+
+
+@pytest.mark.parametrize("shape", [synth.GPTOSS_STACK, synth.INT4_STACK], ids=lambda s: s.name)
+def test_stack_parity_full_size(moe, shape):
+    """The full stacks (10 GB / 15 GB resident), one step at M=1 and one at M=4.
+    The oracle regenerates only the experts each layer's router selects."""
+    L = shape.layers
+    h = create_handle(shape, layers=L)
+    try:
+        for l in range(L):
+            load_layer(h, l, synth.layer_tensors(shape, l))
+        for M in (1, 4):
+            _, r, logits = synth.step_inputs(shape, 100 + M, M=M)
+            got = _run_stack(moe, h, r, logits, shape.top_k)
+            layers = []
+            for l in range(L):
+                idx, _ = oracle.route(logits[l], shape.top_k)
+                layers.append(sparse_layer(shape, l, idx.ravel()))
+            ref = oracle.stack(shape.fmt, shape.hidden, shape.intermediate, shape.experts,
+                               shape.top_k, layers, logits, r, group=shape.group,
+                               nthreads=oracle.max_threads())
+            assert_parity(bf16_bits_to_f64(got), bf16_bits_to_f64(ref), ulps=1.0,
+                          what=f"{shape.name} M={M}")
+    finally:
+        moe.moe_destroy(h)
