@@ -185,7 +185,7 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- GPU arm
 
-def run_ours(args):
+def _setup(args):
     import torch
     import torch.distributed as dist
     rank, world, local = dist_env()
@@ -197,122 +197,207 @@ def run_ours(args):
         build_ext.build()
     if world > 1:
         dist.barrier()
-    import bit_moe_decode_02_gb300 as moe
+    return rank, world
 
-    shape = SHAPE
-    L = shape.layers
-    H, E, k = shape.hidden, shape.experts, shape.top_k
-    h = moe.moe_create(H, shape.intermediate, E, L, 1, k, moe.MOE_FMT_MXFP4, 32, 1)
+
+def _max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _load_all(moe, h, shape, L):
     for l in range(L):
         t = synth.layer_tensors(shape, l)
         moe.moe_load_experts(h, l, t.gu_codes, t.gu_scales, t.gu_bias, t.dn_codes, t.dn_scales,
                              t.dn_bias)
         del t
-    n_in = args.warmup + args.steps
-    xs, rs, ls = [], [], []
+
+
+def run_ours(args):
+    import torch
+    rank, world = _setup(args)
+    import bit_moe_decode_02_gb300 as moe
+
+    shape = SHAPE
+    L = args.layers or shape.layers
+    H, E, k = shape.hidden, shape.experts, shape.top_k
+    h = moe.moe_create(H, shape.intermediate, E, L, 1, k, moe.MOE_FMT_MXFP4, 32, 1)
+    _load_all(moe, h, shape, L)
+    W, K = args.warmup, args.steps
+    n_in = W + K
+    xs = np.empty((n_in, 1, H), np.uint16)
+    rs = np.empty((n_in, 1, H), np.uint16)
+    ls = np.empty((n_in, 1, E), np.float32)
     for s in range(n_in):
         x, r, lg = synth.step_inputs(shape, 1000 + s, M=1, layers=1)
-        xs.append(x)
-        rs.append(r)
-        ls.append(lg[0])
-    xd = torch.from_numpy(np.stack(xs).view(np.int16)).cuda()
-    rd0 = torch.from_numpy(np.stack(rs).view(np.int16)).cuda()
-    ld = torch.from_numpy(np.stack(ls)).cuda()
-    rd = rd0.clone()
-    stream = torch.cuda.current_stream()
+        xs[s], rs[s], ls[s] = x, r, lg[0]
+    xd = torch.from_numpy(xs.view(np.int16)).cuda()
+    rd = torch.from_numpy(rs.view(np.int16)).cuda()
+    ld = torch.from_numpy(ls).cuda()
+    xp = [xd[s].data_ptr() for s in range(n_in)]
+    lp = [ld[s].data_ptr() for s in range(n_in)]
+    rp = [rd[s].data_ptr() for s in range(n_in)]
 
-    def step(s):
-        moe.moe_forward(h, s % L, xd[s], ld[s], 1, k, rd[s], stream)
-
-    for s in range(args.warmup):
-        step(s)
+    # The steps are captured into CUDA graphs so that the timed region is the
+    # GPU's work, not the Python loop that issues the calls.
+    cap = torch.cuda.Stream()
+    gw, gk = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     torch.cuda.synchronize()
-    # algorithmic bytes: distinct selected experts of each timed step
-    bytes_per_step = []
+    with torch.cuda.graph(gw, stream=cap):
+        for s in range(W):
+            moe.moe_forward(h, s % L, xp[s], lp[s], 1, k, rp[s], cap)
+    with torch.cuda.graph(gk, stream=cap):
+        for s in range(W, n_in):
+            moe.moe_forward(h, s % L, xp[s], lp[s], 1, k, rp[s], cap)
+    launches = moe.moe_last_launches(h) * K
+    stream = torch.cuda.current_stream()
+    gw.replay()
+    torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
         ev0.record(stream)
-        for s in range(args.warmup, n_in):
-            step(s)
+        gk.replay()
         ev1.record(stream)
         torch.cuda.synchronize()
-    ms = ev0.elapsed_time(ev1)
-    launches = 2 * args.steps
-    for s in range(args.warmup, n_in):
-        step(s)
-        bytes_per_step.append(moe.moe_last_bytes(h, stream))
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = _max_over_ranks(ev0.elapsed_time(ev1), world)
+    assert moe.moe_get_status(h) == 0
 
-    # end to end through the public API with host buffers (pinned)
-    xh = torch.from_numpy(np.stack(xs).view(np.int16)).pin_memory()
-    lh = torch.from_numpy(np.stack(ls)).pin_memory()
-    oh = torch.from_numpy(np.stack(rs).view(np.int16)).pin_memory()
-    for s in range(args.warmup):
-        moe.moe_forward_host(h, s % L, xh[s], lh[s], 1, k, oh[s], stream)
+    bytes_per_step = []
+    for s in range(W, min(n_in, W + 256)):
+        moe.moe_forward(h, s % L, xp[s], lp[s], 1, k, rp[s], stream)
+        bytes_per_step.append(moe.moe_last_bytes(h, stream))
+
+    # end to end through the public API with host buffers (pinned): every step
+    # copies x, logits and the residual in and the result out.
+    xh = torch.from_numpy(xs.view(np.int16)).pin_memory()
+    lh = torch.from_numpy(ls).pin_memory()
+    oh = torch.from_numpy(rs.view(np.int16)).pin_memory()
+    xhp = [xh[s].data_ptr() for s in range(n_in)]
+    lhp = [lh[s].data_ptr() for s in range(n_in)]
+    ohp = [oh[s].data_ptr() for s in range(n_in)]
+    sp = stream.cuda_stream
+    for s in range(W):
+        moe.moe_forward_host(h, s % L, xhp[s], lhp[s], 1, k, ohp[s], sp)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for s in range(args.warmup, n_in):
-        moe.moe_forward_host(h, s % L, xh[s], lh[s], 1, k, oh[s], stream)
-    e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    for s in range(W, n_in):
+        moe.moe_forward_host(h, s % L, xhp[s], lhp[s], 1, k, ohp[s], sp)
+    e2e_s = _max_over_ranks(time.perf_counter() - t0, world)
 
-    us_per_layer = 1e3 * ms / (args.steps * world)
+    us_per_layer = 1e3 * ms / (K * world)
     avg_bytes = float(np.mean(bytes_per_step))
     peak, peak_kind = measured_peaks()
-    fwd_s = ms / 1e3 / args.steps
-    achieved = avg_bytes / fwd_s / 1e9
+    achieved = avg_bytes / (ms / 1e3 / K) / 1e9
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         n = oracle.max_threads()
-        times = oracle_layer_seconds(args.cpu_steps, 1, n)
+        times = oracle_layer_seconds(args.cpu_steps, 1, n, budget_s=30.0)
         cpu = {"value": 1e6 * sum(times) / len(times), "unit": UNIT, "cores": n, "kind": "oracle",
                "sample": f"{len(times)} single-token layer forwards of this workload, fp64, "
                          f"OpenMP over output rows"}
     moe.moe_destroy(h)
     if rank != 0:
         return 0
-    clocks = clk.summary()
     line = {
         "metric": METRIC, "value": us_per_layer, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "steps": K, "warmup": W, "ms_per_step": ms / K,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp32 (MXFP4 weights, bf16 activations)", "data": "synthetic",
         "config": {"workload": WORKLOAD, "tokens_per_step": 1, "layers_resident": L,
                    "resident_bytes": L * E * shape.expert_bytes(),
-                   "l2": "inputs larger than L2: 24 distinct layers (10.2 GB), one per step",
+                   "l2": f"inputs larger than L2: {L} distinct layers "
+                         f"({L * E * shape.expert_bytes() / 1e9:.1f} GB), one per step",
+                   "launch": "K steps captured in one CUDA graph, replayed once",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "kernel": "moe_forward: gate_up_kernel + down_kernel (PDL-chained)",
                      "bytes_per_launch": avg_bytes, "traffic": stored_traffic()},
-        "e2e": {"value": 1e6 * e2e_s / (args.steps * world), "unit": UNIT,
+        "e2e": {"value": 1e6 * e2e_s / (K * world), "unit": UNIT,
                 "h2d_bytes_per_step": H * 2 * 2 + E * 4, "d2h_bytes_per_step": H * 2},
         "gpu_launches": launches,
-        "clocks": clocks,
+        "clocks": clk.summary(),
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    return 0
+
+
+def run_stack(args):
+    """Extra workloads (not the headline line): the 24-layer MXFP4 stack and
+    the 48-layer int4 stack, tokens/s of the expert path at M = --tokens."""
+    import torch
+    rank, world = _setup(args)
+    import bit_moe_decode_02_gb300 as moe
+    shape = synth.GPTOSS_STACK if args.workload == "stack24" else synth.INT4_STACK
+    L = min(args.layers, shape.layers) if args.layers else shape.layers
+    M, k = args.tokens, shape.top_k
+    fmt = moe.MOE_FMT_MXFP4 if shape.fmt == synth.FMT_MXFP4 else moe.MOE_FMT_INT4
+    h = moe.moe_create(shape.hidden, shape.intermediate, shape.experts, L, M, k, fmt, shape.group,
+                       1 if shape.has_bias else 0)
+    _load_all(moe, h, shape, L)
+    W, K = args.warmup, args.steps
+    logits = np.stack([synth.step_inputs(shape, 5000 + s, M=M, layers=L)[2] for s in range(W + K)])
+    _, r, _ = synth.step_inputs(shape, 4999, M=M, layers=L)
+    ld = torch.from_numpy(logits).cuda()
+    lbuf = torch.empty_like(ld[0])
+    rd = torch.from_numpy(r.view(np.int16)).cuda()
+    stream = torch.cuda.current_stream()
+
+    def step(s):
+        lbuf.copy_(ld[s], non_blocking=True)
+        moe.moe_forward_stack(h, rd, lbuf, M, k, stream)
+
+    for s in range(W):
+        step(s)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ev0.record(stream)
+        for s in range(W, W + K):
+            step(s)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    assert moe.moe_get_status(h) == 0
+    step(0)
+    nbytes = moe.moe_last_bytes(h, stream)
+    moe.moe_destroy(h)
+    us_step = 1e3 * ms / K
+    peak, peak_kind = measured_peaks()
+    line = {"workload": shape.name + f", M={M}, {L} layers", "metric": "tokens/s of the expert stack",
+            "value": M * K / (ms / 1e3), "unit": "tok/s", "us_per_step": us_step,
+            "us_per_layer": us_step / L, "steps": K, "warmup": W,
+            "bytes_per_step": nbytes, "gbs": nbytes / (us_step / 1e6) / 1e9,
+            "frac_of_peak": nbytes / (us_step / 1e6) / 1e9 / peak, "peak": peak,
+            "peak_kind": peak_kind, "clocks": clk.summary(),
+            "launch": "one cached CUDA graph of 2L PDL-chained kernels per step"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
     return 0
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=40000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="resident layers (default: 24 for the layer workload, all for the "
+                         "stacks; smaller for profiling)")
+    ap.add_argument("--workload", choices=["layer", "stack24", "int4stack48"], default="layer")
+    ap.add_argument("--tokens", type=int, default=1, help="M for the stack workloads")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-steps", type=int, default=24)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -321,6 +406,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload != "layer":
+        return run_stack(args)
     return run_ours(args)
 
 

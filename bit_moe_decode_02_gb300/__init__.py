@@ -7,7 +7,7 @@ library fails loudly (build it with ``python -m bit_moe_decode_02_gb300.build_ex
 
 The function names are the C names: moe_create, moe_load_experts, moe_forward,
 moe_forward_host, moe_forward_stack, moe_get_status, moe_debug_dequant,
-moe_debug_route, moe_last_bytes, moe_expert_bytes, moe_last_launches,
+moe_debug_route, moe_debug_stack_trace, moe_last_bytes, moe_expert_bytes, moe_last_launches,
 moe_last_error, moe_destroy.
 """
 from __future__ import annotations
@@ -32,6 +32,7 @@ MOE_FMT_INT4 = 2
 # every symbol include/moe.h declares
 EXPORTS = ("moe_create", "moe_load_experts", "moe_forward", "moe_forward_host",
            "moe_forward_stack", "moe_get_status", "moe_debug_dequant", "moe_debug_route",
+           "moe_debug_stack_trace",
            "moe_last_bytes", "moe_expert_bytes", "moe_last_launches", "moe_last_error",
            "moe_destroy")
 
@@ -76,6 +77,8 @@ def lib() -> ctypes.CDLL:
         L.moe_debug_dequant.restype = i
         L.moe_debug_route.argtypes = [p, p, i, i, p, p, p]
         L.moe_debug_route.restype = i
+        L.moe_debug_stack_trace.argtypes = [p, p, p, i, i, p, p]
+        L.moe_debug_stack_trace.restype = i
         L.moe_last_bytes.argtypes = [p, p, ctypes.POINTER(ll)]
         L.moe_last_bytes.restype = i
         L.moe_expert_bytes.argtypes = [p]
@@ -161,6 +164,11 @@ def moe_debug_dequant(h, layer, expert, proj, out, stream=None):
 def moe_debug_route(h, logits, M, top_k, idx, w, stream=None):
     return _check(lib().moe_debug_route(h, _ptr(logits), M, top_k, _ptr(idx), _ptr(w),
                                         _stream(stream)))
+
+
+def moe_debug_stack_trace(h, resid, logits, M, top_k, trace, stream=None):
+    return _check(lib().moe_debug_stack_trace(h, _ptr(resid), _ptr(logits), M, top_k, _ptr(trace),
+                                              _stream(stream)))
 
 
 def moe_last_bytes(h, stream=None) -> int:

@@ -457,6 +457,43 @@ int moe_forward_stack(moe_handle* h, void* resid_bf16, const float* router_logit
     return MOE_OK;
 }
 
+int moe_debug_stack_trace(moe_handle* h, void* resid_bf16, const float* router_logits, int M,
+                          int top_k, void* trace_bf16, void* stream)
+{
+    int rc = check_forward_args(h, M, top_k);
+    if (rc != MOE_OK)
+        return rc;
+    if (!resid_bf16 || !router_logits || !trace_bf16)
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_stack_trace: NULL argument");
+    if (!aligned16(resid_bf16) || !aligned16(router_logits))
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_stack_trace: resid and logits must be 16-byte aligned");
+    const int L = h->cfg.num_layers;
+    for (int l = 0; l < L; ++l)
+        if (!h->loaded[l])
+            return fail(MOE_ERR_NOT_LOADED, "moe_debug_stack_trace: layer %d has no experts loaded", l);
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t nb = (size_t)M * h->cfg.hidden * 2;
+    uint8_t* tr = static_cast<uint8_t*>(trace_bf16);
+    cudaError_t e = cudaMemcpyAsync(tr, resid_bf16, nb, cudaMemcpyDeviceToDevice, s);
+    for (int l = 0; l < L && e == cudaSuccess; ++l) {
+        moe::LayerParams p = layer_params(h, l);
+        p.logits = router_logits + (size_t)l * M * h->cfg.num_experts;
+        p.x = nullptr;
+        p.resid = static_cast<uint16_t*>(resid_bf16);
+        p.M = M;
+        p.k = top_k;
+        e = moe::launch_layer(p, h->cfg.format, h->num_sms, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(tr + (size_t)(l + 1) * nb, resid_bf16, nb, cudaMemcpyDeviceToDevice, s);
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(e, "moe_debug_stack_trace");
+    h->last_layers = L;
+    h->last_first_layer = 0;
+    h->last_launches = 2 * L;
+    return MOE_OK;
+}
+
 int moe_get_status(moe_handle* h, void* stream)
 {
     if (!h)

@@ -145,6 +145,13 @@ int moe_debug_dequant(moe_handle* h, int layer, int expert, int proj, float* out
 int moe_debug_route(moe_handle* h, const float* logits, int M, int top_k, int* idx, float* w,
                     void* stream);
 
+/* Debug: the expert stack run layer by layer with the same kernels as
+ * moe_forward_stack (no graph), recording the residual after every layer.
+ * resid bf16 [M][H] is updated in place as in moe_forward_stack; trace bf16
+ * [L+1][M][H] device buffer receives r_0 .. r_L. */
+int moe_debug_stack_trace(moe_handle* h, void* resid_bf16, const float* router_logits, int M,
+                          int top_k, void* trace_bf16, void* stream);
+
 /* Algorithmic expert bytes moved by the last forward call on this handle:
  * codes + scales + biases of the distinct experts selected in each layer,
  * counted once per layer.  Synchronises `stream`.  Returns MOE_OK and

@@ -67,6 +67,7 @@ def test_null_arguments_rejected(L):
     assert L.moe_get_status(None, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_debug_dequant(None, 0, 0, 0, None, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_debug_route(None, None, 1, 1, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_debug_stack_trace(None, None, None, 1, 1, None, None) == moe.MOE_ERR_INVALID_ARG
     b = ctypes.c_longlong()
     assert L.moe_last_bytes(None, None, ctypes.byref(b)) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_expert_bytes(None) == 0

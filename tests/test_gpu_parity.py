@@ -56,7 +56,8 @@ def test_dequant_bitexact_mxfp4_every_code_and_scale(moe):
             moe.moe_debug_dequant(h, 0, e, proj, out)
             got = out.cpu().numpy().reshape(N, K)
             c, s = (t.gu_codes[e], t.gu_scales[e]) if proj == 0 else (t.dn_codes[e], t.dn_scales[e])
-            ref = oracle.dequant(oracle.FMT_MXFP4, c, s, N, K).astype(np.float32)
+            with np.errstate(over="ignore"):
+                ref = oracle.dequant(oracle.FMT_MXFP4, c, s, N, K).astype(np.float32)
             assert np.array_equal(np.isnan(got), np.isnan(ref))
             ok = ~np.isnan(ref)
             assert np.array_equal(got[ok].view(np.uint32), ref[ok].view(np.uint32)), (e, proj)
@@ -277,8 +278,17 @@ def test_stack_parity_small(moe, shape, L, M):
 
 @pytest.mark.parametrize("shape", [synth.GPTOSS_STACK, synth.INT4_STACK], ids=lambda s: s.name)
 def test_stack_parity_full_size(moe, shape):
-    """The full stacks (10 GB / 15 GB resident), one step at M=1 and one at M=4.
-    The oracle regenerates only the experts each layer's router selects."""
+    """The full stacks (10 GB / 15 GB resident) at M=1 and M=4.
+
+    With random weights the stack is an iterated map that amplifies a
+    one-ulp difference in a bf16 residual (a rounding-boundary case where the
+    fp32 and fp64 sums land on either side) from layer to layer, so two
+    correct implementations drift apart over 24-48 layers.  The full-size
+    check therefore follows the GPU's own trajectory: the stack traced layer
+    by layer must end bit-identical to the graph-launched stack, and every
+    layer's transition r_l -> r_{l+1} must match the oracle's single layer
+    applied to the GPU's r_l.  The oracle regenerates only the experts each
+    layer's router selects."""
     L = shape.layers
     h = create_handle(shape, layers=L)
     try:
@@ -286,15 +296,22 @@ def test_stack_parity_full_size(moe, shape):
             load_layer(h, l, synth.layer_tensors(shape, l))
         for M in (1, 4):
             _, r, logits = synth.step_inputs(shape, 100 + M, M=M)
-            got = _run_stack(moe, h, r, logits, shape.top_k)
-            layers = []
+            final = _run_stack(moe, h, r, logits, shape.top_k)
+            rd = to_dev_bf16(r)
+            ld = torch.from_numpy(np.ascontiguousarray(logits)).cuda()
+            trace = torch.empty((L + 1, M, shape.hidden), dtype=torch.int16, device="cuda")
+            moe.moe_debug_stack_trace(h, rd, ld, M, shape.top_k, trace)
+            torch.cuda.synchronize()
+            tr = trace.cpu().numpy().view(np.uint16)
+            assert np.array_equal(tr[0], r)
+            assert np.array_equal(tr[L], final)           # same kernels, deterministic
             for l in range(L):
                 idx, _ = oracle.route(logits[l], shape.top_k)
-                layers.append(sparse_layer(shape, l, idx.ravel()))
-            ref = oracle.stack(shape.fmt, shape.hidden, shape.intermediate, shape.experts,
-                               shape.top_k, layers, logits, r, group=shape.group,
-                               nthreads=oracle.max_threads())
-            assert_parity(bf16_bits_to_f64(got), bf16_bits_to_f64(ref), ulps=1.0,
-                          what=f"{shape.name} M={M}")
+                t = sparse_layer(shape, l, idx.ravel())
+                ref = oracle.stack(shape.fmt, shape.hidden, shape.intermediate, shape.experts,
+                                   shape.top_k, [t], logits[l:l + 1], tr[l], group=shape.group,
+                                   nthreads=oracle.max_threads())
+                assert_parity(bf16_bits_to_f64(tr[l + 1]), bf16_bits_to_f64(ref), ulps=1.0,
+                              what=f"{shape.name} M={M} layer {l}")
     finally:
         moe.moe_destroy(h)
