@@ -53,18 +53,23 @@ struct moe_handle {
     moe_config cfg{};
     int device = 0;
     int num_sms = 0;
-    // per-layer tensor sizes in bytes (one layer, all experts)
+    // caller-layout tensor sizes in bytes (one layer, all experts)
     size_t gu_codes_b = 0, gu_scales_b = 0, gu_bias_b = 0;
     size_t dn_codes_b = 0, dn_scales_b = 0, dn_bias_b = 0;
+    // resident layout: per layer [gate_up slabs][down slabs][gu bias][dn bias]
+    int sb = 0;                       // scale bytes per (segment, g) entry
+    int gu_slab = 0, dn_slab = 0;     // bytes of one 16-row slab
+    size_t gu_expert = 0, dn_expert = 0;
     size_t layer_stride = 0;
-    size_t off_gu_scales = 0, off_gu_bias = 0, off_dn_codes = 0, off_dn_scales = 0, off_dn_bias = 0;
-    int sbh = 0, sbi = 0;
+    size_t off_dn = 0, off_gu_bias = 0, off_dn_bias = 0;
+    int slot_bytes = 0, nslots = 0, grid = 0;
     uint8_t* arena = nullptr;
+    uint32_t* special = nullptr;      // [L][E][2]
     std::vector<char> loaded;
     // workspace
     float* h = nullptr;
     float* ypart = nullptr;
-    unsigned int* tile_count = nullptr;
+    unsigned* counters = nullptr;     // done | hmax | slab_cnt | exit (see counter_words)
     int* stats = nullptr;   // distinct experts per layer of the last call
     int* status = nullptr;
     // staging for moe_forward_host
@@ -85,11 +90,11 @@ int check_cfg(const moe_config* c)
 {
     if (!c)
         return fail(MOE_ERR_INVALID_ARG, "moe_create: cfg is NULL");
-    if (c->hidden <= 0 || c->hidden % 32 || c->hidden > moe::kMaxK)
-        return fail(MOE_ERR_INVALID_ARG, "hidden=%d must be a positive multiple of 32, <= %d",
+    if (c->hidden <= 0 || c->hidden % 64 || c->hidden > moe::kMaxK)
+        return fail(MOE_ERR_INVALID_ARG, "hidden=%d must be a positive multiple of 64, <= %d",
                     c->hidden, moe::kMaxK);
-    if (c->intermediate <= 0 || c->intermediate % 32 || c->intermediate > moe::kMaxK)
-        return fail(MOE_ERR_INVALID_ARG, "intermediate=%d must be a positive multiple of 32, <= %d",
+    if (c->intermediate <= 0 || c->intermediate % 64 || c->intermediate > moe::kMaxK)
+        return fail(MOE_ERR_INVALID_ARG, "intermediate=%d must be a positive multiple of 64, <= %d",
                     c->intermediate, moe::kMaxK);
     if (c->num_experts < 1 || c->num_experts > moe::kMaxExperts)
         return fail(MOE_ERR_INVALID_ARG, "num_experts=%d must be in 1..%d", c->num_experts,
@@ -129,9 +134,10 @@ void free_handle(moe_handle* h)
     if (h->capture_stream)
         cudaStreamDestroy(h->capture_stream);
     cudaFree(h->arena);
+    cudaFree(h->special);
     cudaFree(h->h);
     cudaFree(h->ypart);
-    cudaFree(h->tile_count);
+    cudaFree(h->counters);
     cudaFree(h->stats);
     cudaFree(h->status);
     cudaFree(h->st_x);
@@ -158,23 +164,31 @@ moe::LayerParams layer_params(const moe_handle* h, int layer)
     const moe_config& c = h->cfg;
     const uint8_t* base = h->arena + (size_t)layer * h->layer_stride;
     moe::LayerParams p{};
-    p.gu_codes = base;
-    p.gu_scales = base + h->off_gu_scales;
+    p.gu = base;
+    p.dn = base + h->off_dn;
     p.gu_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(base + h->off_gu_bias) : nullptr;
-    p.dn_codes = base + h->off_dn_codes;
-    p.dn_scales = base + h->off_dn_scales;
     p.dn_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(base + h->off_dn_bias) : nullptr;
+    p.special = h->special + (size_t)layer * c.num_experts * 2;
     p.h = h->h;
     p.ypart = h->ypart;
-    p.tile_count = h->tile_count;
+    p.done = h->counters;
+    p.hmax = h->counters + moe::kMaxUnits;
+    p.slab_cnt = p.hmax + moe::kMaxUnits * moe::kMaxTokens;
+    p.exit_cnt = p.slab_cnt + c.hidden / moe::kSlabRows;
+    p.status = h->status;
     p.nu_out = h->stats + layer;
+    p.gu_expert_bytes = (long long)h->gu_expert;
+    p.dn_expert_bytes = (long long)h->dn_expert;
+    p.gu_slab_bytes = h->gu_slab;
+    p.dn_slab_bytes = h->dn_slab;
     p.H = c.hidden;
     p.I = c.intermediate;
     p.E = c.num_experts;
     p.kmax = c.max_top_k;
+    p.mmax = c.max_tokens;
     p.group = c.group;
-    p.sbh = h->sbh;
-    p.sbi = h->sbi;
+    p.nslots = h->nslots;
+    p.slot_bytes = h->slot_bytes;
     return p;
 }
 
@@ -218,26 +232,37 @@ int moe_create(const moe_config* cfg, moe_handle** out)
     h->cfg = *cfg;
     const moe_config& c = h->cfg;
     const size_t H = c.hidden, I = c.intermediate, E = c.num_experts;
-    h->sbh = c.format == MOE_FMT_MXFP4 ? (int)(H / 32) : (int)(2 * H / c.group);
-    h->sbi = c.format == MOE_FMT_MXFP4 ? (int)(I / 32) : (int)(2 * I / c.group);
+    const size_t sbh = c.format == MOE_FMT_MXFP4 ? H / 32 : 2 * H / c.group;
+    const size_t sbi = c.format == MOE_FMT_MXFP4 ? I / 32 : 2 * I / c.group;
     h->gu_codes_b = E * 2 * I * H / 2;
-    h->gu_scales_b = E * 2 * I * h->sbh;
+    h->gu_scales_b = E * 2 * I * sbh;
     h->gu_bias_b = c.has_bias ? E * 2 * I * 2 : 0;
     h->dn_codes_b = E * H * I / 2;
-    h->dn_scales_b = E * H * h->sbi;
+    h->dn_scales_b = E * H * sbi;
     h->dn_bias_b = c.has_bias ? E * H * 2 : 0;
-    size_t off = align_up(h->gu_codes_b, 256);
-    h->off_gu_scales = off;
-    off = align_up(off + h->gu_scales_b, 256);
+    h->sb = moe::scale_entry_bytes(c.format, c.group);
+    h->gu_slab = moe::slab_bytes((int)H, h->sb);
+    h->dn_slab = moe::slab_bytes((int)I, h->sb);
+    h->gu_expert = (2 * I / moe::kSlabRows) * (size_t)h->gu_slab;
+    h->dn_expert = (H / moe::kSlabRows) * (size_t)h->dn_slab;
+    size_t off = align_up(E * h->gu_expert, 256);
+    h->off_dn = off;
+    off = align_up(off + E * h->dn_expert, 256);
     h->off_gu_bias = off;
     off = align_up(off + h->gu_bias_b, 256);
-    h->off_dn_codes = off;
-    off = align_up(off + h->dn_codes_b, 256);
-    h->off_dn_scales = off;
-    off = align_up(off + h->dn_scales_b, 256);
     h->off_dn_bias = off;
     off = align_up(off + h->dn_bias_b, 256);
     h->layer_stride = off;
+    h->slot_bytes = (int)align_up((size_t)(h->gu_slab > h->dn_slab ? h->gu_slab : h->dn_slab), 128);
+    h->nslots = (int)((moe::kSmemBudget - moe::kRedBytes - moe::kXfragBytes -
+                       2 * (size_t)c.max_tokens * I * sizeof(float)) / h->slot_bytes);
+    if (h->nslots > moe::kMaxSlots)
+        h->nslots = moe::kMaxSlots;
+    if (h->nslots < 2) {
+        free_handle(h);
+        return fail(MOE_ERR_UNSUPPORTED, "a 16-row weight slab (%d bytes) is too large for the "
+                    "shared-memory ring", h->slot_bytes);
+    }
 
     cudaError_t e = cudaGetDevice(&h->device);
     if (e != cudaSuccess) {
@@ -249,11 +274,31 @@ int moe_create(const moe_config* cfg, moe_handle** out)
         free_handle(h);
         return cuda_fail(e, "cudaDeviceGetAttribute");
     }
+    {
+        int per_sm = 0;
+        moe::LayerParams lp{};
+        lp.nslots = h->nslots;
+        lp.slot_bytes = h->slot_bytes;
+        lp.mmax = c.max_tokens;
+        lp.I = c.intermediate;
+        e = moe::prepare_layer_kernel(c.format, c.group, moe::layer_smem_bytes(lp), &per_sm);
+        if (e != cudaSuccess) {
+            free_handle(h);
+            return cuda_fail(e, "layer kernel set-up");
+        }
+        if (per_sm < 1) {
+            free_handle(h);
+            return fail(MOE_ERR_UNSUPPORTED, "the layer kernel does not fit on an SM");
+        }
+        h->grid = h->num_sms;   // one CTA per SM: every CTA of a layer is resident at once
+    }
     const size_t Mx = c.max_tokens, Kx = c.max_top_k;
+    const size_t ncount = moe::counter_words((int)H);
     if ((rc = dev_alloc(&h->arena, h->layer_stride * c.num_layers, "expert weights")) ||
+        (rc = dev_alloc(&h->special, (size_t)c.num_layers * E * 2 * sizeof(uint32_t), "flags")) ||
         (rc = dev_alloc(&h->h, Mx * Kx * I * sizeof(float), "h workspace")) ||
         (rc = dev_alloc(&h->ypart, Mx * Kx * H * sizeof(float), "y workspace")) ||
-        (rc = dev_alloc(&h->tile_count, (H / moe::kRowsPerItem) * sizeof(unsigned), "tile counters")) ||
+        (rc = dev_alloc(&h->counters, ncount * sizeof(unsigned), "counters")) ||
         (rc = dev_alloc(&h->stats, c.num_layers * sizeof(int), "stats")) ||
         (rc = dev_alloc(&h->status, sizeof(int), "status")) ||
         (rc = dev_alloc(&h->st_x, Mx * H * 2, "staging x")) ||
@@ -262,7 +307,8 @@ int moe_create(const moe_config* cfg, moe_handle** out)
         free_handle(h);
         return rc;
     }
-    if ((e = cudaMemset(h->tile_count, 0, (H / moe::kRowsPerItem) * sizeof(unsigned))) != cudaSuccess ||
+    if ((e = cudaMemset(h->counters, 0, ncount * sizeof(unsigned))) != cudaSuccess ||
+        (e = cudaMemset(h->special, 0, (size_t)c.num_layers * E * 2 * sizeof(uint32_t))) != cudaSuccess ||
         (e = cudaMemset(h->stats, 0, c.num_layers * sizeof(int))) != cudaSuccess ||
         (e = cudaMemset(h->status, 0, sizeof(int))) != cudaSuccess ||
         (e = cudaStreamCreateWithFlags(&h->capture_stream, cudaStreamNonBlocking)) != cudaSuccess ||
@@ -308,27 +354,41 @@ int moe_load_experts(moe_handle* h, int layer, const void* gu_codes, const void*
     if (h->cfg.has_bias && (!gu_bias || !dn_bias))
         return fail(MOE_ERR_INVALID_ARG, "moe_load_experts: has_bias=1 but a bias pointer is NULL");
     cudaStream_t s = (cudaStream_t)stream;
+    const moe_config& c = h->cfg;
     uint8_t* base = h->arena + (size_t)layer * h->layer_stride;
-    struct {
-        void* dst;
-        const void* src;
-        size_t n;
-    } cp[6] = {{base, gu_codes, h->gu_codes_b},
-               {base + h->off_gu_scales, gu_scales, h->gu_scales_b},
-               {base + h->off_gu_bias, gu_bias, h->gu_bias_b},
-               {base + h->off_dn_codes, dn_codes, h->dn_codes_b},
-               {base + h->off_dn_scales, dn_scales, h->dn_scales_b},
-               {base + h->off_dn_bias, dn_bias, h->dn_bias_b}};
-    for (auto& c : cp) {
-        if (c.n == 0)
-            continue;
-        cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyDefault, s);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "moe_load_experts copy");
+    uint8_t* staging = nullptr;
+    const size_t st_bytes = align_up(h->gu_codes_b, 256) + align_up(h->gu_scales_b, 256) +
+                            align_up(h->dn_codes_b, 256) + align_up(h->dn_scales_b, 256);
+    int rc = dev_alloc(&staging, st_bytes, "load staging");
+    if (rc != MOE_OK)
+        return rc;
+    uint8_t* st_guc = staging;
+    uint8_t* st_gus = st_guc + align_up(h->gu_codes_b, 256);
+    uint8_t* st_dnc = st_gus + align_up(h->gu_scales_b, 256);
+    uint8_t* st_dns = st_dnc + align_up(h->dn_codes_b, 256);
+    uint32_t* special = h->special + (size_t)layer * c.num_experts * 2;
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(st_guc, gu_codes, h->gu_codes_b, cudaMemcpyDefault, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(st_gus, gu_scales, h->gu_scales_b, cudaMemcpyDefault, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(st_dnc, dn_codes, h->dn_codes_b, cudaMemcpyDefault, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(st_dns, dn_scales, h->dn_scales_b, cudaMemcpyDefault, s)) != cudaSuccess ||
+        (h->gu_bias_b && (e = cudaMemcpyAsync(base + h->off_gu_bias, gu_bias, h->gu_bias_b,
+                                              cudaMemcpyDefault, s)) != cudaSuccess) ||
+        (h->dn_bias_b && (e = cudaMemcpyAsync(base + h->off_dn_bias, dn_bias, h->dn_bias_b,
+                                              cudaMemcpyDefault, s)) != cudaSuccess) ||
+        (e = cudaMemsetAsync(special, 0, (size_t)c.num_experts * 2 * sizeof(uint32_t), s)) != cudaSuccess ||
+        (e = moe::launch_repack(c.format, c.group, st_guc, st_gus, c.num_experts, 2 * c.intermediate,
+                                c.hidden, base, (long long)h->gu_expert, h->gu_slab, special, 0, s)) !=
+            cudaSuccess ||
+        (e = moe::launch_repack(c.format, c.group, st_dnc, st_dns, c.num_experts, c.hidden,
+                                c.intermediate, base + h->off_dn, (long long)h->dn_expert, h->dn_slab,
+                                special, 1, s)) != cudaSuccess ||
+        (e = cudaStreamSynchronize(s)) != cudaSuccess) {
+        cudaStreamSynchronize(s);
+        cudaFree(staging);
+        return cuda_fail(e, "moe_load_experts");
     }
-    cudaError_t e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "moe_load_experts sync");
+    cudaFree(staging);
     h->loaded[layer] = 1;
     return MOE_OK;
 }
@@ -356,12 +416,12 @@ int moe_forward(moe_handle* h, int layer, const void* x_bf16, const float* route
     p.resid = static_cast<uint16_t*>(out_bf16);
     p.M = M;
     p.k = top_k;
-    cudaError_t e = moe::launch_layer(p, h->cfg.format, h->num_sms, (cudaStream_t)stream);
+    cudaError_t e = moe::launch_layer(p, h->cfg.format, h->grid, (cudaStream_t)stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "moe_forward launch");
     h->last_layers = 1;
     h->last_first_layer = layer;
-    h->last_launches = 2;
+    h->last_launches = 1;
     return MOE_OK;
 }
 
@@ -421,7 +481,7 @@ int moe_forward_stack(moe_handle* h, void* resid_bf16, const float* router_logit
             p.resid = static_cast<uint16_t*>(resid_bf16);
             p.M = M;
             p.k = top_k;
-            le = moe::launch_layer(p, h->cfg.format, h->num_sms, cs);
+            le = moe::launch_layer(p, h->cfg.format, h->grid, cs);
         }
         cudaGraph_t graph = nullptr;
         e = cudaStreamEndCapture(cs, &graph);
@@ -453,7 +513,7 @@ int moe_forward_stack(moe_handle* h, void* resid_bf16, const float* router_logit
         return cuda_fail(e, "moe_forward_stack launch");
     h->last_layers = L;
     h->last_first_layer = 0;
-    h->last_launches = 2 * L;
+    h->last_launches = L;
     return MOE_OK;
 }
 
@@ -482,7 +542,7 @@ int moe_debug_stack_trace(moe_handle* h, void* resid_bf16, const float* router_l
         p.resid = static_cast<uint16_t*>(resid_bf16);
         p.M = M;
         p.k = top_k;
-        e = moe::launch_layer(p, h->cfg.format, h->num_sms, s);
+        e = moe::launch_layer(p, h->cfg.format, h->grid, s);
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(tr + (size_t)(l + 1) * nb, resid_bf16, nb, cudaMemcpyDeviceToDevice, s);
     }
@@ -490,7 +550,7 @@ int moe_debug_stack_trace(moe_handle* h, void* resid_bf16, const float* router_l
         return cuda_fail(e, "moe_debug_stack_trace");
     h->last_layers = L;
     h->last_first_layer = 0;
-    h->last_launches = 2 * L;
+    h->last_launches = L;
     return MOE_OK;
 }
 
@@ -505,6 +565,13 @@ int moe_get_status(moe_handle* h, void* stream)
         (e = cudaMemcpy(&st, h->status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess ||
         (e = cudaMemset(h->status, 0, sizeof(int))) != cudaSuccess)
         return cuda_fail(e, "moe_get_status");
+    if (st != MOE_OK) {
+        // a call gave up waiting: its cross-CTA counters may be left part-way; clear them
+        const size_t ncount = moe::counter_words(h->cfg.hidden);
+        if ((e = cudaMemset(h->counters, 0, ncount * sizeof(unsigned))) != cudaSuccess ||
+            (e = cudaDeviceSynchronize()) != cudaSuccess)
+            return cuda_fail(e, "moe_get_status reset");
+    }
     return st;
 }
 
@@ -542,11 +609,10 @@ int moe_debug_dequant(moe_handle* h, int layer, int expert, int proj, float* out
     moe::LayerParams p = layer_params(h, layer);
     const int N = proj == 0 ? 2 * c.intermediate : c.hidden;
     const int K = proj == 0 ? c.hidden : c.intermediate;
-    const int sb = proj == 0 ? h->sbh : h->sbi;
-    const uint8_t* codes = (proj == 0 ? p.gu_codes : p.dn_codes) + (size_t)expert * N * (K / 2);
-    const uint8_t* scales = (proj == 0 ? p.gu_scales : p.dn_scales) + (size_t)expert * N * sb;
-    cudaError_t e = moe::launch_dequant(c.format, codes, scales, N, K, c.group, out_dev,
-                                        (cudaStream_t)stream);
+    const uint8_t* slabs = proj == 0 ? p.gu + (size_t)expert * h->gu_expert
+                                     : p.dn + (size_t)expert * h->dn_expert;
+    cudaError_t e = moe::launch_dequant(c.format, c.group, slabs, N, K, proj == 0 ? h->gu_slab : h->dn_slab,
+                                        out_dev, (cudaStream_t)stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "moe_debug_dequant launch");
     return MOE_OK;

@@ -1,5 +1,14 @@
 // moe_internal.h -- declarations shared by the C-ABI layer (moe_api.cu) and
 // the kernels (moe_decode.cu).  Not part of the public interface.
+//
+// Resident weight layout ("slabs").  Every expert projection W [N][K] is
+// stored as N/16 slabs of 16 consecutive rows.  A slab is
+//     [codes: K/64 segments x 32 lanes x 16 bytes][scales: K/64 x 8 x SB bytes]
+// where the 16 code bytes of (segment q, lane l) are exactly the A operands of
+// lane l for the four m16n8k16 MMAs that cover K = 64q .. 64q+63 (g = l/4,
+// t = l%4; word j holds rows g and g+8, elements 16j + {2t, 2t+1, 2t+8, 2t+9}),
+// and the SB scale bytes of (segment q, g) are the scales of rows g and g+8
+// for that segment.  A slab is contiguous, so one bulk copy moves it.
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -9,39 +18,71 @@ namespace moe {
 constexpr int kMaxTokens = 4;      // decode M
 constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 256;
-constexpr int kMaxUnits = kMaxTokens * kMaxTopK;   // distinct experts of one layer
-constexpr int kMaxK = 4096;        // largest H or I
-constexpr int kThreads = 384;      // threads per CTA of the decode kernels
-constexpr int kRowsPerItem = 8;    // rows of one work item (4 gate/up pairs, or 8 down rows)
+constexpr int kMaxUnits = kMaxTokens * kMaxTopK;   // distinct experts of one layer call
+constexpr int kMaxK = 3072;        // largest H or I (12 warps x 4 segments x 64)
+constexpr int kComputeWarps = 12;  // MMA warps of the layer kernel
+constexpr int kThreads = (kComputeWarps + 2) * 32;   // + a producer and a signalling warp
+constexpr int kMaxSegPerWarp = kMaxK / 64 / kComputeWarps;
+constexpr int kSlabRows = 16;
+constexpr int kMaxSlots = 8;       // depth of the shared-memory slab ring
+constexpr int kSmemBudget = 220 * 1024;    // dynamic shared memory of the layer kernel
+constexpr int kRedBytes = 2 * kComputeWarps * 32 * kMaxTokens * 4;
+constexpr int kXfragBytes = kComputeWarps * kMaxSegPerWarp * 4 * 32 * 8;   // x MMA fragments
 
 enum { FMT_MXFP4 = 1, FMT_INT4 = 2 };
 
-// One layer's resident weights and the per-call pointers of a decode forward.
+// Scale bytes per (segment, g) entry: MXFP4 4 (two E8M0 blocks x two rows),
+// int4 with one group per segment or more 4 (one fp16 x two rows), int4 with
+// 32-element groups 8 (two fp16 x two rows).
+inline __host__ __device__ int scale_entry_bytes(int fmt, int group)
+{
+    return fmt == FMT_MXFP4 ? 4 : (group == 32 ? 8 : 4);
+}
+inline __host__ __device__ int slab_bytes(int K, int sb) { return 8 * K + (K / 64) * 8 * sb; }
+
 struct LayerParams {
-    const uint8_t* gu_codes;   // [E][2I][H/2]
-    const uint8_t* gu_scales;  // [E][2I][sbh] bytes per row
-    const uint16_t* gu_bias;   // [E][2I] bf16, or nullptr
-    const uint8_t* dn_codes;   // [E][H][I/2]
-    const uint8_t* dn_scales;  // [E][H][sbi]
-    const uint16_t* dn_bias;   // [E][H] bf16, or nullptr
-    const float* logits;       // [M][E]
-    const uint16_t* x;         // [M][H] bf16 layer input, or nullptr: normalise resid
-    uint16_t* resid;           // [M][H] bf16 residual in, result out
-    float* h;                  // workspace [M][kmax][I]
-    float* ypart;              // workspace [M][kmax][H]
-    unsigned int* tile_count;  // workspace [H/8] arrival counters (zero between calls)
-    int* nu_out;               // distinct experts of this call (written by CTA 0)
-    int H, I, E, M, k, kmax, group;
-    int sbh, sbi;              // scale bytes per row of gate_up / down
+    const uint8_t* gu;          // gate_up slabs of expert 0; expert e at + e * gu_expert_bytes
+    const uint8_t* dn;          // down slabs
+    const uint16_t* gu_bias;    // [E][2I] bf16, or nullptr
+    const uint16_t* dn_bias;    // [E][H] bf16, or nullptr
+    const uint32_t* special;    // [E][2]: 1 if a projection holds an E8M0 byte 0 or 255
+    const float* logits;        // [M][E]
+    const uint16_t* x;          // [M][H] bf16 layer input, or nullptr: normalise resid
+    uint16_t* resid;            // [M][H] bf16 residual in, result out
+    float* h;                   // workspace [M][kmax][I]
+    float* ypart;               // workspace [M][kmax][H]
+    unsigned* done;             // [kMaxUnits] gate_up slab-pairs finished per unit (zero between calls)
+    unsigned* hmax;             // [kMaxUnits][kMaxTokens] bits of max |h| (zero between calls)
+    unsigned* slab_cnt;         // [H/16] units finished per down slab (zero between calls)
+    unsigned* exit_cnt;         // [1] CTAs finished (zero between calls)
+    int* status;                // device status word
+    int* nu_out;                // distinct experts of this call (written by CTA 0)
+    long long gu_expert_bytes, dn_expert_bytes;
+    int gu_slab_bytes, dn_slab_bytes;
+    int H, I, E, M, k, kmax, mmax, group;
+    int nslots, slot_bytes;
 };
 
-// Launch the two kernels of one decode layer on `stream` (programmatic
-// dependent launch between them and towards the preceding kernel).
-cudaError_t launch_layer(const LayerParams& p, int fmt, int num_sms, cudaStream_t stream);
+// Counters of one handle: done | hmax | slab_cnt | exit.
+inline size_t counter_words(int H) { return kMaxUnits + kMaxUnits * kMaxTokens + H / kSlabRows + 1; }
+
+// Launch the layer kernel on `stream` (programmatic dependent launch towards
+// the preceding kernel).  grid = one CTA per SM.
+cudaError_t launch_layer(const LayerParams& p, int fmt, int grid, cudaStream_t stream);
+// Dynamic shared memory the layer kernel needs, and its one-time set-up.
+size_t layer_smem_bytes(const LayerParams& p);
+cudaError_t prepare_layer_kernel(int fmt, int group, size_t smem, int* blocks_per_sm);
+
+// Caller layout -> slabs for E experts of one projection ([E][N][K/2] codes,
+// [E][N][K/32] u8 or [E][N][K/group] fp16 scales).  special[e * 2 + proj]
+// gets 1 if an E8M0 byte is 0 or 255.
+cudaError_t launch_repack(int fmt, int group, const uint8_t* codes, const uint8_t* scales, int E,
+                          int N, int K, uint8_t* out, long long expert_bytes, int slab_bytes,
+                          uint32_t* special, int proj, cudaStream_t stream);
 
 // Debug kernels.
-cudaError_t launch_dequant(int fmt, const uint8_t* codes, const uint8_t* scales, int N, int K,
-                           int group, float* out, cudaStream_t stream);
+cudaError_t launch_dequant(int fmt, int group, const uint8_t* slabs, int N, int K, int slab_bytes,
+                           float* out, cudaStream_t stream);
 cudaError_t launch_route(const float* logits, int M, int E, int k, int* idx, float* w,
                          cudaStream_t stream);
 

@@ -49,6 +49,11 @@
  *   - Failures detected on the device (a bounded wait that gave up, an index
  *     out of range) set the handle's status word; read it with
  *     moe_get_status().  Device code never traps.
+ *   - A layer runs as one persistent launch with one CTA per SM whose CTAs
+ *     wait for one another (the down GEMV of an expert starts once every CTA
+ *     has finished that expert's gate_up rows).  Work that other streams run
+ *     at the same time can delay it; each wait gives up after about a second
+ *     and reports MOE_ERR_DEVICE_TIMEOUT instead of hanging.
  */
 #ifndef MOE_H
 #define MOE_H
@@ -86,9 +91,11 @@ typedef struct {
 
 /* Validate cfg and create a handle on the current CUDA device.  Allocates
  * the resident weight arena for all L layers plus a fixed workspace.
- * Requirements: H and I multiples of 32 and at most 4096; E in 1..256;
+ * Requirements: H and I multiples of 64 and at most 3072; E in 1..256;
  * max_top_k in 1..min(E, 16); max_tokens in 1..4; MXFP4 needs group == 32;
- * int4 needs group a multiple of 32 dividing both H and I.
+ * int4 needs group a multiple of 32 dividing both H and I.  Weights are
+ * repacked at load into 16-row slabs whose bytes are the MMA operands of the
+ * decode kernel (see the layout note in the library source).
  * On success *out receives the handle; on failure *out is set to NULL. */
 int moe_create(const moe_config* cfg, moe_handle** out);
 
@@ -124,12 +131,14 @@ int moe_forward_host(moe_handle* h, int layer, const void* x_bf16, const float* 
  *   r_{l+1} = bf16(r_l + MoE_l(x_l))
  * resid bf16 [M][H] holds r_0 on entry and r_L on return; logits fp32
  * [L][M][E].  Layer l+1 reads its logits only after layer l's output is
- * complete.  Device pointers.  Launched as a cached CUDA graph per (M, top_k). */
+ * complete.  Device pointers.  Launched as a cached CUDA graph of L
+ * programmatically chained layer kernels per (M, top_k, resid, logits). */
 int moe_forward_stack(moe_handle* h, void* resid_bf16, const float* router_logits,
                       int M, int top_k, void* stream);
 
 /* Synchronise `stream` and return (and clear) the handle's device status:
- * MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_FAULT. */
+ * MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_FAULT.  After a non-OK
+ * status the handle's cross-CTA counters are reset, so it can be used again. */
 int moe_get_status(moe_handle* h, void* stream);
 
 /* Debug: decode one stored expert projection to fp32, exactly (each element

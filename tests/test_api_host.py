@@ -41,6 +41,7 @@ def _cfg(**kw):
 
 @pytest.mark.parametrize("bad,needle", [
     (dict(hidden=100), "hidden"), (dict(hidden=0), "hidden"), (dict(hidden=8192), "hidden"),
+    (dict(hidden=96), "hidden"), (dict(intermediate=3136), "intermediate"),
     (dict(intermediate=48), "intermediate"), (dict(num_experts=0), "num_experts"),
     (dict(num_experts=300), "num_experts"), (dict(num_layers=0), "num_layers"),
     (dict(max_tokens=0), "max_tokens"), (dict(max_tokens=5), "max_tokens"),

@@ -120,7 +120,7 @@ def test_route_matches_oracle(moe, E, k):
 
 SMALL = [
     synth.TINY,
-    synth.Shape("ragged H=160 I=96 E=5 top-3", 160, 96, 5, 3, e8m0_lo=118, e8m0_hi=124,
+    synth.Shape("ragged H=192 I=320 E=5 top-3", 192, 320, 5, 3, e8m0_lo=118, e8m0_hi=124,
                 bias_sigma=0.5, seed=11),
     synth.Shape("int4 H=128 I=64 E=6 top-2", 128, 64, 6, 2, fmt=synth.FMT_INT4, group=64,
                 has_bias=False, seed=12),
