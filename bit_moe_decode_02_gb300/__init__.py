@@ -8,7 +8,7 @@ library fails loudly (build it with ``python -m bit_moe_decode_02_gb300.build_ex
 The function names are the C names: moe_create, moe_load_experts, moe_forward,
 moe_forward_host, moe_forward_stack, moe_get_status, moe_debug_dequant,
 moe_debug_route, moe_debug_stack_trace, moe_last_bytes, moe_expert_bytes, moe_last_launches,
-moe_last_error, moe_destroy.
+moe_last_error, moe_forward_noalloc, moe_destroy.
 """
 from __future__ import annotations
 
@@ -34,7 +34,7 @@ EXPORTS = ("moe_create", "moe_load_experts", "moe_forward", "moe_forward_host",
            "moe_forward_stack", "moe_get_status", "moe_debug_dequant", "moe_debug_route",
            "moe_debug_stack_trace",
            "moe_last_bytes", "moe_expert_bytes", "moe_last_launches", "moe_last_error",
-           "moe_destroy")
+           "moe_forward_noalloc", "moe_destroy")
 
 
 class MoeError(RuntimeError):
@@ -87,6 +87,9 @@ def lib() -> ctypes.CDLL:
         L.moe_last_launches.restype = i
         L.moe_last_error.argtypes = []
         L.moe_last_error.restype = ctypes.c_char_p
+        L.moe_forward_noalloc.argtypes = [ctypes.POINTER(moe_config), p, p, p, p, p, p, p, p, i, i,
+                                          p, p]
+        L.moe_forward_noalloc.restype = i
         L.moe_destroy.argtypes = [p]
         L.moe_destroy.restype = None
         _lib = L
@@ -183,6 +186,17 @@ def moe_expert_bytes(h) -> int:
 
 def moe_last_launches(h) -> int:
     return lib().moe_last_launches(h)
+
+
+def moe_forward_noalloc(cfg: moe_config, gu_codes, gu_scales, gu_bias, dn_codes, dn_scales, dn_bias,
+                        x, logits, M, top_k, out, stream=None):
+    """The allocation-free layer forward (see include/moe.h): caller-layout
+    weights, inputs and outputs are all caller memory; scratch is the
+    library's fixed device array."""
+    return _check(lib().moe_forward_noalloc(ctypes.byref(cfg), _ptr(gu_codes), _ptr(gu_scales),
+                                            _ptr(gu_bias), _ptr(dn_codes), _ptr(dn_scales),
+                                            _ptr(dn_bias), _ptr(x), _ptr(logits), M, top_k,
+                                            _ptr(out), _stream(stream)))
 
 
 def moe_destroy(h) -> None:

@@ -49,6 +49,15 @@ struct StackGraph {
 
 }  // namespace
 
+int moe::set_error(int code, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
 struct moe_handle {
     moe_config cfg{};
     int device = 0;

@@ -80,6 +80,10 @@ cudaError_t launch_repack(int fmt, int group, const uint8_t* codes, const uint8_
                           int N, int K, uint8_t* out, long long expert_bytes, int slab_bytes,
                           uint32_t* special, int proj, cudaStream_t stream);
 
+// Record the calling thread's error message (read by moe_last_error) and
+// return `code`.
+int set_error(int code, const char* fmt, ...);
+
 // Debug kernels.
 cudaError_t launch_dequant(int fmt, int group, const uint8_t* slabs, int N, int K, int slab_bytes,
                            float* out, cudaStream_t stream);

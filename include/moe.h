@@ -177,6 +177,39 @@ int moe_last_launches(const moe_handle* h);
 /* Message for the calling thread's most recent failure ("" if none). */
 const char* moe_last_error(void);
 
+/* One decode layer for callers that cannot allocate device memory.
+ *
+ * The pages describe no such call; it exists for users of this library whose
+ * runtime forbids cudaMalloc: an inference engine that serves every buffer
+ * from its own pre-sized pool, code running while a CUDA graph is captured, or
+ * a plug-in that may not touch the CUDA allocator.  Such a caller cannot create
+ * a moe_handle (moe_create allocates), so here every input and output is the
+ * caller's memory and the call allocates nothing: no cudaMalloc, cudaFree or
+ * allocating library routine.
+ *
+ * Computes the same layer as moe_forward: out = r + sum_s w_s * y_s for the
+ * top_k experts of each token.  The weights are the caller-layout tensors of
+ * moe_load_experts for one layer (E experts), on the device; x bf16 [M][H],
+ * router_logits fp32 [M][E] and out bf16 [M][H] (the residual on entry) are
+ * device pointers; x must not overlap out.  cfg gives H, I, E, format, group
+ * and has_bias (its num_layers, max_tokens and max_top_k are ignored).
+ *
+ * Scratch (h, the per-slot down outputs and the output-tile counters) is one
+ * file-scope __device__ array of 1,574,400 bytes that every GPU which loads the
+ * library holds until the process exits.  It fixes the limits: M <= 4,
+ * top_k <= 16, H and I multiples of 32 and at most 3072; larger sizes return
+ * MOE_ERR_INVALID_ARG with a message.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) for that device; make that
+ * first call before any stream capture.  Every call uses the same array, and
+ * it keeps the contents of the last call (the tile counters are cleared at the
+ * start of each call), so calls that overlap on the GPU -- on two streams, or
+ * from two threads -- race and must be serialised by the caller.  Runs
+ * asynchronously on `stream`. */
+int moe_forward_noalloc(const moe_config* cfg, const void* gu_codes, const void* gu_scales,
+                        const void* gu_bias, const void* dn_codes, const void* dn_scales,
+                        const void* dn_bias, const void* x_bf16, const float* router_logits,
+                        int M, int top_k, void* out_bf16, void* stream);
+
 /* Release a handle and all device memory it owns.  NULL is a no-op. */
 void moe_destroy(moe_handle* h);
 
