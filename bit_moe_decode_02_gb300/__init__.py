@@ -32,7 +32,7 @@ MOE_FMT_INT4 = 2
 # every symbol include/moe.h declares
 EXPORTS = ("moe_create", "moe_load_experts", "moe_forward", "moe_forward_host",
            "moe_forward_stack", "moe_get_status", "moe_debug_dequant", "moe_debug_route",
-           "moe_debug_stack_trace",
+           "moe_debug_stack_trace", "moe_debug_mx_quantize", "moe_debug_batched_h",
            "moe_last_bytes", "moe_expert_bytes", "moe_last_launches", "moe_last_error",
            "moe_forward_noalloc", "moe_destroy")
 
@@ -79,6 +79,10 @@ def lib() -> ctypes.CDLL:
         L.moe_debug_route.restype = i
         L.moe_debug_stack_trace.argtypes = [p, p, p, i, i, p, p]
         L.moe_debug_stack_trace.restype = i
+        L.moe_debug_mx_quantize.argtypes = [p, ll, p, p, p]
+        L.moe_debug_mx_quantize.restype = i
+        L.moe_debug_batched_h.argtypes = [p, p, p, p]
+        L.moe_debug_batched_h.restype = i
         L.moe_last_bytes.argtypes = [p, p, ctypes.POINTER(ll)]
         L.moe_last_bytes.restype = i
         L.moe_expert_bytes.argtypes = [p]
@@ -172,6 +176,14 @@ def moe_debug_route(h, logits, M, top_k, idx, w, stream=None):
 def moe_debug_stack_trace(h, resid, logits, M, top_k, trace, stream=None):
     return _check(lib().moe_debug_stack_trace(h, _ptr(resid), _ptr(logits), M, top_k, _ptr(trace),
                                               _stream(stream)))
+
+
+def moe_debug_mx_quantize(x, n, codes, scales, stream=None):
+    return _check(lib().moe_debug_mx_quantize(_ptr(x), n, _ptr(codes), _ptr(scales), _stream(stream)))
+
+
+def moe_debug_batched_h(h, codes, scales, stream=None):
+    return _check(lib().moe_debug_batched_h(h, _ptr(codes), _ptr(scales), _stream(stream)))
 
 
 def moe_last_bytes(h, stream=None) -> int:

@@ -75,6 +75,21 @@ struct moe_handle {
     uint8_t* arena = nullptr;
     uint32_t* special = nullptr;      // [L][E][2]
     std::vector<char> loaded;
+    // batched path (max_tokens > kMaxTokens): tile-layout copy of the weights
+    bool batched = false;
+    size_t t_gu_expert = 0, t_dn_expert = 0, t_off_dn = 0, t_layer_stride = 0;
+    uint8_t* tarena = nullptr;
+    int max_tiles = 0;
+    int* b_int = nullptr;             // idx | slot | etile | erow | ntiles
+    float* b_wt = nullptr;
+    moe::TokTile* b_tiles = nullptr;
+    uint8_t* b_xq = nullptr;
+    uint8_t* b_xsf = nullptr;
+    uint8_t* b_hq = nullptr;
+    uint8_t* b_hsf = nullptr;
+    float* b_h = nullptr;
+    float* b_y = nullptr;
+    int last_bM = 0, last_bk = 0;     // M and top_k of the last batched call
     // workspace
     float* h = nullptr;
     float* ypart = nullptr;
@@ -110,9 +125,9 @@ int check_cfg(const moe_config* c)
                     moe::kMaxExperts);
     if (c->num_layers < 1)
         return fail(MOE_ERR_INVALID_ARG, "num_layers=%d must be >= 1", c->num_layers);
-    if (c->max_tokens < 1 || c->max_tokens > moe::kMaxTokens)
+    if (c->max_tokens < 1 || c->max_tokens > moe::kMaxBatchTokens)
         return fail(MOE_ERR_INVALID_ARG, "max_tokens=%d must be in 1..%d", c->max_tokens,
-                    moe::kMaxTokens);
+                    moe::kMaxBatchTokens);
     if (c->max_top_k < 1 || c->max_top_k > moe::kMaxTopK || c->max_top_k > c->num_experts)
         return fail(MOE_ERR_INVALID_ARG, "max_top_k=%d must be in 1..min(num_experts, %d)",
                     c->max_top_k, moe::kMaxTopK);
@@ -130,6 +145,9 @@ int check_cfg(const moe_config* c)
     }
     if (c->has_bias != 0 && c->has_bias != 1)
         return fail(MOE_ERR_INVALID_ARG, "has_bias must be 0 or 1");
+    if (c->max_tokens > moe::kMaxTokens && c->format != MOE_FMT_MXFP4)
+        return fail(MOE_ERR_UNSUPPORTED, "max_tokens=%d > %d (the tensor-core batched path) needs "
+                    "MOE_FMT_MXFP4", c->max_tokens, moe::kMaxTokens);
     return MOE_OK;
 }
 
@@ -152,6 +170,16 @@ void free_handle(moe_handle* h)
     cudaFree(h->st_x);
     cudaFree(h->st_out);
     cudaFree(h->st_logits);
+    cudaFree(h->tarena);
+    cudaFree(h->b_int);
+    cudaFree(h->b_wt);
+    cudaFree(h->b_tiles);
+    cudaFree(h->b_xq);
+    cudaFree(h->b_xsf);
+    cudaFree(h->b_hq);
+    cudaFree(h->b_hsf);
+    cudaFree(h->b_h);
+    cudaFree(h->b_y);
     delete h;
 }
 
@@ -166,6 +194,12 @@ int dev_alloc(T** p, size_t bytes, const char* what)
                     cudaGetErrorString(e));
     }
     return MOE_OK;
+}
+
+// Token capacity of the decode kernel's workspace and shared memory.
+int decode_tokens(const moe_config& c)
+{
+    return c.max_tokens < moe::kMaxTokens ? c.max_tokens : moe::kMaxTokens;
 }
 
 moe::LayerParams layer_params(const moe_handle* h, int layer)
@@ -194,10 +228,76 @@ moe::LayerParams layer_params(const moe_handle* h, int layer)
     p.I = c.intermediate;
     p.E = c.num_experts;
     p.kmax = c.max_top_k;
-    p.mmax = c.max_tokens;
+    p.mmax = decode_tokens(c);
     p.group = c.group;
     p.nslots = h->nslots;
     p.slot_bytes = h->slot_bytes;
+    return p;
+}
+
+// Tile-layout weights and the workspace of the batched path.
+int create_batched(moe_handle* h)
+{
+    const moe_config& c = h->cfg;
+    const int H = c.hidden, I = c.intermediate, E = c.num_experts;
+    const size_t Mk = (size_t)c.max_tokens * c.max_top_k;
+    h->batched = true;
+    h->t_gu_expert = 2 * (size_t)moe::tile_proj_bytes(I, H);
+    h->t_dn_expert = (size_t)moe::tile_proj_bytes(H, I);
+    h->t_off_dn = align_up(E * h->t_gu_expert, 256);
+    h->t_layer_stride = align_up(h->t_off_dn + E * h->t_dn_expert, 256);
+    h->max_tiles = moe::max_tok_tiles((int)Mk, E);
+    const size_t rows = Mk + 16 * (size_t)h->max_tiles;   // padded activation rows, upper bound
+    int rc;
+    if ((rc = dev_alloc(&h->tarena, h->t_layer_stride * c.num_layers, "tile-layout weights")) ||
+        (rc = dev_alloc(&h->b_int, (4 * Mk + 1) * sizeof(int), "batched tables")) ||
+        (rc = dev_alloc(&h->b_wt, Mk * sizeof(float), "routing weights")) ||
+        (rc = dev_alloc(&h->b_tiles, h->max_tiles * sizeof(moe::TokTile), "token tiles")) ||
+        (rc = dev_alloc(&h->b_xq, rows * H / 2, "x codes")) ||
+        (rc = dev_alloc(&h->b_xsf, (size_t)h->max_tiles * moe::ceil_div(H, 128) * moe::kSfChunk, "x scales")) ||
+        (rc = dev_alloc(&h->b_hq, rows * I / 2, "h codes")) ||
+        (rc = dev_alloc(&h->b_hsf, (size_t)h->max_tiles * moe::ceil_div(I, 128) * moe::kSfChunk, "h scales")) ||
+        (rc = dev_alloc(&h->b_h, Mk * I * sizeof(float), "batched h")) ||
+        (rc = dev_alloc(&h->b_y, Mk * H * sizeof(float), "batched y")))
+        return rc;
+    cudaError_t e = moe::prepare_batched_kernels();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "batched kernel set-up");
+    return MOE_OK;
+}
+
+moe::BatchParams batch_params(const moe_handle* h, int layer)
+{
+    const moe_config& c = h->cfg;
+    const size_t Mk = (size_t)c.max_tokens * c.max_top_k;
+    const uint8_t* tb = h->tarena + (size_t)layer * h->t_layer_stride;
+    const uint8_t* sb = h->arena + (size_t)layer * h->layer_stride;
+    moe::BatchParams p{};
+    p.gu = tb;
+    p.dn = tb + h->t_off_dn;
+    p.gu_expert = (long long)h->t_gu_expert;
+    p.dn_expert = (long long)h->t_dn_expert;
+    p.gu_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(sb + h->off_gu_bias) : nullptr;
+    p.dn_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(sb + h->off_dn_bias) : nullptr;
+    p.idx = h->b_int;
+    p.slot = h->b_int + Mk;
+    p.etile = h->b_int + 2 * Mk;
+    p.erow = h->b_int + 3 * Mk;
+    p.ntiles = h->b_int + 4 * Mk;
+    p.wt = h->b_wt;
+    p.tiles = h->b_tiles;
+    p.xq = h->b_xq;
+    p.xsf = h->b_xsf;
+    p.hq = h->b_hq;
+    p.hsf = h->b_hsf;
+    p.h = h->b_h;
+    p.y = h->b_y;
+    p.status = h->status;
+    p.nu_out = h->stats + layer;
+    p.H = c.hidden;
+    p.I = c.intermediate;
+    p.E = c.num_experts;
+    p.max_tiles = h->max_tiles;
     return p;
 }
 
@@ -220,6 +320,25 @@ int check_forward_args(const moe_handle* h, int M, int top_k)
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Caller layout -> tile layout for one layer (gate rows [0, I) and up rows
+// [I, 2I) of gate_up become two projections of I rows each).
+cudaError_t load_tiles(moe_handle* h, int layer, const uint8_t* guc, const uint8_t* gus,
+                       const uint8_t* dnc, const uint8_t* dns, cudaStream_t s)
+{
+    const moe_config& c = h->cfg;
+    const int H = c.hidden, I = c.intermediate, E = c.num_experts;
+    uint8_t* tb = h->tarena + (size_t)layer * h->t_layer_stride;
+    const long long proj = moe::tile_proj_bytes(I, H);
+    cudaError_t e;
+    if ((e = moe::launch_repack_tiles(guc, gus, E, 2 * I, 0, I, H, tb, (long long)h->t_gu_expert, s)) !=
+            cudaSuccess ||
+        (e = moe::launch_repack_tiles(guc, gus, E, 2 * I, I, I, H, tb + proj, (long long)h->t_gu_expert,
+                                      s)) != cudaSuccess)
+        return e;
+    return moe::launch_repack_tiles(dnc, dns, E, H, 0, H, I, tb + h->t_off_dn, (long long)h->t_dn_expert,
+                                    s);
+}
 
 }  // namespace
 
@@ -264,7 +383,7 @@ int moe_create(const moe_config* cfg, moe_handle** out)
     h->layer_stride = off;
     h->slot_bytes = (int)align_up((size_t)(h->gu_slab > h->dn_slab ? h->gu_slab : h->dn_slab), 128);
     h->nslots = (int)((moe::kSmemBudget - moe::kRedBytes - moe::kXfragBytes -
-                       2 * (size_t)c.max_tokens * I * sizeof(float)) / h->slot_bytes);
+                       2 * (size_t)decode_tokens(c) * I * sizeof(float)) / h->slot_bytes);
     if (h->nslots > moe::kMaxSlots)
         h->nslots = moe::kMaxSlots;
     if (h->nslots < 2) {
@@ -288,7 +407,7 @@ int moe_create(const moe_config* cfg, moe_handle** out)
         moe::LayerParams lp{};
         lp.nslots = h->nslots;
         lp.slot_bytes = h->slot_bytes;
-        lp.mmax = c.max_tokens;
+        lp.mmax = decode_tokens(c);
         lp.I = c.intermediate;
         e = moe::prepare_layer_kernel(c.format, c.group, moe::layer_smem_bytes(lp), &per_sm);
         if (e != cudaSuccess) {
@@ -301,12 +420,12 @@ int moe_create(const moe_config* cfg, moe_handle** out)
         }
         h->grid = h->num_sms;   // one CTA per SM: every CTA of a layer is resident at once
     }
-    const size_t Mx = c.max_tokens, Kx = c.max_top_k;
+    const size_t Mx = c.max_tokens, Kx = c.max_top_k, Md = decode_tokens(c);
     const size_t ncount = moe::counter_words((int)H);
     if ((rc = dev_alloc(&h->arena, h->layer_stride * c.num_layers, "expert weights")) ||
         (rc = dev_alloc(&h->special, (size_t)c.num_layers * E * 2 * sizeof(uint32_t), "flags")) ||
-        (rc = dev_alloc(&h->h, Mx * Kx * I * sizeof(float), "h workspace")) ||
-        (rc = dev_alloc(&h->ypart, Mx * Kx * H * sizeof(float), "y workspace")) ||
+        (rc = dev_alloc(&h->h, Md * Kx * I * sizeof(float), "h workspace")) ||
+        (rc = dev_alloc(&h->ypart, Md * Kx * H * sizeof(float), "y workspace")) ||
         (rc = dev_alloc(&h->counters, ncount * sizeof(unsigned), "counters")) ||
         (rc = dev_alloc(&h->stats, c.num_layers * sizeof(int), "stats")) ||
         (rc = dev_alloc(&h->status, sizeof(int), "status")) ||
@@ -324,6 +443,10 @@ int moe_create(const moe_config* cfg, moe_handle** out)
         (e = cudaDeviceSynchronize()) != cudaSuccess) {
         free_handle(h);
         return cuda_fail(e, "moe_create setup");
+    }
+    if (c.max_tokens > moe::kMaxTokens && (rc = create_batched(h)) != MOE_OK) {
+        free_handle(h);
+        return rc;
     }
     h->loaded.assign(c.num_layers, 0);
     *out = h;
@@ -392,6 +515,7 @@ int moe_load_experts(moe_handle* h, int layer, const void* gu_codes, const void*
         (e = moe::launch_repack(c.format, c.group, st_dnc, st_dns, c.num_experts, c.hidden,
                                 c.intermediate, base + h->off_dn, (long long)h->dn_expert, h->dn_slab,
                                 special, 1, s)) != cudaSuccess ||
+        (h->batched && (e = load_tiles(h, layer, st_guc, st_gus, st_dnc, st_dns, s)) != cudaSuccess) ||
         (e = cudaStreamSynchronize(s)) != cudaSuccess) {
         cudaStreamSynchronize(s);
         cudaFree(staging);
@@ -419,6 +543,24 @@ int moe_forward(moe_handle* h, int layer, const void* x_bf16, const float* route
         return fail(MOE_ERR_INVALID_ARG, "moe_forward: x overlaps out");
     if (!h->loaded[layer])
         return fail(MOE_ERR_NOT_LOADED, "moe_forward: layer %d has no experts loaded", layer);
+    if (M > moe::kMaxTokens) {
+        moe::BatchParams b = batch_params(h, layer);
+        b.logits = router_logits;
+        b.x = static_cast<const uint16_t*>(x_bf16);
+        b.resid = static_cast<uint16_t*>(out_bf16);
+        b.M = M;
+        b.k = top_k;
+        int launches = 0;
+        cudaError_t e = moe::launch_batched(b, h->num_sms, (cudaStream_t)stream, &launches);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "moe_forward (batched) launch");
+        h->last_layers = 1;
+        h->last_first_layer = layer;
+        h->last_launches = launches;
+        h->last_bM = M;
+        h->last_bk = top_k;
+        return MOE_OK;
+    }
     moe::LayerParams p = layer_params(h, layer);
     p.logits = router_logits;
     p.x = static_cast<const uint16_t*>(x_bf16);
@@ -464,6 +606,9 @@ int moe_forward_stack(moe_handle* h, void* resid_bf16, const float* router_logit
     int rc = check_forward_args(h, M, top_k);
     if (rc != MOE_OK)
         return rc;
+    if (M > moe::kMaxTokens)
+        return fail(MOE_ERR_UNSUPPORTED, "moe_forward_stack: M=%d > %d; the stack runs the decode kernel only", M,
+                    moe::kMaxTokens);
     if (!resid_bf16 || !router_logits)
         return fail(MOE_ERR_INVALID_ARG, "moe_forward_stack: resid and logits must not be NULL");
     if (!aligned16(resid_bf16) || !aligned16(router_logits))
@@ -532,6 +677,9 @@ int moe_debug_stack_trace(moe_handle* h, void* resid_bf16, const float* router_l
     int rc = check_forward_args(h, M, top_k);
     if (rc != MOE_OK)
         return rc;
+    if (M > moe::kMaxTokens)
+        return fail(MOE_ERR_UNSUPPORTED, "moe_debug_stack_trace: M=%d > %d; the stack runs the decode kernel only", M,
+                    moe::kMaxTokens);
     if (!resid_bf16 || !router_logits || !trace_bf16)
         return fail(MOE_ERR_INVALID_ARG, "moe_debug_stack_trace: NULL argument");
     if (!aligned16(resid_bf16) || !aligned16(router_logits))
@@ -641,6 +789,38 @@ int moe_debug_route(moe_handle* h, const float* logits, int M, int top_k, int* i
                                       (cudaStream_t)stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "moe_debug_route launch");
+    return MOE_OK;
+}
+
+int moe_debug_mx_quantize(const float* in, long long n, unsigned char* codes, unsigned char* scales,
+                          void* stream)
+{
+    if (!in || !codes || !scales)
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_mx_quantize: NULL argument");
+    if (n < 0 || n % 32)
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_mx_quantize: n=%lld must be a non-negative multiple of 32", n);
+    if (!aligned16(in) || !aligned16(codes))
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_mx_quantize: in and codes must be 16-byte aligned");
+    cudaError_t e = moe::launch_mx_quantize(in, n, codes, scales, (cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "moe_debug_mx_quantize launch");
+    return MOE_OK;
+}
+
+int moe_debug_batched_h(moe_handle* h, unsigned char* codes, unsigned char* scales, void* stream)
+{
+    if (!h || !codes || !scales)
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_batched_h: NULL argument");
+    if (!aligned16(codes))
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_batched_h: codes must be 16-byte aligned");
+    if (!h->batched || h->last_bM == 0)
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_batched_h: no batched forward has run on this handle");
+    moe::BatchParams b = batch_params(h, 0);
+    b.M = h->last_bM;
+    b.k = h->last_bk;
+    cudaError_t e = moe::launch_untile_h(b, codes, scales, (cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "moe_debug_batched_h launch");
     return MOE_OK;
 }
 

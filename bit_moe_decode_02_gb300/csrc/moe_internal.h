@@ -84,6 +84,90 @@ cudaError_t launch_repack(int fmt, int group, const uint8_t* codes, const uint8_
 // return `code`.
 int set_error(int code, const char* fmt, ...);
 
+// ------------------------------------------------------------------ batched
+// Calls with M > kMaxTokens run per-expert grouped GEMMs on the tensor cores
+// (tcgen05.mma kind::mxf4: MXFP4 weights x MXFP4-quantised activations, fp32
+// accumulators in tensor memory).  Weights are kept a second time in a "tile"
+// layout made for that instruction.
+//
+// Tile layout of one projection W [N][K] (N, K multiples of 64).  Row tile t
+// covers rows 128t .. 128t + R_t - 1 (R_t = 128, or N % 128 for the last one),
+// k-step s covers K = 64s .. 64s + 63.
+//   codes  at t*128*K/2 + s*R_t*32: an R_t x 32-byte block in the canonical
+//          no-swizzle K-major order -- row r, byte b at
+//          (r/8)*256 + (b/16)*128 + (r%8)*16 + b%16 (8x16-byte core matrices;
+//          K-direction stride 128, row-group stride 256).
+//   scales at N*K/2 + (t*C + c)*512, C = ceil(K/128): chunk c holds the E8M0
+//          bytes of K-blocks 4c..4c+3 of the tile's 128 rows, row r = i + 32j
+//          and block kb at i*16 + j*4 + kb (the order a 32x128-bit tensor-memory
+//          copy replicated to the four lane quarters expects).
+// Activations (x, h) use the same two orders per token tile: codes
+// [k-step][npad rows x 32 bytes], scales [chunk][512].
+constexpr int kMaxBatchTokens = 8192;
+constexpr int kTokTile = 112;      // tokens of one MMA (N), a multiple of 16
+constexpr int kRowTile = 128;      // weight rows of one MMA (M)
+constexpr int kSfChunk = 512;
+
+inline __host__ __device__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+inline __host__ __device__ long long tile_proj_bytes(int N, int K)
+{
+    return (long long)N * K / 2 + (long long)ceil_div(N, kRowTile) * ceil_div(K, 128) * kSfChunk;
+}
+inline int max_tok_tiles(int Mk, int E) { return E + ceil_div(Mk, kTokTile); }
+
+struct TokTile {
+    int e;          // expert
+    int p0;         // first permuted slot
+    int n;          // tokens (slots) in the tile, 1..kTokTile
+    int npad;       // n rounded up to a multiple of 16 (the MMA's N)
+    long long boff; // byte offset of the tile's codes in an activation buffer, per 64 of K
+};
+
+struct BatchParams {
+    const uint8_t* gu;          // tile layout: expert e at + e*gu_expert = [gate proj][up proj]
+    const uint8_t* dn;          // expert e at + e*dn_expert
+    long long gu_expert, dn_expert;
+    const uint16_t* gu_bias;    // [E][2I] bf16, or nullptr
+    const uint16_t* dn_bias;    // [E][H] bf16, or nullptr
+    const float* logits;        // [M][E]
+    const uint16_t* x;          // [M][H] bf16
+    uint16_t* resid;            // [M][H] bf16 in/out
+    // workspace
+    int* idx;                   // [M][k] selected experts
+    float* wt;                  // [M][k] routing weights
+    int* slot;                  // [M*k] permuted slot of each (token, choice)
+    int* etile;                 // [M*k] token tile of each (token, choice)
+    int* erow;                  // [M*k] row inside that tile
+    int* ntiles;                // [1]
+    TokTile* tiles;             // [max_tok_tiles]
+    uint8_t* xq;                // activation codes, tile order (boff * H/64 per tile)
+    uint8_t* xsf;               // [tile][ceil(H/128)][512]
+    uint8_t* hq;
+    uint8_t* hsf;               // [tile][ceil(I/128)][512]
+    float* h;                   // [M*k][I], slot order
+    float* y;                   // [M*k][H], slot order
+    int* status;
+    int* nu_out;                // experts with at least one token (written by plan_kernel)
+    int H, I, E, M, k;
+    int max_tiles;
+};
+
+// Enqueue the batched layer (route, plan, quantise x, gate_up GEMM + SwiGLU,
+// quantise h, down GEMM, combine) on `stream`; `grid` = SM count.
+cudaError_t launch_batched(const BatchParams& p, int grid, cudaStream_t stream, int* launches);
+cudaError_t prepare_batched_kernels();
+// Caller layout [E][N][K/2] codes + [E][N][K/32] E8M0 -> tile layout (one projection
+// per expert; source rows row0 .. row0+N-1 of a caller matrix with `src_rows` rows).
+cudaError_t launch_repack_tiles(const uint8_t* codes, const uint8_t* scales, int E, int src_rows,
+                                int row0, int N, int K, uint8_t* out, long long expert_bytes,
+                                cudaStream_t stream);
+// MX quantisation of n fp32 values (n % 32 == 0) into natural order codes/scales.
+cudaError_t launch_mx_quantize(const float* in, long long n, uint8_t* codes, uint8_t* scales,
+                               cudaStream_t stream);
+// The h codes of the last batched call, back in [M*k][I/2] / [M*k][I/32] order.
+cudaError_t launch_untile_h(const BatchParams& p, uint8_t* codes, uint8_t* scales,
+                            cudaStream_t stream);
+
 // Debug kernels.
 cudaError_t launch_dequant(int fmt, int group, const uint8_t* slabs, int N, int K, int slab_bytes,
                            float* out, cudaStream_t stream);

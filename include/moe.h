@@ -82,7 +82,8 @@ typedef struct {
     int intermediate;  /* I: expert width; gate_up has 2I rows                 */
     int num_experts;   /* E experts per layer                                  */
     int num_layers;    /* L layers held resident                               */
-    int max_tokens;    /* largest M any forward will be given (1..4 decode)    */
+    int max_tokens;    /* largest M any forward will be given: 1..4 decode
+                          only; 5..8192 also enables the batched path (MXFP4) */
     int max_top_k;     /* largest top_k any forward will be given (<= E)       */
     int format;        /* moe_format                                           */
     int group;         /* elements per scale along K: 32 (MXFP4) or e.g. 64 (int4) */
@@ -92,10 +93,13 @@ typedef struct {
 /* Validate cfg and create a handle on the current CUDA device.  Allocates
  * the resident weight arena for all L layers plus a fixed workspace.
  * Requirements: H and I multiples of 64 and at most 3072; E in 1..256;
- * max_top_k in 1..min(E, 16); max_tokens in 1..4; MXFP4 needs group == 32;
- * int4 needs group a multiple of 32 dividing both H and I.  Weights are
- * repacked at load into 16-row slabs whose bytes are the MMA operands of the
- * decode kernel (see the layout note in the library source).
+ * max_top_k in 1..min(E, 16); max_tokens in 1..8192, above 4 only with
+ * MOE_FMT_MXFP4 (else MOE_ERR_UNSUPPORTED); MXFP4 needs group == 32; int4
+ * needs group a multiple of 32 dividing both H and I.  Weights are repacked
+ * at load into 16-row slabs whose bytes are the MMA operands of the decode
+ * kernel; with max_tokens > 4 they are also kept in the tile layout of the
+ * tensor-core batched path (about twice the memory; see the layout notes in
+ * the library source).
  * On success *out receives the handle; on failure *out is set to NULL. */
 int moe_create(const moe_config* cfg, moe_handle** out);
 
@@ -113,10 +117,18 @@ int moe_load_experts(moe_handle* h, int layer,
                      const void* dn_codes, const void* dn_scales, const void* dn_bias,
                      void* stream);
 
-/* One decode layer.  x bf16 [M][H] (the layer input, already normalised),
+/* One layer.  x bf16 [M][H] (the layer input, already normalised),
  * router_logits fp32 [M][E], out bf16 [M][H]: the residual r on entry and
  * r + MoE(x) on return.  1 <= M <= max_tokens, 1 <= top_k <= max_top_k.
- * x must not overlap out (checked).  All three are device pointers. */
+ * x must not overlap out (checked).  All three are device pointers.
+ * M <= 4 runs the decode kernel (one persistent launch).  M > 4 runs the
+ * batched path: per-expert grouped GEMMs on the tensor cores
+ * (tcgen05.mma kind::mxf4) with x and h quantised to MXFP4 per 32 along K by
+ * the OCP MX v1.0 rule (shared exponent floor(log2 amax) - 2, E2M1 nearest-
+ * even with saturation); seven launches.  Grouped-expert GEMM batching is
+ * the lever "Sovereign gpt-oss-20B (MXFP4) on Apple Silicon", section 5,
+ * names as untried; the activation quantisation is this library's reading
+ * (the tensor-core instruction needs FP4 on both sides). */
 int moe_forward(moe_handle* h, int layer, const void* x_bf16, const float* router_logits,
                 int M, int top_k, void* out_bf16, void* stream);
 
@@ -132,7 +144,8 @@ int moe_forward_host(moe_handle* h, int layer, const void* x_bf16, const float* 
  * resid bf16 [M][H] holds r_0 on entry and r_L on return; logits fp32
  * [L][M][E].  Layer l+1 reads its logits only after layer l's output is
  * complete.  Device pointers.  Launched as a cached CUDA graph of L
- * programmatically chained layer kernels per (M, top_k, resid, logits). */
+ * programmatically chained layer kernels per (M, top_k, resid, logits).
+ * Decode sizes only: M <= 4 (else MOE_ERR_UNSUPPORTED). */
 int moe_forward_stack(moe_handle* h, void* resid_bf16, const float* router_logits,
                       int M, int top_k, void* stream);
 
@@ -153,6 +166,19 @@ int moe_debug_dequant(moe_handle* h, int layer, int expert, int proj, float* out
  * M up to 65536 here. */
 int moe_debug_route(moe_handle* h, const float* logits, int M, int top_k, int* idx, float* w,
                     void* stream);
+
+/* Debug: the batched path's MX quantiser on a flat fp32 vector.  in fp32 [n]
+ * device, n a multiple of 32; codes u8 [n/2] (low nibble = even element) and
+ * scales u8 [n/32] (E8M0) device outputs, natural order.  No handle needed.
+ * in and codes 16-byte aligned. */
+int moe_debug_mx_quantize(const float* in, long long n, unsigned char* codes,
+                          unsigned char* scales, void* stream);
+
+/* Debug: the quantised h of the last batched forward (M > 4) on this handle,
+ * in (token, choice) order: codes u8 [M*top_k][I/2] and E8M0 scales u8
+ * [M*top_k][I/32], device outputs (codes 16-byte aligned).  Choice s of token
+ * m is the s-th selected expert (largest logit first). */
+int moe_debug_batched_h(moe_handle* h, unsigned char* codes, unsigned char* scales, void* stream);
 
 /* Debug: the expert stack run layer by layer with the same kernels as
  * moe_forward_stack (no graph), recording the residual after every layer.

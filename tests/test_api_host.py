@@ -44,7 +44,7 @@ def _cfg(**kw):
     (dict(hidden=96), "hidden"), (dict(intermediate=3136), "intermediate"),
     (dict(intermediate=48), "intermediate"), (dict(num_experts=0), "num_experts"),
     (dict(num_experts=300), "num_experts"), (dict(num_layers=0), "num_layers"),
-    (dict(max_tokens=0), "max_tokens"), (dict(max_tokens=5), "max_tokens"),
+    (dict(max_tokens=0), "max_tokens"), (dict(max_tokens=8193), "max_tokens"),
     (dict(max_top_k=0), "max_top_k"), (dict(max_top_k=9), "max_top_k"),
     (dict(max_top_k=17, num_experts=64), "max_top_k"), (dict(format=3), "format"),
     (dict(group=64), "group"), (dict(format=moe.MOE_FMT_INT4, group=48), "group"),
@@ -56,6 +56,25 @@ def test_create_rejects_bad_config(L, bad, needle):
     assert rc == moe.MOE_ERR_INVALID_ARG
     assert h.value is None
     assert needle in moe.moe_last_error()
+
+
+def test_batched_path_needs_mxfp4(L):
+    """max_tokens > 4 enables the tensor-core path, which runs MXFP4 only."""
+    h = ctypes.c_void_p(123)
+    rc = L.moe_create(ctypes.byref(_cfg(max_tokens=8, format=moe.MOE_FMT_INT4, group=64)), ctypes.byref(h))
+    assert rc == moe.MOE_ERR_UNSUPPORTED
+    assert h.value is None
+    assert "MXFP4" in moe.moe_last_error()
+
+
+def test_debug_entry_points_check_arguments(L):
+    buf = ctypes.create_string_buffer(4096)
+    addr = (ctypes.addressof(buf) + 15) & ~15
+    assert L.moe_debug_mx_quantize(None, 32, addr, addr, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_debug_mx_quantize(addr, 33, addr, addr, None) == moe.MOE_ERR_INVALID_ARG
+    assert "multiple of 32" in moe.moe_last_error()
+    assert L.moe_debug_mx_quantize(addr + 4, 32, addr, addr, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_debug_batched_h(None, addr, addr, None) == moe.MOE_ERR_INVALID_ARG
 
 
 def test_null_arguments_rejected(L):
