@@ -388,6 +388,75 @@ def run_stack(args):
     return 0
 
 
+def run_batched(args):
+    """Extra workloads (not the headline line): the batched MXFP4 layer,
+    H = I = 2880, 128 experts, top-4, M = 512 tokens (uniform router logits,
+    or +2 on experts 0..7), through moe_forward's tensor-core path."""
+    import torch
+    rank, world = _setup(args)
+    import bit_moe_decode_02_gb300 as moe
+    shape = synth.BATCHED if args.workload == "batched" else synth.BATCHED_SKEWED
+    H, I, E, k, M = shape.hidden, shape.intermediate, shape.experts, shape.top_k, shape.tokens
+    h = moe.moe_create(H, I, E, 1, M, k, moe.MOE_FMT_MXFP4, 32, 1)
+    _load_all(moe, h, shape, 1)
+    W, K = args.warmup, args.steps
+    P = 4   # distinct input sets, cycled
+    ins = [synth.step_inputs(shape, 7000 + i) for i in range(P)]
+    xd = [torch.from_numpy(x.view(np.int16)).cuda() for x, _, _ in ins]
+    rd = [torch.from_numpy(r.view(np.int16)).cuda() for _, r, _ in ins]
+    ld = [torch.from_numpy(np.ascontiguousarray(lg[0])).cuda() for _, _, lg in ins]
+    cap = torch.cuda.Stream()
+    gw, gk = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(gw, stream=cap):
+        for s in range(W):
+            moe.moe_forward(h, 0, xd[s % P], ld[s % P], M, k, rd[s % P], cap)
+    with torch.cuda.graph(gk, stream=cap):
+        for s in range(K):
+            moe.moe_forward(h, 0, xd[s % P], ld[s % P], M, k, rd[s % P], cap)
+    launches = moe.moe_last_launches(h) * K
+    stream = torch.cuda.current_stream()
+    gw.replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ev0.record(stream)
+        gk.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    assert moe.moe_get_status(h) == 0
+    nbytes = []
+    for i in range(P):
+        moe.moe_forward(h, 0, xd[i], ld[i], M, k, rd[i], stream)
+        nbytes.append(moe.moe_last_bytes(h, stream))
+    moe.moe_destroy(h)
+    us = 1e3 * ms / K
+    flops = 2.0 * M * k * (2 * I * H + H * I)
+    peak_hbm, kind = measured_peaks()
+    fp4_peak = _fp4_peak()
+    gbs = float(np.mean(nbytes)) / (us / 1e6) / 1e9
+    tflops = flops / (us / 1e6) / 1e12
+    line = {"workload": shape.name, "metric": "us per batched MoE layer; TFLOP/s and expert-weight GB/s",
+            "value": us, "unit": "us/layer", "steps": K, "warmup": W, "tokens": M,
+            "tflops": tflops, "tflops_peak_fp4": fp4_peak, "tflops_frac": tflops / fp4_peak,
+            "bytes_per_step": float(np.mean(nbytes)), "gbs": gbs, "hbm_frac": gbs / peak_hbm,
+            "hbm_peak": peak_hbm, "peak_kind": kind, "gpu_launches": launches,
+            "l2": "each step reads ~1.7 GB of expert weights (13x L2)",
+            "launch": "K steps of 7 kernels captured in one CUDA graph", "clocks": clk.summary()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def _fp4_peak():
+    """Dense FP4 tensor peak: the measured bf16 GEMM peak times the nominal
+    fp4 / bf16 ratio (13.5 / 2.25 PFLOP/s)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    bf16 = json.load(open(p))["bf16_tflops"] if os.path.exists(p) else 1900.0
+    return bf16 * 13.5 / 2.25
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -396,7 +465,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None,
                     help="resident layers (default: 24 for the layer workload, all for the "
                          "stacks; smaller for profiling)")
-    ap.add_argument("--workload", choices=["layer", "stack24", "int4stack48"], default="layer")
+    ap.add_argument("--workload", choices=["layer", "stack24", "int4stack48", "batched", "batched_skewed"],
+                    default="layer")
     ap.add_argument("--tokens", type=int, default=1, help="M for the stack workloads")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-steps", type=int, default=24)
@@ -406,6 +476,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload.startswith("batched"):
+        return run_batched(args)
     if args.workload != "layer":
         return run_stack(args)
     return run_ours(args)

@@ -87,7 +87,6 @@ struct moe_handle {
     uint8_t* b_xsf = nullptr;
     uint8_t* b_hq = nullptr;
     uint8_t* b_hsf = nullptr;
-    float* b_h = nullptr;
     float* b_y = nullptr;
     int last_bM = 0, last_bk = 0;     // M and top_k of the last batched call
     // workspace
@@ -178,7 +177,6 @@ void free_handle(moe_handle* h)
     cudaFree(h->b_xsf);
     cudaFree(h->b_hq);
     cudaFree(h->b_hsf);
-    cudaFree(h->b_h);
     cudaFree(h->b_y);
     delete h;
 }
@@ -257,7 +255,6 @@ int create_batched(moe_handle* h)
         (rc = dev_alloc(&h->b_xsf, (size_t)h->max_tiles * moe::ceil_div(H, 128) * moe::kSfChunk, "x scales")) ||
         (rc = dev_alloc(&h->b_hq, rows * I / 2, "h codes")) ||
         (rc = dev_alloc(&h->b_hsf, (size_t)h->max_tiles * moe::ceil_div(I, 128) * moe::kSfChunk, "h scales")) ||
-        (rc = dev_alloc(&h->b_h, Mk * I * sizeof(float), "batched h")) ||
         (rc = dev_alloc(&h->b_y, Mk * H * sizeof(float), "batched y")))
         return rc;
     cudaError_t e = moe::prepare_batched_kernels();
@@ -290,7 +287,6 @@ moe::BatchParams batch_params(const moe_handle* h, int layer)
     p.xsf = h->b_xsf;
     p.hq = h->b_hq;
     p.hsf = h->b_hsf;
-    p.h = h->b_h;
     p.y = h->b_y;
     p.status = h->status;
     p.nu_out = h->stats + layer;

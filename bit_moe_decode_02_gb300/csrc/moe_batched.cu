@@ -16,8 +16,8 @@
 //   route_kernel (moe_decode.cu)  top-k + softmax per token
 //   plan_kernel                   per-expert stable permutation, token tiles
 //   quant_x_kernel                MX(x) into the token tiles
-//   gemm_kernel<true>             gate and up tiles, + bias, SwiGLU -> h (fp32)
-//   quant_h_kernel                MX(h) into the token tiles
+//   gemm_kernel<true>             gate and up tiles, + bias, SwiGLU, MX(h) into
+//                                 the token tiles (h never leaves the chip in fp32)
 //   gemm_kernel<false>            down tiles, + bias -> y (fp32, slot order)
 //   combine_kernel                out = bf16(r + sum_s w_s y_s)
 #include <cuda_runtime.h>
@@ -198,16 +198,61 @@ __device__ __forceinline__ int act_sf_off(int r, int kb)
 
 // ------------------------------------------------------------------- plan
 
+// Exclusive scan of three per-expert values over threads 0..255 of the block
+// (all 1024 threads call it; threads >= 256 pass zeros); returns the three
+// totals through `tot`.
+__device__ void scan3_256(int (&v)[3], int (&tot)[3], int (*wsum)[3])
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int x[3] = {v[0], v[1], v[2]};
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1)
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+            const int y = __shfl_up_sync(0xffffffffu, x[c], off);
+            if (lane >= off)
+                x[c] += y;
+        }
+    if (lane == 31 && warp < 8)
+        for (int c = 0; c < 3; ++c)
+            wsum[warp][c] = x[c];
+    __syncthreads();
+    if (tid < 32) {
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+            int y = tid < 8 ? wsum[tid][c] : 0;
+#pragma unroll
+            for (int off = 1; off < 8; off <<= 1) {
+                const int z = __shfl_up_sync(0xffffffffu, y, off);
+                if (tid >= off)
+                    y += z;
+            }
+            if (tid < 8)
+                wsum[tid][c] = y;   // inclusive over warps
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+        const int before = warp > 0 && warp < 8 ? wsum[warp - 1][c] : 0;
+        tot[c] = wsum[7][c];
+        v[c] = before + x[c] - v[c];
+    }
+}
+
 // One CTA of 1024 threads.  Entries q = m*k + s (token m, choice s) are ranked
 // within their expert in q order (a stable counting sort), experts get
 // consecutive slot ranges in expert order, and each expert's slots are cut
-// into token tiles of at most kTokTile.
+// into token tiles of at most kTokTile (the expert's tiles before its last
+// are full, so a tile's activation offset follows from the expert's padded
+// row offset).
 __global__ void __launch_bounds__(1024) plan_kernel(BatchParams p)
 {
     __shared__ int cnt[32][kMaxExperts];
     __shared__ int base[kMaxExperts];
     __shared__ int off[kMaxExperts];
     __shared__ int toff[kMaxExperts];
+    __shared__ int wsum[8][3];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Mk = p.M * p.k, E = p.E;
     for (int e = tid; e < kMaxExperts; e += 1024)
@@ -243,28 +288,37 @@ __global__ void __launch_bounds__(1024) plan_kernel(BatchParams p)
             p.erow[q] = cnt[warp][e] + rw;   // rank within the expert, rewritten below
         __syncthreads();
     }
-    if (tid == 0) {
-        int so = 0, to = 0, nu = 0;
-        long long bo = 0;
-        for (int e = 0; e < E; ++e) {
-            const int n = base[e];
-            nu += n > 0;
-            off[e] = so;
-            toff[e] = to;
-            for (int j = 0; j * kTokTile < n; ++j) {
-                TokTile t;
-                t.e = e;
-                t.p0 = so + j * kTokTile;
-                t.n = n - j * kTokTile < kTokTile ? n - j * kTokTile : kTokTile;
-                t.npad = (t.n + 15) & ~15;
-                t.boff = bo;
-                bo += t.npad * 32;
-                if (to < p.max_tiles)
-                    p.tiles[to] = t;
-                ++to;
-            }
-            so += n;
+    // per expert: slots n, tiles ceil(n / kTokTile), padded activation rows
+    const int n = tid < E ? base[tid] : 0;
+    const int full = n / kTokTile, rem = n % kTokTile;
+    int v[3] = {n, full + (rem > 0), full * kTokTile + ((rem + 15) & ~15)};
+    int tot[3];
+    scan3_256(v, tot, wsum);
+    if (tid < E) {
+        off[tid] = v[0];
+        toff[tid] = v[1];
+        for (int j = 0; j * kTokTile < n; ++j) {
+            const int to = v[1] + j;
+            if (to >= p.max_tiles)
+                break;
+            TokTile t;
+            t.e = tid;
+            t.p0 = v[0] + j * kTokTile;
+            t.n = n - j * kTokTile < kTokTile ? n - j * kTokTile : kTokTile;
+            t.npad = (t.n + 15) & ~15;
+            t.boff = (long long)(v[2] + j * kTokTile) * 32;
+            p.tiles[to] = t;
         }
+    }
+    const unsigned busy = __ballot_sync(0xffffffffu, n > 0);
+    if (lane == 0 && warp < 8)
+        wsum[warp][0] = __popc(busy);   // scan3_256 is done with wsum
+    __syncthreads();
+    if (tid == 0) {
+        int nu = 0;
+        for (int w = 0; w < 8; ++w)
+            nu += wsum[w][0];
+        int to = tot[1];
         if (to > p.max_tiles) {
             atomicExch(p.status, MOE_ERR_DEVICE_FAULT);
             to = p.max_tiles;
@@ -273,7 +327,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(BatchParams p)
         if (p.nu_out)
             *p.nu_out = nu;
     }
-    __syncthreads();
     for (int q = tid; q < Mk; q += 1024) {
         int e = p.idx[q];
         e = e < 0 || e >= E ? 0 : e;
@@ -323,35 +376,6 @@ __global__ void quant_x_kernel(BatchParams p)
     }
 }
 
-// One thread per (entry q, K-block kb of I): MX(h[slot][32kb..]).
-__global__ void quant_h_kernel(BatchParams p)
-{
-    const int nkb = p.I / 32;
-    const long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-    if (g >= (long long)p.M * p.k * nkb)
-        return;
-    const int q = (int)(g / nkb), kb = (int)(g % nkb);
-    const int t = p.etile[q], r = p.erow[q];
-    if (t >= *p.ntiles)
-        return;
-    const float4* src = reinterpret_cast<const float4*>(p.h + (size_t)p.slot[q] * p.I + 32 * kb);
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float4 f = src[i];
-        v[4 * i] = f.x;
-        v[4 * i + 1] = f.y;
-        v[4 * i + 2] = f.z;
-        v[4 * i + 3] = f.w;
-    }
-    uint32_t code[4];
-    const uint32_t sb = mx_block(v, code);
-    const TokTile tt = p.tiles[t];
-    *reinterpret_cast<uint4*>(p.hq + tt.boff * (p.I / 64) + act_code_off(tt.npad, r, kb)) =
-        make_uint4(code[0], code[1], code[2], code[3]);
-    p.hsf[(size_t)t * ceil_div(p.I, 128) * kSfChunk + act_sf_off(r, kb)] = (uint8_t)sb;
-}
-
 // Debug: natural-order MX quantisation of a flat vector, one thread per block.
 __global__ void mx_quantize_kernel(const float* __restrict__ in, long long nblk, uint8_t* codes,
                                    uint8_t* scales)
@@ -398,41 +422,83 @@ struct GemmParams {
     const int* ntiles;
     const uint16_t* bias;   // [E][bias_stride] bf16 or nullptr; DUAL: up bias at + rows
     int bias_stride;
-    float* out;             // [slots][rows]
+    float* out;             // single: y [slots][rows] fp32
+    uint8_t* hq;            // DUAL: MX(h) codes in the down GEMM's activation tile order
+    uint8_t* hsf;           // DUAL: MX(h) scale chunks
     int* status;
 };
 
-constexpr int kStageSteps = 4;                          // k-steps (64 of K) per pipeline stage
-constexpr int kAStage = kStageSteps * kRowTile * 32;    // 16 KB of weight codes
-constexpr int kBStage = kStageSteps * kTokTile * 32;    // activation codes
-constexpr int kSfCol = 448;                             // first tensor-memory column of the scale sets
+constexpr int kStageSteps = 8;           // k-steps (64 of K) per pipeline stage
+constexpr int kSfCol = 4 * kTokTile;     // first tensor-memory column of the scale sets
+constexpr int kRingBytes = 200 * 1024;   // shared-memory stage ring (byte-granular FIFO)
+constexpr int kRingSlack = 4096;         // read slack past the ring end (see Stage)
+constexpr int kStageSlots = 16;          // stages in flight at most (mbarrier pairs)
 
 template <bool DUAL>
 struct GemmCfg {
-    static constexpr int kSfBytes = (DUAL ? 3 : 2) * 2 * kSfChunk;
-    static constexpr int kStage = (DUAL ? 2 : 1) * kAStage + kBStage + kSfBytes;
-    static constexpr int kStages = DUAL ? 4 : 6;
-    static constexpr int kSmem = kStages * kStage;
+    static constexpr int kSmem = kRingBytes + kRingSlack;
     static constexpr int kAccCols = (DUAL ? 2 : 1) * kTokTile;   // per accumulator buffer
-    static constexpr int kSfSet = (DUAL ? 3 : 2) * 8;             // tensor-memory columns per scale set
+    static constexpr int kSfSet = (DUAL ? 3 : 2) * 4 * (kStageSteps / 2);   // tensor-memory columns per scale set
+    static_assert(kSfCol + 2 * kSfSet <= 512, "tensor memory: accumulators + two scale sets");
+};
+
+// One pipeline stage: `steps` k-steps of R weight rows (two projections if
+// DUAL) and npad activation rows, with their scale chunks, packed as
+// [A0][A1][B][SFA0][SFA1][SFB] and sized to what it holds, so that a small
+// token tile leaves the ring to weight bytes.  For a partial row tile
+// (R = 64) the MMA still reads 128 rows of the last k-step block, up to 2 KB
+// past A; that lands inside the stage or in the ring's slack.
+template <bool DUAL>
+struct Stage {
+    uint32_t abytes, bbytes, sfbytes, size;
+    __device__ Stage(int steps, int R, int npad)
+    {
+        const int chunks = (steps + 1) >> 1;
+        abytes = steps * R * 32;
+        bbytes = steps * npad * 32;
+        sfbytes = chunks * kSfChunk;
+        size = ((DUAL ? 2 : 1) * (abytes + sfbytes) + bbytes + sfbytes + 127) & ~127u;
+    }
+    __device__ uint32_t b() const { return (DUAL ? 2 : 1) * abytes; }
+    __device__ uint32_t sfa0() const { return b() + bbytes; }
+    __device__ uint32_t sfb() const { return sfa0() + (DUAL ? 2 : 1) * sfbytes; }
+};
+
+// FIFO placement of stages in the ring; a stage never straddles the end.
+// The producer and the MMA thread run the same sequence of placements.
+struct Ring {
+    unsigned long long head = 0;   // virtual bytes handed out so far
+    uint32_t phys = 0;             // head modulo kRingBytes
+    __device__ uint32_t place(uint32_t size, unsigned long long* end)
+    {
+        if (phys + size > (uint32_t)kRingBytes) {
+            head += kRingBytes - phys;
+            phys = 0;
+        }
+        const uint32_t off = phys;
+        phys += size;
+        head += size;
+        *end = head;
+        return off;
+    }
 };
 
 // Persistent: one CTA per SM walks items w = blockIdx.x + i * gridDim.x, item
-// w = (token tile w / T, row tile w % T).  Warp 0 feeds a ring of shared-memory
-// stages with bulk copies; warp 1 owns tensor memory and issues the MMAs from
-// one thread; warps 2..5 (one per lane quarter) drain the accumulators, which
-// are double-buffered so the next item's MMAs overlap this item's epilogue.
+// w = (token tile w / T, row tile w % T).  Warp 0 feeds the stage ring with
+// bulk copies; warp 1 owns tensor memory and issues the MMAs from one thread;
+// warps 2..5 (one per lane quarter) drain the accumulators, which are
+// double-buffered so the next item's MMAs overlap this item's epilogue.
 template <bool DUAL>
 __global__ void __launch_bounds__(192, 1) gemm_kernel(GemmParams p)
 {
     using C = GemmCfg<DUAL>;
     extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ __align__(8) uint64_t full[C::kStages], empty[C::kStages], accf[2], acce[2];
+    __shared__ __align__(8) uint64_t full[kStageSlots], empty[kStageSlots], accf[2], acce[2];
     __shared__ uint32_t tmem_base;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < C::kStages; ++i) {
+        for (int i = 0; i < kStageSlots; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
@@ -457,51 +523,71 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(GemmParams p)
     const int items = *p.ntiles * T;
 
     if (warp == 0) {
-        if (lane == 0) {
-            uint32_t ctr = 0;
-            for (int w = blockIdx.x; w < items; w += gridDim.x) {
-                const int tt = w / T, t = w % T;
-                const TokTile tile = p.tiles[tt];
-                const int R = p.rows - t * kRowTile < kRowTile ? p.rows - t * kRowTile : kRowTile;
-                const uint8_t* a0 = p.w + tile.e * p.w_expert + (long long)t * kRowTile * (p.K / 2);
-                const uint8_t* s0 = p.w + tile.e * p.w_expert + (long long)p.rows * (p.K / 2) +
-                                    (long long)t * CH * kSfChunk;
-                const uint8_t* b0 = p.bq + tile.boff * KS;
-                const uint8_t* sb0 = p.bsf + (long long)tt * CH * kSfChunk;
-                for (int j = 0; j < NSTG; ++j, ++ctr) {
-                    const int slot = ctr % C::kStages;
-                    const uint32_t use = ctr / C::kStages;
-                    if (use > 0)
-                        mbar_wait(&empty[slot], (use - 1) & 1, p.status);
-                    const int steps = KS - j * kStageSteps < kStageSteps ? KS - j * kStageSteps : kStageSteps;
-                    const int chunks = (steps + 1) >> 1;
-                    const uint32_t abytes = steps * R * 32, bbytes = steps * tile.npad * 32;
-                    const uint32_t sfbytes = chunks * kSfChunk;
-                    uint8_t* st = smem + slot * C::kStage;
-                    uint8_t* sA0 = st;
-                    uint8_t* sA1 = st + kAStage;
-                    uint8_t* sB = st + (DUAL ? 2 : 1) * kAStage;
-                    uint8_t* sSF = sB + kBStage;
-                    mbar_expect_tx(&full[slot], (DUAL ? 2 : 1) * (abytes + sfbytes) + bbytes + sfbytes);
-                    const long long aoff = (long long)j * kStageSteps * R * 32;
-                    const long long soff = (long long)j * 2 * kSfChunk;
-                    bulk_copy(sA0, a0 + aoff, abytes, &full[slot]);
-                    bulk_copy(sSF, s0 + soff, sfbytes, &full[slot]);
-                    if (DUAL) {
-                        bulk_copy(sA1, a0 + p.proj2 + aoff, abytes, &full[slot]);
-                        bulk_copy(sSF + 2 * kSfChunk, s0 + p.proj2 + soff, sfbytes, &full[slot]);
-                    }
-                    bulk_copy(sB, b0 + (long long)j * kStageSteps * tile.npad * 32, bbytes, &full[slot]);
-                    bulk_copy(sSF + (DUAL ? 4 : 2) * kSfChunk, sb0 + soff, sfbytes, &full[slot]);
+        // The whole warp runs the producer loop; a stage's copies are issued by
+        // separate lanes in one instruction (one lane issuing them one after
+        // another costs ~0.15 us each, which would bound the stage rate).
+        Ring ring;
+        unsigned long long ends[kStageSlots];
+        unsigned long long rel_end = 0;   // ring bytes released by the consumer
+        uint32_t c = 0, rel = 0;          // stages issued / released
+        TokTile tile = blockIdx.x < items ? p.tiles[blockIdx.x / T] : TokTile{};
+        for (int w = blockIdx.x; w < items; w += gridDim.x) {
+            const int tt = w / T, t = w % T;
+            // the next item's descriptor is loaded now and used one item later,
+            // so its latency never stalls the copy stream
+            const int wn = w + gridDim.x;
+            const TokTile next = wn < items ? p.tiles[wn / T] : tile;
+            const int R = p.rows - t * kRowTile < kRowTile ? p.rows - t * kRowTile : kRowTile;
+            const uint8_t* a0 = p.w + tile.e * p.w_expert + (long long)t * kRowTile * (p.K / 2);
+            const uint8_t* s0 = p.w + tile.e * p.w_expert + (long long)p.rows * (p.K / 2) +
+                                (long long)t * CH * kSfChunk;
+            const uint8_t* b0 = p.bq + tile.boff * KS;
+            const uint8_t* sb0 = p.bsf + (long long)tt * CH * kSfChunk;
+            for (int j = 0; j < NSTG; ++j, ++c) {
+                const int steps = KS - j * kStageSteps < kStageSteps ? KS - j * kStageSteps : kStageSteps;
+                const Stage<DUAL> sg(steps, R, tile.npad);
+                unsigned long long end;
+                const uint32_t off = ring.place(sg.size, &end);
+                // wait until the bytes and the slot are free (stages retire in order)
+                while (rel < c && (end - rel_end > (unsigned long long)kRingBytes || rel + kStageSlots <= c)) {
+                    const uint32_t sl = rel % kStageSlots;
+                    mbar_wait(&empty[sl], (rel / kStageSlots) & 1, p.status);
+                    rel_end = ends[sl];
+                    ++rel;
                 }
+                const uint32_t slot = c % kStageSlots;
+                ends[slot] = end;
+                if (lane == 0)
+                    mbar_expect_tx(&full[slot],
+                                   (DUAL ? 2 : 1) * (sg.abytes + sg.sfbytes) + sg.bbytes + sg.sfbytes);
+                __syncwarp();
+                const long long aoff = (long long)j * kStageSteps * R * 32;
+                const long long soff = (long long)j * (kStageSteps / 2) * kSfChunk;
+                uint8_t* st = smem + off;
+                uint8_t* dst = nullptr;
+                const uint8_t* src = nullptr;
+                uint32_t n = 0;
+                switch (lane) {
+                case 0: dst = st; src = a0 + aoff; n = sg.abytes; break;
+                case 1: dst = st + sg.sfa0(); src = s0 + soff; n = sg.sfbytes; break;
+                case 2: dst = st + sg.b(); src = b0 + (long long)j * kStageSteps * tile.npad * 32; n = sg.bbytes; break;
+                case 3: dst = st + sg.sfb(); src = sb0 + soff; n = sg.sfbytes; break;
+                case 4: if (DUAL) { dst = st + sg.abytes; src = a0 + p.proj2 + aoff; n = sg.abytes; } break;
+                case 5: if (DUAL) { dst = st + sg.sfa0() + sg.sfbytes; src = s0 + p.proj2 + soff; n = sg.sfbytes; } break;
+                default: break;
+                }
+                if (n)
+                    bulk_copy(dst, src, n, &full[slot]);
             }
+            tile = next;
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            uint32_t ctr = 0, it = 0;
+            Ring ring;
+            uint32_t c = 0, it = 0;
             for (int w = blockIdx.x; w < items; w += gridDim.x, ++it) {
-                const int tt = w / T, t = w % T;
-                const TokTile tile = p.tiles[tt];
+                const int t = w % T;
+                const TokTile tile = p.tiles[w / T];
                 const int R = p.rows - t * kRowTile < kRowTile ? p.rows - t * kRowTile : kRowTile;
                 const uint32_t buf = it & 1;
                 if (it >= 2)
@@ -510,23 +596,24 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(GemmParams p)
                 const uint32_t d0 = tmem + buf * C::kAccCols;
                 const uint32_t idesc = (1u << 7) | (1u << 10) | ((uint32_t)(tile.npad >> 3) << 17) |
                                        (1u << 23) | ((uint32_t)(kRowTile >> 4) << 24);
-                for (int j = 0; j < NSTG; ++j, ++ctr) {
-                    const int slot = ctr % C::kStages;
-                    mbar_wait(&full[slot], (ctr / C::kStages) & 1, p.status);
-                    tc_fence_after();
+                for (int j = 0; j < NSTG; ++j, ++c) {
                     const int steps = KS - j * kStageSteps < kStageSteps ? KS - j * kStageSteps : kStageSteps;
+                    const Stage<DUAL> sg(steps, R, tile.npad);
+                    unsigned long long end;
+                    const uint32_t st = su32(smem) + ring.place(sg.size, &end);
+                    const uint32_t slot = c % kStageSlots;
+                    mbar_wait(&full[slot], (c / kStageSlots) & 1, p.status);
+                    tc_fence_after();
                     const int chunks = (steps + 1) >> 1;
-                    const uint32_t st = su32(smem + slot * C::kStage);
-                    const uint32_t sA0 = st, sA1 = st + kAStage;
-                    const uint32_t sB = st + (DUAL ? 2 : 1) * kAStage;
-                    const uint32_t sSF = sB + kBStage;
-                    const uint32_t sf = tmem + kSfCol + (ctr & 1) * C::kSfSet;
-                    const uint32_t sfa0 = sf, sfa1 = sf + 8, sfb = sf + (DUAL ? 16 : 8);
-                    for (int c = 0; c < chunks; ++c) {
-                        tc_cp_sf(sfa0 + 4 * c, sSF + c * kSfChunk);
+                    const uint32_t sA0 = st, sA1 = st + sg.abytes, sB = st + sg.b();
+                    const uint32_t sf = tmem + kSfCol + (c & 1) * C::kSfSet;
+                    constexpr uint32_t kOp = 4 * (kStageSteps / 2);   // columns per operand's scales
+                    const uint32_t sfa0 = sf, sfa1 = sf + kOp, sfb = sf + (DUAL ? 2 : 1) * kOp;
+                    for (int ch = 0; ch < chunks; ++ch) {
+                        tc_cp_sf(sfa0 + 4 * ch, st + sg.sfa0() + ch * kSfChunk);
                         if (DUAL)
-                            tc_cp_sf(sfa1 + 4 * c, sSF + (2 + c) * kSfChunk);
-                        tc_cp_sf(sfb + 4 * c, sSF + ((DUAL ? 4 : 2) + c) * kSfChunk);
+                            tc_cp_sf(sfa1 + 4 * ch, st + sg.sfa0() + sg.sfbytes + ch * kSfChunk);
+                        tc_cp_sf(sfb + 4 * ch, st + sg.sfb() + ch * kSfChunk);
                     }
                     for (int i = 0; i < steps; ++i) {
                         const uint32_t id = (uint32_t)(2 * (i & 1));
@@ -554,7 +641,8 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(GemmParams p)
             mbar_wait(&accf[buf], (it >> 1) & 1, p.status);
             tc_fence_after();
             const int row = t * kRowTile + 32 * q + lane;
-            const bool valid = row < p.rows;
+            // rows come in multiples of 64, so a warp's 32 rows are all valid or all not
+            const bool valid = t * kRowTile + 32 * q < p.rows;
             float b0 = 0.0f, b1 = 0.0f;
             if (p.bias && valid) {
                 const uint16_t* bb = p.bias + (size_t)tile.e * p.bias_stride;
@@ -563,27 +651,48 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(GemmParams p)
                     b1 = bf16f(bb[p.rows + row]);
             }
             const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * C::kAccCols;
-            float* out = p.out + (size_t)tile.p0 * p.rows + row;
             for (int c0 = 0; c0 < tile.n; c0 += 16) {
                 float g[16], u[16];
                 tc_ld16(taddr + c0, g);
                 if (DUAL)
                     tc_ld16(taddr + kTokTile + c0, u);
                 tc_wait_ld();
-                if (valid) {
+                if (!valid)
+                    continue;
+                const int nn = tile.n - c0 < 16 ? tile.n - c0 : 16;
+                if (DUAL) {
+                    // h = silu(gate) * up, then MX-quantised along I: the warp's 32
+                    // rows are one 32-element block of token n's h
+                    const int kb = row >> 5;
+                    uint8_t* hq = p.hq + tile.boff * (p.rows / 64) + 4 * (lane >> 3);
+                    uint8_t* hs = p.hsf + (size_t)tt * ceil_div(p.rows, 128) * kSfChunk;
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
-                        if (c0 + jj < tile.n) {
-                            float v;
-                            if (DUAL) {
-                                const float gg = g[jj] + b0;
-                                v = gg / (1.0f + expf(-gg)) * (u[jj] + b1);
-                            } else {
-                                v = g[jj] + b0;
-                            }
-                            out[(size_t)(c0 + jj) * p.rows] = v;
-                        }
+                        if (jj >= nn)
+                            break;
+                        const float gg = g[jj] + b0;
+                        const float v = gg / (1.0f + expf(-gg)) * (u[jj] + b1);
+                        const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
+                        const int ef = (int)(amax >> 23);
+                        const uint32_t sbyte = ef > 2 ? (uint32_t)(ef - 2) : 0u;
+                        const float inv = __uint_as_float((254u - sbyte) << 23);
+                        const uint32_t code = amax == 0u ? 0u : (e2m1x2(v * inv, 0.0f) & 0xfu);
+                        uint32_t word = code << (4 * (lane & 7));
+                        word |= __shfl_xor_sync(0xffffffffu, word, 1);
+                        word |= __shfl_xor_sync(0xffffffffu, word, 2);
+                        word |= __shfl_xor_sync(0xffffffffu, word, 4);
+                        const int n = c0 + jj;
+                        if ((lane & 7) == 0)
+                            *reinterpret_cast<uint32_t*>(hq + act_code_off(tile.npad, n, kb)) = word;
+                        if (lane == 0)
+                            hs[act_sf_off(n, kb)] = (uint8_t)sbyte;
                     }
+                } else {
+                    float* out = p.out + (size_t)(tile.p0 + c0) * p.rows + row;
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj)
+                        if (jj < nn)
+                            out[(size_t)jj * p.rows] = g[jj] + b0;
                 }
             }
             tc_fence_before();
@@ -723,11 +832,11 @@ cudaError_t launch_batched(const BatchParams& p, int grid, cudaStream_t s, int* 
     g.ntiles = p.ntiles;
     g.bias = p.gu_bias;
     g.bias_stride = 2 * p.I;
-    g.out = p.h;
+    g.hq = p.hq;
+    g.hsf = p.hsf;
     g.status = p.status;
     if ((e = launch_gemm<true>(g, grid, s)) != cudaSuccess)
         return e;
-    quant_h_kernel<<<blocks_for((long long)p.M * p.k * (p.I / 32), 256), 256, 0, s>>>(p);
     g.w = p.dn;
     g.w_expert = p.dn_expert;
     g.proj2 = 0;
@@ -741,7 +850,7 @@ cudaError_t launch_batched(const BatchParams& p, int grid, cudaStream_t s, int* 
     if ((e = launch_gemm<false>(g, grid, s)) != cudaSuccess)
         return e;
     combine_kernel<<<blocks_for((long long)p.M * (p.H / 8), 256), 256, 0, s>>>(p);
-    *launches = 7;
+    *launches = 6;
     return cudaGetLastError();
 }
 

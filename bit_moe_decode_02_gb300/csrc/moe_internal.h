@@ -104,7 +104,7 @@ int set_error(int code, const char* fmt, ...);
 // Activations (x, h) use the same two orders per token tile: codes
 // [k-step][npad rows x 32 bytes], scales [chunk][512].
 constexpr int kMaxBatchTokens = 8192;
-constexpr int kTokTile = 112;      // tokens of one MMA (N), a multiple of 16
+constexpr int kTokTile = 96;       // tokens of one MMA (N), a multiple of 16
 constexpr int kRowTile = 128;      // weight rows of one MMA (M)
 constexpr int kSfChunk = 512;
 
@@ -144,7 +144,6 @@ struct BatchParams {
     uint8_t* xsf;               // [tile][ceil(H/128)][512]
     uint8_t* hq;
     uint8_t* hsf;               // [tile][ceil(I/128)][512]
-    float* h;                   // [M*k][I], slot order
     float* y;                   // [M*k][H], slot order
     int* status;
     int* nu_out;                // experts with at least one token (written by plan_kernel)
@@ -152,7 +151,7 @@ struct BatchParams {
     int max_tiles;
 };
 
-// Enqueue the batched layer (route, plan, quantise x, gate_up GEMM + SwiGLU,
+// Enqueue the batched layer (route, plan, quantise x, gate_up GEMM + SwiGLU +
 // quantise h, down GEMM, combine) on `stream`; `grid` = SM count.
 cudaError_t launch_batched(const BatchParams& p, int grid, cudaStream_t stream, int* launches);
 cudaError_t prepare_batched_kernels();
