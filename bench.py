@@ -40,7 +40,8 @@ UNIT = "us/layer"
 SHAPE = synth.GPTOSS_STACK          # 24 distinct gpt-oss-20B-shaped layers
 WORKLOAD = ("gpt-oss-20B-shaped MXFP4 MoE layer decode, H=I=2880, E=32, top-4, M=1; "
             "step s runs layer s mod 24 of 24 resident layers")
-KERNEL_SOURCES = ("bit_moe_decode_02_gb300/csrc/moe_decode.cu",)
+KERNEL_SOURCES = ("bit_moe_decode_02_gb300/csrc/moe_decode_tc.cu", "bit_moe_decode_02_gb300/csrc/tc_ptx.cuh",
+                  "bit_moe_decode_02_gb300/csrc/route.cuh")
 
 
 def dist_env():
@@ -322,7 +323,7 @@ def run_ours(args):
         "gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "kernel": "layer_kernel (one persistent launch per decode layer)",
+                     "kernel": "decode_tc_kernel (persistent, one CTA per SM; after the x-term kernel)",
                      "bytes_per_launch": avg_bytes, "traffic": stored_traffic()},
         "e2e": {"value": 1e6 * e2e_s / (K * world), "unit": UNIT,
                 "h2d_bytes_per_step": H * 2 * 2 + E * 4, "d2h_bytes_per_step": H * 2},

@@ -75,8 +75,15 @@ struct moe_handle {
     uint8_t* arena = nullptr;
     uint32_t* special = nullptr;      // [L][E][2]
     std::vector<char> loaded;
-    // batched path (max_tokens > kMaxTokens): tile-layout copy of the weights
-    bool batched = false;
+    // MXFP4: tile-layout copy of the weights (tensor-core decode and batched paths)
+    bool tiles = false;
+    bool batched = false;             // max_tokens > kMaxTokens
+    size_t tc_smem = 0;
+    float* tc_part2 = nullptr;
+    uint8_t* tc_xt = nullptr;
+    uint8_t* tc_ht = nullptr;
+    float* tc_y = nullptr;
+    unsigned* tc_cnt = nullptr;
     size_t t_gu_expert = 0, t_dn_expert = 0, t_off_dn = 0, t_layer_stride = 0;
     uint8_t* tarena = nullptr;
     int max_tiles = 0;
@@ -170,6 +177,11 @@ void free_handle(moe_handle* h)
     cudaFree(h->st_out);
     cudaFree(h->st_logits);
     cudaFree(h->tarena);
+    cudaFree(h->tc_part2);
+    cudaFree(h->tc_xt);
+    cudaFree(h->tc_ht);
+    cudaFree(h->tc_y);
+    cudaFree(h->tc_cnt);
     cudaFree(h->b_int);
     cudaFree(h->b_wt);
     cudaFree(h->b_tiles);
@@ -233,22 +245,104 @@ moe::LayerParams layer_params(const moe_handle* h, int layer)
     return p;
 }
 
-// Tile-layout weights and the workspace of the batched path.
+// MXFP4: tile-layout weights and the workspace of the tensor-core decode kernel.
+int create_tiles(moe_handle* h)
+{
+    const moe_config& c = h->cfg;
+    const int H = c.hidden, I = c.intermediate, E = c.num_experts;
+    h->tiles = true;
+    h->t_gu_expert = 2 * (size_t)moe::tile_proj_bytes(I, H);
+    h->t_dn_expert = (size_t)moe::tile_proj_bytes(H, I);
+    h->t_off_dn = align_up(E * h->t_gu_expert, 256);
+    h->t_layer_stride = align_up(h->t_off_dn + E * h->t_dn_expert, 256);
+    const int G = h->num_sms;
+    const size_t u2 = moe::tc_max_units2(G, H, I);
+    const size_t ncnt = moe::tc_counter_words(H, I);
+    int rc;
+    if ((rc = dev_alloc(&h->tarena, h->t_layer_stride * c.num_layers, "tile-layout weights")) ||
+        (rc = dev_alloc(&h->tc_part2, u2 * moe::kRowTile * moe::kMaxTokens * sizeof(float), "partials")) ||
+        (rc = dev_alloc(&h->tc_xt, moe::tc_terms_bytes(H), "x terms")) ||
+        (rc = dev_alloc(&h->tc_ht, (size_t)moe::kMaxUnits * moe::tc_terms_bytes(I), "h terms")) ||
+        (rc = dev_alloc(&h->tc_y, (size_t)moe::kMaxUnits * moe::kMaxTokens * H * sizeof(float), "y")) ||
+        (rc = dev_alloc(&h->tc_cnt, ncnt * sizeof(unsigned), "counters")))
+        return rc;
+    cudaError_t e = cudaMemset(h->tc_cnt, 0, ncnt * sizeof(unsigned));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "counters");
+    h->tc_smem = 220 * 1024;
+    if ((e = moe::prepare_decode_tc(h->tc_smem)) != cudaSuccess)
+        return cuda_fail(e, "tensor-core decode kernel set-up");
+    return MOE_OK;
+}
+
+moe::DecodeTcParams tc_params(const moe_handle* h, int layer)
+{
+    const moe_config& c = h->cfg;
+    const uint8_t* tb = h->tarena + (size_t)layer * h->t_layer_stride;
+    const uint8_t* sb = h->arena + (size_t)layer * h->layer_stride;
+    const int H = c.hidden, I = c.intermediate;
+    const int T1 = moe::ceil_div(I, moe::kRowTile), T2 = moe::ceil_div(H, moe::kRowTile);
+    moe::DecodeTcParams p{};
+    p.gu = tb;
+    p.dn = tb + h->t_off_dn;
+    p.gu_expert = (long long)h->t_gu_expert;
+    p.dn_expert = (long long)h->t_dn_expert;
+    p.gu_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(sb + h->off_gu_bias) : nullptr;
+    p.dn_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(sb + h->off_dn_bias) : nullptr;
+    p.part2 = h->tc_part2;
+    p.xt = h->tc_xt;
+    p.ht = h->tc_ht;
+    p.y = h->tc_y;
+    p.hready = h->tc_cnt;
+    p.dn_cnt = p.hready + moe::kMaxUnits * T1;
+    p.row_cnt = p.dn_cnt + moe::kMaxUnits * T2;
+    p.exit_cnt = p.row_cnt + T2;
+    p.status = h->status;
+    p.nu_out = h->stats + layer;
+    p.H = H;
+    p.I = I;
+    p.E = c.num_experts;
+    p.smem_bytes = (int)h->tc_smem;
+    return p;
+}
+
+// Kernel launches of one decode layer: the x-term and layer kernels (MXFP4),
+// or the layer kernel (int4).
+int decode_launches(const moe_handle* h) { return h->tiles ? 2 : 1; }
+
+// The decode layer on the current kernel of this handle's format.
+cudaError_t launch_decode(const moe_handle* h, int layer, const float* logits, const void* x, void* resid,
+                          int M, int k, cudaStream_t s)
+{
+    if (h->tiles) {
+        moe::DecodeTcParams p = tc_params(h, layer);
+        p.logits = logits;
+        p.x = static_cast<const uint16_t*>(x);
+        p.resid = static_cast<uint16_t*>(resid);
+        p.M = M;
+        p.k = k;
+        return moe::launch_decode_tc(p, h->tc_smem, h->num_sms, s);
+    }
+    moe::LayerParams p = layer_params(h, layer);
+    p.logits = logits;
+    p.x = static_cast<const uint16_t*>(x);
+    p.resid = static_cast<uint16_t*>(resid);
+    p.M = M;
+    p.k = k;
+    return moe::launch_layer(p, h->cfg.format, h->grid, s);
+}
+
+// Workspace of the batched path.
 int create_batched(moe_handle* h)
 {
     const moe_config& c = h->cfg;
     const int H = c.hidden, I = c.intermediate, E = c.num_experts;
     const size_t Mk = (size_t)c.max_tokens * c.max_top_k;
     h->batched = true;
-    h->t_gu_expert = 2 * (size_t)moe::tile_proj_bytes(I, H);
-    h->t_dn_expert = (size_t)moe::tile_proj_bytes(H, I);
-    h->t_off_dn = align_up(E * h->t_gu_expert, 256);
-    h->t_layer_stride = align_up(h->t_off_dn + E * h->t_dn_expert, 256);
     h->max_tiles = moe::max_tok_tiles((int)Mk, E);
     const size_t rows = Mk + 16 * (size_t)h->max_tiles;   // padded activation rows, upper bound
     int rc;
-    if ((rc = dev_alloc(&h->tarena, h->t_layer_stride * c.num_layers, "tile-layout weights")) ||
-        (rc = dev_alloc(&h->b_int, (4 * Mk + 1) * sizeof(int), "batched tables")) ||
+    if ((rc = dev_alloc(&h->b_int, (4 * Mk + 1) * sizeof(int), "batched tables")) ||
         (rc = dev_alloc(&h->b_wt, Mk * sizeof(float), "routing weights")) ||
         (rc = dev_alloc(&h->b_tiles, h->max_tiles * sizeof(moe::TokTile), "token tiles")) ||
         (rc = dev_alloc(&h->b_xq, rows * H / 2, "x codes")) ||
@@ -440,7 +534,8 @@ int moe_create(const moe_config* cfg, moe_handle** out)
         free_handle(h);
         return cuda_fail(e, "moe_create setup");
     }
-    if (c.max_tokens > moe::kMaxTokens && (rc = create_batched(h)) != MOE_OK) {
+    if ((c.format == MOE_FMT_MXFP4 && (rc = create_tiles(h)) != MOE_OK) ||
+        (c.max_tokens > moe::kMaxTokens && (rc = create_batched(h)) != MOE_OK)) {
         free_handle(h);
         return rc;
     }
@@ -511,7 +606,7 @@ int moe_load_experts(moe_handle* h, int layer, const void* gu_codes, const void*
         (e = moe::launch_repack(c.format, c.group, st_dnc, st_dns, c.num_experts, c.hidden,
                                 c.intermediate, base + h->off_dn, (long long)h->dn_expert, h->dn_slab,
                                 special, 1, s)) != cudaSuccess ||
-        (h->batched && (e = load_tiles(h, layer, st_guc, st_gus, st_dnc, st_dns, s)) != cudaSuccess) ||
+        (h->tiles && (e = load_tiles(h, layer, st_guc, st_gus, st_dnc, st_dns, s)) != cudaSuccess) ||
         (e = cudaStreamSynchronize(s)) != cudaSuccess) {
         cudaStreamSynchronize(s);
         cudaFree(staging);
@@ -557,18 +652,12 @@ int moe_forward(moe_handle* h, int layer, const void* x_bf16, const float* route
         h->last_bk = top_k;
         return MOE_OK;
     }
-    moe::LayerParams p = layer_params(h, layer);
-    p.logits = router_logits;
-    p.x = static_cast<const uint16_t*>(x_bf16);
-    p.resid = static_cast<uint16_t*>(out_bf16);
-    p.M = M;
-    p.k = top_k;
-    cudaError_t e = moe::launch_layer(p, h->cfg.format, h->grid, (cudaStream_t)stream);
+    cudaError_t e = launch_decode(h, layer, router_logits, x_bf16, out_bf16, M, top_k, (cudaStream_t)stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "moe_forward launch");
     h->last_layers = 1;
     h->last_first_layer = layer;
-    h->last_launches = 1;
+    h->last_launches = decode_launches(h);
     return MOE_OK;
 }
 
@@ -624,15 +713,9 @@ int moe_forward_stack(moe_handle* h, void* resid_bf16, const float* router_logit
         if (e != cudaSuccess)
             return cuda_fail(e, "moe_forward_stack capture begin");
         cudaError_t le = cudaSuccess;
-        for (int l = 0; l < L && le == cudaSuccess; ++l) {
-            moe::LayerParams p = layer_params(h, l);
-            p.logits = router_logits + (size_t)l * M * h->cfg.num_experts;
-            p.x = nullptr;
-            p.resid = static_cast<uint16_t*>(resid_bf16);
-            p.M = M;
-            p.k = top_k;
-            le = moe::launch_layer(p, h->cfg.format, h->grid, cs);
-        }
+        for (int l = 0; l < L && le == cudaSuccess; ++l)
+            le = launch_decode(h, l, router_logits + (size_t)l * M * h->cfg.num_experts, nullptr, resid_bf16, M,
+                               top_k, cs);
         cudaGraph_t graph = nullptr;
         e = cudaStreamEndCapture(cs, &graph);
         if (le != cudaSuccess || e != cudaSuccess) {
@@ -663,7 +746,7 @@ int moe_forward_stack(moe_handle* h, void* resid_bf16, const float* router_logit
         return cuda_fail(e, "moe_forward_stack launch");
     h->last_layers = L;
     h->last_first_layer = 0;
-    h->last_launches = L;
+    h->last_launches = L * decode_launches(h);
     return MOE_OK;
 }
 
@@ -689,13 +772,8 @@ int moe_debug_stack_trace(moe_handle* h, void* resid_bf16, const float* router_l
     uint8_t* tr = static_cast<uint8_t*>(trace_bf16);
     cudaError_t e = cudaMemcpyAsync(tr, resid_bf16, nb, cudaMemcpyDeviceToDevice, s);
     for (int l = 0; l < L && e == cudaSuccess; ++l) {
-        moe::LayerParams p = layer_params(h, l);
-        p.logits = router_logits + (size_t)l * M * h->cfg.num_experts;
-        p.x = nullptr;
-        p.resid = static_cast<uint16_t*>(resid_bf16);
-        p.M = M;
-        p.k = top_k;
-        e = moe::launch_layer(p, h->cfg.format, h->grid, s);
+        e = launch_decode(h, l, router_logits + (size_t)l * M * h->cfg.num_experts, nullptr, resid_bf16, M, top_k,
+                          s);
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(tr + (size_t)(l + 1) * nb, resid_bf16, nb, cudaMemcpyDeviceToDevice, s);
     }
@@ -703,7 +781,7 @@ int moe_debug_stack_trace(moe_handle* h, void* resid_bf16, const float* router_l
         return cuda_fail(e, "moe_debug_stack_trace");
     h->last_layers = L;
     h->last_first_layer = 0;
-    h->last_launches = L;
+    h->last_launches = L * decode_launches(h);
     return MOE_OK;
 }
 
@@ -721,7 +799,9 @@ int moe_get_status(moe_handle* h, void* stream)
     if (st != MOE_OK) {
         // a call gave up waiting: its cross-CTA counters may be left part-way; clear them
         const size_t ncount = moe::counter_words(h->cfg.hidden);
-        if ((e = cudaMemset(h->counters, 0, ncount * sizeof(unsigned))) != cudaSuccess ||
+        if ((h->tc_cnt && (e = cudaMemset(h->tc_cnt, 0, moe::tc_counter_words(h->cfg.hidden, h->cfg.intermediate) *
+                                                       sizeof(unsigned))) != cudaSuccess) ||
+            (e = cudaMemset(h->counters, 0, ncount * sizeof(unsigned))) != cudaSuccess ||
             (e = cudaDeviceSynchronize()) != cudaSuccess)
             return cuda_fail(e, "moe_get_status reset");
     }

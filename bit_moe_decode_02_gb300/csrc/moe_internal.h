@@ -167,6 +167,48 @@ cudaError_t launch_mx_quantize(const float* in, long long n, uint8_t* codes, uin
 cudaError_t launch_untile_h(const BatchParams& p, uint8_t* codes, uint8_t* scales,
                             cudaStream_t stream);
 
+// ------------------------------------------------------ tensor-core decode
+// The MXFP4 decode layer (M <= 4) on tcgen05 kind::mxf4 (moe_decode_tc.cu);
+// weights in the tile layout above.  Two launches: the x-term kernel, then the
+// persistent layer kernel (PDL-chained).
+
+struct DecodeTcParams {
+    const uint8_t* gu;          // tile layout: expert e at + e*gu_expert = [gate proj][up proj]
+    const uint8_t* dn;
+    long long gu_expert, dn_expert;
+    const uint16_t* gu_bias;    // [E][2I] bf16, or nullptr
+    const uint16_t* dn_bias;    // [E][H] bf16, or nullptr
+    const float* logits;        // [M][E]
+    const uint16_t* x;          // [M][H] bf16, or nullptr: RMS-normalise resid
+    uint16_t* resid;            // [M][H] bf16 in/out
+    float* part2;               // down partial sums [unit][128][4]
+    uint8_t* xt;                // x terms of the layer: [H/64][32 rows x 32 B][ceil(H/128)][512]
+    uint8_t* ht;                // h terms per slot: [slot][I/64][32 x 32 B][ceil(I/128)][512]
+    float* y;                   // [slot][H][4]
+    unsigned* hready;           // [slot][T1] h terms of a gate/up pair published (zero between calls)
+    unsigned* dn_cnt;           // [slot][T2] (zero between calls)
+    unsigned* row_cnt;          // [T2] slots finished per output slice (zero between calls)
+    unsigned* exit_cnt;         // [1]
+    int* status;
+    int* nu_out;
+    int H, I, E, M, k;
+    int smem_bytes;             // dynamic shared memory of the layer kernel: the stage ring
+};
+
+// Workspace bounds for G CTAs.
+// Down units: nu * T2 * KC2 with KC2 <= max(1, ceil((2G - nu*T1) / (nu*T2))) + 1 and KC2 <= ceil(I/128).
+inline int tc_max_units2(int G, int H, int I)
+{
+    return 2 * G + kMaxUnits * ceil_div(H, kRowTile) * 2;
+}
+inline size_t tc_terms_bytes(int K) { return (size_t)(K / 64) * 1024 + (size_t)ceil_div(K, 128) * kSfChunk; }
+inline size_t tc_counter_words(int H, int I)
+{
+    return (size_t)kMaxUnits * (ceil_div(I, kRowTile) + ceil_div(H, kRowTile)) + ceil_div(H, kRowTile) + 1;
+}
+cudaError_t prepare_decode_tc(size_t smem);
+cudaError_t launch_decode_tc(const DecodeTcParams& p, size_t smem, int grid, cudaStream_t stream);
+
 // Debug kernels.
 cudaError_t launch_dequant(int fmt, int group, const uint8_t* slabs, int N, int K, int slab_bytes,
                            float* out, cudaStream_t stream);
