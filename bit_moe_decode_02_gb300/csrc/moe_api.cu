@@ -79,10 +79,10 @@ struct moe_handle {
     bool tiles = false;
     bool batched = false;             // max_tokens > kMaxTokens
     size_t tc_smem = 0;
+    float* tc_part1 = nullptr;
     float* tc_part2 = nullptr;
     uint8_t* tc_xt = nullptr;
     uint8_t* tc_ht = nullptr;
-    float* tc_y = nullptr;
     unsigned* tc_cnt = nullptr;
     size_t t_gu_expert = 0, t_dn_expert = 0, t_off_dn = 0, t_layer_stride = 0;
     uint8_t* tarena = nullptr;
@@ -177,10 +177,10 @@ void free_handle(moe_handle* h)
     cudaFree(h->st_out);
     cudaFree(h->st_logits);
     cudaFree(h->tarena);
+    cudaFree(h->tc_part1);
     cudaFree(h->tc_part2);
     cudaFree(h->tc_xt);
     cudaFree(h->tc_ht);
-    cudaFree(h->tc_y);
     cudaFree(h->tc_cnt);
     cudaFree(h->b_int);
     cudaFree(h->b_wt);
@@ -256,14 +256,14 @@ int create_tiles(moe_handle* h)
     h->t_off_dn = align_up(E * h->t_gu_expert, 256);
     h->t_layer_stride = align_up(h->t_off_dn + E * h->t_dn_expert, 256);
     const int G = h->num_sms;
-    const size_t u2 = moe::tc_max_units2(G, H, I);
+    const size_t u1 = moe::tc_max_units1(G, I), u2 = moe::tc_max_units2(G, H, I);
     const size_t ncnt = moe::tc_counter_words(H, I);
     int rc;
     if ((rc = dev_alloc(&h->tarena, h->t_layer_stride * c.num_layers, "tile-layout weights")) ||
+        (rc = dev_alloc(&h->tc_part1, u1 * 2 * moe::kRowTile * moe::kMaxTokens * sizeof(float), "partials")) ||
         (rc = dev_alloc(&h->tc_part2, u2 * moe::kRowTile * moe::kMaxTokens * sizeof(float), "partials")) ||
         (rc = dev_alloc(&h->tc_xt, moe::tc_terms_bytes(H), "x terms")) ||
         (rc = dev_alloc(&h->tc_ht, (size_t)moe::kMaxUnits * moe::tc_terms_bytes(I), "h terms")) ||
-        (rc = dev_alloc(&h->tc_y, (size_t)moe::kMaxUnits * moe::kMaxTokens * H * sizeof(float), "y")) ||
         (rc = dev_alloc(&h->tc_cnt, ncnt * sizeof(unsigned), "counters")))
         return rc;
     cudaError_t e = cudaMemset(h->tc_cnt, 0, ncnt * sizeof(unsigned));
@@ -289,14 +289,14 @@ moe::DecodeTcParams tc_params(const moe_handle* h, int layer)
     p.dn_expert = (long long)h->t_dn_expert;
     p.gu_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(sb + h->off_gu_bias) : nullptr;
     p.dn_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(sb + h->off_dn_bias) : nullptr;
+    p.part1 = h->tc_part1;
     p.part2 = h->tc_part2;
     p.xt = h->tc_xt;
     p.ht = h->tc_ht;
-    p.y = h->tc_y;
-    p.hready = h->tc_cnt;
+    p.pair_cnt = h->tc_cnt;
+    p.hready = p.pair_cnt + moe::kMaxUnits * T1;
     p.dn_cnt = p.hready + moe::kMaxUnits * T1;
-    p.row_cnt = p.dn_cnt + moe::kMaxUnits * T2;
-    p.exit_cnt = p.row_cnt + T2;
+    p.exit_cnt = p.dn_cnt + T2;
     p.status = h->status;
     p.nu_out = h->stats + layer;
     p.H = H;

@@ -69,14 +69,13 @@ __device__ __forceinline__ int rows_for(int M) { return M * kTerms <= 16 ? 16 : 
 
 struct Geometry {
     int KSH, KSI, CHH, CHI, T1, T2;   // k-steps, 128-element chunks and 128-row tiles of H and I
-    int nu, KC2, U1, U2;
-    int PG;                           // CTAs [0, PG) take the pairs; the rest of the list is spread below
+    int nu, KC1, KC2, U1, U2;
 };
 
-// Work units: U1 gate/up tile pairs (full K) and U2 down tiles split in KC2 K
-// pieces, dealt round-robin over the CTAs from one list, pairs first.  A CTA's
-// down pieces stream into its ring behind its pair (or from the start, for a
-// CTA without one), so that most down weights are resident when h is ready.
+// Work units, dealt round-robin over the CTAs from one list: U1 gate/up
+// pieces (nu*T1 tile pairs in KC1 K pieces), then U2 down pieces (nu*T2
+// tiles in KC2 K pieces).  A CTA's down pieces stream into its ring behind
+// its pair, so most down weights are resident when h is ready.
 __device__ __forceinline__ Geometry geometry(const DecodeTcParams& p, int nu, int G)
 {
     Geometry g;
@@ -87,26 +86,21 @@ __device__ __forceinline__ Geometry geometry(const DecodeTcParams& p, int nu, in
     g.T1 = ceil_div(p.I, kRowTile);
     g.T2 = ceil_div(p.H, kRowTile);
     g.nu = nu;
-    g.U1 = nu * g.T1;
-    const int per = nu * g.T2;
-    // one list, round-robin over the CTAs: pairs first, then down pieces sized
-    // so that the list comes to about two units per CTA
-    g.PG = 0;
-    const int left = 2 * G - g.U1;
-    const int k2 = left > 0 ? (left + per / 2) / per : 1;
+    const int pairs = nu * g.T1, tiles = nu * g.T2;
+    // Gate/up pairs stay whole (a K split makes h wait for the slowest piece, and
+    // measured slower); down tiles split so that the list comes to about two
+    // units per CTA.
+    g.KC1 = 1;
+    const int left = 2 * G - pairs;
+    const int k2 = left > 0 ? (left + tiles / 2) / tiles : 1;
     g.KC2 = k2 < 1 ? 1 : (k2 > g.CHI ? g.CHI : k2);
-    g.U2 = per * g.KC2;
+    g.U1 = pairs * g.KC1;
+    g.U2 = tiles * g.KC2;
     return g;
 }
 
 __device__ __forceinline__ int units_of(const Geometry& g, int b, int G)
 {
-    if (g.PG > 0) {
-        if (b < g.PG)
-            return 1;
-        const int D = G - g.PG, j = b - g.PG;
-        return g.U2 > j ? (g.U2 - j + D - 1) / D : 0;
-    }
     const int U = g.U1 + g.U2;
     return U > b ? (U - b + G - 1) / G : 0;
 }
@@ -117,38 +111,28 @@ struct Unit {
     int ks0, ks1;       // k-steps [ks0, ks1)
     int R;              // rows of the tile (128, or the remainder)
     int tile;           // pair s * T1 + t, or down tile s * T2 + t
-    int id;             // down: unit index d = tile * KC2 + piece
+    int pc;             // K piece
+    int id;             // unit index within its kind: tile * KC + piece
 };
 
-// Unit i of CTA b (a CTA's pairs precede its down units).
+// Unit i of CTA b: list entry b + G * i (a CTA's gate/up pieces precede its down pieces).
 __device__ __forceinline__ Unit unit_at(const Geometry& g, const DecodeTcParams& p, int i, int b, int G)
 {
     Unit u;
-    int x;
-    if (g.PG > 0)
-        x = b < g.PG ? b : g.U1 + (b - g.PG) + (G - g.PG) * i;
-    else
-        x = b + G * i;
+    const int x = b + G * i;
     u.down = x >= g.U1;
-    if (!u.down) {
-        u.tile = x;
-        u.t = x % g.T1;
-        u.s = x / g.T1;
-        u.ks0 = 0;
-        u.ks1 = g.KSH;
-        u.id = x;
-        u.R = p.I - u.t * kRowTile < kRowTile ? p.I - u.t * kRowTile : kRowTile;
-    } else {
-        u.id = x - g.U1;
-        const int c = u.id % g.KC2;
-        u.tile = u.id / g.KC2;
-        u.t = u.tile % g.T2;
-        u.s = u.tile / g.T2;
-        const int c0 = c * g.CHI / g.KC2, c1 = (c + 1) * g.CHI / g.KC2;
-        u.ks0 = 2 * c0;
-        u.ks1 = 2 * c1 < g.KSI ? 2 * c1 : g.KSI;
-        u.R = p.H - u.t * kRowTile < kRowTile ? p.H - u.t * kRowTile : kRowTile;
-    }
+    u.id = u.down ? x - g.U1 : x;
+    const int KC = u.down ? g.KC2 : g.KC1, T = u.down ? g.T2 : g.T1;
+    const int CH = u.down ? g.CHI : g.CHH, KS = u.down ? g.KSI : g.KSH;
+    u.pc = u.id % KC;
+    u.tile = u.id / KC;
+    u.t = u.tile % T;
+    u.s = u.tile / T;
+    const int c0 = u.pc * CH / KC, c1 = (u.pc + 1) * CH / KC;
+    u.ks0 = 2 * c0;
+    u.ks1 = 2 * c1 < KS ? 2 * c1 : KS;
+    const int rows = u.down ? p.H : p.I;
+    u.R = rows - u.t * kRowTile < kRowTile ? rows - u.t * kRowTile : kRowTile;
     return u;
 }
 
@@ -365,6 +349,7 @@ struct TcSmem {
     int nu;
     int unit_expert[kMaxUnits];
     unsigned char unit_of[kMaxExperts];
+    float wslot[kMaxUnits][kMaxTokens];   // routing weight of token m for expert slot s (0 if not chosen)
     int flag;
 };
 
@@ -433,6 +418,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                 ++u;
             }
             const int nu = __shfl_sync(0xffffffffu, incl, 31);
+            for (int x = lane; x < nu * kMaxTokens; x += 32)
+                sh.wslot[x / kMaxTokens][x % kMaxTokens] = 0.f;
+            __syncwarp();
+            for (int x = lane; x < M * p.k; x += 32) {
+                const int m = x / p.k, k2 = x % p.k;
+                sh.wslot[sh.unit_of[sh.sel[m][k2]]][m] = sh.wt[m][k2];
+            }
             if (lane == 0) {
                 sh.nu = nu;
                 asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -674,72 +666,115 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
         unsigned pend = 0u;   // te == 0: down counter before this CTA's previous piece
         int pend_i = -1;
 
-        // last K piece of down tile `u`: y of its expert slot, then (the last slot
-        // of the output slice) out = r + sum_s w_s y_s in each token's choice order
-        auto finish_tile = [&](const Unit& u, const float (&own)[kMaxTokens], bool single) {
-            const int row = u.t * kRowTile + r;
+        // the last piece of output slice t: out = r + sum over expert slots and K
+        // pieces of the weighted partials + sum_s w_s b_s, in a fixed order
+        auto finish_slice = [&](int t) {
+            const int row = t * kRowTile + r;
             if (row < p.H) {
-                const float bd = p.dn_bias ? bf16f(p.dn_bias[(size_t)sh.unit_expert[u.s] * p.H + row]) : 0.f;
-                float ys[kMaxTokens] = {bd, bd, bd, bd};
-                if (single) {
+                float acc[kMaxTokens] = {0.f, 0.f, 0.f, 0.f};
+                const int npc = g.nu * g.KC2;
+                for (int z0 = 0; z0 < npc; z0 += 8) {
+                    float4 a[8];
 #pragma unroll
-                    for (int m = 0; m < kMaxTokens; ++m)
-                        ys[m] += own[m];
-                } else {
-                    for (int c0 = 0; c0 < g.KC2; c0 += 8) {
-                        float4 a[8];
+                    for (int z = 0; z < 8; ++z)
+                        if (z0 + z < npc)
+                            a[z] = __ldcg(reinterpret_cast<const float4*>(
+                                              p.part2 + ((size_t)t * npc + z0 + z) * kRowTile * kMaxTokens) + r);
 #pragma unroll
-                        for (int z = 0; z < 8; ++z)
-                            if (c0 + z < g.KC2)
-                                a[z] = __ldcg(reinterpret_cast<const float4*>(
-                                                  p.part2 + (size_t)(u.tile * g.KC2 + c0 + z) * kRowTile * kMaxTokens) + r);
-#pragma unroll
-                        for (int z = 0; z < 8; ++z)
-                            if (c0 + z < g.KC2) {
-                                ys[0] += a[z].x; ys[1] += a[z].y; ys[2] += a[z].z; ys[3] += a[z].w;
-                            }
-                    }
+                    for (int z = 0; z < 8; ++z)
+                        if (z0 + z < npc) {
+                            acc[0] += a[z].x; acc[1] += a[z].y; acc[2] += a[z].z; acc[3] += a[z].w;
+                        }
                 }
-                reinterpret_cast<float4*>(p.y + (size_t)u.s * p.H * kMaxTokens)[row] =
-                    make_float4(ys[0], ys[1], ys[2], ys[3]);
-            }
-            epi_barrier();
-            if (te == 0)
-                sh.flag = atom_add_acq_rel(p.row_cnt + u.t, 1u) == (unsigned)g.nu - 1u;
-            epi_barrier();
-            if (sh.flag && row < p.H) {
+                if (p.dn_bias)
+                    for (int s2 = 0; s2 < g.nu; ++s2) {
+                        const float bd = bf16f(p.dn_bias[(size_t)sh.unit_expert[s2] * p.H + row]);
+#pragma unroll
+                        for (int m = 0; m < kMaxTokens; ++m)
+                            acc[m] = fmaf(sh.wslot[s2][m], bd, acc[m]);
+                    }
 #pragma unroll
                 for (int m = 0; m < kMaxTokens; ++m) {
                     if (m >= M)
                         break;
-                    float acc = 0.f;
-                    for (int k0 = 0; k0 < p.k; k0 += 8) {   // the slots' y, loads first
-                        float yv[8];
-#pragma unroll
-                        for (int z = 0; z < 8; ++z)
-                            if (k0 + z < p.k)
-                                yv[z] = __ldcg(p.y + ((size_t)sh.unit_of[sh.sel[m][k0 + z]] * p.H + row) * kMaxTokens + m);
-#pragma unroll
-                        for (int z = 0; z < 8; ++z)
-                            if (k0 + z < p.k)
-                                acc = fmaf(sh.wt[m][k0 + z], yv[z], acc);
-                    }
                     uint16_t* o = p.resid + (size_t)m * p.H + row;
-                    *o = f2bf16_rne(bf16f(__ldcg(o)) + acc);
+                    *o = f2bf16_rne(bf16f(__ldcg(o)) + acc[m]);
                 }
             }
-            epi_barrier();   // sh.flag is read before its next write
+        };
+
+        // h = silu(gate + b) * (up + b) of this warp's 32 rows of pair u (the
+        // pieces' partials summed, or the pair's own sums), its MX terms to the
+        // slot's h-term buffer, then the pair's release flag
+        auto publish_h = [&](const Unit& u, const float (&gs_in)[kMaxTokens], const float (&us_in)[kMaxTokens],
+                             bool from_partials) {
+            const int row = u.t * kRowTile + r;
+            if (u.t * kRowTile + 32 * q < p.I) {   // a warp's 32 rows are all valid or all not
+                const int e = sh.unit_expert[u.s];
+                const float bg = p.gu_bias ? bf16f(p.gu_bias[(size_t)e * 2 * p.I + row]) : 0.f;
+                const float bu = p.gu_bias ? bf16f(p.gu_bias[(size_t)e * 2 * p.I + p.I + row]) : 0.f;
+                float gs[kMaxTokens], us[kMaxTokens];
+#pragma unroll
+                for (int m = 0; m < kMaxTokens; ++m) {
+                    gs[m] = gs_in[m] + bg;
+                    us[m] = us_in[m] + bu;
+                }
+                if (from_partials)
+                    for (int c0 = 0; c0 < g.KC1; c0 += 8) {
+                        float4 a[8], c4[8];
+#pragma unroll
+                        for (int z = 0; z < 8; ++z)
+                            if (c0 + z < g.KC1) {
+                                const float4* src = reinterpret_cast<const float4*>(
+                                    p.part1 + ((size_t)(u.tile * g.KC1 + c0 + z) * 2) * kRowTile * kMaxTokens);
+                                a[z] = __ldcg(src + r);
+                                c4[z] = __ldcg(src + kRowTile + r);
+                            }
+#pragma unroll
+                        for (int z = 0; z < 8; ++z)
+                            if (c0 + z < g.KC1) {
+                                gs[0] += a[z].x; gs[1] += a[z].y; gs[2] += a[z].z; gs[3] += a[z].w;
+                                us[0] += c4[z].x; us[1] += c4[z].y; us[2] += c4[z].z; us[3] += c4[z].w;
+                            }
+                    }
+                float hv[kMaxTokens];
+#pragma unroll
+                for (int m = 0; m < kMaxTokens; ++m)
+                    hv[m] = gs[m] / (1.0f + expf(-gs[m])) * us[m];
+                uint8_t* dst = p.ht + (long long)u.s * hstride;
+                warp_terms_rows(hv, M, row >> 5, dst, dst + (long long)KSI * kAtom, lane);
+            }
+            epi_barrier();
+            if (te == 0)
+                st_release_u32(p.hready + u.tile, 1u);
+        };
+        const float zero4[kMaxTokens] = {0.f, 0.f, 0.f, 0.f};
+        // unit pi counted in with counter value `oldv` before it: finish its pair or
+        // output slice if it was the last piece
+        auto resolve = [&](int pi, unsigned oldv) {
+            const Unit pu = unit_at(g, p, pi, b, G);
+            const unsigned need = pu.down ? (unsigned)(g.nu * g.KC2) : (unsigned)g.KC1;
+            if (te == 0)
+                sh.flag = oldv == need - 1u;
+            epi_barrier();
+            const bool last = sh.flag;
+            epi_barrier();
+            if (last) {
+                if (pu.down)
+                    finish_slice(pu.t);
+                else
+                    publish_h(pu, zero4, zero4, true);
+            }
         };
 
         for (int i = 0; i < nunits; ++i) {
             const Unit u = unit_at(g, p, i, b, G);
-            const int row = u.t * kRowTile + r;
-            const bool valid = u.t * kRowTile + 32 * q < (u.down ? p.H : p.I);   // a warp's rows: all or none
-            float bg = 0.f, bu = 0.f;
-            if (!u.down && valid && p.gu_bias) {   // issued before the wait for the accumulators
-                const int e = sh.unit_expert[u.s];
-                bg = bf16f(p.gu_bias[(size_t)e * 2 * p.I + row]);
-                bu = bf16f(p.gu_bias[(size_t)e * 2 * p.I + p.I + row]);
+            if (u.down && pend_i >= 0 && !unit_at(g, p, pend_i, b, G).down) {
+                // a pending gate/up piece is resolved before any down unit is waited
+                // for: that down unit may need the very h this CTA has to publish
+                epi_barrier();
+                resolve(pend_i, pend);
+                pend_i = -1;
             }
             // ---- drain: each token's term columns summed
             const uint32_t buf = i & 1;
@@ -773,62 +808,40 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&sh.acce[buf]);
+            if (!u.down && g.KC1 == 1) {   // a whole pair: h right away
+                publish_h(u, s0, s1, false);
+                continue;
+            }
+            // ---- a piece: its partials (down: weighted by each token's routing weight
+            // for this expert slot), counted into its pair / output slice
+            unsigned* cnt;
             if (!u.down) {
-                // ---- a gate/up pair: h = silu(gate) * up for this warp's 32 rows, its MX
-                // terms to the slot's h-term buffer, then the pair's release flag
-                if (valid) {
-                    float hv[kMaxTokens];
+                float4* dst = reinterpret_cast<float4*>(p.part1 + ((size_t)u.id * 2) * kRowTile * kMaxTokens);
+                dst[r] = make_float4(s0[0], s0[1], s0[2], s0[3]);
+                dst[kRowTile + r] = make_float4(s1[0], s1[1], s1[2], s1[3]);
+                cnt = p.pair_cnt + u.tile;
+            } else {
 #pragma unroll
-                    for (int m = 0; m < kMaxTokens; ++m) {
-                        const float gg = s0[m] + bg;
-                        hv[m] = gg / (1.0f + expf(-gg)) * (s1[m] + bu);
-                    }
-                    uint8_t* dst = p.ht + (long long)u.s * hstride;
-                    warp_terms_rows(hv, M, row >> 5, dst, dst + (long long)KSI * kAtom, lane);
-                }
-                epi_barrier();
-                if (te == 0)
-                    st_release_u32(p.hready + u.tile, 1u);
-                continue;
+                for (int m = 0; m < kMaxTokens; ++m)
+                    s0[m] *= m < M ? sh.wslot[u.s][m] : 0.f;
+                reinterpret_cast<float4*>(p.part2 + ((size_t)u.t * g.nu * g.KC2 + u.s * g.KC2 + u.pc) *
+                                                        kRowTile * kMaxTokens)[r] = make_float4(s0[0], s0[1], s0[2], s0[3]);
+                cnt = p.dn_cnt + u.t;
             }
-            // ---- a down piece
-            if (g.KC2 == 1) {
-                finish_tile(u, s0, true);
-                continue;
-            }
-            reinterpret_cast<float4*>(p.part2 + (size_t)u.id * kRowTile * kMaxTokens)[r] =
-                make_float4(s0[0], s0[1], s0[2], s0[3]);
             epi_barrier();   // the piece's partials are stored
-            // count the piece in; whether it was the tile's last is read one unit later,
-            // so the atomic's latency hides behind the next accumulator wait
-            unsigned prev = pend;
-            if (te == 0)   // releases the partials; acquires the other pieces' if last
-                pend = atom_add_acq_rel(p.dn_cnt + u.tile, 1u);
+            // whether this was the last piece is read one unit later, so the atomic's
+            // latency hides behind the next accumulator wait
+            const unsigned prev = pend;
             const int prev_i = pend_i;
+            if (te == 0)   // releases the partials; acquires the other pieces' if last
+                pend = atom_add_acq_rel(cnt, 1u);
             pend_i = i;
-            if (prev_i >= 0) {
-                if (te == 0)
-                    sh.flag = prev == (unsigned)g.KC2 - 1u;
-                epi_barrier();
-                const bool last = sh.flag;
-                epi_barrier();
-                if (last) {
-                    const float none[kMaxTokens] = {0.f, 0.f, 0.f, 0.f};
-                    finish_tile(unit_at(g, p, prev_i, b, G), none, false);
-                }
-            }
+            if (prev_i >= 0)
+                resolve(prev_i, prev);
         }
         if (pend_i >= 0) {
             epi_barrier();
-            if (te == 0)
-                sh.flag = pend == (unsigned)g.KC2 - 1u;
-            epi_barrier();
-            const bool last = sh.flag;
-            epi_barrier();
-            if (last) {
-                const float none[kMaxTokens] = {0.f, 0.f, 0.f, 0.f};
-                finish_tile(unit_at(g, p, pend_i, b, G), none, false);
-            }
+            resolve(pend_i, pend);
         }
     }
 
@@ -838,12 +851,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
     if (tid == 0) {
         __threadfence();
         if (atomicAdd(p.exit_cnt, 1u) == (unsigned)G - 1u) {
-            for (int i = 0; i < g.nu * g.T1; ++i)
+            for (int i = 0; i < g.nu * g.T1; ++i) {
                 p.hready[i] = 0u;
-            for (int i = 0; i < g.nu * g.T2; ++i)
-                p.dn_cnt[i] = 0u;
+                p.pair_cnt[i] = 0u;
+            }
             for (int i = 0; i < g.T2; ++i)
-                p.row_cnt[i] = 0u;
+                p.dn_cnt[i] = 0u;
             *p.exit_cnt = 0u;
             __threadfence();
         }

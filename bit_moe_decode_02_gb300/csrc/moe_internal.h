@@ -181,13 +181,13 @@ struct DecodeTcParams {
     const float* logits;        // [M][E]
     const uint16_t* x;          // [M][H] bf16, or nullptr: RMS-normalise resid
     uint16_t* resid;            // [M][H] bf16 in/out
-    float* part2;               // down partial sums [unit][128][4]
+    float* part1;               // gate/up partials [pair][K piece][2][128][4]
+    float* part2;               // weighted down partials [output slice][slot][K piece][128][4]
     uint8_t* xt;                // x terms of the layer: [H/64][32 rows x 32 B][ceil(H/128)][512]
     uint8_t* ht;                // h terms per slot: [slot][I/64][32 x 32 B][ceil(I/128)][512]
-    float* y;                   // [slot][H][4]
+    unsigned* pair_cnt;         // [slot][T1] gate/up K pieces finished (zero between calls)
     unsigned* hready;           // [slot][T1] h terms of a gate/up pair published (zero between calls)
-    unsigned* dn_cnt;           // [slot][T2] (zero between calls)
-    unsigned* row_cnt;          // [T2] slots finished per output slice (zero between calls)
+    unsigned* dn_cnt;           // [T2] down pieces finished per output slice (zero between calls)
     unsigned* exit_cnt;         // [1]
     int* status;
     int* nu_out;
@@ -196,15 +196,14 @@ struct DecodeTcParams {
 };
 
 // Workspace bounds for G CTAs.
-// Down units: nu * T2 * KC2 with KC2 <= max(1, ceil((2G - nu*T1) / (nu*T2))) + 1 and KC2 <= ceil(I/128).
-inline int tc_max_units2(int G, int H, int I)
-{
-    return 2 * G + kMaxUnits * ceil_div(H, kRowTile) * 2;
-}
+// Unit counts: U1 = pairs * KC1, U2 = tiles * KC2 with KC1 = 2k, KC2 = k,
+// k = ceil(3G / (2 pairs + tiles)), so U1 < 3G + 2 pairs and U2 < 1.5G + tiles.
+inline int tc_max_units1(int G, int I) { return 3 * G + 2 * kMaxUnits * ceil_div(I, kRowTile); }
+inline int tc_max_units2(int G, int H, int I) { return 2 * G + kMaxUnits * ceil_div(H, kRowTile); }
 inline size_t tc_terms_bytes(int K) { return (size_t)(K / 64) * 1024 + (size_t)ceil_div(K, 128) * kSfChunk; }
 inline size_t tc_counter_words(int H, int I)
 {
-    return (size_t)kMaxUnits * (ceil_div(I, kRowTile) + ceil_div(H, kRowTile)) + ceil_div(H, kRowTile) + 1;
+    return 2 * (size_t)kMaxUnits * ceil_div(I, kRowTile) + ceil_div(H, kRowTile) + 1;
 }
 cudaError_t prepare_decode_tc(size_t smem);
 cudaError_t launch_decode_tc(const DecodeTcParams& p, size_t smem, int grid, cudaStream_t stream);
