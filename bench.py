@@ -323,7 +323,7 @@ def run_ours(args):
         "gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "kernel": "decode_tc_kernel (persistent, one CTA per SM; after the x-term kernel)",
+                     "kernel": "decode_tc_kernel (persistent, one CTA per SM, one launch per layer)",
                      "bytes_per_launch": avg_bytes, "traffic": stored_traffic()},
         "e2e": {"value": 1e6 * e2e_s / (K * world), "unit": UNIT,
                 "h2d_bytes_per_step": H * 2 * 2 + E * 4, "d2h_bytes_per_step": H * 2},

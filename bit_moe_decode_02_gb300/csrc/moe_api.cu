@@ -79,11 +79,9 @@ struct moe_handle {
     bool tiles = false;
     bool batched = false;             // max_tokens > kMaxTokens
     size_t tc_smem = 0;
-    float* tc_part1 = nullptr;
-    float* tc_part2 = nullptr;
+    float* tc_part = nullptr;
     uint8_t* tc_xt = nullptr;
-    uint8_t* tc_ht = nullptr;
-    unsigned* tc_cnt = nullptr;
+    unsigned long long* tc_cnt = nullptr;
     size_t t_gu_expert = 0, t_dn_expert = 0, t_off_dn = 0, t_layer_stride = 0;
     uint8_t* tarena = nullptr;
     int max_tiles = 0;
@@ -177,10 +175,8 @@ void free_handle(moe_handle* h)
     cudaFree(h->st_out);
     cudaFree(h->st_logits);
     cudaFree(h->tarena);
-    cudaFree(h->tc_part1);
-    cudaFree(h->tc_part2);
+    cudaFree(h->tc_part);
     cudaFree(h->tc_xt);
-    cudaFree(h->tc_ht);
     cudaFree(h->tc_cnt);
     cudaFree(h->b_int);
     cudaFree(h->b_wt);
@@ -251,25 +247,30 @@ int create_tiles(moe_handle* h)
     const moe_config& c = h->cfg;
     const int H = c.hidden, I = c.intermediate, E = c.num_experts;
     h->tiles = true;
-    h->t_gu_expert = 2 * (size_t)moe::tile_proj_bytes(I, H);
+    h->t_gu_expert = (size_t)moe::tile_proj_bytes(2 * I, H);   // interleaved gate_up
     h->t_dn_expert = (size_t)moe::tile_proj_bytes(H, I);
     h->t_off_dn = align_up(E * h->t_gu_expert, 256);
     h->t_layer_stride = align_up(h->t_off_dn + E * h->t_dn_expert, 256);
     const int G = h->num_sms;
-    const size_t u1 = moe::tc_max_units1(G, I), u2 = moe::tc_max_units2(G, H, I);
-    const size_t ncnt = moe::tc_counter_words(H, I);
     int rc;
     if ((rc = dev_alloc(&h->tarena, h->t_layer_stride * c.num_layers, "tile-layout weights")) ||
-        (rc = dev_alloc(&h->tc_part1, u1 * 2 * moe::kRowTile * moe::kMaxTokens * sizeof(float), "partials")) ||
-        (rc = dev_alloc(&h->tc_part2, u2 * moe::kRowTile * moe::kMaxTokens * sizeof(float), "partials")) ||
+        (rc = dev_alloc(&h->tc_part, moe::tc_part_bytes(G, H), "per-CTA outputs")) ||
         (rc = dev_alloc(&h->tc_xt, moe::tc_terms_bytes(H), "x terms")) ||
-        (rc = dev_alloc(&h->tc_ht, (size_t)moe::kMaxUnits * moe::tc_terms_bytes(I), "h terms")) ||
-        (rc = dev_alloc(&h->tc_cnt, ncnt * sizeof(unsigned), "counters")))
+        (rc = dev_alloc(&h->tc_cnt, moe::kTcCounterWords * sizeof(unsigned long long), "counters")))
         return rc;
-    cudaError_t e = cudaMemset(h->tc_cnt, 0, ncnt * sizeof(unsigned));
+    cudaError_t e = cudaMemset(h->tc_cnt, 0, moe::kTcCounterWords * sizeof(unsigned long long));
+    // x-term rows past M * 8 are never written and feed MMA columns nobody reads:
+    // keep them zero (valid E2M1 codes, E8M0 byte 0) instead of leftover bytes
+    if (e == cudaSuccess)
+        e = cudaMemset(h->tc_xt, 0, moe::tc_terms_bytes(H));
     if (e != cudaSuccess)
         return cuda_fail(e, "counters");
-    h->tc_smem = 220 * 1024;
+    // all the shared memory a block may have: the kernel's own plus the stage ring
+    int dev = 0, optin = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+        return cuda_fail(e, "shared memory limit");
+    h->tc_smem = (size_t)optin - moe::decode_tc_static_smem();
     if ((e = moe::prepare_decode_tc(h->tc_smem)) != cudaSuccess)
         return cuda_fail(e, "tensor-core decode kernel set-up");
     return MOE_OK;
@@ -280,8 +281,6 @@ moe::DecodeTcParams tc_params(const moe_handle* h, int layer)
     const moe_config& c = h->cfg;
     const uint8_t* tb = h->tarena + (size_t)layer * h->t_layer_stride;
     const uint8_t* sb = h->arena + (size_t)layer * h->layer_stride;
-    const int H = c.hidden, I = c.intermediate;
-    const int T1 = moe::ceil_div(I, moe::kRowTile), T2 = moe::ceil_div(H, moe::kRowTile);
     moe::DecodeTcParams p{};
     p.gu = tb;
     p.dn = tb + h->t_off_dn;
@@ -289,26 +288,21 @@ moe::DecodeTcParams tc_params(const moe_handle* h, int layer)
     p.dn_expert = (long long)h->t_dn_expert;
     p.gu_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(sb + h->off_gu_bias) : nullptr;
     p.dn_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(sb + h->off_dn_bias) : nullptr;
-    p.part1 = h->tc_part1;
-    p.part2 = h->tc_part2;
+    p.part = h->tc_part;
     p.xt = h->tc_xt;
-    p.ht = h->tc_ht;
-    p.pair_cnt = h->tc_cnt;
-    p.hready = p.pair_cnt + moe::kMaxUnits * T1;
-    p.dn_cnt = p.hready + moe::kMaxUnits * T1;
-    p.exit_cnt = p.dn_cnt + T2;
+    p.xcnt = h->tc_cnt;
+    p.done = h->tc_cnt + 1;
     p.status = h->status;
     p.nu_out = h->stats + layer;
-    p.H = H;
-    p.I = I;
+    p.H = c.hidden;
+    p.I = c.intermediate;
     p.E = c.num_experts;
     p.smem_bytes = (int)h->tc_smem;
     return p;
 }
 
-// Kernel launches of one decode layer: the x-term and layer kernels (MXFP4),
-// or the layer kernel (int4).
-int decode_launches(const moe_handle* h) { return h->tiles ? 2 : 1; }
+// Kernel launches of one decode layer: the layer kernel (tensor-core MXFP4 or int4).
+int decode_launches(const moe_handle*) { return 1; }
 
 // The decode layer on the current kernel of this handle's format.
 cudaError_t launch_decode(const moe_handle* h, int layer, const float* logits, const void* x, void* resid,
@@ -419,15 +413,11 @@ cudaError_t load_tiles(moe_handle* h, int layer, const uint8_t* guc, const uint8
     const moe_config& c = h->cfg;
     const int H = c.hidden, I = c.intermediate, E = c.num_experts;
     uint8_t* tb = h->tarena + (size_t)layer * h->t_layer_stride;
-    const long long proj = moe::tile_proj_bytes(I, H);
     cudaError_t e;
-    if ((e = moe::launch_repack_tiles(guc, gus, E, 2 * I, 0, I, H, tb, (long long)h->t_gu_expert, s)) !=
-            cudaSuccess ||
-        (e = moe::launch_repack_tiles(guc, gus, E, 2 * I, I, I, H, tb + proj, (long long)h->t_gu_expert,
-                                      s)) != cudaSuccess)
+    if ((e = moe::launch_repack_tiles(guc, gus, E, 2 * I, 2 * I, H, I, tb, (long long)h->t_gu_expert, s)) !=
+        cudaSuccess)
         return e;
-    return moe::launch_repack_tiles(dnc, dns, E, H, 0, H, I, tb + h->t_off_dn, (long long)h->t_dn_expert,
-                                    s);
+    return moe::launch_repack_tiles(dnc, dns, E, H, H, I, 0, tb + h->t_off_dn, (long long)h->t_dn_expert, s);
 }
 
 }  // namespace
@@ -799,8 +789,7 @@ int moe_get_status(moe_handle* h, void* stream)
     if (st != MOE_OK) {
         // a call gave up waiting: its cross-CTA counters may be left part-way; clear them
         const size_t ncount = moe::counter_words(h->cfg.hidden);
-        if ((h->tc_cnt && (e = cudaMemset(h->tc_cnt, 0, moe::tc_counter_words(h->cfg.hidden, h->cfg.intermediate) *
-                                                       sizeof(unsigned))) != cudaSuccess) ||
+        if ((h->tc_cnt && (e = cudaMemset(h->tc_cnt, 0, moe::kTcCounterWords * sizeof(unsigned long long))) != cudaSuccess) ||
             (e = cudaMemset(h->counters, 0, ncount * sizeof(unsigned))) != cudaSuccess ||
             (e = cudaDeviceSynchronize()) != cudaSuccess)
             return cuda_fail(e, "moe_get_status reset");

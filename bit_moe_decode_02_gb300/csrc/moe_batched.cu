@@ -260,15 +260,14 @@ __global__ void untile_h_kernel(BatchParams p, uint8_t* codes, uint8_t* scales)
 // ------------------------------------------------------------ grouped GEMM
 
 struct GemmParams {
-    const uint8_t* w;       // tile-layout weights; expert e at + e * w_expert
+    const uint8_t* w;       // tile-layout weights; expert e at + e * w_expert (DUAL: interleaved gate_up)
     long long w_expert;
-    long long proj2;        // offset of the second (up) projection, DUAL only
-    int rows, K;            // output rows of one projection, reduction length
+    int rows, K;            // output rows (DUAL: rows of h, the projection has 2 * rows), reduction length
     const uint8_t* bq;      // activation codes (tile order)
     const uint8_t* bsf;     // activation scale chunks
     const TokTile* tiles;
     const int* ntiles;
-    const uint16_t* bias;   // [E][bias_stride] bf16 or nullptr; DUAL: up bias at + rows
+    const uint16_t* bias;   // [E][bias_stride] bf16 or nullptr; DUAL: gate | up
     int bias_stride;
     float* out;             // single: y [slots][rows] fp32
     uint8_t* hq;            // DUAL: MX(h) codes in the down GEMM's activation tile order
@@ -282,21 +281,18 @@ constexpr int kRingBytes = 200 * 1024;   // shared-memory stage ring (byte-granu
 constexpr int kRingSlack = 4096;         // read slack past the ring end (see Stage)
 constexpr int kStageSlots = 16;          // stages in flight at most (mbarrier pairs)
 
-template <bool DUAL>
 struct GemmCfg {
     static constexpr int kSmem = kRingBytes + kRingSlack;
-    static constexpr int kAccCols = (DUAL ? 2 : 1) * kTokTile;   // per accumulator buffer
-    static constexpr int kSfSet = (DUAL ? 3 : 2) * 4 * (kStageSteps / 2);   // tensor-memory columns per scale set
+    static constexpr int kAccCols = kTokTile;                 // per accumulator buffer
+    static constexpr int kSfSet = 2 * 4 * (kStageSteps / 2);  // tensor-memory columns per scale set
     static_assert(kSfCol + 2 * kSfSet <= 512, "tensor memory: accumulators + two scale sets");
 };
 
-// One pipeline stage: `steps` k-steps of R weight rows (two projections if
-// DUAL) and npad activation rows, with their scale chunks, packed as
-// [A0][A1][B][SFA0][SFA1][SFB] and sized to what it holds, so that a small
-// token tile leaves the ring to weight bytes.  For a partial row tile
-// (R = 64) the MMA still reads 128 rows of the last k-step block, up to 2 KB
-// past A; that lands inside the stage or in the ring's slack.
-template <bool DUAL>
+// One pipeline stage: `steps` k-steps of R weight rows and npad activation
+// rows, with their scale chunks, packed as [A][B][SFA][SFB] and sized to what
+// it holds, so that a small token tile leaves the ring to weight bytes.  For
+// a partial row tile (R = 64) the MMA still reads 128 rows of the last k-step
+// block, up to 2 KB past A; that lands inside the stage or in the ring's slack.
 struct Stage {
     uint32_t abytes, bbytes, sfbytes, size;
     __device__ Stage(int steps, int R, int npad)
@@ -305,11 +301,11 @@ struct Stage {
         abytes = steps * R * 32;
         bbytes = steps * npad * 32;
         sfbytes = chunks * kSfChunk;
-        size = ((DUAL ? 2 : 1) * (abytes + sfbytes) + bbytes + sfbytes + 127) & ~127u;
+        size = (abytes + sfbytes + bbytes + sfbytes + 127) & ~127u;
     }
-    __device__ uint32_t b() const { return (DUAL ? 2 : 1) * abytes; }
+    __device__ uint32_t b() const { return abytes; }
     __device__ uint32_t sfa0() const { return b() + bbytes; }
-    __device__ uint32_t sfb() const { return sfa0() + (DUAL ? 2 : 1) * sfbytes; }
+    __device__ uint32_t sfb() const { return sfa0() + sfbytes; }
 };
 
 // FIFO placement of stages in the ring; a stage never straddles the end.
@@ -336,11 +332,16 @@ struct Ring {
 // bulk copies; warp 1 owns tensor memory and issues the MMAs from one thread;
 // warps 2..5 (one per lane quarter) drain the accumulators, which are
 // double-buffered so the next item's MMAs overlap this item's epilogue.
+// DUAL (gate_up): a 128-row tile is 64 gate rows over 64 up rows of the same
+// rows of h, so SwiGLU pairs lane quarters 0, 1 with 2, 3 through shared memory.
 template <bool DUAL>
 __global__ void __launch_bounds__(192, 1) gemm_kernel(GemmParams p)
 {
-    using C = GemmCfg<DUAL>;
+    using C = GemmCfg;
     extern __shared__ __align__(1024) uint8_t smem[];
+    // DUAL: per 16-token chunk (double-buffered), gate warps hand over tokens 8..15
+    // of their gate sums and up warps tokens 0..7 of their up sums: [buf][gate | up][warp][lane][8]
+    __shared__ float xbuf[DUAL ? 2 * 2 * 2 * 32 * 8 : 1];
     __shared__ __align__(8) uint64_t full[kStageSlots], empty[kStageSlots], accf[2], acce[2];
     __shared__ uint32_t tmem_base;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -366,8 +367,9 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(GemmParams p)
     tc_fence_after();
     const uint32_t tmem = tmem_base;
 
-    const int T = ceil_div(p.rows, kRowTile);
+    const int T = DUAL ? p.rows / 64 : ceil_div(p.rows, kRowTile);
     const int KS = p.K / 64, NSTG = ceil_div(KS, kStageSteps), CH = ceil_div(p.K, 128);
+    const int prow = DUAL ? 2 * p.rows : p.rows;   // rows of the stored projection
     const int items = *p.ntiles * T;
 
     if (warp == 0) {
@@ -385,15 +387,15 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(GemmParams p)
             // so its latency never stalls the copy stream
             const int wn = w + gridDim.x;
             const TokTile next = wn < items ? p.tiles[wn / T] : tile;
-            const int R = p.rows - t * kRowTile < kRowTile ? p.rows - t * kRowTile : kRowTile;
+            const int R = prow - t * kRowTile < kRowTile ? prow - t * kRowTile : kRowTile;
             const uint8_t* a0 = p.w + tile.e * p.w_expert + (long long)t * kRowTile * (p.K / 2);
-            const uint8_t* s0 = p.w + tile.e * p.w_expert + (long long)p.rows * (p.K / 2) +
+            const uint8_t* s0 = p.w + tile.e * p.w_expert + (long long)prow * (p.K / 2) +
                                 (long long)t * CH * kSfChunk;
             const uint8_t* b0 = p.bq + tile.boff * KS;
             const uint8_t* sb0 = p.bsf + (long long)tt * CH * kSfChunk;
             for (int j = 0; j < NSTG; ++j, ++c) {
                 const int steps = KS - j * kStageSteps < kStageSteps ? KS - j * kStageSteps : kStageSteps;
-                const Stage<DUAL> sg(steps, R, tile.npad);
+                const Stage sg(steps, R, tile.npad);
                 unsigned long long end;
                 const uint32_t off = ring.place(sg.size, &end);
                 // wait until the bytes and the slot are free (stages retire in order)
@@ -406,8 +408,7 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(GemmParams p)
                 const uint32_t slot = c % kStageSlots;
                 ends[slot] = end;
                 if (lane == 0)
-                    mbar_expect_tx(&full[slot],
-                                   (DUAL ? 2 : 1) * (sg.abytes + sg.sfbytes) + sg.bbytes + sg.sfbytes);
+                    mbar_expect_tx(&full[slot], sg.abytes + sg.sfbytes + sg.bbytes + sg.sfbytes);
                 __syncwarp();
                 const long long aoff = (long long)j * kStageSteps * R * 32;
                 const long long soff = (long long)j * (kStageSteps / 2) * kSfChunk;
@@ -420,8 +421,6 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(GemmParams p)
                 case 1: dst = st + sg.sfa0(); src = s0 + soff; n = sg.sfbytes; break;
                 case 2: dst = st + sg.b(); src = b0 + (long long)j * kStageSteps * tile.npad * 32; n = sg.bbytes; break;
                 case 3: dst = st + sg.sfb(); src = sb0 + soff; n = sg.sfbytes; break;
-                case 4: if (DUAL) { dst = st + sg.abytes; src = a0 + p.proj2 + aoff; n = sg.abytes; } break;
-                case 5: if (DUAL) { dst = st + sg.sfa0() + sg.sfbytes; src = s0 + p.proj2 + soff; n = sg.sfbytes; } break;
                 default: break;
                 }
                 if (n)
@@ -436,7 +435,7 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(GemmParams p)
             for (int w = blockIdx.x; w < items; w += gridDim.x, ++it) {
                 const int t = w % T;
                 const TokTile tile = p.tiles[w / T];
-                const int R = p.rows - t * kRowTile < kRowTile ? p.rows - t * kRowTile : kRowTile;
+                const int R = prow - t * kRowTile < kRowTile ? prow - t * kRowTile : kRowTile;
                 const uint32_t buf = it & 1;
                 if (it >= 2)
                     mbar_wait(&acce[buf], ((it >> 1) - 1) & 1, p.status);
@@ -446,21 +445,19 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(GemmParams p)
                                        (1u << 23) | ((uint32_t)(kRowTile >> 4) << 24);
                 for (int j = 0; j < NSTG; ++j, ++c) {
                     const int steps = KS - j * kStageSteps < kStageSteps ? KS - j * kStageSteps : kStageSteps;
-                    const Stage<DUAL> sg(steps, R, tile.npad);
+                    const Stage sg(steps, R, tile.npad);
                     unsigned long long end;
                     const uint32_t st = su32(smem) + ring.place(sg.size, &end);
                     const uint32_t slot = c % kStageSlots;
                     mbar_wait(&full[slot], (c / kStageSlots) & 1, p.status);
                     tc_fence_after();
                     const int chunks = (steps + 1) >> 1;
-                    const uint32_t sA0 = st, sA1 = st + sg.abytes, sB = st + sg.b();
+                    const uint32_t sA0 = st, sB = st + sg.b();
                     const uint32_t sf = tmem + kSfCol + (c & 1) * C::kSfSet;
                     constexpr uint32_t kOp = 4 * (kStageSteps / 2);   // columns per operand's scales
-                    const uint32_t sfa0 = sf, sfa1 = sf + kOp, sfb = sf + (DUAL ? 2 : 1) * kOp;
+                    const uint32_t sfa0 = sf, sfb = sf + kOp;
                     for (int ch = 0; ch < chunks; ++ch) {
                         tc_cp_sf(sfa0 + 4 * ch, st + sg.sfa0() + ch * kSfChunk);
-                        if (DUAL)
-                            tc_cp_sf(sfa1 + 4 * ch, st + sg.sfa0() + sg.sfbytes + ch * kSfChunk);
                         tc_cp_sf(sfb + 4 * ch, st + sg.sfb() + ch * kSfChunk);
                     }
                     for (int i = 0; i < steps; ++i) {
@@ -470,9 +467,6 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(GemmParams p)
                         const uint32_t acc = (j | i) != 0;
                         tc_mma_mxf4(d0, smem_desc(sA0 + i * R * 32, 128, 256), bd, desc,
                                     sfa0 + 4 * (i >> 1), sfb + 4 * (i >> 1), acc);
-                        if (DUAL)
-                            tc_mma_mxf4(d0 + kTokTile, smem_desc(sA1 + i * R * 32, 128, 256), bd, desc,
-                                        sfa1 + 4 * (i >> 1), sfb + 4 * (i >> 1), acc);
                     }
                     tc_commit(&empty[slot]);
                 }
@@ -481,45 +475,47 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(GemmParams p)
         }
     } else {
         const int q = warp & 3;   // lane quarter this warp may access
-        uint32_t it = 0;
+        uint32_t it = 0, xb = 0;
         for (int w = blockIdx.x; w < items; w += gridDim.x, ++it) {
             const int tt = w / T, t = w % T;
             const TokTile tile = p.tiles[tt];
             const uint32_t buf = it & 1;
             mbar_wait(&accf[buf], (it >> 1) & 1, p.status);
             tc_fence_after();
-            const int row = t * kRowTile + 32 * q + lane;
-            // rows come in multiples of 64, so a warp's 32 rows are all valid or all not
-            const bool valid = t * kRowTile + 32 * q < p.rows;
-            float b0 = 0.0f, b1 = 0.0f;
-            if (p.bias && valid) {
-                const uint16_t* bb = p.bias + (size_t)tile.e * p.bias_stride;
-                b0 = bf16f(bb[row]);
-                if (DUAL)
-                    b1 = bf16f(bb[p.rows + row]);
-            }
             const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * C::kAccCols;
-            for (int c0 = 0; c0 < tile.n; c0 += 16) {
-                float g[16], u[16];
-                tc_ld16(taddr + c0, g);
-                if (DUAL)
-                    tc_ld16(taddr + kTokTile + c0, u);
-                tc_wait_ld();
-                if (!valid)
-                    continue;
-                const int nn = tile.n - c0 < 16 ? tile.n - c0 : 16;
-                if (DUAL) {
-                    // h = silu(gate) * up, then MX-quantised along I: the warp's 32
-                    // rows are one 32-element block of token n's h
-                    const int kb = row >> 5;
-                    uint8_t* hq = p.hq + tile.boff * (p.rows / 64) + 4 * (lane >> 3);
-                    uint8_t* hs = p.hsf + (size_t)tt * ceil_div(p.rows, 128) * kSfChunk;
+            if (DUAL) {
+                // h row of this lane: gate rows (q = 0, 1) and up rows (q = 2, 3) of the
+                // same 64 rows of h; each warp's 32 rows are one 32-element block of h
+                const int hrow = 64 * t + 32 * (q & 1) + lane, kb = hrow >> 5;
+                const bool gate = q < 2;
+                float bg = 0.0f, bu = 0.0f;
+                if (p.bias) {
+                    const uint16_t* bb = p.bias + (size_t)tile.e * p.bias_stride;
+                    bg = bf16f(bb[hrow]);
+                    bu = bf16f(bb[p.rows + hrow]);
+                }
+                uint8_t* hq = p.hq + tile.boff * (p.rows / 64) + 4 * (lane >> 3);
+                uint8_t* hs = p.hsf + (size_t)tt * ceil_div(p.rows, 128) * kSfChunk;
+                for (int c0 = 0; c0 < tile.n; c0 += 16, xb ^= 1u) {
+                    float v16[16];
+                    tc_ld16(taddr + c0, v16);
+                    tc_wait_ld();
+                    // hand over the other half of the chunk: gate warps keep tokens 0..7,
+                    // up warps 8..15
+                    float* mine = xbuf + (((xb * 2 + (gate ? 0 : 1)) * 2 + (q & 1)) * 32 + lane) * 8;
+                    const float* theirs = xbuf + (((xb * 2 + (gate ? 1 : 0)) * 2 + (q & 1)) * 32 + lane) * 8;
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        if (jj >= nn)
+                    for (int jj = 0; jj < 8; ++jj)
+                        mine[jj] = v16[gate ? 8 + jj : jj];
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    const int cb = c0 + (gate ? 0 : 8);
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        if (cb + jj >= tile.n)
                             break;
-                        const float gg = g[jj] + b0;
-                        const float v = gg / (1.0f + expf(-gg)) * (u[jj] + b1);
+                        const float gg = (gate ? v16[jj] : theirs[jj]) + bg;
+                        const float uu = (gate ? theirs[jj] : v16[8 + jj]) + bu;
+                        const float v = gg / (1.0f + expf(-gg)) * uu;
                         const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
                         const int ef = (int)(amax >> 23);
                         const uint32_t sbyte = ef > 2 ? (uint32_t)(ef - 2) : 0u;
@@ -529,13 +525,25 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(GemmParams p)
                         word |= __shfl_xor_sync(0xffffffffu, word, 1);
                         word |= __shfl_xor_sync(0xffffffffu, word, 2);
                         word |= __shfl_xor_sync(0xffffffffu, word, 4);
-                        const int n = c0 + jj;
+                        const int n = cb + jj;
                         if ((lane & 7) == 0)
                             *reinterpret_cast<uint32_t*>(hq + act_code_off(tile.npad, n, kb)) = word;
                         if (lane == 0)
                             hs[act_sf_off(n, kb)] = (uint8_t)sbyte;
                     }
-                } else {
+                }
+            } else {
+                const int row = t * kRowTile + 32 * q + lane;
+                // rows come in multiples of 64, so a warp's 32 rows are all valid or all not
+                const bool valid = t * kRowTile + 32 * q < p.rows;
+                const float b0 = p.bias && valid ? bf16f(p.bias[(size_t)tile.e * p.bias_stride + row]) : 0.0f;
+                for (int c0 = 0; c0 < tile.n; c0 += 16) {
+                    float g[16];
+                    tc_ld16(taddr + c0, g);
+                    tc_wait_ld();
+                    if (!valid)
+                        continue;
+                    const int nn = tile.n - c0 < 16 ? tile.n - c0 : 16;
                     float* out = p.out + (size_t)(tile.p0 + c0) * p.rows + row;
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj)
@@ -594,11 +602,20 @@ __global__ void combine_kernel(BatchParams p)
 
 // --------------------------------------------------------------- repacking
 
-// Caller layout -> tile layout, one projection (rows row0 .. row0+N-1 of each
-// expert's [src_rows][K/2] code matrix).  Work item g < E*N*K/32 moves one
-// 16-byte run of codes; g beyond that writes one scale byte.
+// Caller row of tile-layout row n: n itself, or the interleaved gate_up order.
+__device__ __forceinline__ int src_row(int n, int ilv)
+{
+    if (!ilv)
+        return n;
+    const int t = n / kRowTile, r = n % kRowTile;
+    return r < 64 ? 64 * t + r : ilv + 64 * t + r - 64;
+}
+
+// Caller layout -> tile layout, one projection (N rows of each expert's
+// [src_rows][K/2] code matrix).  Work item g < E*N*K/32 moves one 16-byte run
+// of codes; g beyond that writes one scale byte.
 __global__ void repack_tiles_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
-                                    int E, int src_rows, int row0, int N, int K, uint8_t* out,
+                                    int E, int src_rows, int N, int K, int ilv, uint8_t* out,
                                     long long expert_bytes)
 {
     const int c16 = K / 32;                       // 16-byte runs per row
@@ -614,7 +631,7 @@ __global__ void repack_tiles_kernel(const uint8_t* __restrict__ codes, const uin
             const int t = n / kRowTile, r = n % kRowTile;
             const int R = N - t * kRowTile < kRowTile ? N - t * kRowTile : kRowTile;
             const uint4 v = *reinterpret_cast<const uint4*>(
-                codes + ((size_t)e * src_rows + row0 + n) * (K / 2) + 16 * c);
+                codes + ((size_t)e * src_rows + src_row(n, ilv)) * (K / 2) + 16 * c);
             const long long dst = (long long)e * expert_bytes + (long long)t * kRowTile * (K / 2) +
                                   (long long)(c >> 1) * R * 32 + (r >> 3) * 256 + (c & 1) * 128 + (r & 7) * 16;
             *reinterpret_cast<uint4*>(out + dst) = v;
@@ -628,7 +645,7 @@ __global__ void repack_tiles_kernel(const uint8_t* __restrict__ codes, const uin
             const int n = t * kRowTile + 32 * j + i, blk = 4 * ch + kb;
             uint8_t v = 0;
             if (n < N && blk < K / 32)
-                v = scales[((size_t)e * src_rows + row0 + n) * (K / 32) + blk];
+                v = scales[((size_t)e * src_rows + src_row(n, ilv)) * (K / 32) + blk];
             out[(long long)e * expert_bytes + (long long)N * (K / 2) + rem] = v;
         }
     }
@@ -637,7 +654,7 @@ __global__ void repack_tiles_kernel(const uint8_t* __restrict__ codes, const uin
 template <bool DUAL>
 cudaError_t launch_gemm(const GemmParams& g, int grid, cudaStream_t s)
 {
-    gemm_kernel<DUAL><<<grid, 192, GemmCfg<DUAL>::kSmem, s>>>(g);
+    gemm_kernel<DUAL><<<grid, 192, GemmCfg::kSmem, s>>>(g);
     return cudaGetLastError();
 }
 
@@ -651,11 +668,11 @@ unsigned blocks_for(long long n, int threads)
 cudaError_t prepare_batched_kernels()
 {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         GemmCfg<true>::kSmem);
+                                         GemmCfg::kSmem);
     if (e != cudaSuccess)
         return e;
     return cudaFuncSetAttribute(gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                GemmCfg<false>::kSmem);
+                                GemmCfg::kSmem);
 }
 
 cudaError_t launch_batched(const BatchParams& p, int grid, cudaStream_t s, int* launches)
@@ -671,7 +688,6 @@ cudaError_t launch_batched(const BatchParams& p, int grid, cudaStream_t s, int* 
     GemmParams g{};
     g.w = p.gu;
     g.w_expert = p.gu_expert;
-    g.proj2 = tile_proj_bytes(p.I, p.H);
     g.rows = p.I;
     g.K = p.H;
     g.bq = p.xq;
@@ -687,7 +703,6 @@ cudaError_t launch_batched(const BatchParams& p, int grid, cudaStream_t s, int* 
         return e;
     g.w = p.dn;
     g.w_expert = p.dn_expert;
-    g.proj2 = 0;
     g.rows = p.H;
     g.K = p.I;
     g.bq = p.hq;
@@ -703,13 +718,13 @@ cudaError_t launch_batched(const BatchParams& p, int grid, cudaStream_t s, int* 
 }
 
 cudaError_t launch_repack_tiles(const uint8_t* codes, const uint8_t* scales, int E, int src_rows,
-                                int row0, int N, int K, uint8_t* out, long long expert_bytes,
+                                int N, int K, int interleave, uint8_t* out, long long expert_bytes,
                                 cudaStream_t stream)
 {
     const long long work = (long long)E * N * (K / 32) +
                            (long long)E * ceil_div(N, kRowTile) * ceil_div(K, 128) * kSfChunk;
     const long long blocks = (work + 255) / 256 < 65536 ? (work + 255) / 256 : 65536;
-    repack_tiles_kernel<<<(unsigned)blocks, 256, 0, stream>>>(codes, scales, E, src_rows, row0, N, K, out,
+    repack_tiles_kernel<<<(unsigned)blocks, 256, 0, stream>>>(codes, scales, E, src_rows, N, K, interleave, out,
                                                               expert_bytes);
     return cudaGetLastError();
 }

@@ -1,5 +1,5 @@
 // moe_decode_tc.cu -- the MXFP4 decode layer (M <= 4 tokens) on the
-// 5th-generation tensor cores: one persistent launch, one CTA per SM.
+// 5th-generation tensor cores: one persistent launch per layer, one CTA per SM.
 //
 // The layer is the one of "Sovereign gpt-oss-20B (MXFP4) on Apple Silicon",
 // section 3 (top-k routing, per selected expert an MXFP4 gate_up GEMV,
@@ -8,31 +8,37 @@
 // reads E2M1 codes and E8M0 scales from shared / tensor memory, so no
 // instruction per weight runs on the CUDA cores.  That instruction wants FP4
 // on the activation side too; an activation vector v (x, or h) is therefore
-// fed as a sum of T MXFP4 vectors, v ~ v_1 + ... + v_T with
-// v_j = MX(v - v_1 - ... - v_{j-1}) (OCP MX v1.0 quantiser), each term one
-// column of the MMA's N (token m, term j at column 8m + j; N = 16 for M <= 2,
-// else 32).  Each term cuts the residual of a 32-element block by a factor
-// of at least 4, so T = 8 terms leave a relative error near 1e-6, like fp32
-// activations; a bf16 x is usually exact after fewer terms, and a block
-// whose residual is zero gets zero terms without further arithmetic.  The
-// MMA applies every term's scales, and the epilogue adds a token's columns.
+// fed as a sum of T MXFP4 vectors, v ~ v_1 + ... + v_T, each term one column
+// of the MMA's N (token m, term j at column 8m + j; N = 16 for M <= 2, else
+// 32).  Term j of a 32-element block has the shared exponent X0 - 2j (X0 the
+// OCP MX v1.0 exponent of the block) and the nearest-even E2M1 codes of the
+// residual the earlier terms left; every term cuts the residual by at least
+// 4, so T = 8 terms leave a relative error near 1e-5 of the block maximum.
+// The MMA applies every term's scales, and the epilogue adds a token's columns.
 //
-// Work: gate_up units (selected expert s, 128-row tile t of gate and of up, a
-// K range of H) and down units (s, 128-row tile of down, a K range of I),
-// dealt round-robin over the CTAs; the K split gives every SM work when only
-// 4 experts are selected.  A unit's fp32 partial sums go to global memory;
-// the last unit of a tile to finish (an atomic counter) adds them in a fixed
-// order, so results do not depend on timing.  h of an expert's 128 rows is
-// published with a release flag; a down unit waits only for the h rows its
-// K range covers, while its weights are already streaming into the ring.
-// The last down tile of a 128-row slice of the output to finish, across all
-// experts, writes out = bf16(r + sum_s w_s y_s) in each token's choice order.
+// Work unit: 64 rows of h of one selected expert.  Its gate/up weights are one
+// 128-row tile (64 gate rows over 64 up rows, the interleaved tile layout), so
+// one CTA computes SwiGLU for those rows with nothing exchanged; it folds in
+// each token's routing weight, h'_m = w_m h_m, and runs the down projection's
+// 64 matching K columns for every output row.  CTA b takes the units
+// [b U / G, (b+1) U / G), so no activation ever crosses CTAs: each CTA adds
+// its down products into its own fp32 copy of the output, and after one grid
+// barrier CTA b sums the CTAs' copies for its slice of the output rows in CTA
+// order (results do not depend on timing) and writes
+// out = bf16(r + sum + sum_s w_s b_s).
 //
-// Warp roles (192 threads): warp 0 streams weight tiles into a byte ring of
-// shared memory (each stage's copies issued from separate lanes in one
-// instruction); warp 1 owns tensor memory and issues the MMAs from one
-// thread; warps 2..5 (one per lane quarter) build the activation terms, drain
-// the accumulators and run the cross-CTA reductions.
+// The x terms are built inside the layer: the (token, 32-element block) items
+// are dealt over the CTAs, written to global memory and counted; gate/up
+// stages carry them once the count is complete.  Weight copies never wait.
+//
+// The launch signals its dependents at entry, so the next layer's CTAs take
+// over each SM as soon as this layer's CTA there exits and set up before they
+// wait for this grid to complete.
+//
+// Warp roles (192 threads): warp 0 streams weights into a byte ring of shared
+// memory (each stage's copies issued from separate lanes in one instruction);
+// warp 1 owns tensor memory and issues the MMAs; warps 2..5 (one per lane
+// quarter) build the x terms and drain the accumulators.  Warps 0 and 1 route.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -47,112 +53,74 @@ namespace {
 
 using namespace tc;
 
-constexpr int kRows = 32;          // activation rows: token m, term j at m * kTerms + j
-constexpr int kTerms = 8;          // MX terms per activation vector
-constexpr int kAtom = kRows * 32;  // bytes of one k-step of activation terms
-constexpr int kSteps = 8;          // k-steps (64 of K) per pipeline stage (the producer's issue cost is per stage)
-constexpr int kSlots = 16;         // stages in flight at most
-constexpr int kAcc = 2 * kRows;    // accumulator columns of one buffer: gate | up (down: issuer A | B)
-constexpr int kSfSetCol = 2 * kAcc;   // per-issuer stage scale sets: 2 issuers x 2 sets
-constexpr int kSfSetCols = 32;        // one set: A scales (4 chunks) | B scales (4 chunks)
-static_assert(kSfSetCols / 2 >= 4 * ((kSteps + 1) / 2), "scale set holds a stage's chunks");
-constexpr int kMmaWarpB = 6;
+constexpr int kTerms = 8;            // MX terms per activation vector
+constexpr int kGuSteps = 8;          // k-steps (64 of K) per gate/up stage
+constexpr int kDnStageTiles = 5;     // 128-row down tiles per down stage
+constexpr int kSlots = 16;           // stages in flight at most
+// tensor memory columns
+constexpr int kGuCol = 0;            // gate/up accumulators: 2 buffers x 32
+constexpr int kDnCol = 64;           // down accumulators: 2 regions x 160
+constexpr int kDnRegion = 160;
+constexpr int kSfCol = 384;          // stage scale sets: 2 issuers x 2 sets x 32
+constexpr int kSfSet = 32;
 constexpr int kTmemCols = 512;
-static_assert(kSfSetCol + 4 * kSfSetCols <= kTmemCols, "tensor memory");
-constexpr int kRingSlack = 4096;   // read slack past the ring (partial row tiles)
-constexpr int kThreadsTc = 224;    // producer, MMA issuer A, 4 epilogue warps, MMA issuer B
-constexpr int kEpi = 128;          // epilogue threads (warps 2..5)
-constexpr int kPend = 16;          // queued h-term copies of the producer
+static_assert(kDnCol + 2 * kDnRegion <= kSfCol && kSfCol + 4 * kSfSet <= kTmemCols, "tensor memory");
+static_assert(kDnRegion % (kDnStageTiles * 32) == 0, "a region holds whole down stages");
+static_assert(kSfSet >= 8 * ((kGuSteps + 1) / 2), "a gate/up stage's A and B scale chunks fit a set");
+static_assert(kSfSet >= 4 * (kDnStageTiles + 1), "a down stage's scale chunks fit a set");
+constexpr int kThreadsTc = 224;      // producer, MMA issuer A, 4 epilogue warps, MMA issuer B
+constexpr int kMmaWarpB = 6;
+constexpr int kEpi = 128;            // epilogue threads (warps 2..5)
+constexpr int kPend = 16;            // gate/up stages waiting for the x terms
+constexpr int kTileA = kRowTile * 32;            // one k-step of a 128-row tile: 4 KB
+constexpr int kHTerm = 1024 + kSfChunk;          // h' terms of a unit: one k-step atom + its scale chunk
 
-// MMA N: the rows that hold terms, rounded up to 16.
+// MMA N: the rows that hold terms, rounded up to 16; a k-step of terms is
+// N rows x 32 bytes (8-row groups 256 bytes apart).
 __device__ __forceinline__ int rows_for(int M) { return M * kTerms <= 16 ? 16 : 32; }
 
-struct Geometry {
-    int KSH, KSI, CHH, CHI, T1, T2;   // k-steps, 128-element chunks and 128-row tiles of H and I
-    int nu, KC1, KC2, U1, U2;
-};
-
-// Work units, dealt round-robin over the CTAs from one list: U1 gate/up
-// pieces (nu*T1 tile pairs in KC1 K pieces), then U2 down pieces (nu*T2
-// tiles in KC2 K pieces).  A CTA's down pieces stream into its ring behind
-// its pair, so most down weights are resident when h is ready.
-__device__ __forceinline__ Geometry geometry(const DecodeTcParams& p, int nu, int G)
+// Shared memory past the stage ring: two h'-term buffers, the up-sum exchange
+// (2 warps x 32 lanes x float4) and the CTA's fp32 output copy [H][M].
+__device__ __forceinline__ uint32_t tail_bytes(int H, int M)
 {
-    Geometry g;
-    g.KSH = p.H / 64;
-    g.KSI = p.I / 64;
-    g.CHH = ceil_div(p.H, 128);
-    g.CHI = ceil_div(p.I, 128);
-    g.T1 = ceil_div(p.I, kRowTile);
-    g.T2 = ceil_div(p.H, kRowTile);
-    g.nu = nu;
-    const int pairs = nu * g.T1, tiles = nu * g.T2;
-    // Gate/up pairs stay whole (a K split makes h wait for the slowest piece, and
-    // measured slower); down tiles split so that the list comes to about two
-    // units per CTA.
-    g.KC1 = 1;
-    const int left = 2 * G - pairs;
-    const int k2 = left > 0 ? (left + tiles / 2) / tiles : 1;
-    g.KC2 = k2 < 1 ? 1 : (k2 > g.CHI ? g.CHI : k2);
-    g.U1 = pairs * g.KC1;
-    g.U2 = tiles * g.KC2;
-    return g;
+    return 2 * kHTerm + 2 * 32 * 16 + (((uint32_t)H * M * 4 + 127) & ~127u);
 }
 
-__device__ __forceinline__ int units_of(const Geometry& g, int b, int G)
+// Items of a CTA with n units, in the order the producer, the MMA issuer and
+// the epilogue walk them: gate/up of unit 0, then (gate/up of unit i+1, down
+// of unit i) pairs, then the last down -- a unit's SwiGLU epilogue overlaps
+// the next unit's gate/up MMAs.
+__device__ __forceinline__ void item_at(int k, int n, bool& down, int& i)
 {
-    const int U = g.U1 + g.U2;
-    return U > b ? (U - b + G - 1) / G : 0;
+    if (k == 0) {
+        down = false;
+        i = 0;
+    } else if ((k & 1) && (k + 1) / 2 < n) {
+        down = false;
+        i = (k + 1) / 2;
+    } else {
+        down = true;
+        i = (k & 1) ? (k - 1) / 2 : k / 2 - 1;
+    }
 }
 
-struct Unit {
-    bool down;
-    int s, t;           // expert slot, row tile
-    int ks0, ks1;       // k-steps [ks0, ks1)
-    int R;              // rows of the tile (128, or the remainder)
-    int tile;           // pair s * T1 + t, or down tile s * T2 + t
-    int pc;             // K piece
-    int id;             // unit index within its kind: tile * KC + piece
-};
-
-// Unit i of CTA b: list entry b + G * i (a CTA's gate/up pieces precede its down pieces).
-__device__ __forceinline__ Unit unit_at(const Geometry& g, const DecodeTcParams& p, int i, int b, int G)
-{
-    Unit u;
-    const int x = b + G * i;
-    u.down = x >= g.U1;
-    u.id = u.down ? x - g.U1 : x;
-    const int KC = u.down ? g.KC2 : g.KC1, T = u.down ? g.T2 : g.T1;
-    const int CH = u.down ? g.CHI : g.CHH, KS = u.down ? g.KSI : g.KSH;
-    u.pc = u.id % KC;
-    u.tile = u.id / KC;
-    u.t = u.tile % T;
-    u.s = u.tile / T;
-    const int c0 = u.pc * CH / KC, c1 = (u.pc + 1) * CH / KC;
-    u.ks0 = 2 * c0;
-    u.ks1 = 2 * c1 < KS ? 2 * c1 : KS;
-    const int rows = u.down ? p.H : p.I;
-    u.R = rows - u.t * kRowTile < kRowTile ? rows - u.t * kRowTile : kRowTile;
-    return u;
-}
-
-// One stage: [A0][A1][SFA0][SFA1][B][SFB] -- A1 / SFA1 the up tile of a pair;
-// B / SFB the activation terms of the stage's k-steps (x, or h for down).
-// For a partial row tile (R = 64) the MMA still reads 128 rows of a k-step
-// block, up to 2 KB past A; that lands in the stage or in the ring's slack.
-struct StageTc {
-    uint32_t abytes, sfbytes, bbytes, size, sfa0, b, sfb;
-    __device__ StageTc(int steps, int R, bool dual)
+// Gate/up stage: [A: steps x 4 KB][SFA: chunks x 512][B: steps x atom][SFB: chunks x 512].
+struct GuStage {
+    uint32_t abytes, sfbytes, bbytes, sfa, b, sfb, size;
+    __device__ GuStage(int steps, int atom)
     {
-        abytes = steps * R * 32;
+        abytes = steps * kTileA;
         sfbytes = ((steps + 1) >> 1) * kSfChunk;
-        bbytes = steps * kAtom;
-        sfa0 = (dual ? 2 : 1) * abytes;
-        b = sfa0 + (dual ? 2 : 1) * sfbytes;
+        bbytes = steps * atom;
+        sfa = abytes;
+        b = sfa + sfbytes;
         sfb = b + bbytes;
         size = (sfb + sfbytes + 127) & ~127u;
     }
 };
+// Down stage of n tiles: [A: n x 4 KB][SFA: n x 512].  A partial tile (64 rows)
+// still has a 4 KB slot, so the MMA's 128-row read stays inside the stage.
+__device__ __forceinline__ uint32_t dn_stage_size(int n) { return (uint32_t)n * (kTileA + kSfChunk); }
 
 struct RingTc {
     unsigned long long head = 0;
@@ -172,78 +140,27 @@ struct RingTc {
 };
 
 __device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, %0;" ::"r"(kEpi) : "memory"); }
+__device__ __forceinline__ void route_barrier() { asm volatile("bar.sync 2, 96;" ::: "memory"); }
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p)
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p)
 {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
-__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v)
+__device__ __forceinline__ unsigned long long atom_add_release_u64(unsigned long long* p, unsigned long long v)
 {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+    unsigned long long old;
+    asm volatile("atom.add.release.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+    return old;
 }
-
-// One warp, up to 4 groups of four consecutive 32-element blocks.  In group
-// w (token m[w], first block kb0[w], nvalid[w] blocks in range), lanes
-// 8g .. 8g+7 hold block kb0[w] + g, lane 8g + i its elements 4i .. 4i+3 in
-// r[w].  Writes the kTerms MX terms of each block (term j to row 8m + j):
-// codes to the k-step atoms at `q`, E8M0 bytes to the scale chunks at `sf`.
-// Each term is the OCP MX quantisation of the residual the previous terms
-// left; a zero residual gives zero terms.  The groups' chains are independent
-// and interleaved (one warp per SM sub-partition has no other latency cover).
-template <int NG>
-__device__ __forceinline__ void warp_terms(float (&r)[NG][4], const int (&m)[NG], const int (&kb0)[NG],
-                                           const int (&nvalid)[NG], uint8_t* q, uint8_t* sf, int lane)
+// The counters only grow: every CTA adds 1 per call, so a call's count is
+// complete at the next multiple of G above what this CTA's own add saw.
+__device__ __forceinline__ unsigned long long count_target(unsigned long long old, int G)
 {
-    const int g = lane >> 3, sub = lane & 7;
-    for (int j = 0; j < kTerms; ++j) {
-        uint32_t a[NG];
-#pragma unroll
-        for (int w = 0; w < NG; ++w)
-            a[w] = max(max(__float_as_uint(fabsf(r[w][0])), __float_as_uint(fabsf(r[w][1]))),
-                       max(__float_as_uint(fabsf(r[w][2])), __float_as_uint(fabsf(r[w][3]))));
-#pragma unroll
-        for (int off = 1; off < 8; off <<= 1)
-#pragma unroll
-            for (int w = 0; w < NG; ++w)
-                a[w] = max(a[w], __shfl_xor_sync(0xffffffffu, a[w], off));
-        uint32_t half[NG], sb[NG], b0[NG], b1[NG];
-#pragma unroll
-        for (int w = 0; w < NG; ++w) {
-            const int ef = (int)(a[w] >> 23);
-            sb[w] = ef > 2 ? (uint32_t)(ef - 2) : 0u;
-            const float inv = __uint_as_float((254u - sb[w]) << 23);   // 2^(127 - sb)
-            b0[w] = e2m1x2(r[w][0] * inv, r[w][1] * inv);
-            b1[w] = e2m1x2(r[w][2] * inv, r[w][3] * inv);
-            if (a[w] == 0u)
-                b0[w] = b1[w] = 0u;
-            half[w] = b0[w] | (b1[w] << 8);
-        }
-#pragma unroll
-        for (int w = 0; w < NG; ++w) {
-            const uint32_t other = __shfl_xor_sync(0xffffffffu, half[w], 1);
-            const int row = m[w] * kTerms + j, kb = kb0[w] + g;
-            if (g < nvalid[w]) {
-                if ((sub & 1) == 0)
-                    *reinterpret_cast<uint32_t*>(q + (kb >> 1) * kAtom + (row >> 3) * 256 + (kb & 1) * 128 +
-                                                 (row & 7) * 16 + 4 * (sub >> 1)) = half[w] | (other << 16);
-                if (sub == 0)
-                    sf[(kb >> 2) * kSfChunk + row * 16 + (kb & 3)] = (uint8_t)sb[w];
-            }
-        }
-        if (j + 1 < kTerms)
-#pragma unroll
-            for (int w = 0; w < NG; ++w) {
-                const float scale = __uint_as_float(sb[w] == 0u ? 0x00400000u : (sb[w] << 23));   // 2^(sb - 127)
-                const float2 e0 = e2m1x2_to_f32(b0[w]), e1 = e2m1x2_to_f32(b1[w]);
-                r[w][0] -= e0.x * scale;
-                r[w][1] -= e0.y * scale;
-                r[w][2] -= e1.x * scale;
-                r[w][3] -= e1.y * scale;
-            }
-    }
+    return (old / (unsigned long long)G + 1ull) * (unsigned long long)G;
 }
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
 // Nearest-even E2M1 value of |x| (x already divided by the block scale, so
 // |x| < 8), saturating at 6, and its 3-bit magnitude code.  Plain fp32
@@ -263,16 +180,19 @@ __device__ __forceinline__ float e2m1_rne(float ax, uint32_t& code)
     return qv;
 }
 
-// One warp, one 32-element block kb per token (lane i holds element i of
-// token m's block in r[m], m < M): kTerms MX terms of each.  Term 0 takes the
-// OCP shared exponent X0 = floor(log2 amax) - 2; term j uses X0 - 2j.  A
-// term leaves an error of at most 2 * 2^Xj per element (half a step below 6,
-// or the saturation from < 8 to 6), i.e. at most 8 * 2^X(j+1), so no later
-// term exceeds the E2M1 range and every term cuts the error by at least 4:
-// the block maximum is reduced once instead of per term.  The tokens' chains
-// are interleaved; packing the codes into bytes and the stores come after.
-__device__ __forceinline__ void warp_terms_rows(float (&r)[kMaxTokens], int M, int kb, uint8_t* q, uint8_t* sf,
-                                                int lane)
+// One warp, one 32-element block kb of M tokens m0 .. m0+M-1 (lane i holds
+// element i of token m0+t's block in r[t]): kTerms MX terms of each, term j
+// of token m to row m * kTerms + j of the k-step atoms at `q` (atom bytes per
+// k-step), its E8M0 byte to the scale chunks at `sf`.  Term 0 takes the OCP
+// shared exponent X0 = floor(log2 amax) - 2; term j uses X0 - 2j.  A term
+// leaves an error of at most 2 * 2^Xj per element (half a step below 6, or
+// the saturation from < 8 to 6), i.e. at most 8 * 2^X(j+1), so no later term
+// exceeds the E2M1 range and every term cuts the error by at least 4: the
+// block maximum is reduced once instead of per term.  The tokens' chains are
+// interleaved; packing the codes into bytes and the stores come after.
+template <int M>
+__device__ __forceinline__ void warp_terms_rows(float (&r)[kMaxTokens], int m0, int kb, uint8_t* q, uint8_t* sf,
+                                                int atom, int lane)
 {
     uint32_t codes[kMaxTokens] = {0u, 0u, 0u, 0u};   // nibble j = term j's code of this lane's element
     uint32_t sblo[kMaxTokens] = {0u, 0u, 0u, 0u}, sbhi[kMaxTokens] = {0u, 0u, 0u, 0u};   // byte j%4 = scale
@@ -308,25 +228,18 @@ __device__ __forceinline__ void warp_terms_rows(float (&r)[kMaxTokens], int M, i
             }
         }
     }
-#pragma unroll 1
-    for (int m = 0; m < M; ++m) {
-        uint32_t cm = codes[0], lo = sblo[0], hi = sbhi[0];
 #pragma unroll
-        for (int t = 1; t < kMaxTokens; ++t)
-            if (m == t) {
-                cm = codes[t];
-                lo = sblo[t];
-                hi = sbhi[t];
-            }
+    for (int m = 0; m < M; ++m) {
+        const uint32_t cm = codes[m], lo = sblo[m], hi = sbhi[m];
 #pragma unroll
         for (int j = 0; j < kTerms; ++j) {
             uint32_t word = ((cm >> (4 * j)) & 0xfu) << (4 * (lane & 7));
             word |= __shfl_xor_sync(0xffffffffu, word, 1);
             word |= __shfl_xor_sync(0xffffffffu, word, 2);
             word |= __shfl_xor_sync(0xffffffffu, word, 4);
-            const int row = m * kTerms + j;
+            const int row = (m0 + m) * kTerms + j;
             if ((lane & 7) == 0)
-                *reinterpret_cast<uint32_t*>(q + (kb >> 1) * kAtom + (row >> 3) * 256 + (kb & 1) * 128 +
+                *reinterpret_cast<uint32_t*>(q + (kb >> 1) * atom + (row >> 3) * 256 + (kb & 1) * 128 +
                                              (row & 7) * 16 + 4 * (lane >> 3)) = word;
             if (lane == 0)
                 sf[(kb >> 2) * kSfChunk + row * 16 + (kb & 3)] = (uint8_t)((j < 4 ? lo : hi) >> (8 * (j & 3)));
@@ -334,15 +247,33 @@ __device__ __forceinline__ void warp_terms_rows(float (&r)[kMaxTokens], int M, i
     }
 }
 
-__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v)
+// 1 / sqrt(mean(v^2) + 1e-6) of a bf16 row of n elements (n % 8 == 0), the
+// same value on every lane of the warp.
+__device__ __forceinline__ float row_inv_rms(const uint16_t* row, int n, int lane)
 {
-    unsigned old;
-    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
+    float a = 0.f;
+    for (int i = lane; i < n / 8; i += 32) {
+        const uint4 w = __ldcg(reinterpret_cast<const uint4*>(row) + i);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int z = 0; z < 4; ++z) {
+            const float lo = __uint_as_float(ws[z] << 16), hi = __uint_as_float(ws[z] & 0xffff0000u);
+            a = fmaf(lo, lo, a);
+            a = fmaf(hi, hi, a);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+        a += __shfl_xor_sync(0xffffffffu, a, off);
+    return 1.0f / sqrtf(a / (float)n + 1e-6f);
 }
 
 struct TcSmem {
-    uint64_t full[kSlots], empty[kSlots], accf[2], acce[2], routed;
+    uint64_t full[kSlots], empty[kSlots];
+    uint64_t accf[2], acce[2];   // gate/up accumulator buffers: full / drained
+    uint64_t dnf[2], dne[2];     // down accumulator regions: full (both issuers) / drained
+    uint64_t hbar[2];            // h' terms of a unit written
+    uint64_t routed, xready;     // routing done; every CTA's x terms published
     uint32_t tmem_base;
     int sel[kMaxTokens][kMaxTopK];
     float wt[kMaxTokens][kMaxTopK];
@@ -350,30 +281,55 @@ struct TcSmem {
     int unit_expert[kMaxUnits];
     unsigned char unit_of[kMaxExperts];
     float wslot[kMaxUnits][kMaxTokens];   // routing weight of token m for expert slot s (0 if not chosen)
-    int flag;
 };
 
 __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTcParams p)
 {
     extern __shared__ __align__(1024) uint8_t ring[];
     __shared__ __align__(8) TcSmem sh;
+    // the next layer's CTAs may take each SM as soon as this CTA leaves it
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, b = blockIdx.x, M = p.M;
-    const int nrows = rows_for(M);
-    const uint32_t ring_cap = (uint32_t)(p.smem_bytes - kRingSlack) & ~127u;
-    const int KSI = p.I / 64, CHI = ceil_div(p.I, 128), KSH = p.H / 64;
-    const long long hstride = (long long)KSI * kAtom + (long long)CHI * kSfChunk;   // h terms of one slot
+    const int nrows = rows_for(M), atom = nrows * 32;
+    const int KSH = p.H / 64, CHH = ceil_div(p.H, 128), CHI = ceil_div(p.I, 128);
+    const int T1 = p.I / 64, T2 = ceil_div(p.H, kRowTile);   // units per expert, down row tiles
+    const int TG = kDnRegion / nrows;                           // down tiles per accumulator region
+    const int NG = ceil_div(T2, TG);                            // down groups per unit
+    const int nblk = p.H / 32, nitems = M * nblk;               // x-term items: (token, 32-element block)
+    const int V = M == 1 ? 1 : (M == 2 ? 2 : 4);                // floats per row of a CTA's output copy
+    const uint32_t tail_off = ((uint32_t)p.smem_bytes - tail_bytes(p.H, M)) & ~127u;
+    const uint32_t ring_cap = tail_off & ~127u;
+    uint8_t* hterm = ring + tail_off;                           // [2][kHTerm]
+    float4* xch = reinterpret_cast<float4*>(ring + tail_off + 2 * kHTerm);   // [2][32]
+    float* oacc = reinterpret_cast<float*>(ring + tail_off + 2 * kHTerm + 2 * 32 * 16);   // [H][M]
 
+    // warm L2 and the TLB for what the first steps read once the previous grid
+    // is complete (a prefetch returns no data, so it cannot see a stale value)
+    if (warp == 2 && lane < M)
+        prefetch_l2(p.logits + (size_t)lane * p.E);
+    if (warp >= 3 && warp <= 5 && b < nitems) {
+        const int it = b + G * (warp - 3);
+        if (it < nitems) {
+            const int m = it / nblk, kb = it - m * nblk;
+            if (lane == 0)
+                prefetch_l2((p.x ? p.x : p.resid) + (size_t)m * p.H + 32 * kb);
+        }
+    }
     if (tid == 0) {
         for (int i = 0; i < kSlots; ++i) {
             mbar_init(&sh.full[i], 1);
-            mbar_init(&sh.empty[i], 2);   // both issuers
+            mbar_init(&sh.empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sh.accf[i], 2);
+            mbar_init(&sh.accf[i], 1);
             mbar_init(&sh.acce[i], 4);
+            mbar_init(&sh.dnf[i], 2);
+            mbar_init(&sh.dne[i], 4);
+            mbar_init(&sh.hbar[i], 1);
         }
         mbar_init(&sh.routed, 1);
+        mbar_init(&sh.xready, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -385,13 +341,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
-    // The logits were written before the x-term kernel started, which had waited
-    // for them: routing may run before this kernel waits for its predecessor.
-    if (warp < 2) {
-        // ---- routing (warps 0, 1): top-k per token, then the distinct experts in ascending order
-        for (int m = warp; m < M; m += 2)
-            rt::warp_topk(p.logits + (size_t)m * p.E, p.E, p.k, sh.sel[m], sh.wt[m]);
-        asm volatile("bar.sync 2, 64;" ::: "memory");
+    // everything below reads what the previous grid in the stream wrote (the
+    // logits, x, the residual) or shares its workspace
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    if (warp < 2 || warp == kMmaWarpB) {
+        // ---- routing (warps 0, 1, 6): token m on the (m % 3)-th of them, then the
+        // distinct experts in ascending order
+#pragma unroll 1
+        for (int m = warp == kMmaWarpB ? 2 : warp; m < M; m += 3)
+            rt::warp_topk_fit(p.logits + (size_t)m * p.E, p.E, p.k, sh.sel[m], sh.wt[m]);
+        route_barrier();
         if (warp == 0) {
             uint32_t bits = 0;
             if (lane < kMaxExperts / 32)
@@ -425,505 +385,541 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                 const int m = x / p.k, k2 = x % p.k;
                 sh.wslot[sh.unit_of[sh.sel[m][k2]]][m] = sh.wt[m][k2];
             }
-            if (lane == 0) {
+            if (lane == 0)
                 sh.nu = nu;
-                asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        }
+        route_barrier();
+        if (warp == 1 && lane == 0)
+            mbar_arrive(&sh.routed);   // hands the routing to the epilogue warps
+    } else if (warp <= 5) {
+        // ---- x terms (warps 2..5): items b + G q + 4 G i, token-major (q = warp - 2)
+        const int q = warp - 2, te = tid - 64;
+        if (b < nitems) {
+            int cm = -1;
+            float inv = 1.f;
+            for (int it = b + G * q; it < nitems; it += 4 * G) {
+                const int m = it / nblk, kb = it - m * nblk;
+                float v;
+                if (p.x) {
+                    v = bf16f(__ldcg(p.x + (size_t)m * p.H + 32 * kb + lane));
+                } else {
+                    if (m != cm) {
+                        inv = row_inv_rms(p.resid + (size_t)m * p.H, p.H, lane);
+                        cm = m;
+                    }
+                    v = bf16f(f2bf16_rne(bf16f(__ldcg(p.resid + (size_t)m * p.H + 32 * kb + lane)) * inv));
+                }
+                float r4[kMaxTokens] = {v, 0.f, 0.f, 0.f};
+                warp_terms_rows<1>(r4, m, kb, p.xt, p.xt + (long long)KSH * atom, atom, lane);
             }
         }
-        asm volatile("bar.sync 2, 64;" ::: "memory");
-        if (warp == 1 && lane == 0)
-            mbar_arrive(&sh.routed);   // hands the routing to the other warps
-    } else {
+        epi_barrier();
+        if (te == 0) {
+            // publish this CTA's x terms (every CTA counts itself in), then wait for
+            // the whole count and hand it to the producer through an mbarrier, so the
+            // producer never waits on a load
+            const unsigned long long tgt = count_target(atom_add_release_u64(p.xcnt, 1ull), G);
+            int spins = 0;
+#pragma unroll 1
+            while (ld_acquire_u64(p.xcnt) < tgt) {
+                if (++spins > (1 << 24)) {
+                    atomicExch(p.status, MOE_ERR_DEVICE_TIMEOUT);
+                    break;
+                }
+            }
+            mbar_arrive(&sh.xready);
+        }
+        __syncwarp();   // lane 0 rejoins before the warp's collective instructions
+        for (int i = te; i < p.H * M; i += kEpi)
+            oacc[i] = 0.f;
+        // h'-term rows past M * 8 feed MMA columns nobody reads: give them zero
+        // codes and unit-range scales rather than whatever shared memory held
+        for (int i = te; i < 2 * kHTerm / 4; i += kEpi)
+            reinterpret_cast<uint32_t*>(hterm)[i] = 0u;
         mbar_wait(&sh.routed, 0, p.status);
     }
-    const Geometry g = geometry(p, sh.nu, G);
-    const int nunits = units_of(g, b, G);
+
+    const int nu = sh.nu;
+    const int U = nu * T1;
+    // (products below stay under 2^31: U <= kMaxUnits * kMaxK / 64, G and H small)
+    const int u0 = (int)((unsigned)b * U / G), nun = (int)((unsigned)(b + 1) * U / G) - u0;
+    const int nact = U < G ? U : G;   // CTAs with units
+    const int nitem = 2 * nun;
     if (b == 0 && tid == 0 && p.nu_out)
-        *p.nu_out = g.nu;
+        *p.nu_out = nu;
 
     if (warp == 0) {
         // ================================================================ producer
-        // Weight tiles stream in unit order; a pair's stage also carries the x
-        // terms of its k-steps.  A down stage's h terms can only be copied once
-        // the pairs that produce them have published their flag: such copies
-        // wait in a queue that is served whenever the producer would otherwise
-        // wait, so the weight stream never stalls on h.
-        asm volatile("griddepcontrol.wait;" ::: "memory");   // the x terms are written
+        // Weights stream in item order.  A gate/up stage also carries the x terms
+        // of its k-steps; until they are published those two copies wait in a
+        // queue, served whenever the producer polls, so weights never wait.
         RingTc ring_alloc;
         unsigned long long ends[kSlots];
         unsigned long long rel_end = 0;
         uint32_t c = 0, rel = 0;
-        // h-term copies of down stages placed before their pairs were ready, in
-        // placement order; every entry names its unit's slot and chunk range
-        // (all lanes hold the queue)
-        uint32_t pq_off[kPend], pq_slot[kPend];
-        int pq_ks[kPend], pq_steps[kPend], pq_s[kPend], pq_c0[kPend], pq_c1[kPend];
-        int pq_head = 0, pq_n = 0;
-        int ok_s = -1, ok_c0 = 0, ok_c1 = 0;   // the last chunk range found published
-        // the whole warp: are all pairs of chunks [c0, c1) of slot s published?
-        auto pairs_ready = [&](int s, int c0, int c1) -> bool {
-            if (s == ok_s && c0 == ok_c0 && c1 == ok_c1)
-                return true;
-            bool ok = true;
-            for (int ch = c0 + lane; ch < c1; ch += 32)
-                ok = ok && ld_acquire_u32(p.hready + s * g.T1 + ch) != 0u;
-            if (__all_sync(0xffffffffu, ok)) {
-                ok_s = s;
-                ok_c0 = c0;
-                ok_c1 = c1;
-                return true;
-            }
-            return false;
-        };
-        // the whole warp: issue the queued copies whose pairs are published, in order
-        auto serve = [&]() {
-            while (pq_n > 0) {
-                const int h0 = pq_head % kPend;
-                if (!pairs_ready(pq_s[h0], pq_c0[h0], pq_c1[h0]))
-                    return;
-                // the run of entries of the same unit, up to 16 (two copies each, one per lane)
-                int run = 1;
-                while (run < pq_n && run < 16) {
-                    const int hq_ = (pq_head + run) % kPend;
-                    if (pq_s[hq_] != pq_s[h0] || pq_c0[hq_] != pq_c0[h0] || pq_c1[hq_] != pq_c1[h0])
-                        break;
-                    ++run;
-                }
-                asm volatile("fence.proxy.async.global;" ::: "memory");   // published h terms -> bulk reads
-                const uint8_t* src = p.ht + (long long)pq_s[h0] * hstride;
-                const int q = lane >> 1;
-                if (q < run) {
-                    const int e = (pq_head + q) % kPend;
-                    const StageTc sg(pq_steps[e], kRowTile, false);   // B / SFB sizes do not depend on R
-                    if ((lane & 1) == 0)
-                        bulk_copy(ring + pq_off[e], src + (long long)pq_ks[e] * kAtom, sg.bbytes, &sh.full[pq_slot[e]]);
-                    else
-                        bulk_copy(ring + pq_off[e] + sg.bbytes, src + (long long)KSI * kAtom + (pq_ks[e] >> 1) * kSfChunk,
-                                  sg.sfbytes, &sh.full[pq_slot[e]]);
-                }
-                pq_head += run;
-                pq_n -= run;
-            }
-        };
-        for (int i = 0; i < nunits; ++i) {
-            const Unit u = unit_at(g, p, i, b, G);
-            const int e = sh.unit_expert[u.s];
-            const int K = u.down ? p.I : p.H, rows = u.down ? p.H : p.I;
-            const int CH = u.down ? g.CHI : g.CHH;
-            const uint8_t* proj = u.down ? p.dn + (long long)e * p.dn_expert : p.gu + (long long)e * p.gu_expert;
-            const uint8_t* a0 = proj + (long long)u.t * kRowTile * (K / 2);
-            const uint8_t* s0 = proj + (long long)rows * (K / 2) + (long long)u.t * CH * kSfChunk;
-            const long long up = tile_proj_bytes(p.I, p.H);
-            bool hready = false;   // down: the pairs of this unit's K range are published
-            const int uc0 = u.ks0 >> 1, uc1 = (u.ks1 + 1) >> 1;
-            if (u.down) {
-                serve();
-                hready = pq_n == 0 && pairs_ready(u.s, uc0, uc1);   // stages keep their order
-                if (hready)
-                    asm volatile("fence.proxy.async.global;" ::: "memory");
-            }
-            for (int ks = u.ks0; ks < u.ks1; ks += kSteps, ++c) {
-                const int steps = u.ks1 - ks < kSteps ? u.ks1 - ks : kSteps;
-                const StageTc sg(steps, u.R, !u.down);
-                unsigned long long end;
-                const uint32_t off = ring_alloc.place(sg.size, ring_cap, &end);
-                // wait until the bytes and the slot are free (stages retire in order)
-                int spins = 0;
-                while (rel < c && (end - rel_end > (unsigned long long)ring_cap || rel + kSlots <= c)) {
-                    const uint32_t sl = rel % kSlots;
-                    if (__shfl_sync(0xffffffffu, mbar_test_wait(&sh.empty[sl], (rel / kSlots) & 1) ? 1 : 0, 0)) {
-                        rel_end = ends[sl];
-                        ++rel;
-                    } else {
-                        serve();
-                        if (++spins > (1 << 22)) {
-                            if (lane == 0)
-                                atomicExch(p.status, MOE_ERR_DEVICE_TIMEOUT);
-                            break;
-                        }
-                    }
-                }
-                const uint32_t slot = c % kSlots;
-                ends[slot] = end;
-                if (lane == 0)
-                    mbar_expect_tx(&sh.full[slot], (u.down ? 1 : 2) * (sg.abytes + sg.sfbytes) + sg.bbytes + sg.sfbytes);
+        const uint64_t wpol = l2_evict_first();
+        uint32_t pq_off[kPend] = {}, pq_slot[kPend] = {};
+        int pq_ks[kPend] = {}, pq_steps[kPend] = {};
+        int pq_n = 0;
+        bool x_ok = false;
+        // the whole warp: once the x terms are all published (a non-blocking test),
+        // issue the queued copies
+        auto poll = [&]() {
+            if (!x_ok && __shfl_sync(0xffffffffu, mbar_test_wait(&sh.xready, 0) ? 1 : 0, 0)) {
                 __syncwarp();
-                uint8_t* st = ring + off;
-                const long long aoff = (long long)ks * u.R * 32, soff = (long long)(ks >> 1) * kSfChunk;
-                const uint8_t* hsrc = p.ht + (long long)u.s * hstride;
-                const uint8_t* src = nullptr;
-                uint32_t dsto = 0, n = 0;
-                switch (lane) {
-                case 0: dsto = 0; src = a0 + aoff; n = sg.abytes; break;
-                case 1: dsto = sg.sfa0; src = s0 + soff; n = sg.sfbytes; break;
-                case 2: if (!u.down) { dsto = sg.abytes; src = a0 + up + aoff; n = sg.abytes; } break;
-                case 3: if (!u.down) { dsto = sg.sfa0 + sg.sfbytes; src = s0 + up + soff; n = sg.sfbytes; } break;
-                case 4:
-                    dsto = sg.b;
-                    n = !u.down || hready ? sg.bbytes : 0u;
-                    src = u.down ? hsrc + (long long)ks * kAtom : p.xt + (long long)ks * kAtom;
-                    break;
-                case 5:
-                    dsto = sg.sfb;
-                    n = !u.down || hready ? sg.sfbytes : 0u;
-                    src = u.down ? hsrc + (long long)KSI * kAtom + soff : p.xt + (long long)KSH * kAtom + soff;
-                    break;
-                default: break;
+                asm volatile("fence.proxy.async.global;" ::: "memory");   // published x terms -> bulk reads
+                x_ok = true;
+            }
+            if (x_ok && pq_n > 0) {
+                const int qq = lane >> 1;
+                if (qq < pq_n) {
+                    const GuStage sg(pq_steps[qq], atom);
+                    if ((lane & 1) == 0)
+                        bulk_copy(ring + pq_off[qq], p.xt + (long long)pq_ks[qq] * atom, sg.bbytes,
+                                  &sh.full[pq_slot[qq]]);
+                    else
+                        bulk_copy(ring + pq_off[qq] + sg.bbytes,
+                                  p.xt + (long long)KSH * atom + (pq_ks[qq] >> 1) * kSfChunk, sg.sfbytes,
+                                  &sh.full[pq_slot[qq]]);
                 }
-                if (n)
-                    bulk_copy(st + dsto, src, n, &sh.full[slot]);
-                if (u.down && !hready) {
-                    if (pq_n == kPend) {   // full: wait for the head's pairs
-                        for (int w = 0; w < (1 << 22) && pq_n == kPend; ++w)
-                            serve();
-                        if (pq_n == kPend) {
-                            if (lane == 0)
-                                atomicExch(p.status, MOE_ERR_DEVICE_TIMEOUT);
-                            ++pq_head;   // give up on the oldest entry (its stage will time out)
-                            --pq_n;
+                pq_n = 0;
+            }
+        };
+        // the whole warp: claim ring bytes and a slot for a stage (stages retire in order)
+        auto claim = [&](uint32_t size, uint32_t& off) -> uint32_t {
+            unsigned long long end;
+            off = ring_alloc.place(size, ring_cap, &end);
+            int spins = 0;
+#pragma unroll 1
+            while (rel < c && (end - rel_end > (unsigned long long)ring_cap || rel + kSlots <= c)) {
+                const uint32_t sl = rel % kSlots;
+                if (__shfl_sync(0xffffffffu, mbar_test_wait(&sh.empty[sl], (rel / kSlots) & 1) ? 1 : 0, 0)) {
+                    rel_end = ends[sl];
+                    ++rel;
+                } else {
+                    poll();
+                    if (++spins > (1 << 22)) {
+                        if (lane == 0)
+                            atomicExch(p.status, MOE_ERR_DEVICE_TIMEOUT);
+                        break;
+                    }
+                }
+            }
+            const uint32_t slot = c % kSlots;
+            ends[slot] = end;
+            return slot;
+        };
+        for (int k = 0; k < nitem; ++k) {
+            bool down;
+            int i;
+            item_at(k, nun, down, i);
+            const int unit = u0 + i, s = unit / T1, t = unit % T1;
+            const int e = sh.unit_expert[s];
+            if (!down) {
+                const uint8_t* a0 = p.gu + (long long)e * p.gu_expert + (long long)t * kRowTile * (p.H / 2);
+                const uint8_t* s0 = p.gu + (long long)e * p.gu_expert + (long long)(2 * p.I) * (p.H / 2) +
+                                    (long long)t * CHH * kSfChunk;
+                for (int ks = 0; ks < KSH; ks += kGuSteps, ++c) {
+                    const int steps = KSH - ks < kGuSteps ? KSH - ks : kGuSteps;
+                    const GuStage sg(steps, atom);
+                    uint32_t off;
+                    const uint32_t slot = claim(sg.size, off);
+                    if (lane == 0)
+                        mbar_expect_tx(&sh.full[slot], sg.abytes + sg.sfbytes + sg.bbytes + sg.sfbytes);
+                    __syncwarp();
+                    uint8_t* st = ring + off;
+                    const uint8_t* src = nullptr;
+                    uint32_t dsto = 0, n = 0;
+                    switch (lane) {
+                    case 0: dsto = 0; src = a0 + (long long)ks * kTileA; n = sg.abytes; break;
+                    case 1: dsto = sg.sfa; src = s0 + (ks >> 1) * kSfChunk; n = sg.sfbytes; break;
+                    case 2: dsto = sg.b; src = p.xt + (long long)ks * atom; n = x_ok ? sg.bbytes : 0u; break;
+                    case 3:
+                        dsto = sg.sfb;
+                        src = p.xt + (long long)KSH * atom + (ks >> 1) * kSfChunk;
+                        n = x_ok ? sg.sfbytes : 0u;
+                        break;
+                    default: break;
+                    }
+                    if (n) {
+                        if (lane < 2)   // weights: read once per call
+                            bulk_copy_hint(st + dsto, src, n, &sh.full[slot], wpol);
+                        else
+                            bulk_copy(st + dsto, src, n, &sh.full[slot]);
+                    }
+                    if (!x_ok) {
+                        if (pq_n == kPend) {   // full: wait for the x terms
+#pragma unroll 1
+                            for (int w = 0; w < (1 << 22) && pq_n == kPend; ++w)
+                                poll();
+                            if (pq_n == kPend) {
+                                if (lane == 0)
+                                    atomicExch(p.status, MOE_ERR_DEVICE_TIMEOUT);
+                                pq_n = 0;   // give up (those stages will time out)
+                            }
+                        }
+                        pq_off[pq_n] = off + sg.b;
+                        pq_slot[pq_n] = slot;
+                        pq_ks[pq_n] = ks;
+                        pq_steps[pq_n] = steps;
+                        ++pq_n;
+                    }
+                    poll();
+                }
+            } else {
+                // down rows of all tiles, k-step t of K = I (h rows 64t .. 64t+63)
+                const uint8_t* d0 = p.dn + (long long)e * p.dn_expert;
+                const uint8_t* sd0 = d0 + (long long)p.H * (p.I / 2) + (long long)(t >> 1) * kSfChunk;
+                for (int g = 0; g < NG; ++g) {
+                    const int ta = g * TG, tb = ta + TG < T2 ? ta + TG : T2;
+                    for (int t2 = ta; t2 < tb; t2 += kDnStageTiles, ++c) {
+                        const int n = tb - t2 < kDnStageTiles ? tb - t2 : kDnStageTiles;
+                        uint32_t off;
+                        const uint32_t slot = claim(dn_stage_size(n), off);
+                        uint32_t bytes = 0;
+                        for (int j = 0; j < n; ++j) {
+                            const int R2 = p.H - (t2 + j) * kRowTile < kRowTile ? p.H - (t2 + j) * kRowTile : kRowTile;
+                            bytes += (uint32_t)R2 * 32 + kSfChunk;
+                        }
+                        if (lane == 0)
+                            mbar_expect_tx(&sh.full[slot], bytes);
+                        __syncwarp();
+                        uint8_t* st = ring + off;
+                        const int j = lane & 15;
+                        if (j < n) {
+                            const int tt = t2 + j;
+                            const int R2 = p.H - tt * kRowTile < kRowTile ? p.H - tt * kRowTile : kRowTile;
+                            if (lane < 16)
+                                bulk_copy_hint(st + j * kTileA,
+                                          d0 + (long long)tt * kRowTile * (p.I / 2) + (long long)t * R2 * 32,
+                                          (uint32_t)R2 * 32, &sh.full[slot], wpol);
+                            else
+                                bulk_copy_hint(st + n * kTileA + j * kSfChunk, sd0 + (long long)tt * CHI * kSfChunk,
+                                               kSfChunk, &sh.full[slot], wpol);
                         }
                     }
-                    const int e = (pq_head + pq_n) % kPend;
-                    pq_off[e] = off + sg.b;
-                    pq_slot[e] = slot;
-                    pq_ks[e] = ks;
-                    pq_steps[e] = steps;
-                    pq_s[e] = u.s;
-                    pq_c0[e] = uc0;
-                    pq_c1[e] = uc1;
-                    ++pq_n;
-                    serve();
-                    if (pq_n == 0)
-                        hready = true;   // the rest of this unit's stages carry their h terms directly
                 }
             }
         }
+#pragma unroll 1
         for (int w = 0; w < (1 << 22) && pq_n > 0; ++w)
-            serve();
+            poll();
         if (pq_n > 0 && lane == 0)
             atomicExch(p.status, MOE_ERR_DEVICE_TIMEOUT);
     } else if (warp == 1 || warp == kMmaWarpB) {
         // ================================================================ MMA issuers
-        // Issuing a tcgen05 instruction costs one thread ~60-80 cycles, so two
-        // threads share the work: A (warp 1) the gate MMAs, B (warp 6) the up
-        // MMAs of a pair; down units alternate their stages between A and B,
-        // each into its own half of the accumulator (the drain adds the halves).
-        // Each issuer copies its stage scales into its own tensor-memory columns.
+        // Issuing a tcgen05 instruction costs one thread ~60-80 cycles.  Issuer A
+        // (warp 1) takes the gate/up stages; the down stages, which all wait on
+        // the same h' and then run back to back, alternate between A and B
+        // (warp 6), each on its own tiles of the region and its own scale sets.
         const int role = warp == 1 ? 0 : 1;
         if (lane == 0) {
             RingTc ring_alloc;
             const uint32_t idesc = (1u << 7) | (1u << 10) | ((uint32_t)(nrows >> 3) << 17) | (1u << 23) |
                                    ((uint32_t)(kRowTile >> 4) << 24);
-            const uint32_t myset = tmem + kSfSetCol + role * 2 * kSfSetCols;
-            uint32_t c = 0, mine = 0;
-            for (int i = 0; i < nunits; ++i) {
-                const Unit u = unit_at(g, p, i, b, G);
-                const uint32_t buf = i & 1;
-                if (i >= 2)
-                    mbar_wait(&sh.acce[buf], ((i >> 1) - 1) & 1, p.status);
-                tc_fence_after();
-                const uint32_t dme = tmem + buf * kAcc + role * kRows;   // this issuer's accumulator half
-                bool first = true;
-                int jst = 0;
-                for (int ks = u.ks0; ks < u.ks1; ks += kSteps, ++c, ++jst) {
-                    const int steps = u.ks1 - ks < kSteps ? u.ks1 - ks : kSteps;
-                    const StageTc sg(steps, u.R, !u.down);
-                    unsigned long long end;
-                    const uint32_t st = su32(ring) + ring_alloc.place(sg.size, ring_cap, &end);
-                    const uint32_t slot = c % kSlots;
-                    mbar_wait(&sh.full[slot], (c / kSlots) & 1, p.status);
-                    if (u.down && (jst & 1) != role) {
-                        mbar_arrive(&sh.empty[slot]);   // the other issuer owns this down stage
+            const uint32_t myset = tmem + kSfCol + role * 2 * kSfSet;
+            uint32_t c = 0, kk = 0, mine = 0;
+            for (int k = 0; k < nitem; ++k) {
+                bool down;
+                int i;
+                item_at(k, nun, down, i);
+                const int t = (u0 + i) % T1;
+                if (!down) {
+                    if (role == 1) {   // issuer A's: only keep the ring placement in step
+                        for (int ks = 0; ks < KSH; ks += kGuSteps, ++c) {
+                            const int steps = KSH - ks < kGuSteps ? KSH - ks : kGuSteps;
+                            unsigned long long end;
+                            ring_alloc.place(GuStage(steps, atom).size, ring_cap, &end);
+                        }
                         continue;
                     }
+                    const uint32_t buf = i & 1;
+                    if (i >= 2)
+                        mbar_wait(&sh.acce[buf], ((i >> 1) - 1) & 1, p.status);
                     tc_fence_after();
-                    const uint32_t sa = st + (u.down || role == 0 ? 0u : sg.abytes);   // gate / up / down A
-                    const uint32_t sfa = st + sg.sfa0 + (u.down || role == 0 ? 0u : sg.sfbytes);
-                    const uint32_t set = myset + (mine & 1) * kSfSetCols;
-                    ++mine;
-                    const int chunks = (steps + 1) >> 1;
-                    for (int ch = 0; ch < chunks; ++ch) {
-                        tc_cp_sf(set + 4 * ch, sfa + ch * kSfChunk);
-                        tc_cp_sf(set + kSfSetCols / 2 + 4 * ch, st + sg.sfb + ch * kSfChunk);
+                    const uint32_t d = tmem + kGuCol + buf * 32;
+                    bool first = true;
+                    for (int ks = 0; ks < KSH; ks += kGuSteps, ++c) {
+                        const int steps = KSH - ks < kGuSteps ? KSH - ks : kGuSteps;
+                        const GuStage sg(steps, atom);
+                        unsigned long long end;
+                        const uint32_t st = su32(ring) + ring_alloc.place(sg.size, ring_cap, &end);
+                        const uint32_t slot = c % kSlots;
+                        mbar_wait(&sh.full[slot], (c / kSlots) & 1, p.status);
+                        tc_fence_after();
+                        const uint32_t set = myset + (mine++ & 1) * kSfSet;
+                        const int chunks = (steps + 1) >> 1;
+#pragma unroll 1
+                        for (int ch = 0; ch < chunks; ++ch) {
+                            tc_cp_sf(set + 4 * ch, st + sg.sfa + ch * kSfChunk);
+                            tc_cp_sf(set + kSfSet / 2 + 4 * ch, st + sg.sfb + ch * kSfChunk);
+                        }
+#pragma unroll 1
+                        for (int j = 0; j < steps; ++j) {
+                            const uint32_t id = (uint32_t)(2 * (j & 1));
+                            tc_mma_mxf4(d, smem_desc(st + j * kTileA, 128, 256), smem_desc(st + sg.b + j * atom, 128, 256),
+                                        idesc | (id << 4) | (id << 29), set + 4 * (j >> 1),
+                                        set + kSfSet / 2 + 4 * (j >> 1), first ? 0u : 1u);
+                            first = false;
+                        }
+                        tc_commit(&sh.empty[slot]);
                     }
-                    for (int j = 0; j < steps; ++j) {
-                        const uint32_t id = (uint32_t)(2 * (j & 1));
-                        const uint32_t desc = idesc | (id << 4) | (id << 29);
-                        tc_mma_mxf4(dme, smem_desc(sa + j * u.R * 32, 128, 256), smem_desc(st + sg.b + j * kAtom, 128, 256),
-                                    desc, set + 4 * (j >> 1), set + kSfSetCols / 2 + 4 * (j >> 1), first ? 0u : 1u);
-                        first = false;
+                    tc_commit(&sh.accf[buf]);
+                } else {
+                    const uint32_t hb = su32(hterm + (i & 1) * kHTerm);
+                    mbar_wait(&sh.hbar[i & 1], (i >> 1) & 1, p.status);
+                    tc_fence_after();
+                    const uint32_t aid = (uint32_t)(2 * (t & 1));   // A scale bytes of k-step t in its chunk
+                    int jst = 0;                                     // down stage of this unit
+                    for (int g = 0; g < NG; ++g, ++kk) {
+                        if (kk >= 2)
+                            mbar_wait(&sh.dne[kk & 1], ((kk >> 1) - 1) & 1, p.status);
+                        tc_fence_after();
+                        const uint32_t dreg = tmem + kDnCol + (kk & 1) * kDnRegion;
+                        const int ta = g * TG, tb = ta + TG < T2 ? ta + TG : T2;
+                        for (int t2 = ta; t2 < tb; t2 += kDnStageTiles, ++c, ++jst) {
+                            const int n = tb - t2 < kDnStageTiles ? tb - t2 : kDnStageTiles;
+                            unsigned long long end;
+                            const uint32_t st = su32(ring) + ring_alloc.place(dn_stage_size(n), ring_cap, &end);
+                            if ((jst & 1) != role)
+                                continue;   // the other issuer's stage
+                            const uint32_t slot = c % kSlots;
+                            mbar_wait(&sh.full[slot], (c / kSlots) & 1, p.status);
+                            tc_fence_after();
+                            const uint32_t set = myset + (mine++ & 1) * kSfSet;
+                            tc_cp_sf(set, hb + 1024);
+#pragma unroll 1
+                            for (int j = 0; j < n; ++j)
+                                tc_cp_sf(set + 4 + 4 * j, st + n * kTileA + j * kSfChunk);
+#pragma unroll 1
+                            for (int j = 0; j < n; ++j)
+                                tc_mma_mxf4(dreg + (t2 - ta + j) * nrows, smem_desc(st + j * kTileA, 128, 256),
+                                            smem_desc(hb, 128, 256), idesc | (aid << 29), set + 4 + 4 * j, set, 0u);
+                            tc_commit(&sh.empty[slot]);
+                        }
+                        tc_commit(&sh.dnf[kk & 1]);   // both issuers: the group's region is full
                     }
-                    tc_commit(&sh.empty[slot]);
                 }
-                tc_commit(&sh.accf[buf]);
             }
         }
-    } else if (warp >= 2 && warp <= 5) {
+    } else {
         // ================================================================ epilogue warps
-        const int te = tid - 64, q = warp & 3;
-        asm volatile("griddepcontrol.wait;" ::: "memory");   // the residual is this kernel's to write
-        const int r = 32 * q + lane;   // row within the tile
-        unsigned pend = 0u;   // te == 0: down counter before this CTA's previous piece
-        int pend_i = -1;
-
-        // the last piece of output slice t: out = r + sum over expert slots and K
-        // pieces of the weighted partials + sum_s w_s b_s, in a fixed order
-        auto finish_slice = [&](int t) {
-            const int row = t * kRowTile + r;
-            if (row < p.H) {
-                float acc[kMaxTokens] = {0.f, 0.f, 0.f, 0.f};
-                const int npc = g.nu * g.KC2;
-                for (int z0 = 0; z0 < npc; z0 += 8) {
-                    float4 a[8];
+        const int te = tid - 64, q = warp & 3;   // q: the lane quarter this warp may read
+        uint32_t kk = 0;
+        for (int k = 0; k < nitem; ++k) {
+            bool down;
+            int i;
+            item_at(k, nun, down, i);
+            const int unit = u0 + i, s = unit / T1, t = unit % T1;
+            if (!down) {
+                // ---- gate (rows 0..63) and up (rows 64..127) sums of 64 h rows; the
+                // biases are loaded before the accumulator is waited for
+                const uint32_t buf = i & 1;
+                const int hrow = 64 * t + 32 * (q & 1) + lane;
+                const int e = sh.unit_expert[s];
+                float bg = 0.f, bu = 0.f;
+                if (q < 2 && p.gu_bias) {
+                    bg = bf16f(__ldg(p.gu_bias + (size_t)e * 2 * p.I + hrow));
+                    bu = bf16f(__ldg(p.gu_bias + (size_t)e * 2 * p.I + p.I + hrow));
+                }
+                mbar_wait(&sh.accf[buf], (i >> 1) & 1, p.status);
+                tc_fence_after();
+                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + kGuCol + buf * 32;
+                float sm[kMaxTokens] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int z = 0; z < 8; ++z)
-                        if (z0 + z < npc)
-                            a[z] = __ldcg(reinterpret_cast<const float4*>(
-                                              p.part2 + ((size_t)t * npc + z0 + z) * kRowTile * kMaxTokens) + r);
+                for (int h16 = 0; h16 < 32; h16 += 16) {
+                    if (h16 < nrows) {
+                        float d0[16];
+                        tc_ld16(taddr + h16, d0);
+                        tc_wait_ld();
 #pragma unroll
-                    for (int z = 0; z < 8; ++z)
-                        if (z0 + z < npc) {
-                            acc[0] += a[z].x; acc[1] += a[z].y; acc[2] += a[z].z; acc[3] += a[z].w;
+                        for (int col = 0; col < 16; ++col) {
+                            const int m = (h16 + col) / kTerms;   // compile-time after unrolling
+                            if (m < M)
+                                sm[m] += d0[col];
                         }
-                }
-                if (p.dn_bias)
-                    for (int s2 = 0; s2 < g.nu; ++s2) {
-                        const float bd = bf16f(p.dn_bias[(size_t)sh.unit_expert[s2] * p.H + row]);
-#pragma unroll
-                        for (int m = 0; m < kMaxTokens; ++m)
-                            acc[m] = fmaf(sh.wslot[s2][m], bd, acc[m]);
                     }
-#pragma unroll
-                for (int m = 0; m < kMaxTokens; ++m) {
-                    if (m >= M)
-                        break;
-                    uint16_t* o = p.resid + (size_t)m * p.H + row;
-                    *o = f2bf16_rne(bf16f(__ldcg(o)) + acc[m]);
                 }
-            }
-        };
-
-        // h = silu(gate + b) * (up + b) of this warp's 32 rows of pair u (the
-        // pieces' partials summed, or the pair's own sums), its MX terms to the
-        // slot's h-term buffer, then the pair's release flag
-        auto publish_h = [&](const Unit& u, const float (&gs_in)[kMaxTokens], const float (&us_in)[kMaxTokens],
-                             bool from_partials) {
-            const int row = u.t * kRowTile + r;
-            if (u.t * kRowTile + 32 * q < p.I) {   // a warp's 32 rows are all valid or all not
-                const int e = sh.unit_expert[u.s];
-                const float bg = p.gu_bias ? bf16f(p.gu_bias[(size_t)e * 2 * p.I + row]) : 0.f;
-                const float bu = p.gu_bias ? bf16f(p.gu_bias[(size_t)e * 2 * p.I + p.I + row]) : 0.f;
-                float gs[kMaxTokens], us[kMaxTokens];
-#pragma unroll
-                for (int m = 0; m < kMaxTokens; ++m) {
-                    gs[m] = gs_in[m] + bg;
-                    us[m] = us_in[m] + bu;
-                }
-                if (from_partials)
-                    for (int c0 = 0; c0 < g.KC1; c0 += 8) {
-                        float4 a[8], c4[8];
-#pragma unroll
-                        for (int z = 0; z < 8; ++z)
-                            if (c0 + z < g.KC1) {
-                                const float4* src = reinterpret_cast<const float4*>(
-                                    p.part1 + ((size_t)(u.tile * g.KC1 + c0 + z) * 2) * kRowTile * kMaxTokens);
-                                a[z] = __ldcg(src + r);
-                                c4[z] = __ldcg(src + kRowTile + r);
-                            }
-#pragma unroll
-                        for (int z = 0; z < 8; ++z)
-                            if (c0 + z < g.KC1) {
-                                gs[0] += a[z].x; gs[1] += a[z].y; gs[2] += a[z].z; gs[3] += a[z].w;
-                                us[0] += c4[z].x; us[1] += c4[z].y; us[2] += c4[z].z; us[3] += c4[z].w;
-                            }
-                    }
-                float hv[kMaxTokens];
-#pragma unroll
-                for (int m = 0; m < kMaxTokens; ++m)
-                    hv[m] = gs[m] / (1.0f + expf(-gs[m])) * us[m];
-                uint8_t* dst = p.ht + (long long)u.s * hstride;
-                warp_terms_rows(hv, M, row >> 5, dst, dst + (long long)KSI * kAtom, lane);
-            }
-            epi_barrier();
-            if (te == 0)
-                st_release_u32(p.hready + u.tile, 1u);
-        };
-        const float zero4[kMaxTokens] = {0.f, 0.f, 0.f, 0.f};
-        // unit pi counted in with counter value `oldv` before it: finish its pair or
-        // output slice if it was the last piece
-        auto resolve = [&](int pi, unsigned oldv) {
-            const Unit pu = unit_at(g, p, pi, b, G);
-            const unsigned need = pu.down ? (unsigned)(g.nu * g.KC2) : (unsigned)g.KC1;
-            if (te == 0)
-                sh.flag = oldv == need - 1u;
-            epi_barrier();
-            const bool last = sh.flag;
-            epi_barrier();
-            if (last) {
-                if (pu.down)
-                    finish_slice(pu.t);
-                else
-                    publish_h(pu, zero4, zero4, true);
-            }
-        };
-
-        for (int i = 0; i < nunits; ++i) {
-            const Unit u = unit_at(g, p, i, b, G);
-            if (u.down && pend_i >= 0 && !unit_at(g, p, pend_i, b, G).down) {
-                // a pending gate/up piece is resolved before any down unit is waited
-                // for: that down unit may need the very h this CTA has to publish
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&sh.acce[buf]);
+                if (q >= 2)
+                    xch[(q - 2) * 32 + lane] = make_float4(sm[0], sm[1], sm[2], sm[3]);
                 epi_barrier();
-                resolve(pend_i, pend);
-                pend_i = -1;
-            }
-            // ---- drain: each token's term columns summed
-            const uint32_t buf = i & 1;
-            mbar_wait(&sh.accf[buf], (i >> 1) & 1, p.status);
-            tc_fence_after();
-            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * kAcc;
-            const bool two = !u.down || u.ks1 - u.ks0 > kSteps;   // issuer B wrote its half
-            float s0[kMaxTokens] = {0.f, 0.f, 0.f, 0.f}, s1[kMaxTokens] = {0.f, 0.f, 0.f, 0.f};
+                if (q < 2) {
+                    // h'_m = w_m silu(gate + b) (up + b) for h row 64t + 32q + lane: one
+                    // 32-element block (k-block q of the down k-step t)
+                    const float4 u4 = xch[q * 32 + lane];
+                    const float us[kMaxTokens] = {u4.x, u4.y, u4.z, u4.w};
+                    float hv[kMaxTokens];
 #pragma unroll
-            for (int h16 = 0; h16 < kRows; h16 += 16) {
-                if (h16 < nrows) {
-                    float d0[16], d1[16];
-                    tc_ld16(taddr + h16, d0);
-                    if (two)
-                        tc_ld16(taddr + kRows + h16, d1);
-                    tc_wait_ld();
-#pragma unroll
-                    for (int col = 0; col < 16; ++col) {
-                        const int m = (h16 + col) / kTerms;   // compile-time after unrolling
-                        if (m < M) {
-                            s0[m] += d0[col];
-                            if (!u.down)
-                                s1[m] += d1[col];
-                            else if (two)
-                                s0[m] += d1[col];
-                        }
+                    for (int m = 0; m < kMaxTokens; ++m) {
+                        const float g = sm[m] + bg;
+                        hv[m] = m < M ? sh.wslot[s][m] * (g / (1.0f + expf(-g))) * (us[m] + bu) : 0.f;
                     }
+                    uint8_t* hb = hterm + buf * kHTerm;
+                    switch (M) {   // one copy of the code runs
+                    case 1: warp_terms_rows<1>(hv, 0, q, hb, hb + 1024, atom, lane); break;
+                    case 2: warp_terms_rows<2>(hv, 0, q, hb, hb + 1024, atom, lane); break;
+                    case 3: warp_terms_rows<3>(hv, 0, q, hb, hb + 1024, atom, lane); break;
+                    default: warp_terms_rows<4>(hv, 0, q, hb, hb + 1024, atom, lane); break;
+                    }
+                    fence_proxy_async_smem();
+                }
+                epi_barrier();
+                if (te == 0)
+                    mbar_arrive(&sh.hbar[buf]);
+            } else {
+                // ---- down products of unit i into the CTA's output copy
+                for (int g = 0; g < NG; ++g, ++kk) {
+                    mbar_wait(&sh.dnf[kk & 1], (kk >> 1) & 1, p.status);
+                    tc_fence_after();
+                    const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + kDnCol + (kk & 1) * kDnRegion;
+                    const int ta = g * TG, tb = ta + TG < T2 ? ta + TG : T2;
+                    for (int t2 = ta; t2 < tb; ++t2) {
+                        float sm[kMaxTokens] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int h16 = 0; h16 < 32; h16 += 16) {
+                            if (h16 < nrows) {
+                                float d0[16];
+                                tc_ld16(taddr + (t2 - ta) * nrows + h16, d0);
+                                tc_wait_ld();
+#pragma unroll
+                                for (int col = 0; col < 16; ++col) {
+                                    const int m = (h16 + col) / kTerms;
+                                    if (m < M)
+                                        sm[m] += d0[col];
+                                }
+                            }
+                        }
+                        const int row = t2 * kRowTile + 32 * q + lane;
+                        if (row < p.H)
+#pragma unroll
+                            for (int m = 0; m < kMaxTokens; ++m)
+                                if (m < M)
+                                    oacc[row * M + m] += sm[m];
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&sh.dne[kk & 1]);
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&sh.acce[buf]);
-            if (!u.down && g.KC1 == 1) {   // a whole pair: h right away
-                publish_h(u, s0, s1, false);
-                continue;
-            }
-            // ---- a piece: its partials (down: weighted by each token's routing weight
-            // for this expert slot), counted into its pair / output slice
-            unsigned* cnt;
-            if (!u.down) {
-                float4* dst = reinterpret_cast<float4*>(p.part1 + ((size_t)u.id * 2) * kRowTile * kMaxTokens);
-                dst[r] = make_float4(s0[0], s0[1], s0[2], s0[3]);
-                dst[kRowTile + r] = make_float4(s1[0], s1[1], s1[2], s1[3]);
-                cnt = p.pair_cnt + u.tile;
-            } else {
+        }
+        // ---- the CTA's output copy to its partial slot [H][V] (rows drained by other warps)
+        epi_barrier();
+        if (nun > 0) {
+            float* dst = p.part + (size_t)b * p.H * V;
+            for (int row = te; row < p.H; row += kEpi) {
+                float v[kMaxTokens] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int m = 0; m < kMaxTokens; ++m)
-                    s0[m] *= m < M ? sh.wslot[u.s][m] : 0.f;
-                reinterpret_cast<float4*>(p.part2 + ((size_t)u.t * g.nu * g.KC2 + u.s * g.KC2 + u.pc) *
-                                                        kRowTile * kMaxTokens)[r] = make_float4(s0[0], s0[1], s0[2], s0[3]);
-                cnt = p.dn_cnt + u.t;
+                    if (m < M)
+                        v[m] = oacc[row * M + m];
+                if (V == 1)
+                    dst[row] = v[0];
+                else if (V == 2)
+                    reinterpret_cast<float2*>(dst)[row] = make_float2(v[0], v[1]);
+                else
+                    reinterpret_cast<float4*>(dst)[row] = make_float4(v[0], v[1], v[2], v[3]);
             }
-            epi_barrier();   // the piece's partials are stored
-            // whether this was the last piece is read one unit later, so the atomic's
-            // latency hides behind the next accumulator wait
-            const unsigned prev = pend;
-            const int prev_i = pend_i;
-            if (te == 0)   // releases the partials; acquires the other pieces' if last
-                pend = atom_add_acq_rel(cnt, 1u);
-            pend_i = i;
-            if (prev_i >= 0)
-                resolve(prev_i, prev);
-        }
-        if (pend_i >= 0) {
-            epi_barrier();
-            resolve(pend_i, pend);
         }
     }
 
-    // ---- exit: the last CTA out resets the counters for the next call
+    // ---- this CTA's output rows [r0, r1): their bias terms sum_s w_s b_s and the
+    // residual are loaded before the grid barrier
+    const int r0 = (int)((unsigned)b * p.H / G), r1 = (int)((unsigned)(b + 1) * p.H / G);
+    const int nr = r1 - r0;
+    float bsum[kMaxTokens] = {0.f, 0.f, 0.f, 0.f}, rv[kMaxTokens] = {0.f, 0.f, 0.f, 0.f};
+    if (tid < nr) {
+        const int row = r0 + tid;
+        if (p.dn_bias)
+            for (int s2 = 0; s2 < nu; ++s2) {
+                const float bd = bf16f(__ldg(p.dn_bias + (size_t)sh.unit_expert[s2] * p.H + row));
+#pragma unroll
+                for (int m = 0; m < kMaxTokens; ++m)
+                    bsum[m] = fmaf(sh.wslot[s2][m], bd, bsum[m]);
+            }
+#pragma unroll
+        for (int m = 0; m < kMaxTokens; ++m)
+            if (m < M)
+                rv[m] = bf16f(__ldcg(p.resid + (size_t)m * p.H + row));
+    }
+
+    // ---- grid barrier: every CTA's output copy is stored (every CTA counts itself in)
     tc_fence_before();
     __syncthreads();
     if (tid == 0) {
-        __threadfence();
-        if (atomicAdd(p.exit_cnt, 1u) == (unsigned)G - 1u) {
-            for (int i = 0; i < g.nu * g.T1; ++i) {
-                p.hready[i] = 0u;
-                p.pair_cnt[i] = 0u;
+        const unsigned long long tgt = count_target(atom_add_release_u64(p.done, 1ull), G);
+        int spins = 0;
+#pragma unroll 1
+        while (ld_acquire_u64(p.done) < tgt) {
+            if (++spins > (1 << 24)) {
+                atomicExch(p.status, MOE_ERR_DEVICE_TIMEOUT);
+                break;
             }
-            for (int i = 0; i < g.T2; ++i)
-                p.dn_cnt[i] = 0u;
-            *p.exit_cnt = 0u;
-            __threadfence();
         }
     }
+    __syncthreads();
+
+    // ---- output rows [r0, r1): the active CTAs' copies summed in CTA order, split
+    // over P thread groups (group g takes CTAs g, g + P, ...), then the groups in order
+    if (nr > 0) {
+        float4* red = reinterpret_cast<float4*>(ring);   // [P][nr]; the ring is idle now
+        const int P = kThreadsTc / nr < 1 ? 1 : kThreadsTc / nr;
+        if (tid < P * nr) {
+            const int j = tid % nr, g = tid / nr;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            // group g's CTAs: with U >= G every CTA, else the owners of the U units
+            auto cta_of = [&](int cc) { return U < G ? (int)(((unsigned)(cc + 1) * G + U - 1) / U) - 1 : cc; };
+            // the copies' rows are V floats; one loop per V, so one copy of the code runs
+            auto sum_rows = [&](auto vtag) {
+                using VT = decltype(vtag);
+                constexpr int VW = sizeof(VT) / sizeof(float);
+                for (int c0 = g; c0 < nact; c0 += 8 * P) {
+                    VT a[8];
+#pragma unroll
+                    for (int z = 0; z < 8; ++z)
+                        if (c0 + z * P < nact)
+                            a[z] = __ldcg(reinterpret_cast<const VT*>(p.part + ((size_t)cta_of(c0 + z * P) * p.H + r0 + j) * VW));
+#pragma unroll
+                    for (int z = 0; z < 8; ++z)
+                        if (c0 + z * P < nact) {
+                            const float* f = reinterpret_cast<const float*>(&a[z]);
+                            acc.x += f[0];
+                            if (VW > 1) acc.y += f[VW > 1 ? 1 : 0];
+                            if (VW > 2) { acc.z += f[VW > 2 ? 2 : 0]; acc.w += f[VW > 2 ? 3 : 0]; }
+                        }
+                }
+            };
+            if (V == 1)
+                sum_rows(0.f);
+            else if (V == 2)
+                sum_rows(make_float2(0.f, 0.f));
+            else
+                sum_rows(make_float4(0.f, 0.f, 0.f, 0.f));
+            red[g * nr + j] = acc;
+        }
+        __syncthreads();
+        if (tid < nr) {
+            const int row = r0 + tid;
+            float acc[kMaxTokens] = {0.f, 0.f, 0.f, 0.f};
+            for (int g = 0; g < P; ++g) {
+                const float4 a = red[g * nr + tid];
+                acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+            }
+#pragma unroll
+            for (int m = 0; m < kMaxTokens; ++m)
+                if (m < M)
+                    p.resid[(size_t)m * p.H + row] = f2bf16_rne(rv[m] + (acc[m] + bsum[m]));
+        }
+    }
+
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
     }
-}
-
-// x terms of a layer (PDL-chained before the decode kernel): one warp per
-// group of 4 blocks of one token, into the buffer the decode kernel copies
-// from ([H/64 k-step atoms][ceil(H/128) scale chunks], the shared-memory order).
-// With x = nullptr the input is the RMS-normalised residual,
-// x = bf16(r / sqrt(mean(r^2) + 1e-6)).
-__global__ void __launch_bounds__(128) xterms_kernel(const DecodeTcParams p)
-{
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    __shared__ float nrm[4][kMaxTokens];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, M = p.M;
-    const uint16_t* xs = p.x ? p.x : p.resid;
-    float inv[kMaxTokens] = {1.f, 1.f, 1.f, 1.f};
-    if (!p.x) {
-        for (int m = 0; m < M; ++m) {
-            float a = 0.f;
-            for (int i = tid; i < p.H / 2; i += 128) {
-                const uint32_t w = __ldcg(reinterpret_cast<const unsigned*>(xs + (size_t)m * p.H) + i);
-                const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
-                a = fmaf(lo, lo, a);
-                a = fmaf(hi, hi, a);
-            }
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1)
-                a += __shfl_xor_sync(0xffffffffu, a, off);
-            if (lane == 0)
-                nrm[warp][m] = a;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int m = 0; m < kMaxTokens; ++m)
-            inv[m] = 1.0f / sqrtf((nrm[0][m] + nrm[1][m] + nrm[2][m] + nrm[3][m]) / (float)p.H + 1e-6f);
-    }
-    const int nkb = p.H / 32, ngr = (nkb + 3) / 4;
-    const int x = blockIdx.x * 4 + warp;
-    if (x >= M * ngr)
-        return;
-    const int m = x / ngr, kbg = 4 * (x % ngr);
-    float v[1][4];
-    uint2 u2 = make_uint2(0u, 0u);
-    if (kbg + (lane >> 3) < nkb)
-        u2 = __ldcg(reinterpret_cast<const uint2*>(xs + (size_t)m * p.H + 32 * kbg + 4 * lane));
-    v[0][0] = __uint_as_float(u2.x << 16);
-    v[0][1] = __uint_as_float(u2.x & 0xffff0000u);
-    v[0][2] = __uint_as_float(u2.y << 16);
-    v[0][3] = __uint_as_float(u2.y & 0xffff0000u);
-    if (!p.x) {
-        float im = inv[0];
-#pragma unroll
-        for (int t = 1; t < kMaxTokens; ++t)
-            im = m == t ? inv[t] : im;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            v[0][i] = bf16f(f2bf16_rne(v[0][i] * im));
-    }
-    const int mm[1] = {m}, kk[1] = {kbg}, nv[1] = {nkb - kbg};
-    warp_terms<1>(v, mm, kk, nv, p.xt, p.xt + (long long)(p.H / 64) * kAtom, lane);
 }
 
 }  // namespace
@@ -933,21 +929,14 @@ cudaError_t prepare_decode_tc(size_t smem)
     return cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
+size_t decode_tc_static_smem()
+{
+    cudaFuncAttributes a{};
+    return cudaFuncGetAttributes(&a, decode_tc_kernel) == cudaSuccess ? a.sharedSizeBytes : 0;
+}
+
 cudaError_t launch_decode_tc(const DecodeTcParams& p, size_t smem, int grid, cudaStream_t stream)
 {
-    const int ngr = (p.H / 32 + 3) / 4;
-    cudaLaunchAttribute pre[1];
-    pre[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    pre[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t pc = {};
-    pc.gridDim = dim3((p.M * ngr + 3) / 4);
-    pc.blockDim = dim3(128);
-    pc.stream = stream;
-    pc.attrs = pre;
-    pc.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&pc, xterms_kernel, p);
-    if (e != cudaSuccess)
-        return e;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;

@@ -101,6 +101,10 @@ int set_error(int code, const char* fmt, ...);
 //          bytes of K-blocks 4c..4c+3 of the tile's 128 rows, row r = i + 32j
 //          and block kb at i*16 + j*4 + kb (the order a 32x128-bit tensor-memory
 //          copy replicated to the four lane quarters expects).
+// The gate_up matrix [2I][K] (gate rows 0..I-1, up rows I..2I-1) is stored as
+// one projection of 2I rows in the interleaved row order: tile t holds gate rows
+// 64t .. 64t+63 as its rows 0..63 and up rows 64t .. 64t+63 as its rows
+// 64..127, so one 128-row MMA gives gate and up of the same 64 rows of h.
 // Activations (x, h) use the same two orders per token tile: codes
 // [k-step][npad rows x 32 bytes], scales [chunk][512].
 constexpr int kMaxBatchTokens = 8192;
@@ -124,7 +128,7 @@ struct TokTile {
 };
 
 struct BatchParams {
-    const uint8_t* gu;          // tile layout: expert e at + e*gu_expert = [gate proj][up proj]
+    const uint8_t* gu;          // interleaved tile layout: expert e at + e*gu_expert
     const uint8_t* dn;          // expert e at + e*dn_expert
     long long gu_expert, dn_expert;
     const uint16_t* gu_bias;    // [E][2I] bf16, or nullptr
@@ -156,9 +160,11 @@ struct BatchParams {
 cudaError_t launch_batched(const BatchParams& p, int grid, cudaStream_t stream, int* launches);
 cudaError_t prepare_batched_kernels();
 // Caller layout [E][N][K/2] codes + [E][N][K/32] E8M0 -> tile layout (one projection
-// per expert; source rows row0 .. row0+N-1 of a caller matrix with `src_rows` rows).
+// per expert of N rows of a caller matrix with `src_rows` rows).  Tile row n comes
+// from caller row n, or with `interleave` = I > 0 (N = 2I) from the interleaved
+// gate_up order: row 64t + r (r < 64) or I + 64t + r - 64 of tile t.
 cudaError_t launch_repack_tiles(const uint8_t* codes, const uint8_t* scales, int E, int src_rows,
-                                int row0, int N, int K, uint8_t* out, long long expert_bytes,
+                                int N, int K, int interleave, uint8_t* out, long long expert_bytes,
                                 cudaStream_t stream);
 // MX quantisation of n fp32 values (n % 32 == 0) into natural order codes/scales.
 cudaError_t launch_mx_quantize(const float* in, long long n, uint8_t* codes, uint8_t* scales,
@@ -169,43 +175,33 @@ cudaError_t launch_untile_h(const BatchParams& p, uint8_t* codes, uint8_t* scale
 
 // ------------------------------------------------------ tensor-core decode
 // The MXFP4 decode layer (M <= 4) on tcgen05 kind::mxf4 (moe_decode_tc.cu);
-// weights in the tile layout above.  Two launches: the x-term kernel, then the
-// persistent layer kernel (PDL-chained).
+// weights in the tile layout above.  One persistent launch per layer, chained
+// to the previous grid with programmatic dependent launch.
 
 struct DecodeTcParams {
-    const uint8_t* gu;          // tile layout: expert e at + e*gu_expert = [gate proj][up proj]
-    const uint8_t* dn;
+    const uint8_t* gu;          // interleaved tile layout: expert e at + e*gu_expert
+    const uint8_t* dn;          // tile layout: expert e at + e*dn_expert
     long long gu_expert, dn_expert;
-    const uint16_t* gu_bias;    // [E][2I] bf16, or nullptr
+    const uint16_t* gu_bias;    // [E][2I] bf16 (gate | up), or nullptr
     const uint16_t* dn_bias;    // [E][H] bf16, or nullptr
     const float* logits;        // [M][E]
     const uint16_t* x;          // [M][H] bf16, or nullptr: RMS-normalise resid
     uint16_t* resid;            // [M][H] bf16 in/out
-    float* part1;               // gate/up partials [pair][K piece][2][128][4]
-    float* part2;               // weighted down partials [output slice][slot][K piece][128][4]
-    uint8_t* xt;                // x terms of the layer: [H/64][32 rows x 32 B][ceil(H/128)][512]
-    uint8_t* ht;                // h terms per slot: [slot][I/64][32 x 32 B][ceil(I/128)][512]
-    unsigned* pair_cnt;         // [slot][T1] gate/up K pieces finished (zero between calls)
-    unsigned* hready;           // [slot][T1] h terms of a gate/up pair published (zero between calls)
-    unsigned* dn_cnt;           // [T2] down pieces finished per output slice (zero between calls)
-    unsigned* exit_cnt;         // [1]
+    float* part;                // [G][H][4] each CTA's fp32 copy of the expert output
+    uint8_t* xt;                // x terms of the layer: [H/64][N rows x 32 B][ceil(H/128)][512]
+    unsigned long long* xcnt;   // [1] x-term publications, G per call (only grows)
+    unsigned long long* done;   // [1] output copies stored, G per call (only grows)
     int* status;
     int* nu_out;
     int H, I, E, M, k;
-    int smem_bytes;             // dynamic shared memory of the layer kernel: the stage ring
+    int smem_bytes;             // dynamic shared memory of the layer kernel
 };
 
-// Workspace bounds for G CTAs.
-// Unit counts: U1 = pairs * KC1, U2 = tiles * KC2 with KC1 = 2k, KC2 = k,
-// k = ceil(3G / (2 pairs + tiles)), so U1 < 3G + 2 pairs and U2 < 1.5G + tiles.
-inline int tc_max_units1(int G, int I) { return 3 * G + 2 * kMaxUnits * ceil_div(I, kRowTile); }
-inline int tc_max_units2(int G, int H, int I) { return 2 * G + kMaxUnits * ceil_div(H, kRowTile); }
 inline size_t tc_terms_bytes(int K) { return (size_t)(K / 64) * 1024 + (size_t)ceil_div(K, 128) * kSfChunk; }
-inline size_t tc_counter_words(int H, int I)
-{
-    return 2 * (size_t)kMaxUnits * ceil_div(I, kRowTile) + ceil_div(H, kRowTile) + 1;
-}
+inline size_t tc_part_bytes(int G, int H) { return (size_t)G * H * 4 * sizeof(float); }
+constexpr int kTcCounterWords = 2;   // xcnt, done (64-bit)
 cudaError_t prepare_decode_tc(size_t smem);
+size_t decode_tc_static_smem();
 cudaError_t launch_decode_tc(const DecodeTcParams& p, size_t smem, int grid, cudaStream_t stream);
 
 // Debug kernels.

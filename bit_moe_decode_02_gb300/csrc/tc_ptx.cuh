@@ -58,8 +58,11 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity)
 
 // Bounded wait on one phase of an mbarrier; on give-up record a timeout and
 // return false (the caller carries on: every loop of these kernels is bounded).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status)
+// Not inlined: the kernels wait at many places, and one copy keeps the code
+// small enough for the instruction caches.
+static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status)
 {
+#pragma unroll 1
     for (int i = 0; i < (1 << 22); ++i)
         if (mbar_try_wait(bar, parity))
             return true;
@@ -72,6 +75,22 @@ __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t b
 {
     asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(su32(dst)), "l"(src), "r"(bytes), "r"(su32(bar)) : "memory");
+}
+
+// L2 policy for data read once per call (streamed weights): evict first, so
+// it does not push out what is reused (activations, partial sums, code).
+__device__ __forceinline__ uint64_t l2_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Bulk copy global -> shared with an L2 cache policy.
+__device__ __forceinline__ void bulk_copy_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol)
+{
+    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+                 ::"r"(su32(dst)), "l"(src), "r"(bytes), "r"(su32(bar)), "l"(pol) : "memory");
 }
 
 // Shared-memory matrix descriptor, no swizzle, K-major canonical layout:
