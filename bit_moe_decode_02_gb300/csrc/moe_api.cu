@@ -80,6 +80,8 @@ struct moe_handle {
     bool batched = false;             // max_tokens > kMaxTokens
     size_t tc_smem = 0;
     float* tc_part = nullptr;
+    float* tc_gpart = nullptr;      // split units: pieces' gate/up partial sums
+    unsigned* tc_flags = nullptr;   // split units: [G] piece flags
     uint8_t* tc_xt = nullptr;
     unsigned long long* tc_cnt = nullptr;
     size_t t_gu_expert = 0, t_dn_expert = 0, t_off_dn = 0, t_layer_stride = 0;
@@ -176,6 +178,8 @@ void free_handle(moe_handle* h)
     cudaFree(h->st_logits);
     cudaFree(h->tarena);
     cudaFree(h->tc_part);
+    cudaFree(h->tc_gpart);
+    cudaFree(h->tc_flags);
     cudaFree(h->tc_xt);
     cudaFree(h->tc_cnt);
     cudaFree(h->b_int);
@@ -255,6 +259,8 @@ int create_tiles(moe_handle* h)
     int rc;
     if ((rc = dev_alloc(&h->tarena, h->t_layer_stride * c.num_layers, "tile-layout weights")) ||
         (rc = dev_alloc(&h->tc_part, moe::tc_part_bytes(G, H), "per-CTA outputs")) ||
+        (rc = dev_alloc(&h->tc_gpart, (size_t)G * moe::kRowTile * 4 * sizeof(float), "split-unit partials")) ||
+        (rc = dev_alloc(&h->tc_flags, (size_t)G * sizeof(unsigned), "split-unit flags")) ||
         (rc = dev_alloc(&h->tc_xt, moe::tc_terms_bytes(H), "x terms")) ||
         (rc = dev_alloc(&h->tc_cnt, moe::kTcCounterWords * sizeof(unsigned long long), "counters")))
         return rc;
@@ -263,6 +269,8 @@ int create_tiles(moe_handle* h)
     // keep them zero (valid E2M1 codes, E8M0 byte 0) instead of leftover bytes
     if (e == cudaSuccess)
         e = cudaMemset(h->tc_xt, 0, moe::tc_terms_bytes(H));
+    if (e == cudaSuccess)
+        e = cudaMemset(h->tc_flags, 0, (size_t)G * sizeof(unsigned));
     if (e != cudaSuccess)
         return cuda_fail(e, "counters");
     // all the shared memory a block may have: the kernel's own plus the stage ring
@@ -289,6 +297,8 @@ moe::DecodeTcParams tc_params(const moe_handle* h, int layer)
     p.gu_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(sb + h->off_gu_bias) : nullptr;
     p.dn_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(sb + h->off_dn_bias) : nullptr;
     p.part = h->tc_part;
+    p.gpart = h->tc_gpart;
+    p.pflag = h->tc_flags;
     p.xt = h->tc_xt;
     p.xcnt = h->tc_cnt;
     p.done = h->tc_cnt + 1;
@@ -789,7 +799,9 @@ int moe_get_status(moe_handle* h, void* stream)
     if (st != MOE_OK) {
         // a call gave up waiting: its cross-CTA counters may be left part-way; clear them
         const size_t ncount = moe::counter_words(h->cfg.hidden);
+        // (the call tags restart with the counters, so the flags are cleared too)
         if ((h->tc_cnt && (e = cudaMemset(h->tc_cnt, 0, moe::kTcCounterWords * sizeof(unsigned long long))) != cudaSuccess) ||
+            (h->tc_flags && (e = cudaMemset(h->tc_flags, 0, (size_t)h->num_sms * sizeof(unsigned))) != cudaSuccess) ||
             (e = cudaMemset(h->counters, 0, ncount * sizeof(unsigned))) != cudaSuccess ||
             (e = cudaDeviceSynchronize()) != cudaSuccess)
             return cuda_fail(e, "moe_get_status reset");

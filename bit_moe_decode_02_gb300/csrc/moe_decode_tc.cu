@@ -35,10 +35,11 @@
 // over each SM as soon as this layer's CTA there exits and set up before they
 // wait for this grid to complete.
 //
-// Warp roles (192 threads): warp 0 streams weights into a byte ring of shared
+// Warp roles (256 threads): warp 0 streams weights into a byte ring of shared
 // memory (each stage's copies issued from separate lanes in one instruction);
-// warp 1 owns tensor memory and issues the MMAs; warps 2..5 (one per lane
-// quarter) build the x terms and drain the accumulators.  Warps 0 and 1 route.
+// warps 1 and 6 issue the MMAs (warp 1 owns tensor memory); warps 2..5 (one
+// per lane quarter) build the x terms and drain the accumulators; warp 7
+// combines a split unit's partial sums.  Warps 0, 1 and 6 route.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -55,35 +56,43 @@ using namespace tc;
 
 constexpr int kTerms = 8;            // MX terms per activation vector
 constexpr int kGuSteps = 8;          // k-steps (64 of K) per gate/up stage
-constexpr int kDnStageTiles = 5;     // 128-row down tiles per down stage
+constexpr int kDnStageTiles = 4;     // 128-row down tiles per down stage
 constexpr int kSlots = 16;           // stages in flight at most
 // tensor memory columns
-constexpr int kGuCol = 0;            // gate/up accumulators: 2 buffers x 32
-constexpr int kDnCol = 64;           // down accumulators: 2 regions x 160
-constexpr int kDnRegion = 160;
+constexpr int kGuCol = 0;            // gate/up accumulators: 2 buffers x (issuer A | B) x 32
+constexpr int kGuBuf = 64;
+constexpr int kDnCol = 128;          // down accumulators: 2 regions x 128
+constexpr int kDnRegion = 128;
 constexpr int kSfCol = 384;          // stage scale sets: 2 issuers x 2 sets x 32
+static_assert(kGuCol + 2 * kGuBuf <= kDnCol, "gate/up accumulators");
 constexpr int kSfSet = 32;
 constexpr int kTmemCols = 512;
 static_assert(kDnCol + 2 * kDnRegion <= kSfCol && kSfCol + 4 * kSfSet <= kTmemCols, "tensor memory");
 static_assert(kDnRegion % (kDnStageTiles * 32) == 0, "a region holds whole down stages");
 static_assert(kSfSet >= 8 * ((kGuSteps + 1) / 2), "a gate/up stage's A and B scale chunks fit a set");
 static_assert(kSfSet >= 4 * (kDnStageTiles + 1), "a down stage's scale chunks fit a set");
-constexpr int kThreadsTc = 224;      // producer, MMA issuer A, 4 epilogue warps, MMA issuer B
+constexpr int kThreadsTc = 256;      // producer, MMA issuer A, 4 epilogue warps, MMA issuer B, combiner
 constexpr int kMmaWarpB = 6;
+constexpr int kCombineWarp = 7;
 constexpr int kEpi = 128;            // epilogue threads (warps 2..5)
-constexpr int kPend = 16;            // gate/up stages waiting for the x terms
 constexpr int kTileA = kRowTile * 32;            // one k-step of a 128-row tile: 4 KB
-constexpr int kHTerm = 1024 + kSfChunk;          // h' terms of a unit: one k-step atom + its scale chunk
+constexpr int kHTerm = kHTermBytes;              // h' terms of a unit: one k-step atom + its scale chunk
 
 // MMA N: the rows that hold terms, rounded up to 16; a k-step of terms is
 // N rows x 32 bytes (8-row groups 256 bytes apart).
 __device__ __forceinline__ int rows_for(int M) { return M * kTerms <= 16 ? 16 : 32; }
 
-// Shared memory past the stage ring: two h'-term buffers, the up-sum exchange
-// (2 warps x 32 lanes x float4) and the CTA's fp32 output copy [H][M].
-__device__ __forceinline__ uint32_t tail_bytes(int H, int M)
+// Shared memory past the stage ring: the layer's x terms (H/64 k-step atoms,
+// then ceil(H/128) scale chunks), three h'-term buffers (two for whole units,
+// one for a split unit's), the up-sum exchange (2 warps x 32 lanes x float4)
+// and the CTA's fp32 output copy [H][M].
+__device__ __forceinline__ uint32_t xterm_bytes(int H, int atom)
 {
-    return 2 * kHTerm + 2 * 32 * 16 + (((uint32_t)H * M * 4 + 127) & ~127u);
+    return (uint32_t)(H / 64) * atom + (uint32_t)ceil_div(H, 128) * kSfChunk;
+}
+__device__ __forceinline__ uint32_t tail_bytes(int H, int M, int atom)
+{
+    return ((xterm_bytes(H, atom) + 127) & ~127u) + 3 * kHTerm + 2 * 32 * 16 + (((uint32_t)H * M * 4 + 127) & ~127u);
 }
 
 // Items of a CTA with n units, in the order the producer, the MMA issuer and
@@ -104,18 +113,82 @@ __device__ __forceinline__ void item_at(int k, int n, bool& down, int& i)
     }
 }
 
-// Gate/up stage: [A: steps x 4 KB][SFA: chunks x 512][B: steps x atom][SFB: chunks x 512].
+// What a CTA does.  With U >= G units and rem = U mod G left over after q
+// whole units per CTA, a leftover unit is split in S = min(G / rem, ...) pieces
+// (S >= 2), each a K range of its gate/up and a range of its down tiles: piece
+// p of leftover unit j goes to CTA j S + p.  The pieces publish their gate/up
+// partial sums; every piece's CTA adds all of them in piece order (the same
+// fp32 operations everywhere, so the same h') and computes the unit's h' for
+// its own down tiles -- a warp of its own does this, so neither the weight
+// stream nor the drains wait for the exchange.  Otherwise the units are
+// dealt whole, CTA b taking [b U / G, (b+1) U / G).
+struct Plan {
+    int u0, nun;          // whole units [u0, u0 + nun)
+    int piece;            // 1: this CTA holds a piece of a split unit
+    int su, sj, pp, S;    // the split unit, its leftover index, the piece, the pieces
+    int ks0, ks1, ta, tb; // the piece's gate/up k-steps and down tiles
+    int nitem;
+};
+__device__ __forceinline__ Plan make_plan(int b, int G, int U, int KSH, int CHH, int T2)
+{
+    Plan pl{};
+    const int q = U / G, rem = U - q * G;
+    int S = rem > 0 ? G / rem : 0;
+    S = S < CHH ? S : CHH;
+    S = S < T2 ? S : T2;
+    if (q >= 1 && S >= 2) {
+        pl.u0 = b * q;
+        pl.nun = q;
+        if (b < rem * S) {
+            pl.piece = 1;
+            pl.sj = b / S;
+            pl.pp = b - pl.sj * S;
+            pl.S = S;
+            pl.su = G * q + pl.sj;
+            const int c0 = pl.pp * CHH / S, c1 = (pl.pp + 1) * CHH / S;
+            pl.ks0 = 2 * c0;
+            pl.ks1 = 2 * c1 < KSH ? 2 * c1 : KSH;
+            pl.ta = pl.pp * T2 / S;
+            pl.tb = (pl.pp + 1) * T2 / S;
+        }
+    } else {
+        pl.u0 = (int)((unsigned)b * U / G);
+        pl.nun = (int)((unsigned)(b + 1) * U / G) - pl.u0;
+    }
+    pl.nitem = 2 * pl.nun + 2 * pl.piece;
+    return pl;
+}
+
+enum ItemKind { kGu = 0, kDn = 1, kGuPiece = 2, kDnPiece = 3 };
+// Item k of a plan: the piece's gate/up first (its partial sums are published
+// early), the whole units' items, the piece's down tiles last.  The epilogue
+// combines the pieces' partials only after the last whole unit's gate/up, so
+// that unit's SwiGLU never waits for the exchange.
+__device__ __forceinline__ void item_of(const Plan& pl, int k, int& kind, int& i)
+{
+    if (pl.piece && k == 0) {
+        kind = kGuPiece;
+        i = 0;
+    } else if (pl.piece && k == pl.nitem - 1) {
+        kind = kDnPiece;
+        i = 0;
+    } else {
+        bool down;
+        item_at(k - pl.piece, pl.nun, down, i);
+        kind = down ? kDn : kGu;
+    }
+}
+
+// Gate/up stage: [A: steps x 4 KB][SFA: chunks x 512] (the x terms stay in
+// shared memory for the whole layer).
 struct GuStage {
-    uint32_t abytes, sfbytes, bbytes, sfa, b, sfb, size;
-    __device__ GuStage(int steps, int atom)
+    uint32_t abytes, sfbytes, sfa, size;
+    __device__ GuStage(int steps)
     {
         abytes = steps * kTileA;
         sfbytes = ((steps + 1) >> 1) * kSfChunk;
-        bbytes = steps * atom;
         sfa = abytes;
-        b = sfa + sfbytes;
-        sfb = b + bbytes;
-        size = (sfb + sfbytes + 127) & ~127u;
+        size = (sfa + sfbytes + 127) & ~127u;
     }
 };
 // Down stage of n tiles: [A: n x 4 KB][SFA: n x 512].  A partial tile (64 rows)
@@ -142,6 +215,16 @@ struct RingTc {
 __device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, %0;" ::"r"(kEpi) : "memory"); }
 __device__ __forceinline__ void route_barrier() { asm volatile("bar.sync 2, 96;" ::: "memory"); }
 
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p)
 {
     unsigned long long v;
@@ -228,22 +311,25 @@ __device__ __forceinline__ void warp_terms_rows(float (&r)[kMaxTokens], int m0, 
             }
         }
     }
+    // Packing: an 8 x 8 nibble transpose within each group of 8 lanes (3
+    // butterfly exchanges of 16-, 8- and 4-bit fields) leaves lane 8g + i with
+    // term i's codes of elements 8g .. 8g+7, one 32-bit store per lane per token;
+    // lane i < 8 writes term i's scale byte.
+    const int i8 = lane & 7;
 #pragma unroll
     for (int m = 0; m < M; ++m) {
-        const uint32_t cm = codes[m], lo = sblo[m], hi = sbhi[m];
-#pragma unroll
-        for (int j = 0; j < kTerms; ++j) {
-            uint32_t word = ((cm >> (4 * j)) & 0xfu) << (4 * (lane & 7));
-            word |= __shfl_xor_sync(0xffffffffu, word, 1);
-            word |= __shfl_xor_sync(0xffffffffu, word, 2);
-            word |= __shfl_xor_sync(0xffffffffu, word, 4);
-            const int row = (m0 + m) * kTerms + j;
-            if ((lane & 7) == 0)
-                *reinterpret_cast<uint32_t*>(q + (kb >> 1) * atom + (row >> 3) * 256 + (kb & 1) * 128 +
-                                             (row & 7) * 16 + 4 * (lane >> 3)) = word;
-            if (lane == 0)
-                sf[(kb >> 2) * kSfChunk + row * 16 + (kb & 3)] = (uint8_t)((j < 4 ? lo : hi) >> (8 * (j & 3)));
-        }
+        uint32_t x = codes[m];
+        uint32_t y = __shfl_xor_sync(0xffffffffu, x, 4);
+        x = (lane & 4) ? ((x & 0xFFFF0000u) | (y >> 16)) : ((x & 0x0000FFFFu) | (y << 16));
+        y = __shfl_xor_sync(0xffffffffu, x, 2);
+        x = (lane & 2) ? ((x & 0xFF00FF00u) | ((y >> 8) & 0x00FF00FFu)) : ((x & 0x00FF00FFu) | ((y << 8) & 0xFF00FF00u));
+        y = __shfl_xor_sync(0xffffffffu, x, 1);
+        x = (lane & 1) ? ((x & 0xF0F0F0F0u) | ((y >> 4) & 0x0F0F0F0Fu)) : ((x & 0x0F0F0F0Fu) | ((y << 4) & 0xF0F0F0F0u));
+        const int row = (m0 + m) * kTerms + i8;
+        *reinterpret_cast<uint32_t*>(q + (kb >> 1) * atom + (row >> 3) * 256 + (kb & 1) * 128 + i8 * 16 +
+                                     4 * (lane >> 3)) = x;
+        if (lane < 8)
+            sf[(kb >> 2) * kSfChunk + row * 16 + (kb & 3)] = (uint8_t)((i8 < 4 ? sblo[m] : sbhi[m]) >> (8 * (i8 & 3)));
     }
 }
 
@@ -273,7 +359,9 @@ struct TcSmem {
     uint64_t accf[2], acce[2];   // gate/up accumulator buffers: full / drained
     uint64_t dnf[2], dne[2];     // down accumulator regions: full (both issuers) / drained
     uint64_t hbar[2];            // h' terms of a unit written
-    uint64_t routed, xready;     // routing done; every CTA's x terms published
+    uint64_t routed, xfull;      // routing done; the layer's x terms copied in
+    uint64_t hsfull;             // the split unit's h' terms copied in
+    unsigned epoch;              // this call's tag for the exchange flags (call index + 1)
     uint32_t tmem_base;
     int sel[kMaxTokens][kMaxTopK];
     float wt[kMaxTokens][kMaxTopK];
@@ -295,14 +383,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
     const int KSH = p.H / 64, CHH = ceil_div(p.H, 128), CHI = ceil_div(p.I, 128);
     const int T1 = p.I / 64, T2 = ceil_div(p.H, kRowTile);   // units per expert, down row tiles
     const int TG = kDnRegion / nrows;                           // down tiles per accumulator region
-    const int NG = ceil_div(T2, TG);                            // down groups per unit
     const int nblk = p.H / 32, nitems = M * nblk;               // x-term items: (token, 32-element block)
     const int V = M == 1 ? 1 : (M == 2 ? 2 : 4);                // floats per row of a CTA's output copy
-    const uint32_t tail_off = ((uint32_t)p.smem_bytes - tail_bytes(p.H, M)) & ~127u;
-    const uint32_t ring_cap = tail_off & ~127u;
-    uint8_t* hterm = ring + tail_off;                           // [2][kHTerm]
-    float4* xch = reinterpret_cast<float4*>(ring + tail_off + 2 * kHTerm);   // [2][32]
-    float* oacc = reinterpret_cast<float*>(ring + tail_off + 2 * kHTerm + 2 * 32 * 16);   // [H][M]
+    const uint32_t tail_off = ((uint32_t)p.smem_bytes - tail_bytes(p.H, M, atom)) & ~127u;
+    const uint32_t ring_cap = tail_off;
+    uint8_t* xs = ring + tail_off;                              // x terms of the layer
+    uint8_t* hterm = xs + ((xterm_bytes(p.H, atom) + 127) & ~127u);   // [3][kHTerm]
+    float4* xch = reinterpret_cast<float4*>(hterm + 3 * kHTerm);       // [2][32]
+    float* oacc = reinterpret_cast<float*>(hterm + 3 * kHTerm + 2 * 32 * 16);   // [H][M]
 
     // warm L2 and the TLB for what the first steps read once the previous grid
     // is complete (a prefetch returns no data, so it cannot see a stale value)
@@ -322,14 +410,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
             mbar_init(&sh.empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sh.accf[i], 1);
+            mbar_init(&sh.accf[i], 2);
             mbar_init(&sh.acce[i], 4);
             mbar_init(&sh.dnf[i], 2);
             mbar_init(&sh.dne[i], 4);
             mbar_init(&sh.hbar[i], 1);
         }
         mbar_init(&sh.routed, 1);
-        mbar_init(&sh.xready, 1);
+        mbar_init(&sh.xfull, 1);
+        mbar_init(&sh.hsfull, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -418,7 +507,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
             // publish this CTA's x terms (every CTA counts itself in), then wait for
             // the whole count and hand it to the producer through an mbarrier, so the
             // producer never waits on a load
-            const unsigned long long tgt = count_target(atom_add_release_u64(p.xcnt, 1ull), G);
+            const unsigned long long old = atom_add_release_u64(p.xcnt, 1ull);
+            const unsigned long long tgt = count_target(old, G);
+            sh.epoch = (unsigned)(old / (unsigned long long)G) + 1u;
             int spins = 0;
 #pragma unroll 1
             while (ld_acquire_u64(p.xcnt) < tgt) {
@@ -427,64 +518,44 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                     break;
                 }
             }
-            mbar_arrive(&sh.xready);
+            // the whole layer's x terms into shared memory, once
+            asm volatile("fence.proxy.async.global;" ::: "memory");   // published x terms -> bulk reads
+            const uint32_t ab = (uint32_t)KSH * atom, sb = (uint32_t)CHH * kSfChunk;
+            mbar_expect_tx(&sh.xfull, ab + sb);
+            bulk_copy(xs, p.xt, ab, &sh.xfull);
+            bulk_copy(xs + ab, p.xt + (size_t)KSH * atom, sb, &sh.xfull);
         }
         __syncwarp();   // lane 0 rejoins before the warp's collective instructions
         for (int i = te; i < p.H * M; i += kEpi)
             oacc[i] = 0.f;
         // h'-term rows past M * 8 feed MMA columns nobody reads: give them zero
         // codes and unit-range scales rather than whatever shared memory held
-        for (int i = te; i < 2 * kHTerm / 4; i += kEpi)
+        for (int i = te; i < 3 * kHTerm / 4; i += kEpi)
             reinterpret_cast<uint32_t*>(hterm)[i] = 0u;
+        mbar_wait(&sh.routed, 0, p.status);
+    } else {
         mbar_wait(&sh.routed, 0, p.status);
     }
 
     const int nu = sh.nu;
     const int U = nu * T1;
     // (products below stay under 2^31: U <= kMaxUnits * kMaxK / 64, G and H small)
-    const int u0 = (int)((unsigned)b * U / G), nun = (int)((unsigned)(b + 1) * U / G) - u0;
+    const Plan pl = make_plan(b, G, U, KSH, CHH, T2);
+    const int u0 = pl.u0, nun = pl.nun, nitem = pl.nitem;
     const int nact = U < G ? U : G;   // CTAs with units
-    const int nitem = 2 * nun;
     if (b == 0 && tid == 0 && p.nu_out)
         *p.nu_out = nu;
 
     if (warp == 0) {
         // ================================================================ producer
-        // Weights stream in item order.  A gate/up stage also carries the x terms
-        // of its k-steps; until they are published those two copies wait in a
-        // queue, served whenever the producer polls, so weights never wait.
+        // Weights stream in item order: every stage is weights only (the x terms
+        // and the h' terms are in shared memory), so nothing but ring space is
+        // ever waited for.
         RingTc ring_alloc;
         unsigned long long ends[kSlots];
         unsigned long long rel_end = 0;
         uint32_t c = 0, rel = 0;
         const uint64_t wpol = l2_evict_first();
-        uint32_t pq_off[kPend] = {}, pq_slot[kPend] = {};
-        int pq_ks[kPend] = {}, pq_steps[kPend] = {};
-        int pq_n = 0;
-        bool x_ok = false;
-        // the whole warp: once the x terms are all published (a non-blocking test),
-        // issue the queued copies
-        auto poll = [&]() {
-            if (!x_ok && __shfl_sync(0xffffffffu, mbar_test_wait(&sh.xready, 0) ? 1 : 0, 0)) {
-                __syncwarp();
-                asm volatile("fence.proxy.async.global;" ::: "memory");   // published x terms -> bulk reads
-                x_ok = true;
-            }
-            if (x_ok && pq_n > 0) {
-                const int qq = lane >> 1;
-                if (qq < pq_n) {
-                    const GuStage sg(pq_steps[qq], atom);
-                    if ((lane & 1) == 0)
-                        bulk_copy(ring + pq_off[qq], p.xt + (long long)pq_ks[qq] * atom, sg.bbytes,
-                                  &sh.full[pq_slot[qq]]);
-                    else
-                        bulk_copy(ring + pq_off[qq] + sg.bbytes,
-                                  p.xt + (long long)KSH * atom + (pq_ks[qq] >> 1) * kSfChunk, sg.sfbytes,
-                                  &sh.full[pq_slot[qq]]);
-                }
-                pq_n = 0;
-            }
-        };
         // the whole warp: claim ring bytes and a slot for a stage (stages retire in order)
         auto claim = [&](uint32_t size, uint32_t& off) -> uint32_t {
             unsigned long long end;
@@ -497,8 +568,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                     rel_end = ends[sl];
                     ++rel;
                 } else {
-                    poll();
-                    if (++spins > (1 << 22)) {
+                    if (++spins > (1 << 24)) {
                         if (lane == 0)
                             atomicExch(p.status, MOE_ERR_DEVICE_TIMEOUT);
                         break;
@@ -510,73 +580,43 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
             return slot;
         };
         for (int k = 0; k < nitem; ++k) {
-            bool down;
-            int i;
-            item_at(k, nun, down, i);
-            const int unit = u0 + i, s = unit / T1, t = unit % T1;
+            int kind, i;
+            item_of(pl, k, kind, i);
+            const bool piece = kind >= kGuPiece;
+            const int unit = piece ? pl.su : u0 + i, s = unit / T1, t = unit % T1;
             const int e = sh.unit_expert[s];
-            if (!down) {
+            if (kind == kGu || kind == kGuPiece) {
+                const int kA = piece ? pl.ks0 : 0, kB = piece ? pl.ks1 : KSH;
                 const uint8_t* a0 = p.gu + (long long)e * p.gu_expert + (long long)t * kRowTile * (p.H / 2);
                 const uint8_t* s0 = p.gu + (long long)e * p.gu_expert + (long long)(2 * p.I) * (p.H / 2) +
                                     (long long)t * CHH * kSfChunk;
-                for (int ks = 0; ks < KSH; ks += kGuSteps, ++c) {
-                    const int steps = KSH - ks < kGuSteps ? KSH - ks : kGuSteps;
-                    const GuStage sg(steps, atom);
+                for (int ks = kA; ks < kB; ks += kGuSteps, ++c) {
+                    const int steps = kB - ks < kGuSteps ? kB - ks : kGuSteps;
+                    const GuStage sg(steps);
                     uint32_t off;
                     const uint32_t slot = claim(sg.size, off);
                     if (lane == 0)
-                        mbar_expect_tx(&sh.full[slot], sg.abytes + sg.sfbytes + sg.bbytes + sg.sfbytes);
+                        mbar_expect_tx(&sh.full[slot], sg.abytes + sg.sfbytes);
                     __syncwarp();
                     uint8_t* st = ring + off;
-                    const uint8_t* src = nullptr;
-                    uint32_t dsto = 0, n = 0;
-                    switch (lane) {
-                    case 0: dsto = 0; src = a0 + (long long)ks * kTileA; n = sg.abytes; break;
-                    case 1: dsto = sg.sfa; src = s0 + (ks >> 1) * kSfChunk; n = sg.sfbytes; break;
-                    case 2: dsto = sg.b; src = p.xt + (long long)ks * atom; n = x_ok ? sg.bbytes : 0u; break;
-                    case 3:
-                        dsto = sg.sfb;
-                        src = p.xt + (long long)KSH * atom + (ks >> 1) * kSfChunk;
-                        n = x_ok ? sg.sfbytes : 0u;
-                        break;
-                    default: break;
-                    }
-                    if (n) {
-                        if (lane < 2)   // weights: read once per call
-                            bulk_copy_hint(st + dsto, src, n, &sh.full[slot], wpol);
-                        else
-                            bulk_copy(st + dsto, src, n, &sh.full[slot]);
-                    }
-                    if (!x_ok) {
-                        if (pq_n == kPend) {   // full: wait for the x terms
-#pragma unroll 1
-                            for (int w = 0; w < (1 << 22) && pq_n == kPend; ++w)
-                                poll();
-                            if (pq_n == kPend) {
-                                if (lane == 0)
-                                    atomicExch(p.status, MOE_ERR_DEVICE_TIMEOUT);
-                                pq_n = 0;   // give up (those stages will time out)
-                            }
-                        }
-                        pq_off[pq_n] = off + sg.b;
-                        pq_slot[pq_n] = slot;
-                        pq_ks[pq_n] = ks;
-                        pq_steps[pq_n] = steps;
-                        ++pq_n;
-                    }
-                    poll();
+                    if (lane == 0)   // weights: read once per call
+                        bulk_copy_hint(st, a0 + (long long)ks * kTileA, sg.abytes, &sh.full[slot], wpol);
+                    else if (lane == 1)
+                        bulk_copy_hint(st + sg.sfa, s0 + (ks >> 1) * kSfChunk, sg.sfbytes, &sh.full[slot], wpol);
                 }
             } else {
-                // down rows of all tiles, k-step t of K = I (h rows 64t .. 64t+63)
+                // down rows of tiles [tA, tB), k-step t of K = I (h rows 64t .. 64t+63)
+                const int tA = piece ? pl.ta : 0, tB = piece ? pl.tb : T2;
                 const uint8_t* d0 = p.dn + (long long)e * p.dn_expert;
                 const uint8_t* sd0 = d0 + (long long)p.H * (p.I / 2) + (long long)(t >> 1) * kSfChunk;
-                for (int g = 0; g < NG; ++g) {
-                    const int ta = g * TG, tb = ta + TG < T2 ? ta + TG : T2;
-                    for (int t2 = ta; t2 < tb; t2 += kDnStageTiles, ++c) {
-                        const int n = tb - t2 < kDnStageTiles ? tb - t2 : kDnStageTiles;
+                for (int ga = tA; ga < tB; ga += TG) {
+                    const int gb = ga + TG < tB ? ga + TG : tB;
+                    for (int t2 = ga; t2 < gb; t2 += kDnStageTiles, ++c) {
+                        const int n = gb - t2 < kDnStageTiles ? gb - t2 : kDnStageTiles;
                         uint32_t off;
                         const uint32_t slot = claim(dn_stage_size(n), off);
                         uint32_t bytes = 0;
+#pragma unroll 1
                         for (int j = 0; j < n; ++j) {
                             const int R2 = p.H - (t2 + j) * kRowTile < kRowTile ? p.H - (t2 + j) * kRowTile : kRowTile;
                             bytes += (uint32_t)R2 * 32 + kSfChunk;
@@ -591,8 +631,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                             const int R2 = p.H - tt * kRowTile < kRowTile ? p.H - tt * kRowTile : kRowTile;
                             if (lane < 16)
                                 bulk_copy_hint(st + j * kTileA,
-                                          d0 + (long long)tt * kRowTile * (p.I / 2) + (long long)t * R2 * 32,
-                                          (uint32_t)R2 * 32, &sh.full[slot], wpol);
+                                               d0 + (long long)tt * kRowTile * (p.I / 2) + (long long)t * R2 * 32,
+                                               (uint32_t)R2 * 32, &sh.full[slot], wpol);
                             else
                                 bulk_copy_hint(st + n * kTileA + j * kSfChunk, sd0 + (long long)tt * CHI * kSfChunk,
                                                kSfChunk, &sh.full[slot], wpol);
@@ -601,11 +641,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                 }
             }
         }
-#pragma unroll 1
-        for (int w = 0; w < (1 << 22) && pq_n > 0; ++w)
-            poll();
-        if (pq_n > 0 && lane == 0)
-            atomicExch(p.status, MOE_ERR_DEVICE_TIMEOUT);
     } else if (warp == 1 || warp == kMmaWarpB) {
         // ================================================================ MMA issuers
         // Issuing a tcgen05 instruction costs one thread ~60-80 cycles.  Issuer A
@@ -620,65 +655,79 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
             const uint32_t myset = tmem + kSfCol + role * 2 * kSfSet;
             uint32_t c = 0, kk = 0, mine = 0;
             for (int k = 0; k < nitem; ++k) {
-                bool down;
-                int i;
-                item_at(k, nun, down, i);
-                const int t = (u0 + i) % T1;
-                if (!down) {
-                    if (role == 1) {   // issuer A's: only keep the ring placement in step
-                        for (int ks = 0; ks < KSH; ks += kGuSteps, ++c) {
-                            const int steps = KSH - ks < kGuSteps ? KSH - ks : kGuSteps;
-                            unsigned long long end;
-                            ring_alloc.place(GuStage(steps, atom).size, ring_cap, &end);
-                        }
-                        continue;
-                    }
-                    const uint32_t buf = i & 1;
-                    if (i >= 2)
-                        mbar_wait(&sh.acce[buf], ((i >> 1) - 1) & 1, p.status);
+                int kind, i;
+                item_of(pl, k, kind, i);
+                const bool piece = kind >= kGuPiece;
+                const int t = (piece ? pl.su : u0 + i) % T1;
+                if (kind == kGu || kind == kGuPiece) {
+                    const int gi = piece ? 0 : i + pl.piece;   // gate/up accumulator use
+                    const int kA = piece ? pl.ks0 : 0, kB = piece ? pl.ks1 : KSH;
+                    // stages alternate between the issuers, each into its own half
+                    const uint32_t buf = gi & 1;
+                    if (gi == 0)
+                        mbar_wait(&sh.xfull, 0, p.status);   // the layer's x terms are in
+                    if (gi >= 2)
+                        mbar_wait(&sh.acce[buf], ((gi >> 1) - 1) & 1, p.status);
                     tc_fence_after();
-                    const uint32_t d = tmem + kGuCol + buf * 32;
+                    const uint32_t d = tmem + kGuCol + buf * kGuBuf + role * 32;
                     bool first = true;
-                    for (int ks = 0; ks < KSH; ks += kGuSteps, ++c) {
-                        const int steps = KSH - ks < kGuSteps ? KSH - ks : kGuSteps;
-                        const GuStage sg(steps, atom);
+                    int jst = 0;
+                    for (int ks = kA; ks < kB; ks += kGuSteps, ++c, ++jst) {
+                        const int steps = kB - ks < kGuSteps ? kB - ks : kGuSteps;
+                        const GuStage sg(steps);
                         unsigned long long end;
                         const uint32_t st = su32(ring) + ring_alloc.place(sg.size, ring_cap, &end);
+                        if ((jst & 1) != role)
+                            continue;   // the other issuer's stage
                         const uint32_t slot = c % kSlots;
                         mbar_wait(&sh.full[slot], (c / kSlots) & 1, p.status);
                         tc_fence_after();
                         const uint32_t set = myset + (mine++ & 1) * kSfSet;
                         const int chunks = (steps + 1) >> 1;
-#pragma unroll 1
-                        for (int ch = 0; ch < chunks; ++ch) {
-                            tc_cp_sf(set + 4 * ch, st + sg.sfa + ch * kSfChunk);
-                            tc_cp_sf(set + kSfSet / 2 + 4 * ch, st + sg.sfb + ch * kSfChunk);
-                        }
-#pragma unroll 1
-                        for (int j = 0; j < steps; ++j) {
-                            const uint32_t id = (uint32_t)(2 * (j & 1));
-                            tc_mma_mxf4(d, smem_desc(st + j * kTileA, 128, 256), smem_desc(st + sg.b + j * atom, 128, 256),
-                                        idesc | (id << 4) | (id << 29), set + 4 * (j >> 1),
-                                        set + kSfSet / 2 + 4 * (j >> 1), first ? 0u : 1u);
-                            first = false;
-                        }
+                        const uint32_t xb = su32(xs) + ks * atom;                               // B: x terms
+                        const uint32_t xsf = su32(xs) + KSH * atom + (ks >> 1) * kSfChunk;     // and their scales
+                        // (the hot loop: unrolled, descriptors stepped by adding the byte
+                        // offset / 16 to the start-address field)
+#pragma unroll
+                        for (int ch = 0; ch < (kGuSteps + 1) / 2; ++ch)
+                            if (ch < chunks) {
+                                tc_cp_sf(set + 4 * ch, st + sg.sfa + ch * kSfChunk);
+                                tc_cp_sf(set + kSfSet / 2 + 4 * ch, xsf + ch * kSfChunk);
+                            }
+                        const uint64_t da = smem_desc(st, 128, 256), db = smem_desc(xb, 128, 256);
+                        const uint32_t id_odd = (2u << 4) | (2u << 29);
+#pragma unroll
+                        for (int j = 0; j < kGuSteps; ++j)
+                            if (j < steps) {
+                                tc_mma_mxf4(d, da + (uint64_t)(j * (kTileA >> 4)), db + (uint64_t)(j * (atom >> 4)),
+                                            idesc | ((j & 1) ? id_odd : 0u), set + 4 * (j >> 1),
+                                            set + kSfSet / 2 + 4 * (j >> 1), (first && j == 0) ? 0u : 1u);
+                            }
+                        first = false;
                         tc_commit(&sh.empty[slot]);
                     }
-                    tc_commit(&sh.accf[buf]);
+                    tc_commit(&sh.accf[buf]);   // both issuers
                 } else {
-                    const uint32_t hb = su32(hterm + (i & 1) * kHTerm);
-                    mbar_wait(&sh.hbar[i & 1], (i >> 1) & 1, p.status);
+                    uint32_t hb;
+                    if (piece) {
+                        hb = su32(hterm + 2 * kHTerm);
+                        mbar_wait(&sh.hsfull, 0, p.status);
+                    } else {
+                        hb = su32(hterm + (i & 1) * kHTerm);
+                        mbar_wait(&sh.hbar[i & 1], (i >> 1) & 1, p.status);
+                    }
                     tc_fence_after();
                     const uint32_t aid = (uint32_t)(2 * (t & 1));   // A scale bytes of k-step t in its chunk
-                    int jst = 0;                                     // down stage of this unit
-                    for (int g = 0; g < NG; ++g, ++kk) {
+                    const int tA = piece ? pl.ta : 0, tB = piece ? pl.tb : T2;
+                    int jst = 0;                                     // down stage of this item
+                    for (int ga = tA; ga < tB; ga += TG, ++kk) {
+                        const int gb = ga + TG < tB ? ga + TG : tB;
                         if (kk >= 2)
                             mbar_wait(&sh.dne[kk & 1], ((kk >> 1) - 1) & 1, p.status);
                         tc_fence_after();
                         const uint32_t dreg = tmem + kDnCol + (kk & 1) * kDnRegion;
-                        const int ta = g * TG, tb = ta + TG < T2 ? ta + TG : T2;
-                        for (int t2 = ta; t2 < tb; t2 += kDnStageTiles, ++c, ++jst) {
-                            const int n = tb - t2 < kDnStageTiles ? tb - t2 : kDnStageTiles;
+                        for (int t2 = ga; t2 < gb; t2 += kDnStageTiles, ++c, ++jst) {
+                            const int n = gb - t2 < kDnStageTiles ? gb - t2 : kDnStageTiles;
                             unsigned long long end;
                             const uint32_t st = su32(ring) + ring_alloc.place(dn_stage_size(n), ring_cap, &end);
                             if ((jst & 1) != role)
@@ -688,13 +737,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                             tc_fence_after();
                             const uint32_t set = myset + (mine++ & 1) * kSfSet;
                             tc_cp_sf(set, hb + 1024);
-#pragma unroll 1
-                            for (int j = 0; j < n; ++j)
-                                tc_cp_sf(set + 4 + 4 * j, st + n * kTileA + j * kSfChunk);
-#pragma unroll 1
-                            for (int j = 0; j < n; ++j)
-                                tc_mma_mxf4(dreg + (t2 - ta + j) * nrows, smem_desc(st + j * kTileA, 128, 256),
-                                            smem_desc(hb, 128, 256), idesc | (aid << 29), set + 4 + 4 * j, set, 0u);
+#pragma unroll
+                            for (int j = 0; j < kDnStageTiles; ++j)
+                                if (j < n)
+                                    tc_cp_sf(set + 4 + 4 * j, st + n * kTileA + j * kSfChunk);
+                            const uint64_t da = smem_desc(st, 128, 256), db = smem_desc(hb, 128, 256);
+                            const uint32_t dcol = dreg + (t2 - ga) * nrows;
+#pragma unroll
+                            for (int j = 0; j < kDnStageTiles; ++j)
+                                if (j < n)
+                                    tc_mma_mxf4(dcol + j * nrows, da + (uint64_t)(j * (kTileA >> 4)), db,
+                                                idesc | (aid << 29), set + 4 + 4 * j, set, 0u);
                             tc_commit(&sh.empty[slot]);
                         }
                         tc_commit(&sh.dnf[kk & 1]);   // both issuers: the group's region is full
@@ -702,19 +755,119 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                 }
             }
         }
+    } else if (warp == kCombineWarp) {
+        // ================================================================ combiner
+        if (pl.piece) {
+            // the split unit's h' for this CTA's down tiles: wait for every piece's
+            // partial sums (one flag per lane), add them in piece order, SwiGLU,
+            // MX terms (lane = h row within each of the two 32-row blocks)
+            const int s = pl.su / T1, t = pl.su % T1, e = sh.unit_expert[s];
+            // the biases first: HBM is busy with the weight stream, so their
+            // latency overlaps the wait for the other pieces
+            float bg[2] = {0.f, 0.f}, bu[2] = {0.f, 0.f};
+            if (p.gu_bias)
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb) {
+                    const int hrow = 64 * t + 32 * kb + lane;
+                    bg[kb] = bf16f(__ldg(p.gu_bias + (size_t)e * 2 * p.I + hrow));
+                    bu[kb] = bf16f(__ldg(p.gu_bias + (size_t)e * 2 * p.I + p.I + hrow));
+                }
+            mbar_wait(&sh.xfull, 0, p.status);   // (orders the call tag written before it)
+            const unsigned tag = sh.epoch;
+            const int b0 = pl.sj * pl.S;   // the CTA of piece 0
+            int spins = 0;
+            bool all = false;
+#pragma unroll 1
+            while (!all && ++spins < (1 << 24))
+                all = __all_sync(0xffffffffu, lane >= pl.S || ld_acquire_u32(p.pflag + b0 + lane) == tag);
+            if (!all && lane == 0)
+                atomicExch(p.status, MOE_ERR_DEVICE_TIMEOUT);
+            // gate (rows r) and up (rows 64 + r) sums of both 32-row blocks, every
+            // piece's loads in flight together, added in piece order
+            float g[2][kMaxTokens] = {}, u[2][kMaxTokens] = {};
+            for (int p0 = 0; p0 < pl.S; p0 += 4) {
+                float4 v[4][4];
+#pragma unroll
+                for (int z = 0; z < 4; ++z)
+                    if (p0 + z < pl.S) {
+                        const float4* src = reinterpret_cast<const float4*>(p.gpart) + (size_t)(b0 + p0 + z) * kRowTile;
+#pragma unroll
+                        for (int kb = 0; kb < 2; ++kb) {
+                            v[z][2 * kb] = __ldcg(src + 32 * kb + lane);
+                            v[z][2 * kb + 1] = __ldcg(src + 64 + 32 * kb + lane);
+                        }
+                    }
+#pragma unroll
+                for (int z = 0; z < 4; ++z)
+                    if (p0 + z < pl.S)
+#pragma unroll
+                        for (int kb = 0; kb < 2; ++kb) {
+                            const float4 gv = v[z][2 * kb], uv = v[z][2 * kb + 1];
+                            g[kb][0] += gv.x; g[kb][1] += gv.y; g[kb][2] += gv.z; g[kb][3] += gv.w;
+                            u[kb][0] += uv.x; u[kb][1] += uv.y; u[kb][2] += uv.z; u[kb][3] += uv.w;
+                        }
+            }
+            uint8_t* hb = hterm + 2 * kHTerm;
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+                float hv[kMaxTokens];
+#pragma unroll
+                for (int m = 0; m < kMaxTokens; ++m) {
+                    const float gg = g[kb][m] + bg[kb];
+                    hv[m] = m < M ? sh.wslot[s][m] * (gg / (1.0f + expf(-gg))) * (u[kb][m] + bu[kb]) : 0.f;
+                }
+                switch (M) {
+                case 1: warp_terms_rows<1>(hv, 0, kb, hb, hb + 1024, atom, lane); break;
+                case 2: warp_terms_rows<2>(hv, 0, kb, hb, hb + 1024, atom, lane); break;
+                case 3: warp_terms_rows<3>(hv, 0, kb, hb, hb + 1024, atom, lane); break;
+                default: warp_terms_rows<4>(hv, 0, kb, hb, hb + 1024, atom, lane); break;
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sh.hsfull);
+        }
+
     } else {
         // ================================================================ epilogue warps
         const int te = tid - 64, q = warp & 3;   // q: the lane quarter this warp may read
+        // SwiGLU of 64 h rows from the gate sums (lane quarters 0, 1) and up sums
+        // (2, 3) of token m, times the routing weight, into MX terms at dst: the up
+        // sums go through shared memory, then warps q < 2 each write one
+        // 32-element block (k-block q of the down k-step)
+        auto swiglu_terms = [&](const float (&sm)[kMaxTokens], int s, float bg, float bu, uint8_t* dst) {
+            if (q >= 2)
+                xch[(q - 2) * 32 + lane] = make_float4(sm[0], sm[1], sm[2], sm[3]);
+            epi_barrier();
+            if (q < 2) {
+                const float4 u4 = xch[q * 32 + lane];
+                const float us[kMaxTokens] = {u4.x, u4.y, u4.z, u4.w};
+                float hv[kMaxTokens];
+#pragma unroll
+                for (int m = 0; m < kMaxTokens; ++m) {
+                    const float g = sm[m] + bg;
+                    hv[m] = m < M ? sh.wslot[s][m] * (g / (1.0f + expf(-g))) * (us[m] + bu) : 0.f;
+                }
+                switch (M) {   // one copy of the code runs
+                case 1: warp_terms_rows<1>(hv, 0, q, dst, dst + 1024, atom, lane); break;
+                case 2: warp_terms_rows<2>(hv, 0, q, dst, dst + 1024, atom, lane); break;
+                case 3: warp_terms_rows<3>(hv, 0, q, dst, dst + 1024, atom, lane); break;
+                default: warp_terms_rows<4>(hv, 0, q, dst, dst + 1024, atom, lane); break;
+                }
+            }
+        };
         uint32_t kk = 0;
         for (int k = 0; k < nitem; ++k) {
-            bool down;
-            int i;
-            item_at(k, nun, down, i);
-            const int unit = u0 + i, s = unit / T1, t = unit % T1;
-            if (!down) {
+            int kind, i;
+            item_of(pl, k, kind, i);
+            const bool piece = kind >= kGuPiece;
+            const int unit = piece ? pl.su : u0 + i, s = unit / T1, t = unit % T1;
+            if (kind == kGu || kind == kGuPiece) {
                 // ---- gate (rows 0..63) and up (rows 64..127) sums of 64 h rows; the
                 // biases are loaded before the accumulator is waited for
-                const uint32_t buf = i & 1;
+                const int gi = piece ? 0 : i + pl.piece;
+                const uint32_t buf = gi & 1;
                 const int hrow = 64 * t + 32 * (q & 1) + lane;
                 const int e = sh.unit_expert[s];
                 float bg = 0.f, bu = 0.f;
@@ -722,21 +875,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                     bg = bf16f(__ldg(p.gu_bias + (size_t)e * 2 * p.I + hrow));
                     bu = bf16f(__ldg(p.gu_bias + (size_t)e * 2 * p.I + p.I + hrow));
                 }
-                mbar_wait(&sh.accf[buf], (i >> 1) & 1, p.status);
+                mbar_wait(&sh.accf[buf], (gi >> 1) & 1, p.status);
                 tc_fence_after();
-                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + kGuCol + buf * 32;
+                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + kGuCol + buf * kGuBuf;
+                const int kA = piece ? pl.ks0 : 0, kB = piece ? pl.ks1 : KSH;
+                const bool two = kB - kA > kGuSteps;   // issuer B wrote its half too
                 float sm[kMaxTokens] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int h16 = 0; h16 < 32; h16 += 16) {
                     if (h16 < nrows) {
-                        float d0[16];
+                        float d0[16], d1[16];
                         tc_ld16(taddr + h16, d0);
+                        if (two)
+                            tc_ld16(taddr + 32 + h16, d1);
                         tc_wait_ld();
 #pragma unroll
                         for (int col = 0; col < 16; ++col) {
                             const int m = (h16 + col) / kTerms;   // compile-time after unrolling
                             if (m < M)
-                                sm[m] += d0[col];
+                                sm[m] += two ? d0[col] + d1[col] : d0[col];
                         }
                     }
                 }
@@ -744,46 +901,38 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&sh.acce[buf]);
-                if (q >= 2)
-                    xch[(q - 2) * 32 + lane] = make_float4(sm[0], sm[1], sm[2], sm[3]);
-                epi_barrier();
-                if (q < 2) {
-                    // h'_m = w_m silu(gate + b) (up + b) for h row 64t + 32q + lane: one
-                    // 32-element block (k-block q of the down k-step t)
-                    const float4 u4 = xch[q * 32 + lane];
-                    const float us[kMaxTokens] = {u4.x, u4.y, u4.z, u4.w};
-                    float hv[kMaxTokens];
-#pragma unroll
-                    for (int m = 0; m < kMaxTokens; ++m) {
-                        const float g = sm[m] + bg;
-                        hv[m] = m < M ? sh.wslot[s][m] * (g / (1.0f + expf(-g))) * (us[m] + bu) : 0.f;
-                    }
-                    uint8_t* hb = hterm + buf * kHTerm;
-                    switch (M) {   // one copy of the code runs
-                    case 1: warp_terms_rows<1>(hv, 0, q, hb, hb + 1024, atom, lane); break;
-                    case 2: warp_terms_rows<2>(hv, 0, q, hb, hb + 1024, atom, lane); break;
-                    case 3: warp_terms_rows<3>(hv, 0, q, hb, hb + 1024, atom, lane); break;
-                    default: warp_terms_rows<4>(hv, 0, q, hb, hb + 1024, atom, lane); break;
-                    }
-                    fence_proxy_async_smem();
+                if (!piece) {
+                    uint8_t* hb = hterm + (i & 1) * kHTerm;
+                    swiglu_terms(sm, s, bg, bu, hb);
+                    if (q < 2)
+                        fence_proxy_async_smem();
+                    epi_barrier();
+                    if (te == 0)
+                        mbar_arrive(&sh.hbar[i & 1]);
+                    continue;
                 }
+                // ---- a piece of a split unit: publish its partial sums (warp 7
+                // combines them)
+                float4* gp = reinterpret_cast<float4*>(p.gpart) + (size_t)b * kRowTile;
+                gp[32 * q + lane] = make_float4(sm[0], sm[1], sm[2], sm[3]);
                 epi_barrier();
                 if (te == 0)
-                    mbar_arrive(&sh.hbar[buf]);
+                    st_release_u32(p.pflag + b, sh.epoch);
             } else {
-                // ---- down products of unit i into the CTA's output copy
-                for (int g = 0; g < NG; ++g, ++kk) {
+                // ---- down products of tiles [tA, tB) into the CTA's output copy
+                const int tA = piece ? pl.ta : 0, tB = piece ? pl.tb : T2;
+                for (int ga = tA; ga < tB; ga += TG, ++kk) {
+                    const int gb = ga + TG < tB ? ga + TG : tB;
                     mbar_wait(&sh.dnf[kk & 1], (kk >> 1) & 1, p.status);
                     tc_fence_after();
                     const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + kDnCol + (kk & 1) * kDnRegion;
-                    const int ta = g * TG, tb = ta + TG < T2 ? ta + TG : T2;
-                    for (int t2 = ta; t2 < tb; ++t2) {
+                    for (int t2 = ga; t2 < gb; ++t2) {
                         float sm[kMaxTokens] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                         for (int h16 = 0; h16 < 32; h16 += 16) {
                             if (h16 < nrows) {
                                 float d0[16];
-                                tc_ld16(taddr + (t2 - ta) * nrows + h16, d0);
+                                tc_ld16(taddr + (t2 - ga) * nrows + h16, d0);
                                 tc_wait_ld();
 #pragma unroll
                                 for (int col = 0; col < 16; ++col) {
@@ -827,24 +976,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
         }
     }
 
-    // ---- this CTA's output rows [r0, r1): their bias terms sum_s w_s b_s and the
-    // residual are loaded before the grid barrier
-    const int r0 = (int)((unsigned)b * p.H / G), r1 = (int)((unsigned)(b + 1) * p.H / G);
-    const int nr = r1 - r0;
-    float bsum[kMaxTokens] = {0.f, 0.f, 0.f, 0.f}, rv[kMaxTokens] = {0.f, 0.f, 0.f, 0.f};
-    if (tid < nr) {
-        const int row = r0 + tid;
-        if (p.dn_bias)
-            for (int s2 = 0; s2 < nu; ++s2) {
-                const float bd = bf16f(__ldg(p.dn_bias + (size_t)sh.unit_expert[s2] * p.H + row));
+    // ---- this CTA's slice of the output: float4s [f0, f1) of a copy [H][V] (4 / V
+    // rows x V tokens each); the residual and the bias terms sum_s w_s b_s of its
+    // elements are loaded before the grid barrier
+    const int U4 = p.H * V / 4;
+    const int f0 = (int)((unsigned)b * U4 / G), f1 = (int)((unsigned)(b + 1) * U4 / G), nf = f1 - f0;
+    float bsum[4] = {0.f, 0.f, 0.f, 0.f}, rv[4] = {0.f, 0.f, 0.f, 0.f};
+    if (tid < nf) {
 #pragma unroll
-                for (int m = 0; m < kMaxTokens; ++m)
-                    bsum[m] = fmaf(sh.wslot[s2][m], bd, bsum[m]);
+        for (int z = 0; z < 4; ++z) {
+            const int el = (f0 + tid) * 4 + z, row = el / V, m = el - row * V;
+            if (m < M) {
+                if (p.dn_bias)
+                    for (int s2 = 0; s2 < nu; ++s2)
+                        bsum[z] = fmaf(sh.wslot[s2][m], bf16f(__ldg(p.dn_bias + (size_t)sh.unit_expert[s2] * p.H + row)),
+                                       bsum[z]);
+                rv[z] = bf16f(__ldcg(p.resid + (size_t)m * p.H + row));
             }
-#pragma unroll
-        for (int m = 0; m < kMaxTokens; ++m)
-            if (m < M)
-                rv[m] = bf16f(__ldcg(p.resid + (size_t)m * p.H + row));
+        }
     }
 
     // ---- grid barrier: every CTA's output copy is stored (every CTA counts itself in)
@@ -863,56 +1012,44 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
     }
     __syncthreads();
 
-    // ---- output rows [r0, r1): the active CTAs' copies summed in CTA order, split
-    // over P thread groups (group g takes CTAs g, g + P, ...), then the groups in order
-    if (nr > 0) {
-        float4* red = reinterpret_cast<float4*>(ring);   // [P][nr]; the ring is idle now
-        const int P = kThreadsTc / nr < 1 ? 1 : kThreadsTc / nr;
-        if (tid < P * nr) {
-            const int j = tid % nr, g = tid / nr;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            // group g's CTAs: with U >= G every CTA, else the owners of the U units
+    // ---- the slice: the active CTAs' copies summed in CTA order, split over P
+    // thread groups (group g takes CTAs g, g + P, ...; all its loads in flight at
+    // once), then the groups in order
+    if (nf > 0) {
+        float4* red = reinterpret_cast<float4*>(ring);   // [P][nf]; the ring is idle now
+        const int P = kThreadsTc / nf < 1 ? 1 : kThreadsTc / nf;
+        if (tid < P * nf) {
+            const int j = tid % nf, g = tid / nf;
             auto cta_of = [&](int cc) { return U < G ? (int)(((unsigned)(cc + 1) * G + U - 1) / U) - 1 : cc; };
-            // the copies' rows are V floats; one loop per V, so one copy of the code runs
-            auto sum_rows = [&](auto vtag) {
-                using VT = decltype(vtag);
-                constexpr int VW = sizeof(VT) / sizeof(float);
-                for (int c0 = g; c0 < nact; c0 += 8 * P) {
-                    VT a[8];
+            const float4* part = reinterpret_cast<const float4*>(p.part);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int c0 = g; c0 < nact; c0 += 16 * P) {
+                float4 a[16];
 #pragma unroll
-                    for (int z = 0; z < 8; ++z)
-                        if (c0 + z * P < nact)
-                            a[z] = __ldcg(reinterpret_cast<const VT*>(p.part + ((size_t)cta_of(c0 + z * P) * p.H + r0 + j) * VW));
+                for (int z = 0; z < 16; ++z)
+                    if (c0 + z * P < nact)
+                        a[z] = __ldcg(part + (size_t)cta_of(c0 + z * P) * U4 + f0 + j);
 #pragma unroll
-                    for (int z = 0; z < 8; ++z)
-                        if (c0 + z * P < nact) {
-                            const float* f = reinterpret_cast<const float*>(&a[z]);
-                            acc.x += f[0];
-                            if (VW > 1) acc.y += f[VW > 1 ? 1 : 0];
-                            if (VW > 2) { acc.z += f[VW > 2 ? 2 : 0]; acc.w += f[VW > 2 ? 3 : 0]; }
-                        }
-                }
-            };
-            if (V == 1)
-                sum_rows(0.f);
-            else if (V == 2)
-                sum_rows(make_float2(0.f, 0.f));
-            else
-                sum_rows(make_float4(0.f, 0.f, 0.f, 0.f));
-            red[g * nr + j] = acc;
+                for (int z = 0; z < 16; ++z)
+                    if (c0 + z * P < nact) {
+                        acc.x += a[z].x; acc.y += a[z].y; acc.z += a[z].z; acc.w += a[z].w;
+                    }
+            }
+            red[g * nf + j] = acc;
         }
         __syncthreads();
-        if (tid < nr) {
-            const int row = r0 + tid;
-            float acc[kMaxTokens] = {0.f, 0.f, 0.f, 0.f};
+        if (tid < nf) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
             for (int g = 0; g < P; ++g) {
-                const float4 a = red[g * nr + tid];
+                const float4 a = red[g * nf + tid];
                 acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
             }
 #pragma unroll
-            for (int m = 0; m < kMaxTokens; ++m)
+            for (int z = 0; z < 4; ++z) {
+                const int el = (f0 + tid) * 4 + z, row = el / V, m = el - row * V;
                 if (m < M)
-                    p.resid[(size_t)m * p.H + row] = f2bf16_rne(rv[m] + (acc[m] + bsum[m]));
+                    p.resid[(size_t)m * p.H + row] = f2bf16_rne(rv[z] + (acc[z] + bsum[z]));
+            }
         }
     }
 

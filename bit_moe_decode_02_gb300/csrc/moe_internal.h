@@ -189,6 +189,8 @@ struct DecodeTcParams {
     uint16_t* resid;            // [M][H] bf16 in/out
     float* part;                // [G][H][4] each CTA's fp32 copy of the expert output
     uint8_t* xt;                // x terms of the layer: [H/64][N rows x 32 B][ceil(H/128)][512]
+    float* gpart;               // [G][128][4] gate/up partial sums of split-unit pieces
+    unsigned* pflag;            // [G] piece partial published: the call's tag
     unsigned long long* xcnt;   // [1] x-term publications, G per call (only grows)
     unsigned long long* done;   // [1] output copies stored, G per call (only grows)
     int* status;
@@ -197,6 +199,7 @@ struct DecodeTcParams {
     int smem_bytes;             // dynamic shared memory of the layer kernel
 };
 
+constexpr int kHTermBytes = 1024 + kSfChunk;   // one k-step of activation terms + its scale chunk
 inline size_t tc_terms_bytes(int K) { return (size_t)(K / 64) * 1024 + (size_t)ceil_div(K, 128) * kSfChunk; }
 inline size_t tc_part_bytes(int G, int H) { return (size_t)G * H * 4 * sizeof(float); }
 constexpr int kTcCounterWords = 2;   // xcnt, done (64-bit)
