@@ -27,9 +27,18 @@
  *                  `group` consecutive elements along K.  Scales fp16
  *                  [N][K/group].
  *
- * Precision: x, r and out are bfloat16; routing weights, gate_up outputs, h
- * and down outputs are fp32 and never rounded to 16 bits; dot products are
- * accumulated in fp32.  Denormal scales are kept (no flush to zero).
+ * Precision: x, r and out are bfloat16; routing weights are fp32; dot
+ * products are accumulated in fp32.  Denormal scales are kept (no flush to
+ * zero).  How the activations reach the multiplier depends on the path:
+ *   - MXFP4, M <= 4 (tensor cores, kind::mxf4): x and h' = w h enter as sums
+ *     of 8 MXFP4 vectors (term j of a 32-element block has the shared
+ *     exponent X0 - 2j, X0 the OCP MX exponent of the block; each term takes
+ *     the nearest-even E2M1 codes of what the earlier ones left), within
+ *     2^-15 of each block's largest magnitude;
+ *   - MXFP4, M > 4 (batched grouped GEMMs): x and h are quantised to one
+ *     MXFP4 vector each (OCP MX v1.0, nearest even);
+ *   - int4: x enters as f16 after an exact power-of-two rescale, h as f16
+ *     hi + lo (about 22 bits).
  *
  * Conventions:
  *   - Every call returns a moe_status (0 = MOE_OK).  Arguments are checked
@@ -49,11 +58,11 @@
  *   - Failures detected on the device (a bounded wait that gave up, an index
  *     out of range) set the handle's status word; read it with
  *     moe_get_status().  Device code never traps.
- *   - A layer runs as one persistent launch with one CTA per SM whose CTAs
- *     wait for one another (the down GEMV of an expert starts once every CTA
- *     has finished that expert's gate_up rows).  Work that other streams run
- *     at the same time can delay it; each wait gives up after about a second
- *     and reports MOE_ERR_DEVICE_TIMEOUT instead of hanging.
+ *   - A decode layer runs as one persistent launch with one CTA per SM whose
+ *     CTAs wait for one another (a grid barrier before the output is summed;
+ *     the pieces of a split unit exchange partial sums).  Work that other
+ *     streams run at the same time can delay it; each wait gives up after
+ *     about a second and reports MOE_ERR_DEVICE_TIMEOUT instead of hanging.
  */
 #ifndef MOE_H
 #define MOE_H
