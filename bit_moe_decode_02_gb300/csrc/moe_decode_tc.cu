@@ -354,6 +354,8 @@ __device__ __forceinline__ float row_inv_rms(const uint16_t* row, int n, int lan
     return 1.0f / sqrtf(a / (float)n + 1e-6f);
 }
 
+constexpr int kFinSlots = 64;   // output float4s of a CTA's slice whose final terms are prefetched
+
 struct TcSmem {
     uint64_t full[kSlots], empty[kSlots];
     uint64_t accf[2], acce[2];   // gate/up accumulator buffers: full / drained
@@ -369,6 +371,7 @@ struct TcSmem {
     int unit_expert[kMaxUnits];
     unsigned char unit_of[kMaxExperts];
     float wslot[kMaxUnits][kMaxTokens];   // routing weight of token m for expert slot s (0 if not chosen)
+    float fin[kFinSlots][4];              // r + sum_s w_s b_s of the slice's elements (loaded before the grid barrier)
 };
 
 __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTcParams p)
@@ -981,20 +984,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
     // elements are loaded before the grid barrier
     const int U4 = p.H * V / 4;
     const int f0 = (int)((unsigned)b * U4 / G), f1 = (int)((unsigned)(b + 1) * U4 / G), nf = f1 - f0;
-    float bsum[4] = {0.f, 0.f, 0.f, 0.f}, rv[4] = {0.f, 0.f, 0.f, 0.f};
-    if (tid < nf) {
-#pragma unroll
-        for (int z = 0; z < 4; ++z) {
-            const int el = (f0 + tid) * 4 + z, row = el / V, m = el - row * V;
-            if (m < M) {
-                if (p.dn_bias)
-                    for (int s2 = 0; s2 < nu; ++s2)
-                        bsum[z] = fmaf(sh.wslot[s2][m], bf16f(__ldg(p.dn_bias + (size_t)sh.unit_expert[s2] * p.H + row)),
-                                       bsum[z]);
-                rv[z] = bf16f(__ldcg(p.resid + (size_t)m * p.H + row));
-            }
+    // r + sum_s w_s b_s of element z of the slice's float4 j
+    auto fin_term = [&](int j, int z) -> float {
+        const int el = (f0 + j) * 4 + z, row = el / V, m = el - row * V;
+        float v = 0.f;
+        if (m < M) {
+            if (p.dn_bias)
+                for (int s2 = 0; s2 < nu; ++s2)
+                    v = fmaf(sh.wslot[s2][m], bf16f(__ldg(p.dn_bias + (size_t)sh.unit_expert[s2] * p.H + row)), v);
+            v += bf16f(__ldcg(p.resid + (size_t)m * p.H + row));
         }
-    }
+        return v;
+    };
+    if (tid < nf && tid < kFinSlots)
+#pragma unroll
+        for (int z = 0; z < 4; ++z)
+            sh.fin[tid][z] = fin_term(tid, z);
 
     // ---- grid barrier: every CTA's output copy is stored (every CTA counts itself in)
     tc_fence_before();
@@ -1012,43 +1017,46 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
     }
     __syncthreads();
 
-    // ---- the slice: the active CTAs' copies summed in CTA order, split over P
-    // thread groups (group g takes CTAs g, g + P, ...; all its loads in flight at
-    // once), then the groups in order
-    if (nf > 0) {
-        float4* red = reinterpret_cast<float4*>(ring);   // [P][nf]; the ring is idle now
-        const int P = kThreadsTc / nf < 1 ? 1 : kThreadsTc / nf;
-        if (tid < P * nf) {
-            const int j = tid % nf, g = tid / nf;
-            auto cta_of = [&](int cc) { return U < G ? (int)(((unsigned)(cc + 1) * G + U - 1) / U) - 1 : cc; };
-            const float4* part = reinterpret_cast<const float4*>(p.part);
+    // ---- the slice: float4 j of it summed over the active CTAs' copies by warp
+    // j mod 8 -- lane l takes CTAs l, l + 32, ... (all its loads in flight at
+    // once), then a fixed shuffle tree -- so the order never depends on timing
+    {
+        auto cta_of = [&](int cc) { return U < G ? (int)(((unsigned)(cc + 1) * G + U - 1) / U) - 1 : cc; };
+        const float4* part = reinterpret_cast<const float4*>(p.part);
+        for (int j = warp; j < nf; j += kThreadsTc / 32) {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int c0 = g; c0 < nact; c0 += 16 * P) {
-                float4 a[16];
+            for (int c0 = lane; c0 < nact; c0 += 8 * 32) {
+                float4 a[8];
 #pragma unroll
-                for (int z = 0; z < 16; ++z)
-                    if (c0 + z * P < nact)
-                        a[z] = __ldcg(part + (size_t)cta_of(c0 + z * P) * U4 + f0 + j);
+                for (int z = 0; z < 8; ++z)
+                    if (c0 + 32 * z < nact)
+                        a[z] = __ldcg(part + (size_t)cta_of(c0 + 32 * z) * U4 + f0 + j);
 #pragma unroll
-                for (int z = 0; z < 16; ++z)
-                    if (c0 + z * P < nact) {
+                for (int z = 0; z < 8; ++z)
+                    if (c0 + 32 * z < nact) {
                         acc.x += a[z].x; acc.y += a[z].y; acc.z += a[z].z; acc.w += a[z].w;
                     }
             }
-            red[g * nf + j] = acc;
-        }
-        __syncthreads();
-        if (tid < nf) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int g = 0; g < P; ++g) {
-                const float4 a = red[g * nf + tid];
-                acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-            }
 #pragma unroll
-            for (int z = 0; z < 4; ++z) {
-                const int el = (f0 + tid) * 4 + z, row = el / V, m = el - row * V;
+            for (int off = 16; off >= 1; off >>= 1) {
+                acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
+                acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
+                acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
+                acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
+            }
+            // lane z < 4 writes element z of the float4 (its residual and bias terms
+            // were loaded by thread j before the barrier: handed over by shuffle)
+            const float sums[4] = {acc.x, acc.y, acc.z, acc.w};
+            float mine = 0.f;
+#pragma unroll
+            for (int z = 0; z < 4; ++z)
+                if (lane == z)
+                    mine = sums[z];
+            if (lane < 4) {
+                const int el = (f0 + j) * 4 + lane, row = el / V, m = el - row * V;
                 if (m < M)
-                    p.resid[(size_t)m * p.H + row] = f2bf16_rne(rv[z] + (acc[z] + bsum[z]));
+                    p.resid[(size_t)m * p.H + row] =
+                        f2bf16_rne((j < kFinSlots ? sh.fin[j][lane] : fin_term(j, lane)) + mine);
             }
         }
     }

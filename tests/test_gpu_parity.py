@@ -147,6 +147,40 @@ def test_layer_parity_small(moe, shape, M):
         moe.moe_destroy(h)
 
 
+@pytest.mark.parametrize("M,H", [(1, 256), (4, 256), (4, 384)])
+def test_layer_parity_split_units(moe, M, H):
+    """Shapes whose 64-row h units outnumber the SMs by a small remainder, so the
+    MXFP4 decode layer cuts the leftover units into pieces spread over CTAs
+    (partial sums exchanged, h recomputed per piece): every token takes 4
+    distinct experts and I is chosen from the SM count."""
+    G = torch.cuda.get_device_properties(0).multi_processor_count
+    k = 4
+    nu = k * M                      # distinct selected experts
+    T1 = G // nu + 1                # units per expert: nu * T1 = G + a small remainder
+    I = 64 * T1
+    E = nu + 2
+    shape = synth.Shape(f"split units H={H} I={I} E={E} top-4", H, I, E, k, e8m0_lo=118, e8m0_hi=123,
+                        bias_sigma=0.3, seed=41)
+    t = synth.layer_tensors(shape)
+    h = create_handle(shape)
+    try:
+        load_layer(h, 0, t)
+        for step in range(2):
+            x, r, _ = synth.step_inputs(shape, step, M=M, layers=1)
+            logits = np.full((M, E), -5.0, np.float32)
+            for m in range(M):
+                logits[m, k * m:k * m + k] = np.array([3.0, 2.5, 2.0, 1.5], np.float32) + 0.1 * step
+            got = _run_layer(moe, h, 0, x, r, logits, k)
+            ref, idx, _ = oracle_layer(shape, t, x, logits, r)
+            assert len(set(idx.ravel().tolist())) == nu
+            assert_parity(got, ref, what=f"{shape.name} M={M} step={step}")
+        # a repeat call gives the same bits (piece sums are added in a fixed order)
+        again = _run_layer(moe, h, 0, x, r, logits, k)
+        assert np.array_equal(np.nan_to_num(got), np.nan_to_num(again))
+    finally:
+        moe.moe_destroy(h)
+
+
 def test_layer_topk_ties_and_nan_logits(moe):
     shape = synth.TINY
     t = synth.layer_tensors(shape)
