@@ -354,6 +354,67 @@ __device__ __forceinline__ float row_inv_rms(const uint16_t* row, int n, int lan
     return 1.0f / sqrtf(a / (float)n + 1e-6f);
 }
 
+// Adds the down products of tiles [0, n) of an accumulator region (tile j at
+// columns j * nrows, token m's terms at columns 8m .. 8m+7 of it) into the
+// output copy oacc [H][M], row row0 + 128 j for this thread.  A TMEM load
+// round trip costs far more than the sums, so TB tiles' loads go out before
+// one wait: NC columns a tile (8 for one token, 16 for two, 32 for four).
+template <int NC, int TB>
+__device__ __forceinline__ void drain_region(uint32_t taddr, int n, int nrows, int row0, float* oacc, int H, int M)
+{
+    constexpr int W = NC < 16 ? NC : 16;   // columns per load instruction
+    constexpr int P = NC / W;              // loads per tile
+#pragma unroll 1
+    for (int j0 = 0; j0 < n; j0 += TB) {
+        float d[TB * P][W];
+#pragma unroll
+        for (int j = 0; j < TB; ++j) {
+            if (j0 + j < n) {
+                const uint32_t a = taddr + (uint32_t)((j0 + j) * nrows);
+#pragma unroll
+                for (int h = 0; h < P; ++h) {
+                    if constexpr (W == 8)
+                        tc_ld8(a, d[j * P + h]);
+                    else
+                        tc_ld16(a + 16 * h, d[j * P + h]);
+                }
+            }
+        }
+        tc_wait_ld();
+#pragma unroll
+        for (int j = 0; j < TB; ++j) {
+            const int row = row0 + (j0 + j) * kRowTile;
+            if (j0 + j < n && row < H) {
+                float s[NC / 8];
+#pragma unroll
+                for (int m = 0; m < NC / 8; ++m) {
+                    s[m] = 0.f;
+#pragma unroll
+                    for (int c = 0; c < kTerms; ++c)
+                        s[m] += d[j * P + (8 * m + c) / W][(8 * m + c) % W];
+                }
+                if constexpr (NC == 8) {
+                    oacc[row] += s[0];
+                } else if constexpr (NC == 16) {
+                    float2* o = reinterpret_cast<float2*>(oacc) + row;
+                    const float2 v = *o;
+                    *o = make_float2(v.x + s[0], v.y + s[1]);
+                } else {
+                    if (M == 4) {
+                        float4* o = reinterpret_cast<float4*>(oacc) + row;
+                        const float4 v = *o;
+                        *o = make_float4(v.x + s[0], v.y + s[1], v.z + s[2], v.w + s[3]);
+                    } else {
+#pragma unroll
+                        for (int m = 0; m < 3; ++m)
+                            oacc[row * 3 + m] += s[m];
+                    }
+                }
+            }
+        }
+    }
+}
+
 constexpr int kFinSlots = 64;   // output float4s of a CTA's slice whose final terms are prefetched
 
 struct TcSmem {
@@ -884,19 +945,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                 const int kA = piece ? pl.ks0 : 0, kB = piece ? pl.ks1 : KSH;
                 const bool two = kB - kA > kGuSteps;   // issuer B wrote its half too
                 float sm[kMaxTokens] = {0.f, 0.f, 0.f, 0.f};
+                float d0[2][16], d1[2][16];   // both halves' loads in flight before one wait
 #pragma unroll
-                for (int h16 = 0; h16 < 32; h16 += 16) {
-                    if (h16 < nrows) {
-                        float d0[16], d1[16];
-                        tc_ld16(taddr + h16, d0);
+                for (int h = 0; h < 2; ++h) {
+                    if (16 * h < nrows) {
+                        tc_ld16(taddr + 16 * h, d0[h]);
                         if (two)
-                            tc_ld16(taddr + 32 + h16, d1);
-                        tc_wait_ld();
+                            tc_ld16(taddr + 32 + 16 * h, d1[h]);
+                    }
+                }
+                tc_wait_ld();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (16 * h < nrows) {
 #pragma unroll
                         for (int col = 0; col < 16; ++col) {
-                            const int m = (h16 + col) / kTerms;   // compile-time after unrolling
+                            const int m = (16 * h + col) / kTerms;   // compile-time after unrolling
                             if (m < M)
-                                sm[m] += two ? d0[col] + d1[col] : d0[col];
+                                sm[m] += two ? d0[h][col] + d1[h][col] : d0[h][col];
                         }
                     }
                 }
@@ -929,29 +995,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                     mbar_wait(&sh.dnf[kk & 1], (kk >> 1) & 1, p.status);
                     tc_fence_after();
                     const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + kDnCol + (kk & 1) * kDnRegion;
-                    for (int t2 = ga; t2 < gb; ++t2) {
-                        float sm[kMaxTokens] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                        for (int h16 = 0; h16 < 32; h16 += 16) {
-                            if (h16 < nrows) {
-                                float d0[16];
-                                tc_ld16(taddr + (t2 - ga) * nrows + h16, d0);
-                                tc_wait_ld();
-#pragma unroll
-                                for (int col = 0; col < 16; ++col) {
-                                    const int m = (h16 + col) / kTerms;
-                                    if (m < M)
-                                        sm[m] += d0[col];
-                                }
-                            }
-                        }
-                        const int row = t2 * kRowTile + 32 * q + lane;
-                        if (row < p.H)
-#pragma unroll
-                            for (int m = 0; m < kMaxTokens; ++m)
-                                if (m < M)
-                                    oacc[row * M + m] += sm[m];
-                    }
+                    const int row0 = ga * kRowTile + 32 * q + lane;
+                    if (M == 1)
+                        drain_region<8, 8>(taddr, gb - ga, nrows, row0, oacc, p.H, M);
+                    else if (M == 2)
+                        drain_region<16, 4>(taddr, gb - ga, nrows, row0, oacc, p.H, M);
+                    else
+                        drain_region<32, 1>(taddr, gb - ga, nrows, row0, oacc, p.H, M);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0)
