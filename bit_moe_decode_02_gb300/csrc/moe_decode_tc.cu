@@ -358,56 +358,79 @@ __device__ __forceinline__ float row_inv_rms(const uint16_t* row, int n, int lan
 // columns j * nrows, token m's terms at columns 8m .. 8m+7 of it) into the
 // output copy oacc [H][M], row row0 + 128 j for this thread.  A TMEM load
 // round trip costs far more than the sums, so TB tiles' loads go out before
-// one wait: NC columns a tile (8 for one token, 16 for two, 32 for four).
+// one wait: NC columns a tile (8 for one token, 16 for two, 32 for four).  The
+// loads are unconditional (a batch never reaches past the region's 128
+// columns; columns of absent tiles are read and dropped), the term sums are
+// trees and the read-modify-writes of oacc are predicated, so the tiles of a
+// batch run side by side instead of one branch after another.
 template <int NC, int TB>
 __device__ __forceinline__ void drain_region(uint32_t taddr, int n, int nrows, int row0, float* oacc, int H, int M)
 {
     constexpr int W = NC < 16 ? NC : 16;   // columns per load instruction
     constexpr int P = NC / W;              // loads per tile
+    constexpr int T = NC / 8;              // tokens a tile holds
 #pragma unroll 1
     for (int j0 = 0; j0 < n; j0 += TB) {
         float d[TB * P][W];
 #pragma unroll
         for (int j = 0; j < TB; ++j) {
-            if (j0 + j < n) {
-                const uint32_t a = taddr + (uint32_t)((j0 + j) * nrows);
+            const uint32_t a = taddr + (uint32_t)((j0 + j) * nrows);
 #pragma unroll
-                for (int h = 0; h < P; ++h) {
-                    if constexpr (W == 8)
-                        tc_ld8(a, d[j * P + h]);
-                    else
-                        tc_ld16(a + 16 * h, d[j * P + h]);
-                }
+            for (int h = 0; h < P; ++h) {
+                if constexpr (W == 8)
+                    tc_ld8(a, d[j * P + h]);
+                else
+                    tc_ld16(a + 16 * h, d[j * P + h]);
             }
         }
         tc_wait_ld();
+        float s[TB][T];
 #pragma unroll
-        for (int j = 0; j < TB; ++j) {
-            const int row = row0 + (j0 + j) * kRowTile;
-            if (j0 + j < n && row < H) {
-                float s[NC / 8];
+        for (int j = 0; j < TB; ++j)
 #pragma unroll
-                for (int m = 0; m < NC / 8; ++m) {
-                    s[m] = 0.f;
+            for (int m = 0; m < T; ++m) {
+                float v[kTerms];
 #pragma unroll
-                    for (int c = 0; c < kTerms; ++c)
-                        s[m] += d[j * P + (8 * m + c) / W][(8 * m + c) % W];
-                }
-                if constexpr (NC == 8) {
-                    oacc[row] += s[0];
-                } else if constexpr (NC == 16) {
-                    float2* o = reinterpret_cast<float2*>(oacc) + row;
-                    const float2 v = *o;
-                    *o = make_float2(v.x + s[0], v.y + s[1]);
-                } else {
+                for (int c = 0; c < kTerms; ++c)
+                    v[c] = d[j * P + (8 * m + c) / W][(8 * m + c) % W];
+                s[j][m] = ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+            }
+        bool ok[TB];
+#pragma unroll
+        for (int j = 0; j < TB; ++j)
+            ok[j] = j0 + j < n && row0 + (j0 + j) * kRowTile < H;
+        if constexpr (NC == 8) {
+            float o[TB];
+#pragma unroll
+            for (int j = 0; j < TB; ++j)
+                o[j] = ok[j] ? oacc[row0 + (j0 + j) * kRowTile] : 0.f;
+#pragma unroll
+            for (int j = 0; j < TB; ++j)
+                if (ok[j])
+                    oacc[row0 + (j0 + j) * kRowTile] = o[j] + s[j][0];
+        } else if constexpr (NC == 16) {
+            float2* o2 = reinterpret_cast<float2*>(oacc);
+            float2 o[TB];
+#pragma unroll
+            for (int j = 0; j < TB; ++j)
+                o[j] = ok[j] ? o2[row0 + (j0 + j) * kRowTile] : make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < TB; ++j)
+                if (ok[j])
+                    o2[row0 + (j0 + j) * kRowTile] = make_float2(o[j].x + s[j][0], o[j].y + s[j][1]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < TB; ++j) {
+                const int row = row0 + (j0 + j) * kRowTile;
+                if (ok[j]) {
                     if (M == 4) {
                         float4* o = reinterpret_cast<float4*>(oacc) + row;
                         const float4 v = *o;
-                        *o = make_float4(v.x + s[0], v.y + s[1], v.z + s[2], v.w + s[3]);
+                        *o = make_float4(v.x + s[j][0], v.y + s[j][1], v.z + s[j][2], v.w + s[j][3]);
                     } else {
 #pragma unroll
                         for (int m = 0; m < 3; ++m)
-                            oacc[row * 3 + m] += s[m];
+                            oacc[row * 3 + m] += s[j][m];
                     }
                 }
             }
@@ -1011,7 +1034,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
         }
         // ---- the CTA's output copy to its partial slot [H][V] (rows drained by other warps)
         epi_barrier();
-        if (nun > 0) {
+        if (nun > 0 && M != 3) {
+            // [H][M] and [H][V] coincide: a straight float4 copy
+            const float4* src4 = reinterpret_cast<const float4*>(oacc);
+            float4* dst4 = reinterpret_cast<float4*>(p.part + (size_t)b * p.H * V);
+            const int n4 = p.H * M / 4;
+#pragma unroll 4
+            for (int i = te; i < n4; i += kEpi)
+                dst4[i] = src4[i];
+        } else if (nun > 0) {
             float* dst = p.part + (size_t)b * p.H * V;
             for (int row = te; row < p.H; row += kEpi) {
                 float v[kMaxTokens] = {0.f, 0.f, 0.f, 0.f};
