@@ -494,7 +494,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
     if (tid == 0) {
         for (int i = 0; i < kSlots; ++i) {
             mbar_init(&sh.full[i], 1);
-            mbar_init(&sh.empty[i], 1);
+            mbar_init(&sh.empty[i], 2);   // both MMA issuers release every stage
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.accf[i], 2);
@@ -730,10 +730,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
         }
     } else if (warp == 1 || warp == kMmaWarpB) {
         // ================================================================ MMA issuers
-        // Issuing a tcgen05 instruction costs one thread ~60-80 cycles.  Issuer A
-        // (warp 1) takes the gate/up stages; the down stages, which all wait on
-        // the same h' and then run back to back, alternate between A and B
-        // (warp 6), each on its own tiles of the region and its own scale sets.
+        // Issuing a tcgen05 instruction holds its thread ~75-95 cycles (a scale
+        // copy as long as an MMA), while the pipe takes one every ~40 cycles from
+        // two threads.  So every stage is split between issuer A (warp 1) and B
+        // (warp 6): A takes the first half of its scale chunks (gate/up k-step
+        // pairs) or down tiles, B the rest, each with its own scale sets and
+        // accumulator half / tiles, and both release the stage.  A stage is then
+        // consumed in half the time, which is ring space handed back to the
+        // weight stream sooner.
         const int role = warp == 1 ? 0 : 1;
         if (lane == 0) {
             RingTc ring_alloc;
@@ -758,39 +762,41 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                     tc_fence_after();
                     const uint32_t d = tmem + kGuCol + buf * kGuBuf + role * 32;
                     bool first = true;
-                    int jst = 0;
-                    for (int ks = kA; ks < kB; ks += kGuSteps, ++c, ++jst) {
+                    for (int ks = kA; ks < kB; ks += kGuSteps, ++c) {
                         const int steps = kB - ks < kGuSteps ? kB - ks : kGuSteps;
                         const GuStage sg(steps);
                         unsigned long long end;
                         const uint32_t st = su32(ring) + ring_alloc.place(sg.size, ring_cap, &end);
-                        if ((jst & 1) != role)
-                            continue;   // the other issuer's stage
+                        // this issuer's scale chunks [c0, c1) = k-steps [2 c0, min(2 c1, steps))
+                        const int chunks = (steps + 1) >> 1, half = (chunks + 1) >> 1;
+                        const int c0 = role ? half : 0, c1 = role ? chunks : half;
                         const uint32_t slot = c % kSlots;
-                        mbar_wait(&sh.full[slot], (c / kSlots) & 1, p.status);
-                        tc_fence_after();
-                        const uint32_t set = myset + (mine++ & 1) * kSfSet;
-                        const int chunks = (steps + 1) >> 1;
-                        const uint32_t xb = su32(xs) + ks * atom;                               // B: x terms
-                        const uint32_t xsf = su32(xs) + KSH * atom + (ks >> 1) * kSfChunk;     // and their scales
-                        // (the hot loop: unrolled, descriptors stepped by adding the byte
-                        // offset / 16 to the start-address field)
+                        if (c0 < c1) {
+                            mbar_wait(&sh.full[slot], (c / kSlots) & 1, p.status);
+                            tc_fence_after();
+                            const uint32_t set = myset + (mine++ & 1) * kSfSet;
+                            const uint32_t xsf = su32(xs) + KSH * atom + (ks >> 1) * kSfChunk;   // x-term scales
+                            // (the hot loop: unrolled, descriptors stepped by adding the byte
+                            // offset / 16 to the start-address field)
 #pragma unroll
-                        for (int ch = 0; ch < (kGuSteps + 1) / 2; ++ch)
-                            if (ch < chunks) {
-                                tc_cp_sf(set + 4 * ch, st + sg.sfa + ch * kSfChunk);
-                                tc_cp_sf(set + kSfSet / 2 + 4 * ch, xsf + ch * kSfChunk);
-                            }
-                        const uint64_t da = smem_desc(st, 128, 256), db = smem_desc(xb, 128, 256);
-                        const uint32_t id_odd = (2u << 4) | (2u << 29);
+                            for (int ch = 0; ch < (kGuSteps + 3) / 4; ++ch)
+                                if (c0 + ch < c1) {
+                                    tc_cp_sf(set + 4 * ch, st + sg.sfa + (c0 + ch) * kSfChunk);
+                                    tc_cp_sf(set + kSfSet / 2 + 4 * ch, xsf + (c0 + ch) * kSfChunk);
+                                }
+                            const int j0 = 2 * c0, nj = (2 * c1 < steps ? 2 * c1 : steps) - j0;
+                            const uint64_t da = smem_desc(st + j0 * kTileA, 128, 256);
+                            const uint64_t db = smem_desc(su32(xs) + (ks + j0) * atom, 128, 256);   // B: x terms
+                            const uint32_t id_odd = (2u << 4) | (2u << 29);
 #pragma unroll
-                        for (int j = 0; j < kGuSteps; ++j)
-                            if (j < steps) {
-                                tc_mma_mxf4(d, da + (uint64_t)(j * (kTileA >> 4)), db + (uint64_t)(j * (atom >> 4)),
-                                            idesc | ((j & 1) ? id_odd : 0u), set + 4 * (j >> 1),
-                                            set + kSfSet / 2 + 4 * (j >> 1), (first && j == 0) ? 0u : 1u);
-                            }
-                        first = false;
+                            for (int j = 0; j < (kGuSteps + 1) / 2; ++j)
+                                if (j < nj) {
+                                    tc_mma_mxf4(d, da + (uint64_t)(j * (kTileA >> 4)), db + (uint64_t)(j * (atom >> 4)),
+                                                idesc | ((j & 1) ? id_odd : 0u), set + 4 * (j >> 1),
+                                                set + kSfSet / 2 + 4 * (j >> 1), (first && j == 0) ? 0u : 1u);
+                                }
+                            first = false;
+                        }
                         tc_commit(&sh.empty[slot]);
                     }
                     tc_commit(&sh.accf[buf]);   // both issuers
@@ -806,35 +812,36 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                     tc_fence_after();
                     const uint32_t aid = (uint32_t)(2 * (t & 1));   // A scale bytes of k-step t in its chunk
                     const int tA = piece ? pl.ta : 0, tB = piece ? pl.tb : T2;
-                    int jst = 0;                                     // down stage of this item
                     for (int ga = tA; ga < tB; ga += TG, ++kk) {
                         const int gb = ga + TG < tB ? ga + TG : tB;
                         if (kk >= 2)
                             mbar_wait(&sh.dne[kk & 1], ((kk >> 1) - 1) & 1, p.status);
                         tc_fence_after();
                         const uint32_t dreg = tmem + kDnCol + (kk & 1) * kDnRegion;
-                        for (int t2 = ga; t2 < gb; t2 += kDnStageTiles, ++c, ++jst) {
+                        for (int t2 = ga; t2 < gb; t2 += kDnStageTiles, ++c) {
                             const int n = gb - t2 < kDnStageTiles ? gb - t2 : kDnStageTiles;
                             unsigned long long end;
                             const uint32_t st = su32(ring) + ring_alloc.place(dn_stage_size(n), ring_cap, &end);
-                            if ((jst & 1) != role)
-                                continue;   // the other issuer's stage
+                            // this issuer's tiles [j0, j1) of the stage
+                            const int hn = (n + 1) >> 1, j0 = role ? hn : 0, j1 = role ? n : hn;
                             const uint32_t slot = c % kSlots;
-                            mbar_wait(&sh.full[slot], (c / kSlots) & 1, p.status);
-                            tc_fence_after();
-                            const uint32_t set = myset + (mine++ & 1) * kSfSet;
-                            tc_cp_sf(set, hb + 1024);
+                            if (j0 < j1) {
+                                mbar_wait(&sh.full[slot], (c / kSlots) & 1, p.status);
+                                tc_fence_after();
+                                const uint32_t set = myset + (mine++ & 1) * kSfSet;
+                                tc_cp_sf(set, hb + 1024);
 #pragma unroll
-                            for (int j = 0; j < kDnStageTiles; ++j)
-                                if (j < n)
-                                    tc_cp_sf(set + 4 + 4 * j, st + n * kTileA + j * kSfChunk);
-                            const uint64_t da = smem_desc(st, 128, 256), db = smem_desc(hb, 128, 256);
-                            const uint32_t dcol = dreg + (t2 - ga) * nrows;
+                                for (int j = 0; j < (kDnStageTiles + 1) / 2; ++j)
+                                    if (j0 + j < j1)
+                                        tc_cp_sf(set + 4 + 4 * j, st + n * kTileA + (j0 + j) * kSfChunk);
+                                const uint64_t da = smem_desc(st + j0 * kTileA, 128, 256), db = smem_desc(hb, 128, 256);
+                                const uint32_t dcol = dreg + (t2 - ga + j0) * nrows;
 #pragma unroll
-                            for (int j = 0; j < kDnStageTiles; ++j)
-                                if (j < n)
-                                    tc_mma_mxf4(dcol + j * nrows, da + (uint64_t)(j * (kTileA >> 4)), db,
-                                                idesc | (aid << 29), set + 4 + 4 * j, set, 0u);
+                                for (int j = 0; j < (kDnStageTiles + 1) / 2; ++j)
+                                    if (j0 + j < j1)
+                                        tc_mma_mxf4(dcol + j * nrows, da + (uint64_t)(j * (kTileA >> 4)), db,
+                                                    idesc | (aid << 29), set + 4 + 4 * j, set, 0u);
+                            }
                             tc_commit(&sh.empty[slot]);
                         }
                         tc_commit(&sh.dnf[kk & 1]);   // both issuers: the group's region is full
@@ -966,7 +973,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                 tc_fence_after();
                 const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + kGuCol + buf * kGuBuf;
                 const int kA = piece ? pl.ks0 : 0, kB = piece ? pl.ks1 : KSH;
-                const bool two = kB - kA > kGuSteps;   // issuer B wrote its half too
+                const bool two = kB - kA >= 3;   // issuer B wrote its half too (some stage has 2+ chunks)
                 float sm[kMaxTokens] = {0.f, 0.f, 0.f, 0.f};
                 float d0[2][16], d1[2][16];   // both halves' loads in flight before one wait
 #pragma unroll
@@ -1024,7 +1031,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                     else if (M == 2)
                         drain_region<16, 4>(taddr, gb - ga, nrows, row0, oacc, p.H, M);
                     else
-                        drain_region<32, 1>(taddr, gb - ga, nrows, row0, oacc, p.H, M);
+                        drain_region<32, 4>(taddr, gb - ga, nrows, row0, oacc, p.H, M);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0)
