@@ -34,55 +34,69 @@ __device__ __forceinline__ void topk_load(const float* __restrict__ lg, int E, f
 }
 
 // One warp: top-k of the loaded logits (largest first; ties to the lower
-// index), then softmax over the k selected.  Lane 0 writes sel[0..k) and the
-// weights wt[0..k).
+// index), then softmax over the k selected.  Lanes s < k write sel[s] and the
+// weight wt[s].  Each round is two warp reductions: the maximum of an
+// order-preserving integer key of the logits (redux.sync), then the lowest
+// expert index among the lanes holding it.  -0 is taken as +0 first, so equal
+// logits stay ties exactly as under a float comparison.  The softmax takes the
+// k selected logits from registers: exp(l - l_max) summed by a fixed
+// butterfly, so the result does not depend on timing.
+__device__ __forceinline__ uint32_t order_key(float v)
+{
+    const uint32_t u = __float_as_uint(v + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t key)
+{
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
 template <int NR = kTopkRegs>
 __device__ __forceinline__ void topk_select(float (&v)[NR], int E, int k, int* sel, float* wt)
 {
     const int lane = threadIdx.x & 31;
+    uint32_t key[NR];
     uint32_t avail = 0;
 #pragma unroll
-    for (int j = 0; j < NR; ++j)
+    for (int j = 0; j < NR; ++j) {
+        key[j] = order_key(v[j]);
         if (lane + 32 * j < E)
             avail |= 1u << j;
+    }
+    float myv = -INFINITY, vmax = -INFINITY;
+    int mye = 0;
     for (int s = 0; s < k; ++s) {
-        float bv = -INFINITY;
-        int be = 0x7fffffff;
+        // this lane's best available key, ties to the lower register (lower index)
+        uint32_t bk = 0u;
+        int bj = 0;
 #pragma unroll
-        for (int j = 0; j < NR; ++j) {
-            const int e = lane + 32 * j;
-            if (((avail >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < be))) {
-                bv = v[j];
-                be = e;
+        for (int j = NR - 1; j >= 0; --j)
+            if (((avail >> j) & 1u) && key[j] >= bk) {
+                bk = key[j];
+                bj = j;
             }
-        }
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-            if (ov > bv || (ov == bv && oe < be)) {
-                bv = ov;
-                be = oe;
-            }
-        }
-        if ((be & 31) == lane)
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t be = __reduce_min_sync(0xffffffffu, (bk == mk && avail) ? (uint32_t)(lane + 32 * bj)
+                                                                               : 0xffffffffu);
+        if ((int)(be & 31u) == lane)
             avail &= ~(1u << (be >> 5));
-        if (lane == 0) {
-            sel[s] = be;
-            wt[s] = bv;
+        const float bv = key_value(mk);
+        if (s == 0)
+            vmax = bv;
+        if (lane == s) {
+            myv = bv;
+            mye = (int)be;
         }
     }
-    __syncwarp();
-    const float lmax = wt[0];
-    const float l = lane < k ? wt[lane] : -INFINITY;
-    const float e = lane < k ? expf(l - lmax) : 0.0f;
+    const float e = lane < k ? expf(myv - vmax) : 0.0f;
     float sum = e;
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1)
         sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    __syncwarp();
-    if (lane < k)
+    if (lane < k) {
+        sel[lane] = mye;
         wt[lane] = e / sum;
+    }
 }
 
 // One warp, one token: load, then select.
