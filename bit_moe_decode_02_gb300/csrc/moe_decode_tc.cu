@@ -159,6 +159,30 @@ __device__ __forceinline__ Plan make_plan(int b, int G, int U, int KSH, int CHH,
     return pl;
 }
 
+// Plans for the distinct-expert counts a call can have (nu = k .. min(M k, E)),
+// worked out before the routing is known, so the integer divisions of
+// make_plan are off the path from the routing to the first weight copy.
+constexpr int kPlanTab = 32;
+struct PackedPlan {
+    short v[12];
+};
+__device__ __forceinline__ PackedPlan pack_plan(const Plan& pl)
+{
+    PackedPlan q;
+    const int f[12] = {pl.u0, pl.nun, pl.piece, pl.su, pl.sj, pl.pp, pl.S, pl.ks0, pl.ks1, pl.ta, pl.tb, pl.nitem};
+#pragma unroll
+    for (int i = 0; i < 12; ++i)
+        q.v[i] = (short)f[i];
+    return q;
+}
+__device__ __forceinline__ Plan unpack_plan(const PackedPlan& q)
+{
+    Plan pl;
+    pl.u0 = q.v[0]; pl.nun = q.v[1]; pl.piece = q.v[2]; pl.su = q.v[3]; pl.sj = q.v[4]; pl.pp = q.v[5];
+    pl.S = q.v[6]; pl.ks0 = q.v[7]; pl.ks1 = q.v[8]; pl.ta = q.v[9]; pl.tb = q.v[10]; pl.nitem = q.v[11];
+    return pl;
+}
+
 enum ItemKind { kGu = 0, kDn = 1, kGuPiece = 2, kDnPiece = 3 };
 // Item k of a plan: the piece's gate/up first (its partial sums are published
 // early), the whole units' items, the piece's down tiles last.  The epilogue
@@ -447,6 +471,7 @@ struct TcSmem {
     uint64_t hbar[2];            // h' terms of a unit written
     uint64_t routed, xfull;      // routing done; the layer's x terms copied in
     uint64_t hsfull;             // the split unit's h' terms copied in
+    uint64_t planbar;            // the plan table is written
     unsigned epoch;              // this call's tag for the exchange flags (call index + 1)
     uint32_t tmem_base;
     int sel[kMaxTokens][kMaxTopK];
@@ -456,6 +481,7 @@ struct TcSmem {
     unsigned char unit_of[kMaxExperts];
     float wslot[kMaxUnits][kMaxTokens];   // routing weight of token m for expert slot s (0 if not chosen)
     float fin[kFinSlots][4];              // r + sum_s w_s b_s of the slice's elements (loaded before the grid barrier)
+    PackedPlan plan_tab[kPlanTab];        // plan of nu = k + i distinct experts
 };
 
 __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTcParams p)
@@ -506,6 +532,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
         mbar_init(&sh.routed, 1);
         mbar_init(&sh.xfull, 1);
         mbar_init(&sh.hsfull, 1);
+        mbar_init(&sh.planbar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -517,6 +544,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
+    // the plan of every distinct-expert count the call can have (lane i: nu =
+    // k + i), from the shapes alone, so before the previous grid is waited for
+    const int nu_hi = (M * p.k < p.E ? M * p.k : p.E) < kMaxUnits ? (M * p.k < p.E ? M * p.k : p.E) : kMaxUnits;
+    if (warp == kCombineWarp) {
+        const int nu = p.k + lane;
+        if (lane < kPlanTab && nu <= nu_hi)
+            sh.plan_tab[lane] = pack_plan(make_plan(b, G, nu * T1, KSH, CHH, T2));
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&sh.planbar);
+    }
     // everything below reads what the previous grid in the stream wrote (the
     // logits, x, the residual) or shares its workspace
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -554,19 +592,26 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                 ++u;
             }
             const int nu = __shfl_sync(0xffffffffu, incl, 31);
-            for (int x = lane; x < nu * kMaxTokens; x += 32)
-                sh.wslot[x / kMaxTokens][x % kMaxTokens] = 0.f;
-            __syncwarp();
-            for (int x = lane; x < M * p.k; x += 32) {
-                const int m = x / p.k, k2 = x % p.k;
-                sh.wslot[sh.unit_of[sh.sel[m][k2]]][m] = sh.wt[m][k2];
-            }
             if (lane == 0)
                 sh.nu = nu;
         }
         route_barrier();
-        if (warp == 1 && lane == 0)
-            mbar_arrive(&sh.routed);   // hands the routing to the epilogue warps
+        if (warp == 1) {
+            // the routing weights by (expert slot, token): read by SwiGLU and the
+            // output's bias terms only, so off the producer's path
+            const int nu = sh.nu;
+            for (int x = lane; x < nu * kMaxTokens; x += 32)
+                sh.wslot[x / kMaxTokens][x % kMaxTokens] = 0.f;
+            __syncwarp();
+            for (int x = lane; x < kMaxTokens * kMaxTopK; x += 32) {
+                const int m = x / kMaxTopK, k2 = x % kMaxTopK;
+                if (m < M && k2 < p.k)
+                    sh.wslot[sh.unit_of[sh.sel[m][k2]]][m] = sh.wt[m][k2];
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sh.routed);   // hands the routing to the epilogue warps
+        }
     } else if (warp <= 5) {
         // ---- x terms (warps 2..5): items b + G q + 4 G i, token-major (q = warp - 2)
         const int q = warp - 2, te = tid - 64;
@@ -627,7 +672,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
     const int nu = sh.nu;
     const int U = nu * T1;
     // (products below stay under 2^31: U <= kMaxUnits * kMaxK / 64, G and H small)
-    const Plan pl = make_plan(b, G, U, KSH, CHH, T2);
+    mbar_wait(&sh.planbar, 0, p.status);
+    const Plan pl = nu - p.k >= 0 && nu - p.k < kPlanTab && nu <= nu_hi ? unpack_plan(sh.plan_tab[nu - p.k])
+                                                                        : make_plan(b, G, U, KSH, CHH, T2);
     const int u0 = pl.u0, nun = pl.nun, nitem = pl.nitem;
     const int nact = U < G ? U : G;   // CTAs with units
     if (b == 0 && tid == 0 && p.nu_out)
@@ -1084,10 +1131,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
         }
         return v;
     };
-    if (tid < nf && tid < kFinSlots)
+    if (tid < nf && tid < kFinSlots) {
+        mbar_wait(&sh.routed, 0, p.status);   // the weight slots (warp 1 writes them)
 #pragma unroll
         for (int z = 0; z < 4; ++z)
             sh.fin[tid][z] = fin_term(tid, z);
+    }
 
     // ---- grid barrier: every CTA's output copy is stored (every CTA counts itself in)
     tc_fence_before();
