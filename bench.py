@@ -20,6 +20,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -49,10 +50,18 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def _code_only(src: str) -> str:
+    """The source without its comments and trailing blanks: the counters stay
+    valid across comment edits, not across code changes."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
 def kernel_hash() -> str:
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        h.update(open(os.path.join(ROOT, f), "rb").read())
+        h.update(_code_only(open(os.path.join(ROOT, f)).read()).encode())
     return h.hexdigest()[:16]
 
 

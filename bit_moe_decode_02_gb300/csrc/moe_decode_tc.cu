@@ -20,26 +20,29 @@
 // 128-row tile (64 gate rows over 64 up rows, the interleaved tile layout), so
 // one CTA computes SwiGLU for those rows with nothing exchanged; it folds in
 // each token's routing weight, h'_m = w_m h_m, and runs the down projection's
-// 64 matching K columns for every output row.  CTA b takes the units
-// [b U / G, (b+1) U / G), so no activation ever crosses CTAs: each CTA adds
-// its down products into its own fp32 copy of the output, and after one grid
-// barrier CTA b sums the CTAs' copies for its slice of the output rows in CTA
-// order (results do not depend on timing) and writes
-// out = bf16(r + sum + sum_s w_s b_s).
+// 64 matching K columns for every output row.  Each CTA takes q = U / G whole
+// units; the U mod G leftover units are cut into pieces (a K range of the
+// gate/up, a range of the down tiles) whose CTAs exchange only their gate/up
+// partial sums (see make_plan).  Each CTA adds its down products into its own
+// fp32 copy of the output, and after one grid barrier CTA b sums the CTAs'
+// copies for its slice of the output rows in CTA order (results do not depend
+// on timing) and writes out = bf16(r + sum + sum_s w_s b_s).
 //
 // The x terms are built inside the layer: the (token, 32-element block) items
-// are dealt over the CTAs, written to global memory and counted; gate/up
-// stages carry them once the count is complete.  Weight copies never wait.
+// are dealt over the CTAs, written to global memory and counted; once the
+// count is complete each CTA copies the whole set into shared memory, where it
+// stays for the layer.  Weight copies never wait on activations.
 //
 // The launch signals its dependents at entry, so the next layer's CTAs take
 // over each SM as soon as this layer's CTA there exits and set up before they
 // wait for this grid to complete.
 //
 // Warp roles (256 threads): warp 0 streams weights into a byte ring of shared
-// memory (each stage's copies issued from separate lanes in one instruction);
-// warps 1 and 6 issue the MMAs (warp 1 owns tensor memory); warps 2..5 (one
-// per lane quarter) build the x terms and drain the accumulators; warp 7
-// combines a split unit's partial sums.  Warps 0, 1 and 6 route.
+// memory (a stage's copies issued from separate lanes); warps 1 and 6 issue
+// the MMAs, each half of every stage (warp 1 owns tensor memory); warps 2..5
+// (one per lane quarter) build the x terms and drain the accumulators; warp 7
+// works out the plans before the grid wait and combines a split unit's partial
+// sums.  Warps 0, 1 and 6 route.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -800,7 +803,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                 if (kind == kGu || kind == kGuPiece) {
                     const int gi = piece ? 0 : i + pl.piece;   // gate/up accumulator use
                     const int kA = piece ? pl.ks0 : 0, kB = piece ? pl.ks1 : KSH;
-                    // stages alternate between the issuers, each into its own half
+                    // each issuer adds its half of every stage into its own accumulator half
                     const uint32_t buf = gi & 1;
                     if (gi == 0)
                         mbar_wait(&sh.xfull, 0, p.status);   // the layer's x terms are in
