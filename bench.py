@@ -211,11 +211,12 @@ def _setup(args):
 
 
 def _max_over_ranks(v, world):
+    """The maximum of v over the ranks (the slowest rank's time)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
