@@ -164,7 +164,8 @@ __device__ __forceinline__ Plan make_plan(int b, int G, int U, int KSH, int CHH,
 
 // Plans for the distinct-expert counts a call can have (nu = k .. min(M k, E)),
 // worked out before the routing is known, so the integer divisions of
-// make_plan are off the path from the routing to the first weight copy.
+// make_plan are off the path from the routing to the first weight copy.  The
+// fields fit 16 bits: every one is at most U <= kMaxUnits * kMaxK / 64 = 3072.
 constexpr int kPlanTab = 32;
 struct PackedPlan {
     short v[12];
