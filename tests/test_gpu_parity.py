@@ -181,6 +181,44 @@ def test_layer_parity_split_units(moe, M, H):
         moe.moe_destroy(h)
 
 
+def _disjoint_logits(M, E, k, overlap_last=False):
+    """Router logits giving token m the k experts k m .. k m + k - 1 (descending
+    logits); with overlap_last the last token's first choice repeats the
+    previous token's last expert, so one expert is shared."""
+    logits = np.full((M, E), -5.0, np.float32)
+    for m in range(M):
+        e0 = k * m - (1 if overlap_last and m == M - 1 and m > 0 else 0)
+        logits[m, e0:e0 + k] = 3.0 - 0.1 * np.arange(k, dtype=np.float32)
+    return logits
+
+
+@pytest.mark.parametrize("M,H,I,overlap", [(3, 128, 128, True), (3, 128, 128, False), (4, 128, 128, False),
+                                           (4, 256, 192, False)],
+                         ids=["nu=47", "nu=48", "nu=64", "nu=64 split units"])
+def test_layer_parity_many_distinct_experts(moe, M, H, I, overlap):
+    """Top-16 of 256 experts for up to 4 tokens: up to 64 distinct experts in one
+    MXFP4 decode call (the largest the library accepts), at both ends of the
+    plans the layer works out ahead of the routing (nu = k .. k + 31) and past
+    them (nu >= k + 32), with whole and split units."""
+    E, k = 256, 16
+    shape = synth.Shape(f"many experts H={H} I={I} E={E} top-{k}", H, I, E, k, e8m0_lo=118, e8m0_hi=123,
+                        bias_sigma=0.3, seed=43)
+    logits = _disjoint_logits(M, E, k, overlap)
+    nu = k * M - (1 if overlap else 0)
+    t = synth.layer_tensors(shape)
+    h = create_handle(shape, max_top_k=k)
+    try:
+        load_layer(h, 0, t)
+        x, r, _ = synth.step_inputs(shape, 0, M=M, layers=1)
+        got = _run_layer(moe, h, 0, x, r, logits, k)
+        ref, idx, _ = oracle_layer(shape, t, x, logits, r)
+        assert len(set(idx.ravel().tolist())) == nu
+        assert_parity(got, ref, what=f"{shape.name} M={M} nu={nu}")
+        assert moe.moe_last_bytes(h) == nu * shape.expert_bytes()
+    finally:
+        moe.moe_destroy(h)
+
+
 def test_layer_topk_ties_and_nan_logits(moe):
     shape = synth.TINY
     t = synth.layer_tensors(shape)
