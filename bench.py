@@ -10,6 +10,13 @@ synthetic inputs (x, residual and router logits ~N(0,1)).  Step s uses layer
 s mod 24 of 24 resident layers (10.2 GB of distinct weights), so the 53 MB a
 step reads is never L2-resident from a previous step (L2 is 129 MB).
 
+The same JSON line carries an "extra" object with the other workloads, each
+measured in the same run with its own clock record: the 24-layer MXFP4 stack
+and the 48-layer int4 stack at M = 1 and 4 (tokens/s of the expert path, one
+CUDA graph of the stack per step, fresh router logits every step), and the
+batched M = 512 layer, uniform and skewed (µs, TFLOP/s, HBM fraction).
+--no-extra leaves them out.
+
 --impl reference times the fp64 CPU oracle on the host cores on the same
 workload (a bounded sample: each step is one layer for one token).
 
@@ -237,7 +244,8 @@ def run_ours(args):
     shape = SHAPE
     L = args.layers or shape.layers
     H, E, k = shape.hidden, shape.experts, shape.top_k
-    h = moe.moe_create(H, shape.intermediate, E, L, 1, k, moe.MOE_FMT_MXFP4, 32, 1)
+    # max_tokens 4: the same resident layers also serve the M = 4 stack of "extra"
+    h = moe.moe_create(H, shape.intermediate, E, L, 4, k, moe.MOE_FMT_MXFP4, 32, 1)
     _load_all(moe, h, shape, L)
     W, K = args.warmup, args.steps
     n_in = W + K
@@ -308,6 +316,11 @@ def run_ours(args):
     avg_bytes = float(np.mean(bytes_per_step))
     peak, peak_kind = measured_peaks()
     achieved = avg_bytes / (ms / 1e3 / K) / 1e9
+    extra = None
+    if not args.no_extra:
+        extra = {}
+        for M in (1, 4):
+            extra[f"stack24_m{M}"] = measure_stack(moe, h, synth.GPTOSS_STACK, L, M, args.extra_steps, 8)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -317,6 +330,8 @@ def run_ours(args):
                "sample": f"{len(times)} single-token layer forwards of this workload, fp64, "
                          f"OpenMP over output rows"}
     moe.moe_destroy(h)
+    if extra is not None:
+        extra.update(extra_workloads(moe, args))
     if rank != 0:
         return 0
     line = {
@@ -341,25 +356,20 @@ def run_ours(args):
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
     }
+    if extra is not None:
+        line["extra"] = extra
     print(json.dumps(line), flush=True)
     return 0
 
 
-def run_stack(args):
-    """Extra workloads (not the headline line): the 24-layer MXFP4 stack and
-    the 48-layer int4 stack, tokens/s of the expert path at M = --tokens."""
+def measure_stack(moe, h, shape, L, M, steps, warmup):
+    """Tokens/s of the expert stack through moe_forward_stack on a loaded
+    handle: every step copies fresh router logits [L][M][E] into the buffer the
+    cached graph reads, then runs the L layers (each layer reads its logits only
+    after the previous layer's output is complete)."""
     import torch
-    rank, world = _setup(args)
-    import bit_moe_decode_02_gb300 as moe
-    shape = synth.GPTOSS_STACK if args.workload == "stack24" else synth.INT4_STACK
-    L = min(args.layers, shape.layers) if args.layers else shape.layers
-    M, k = args.tokens, shape.top_k
-    fmt = moe.MOE_FMT_MXFP4 if shape.fmt == synth.FMT_MXFP4 else moe.MOE_FMT_INT4
-    h = moe.moe_create(shape.hidden, shape.intermediate, shape.experts, L, M, k, fmt, shape.group,
-                       1 if shape.has_bias else 0)
-    _load_all(moe, h, shape, L)
-    W, K = args.warmup, args.steps
-    logits = np.stack([synth.step_inputs(shape, 5000 + s, M=M, layers=L)[2] for s in range(W + K)])
+    k = shape.top_k
+    logits = np.stack([synth.step_inputs(shape, 5000 + s, M=M, layers=L)[2] for s in range(warmup + steps)])
     _, r, _ = synth.step_inputs(shape, 4999, M=M, layers=L)
     ld = torch.from_numpy(logits).cuda()
     lbuf = torch.empty_like(ld[0])
@@ -370,48 +380,44 @@ def run_stack(args):
         lbuf.copy_(ld[s], non_blocking=True)
         moe.moe_forward_stack(h, rd, lbuf, M, k, stream)
 
-    for s in range(W):
+    for s in range(warmup):
         step(s)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
         ev0.record(stream)
-        for s in range(W, W + K):
+        for s in range(warmup, warmup + steps):
             step(s)
         ev1.record(stream)
         torch.cuda.synchronize()
     ms = ev0.elapsed_time(ev1)
     assert moe.moe_get_status(h) == 0
-    step(0)
-    nbytes = moe.moe_last_bytes(h, stream)
-    moe.moe_destroy(h)
-    us_step = 1e3 * ms / K
+    launches = moe.moe_last_launches(h)
+    nbytes = []
+    for s in range(warmup, warmup + min(steps, 16)):
+        step(s)
+        nbytes.append(moe.moe_last_bytes(h, stream))
+    us_step = 1e3 * ms / steps
     peak, peak_kind = measured_peaks()
-    line = {"workload": shape.name + f", M={M}, {L} layers", "metric": "tokens/s of the expert stack",
-            "value": M * K / (ms / 1e3), "unit": "tok/s", "us_per_step": us_step,
-            "us_per_layer": us_step / L, "steps": K, "warmup": W,
-            "bytes_per_step": nbytes, "gbs": nbytes / (us_step / 1e6) / 1e9,
-            "frac_of_peak": nbytes / (us_step / 1e6) / 1e9 / peak, "peak": peak,
-            "peak_kind": peak_kind, "clocks": clk.summary(),
-            "launch": "one cached CUDA graph of 2L PDL-chained kernels per step"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    return 0
+    gbs = float(np.mean(nbytes)) / (us_step / 1e6) / 1e9
+    return {"workload": shape.name + f", M={M}, {L} layers", "metric": "tokens/s of the expert stack",
+            "value": M * steps / (ms / 1e3), "unit": "tok/s", "us_per_step": us_step,
+            "us_per_layer": us_step / L, "steps": steps, "warmup": warmup,
+            "bytes_per_step": float(np.mean(nbytes)), "gbs": gbs, "frac_of_peak": gbs / peak, "peak": peak,
+            "peak_kind": peak_kind, "clocks": clk.summary(), "gpu_launches_per_step": launches,
+            "launch": f"one cached CUDA graph of {launches} PDL-chained layer kernels per step"}
 
 
-def run_batched(args):
-    """Extra workloads (not the headline line): the batched MXFP4 layer,
-    H = I = 2880, 128 experts, top-4, M = 512 tokens (uniform router logits,
-    or +2 on experts 0..7), through moe_forward's tensor-core path."""
+def measure_batched(moe, shape, steps, warmup):
+    """The batched MXFP4 layer (H = I = 2880, 128 experts, top-4, M = 512)
+    through moe_forward's tensor-core path.  One layer is resident (1.7 GB of
+    expert weights, 13x L2); P = 4 input sets are cycled, so a step's weights
+    are never L2-resident from the previous step."""
     import torch
-    rank, world = _setup(args)
-    import bit_moe_decode_02_gb300 as moe
-    shape = synth.BATCHED if args.workload == "batched" else synth.BATCHED_SKEWED
     H, I, E, k, M = shape.hidden, shape.intermediate, shape.experts, shape.top_k, shape.tokens
     h = moe.moe_create(H, I, E, 1, M, k, moe.MOE_FMT_MXFP4, 32, 1)
     _load_all(moe, h, shape, 1)
-    W, K = args.warmup, args.steps
-    P = 4   # distinct input sets, cycled
+    P = 4
     ins = [synth.step_inputs(shape, 7000 + i) for i in range(P)]
     xd = [torch.from_numpy(x.view(np.int16)).cuda() for x, _, _ in ins]
     rd = [torch.from_numpy(r.view(np.int16)).cuda() for _, r, _ in ins]
@@ -420,12 +426,12 @@ def run_batched(args):
     gw, gk = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     torch.cuda.synchronize()
     with torch.cuda.graph(gw, stream=cap):
-        for s in range(W):
+        for s in range(warmup):
             moe.moe_forward(h, 0, xd[s % P], ld[s % P], M, k, rd[s % P], cap)
     with torch.cuda.graph(gk, stream=cap):
-        for s in range(K):
+        for s in range(steps):
             moe.moe_forward(h, 0, xd[s % P], ld[s % P], M, k, rd[s % P], cap)
-    launches = moe.moe_last_launches(h) * K
+    launches = moe.moe_last_launches(h)
     stream = torch.cuda.current_stream()
     gw.replay()
     torch.cuda.synchronize()
@@ -442,30 +448,78 @@ def run_batched(args):
         moe.moe_forward(h, 0, xd[i], ld[i], M, k, rd[i], stream)
         nbytes.append(moe.moe_last_bytes(h, stream))
     moe.moe_destroy(h)
-    us = 1e3 * ms / K
+    us = 1e3 * ms / steps
     flops = 2.0 * M * k * (2 * I * H + H * I)
     peak_hbm, kind = measured_peaks()
-    fp4_peak = _fp4_peak()
+    fp4_peak, fp4_src = _fp4_peak()
     gbs = float(np.mean(nbytes)) / (us / 1e6) / 1e9
     tflops = flops / (us / 1e6) / 1e12
-    line = {"workload": shape.name, "metric": "us per batched MoE layer; TFLOP/s and expert-weight GB/s",
-            "value": us, "unit": "us/layer", "steps": K, "warmup": W, "tokens": M,
-            "tflops": tflops, "tflops_peak_fp4": fp4_peak, "tflops_frac": tflops / fp4_peak,
-            "bytes_per_step": float(np.mean(nbytes)), "gbs": gbs, "hbm_frac": gbs / peak_hbm,
-            "hbm_peak": peak_hbm, "peak_kind": kind, "gpu_launches": launches,
-            "l2": "each step reads ~1.7 GB of expert weights (13x L2)",
-            "launch": "K steps of 7 kernels captured in one CUDA graph", "clocks": clk.summary()}
+    return {"workload": shape.name, "metric": "us per batched MoE layer; TFLOP/s and expert-weight GB/s",
+            "value": us, "unit": "us/layer", "steps": steps, "warmup": warmup, "tokens": M,
+            "tflops": tflops, "tflops_peak_fp4": fp4_peak, "tflops_peak_source": fp4_src,
+            "tflops_frac": tflops / fp4_peak, "bytes_per_step": float(np.mean(nbytes)), "gbs": gbs,
+            "hbm_frac": gbs / peak_hbm, "hbm_peak": peak_hbm, "peak_kind": kind,
+            "gpu_launches_per_step": launches,
+            "l2": "each step reads ~1.7 GB of expert weights (13x L2); 4 input sets cycled",
+            "launch": f"K steps of {launches} kernels captured in one CUDA graph", "clocks": clk.summary()}
+
+
+def extra_workloads(moe, args):
+    """The int4 stack and the batched layer (the MXFP4 stack runs on the
+    headline handle)."""
+    out = {}
+    shape = synth.INT4_STACK
+    L = shape.layers
+    h = moe.moe_create(shape.hidden, shape.intermediate, shape.experts, L, 4, shape.top_k, moe.MOE_FMT_INT4,
+                       shape.group, 0)
+    _load_all(moe, h, shape, L)
+    for M in (1, 4):
+        out[f"int4stack48_m{M}"] = measure_stack(moe, h, shape, L, M, args.extra_steps, 8)
+    moe.moe_destroy(h)
+    out["batched"] = measure_batched(moe, synth.BATCHED, max(args.extra_steps // 4, 8), 3)
+    out["batched_skewed"] = measure_batched(moe, synth.BATCHED_SKEWED, max(args.extra_steps // 4, 8), 3)
+    return out
+
+
+def run_stack(args):
+    """One stack workload alone (--workload stack24 / int4stack48)."""
+    rank, world = _setup(args)
+    import bit_moe_decode_02_gb300 as moe
+    shape = synth.GPTOSS_STACK if args.workload == "stack24" else synth.INT4_STACK
+    L = min(args.layers, shape.layers) if args.layers else shape.layers
+    fmt = moe.MOE_FMT_MXFP4 if shape.fmt == synth.FMT_MXFP4 else moe.MOE_FMT_INT4
+    h = moe.moe_create(shape.hidden, shape.intermediate, shape.experts, L, args.tokens, shape.top_k, fmt,
+                       shape.group, 1 if shape.has_bias else 0)
+    _load_all(moe, h, shape, L)
+    line = measure_stack(moe, h, shape, L, args.tokens, args.steps, args.warmup)
+    moe.moe_destroy(h)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_batched(args):
+    """One batched workload alone (--workload batched / batched_skewed)."""
+    rank, world = _setup(args)
+    import bit_moe_decode_02_gb300 as moe
+    shape = synth.BATCHED if args.workload == "batched" else synth.BATCHED_SKEWED
+    line = measure_batched(moe, shape, args.steps, args.warmup)
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
 
 
 def _fp4_peak():
-    """Dense FP4 tensor peak: the measured bf16 GEMM peak times the nominal
-    fp4 / bf16 ratio (13.5 / 2.25 PFLOP/s)."""
+    """Dense FP4 tensor peak in TFLOP/s and where it comes from: the measured
+    cuBLAS bf16 GEMM peak (MEASURED_PEAKS.json, burst) times the ratio of
+    NVIDIA's nominal dense GB300 rates, 13.5 PFLOP/s FP4 to 2.25 PFLOP/s bf16
+    (the figures without 2:4 sparsity); 1.9 PFLOP/s bf16 if no measurement."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    bf16 = json.load(open(p))["bf16_tflops"] if os.path.exists(p) else 1900.0
-    return bf16 * 13.5 / 2.25
+    if os.path.exists(p):
+        bf16, src = json.load(open(p))["bf16_tflops"], "measured bf16 (MEASURED_PEAKS.json) x 13.5/2.25"
+    else:
+        bf16, src = 1900.0, "fallback bf16 1.9 PFLOP/s x 13.5/2.25"
+    return bf16 * 13.5 / 2.25, src
 
 
 def main():
@@ -482,6 +536,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-steps", type=int, default=24)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--extra-steps", type=int, default=128,
+                    help="timed steps of the stack workloads in extra (batched: a quarter)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -7,8 +7,9 @@ library fails loudly (build it with ``python -m bit_moe_decode_02_gb300.build_ex
 
 The function names are the C names: moe_create, moe_load_experts, moe_forward,
 moe_forward_host, moe_forward_stack, moe_get_status, moe_debug_dequant,
-moe_debug_route, moe_debug_stack_trace, moe_last_bytes, moe_expert_bytes, moe_last_launches,
-moe_last_error, moe_forward_noalloc, moe_destroy.
+moe_debug_route, moe_debug_stack_trace, moe_debug_forward_f32, moe_debug_set_wait,
+moe_last_bytes, moe_expert_bytes, moe_last_launches, moe_last_error, moe_forward_noalloc,
+moe_destroy.
 """
 from __future__ import annotations
 
@@ -33,6 +34,7 @@ MOE_FMT_INT4 = 2
 EXPORTS = ("moe_create", "moe_load_experts", "moe_forward", "moe_forward_host",
            "moe_forward_stack", "moe_get_status", "moe_debug_dequant", "moe_debug_route",
            "moe_debug_stack_trace", "moe_debug_mx_quantize", "moe_debug_batched_h",
+           "moe_debug_forward_f32", "moe_debug_set_wait",
            "moe_last_bytes", "moe_expert_bytes", "moe_last_launches", "moe_last_error",
            "moe_forward_noalloc", "moe_destroy")
 
@@ -83,6 +85,10 @@ def lib() -> ctypes.CDLL:
         L.moe_debug_mx_quantize.restype = i
         L.moe_debug_batched_h.argtypes = [p, p, p, p]
         L.moe_debug_batched_h.restype = i
+        L.moe_debug_forward_f32.argtypes = [p, i, p, p, i, i, p, p, p]
+        L.moe_debug_forward_f32.restype = i
+        L.moe_debug_set_wait.argtypes = [p, i, i]
+        L.moe_debug_set_wait.restype = i
         L.moe_last_bytes.argtypes = [p, p, ctypes.POINTER(ll)]
         L.moe_last_bytes.restype = i
         L.moe_expert_bytes.argtypes = [p]
@@ -184,6 +190,15 @@ def moe_debug_mx_quantize(x, n, codes, scales, stream=None):
 
 def moe_debug_batched_h(h, codes, scales, stream=None):
     return _check(lib().moe_debug_batched_h(h, _ptr(codes), _ptr(scales), _stream(stream)))
+
+
+def moe_debug_forward_f32(h, layer, x, logits, M, top_k, out, out_f32, stream=None):
+    return _check(lib().moe_debug_forward_f32(h, layer, _ptr(x), _ptr(logits), M, top_k, _ptr(out),
+                                              _ptr(out_f32), _stream(stream)))
+
+
+def moe_debug_set_wait(h, spin_limit, skip_cta=-1):
+    return _check(lib().moe_debug_set_wait(h, spin_limit, skip_cta))
 
 
 def moe_last_bytes(h, stream=None) -> int:

@@ -65,7 +65,8 @@ struct moe_handle {
     // caller-layout tensor sizes in bytes (one layer, all experts)
     size_t gu_codes_b = 0, gu_scales_b = 0, gu_bias_b = 0;
     size_t dn_codes_b = 0, dn_scales_b = 0, dn_bias_b = 0;
-    // resident layout: per layer [gate_up slabs][down slabs][gu bias][dn bias]
+    // resident layout: per layer [gate_up slabs][down slabs][gu bias][dn bias];
+    // MXFP4 keeps no slabs (its kernels read the tile layout): [gu bias][dn bias]
     int sb = 0;                       // scale bytes per (segment, g) entry
     int gu_slab = 0, dn_slab = 0;     // bytes of one 16-row slab
     size_t gu_expert = 0, dn_expert = 0;
@@ -102,10 +103,14 @@ struct moe_handle {
     unsigned* counters = nullptr;     // done | hmax | slab_cnt | exit (see counter_words)
     int* stats = nullptr;   // distinct experts per layer of the last call
     int* status = nullptr;
-    // staging for moe_forward_host
-    uint16_t* st_x = nullptr;
-    uint16_t* st_out = nullptr;
-    float* st_logits = nullptr;
+    // staging for moe_forward_host: [x][residual / out][logits], on the device
+    // and in pinned host memory, so one copy each way moves a call's data
+    uint8_t* st_dev = nullptr;
+    uint8_t* st_host = nullptr;
+    size_t st_off_r = 0, st_off_l = 0, st_bytes = 0;
+    // cross-CTA waits of the MXFP4 decode layer (moe_debug_set_wait)
+    int spin_limit = moe::kSpinLimit;
+    int skip_cta = -1;
     // stack graphs
     cudaStream_t capture_stream = nullptr;
     std::vector<StackGraph> graphs;
@@ -173,9 +178,8 @@ void free_handle(moe_handle* h)
     cudaFree(h->counters);
     cudaFree(h->stats);
     cudaFree(h->status);
-    cudaFree(h->st_x);
-    cudaFree(h->st_out);
-    cudaFree(h->st_logits);
+    cudaFree(h->st_dev);
+    cudaFreeHost(h->st_host);
     cudaFree(h->tarena);
     cudaFree(h->tc_part);
     cudaFree(h->tc_gpart);
@@ -308,21 +312,25 @@ moe::DecodeTcParams tc_params(const moe_handle* h, int layer)
     p.I = c.intermediate;
     p.E = c.num_experts;
     p.smem_bytes = (int)h->tc_smem;
+    p.spin_limit = h->spin_limit;
+    p.skip_cta = h->skip_cta;
     return p;
 }
 
 // Kernel launches of one decode layer: the layer kernel (tensor-core MXFP4 or int4).
 int decode_launches(const moe_handle*) { return 1; }
 
-// The decode layer on the current kernel of this handle's format.
+// The decode layer on the current kernel of this handle's format; out_f32
+// (debug, nullable) also receives the result before its bf16 rounding.
 cudaError_t launch_decode(const moe_handle* h, int layer, const float* logits, const void* x, void* resid,
-                          int M, int k, cudaStream_t s)
+                          int M, int k, cudaStream_t s, float* out_f32 = nullptr)
 {
     if (h->tiles) {
         moe::DecodeTcParams p = tc_params(h, layer);
         p.logits = logits;
         p.x = static_cast<const uint16_t*>(x);
         p.resid = static_cast<uint16_t*>(resid);
+        p.out_f32 = out_f32;
         p.M = M;
         p.k = k;
         return moe::launch_decode_tc(p, h->tc_smem, h->num_sms, s);
@@ -331,6 +339,7 @@ cudaError_t launch_decode(const moe_handle* h, int layer, const float* logits, c
     p.logits = logits;
     p.x = static_cast<const uint16_t*>(x);
     p.resid = static_cast<uint16_t*>(resid);
+    p.out_f32 = out_f32;
     p.M = M;
     p.k = k;
     return moe::launch_layer(p, h->cfg.format, h->grid, s);
@@ -458,11 +467,14 @@ int moe_create(const moe_config* cfg, moe_handle** out)
     h->dn_codes_b = E * H * I / 2;
     h->dn_scales_b = E * H * sbi;
     h->dn_bias_b = c.has_bias ? E * H * 2 : 0;
+    const bool slabs = c.format == MOE_FMT_INT4;   // MXFP4 weights live in the tile layout only
     h->sb = moe::scale_entry_bytes(c.format, c.group);
-    h->gu_slab = moe::slab_bytes((int)H, h->sb);
-    h->dn_slab = moe::slab_bytes((int)I, h->sb);
-    h->gu_expert = (2 * I / moe::kSlabRows) * (size_t)h->gu_slab;
-    h->dn_expert = (H / moe::kSlabRows) * (size_t)h->dn_slab;
+    if (slabs) {
+        h->gu_slab = moe::slab_bytes((int)H, h->sb);
+        h->dn_slab = moe::slab_bytes((int)I, h->sb);
+        h->gu_expert = (2 * I / moe::kSlabRows) * (size_t)h->gu_slab;
+        h->dn_expert = (H / moe::kSlabRows) * (size_t)h->dn_slab;
+    }
     size_t off = align_up(E * h->gu_expert, 256);
     h->off_dn = off;
     off = align_up(off + E * h->dn_expert, 256);
@@ -470,16 +482,18 @@ int moe_create(const moe_config* cfg, moe_handle** out)
     off = align_up(off + h->gu_bias_b, 256);
     h->off_dn_bias = off;
     off = align_up(off + h->dn_bias_b, 256);
-    h->layer_stride = off;
-    h->slot_bytes = (int)align_up((size_t)(h->gu_slab > h->dn_slab ? h->gu_slab : h->dn_slab), 128);
-    h->nslots = (int)((moe::kSmemBudget - moe::kRedBytes - moe::kXfragBytes -
-                       2 * (size_t)decode_tokens(c) * I * sizeof(float)) / h->slot_bytes);
-    if (h->nslots > moe::kMaxSlots)
-        h->nslots = moe::kMaxSlots;
-    if (h->nslots < 2) {
-        free_handle(h);
-        return fail(MOE_ERR_UNSUPPORTED, "a 16-row weight slab (%d bytes) is too large for the "
-                    "shared-memory ring", h->slot_bytes);
+    h->layer_stride = off > 256 ? off : 256;
+    if (slabs) {
+        h->slot_bytes = (int)align_up((size_t)(h->gu_slab > h->dn_slab ? h->gu_slab : h->dn_slab), 128);
+        h->nslots = (int)((moe::kSmemBudget - moe::kRedBytes - moe::kXfragBytes -
+                           2 * (size_t)decode_tokens(c) * I * sizeof(float)) / h->slot_bytes);
+        if (h->nslots > moe::kMaxSlots)
+            h->nslots = moe::kMaxSlots;
+        if (h->nslots < 2) {
+            free_handle(h);
+            return fail(MOE_ERR_UNSUPPORTED, "a 16-row weight slab (%d bytes) is too large for the "
+                        "shared-memory ring", h->slot_bytes);
+        }
     }
 
     cudaError_t e = cudaGetDevice(&h->device);
@@ -492,7 +506,8 @@ int moe_create(const moe_config* cfg, moe_handle** out)
         free_handle(h);
         return cuda_fail(e, "cudaDeviceGetAttribute");
     }
-    {
+    h->grid = h->num_sms;   // one CTA per SM: every CTA of a layer is resident at once
+    if (slabs) {
         int per_sm = 0;
         moe::LayerParams lp{};
         lp.nslots = h->nslots;
@@ -508,10 +523,12 @@ int moe_create(const moe_config* cfg, moe_handle** out)
             free_handle(h);
             return fail(MOE_ERR_UNSUPPORTED, "the layer kernel does not fit on an SM");
         }
-        h->grid = h->num_sms;   // one CTA per SM: every CTA of a layer is resident at once
     }
     const size_t Mx = c.max_tokens, Kx = c.max_top_k, Md = decode_tokens(c);
     const size_t ncount = moe::counter_words((int)H);
+    h->st_off_r = align_up(Mx * H * 2, 256);
+    h->st_off_l = h->st_off_r + align_up(Mx * H * 2, 256);
+    h->st_bytes = h->st_off_l + Mx * E * sizeof(float);
     if ((rc = dev_alloc(&h->arena, h->layer_stride * c.num_layers, "expert weights")) ||
         (rc = dev_alloc(&h->special, (size_t)c.num_layers * E * 2 * sizeof(uint32_t), "flags")) ||
         (rc = dev_alloc(&h->h, Md * Kx * I * sizeof(float), "h workspace")) ||
@@ -519,11 +536,15 @@ int moe_create(const moe_config* cfg, moe_handle** out)
         (rc = dev_alloc(&h->counters, ncount * sizeof(unsigned), "counters")) ||
         (rc = dev_alloc(&h->stats, c.num_layers * sizeof(int), "stats")) ||
         (rc = dev_alloc(&h->status, sizeof(int), "status")) ||
-        (rc = dev_alloc(&h->st_x, Mx * H * 2, "staging x")) ||
-        (rc = dev_alloc(&h->st_out, Mx * H * 2, "staging out")) ||
-        (rc = dev_alloc(&h->st_logits, Mx * E * sizeof(float), "staging logits"))) {
+        (rc = dev_alloc(&h->st_dev, h->st_bytes, "staging"))) {
         free_handle(h);
         return rc;
+    }
+    if ((e = cudaHostAlloc((void**)&h->st_host, h->st_bytes, cudaHostAllocDefault)) != cudaSuccess) {
+        cudaGetLastError();
+        h->st_host = nullptr;
+        free_handle(h);
+        return fail(MOE_ERR_OOM, "cudaHostAlloc(%zu bytes) for the host staging failed", h->st_bytes);
     }
     if ((e = cudaMemset(h->counters, 0, ncount * sizeof(unsigned))) != cudaSuccess ||
         (e = cudaMemset(h->special, 0, (size_t)c.num_layers * E * 2 * sizeof(uint32_t))) != cudaSuccess ||
@@ -600,12 +621,12 @@ int moe_load_experts(moe_handle* h, int layer, const void* gu_codes, const void*
         (h->dn_bias_b && (e = cudaMemcpyAsync(base + h->off_dn_bias, dn_bias, h->dn_bias_b,
                                               cudaMemcpyDefault, s)) != cudaSuccess) ||
         (e = cudaMemsetAsync(special, 0, (size_t)c.num_experts * 2 * sizeof(uint32_t), s)) != cudaSuccess ||
-        (e = moe::launch_repack(c.format, c.group, st_guc, st_gus, c.num_experts, 2 * c.intermediate,
-                                c.hidden, base, (long long)h->gu_expert, h->gu_slab, special, 0, s)) !=
-            cudaSuccess ||
-        (e = moe::launch_repack(c.format, c.group, st_dnc, st_dns, c.num_experts, c.hidden,
-                                c.intermediate, base + h->off_dn, (long long)h->dn_expert, h->dn_slab,
-                                special, 1, s)) != cudaSuccess ||
+        (!h->tiles && (e = moe::launch_repack(c.format, c.group, st_guc, st_gus, c.num_experts, 2 * c.intermediate,
+                                              c.hidden, base, (long long)h->gu_expert, h->gu_slab, special, 0,
+                                              s)) != cudaSuccess) ||
+        (!h->tiles && (e = moe::launch_repack(c.format, c.group, st_dnc, st_dns, c.num_experts, c.hidden,
+                                              c.intermediate, base + h->off_dn, (long long)h->dn_expert,
+                                              h->dn_slab, special, 1, s)) != cudaSuccess) ||
         (h->tiles && (e = load_tiles(h, layer, st_guc, st_gus, st_dnc, st_dns, s)) != cudaSuccess) ||
         (e = cudaStreamSynchronize(s)) != cudaSuccess) {
         cudaStreamSynchronize(s);
@@ -617,8 +638,12 @@ int moe_load_experts(moe_handle* h, int layer, const void* gu_codes, const void*
     return MOE_OK;
 }
 
-int moe_forward(moe_handle* h, int layer, const void* x_bf16, const float* router_logits, int M,
-                int top_k, void* out_bf16, void* stream)
+}  // extern "C"
+
+namespace {
+
+int forward_impl(moe_handle* h, int layer, const void* x_bf16, const float* router_logits, int M,
+                 int top_k, void* out_bf16, float* out_f32, void* stream)
 {
     int rc = check_forward_args(h, M, top_k);
     if (rc != MOE_OK)
@@ -639,6 +664,7 @@ int moe_forward(moe_handle* h, int layer, const void* x_bf16, const float* route
         b.logits = router_logits;
         b.x = static_cast<const uint16_t*>(x_bf16);
         b.resid = static_cast<uint16_t*>(out_bf16);
+        b.out_f32 = out_f32;
         b.M = M;
         b.k = top_k;
         int launches = 0;
@@ -652,12 +678,44 @@ int moe_forward(moe_handle* h, int layer, const void* x_bf16, const float* route
         h->last_bk = top_k;
         return MOE_OK;
     }
-    cudaError_t e = launch_decode(h, layer, router_logits, x_bf16, out_bf16, M, top_k, (cudaStream_t)stream);
+    cudaError_t e = launch_decode(h, layer, router_logits, x_bf16, out_bf16, M, top_k, (cudaStream_t)stream,
+                                  out_f32);
     if (e != cudaSuccess)
         return cuda_fail(e, "moe_forward launch");
     h->last_layers = 1;
     h->last_first_layer = layer;
     h->last_launches = decode_launches(h);
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_forward(moe_handle* h, int layer, const void* x_bf16, const float* router_logits, int M,
+                int top_k, void* out_bf16, void* stream)
+{
+    return forward_impl(h, layer, x_bf16, router_logits, M, top_k, out_bf16, nullptr, stream);
+}
+
+int moe_debug_forward_f32(moe_handle* h, int layer, const void* x_bf16, const float* router_logits, int M,
+                          int top_k, void* out_bf16, float* out_f32, void* stream)
+{
+    if (!out_f32)
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_forward_f32: out_f32 is NULL");
+    if (reinterpret_cast<uintptr_t>(out_f32) & 15u)
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_forward_f32: out_f32 must be 16-byte aligned");
+    return forward_impl(h, layer, x_bf16, router_logits, M, top_k, out_bf16, out_f32, stream);
+}
+
+int moe_debug_set_wait(moe_handle* h, int spin_limit, int skip_cta)
+{
+    if (!h)
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_set_wait: handle is NULL");
+    if (spin_limit < 0 || skip_cta < -1)
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_set_wait: spin_limit must be >= 0, skip_cta >= -1");
+    h->spin_limit = spin_limit == 0 ? moe::kSpinLimit : spin_limit;
+    h->skip_cta = skip_cta;
     return MOE_OK;
 }
 
@@ -669,19 +727,31 @@ int moe_forward_host(moe_handle* h, int layer, const void* x_bf16, const float* 
         return rc;
     if (!x_bf16 || !router_logits || !out_bf16)
         return fail(MOE_ERR_INVALID_ARG, "moe_forward_host: x, logits and out must not be NULL");
+    if (layer < 0 || layer >= h->cfg.num_layers)
+        return fail(MOE_ERR_INVALID_ARG, "layer=%d out of range 0..%d", layer, h->cfg.num_layers - 1);
+    if (!h->loaded[layer])
+        return fail(MOE_ERR_NOT_LOADED, "moe_forward_host: layer %d has no experts loaded", layer);
     cudaStream_t s = (cudaStream_t)stream;
     const size_t nb = (size_t)M * h->cfg.hidden * 2, nl = (size_t)M * h->cfg.num_experts * 4;
+    // x, the residual and the logits packed into the handle's pinned staging
+    // buffer by the host, so that one copy moves them; one copy brings the
+    // result back (the pages' lesson on per-token host work: keep it to a
+    // fixed, small amount)
+    std::memcpy(h->st_host, x_bf16, nb);
+    std::memcpy(h->st_host + h->st_off_r, out_bf16, nb);
+    std::memcpy(h->st_host + h->st_off_l, router_logits, nl);
     cudaError_t e;
-    if ((e = cudaMemcpyAsync(h->st_x, x_bf16, nb, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(h->st_logits, router_logits, nl, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(h->st_out, out_bf16, nb, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    if ((e = cudaMemcpyAsync(h->st_dev, h->st_host, h->st_off_l + nl, cudaMemcpyHostToDevice, s)) != cudaSuccess)
         return cuda_fail(e, "moe_forward_host upload");
-    rc = moe_forward(h, layer, h->st_x, h->st_logits, M, top_k, h->st_out, stream);
+    rc = moe_forward(h, layer, h->st_dev, reinterpret_cast<const float*>(h->st_dev + h->st_off_l), M, top_k,
+                     h->st_dev + h->st_off_r, stream);
     if (rc != MOE_OK)
         return rc;
-    if ((e = cudaMemcpyAsync(out_bf16, h->st_out, nb, cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
+    if ((e = cudaMemcpyAsync(h->st_host + h->st_off_r, h->st_dev + h->st_off_r, nb, cudaMemcpyDeviceToHost, s)) !=
+            cudaSuccess ||
         (e = cudaStreamSynchronize(s)) != cudaSuccess)
         return cuda_fail(e, "moe_forward_host download");
+    std::memcpy(out_bf16, h->st_host + h->st_off_r, nb);
     return MOE_OK;
 }
 
@@ -840,9 +910,21 @@ int moe_debug_dequant(moe_handle* h, int layer, int expert, int proj, float* out
         return fail(MOE_ERR_INVALID_ARG, "moe_debug_dequant: layer/expert/proj out of range");
     if (!h->loaded[layer])
         return fail(MOE_ERR_NOT_LOADED, "moe_debug_dequant: layer %d has no experts loaded", layer);
-    moe::LayerParams p = layer_params(h, layer);
     const int N = proj == 0 ? 2 * c.intermediate : c.hidden;
     const int K = proj == 0 ? c.hidden : c.intermediate;
+    if (h->tiles) {
+        // the bytes the tensor-core kernels stream (interleaved gate/up tiles,
+        // scale chunks in tensor-memory order), decoded back to caller order
+        const uint8_t* tb = h->tarena + (size_t)layer * h->t_layer_stride;
+        const uint8_t* src = proj == 0 ? tb + (size_t)expert * h->t_gu_expert
+                                       : tb + h->t_off_dn + (size_t)expert * h->t_dn_expert;
+        cudaError_t e = moe::launch_dequant_tiles(src, N, K, proj == 0 ? c.intermediate : 0, out_dev,
+                                                  (cudaStream_t)stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "moe_debug_dequant launch");
+        return MOE_OK;
+    }
+    moe::LayerParams p = layer_params(h, layer);
     const uint8_t* slabs = proj == 0 ? p.gu + (size_t)expert * h->gu_expert
                                      : p.dn + (size_t)expert * h->dn_expert;
     cudaError_t e = moe::launch_dequant(c.format, c.group, slabs, N, K, proj == 0 ? h->gu_slab : h->dn_slab,

@@ -592,12 +592,20 @@ __global__ void combine_kernel(BatchParams p)
         sum[0] += wq * a.x; sum[1] += wq * a.y; sum[2] += wq * a.z; sum[3] += wq * a.w;
         sum[4] += wq * b.x; sum[5] += wq * b.y; sum[6] += wq * b.z; sum[7] += wq * b.w;
     }
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        v[i] = acc[i] + sum[i];
     uint32_t o[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-        o[i] = (uint32_t)f2bf16_rne(acc[2 * i] + sum[2 * i]) |
-               ((uint32_t)f2bf16_rne(acc[2 * i + 1] + sum[2 * i + 1]) << 16);
+        o[i] = (uint32_t)f2bf16_rne(v[2 * i]) | ((uint32_t)f2bf16_rne(v[2 * i + 1]) << 16);
     *rp = make_uint4(o[0], o[1], o[2], o[3]);
+    if (p.out_f32) {
+        float4* f = reinterpret_cast<float4*>(p.out_f32 + (size_t)m * p.H + j0);
+        f[0] = make_float4(v[0], v[1], v[2], v[3]);
+        f[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
 }
 
 // --------------------------------------------------------------- repacking
@@ -648,6 +656,39 @@ __global__ void repack_tiles_kernel(const uint8_t* __restrict__ codes, const uin
                 v = scales[((size_t)e * src_rows + src_row(n, ilv)) * (K / 32) + blk];
             out[(long long)e * expert_bytes + (long long)N * (K / 2) + rem] = v;
         }
+    }
+}
+
+// Element (n, k) of one projection in caller row order, read back from the
+// tile layout the tensor-core kernels stream: its E2M1 code times its E8M0
+// scale 2^(s - 127), in fp32 (exact; byte 0 gives 2^-127, byte 255 NaN, and a
+// product past the fp32 range overflows to infinity).
+__global__ void dequant_tiles_kernel(const uint8_t* __restrict__ tiles, int N, int K, int ilv,
+                                     float* __restrict__ out)
+{
+    const int CH = ceil_div(K, 128);
+    const long long total = (long long)N * K;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int nc = (int)(idx / K), k = (int)(idx % K);
+        int n = nc;   // row in the tile order
+        if (ilv) {
+            const int up = nc >= ilv, rr = up ? nc - ilv : nc;
+            n = (rr / 64) * kRowTile + (up ? 64 : 0) + rr % 64;
+        }
+        const int t = n / kRowTile, r = n % kRowTile;
+        const int R = N - t * kRowTile < kRowTile ? N - t * kRowTile : kRowTile;
+        const int s = k / 64, b = (k % 64) / 2;
+        const uint8_t byte = tiles[(long long)t * kRowTile * (K / 2) + (long long)s * R * 32 + (r >> 3) * 256 +
+                                   (b >> 4) * 128 + (r & 7) * 16 + (b & 15)];
+        const uint32_t code = (k & 1) ? byte >> 4 : byte & 0xfu;
+        const int blk = k / 32;
+        const uint32_t sbyte = tiles[(long long)N * (K / 2) + (long long)(t * CH + blk / 4) * kSfChunk +
+                                     (r & 31) * 16 + (r >> 5) * 4 + (blk & 3)];
+        const float mag[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+        const float v = (code & 8u) ? -mag[code & 7u] : mag[code & 7u];
+        const float sc = __uint_as_float(sbyte == 0u ? 0x00400000u : (sbyte == 255u ? 0x7fc00000u : sbyte << 23));
+        out[idx] = v * sc;
     }
 }
 
@@ -726,6 +767,14 @@ cudaError_t launch_repack_tiles(const uint8_t* codes, const uint8_t* scales, int
     const long long blocks = (work + 255) / 256 < 65536 ? (work + 255) / 256 : 65536;
     repack_tiles_kernel<<<(unsigned)blocks, 256, 0, stream>>>(codes, scales, E, src_rows, N, K, interleave, out,
                                                               expert_bytes);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_tiles(const uint8_t* tiles, int N, int K, int interleave, float* out,
+                                 cudaStream_t stream)
+{
+    const long long total = (long long)N * K;
+    dequant_tiles_kernel<<<blocks_for(total, 256), 256, 0, stream>>>(tiles, N, K, interleave, out);
     return cudaGetLastError();
 }
 

@@ -625,7 +625,10 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(const LayerParams p)
                             for (int k2 = 0; k2 < p.k; ++k2)
                                 acc = fmaf(rs.wt[m][k2], __ldcg(p.ypart + ((size_t)m * p.kmax + k2) * p.H + jj), acc);
                             uint16_t* o = p.resid + (size_t)m * p.H + jj;
-                            *o = f32_to_bf16_rn(bf16_to_f32(__ldcg(o)) + acc);
+                            const float v = bf16_to_f32(__ldcg(o)) + acc;
+                            *o = f32_to_bf16_rn(v);
+                            if (p.out_f32)
+                                p.out_f32[(size_t)m * p.H + jj] = v;
                         }
                         __syncwarp();
                         if (lane == 0)
@@ -1034,8 +1037,8 @@ size_t layer_smem_bytes(const LayerParams& p)
 
 cudaError_t prepare_layer_kernel(int fmt, int group, size_t smem, int* blocks_per_sm)
 {
-    if (fmt == FMT_MXFP4)
-        return prepare_t<FMT_MXFP4, 4>(smem, blocks_per_sm);
+    if (fmt != FMT_INT4)
+        return cudaErrorInvalidValue;
     if (scale_entry_bytes(fmt, group) == 8)
         return prepare_t<FMT_INT4, 8>(smem, blocks_per_sm);
     return prepare_t<FMT_INT4, 4>(smem, blocks_per_sm);
@@ -1043,8 +1046,8 @@ cudaError_t prepare_layer_kernel(int fmt, int group, size_t smem, int* blocks_pe
 
 cudaError_t launch_layer(const LayerParams& p, int fmt, int grid, cudaStream_t stream)
 {
-    if (fmt == FMT_MXFP4)
-        return launch_layer_t<FMT_MXFP4, 4>(p, grid, stream);
+    if (fmt != FMT_INT4)
+        return cudaErrorInvalidValue;
     if (scale_entry_bytes(fmt, p.group) == 8)
         return launch_layer_t<FMT_INT4, 8>(p, grid, stream);
     return launch_layer_t<FMT_INT4, 4>(p, grid, stream);
@@ -1056,10 +1059,9 @@ cudaError_t launch_repack(int fmt, int group, const uint8_t* codes, const uint8_
 {
     const long long work = (long long)E * (N / kSlabRows) * (K / 64) * (128 + 8);
     const int blocks = (int)((work + 255) / 256 < 65536 ? (work + 255) / 256 : 65536);
-    if (fmt == FMT_MXFP4)
-        repack_kernel<FMT_MXFP4, 4><<<blocks, 256, 0, stream>>>(codes, scales, E, N, K, group, out,
-                                                                expert_bytes, slab_bytes, special, proj);
-    else if (scale_entry_bytes(fmt, group) == 8)
+    if (fmt != FMT_INT4)
+        return cudaErrorInvalidValue;
+    if (scale_entry_bytes(fmt, group) == 8)
         repack_kernel<FMT_INT4, 8><<<blocks, 256, 0, stream>>>(codes, scales, E, N, K, group, out,
                                                                expert_bytes, slab_bytes, special, proj);
     else
@@ -1073,9 +1075,9 @@ cudaError_t launch_dequant(int fmt, int group, const uint8_t* slabs, int N, int 
 {
     const long long total = (long long)N * K;
     const int blocks = (int)((total + 255) / 256 < 8192 ? (total + 255) / 256 : 8192);
-    if (fmt == FMT_MXFP4)
-        dequant_kernel<FMT_MXFP4, 4><<<blocks, 256, 0, stream>>>(slabs, N, K, slab_bytes, out);
-    else if (scale_entry_bytes(fmt, group) == 8)
+    if (fmt != FMT_INT4)
+        return cudaErrorInvalidValue;
+    if (scale_entry_bytes(fmt, group) == 8)
         dequant_kernel<FMT_INT4, 8><<<blocks, 256, 0, stream>>>(slabs, N, K, slab_bytes, out);
     else
         dequant_kernel<FMT_INT4, 4><<<blocks, 256, 0, stream>>>(slabs, N, K, slab_bytes, out);

@@ -86,12 +86,12 @@ constexpr int kHTerm = kHTermBytes;              // h' terms of a unit: one k-st
 __device__ __forceinline__ int rows_for(int M) { return M * kTerms <= 16 ? 16 : 32; }
 
 // Shared memory past the stage ring: the layer's x terms (H/64 k-step atoms,
-// then ceil(H/128) scale chunks), three h'-term buffers (two for whole units,
+// then ceil(H/128) scale chunks, then 2^-S_m of each token), three h'-term buffers (two for whole units,
 // one for a split unit's), the up-sum exchange (2 warps x 32 lanes x float4)
 // and the CTA's fp32 output copy [H][M].
 __device__ __forceinline__ uint32_t xterm_bytes(int H, int atom)
 {
-    return (uint32_t)(H / 64) * atom + (uint32_t)ceil_div(H, 128) * kSfChunk;
+    return (uint32_t)(H / 64) * atom + (uint32_t)ceil_div(H, 128) * kSfChunk + 16;
 }
 __device__ __forceinline__ uint32_t tail_bytes(int H, int M, int atom)
 {
@@ -361,25 +361,79 @@ __device__ __forceinline__ void warp_terms_rows(float (&r)[kMaxTokens], int m0, 
     }
 }
 
-// 1 / sqrt(mean(v^2) + 1e-6) of a bf16 row of n elements (n % 8 == 0), the
-// same value on every lane of the warp.
-__device__ __forceinline__ float row_inv_rms(const uint16_t* row, int n, int lane)
+// A bf16 row of n elements (n % 8 == 0, n <= kMaxK) held by a warp: 16-byte
+// vector i at lane i % 32, step i / 32 (the loads all in flight together).
+constexpr int kRowVec = kMaxK / 8 / 32;
+__device__ __forceinline__ void load_row(const uint16_t* row, int n, int lane, uint4 (&v)[kRowVec])
+{
+#pragma unroll
+    for (int z = 0; z < kRowVec; ++z) {
+        const int i = lane + 32 * z;
+        v[z] = i < n / 8 ? __ldcg(reinterpret_cast<const uint4*>(row) + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// Element 32 kb + lane of a row held as above: its vector 4 kb + lane / 8 is
+// at step (4 kb) / 32 (the same for the four vectors of a block) on lane
+// (4 kb) % 32 + lane / 8.
+__device__ __forceinline__ uint16_t row_elem(const uint4 (&v)[kRowVec], int kb, int lane)
+{
+    const int zs = (4 * kb) >> 5;
+    uint4 u = v[0];
+#pragma unroll
+    for (int z = 1; z < kRowVec; ++z)
+        if (z == zs)
+            u = v[z];
+    const int src = ((4 * kb) & 31) + (lane >> 3);
+    const uint32_t w0 = __shfl_sync(0xffffffffu, u.x, src), w1 = __shfl_sync(0xffffffffu, u.y, src);
+    const uint32_t w2 = __shfl_sync(0xffffffffu, u.z, src), w3 = __shfl_sync(0xffffffffu, u.w, src);
+    const int wi = (lane & 7) >> 1;
+    const uint32_t w = wi == 0 ? w0 : (wi == 1 ? w1 : (wi == 2 ? w2 : w3));
+    return (uint16_t)((lane & 1) ? w >> 16 : w & 0xffffu);
+}
+
+// Over a row held as above, the same values on every lane of the warp: the
+// largest magnitude (as bf16 bits) and, with want_rms, 1 / sqrt(mean(v^2) + 1e-6).
+__device__ __forceinline__ float row_stats(const uint4 (&v)[kRowVec], int n, bool want_rms, uint32_t& amax)
 {
     float a = 0.f;
-    for (int i = lane; i < n / 8; i += 32) {
-        const uint4 w = __ldcg(reinterpret_cast<const uint4*>(row) + i);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    uint32_t mx = 0u;
 #pragma unroll
-        for (int z = 0; z < 4; ++z) {
-            const float lo = __uint_as_float(ws[z] << 16), hi = __uint_as_float(ws[z] & 0xffff0000u);
+    for (int z = 0; z < kRowVec; ++z) {
+        const uint32_t ws[4] = {v[z].x, v[z].y, v[z].z, v[z].w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const float lo = __uint_as_float(ws[c] << 16), hi = __uint_as_float(ws[c] & 0xffff0000u);
             a = fmaf(lo, lo, a);
             a = fmaf(hi, hi, a);
+            mx = max(mx, max(ws[c] & 0x7fffu, (ws[c] >> 16) & 0x7fffu));
         }
     }
+    amax = __reduce_max_sync(0xffffffffu, mx);
+    if (!want_rms)
+        return 1.f;
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1)
         a += __shfl_xor_sync(0xffffffffu, a, off);
     return 1.0f / sqrtf(a / (float)n + 1e-6f);
+}
+
+// The power-of-two factor 2^S (S >= 0) that a token's activation is multiplied
+// by before it is cut into MX terms, from its largest magnitude amax.  Term j
+// of a block has the shared exponent X0 - 2j, and E8M0 holds no exponent below
+// -127, so a block with X0 < -113 would lose its last terms.  S = 0 unless
+// the token's largest block exponent X0 = floor(log2 amax) - 2 is below -100;
+// then S lifts it to -100.  Blocks far below the token's largest lose terms,
+// at 2^-13 or less of its largest block's contribution.  The sums are
+// multiplied by 2^-S afterwards (exact: both are powers of two, and no sum can
+// overflow, since |x| 2^S < 2^-97 and |w| < 2^130).
+__device__ __forceinline__ int token_shift(float amax)
+{
+    const uint32_t u = __float_as_uint(amax);
+    if (u == 0u)
+        return 0;
+    const int e = u >= 0x00800000u ? (int)(u >> 23) - 127 : (31 - __clz((int)u)) - 149;   // floor(log2 amax)
+    return -98 - e > 0 ? -98 - e : 0;
 }
 
 // Adds the down products of tiles [0, n) of an accumulator region (tile j at
@@ -621,19 +675,28 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
         const int q = warp - 2, te = tid - 64;
         if (b < nitems) {
             int cm = -1;
-            float inv = 1.f;
+            float inv = 1.f, sx = 1.f;
+            uint4 rowv[kRowVec];
             for (int it = b + G * q; it < nitems; it += 4 * G) {
                 const int m = it / nblk, kb = it - m * nblk;
-                float v;
-                if (p.x) {
-                    v = bf16f(__ldcg(p.x + (size_t)m * p.H + 32 * kb + lane));
-                } else {
-                    if (m != cm) {
-                        inv = row_inv_rms(p.resid + (size_t)m * p.H, p.H, lane);
-                        cm = m;
-                    }
-                    v = bf16f(f2bf16_rne(bf16f(__ldcg(p.resid + (size_t)m * p.H + 32 * kb + lane)) * inv));
+                if (m != cm) {
+                    // the token's row once; its shift S from its largest |x| (for
+                    // x = bf16(r inv), the rounding is monotone, so that is bf16(max|r| inv))
+                    load_row((p.x ? p.x : p.resid) + (size_t)m * p.H, p.H, lane, rowv);
+                    uint32_t ab;
+                    inv = row_stats(rowv, p.H, p.x == nullptr, ab);
+                    float amax = bf16f((uint16_t)ab);
+                    if (!p.x)
+                        amax = bf16f(f2bf16_rne(amax * inv));
+                    const int S = token_shift(amax);
+                    sx = __uint_as_float((uint32_t)(127 + S) << 23);
+                    if (lane == 0)   // every builder of token m writes the same 2^-S
+                        reinterpret_cast<float*>(p.xt + (long long)KSH * atom + CHH * kSfChunk)[m] =
+                            __uint_as_float((uint32_t)(127 - S) << 23);
+                    cm = m;
                 }
+                const uint16_t raw = row_elem(rowv, kb, lane);
+                const float v = (p.x ? bf16f(raw) : bf16f(f2bf16_rne(bf16f(raw) * inv))) * sx;
                 float r4[kMaxTokens] = {v, 0.f, 0.f, 0.f};
                 warp_terms_rows<1>(r4, m, kb, p.xt, p.xt + (long long)KSH * atom, atom, lane);
             }
@@ -649,7 +712,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
             int spins = 0;
 #pragma unroll 1
             while (ld_acquire_u64(p.xcnt) < tgt) {
-                if (++spins > (1 << 24)) {
+                if (++spins > p.spin_limit) {
                     atomicExch(p.status, MOE_ERR_DEVICE_TIMEOUT);
                     break;
                 }
@@ -657,9 +720,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
             // the whole layer's x terms into shared memory, once
             asm volatile("fence.proxy.async.global;" ::: "memory");   // published x terms -> bulk reads
             const uint32_t ab = (uint32_t)KSH * atom, sb = (uint32_t)CHH * kSfChunk;
-            mbar_expect_tx(&sh.xfull, ab + sb);
+            mbar_expect_tx(&sh.xfull, ab + sb + 16);
             bulk_copy(xs, p.xt, ab, &sh.xfull);
-            bulk_copy(xs + ab, p.xt + (size_t)KSH * atom, sb, &sh.xfull);
+            bulk_copy(xs + ab, p.xt + (size_t)KSH * atom, sb + 16, &sh.xfull);
         }
         __syncwarp();   // lane 0 rejoins before the warp's collective instructions
         for (int i = te; i < p.H * M; i += kEpi)
@@ -923,7 +986,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
             int spins = 0;
             bool all = false;
 #pragma unroll 1
-            while (!all && ++spins < (1 << 24))
+            while (!all && ++spins < p.spin_limit)
                 all = __all_sync(0xffffffffu, lane >= pl.S || ld_acquire_u32(p.pflag + b0 + lane) == tag);
             if (!all && lane == 0)
                 atomicExch(p.status, MOE_ERR_DEVICE_TIMEOUT);
@@ -958,8 +1021,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                 float hv[kMaxTokens];
 #pragma unroll
                 for (int m = 0; m < kMaxTokens; ++m) {
-                    const float gg = g[kb][m] + bg[kb];
-                    hv[m] = m < M ? sh.wslot[s][m] * (gg / (1.0f + expf(-gg))) * (u[kb][m] + bu[kb]) : 0.f;
+                    // a token that did not choose this expert gets exactly 0 (its sums may
+                    // even be infinite: the expert's weights were applied to every column)
+                    const float gg = g[kb][m] + bg[kb], wt = sh.wslot[s][m];
+                    hv[m] = m < M && wt != 0.f ? wt * (gg / (1.0f + expf(-gg))) * (u[kb][m] + bu[kb]) : 0.f;
                 }
                 switch (M) {
                 case 1: warp_terms_rows<1>(hv, 0, kb, hb, hb + 1024, atom, lane); break;
@@ -991,8 +1056,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                 float hv[kMaxTokens];
 #pragma unroll
                 for (int m = 0; m < kMaxTokens; ++m) {
-                    const float g = sm[m] + bg;
-                    hv[m] = m < M ? sh.wslot[s][m] * (g / (1.0f + expf(-g))) * (us[m] + bu) : 0.f;
+                    // 0 for a token that did not choose this expert, whatever its sums
+                    const float g = sm[m] + bg, wt = sh.wslot[s][m];
+                    hv[m] = m < M && wt != 0.f ? wt * (g / (1.0f + expf(-g))) * (us[m] + bu) : 0.f;
                 }
                 switch (M) {   // one copy of the code runs
                 case 1: warp_terms_rows<1>(hv, 0, q, dst, dst + 1024, atom, lane); break;
@@ -1003,6 +1069,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
             }
         };
         uint32_t kk = 0;
+        // 2^-S_m of each token: the gate/up sums carry the x terms' shift
+        float ush[kMaxTokens] = {1.f, 1.f, 1.f, 1.f};
+        if (nitem > 0) {
+            mbar_wait(&sh.xfull, 0, p.status);
+#pragma unroll
+            for (int m = 0; m < kMaxTokens; ++m)
+                if (m < M)
+                    ush[m] = reinterpret_cast<const float*>(xs + KSH * atom + CHH * kSfChunk)[m];
+        }
         for (int k = 0; k < nitem; ++k) {
             int kind, i;
             item_of(pl, k, kind, i);
@@ -1047,6 +1122,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                         }
                     }
                 }
+#pragma unroll
+                for (int m = 0; m < kMaxTokens; ++m)
+                    sm[m] *= ush[m];
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
@@ -1146,11 +1224,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
     tc_fence_before();
     __syncthreads();
     if (tid == 0) {
-        const unsigned long long tgt = count_target(atom_add_release_u64(p.done, 1ull), G);
+        // (a debug run may have one CTA skip its arrival, to test that the others give up)
+        const unsigned long long tgt =
+            count_target(b == p.skip_cta ? ld_acquire_u64(p.done) : atom_add_release_u64(p.done, 1ull), G);
         int spins = 0;
 #pragma unroll 1
         while (ld_acquire_u64(p.done) < tgt) {
-            if (++spins > (1 << 24)) {
+            if (++spins > p.spin_limit) {
                 atomicExch(p.status, MOE_ERR_DEVICE_TIMEOUT);
                 break;
             }
@@ -1195,9 +1275,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                     mine = sums[z];
             if (lane < 4) {
                 const int el = (f0 + j) * 4 + lane, row = el / V, m = el - row * V;
-                if (m < M)
-                    p.resid[(size_t)m * p.H + row] =
-                        f2bf16_rne((j < kFinSlots ? sh.fin[j][lane] : fin_term(j, lane)) + mine);
+                if (m < M) {
+                    const float v = (j < kFinSlots ? sh.fin[j][lane] : fin_term(j, lane)) + mine;
+                    p.resid[(size_t)m * p.H + row] = f2bf16_rne(v);
+                    if (p.out_f32)
+                        p.out_f32[(size_t)m * p.H + row] = v;
+                }
             }
         }
     }

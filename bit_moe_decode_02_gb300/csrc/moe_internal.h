@@ -57,6 +57,7 @@ struct LayerParams {
     unsigned* exit_cnt;         // [1] CTAs finished (zero between calls)
     int* status;                // device status word
     int* nu_out;                // distinct experts of this call (written by CTA 0)
+    float* out_f32;             // [M][H] fp32 result before the bf16 rounding, or nullptr
     long long gu_expert_bytes, dn_expert_bytes;
     int gu_slab_bytes, dn_slab_bytes;
     int H, I, E, M, k, kmax, mmax, group;
@@ -151,6 +152,7 @@ struct BatchParams {
     float* y;                   // [M*k][H], slot order
     int* status;
     int* nu_out;                // experts with at least one token (written by plan_kernel)
+    float* out_f32;             // [M][H] fp32 result before the bf16 rounding, or nullptr
     int H, I, E, M, k;
     int max_tiles;
 };
@@ -195,12 +197,21 @@ struct DecodeTcParams {
     unsigned long long* done;   // [1] output copies stored, G per call (only grows)
     int* status;
     int* nu_out;
+    float* out_f32;             // [M][H] fp32 result before the bf16 rounding, or nullptr
     int H, I, E, M, k;
     int smem_bytes;             // dynamic shared memory of the layer kernel
+    int spin_limit;             // polls before a cross-CTA wait gives up (kSpinLimit by default)
+    int skip_cta;               // debug: this CTA skips its grid-barrier arrival (-1: none)
 };
+constexpr int kSpinLimit = 1 << 24;
 
 constexpr int kHTermBytes = 1024 + kSfChunk;   // one k-step of activation terms + its scale chunk
-inline size_t tc_terms_bytes(int K) { return (size_t)(K / 64) * 1024 + (size_t)ceil_div(K, 128) * kSfChunk; }
+// x terms of a layer: k-step atoms, scale chunks, then 16 bytes holding 2^-S_m
+// for each token m (S_m >= 0: the power-of-two shift the token's terms carry)
+inline size_t tc_terms_bytes(int K)
+{
+    return (size_t)(K / 64) * 1024 + (size_t)ceil_div(K, 128) * kSfChunk + 16;
+}
 inline size_t tc_part_bytes(int G, int H) { return (size_t)G * H * 4 * sizeof(float); }
 constexpr int kTcCounterWords = 2;   // xcnt, done (64-bit)
 cudaError_t prepare_decode_tc(size_t smem);
@@ -208,6 +219,10 @@ size_t decode_tc_static_smem();
 cudaError_t launch_decode_tc(const DecodeTcParams& p, size_t smem, int grid, cudaStream_t stream);
 
 // Debug kernels.
+// One expert projection of the tile layout back to fp32 in caller row order
+// (gate_up: interleave = I, rows [0, I) gate and [I, 2I) up; down: 0).
+cudaError_t launch_dequant_tiles(const uint8_t* tiles, int N, int K, int interleave, float* out,
+                                 cudaStream_t stream);
 cudaError_t launch_dequant(int fmt, int group, const uint8_t* slabs, int N, int K, int slab_bytes,
                            float* out, cudaStream_t stream);
 cudaError_t launch_route(const float* logits, int M, int E, int k, int* idx, float* w,

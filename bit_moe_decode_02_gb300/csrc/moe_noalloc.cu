@@ -397,7 +397,6 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up_kernel(const LayerParams 
     constexpr int S = R * MT;
     __shared__ RouteSmem rs;
     __shared__ float red[kThreads / 32][2][S];
-    __shared__ float nrm[kThreads / 32][MT];
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     pdl_wait();   // the previous kernel (the prior layer, or whoever wrote x/logits) is done
@@ -430,8 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up_kernel(const LayerParams 
         return;   // warps left over when GW does not divide the CTA; no block barrier follows
     const int bar_id = 1 + sp.g, bar_n = sp.GW * 32;
 
-    // x slice of every token in registers (fp32).  Without x, normalise the
-    // residual: x = bf16(r / sqrt(mean(r^2) + 1e-6)).
+    // x slice of every token in registers (fp32)
     float xr[MT][KT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
@@ -447,35 +445,6 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up_kernel(const LayerParams 
                 xr[m][8 * c + 2 * i] = bf16_to_f32((uint16_t)(u4[i] & 0xffffu));
                 xr[m][8 * c + 2 * i + 1] = bf16_to_f32((uint16_t)(u4[i] >> 16));
             }
-        }
-    }
-    if (!p.x) {
-        float ss[MT];
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            float a = 0.0f;
-#pragma unroll
-            for (int i = 0; i < KT; ++i)
-                a = fmaf(xr[m][i], xr[m][i], a);
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1)
-                a += __shfl_xor_sync(0xffffffffu, a, off);
-            ss[m] = a;
-        }
-        if (lane == 0)
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-                nrm[warp][m] = ss[m];
-        named_barrier(bar_id, bar_n);
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            float tot = 0.0f;
-            for (int j = 0; j < sp.GW; ++j)
-                tot += nrm[sp.g * sp.GW + j][m];
-            const float inv = 1.0f / sqrtf(tot / (float)p.H + 1e-6f);
-#pragma unroll
-            for (int i = 0; i < KT; ++i)
-                xr[m][i] = bf16_to_f32(f32_to_bf16_rn(xr[m][i] * inv));
         }
     }
 
@@ -768,8 +737,15 @@ extern "C" int moe_forward_noalloc(const moe_config* cfg, const void* gu_codes, 
         return fail(MOE_ERR_INVALID_ARG, "a required pointer is NULL");
     if (cfg->has_bias && (!gu_bias || !dn_bias))
         return fail(MOE_ERR_INVALID_ARG, "has_bias is set but a bias pointer is NULL");
-    if (((uintptr_t)x_bf16 | (uintptr_t)out_bf16 | (uintptr_t)gu_codes | (uintptr_t)dn_codes) & 15u)
-        return fail(MOE_ERR_INVALID_ARG, "x, out and the code arrays must be 16-byte aligned");
+    // x, out and the codes are read and written with 16-byte vector accesses, and
+    // the scale arrays are prefetched into L2 in runs that must start on 16-byte
+    // boundaries; the biases are bf16 and the logits fp32 loads
+    if (((uintptr_t)x_bf16 | (uintptr_t)out_bf16 | (uintptr_t)gu_codes | (uintptr_t)dn_codes |
+         (uintptr_t)gu_scales | (uintptr_t)dn_scales) & 15u)
+        return fail(MOE_ERR_INVALID_ARG, "x, out and the code and scale arrays must be 16-byte aligned");
+    if (((uintptr_t)router_logits & 3u) ||
+        (cfg->has_bias && (((uintptr_t)gu_bias | (uintptr_t)dn_bias) & 1u)))
+        return fail(MOE_ERR_INVALID_ARG, "router_logits must be 4-byte and the biases 2-byte aligned");
     const uintptr_t xa = (uintptr_t)x_bf16, oa = (uintptr_t)out_bf16, nb = (uintptr_t)M * H * 2;
     if (xa < oa + nb && oa < xa + nb)
         return fail(MOE_ERR_INVALID_ARG, "x overlaps out");

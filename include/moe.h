@@ -100,19 +100,26 @@ typedef struct {
 } moe_config;
 
 /* Validate cfg and create a handle on the current CUDA device.  Allocates
- * the resident weight arena for all L layers plus a fixed workspace.
+ * the resident weight arena for all L layers plus a fixed workspace, and a
+ * small pinned host staging buffer for moe_forward_host.
  * Requirements: H and I multiples of 64 and at most 3072; E in 1..256;
  * max_top_k in 1..min(E, 16); max_tokens in 1..8192, above 4 only with
  * MOE_FMT_MXFP4 (else MOE_ERR_UNSUPPORTED); MXFP4 needs group == 32; int4
  * needs group a multiple of 32 dividing both H and I.  Weights are repacked
- * at load into 16-row slabs whose bytes are the MMA operands of the decode
- * kernel; with max_tokens > 4 they are also kept in the tile layout of the
- * tensor-core batched path (about twice the memory; see the layout notes in
- * the library source).
- * On success *out receives the handle; on failure *out is set to NULL. */
+ * at load into the layout their kernels stream, once: MXFP4 into 128-row
+ * tiles whose bytes are the operands of the tensor-core MMA (gate and up rows
+ * interleaved per 64), int4 into 16-row slabs of MMA fragments.  The codes,
+ * scales and biases take the same bytes as in the caller layout (MXFP4 pads
+ * the scales of a partial 128-row tile).  The formats are those of the
+ * "MXFP4 reader" ("Sovereign gpt-oss-20B (MXFP4) on Apple Silicon", section 3)
+ * and of packed int4 ("Single-stream int4 decode of a 30B MoE", section 1).
+ * On success *out receives the handle; on failure *out is set to NULL and
+ * nothing stays allocated. */
 int moe_create(const moe_config* cfg, moe_handle** out);
 
-/* Copy one layer's experts into the handle.  Each pointer may be host or
+/* Copy one layer's experts into the handle (the load-once tables the pages
+ * build at start-up instead of per token: "Amortizing the per-token host-sync
+ * setup tax ...", section 3).  Each pointer may be host or
  * device memory (any address the CUDA runtime can copy from); the caller keeps
  * ownership and may free or reuse its buffers once the call returns (the call
  * synchronises `stream`).  Layouts (E experts, caller order):
@@ -141,15 +148,22 @@ int moe_load_experts(moe_handle* h, int layer,
 int moe_forward(moe_handle* h, int layer, const void* x_bf16, const float* router_logits,
                 int M, int top_k, void* out_bf16, void* stream);
 
-/* The same layer with host buffers: copies x, logits and the residual to the
- * handle's device workspace, runs moe_forward on `stream`, copies the result
- * back into out_bf16 and synchronises the stream before returning. */
+/* The same layer with host buffers (any host memory, pinned or not): packs x,
+ * the residual and the logits into the handle's pinned staging buffer, moves
+ * them with one host-to-device copy, runs moe_forward on `stream`, moves the
+ * result back with one device-to-host copy, synchronises the stream and copies
+ * the result into out_bf16.  Argument checks as for moe_forward. */
 int moe_forward_host(moe_handle* h, int layer, const void* x_bf16, const float* router_logits,
                      int M, int top_k, void* out_bf16, void* stream);
 
-/* The whole L-layer expert stack for one decode step.  For l = 0..L-1:
+/* The whole L-layer expert stack for one decode step ("one command buffer per
+ * decode", "Single-stream int4 decode of a 30B MoE", sections 1 and 6).  For
+ * l = 0..L-1:
  *   x_l = bf16(r_l / sqrt(mean(r_l^2) + 1e-6))   (weightless RMSNorm, per token)
  *   r_{l+1} = bf16(r_l + MoE_l(x_l))
+ * The pages name a residual add between layers but no coupling; the
+ * normalised input is this library's reading (a literal x + MoE(x) chain
+ * overflows within a few layers on these value distributions).
  * resid bf16 [M][H] holds r_0 on entry and r_L on return; logits fp32
  * [L][M][E].  Layer l+1 reads its logits only after layer l's output is
  * complete.  Device pointers.  Launched as a cached CUDA graph of L
@@ -160,13 +174,17 @@ int moe_forward_stack(moe_handle* h, void* resid_bf16, const float* router_logit
 
 /* Synchronise `stream` and return (and clear) the handle's device status:
  * MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_FAULT.  After a non-OK
- * status the handle's cross-CTA counters are reset, so it can be used again. */
+ * status the handle's cross-CTA counters are reset, so it can be used again.
+ * (Failure detection: the pages describe none for the GPU path; every wait in
+ * this library is bounded and reports here instead of hanging.) */
 int moe_get_status(moe_handle* h, void* stream);
 
 /* Debug: decode one stored expert projection to fp32, exactly (each element
- * is e2m1 * 2^(s-127) or (q - 8) * fp16 scale, rounded to fp32 once).
- * proj 0 = gate_up ([2I][H], caller row order), 1 = down ([H][I]).
- * out_dev fp32 device buffer of N*K elements. */
+ * is e2m1 * 2^(s-127) or (q - 8) * fp16 scale, rounded to fp32 once), from
+ * the very bytes the forward kernels stream: MXFP4 from the tile layout, int4
+ * from the slabs.  proj 0 = gate_up ([2I][H], caller row order), 1 = down
+ * ([H][I]).  out_dev fp32 device buffer of N*K elements.  The bit-exact check
+ * of the "MXFP4 reader" against its golden, gpt-oss page section 1. */
 int moe_debug_dequant(moe_handle* h, int layer, int expert, int proj, float* out_dev,
                       void* stream);
 
@@ -196,10 +214,29 @@ int moe_debug_batched_h(moe_handle* h, unsigned char* codes, unsigned char* scal
 int moe_debug_stack_trace(moe_handle* h, void* resid_bf16, const float* router_logits, int M,
                           int top_k, void* trace_bf16, void* stream);
 
+/* Debug: moe_forward that also writes the fp32 result before its bf16
+ * rounding, out_f32 fp32 [M][H] device (16-byte aligned), for checking the
+ * fp32-accumulated output itself.  Everything else as moe_forward. */
+int moe_debug_forward_f32(moe_handle* h, int layer, const void* x_bf16, const float* router_logits,
+                          int M, int top_k, void* out_bf16, float* out_f32, void* stream);
+
+/* Debug (failure detection): the cross-CTA waits of the MXFP4 decode layer
+ * give up after `spin_limit` polls (0 restores the default, about a second),
+ * and CTA `skip_cta` (-1: none) skips its arrival at the layer's grid barrier,
+ * so that the other CTAs' waits run out.  Applies to moe_forward and
+ * moe_debug_forward_f32 calls made after it (stack graphs already captured keep
+ * the settings they were captured with).  A call whose wait ran out reports
+ * MOE_ERR_DEVICE_TIMEOUT through moe_get_status, which also resets the
+ * counters so the handle works again.  Every access stays inside the handle's
+ * buffers; nothing traps. */
+int moe_debug_set_wait(moe_handle* h, int spin_limit, int skip_cta);
+
 /* Algorithmic expert bytes moved by the last forward call on this handle:
  * codes + scales + biases of the distinct experts selected in each layer,
- * counted once per layer.  Synchronises `stream`.  Returns MOE_OK and
- * writes *bytes, or an error. */
+ * counted once per layer (the byte counters of the pages' tracing, TinyTitan
+ * tracker).  Synchronises `stream` (so the signature takes the stream and
+ * returns a status, writing *bytes).  Returns MOE_OK and writes *bytes, or an
+ * error. */
 int moe_last_bytes(moe_handle* h, void* stream, long long* bytes);
 
 /* Bytes of one expert (codes + scales + biases) for this handle's config. */
@@ -226,8 +263,10 @@ const char* moe_last_error(void);
  * top_k experts of each token.  The weights are the caller-layout tensors of
  * moe_load_experts for one layer (E experts), on the device; x bf16 [M][H],
  * router_logits fp32 [M][E] and out bf16 [M][H] (the residual on entry) are
- * device pointers; x must not overlap out.  cfg gives H, I, E, format, group
- * and has_bias (its num_layers, max_tokens and max_top_k are ignored).
+ * device pointers; x must not overlap out.  Alignment: x, out and the code
+ * and scale arrays 16-byte aligned, router_logits 4-byte, biases 2-byte
+ * (else MOE_ERR_INVALID_ARG).  cfg gives H, I, E, format, group and has_bias
+ * (its num_layers, max_tokens and max_top_k are ignored).
  *
  * Scratch (h, the per-slot down outputs and the output-tile counters) is one
  * file-scope __device__ array of 1,574,400 bytes that every GPU which loads the

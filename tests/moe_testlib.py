@@ -41,6 +41,26 @@ def assert_parity(gpu: np.ndarray, ref: np.ndarray, ulps: float = 0.5, rel: floa
     return float(err.max() / max(np.abs(ref).max(), 1e-300))
 
 
+def assert_parity_f32(got32: np.ndarray, ref: np.ndarray, what=""):
+    """The stated bar on the fp32-accumulated output itself (before its bf16
+    rounding): max |gpu - oracle| <= 2e-3 * max|oracle|, nothing added."""
+    return assert_parity(got32, ref, ulps=0.0, what=what + " (fp32, before rounding)")
+
+
+def forward_both(moe, h, layer, x, r, logits, k):
+    """One forward through moe_debug_forward_f32: (bf16 output as f64, fp32
+    output before rounding as f64)."""
+    import torch
+    xd = to_dev_bf16(x)
+    out = to_dev_bf16(r)
+    o32 = torch.empty(out.shape, dtype=torch.float32, device="cuda")
+    ld = torch.from_numpy(np.ascontiguousarray(logits, np.float32)).cuda()
+    moe.moe_debug_forward_f32(h, layer, xd, ld, x.shape[0], k, out, o32)
+    torch.cuda.synchronize()
+    assert moe.moe_get_status(h) == 0
+    return bf16_bits_to_f64(dev_to_bits(out)), o32.cpu().numpy().astype(np.float64)
+
+
 def to_dev_bf16(bits: np.ndarray):
     import torch
     return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16)).cuda()

@@ -18,7 +18,7 @@ torch = pytest.importorskip("torch")
 
 import oracle
 from bit_moe_decode_02_gb300 import synth
-from moe_testlib import assert_parity, bf16_bits_to_f64, dev_to_bits, load_layer, to_dev_bf16
+from moe_testlib import assert_parity, assert_parity_f32, forward_both, load_layer
 
 pytestmark = pytest.mark.gpu
 
@@ -84,13 +84,9 @@ def _create(moe, shape, M, k=None):
                           moe.MOE_FMT_MXFP4, 32, 1 if shape.has_bias else 0)
 
 
-def _forward(moe, h, x, r, logits, k):
-    xd, out = to_dev_bf16(x), to_dev_bf16(r)
-    ld = torch.from_numpy(np.ascontiguousarray(logits, np.float32)).cuda()
-    moe.moe_forward(h, 0, xd, ld, x.shape[0], k, out)
-    torch.cuda.synchronize()
-    assert moe.moe_get_status(h) == 0
-    return bf16_bits_to_f64(dev_to_bits(out))
+def _forward(moe, h, x, r, logits, k, want_f32=False):
+    got, got32 = forward_both(moe, h, 0, x, r, logits, k)
+    return (got, got32) if want_f32 else got
 
 
 def _gpu_h(moe, h, Mk, I):
@@ -109,7 +105,7 @@ def _check_layer(moe, shape, t, x, r, logits, k, h, tokens=None):
     """Run one batched forward on all tokens; compare `tokens` (all if None)."""
     H, I, E = shape.hidden, shape.intermediate, shape.experts
     M = x.shape[0]
-    got = _forward(moe, h, x, r, logits, k)
+    got, got32 = _forward(moe, h, x, r, logits, k, want_f32=True)
     gh, gs = _gpu_h(moe, h, M * k, I)
     sel = np.arange(M) if tokens is None else np.asarray(tokens)
     slots = (sel[:, None] * k + np.arange(k)[None, :]).ravel()
@@ -127,6 +123,7 @@ def _check_layer(moe, shape, t, x, r, logits, k, h, tokens=None):
                                h_codes_in=np.ascontiguousarray(gh[slots]),
                                h_scales_in=np.ascontiguousarray(gs[slots]), nthreads=nt)
     rel = assert_parity(got[sel], ref, what=f"batched {shape.name} M={M}")
+    assert_parity_f32(got32[sel], ref, what=f"batched {shape.name} M={M}")
     return got, rel, flips
 
 

@@ -2,7 +2,8 @@
 
 Bars: bit-exact for dequantised weights and expert selection; routing weights
 within 1e-6; layer outputs within 2e-3 of the output's max-norm plus the bf16
-output rounding (see moe_testlib.assert_parity).
+output rounding (see moe_testlib.assert_parity), and the fp32 result before
+that rounding within the bare 2e-3 of the max-norm.
 """
 import numpy as np
 import pytest
@@ -11,8 +12,8 @@ torch = pytest.importorskip("torch")
 
 import oracle
 from bit_moe_decode_02_gb300 import synth
-from moe_testlib import (assert_parity, bf16_bits_to_f64, create_handle, dev_to_bits, load_layer,
-                         oracle_layer, sparse_layer, to_dev_bf16)
+from moe_testlib import (assert_parity, assert_parity_f32, bf16_bits_to_f64, create_handle, dev_to_bits,
+                         forward_both, load_layer, oracle_layer, sparse_layer, to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -37,21 +38,45 @@ def _run_layer(moe, h, layer, x, r, logits, k):
     return bf16_bits_to_f64(dev_to_bits(out))
 
 
+def _check_both(moe, h, shape, t, x, r, logits, k, what):
+    """bf16 output against the oracle (2e-3 of the max-norm + half a bf16 ulp)
+    and the fp32 result before rounding at the bare 2e-3; the two outputs of
+    the call agree (the bf16 one is the fp32 one rounded)."""
+    got, got32 = forward_both(moe, h, 0, x, r, logits, k)
+    ref, idx, _ = oracle_layer(shape, t, x, logits, r, k=k)
+    assert_parity(got, ref, what=what)
+    assert_parity_f32(got32, ref, what=what)
+    again = torch.from_numpy(got32.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(np.nan_to_num(again), np.nan_to_num(got))
+    return got, ref, idx
+
+
 # ------------------------------------------------------------------ dequant
 
-def test_dequant_bitexact_mxfp4_every_code_and_scale(moe):
-    # gate_up rows n use scale byte n % 256 in every block and codes cycling
-    # through all 16 values, so every (code, E8M0) pair appears.
-    H, I, E = 64, 256, 2
+@pytest.mark.parametrize("H,I,max_tokens", [(64, 256, 1), (192, 128, 1), (320, 384, 16)],
+                         ids=["H=64 (one 64-row down tile)", "H=192 (1.5 down tiles)", "H=320 batched handle"])
+def test_dequant_bitexact_mxfp4_every_code_and_scale(moe, H, I, max_tokens):
+    """The MXFP4 weights as the tensor-core kernels stream them (the 128-row
+    tile layout: gate and up rows interleaved per 64, scale chunks in
+    tensor-memory order) decode bit-exactly to the oracle's values, for both
+    projections of several experts.  gate_up row n of expert 0 uses scale byte
+    n % 256 and the down rows of expert 1 byte (n + 128) % 256, with codes
+    cycling through all 16 values, so every (code, E8M0) pair appears
+    (byte 255 = NaN, products past the fp32 range = inf)."""
+    E = 3
     shp = synth.Shape("dequant", H, I, E, 1, e8m0_lo=0, e8m0_hi=254)
     t = synth.layer_tensors(shp)
     codes = np.array([(j + n) % 16 for n in range(2 * I) for j in range(H)], np.uint8).reshape(2 * I, H)
     t.gu_codes[0] = codes[:, 0::2] | (codes[:, 1::2] << 4)
     t.gu_scales[0] = (np.arange(2 * I) % 256).astype(np.uint8)[:, None]
-    h = create_handle(shp, max_top_k=1)
+    dcodes = np.array([(3 * j + n) % 16 for n in range(H) for j in range(I)], np.uint8).reshape(H, I)
+    t.dn_codes[1] = dcodes[:, 0::2] | (dcodes[:, 1::2] << 4)
+    t.dn_scales[1] = ((np.arange(H) + 128) % 256).astype(np.uint8)[:, None]
+    h = create_handle(shp, max_tokens=max_tokens, max_top_k=1)
     try:
         load_layer(h, 0, t)
-        for e, proj, N, K in [(0, 0, 2 * I, H), (1, 0, 2 * I, H), (0, 1, H, I), (1, 1, H, I)]:
+        for e, proj, N, K in [(0, 0, 2 * I, H), (1, 0, 2 * I, H), (2, 0, 2 * I, H), (0, 1, H, I),
+                              (1, 1, H, I), (2, 1, H, I)]:
             out = torch.empty(N * K, dtype=torch.float32, device="cuda")
             moe.moe_debug_dequant(h, 0, e, proj, out)
             got = out.cpu().numpy().reshape(N, K)
@@ -140,9 +165,7 @@ def test_layer_parity_small(moe, shape, M):
         load_layer(h, 0, t)
         for step in range(2):
             x, r, logits = synth.step_inputs(shape, step, M=M, layers=1)
-            got = _run_layer(moe, h, 0, x, r, logits[0], shape.top_k)
-            ref, _, _ = oracle_layer(shape, t, x, logits[0], r)
-            assert_parity(got, ref, what=f"{shape.name} M={M} step={step}")
+            _check_both(moe, h, shape, t, x, r, logits[0], shape.top_k, f"{shape.name} M={M} step={step}")
     finally:
         moe.moe_destroy(h)
 
@@ -170,10 +193,8 @@ def test_layer_parity_split_units(moe, M, H):
             logits = np.full((M, E), -5.0, np.float32)
             for m in range(M):
                 logits[m, k * m:k * m + k] = np.array([3.0, 2.5, 2.0, 1.5], np.float32) + 0.1 * step
-            got = _run_layer(moe, h, 0, x, r, logits, k)
-            ref, idx, _ = oracle_layer(shape, t, x, logits, r)
+            got, ref, idx = _check_both(moe, h, shape, t, x, r, logits, k, f"{shape.name} M={M} step={step}")
             assert len(set(idx.ravel().tolist())) == nu
-            assert_parity(got, ref, what=f"{shape.name} M={M} step={step}")
         # a repeat call gives the same bits (piece sums are added in a fixed order)
         again = _run_layer(moe, h, 0, x, r, logits, k)
         assert np.array_equal(np.nan_to_num(got), np.nan_to_num(again))
@@ -210,10 +231,8 @@ def test_layer_parity_many_distinct_experts(moe, M, H, I, overlap):
     try:
         load_layer(h, 0, t)
         x, r, _ = synth.step_inputs(shape, 0, M=M, layers=1)
-        got = _run_layer(moe, h, 0, x, r, logits, k)
-        ref, idx, _ = oracle_layer(shape, t, x, logits, r)
+        got, ref, idx = _check_both(moe, h, shape, t, x, r, logits, k, f"{shape.name} M={M} nu={nu}")
         assert len(set(idx.ravel().tolist())) == nu
-        assert_parity(got, ref, what=f"{shape.name} M={M} nu={nu}")
         assert moe.moe_last_bytes(h) == nu * shape.expert_bytes()
     finally:
         moe.moe_destroy(h)
@@ -251,9 +270,7 @@ def test_layer_parity_full_size(moe, shape, M):
         load_layer(h, 0, t)
         for step in range(2):
             x, r, logits = synth.step_inputs(shape, step, M=M, layers=1)
-            got = _run_layer(moe, h, 0, x, r, logits[0], shape.top_k)
-            ref, idx, _ = oracle_layer(shape, t, x, logits[0], r)
-            assert_parity(got, ref, what=f"{shape.name} M={M}")
+            got, ref, idx = _check_both(moe, h, shape, t, x, r, logits[0], shape.top_k, f"{shape.name} M={M}")
         # the expert bytes of the last call: distinct selected experts x bytes per expert
         nu = len(set(idx.ravel().tolist()))
         assert moe.moe_expert_bytes(h) == shape.expert_bytes()
@@ -362,8 +379,15 @@ def test_stack_parity_full_size(moe, shape):
     applied to the GPU's r_l.  The oracle regenerates only the experts each
     layer's router selects."""
     L = shape.layers
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
     h = create_handle(shape, layers=L)
     try:
+        # the weights are held once, in the layout the kernels stream: the
+        # handle takes the packed bytes of L x E experts plus a small workspace
+        used = free0 - torch.cuda.mem_get_info()[0]
+        packed = L * shape.experts * shape.expert_bytes()
+        assert packed <= used <= packed * 1.02 + (256 << 20), (used, packed)
         for l in range(L):
             load_layer(h, l, synth.layer_tensors(shape, l))
         for M in (1, 4):
