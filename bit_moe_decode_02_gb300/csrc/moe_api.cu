@@ -1,6 +1,5 @@
 // moe_api.cu -- the C ABI declared in include/moe.h: handle, argument checks,
-// resident weight arena, workspace, launch of the decode kernels and the
-// cached CUDA graph of the expert stack.
+// resident weight arena, workspace and the launches of the layer kernels.
 //
 // All tables the kernels need are fixed at moe_create / moe_load_experts; a
 // forward call does no host-side work that depends on the routing (the pages'
@@ -8,6 +7,12 @@
 // "Amortizing the per-token host-sync setup tax ...", section 3), and it
 // allocates nothing (the grow-only buffer cache that reallocated on every
 // count change, TinyTitan tracker D114).
+//
+// Resident layout, per layer: [gate_up of E experts][down of E experts]
+// [gate_up biases bf16 [E][2I]][down biases bf16 [E][H]], 256-byte aligned.
+// MXFP4 experts are in the 128-row tile layout of the tensor-core kernels,
+// int4 experts in the 64-row unit layout of the int4 kernel (each described
+// with its kernel); both hold exactly the caller's bytes, reordered.
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -40,13 +45,6 @@ int cuda_fail(cudaError_t e, const char* what)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-struct StackGraph {
-    int M = 0, k = 0;
-    const void* resid = nullptr;
-    const void* logits = nullptr;
-    cudaGraphExec_t exec = nullptr;
-};
-
 }  // namespace
 
 int moe::set_error(int code, const char* fmt, ...)
@@ -62,33 +60,27 @@ struct moe_handle {
     moe_config cfg{};
     int device = 0;
     int num_sms = 0;
+    bool mxfp4 = false;
     // caller-layout tensor sizes in bytes (one layer, all experts)
     size_t gu_codes_b = 0, gu_scales_b = 0, gu_bias_b = 0;
     size_t dn_codes_b = 0, dn_scales_b = 0, dn_bias_b = 0;
-    // resident layout: per layer [gate_up slabs][down slabs][gu bias][dn bias];
-    // MXFP4 keeps no slabs (its kernels read the tile layout): [gu bias][dn bias]
-    int sb = 0;                       // scale bytes per (segment, g) entry
-    int gu_slab = 0, dn_slab = 0;     // bytes of one 16-row slab
-    size_t gu_expert = 0, dn_expert = 0;
-    size_t layer_stride = 0;
-    size_t off_dn = 0, off_gu_bias = 0, off_dn_bias = 0;
-    int slot_bytes = 0, nslots = 0, grid = 0;
+    // resident layout
+    size_t gu_expert = 0, dn_expert = 0;      // bytes of one expert's projection
+    size_t off_dn = 0, off_gu_bias = 0, off_dn_bias = 0, layer_stride = 0;
     uint8_t* arena = nullptr;
-    uint32_t* special = nullptr;      // [L][E][2]
     std::vector<char> loaded;
-    // MXFP4: tile-layout copy of the weights (tensor-core decode and batched paths)
-    bool tiles = false;
-    bool batched = false;             // max_tokens > kMaxTokens
-    size_t tc_smem = 0;
-    float* tc_part = nullptr;
-    float* tc_gpart = nullptr;      // split units: pieces' gate/up partial sums
-    unsigned* tc_flags = nullptr;   // split units: [G] piece flags
-    uint8_t* tc_xt = nullptr;
-    unsigned long long* tc_cnt = nullptr;
-    size_t t_gu_expert = 0, t_dn_expert = 0, t_off_dn = 0, t_layer_stride = 0;
-    uint8_t* tarena = nullptr;
+    // decode workspace (both formats): per-CTA output copies and the counters
+    size_t dec_smem = 0;                      // dynamic shared memory of the decode kernel
+    float* part = nullptr;                    // [G][H][4]
+    unsigned long long* cnt = nullptr;        // xcnt, done (only grow)
+    // MXFP4 decode: split-unit partials and flags, the layer's x terms
+    float* gpart = nullptr;
+    unsigned* pflag = nullptr;
+    uint8_t* xt = nullptr;
+    // batched path (MXFP4, M > 4)
+    bool batched = false;
     int max_tiles = 0;
-    int* b_int = nullptr;             // idx | slot | etile | erow | ntiles
+    int* b_int = nullptr;                     // idx | slot | etile | erow | ntiles
     float* b_wt = nullptr;
     moe::TokTile* b_tiles = nullptr;
     uint8_t* b_xq = nullptr;
@@ -96,26 +88,19 @@ struct moe_handle {
     uint8_t* b_hq = nullptr;
     uint8_t* b_hsf = nullptr;
     float* b_y = nullptr;
-    int last_bM = 0, last_bk = 0;     // M and top_k of the last batched call
-    // workspace
-    float* h = nullptr;
-    float* ypart = nullptr;
-    unsigned* counters = nullptr;     // done | hmax | slab_cnt | exit (see counter_words)
-    int* stats = nullptr;   // distinct experts per layer of the last call
+    int last_bM = 0, last_bk = 0;             // M and top_k of the last batched call
+    int* stats = nullptr;                     // distinct experts of the last call on each layer
     int* status = nullptr;
     // staging for moe_forward_host: [x][residual / out][logits], on the device
     // and in pinned host memory, so one copy each way moves a call's data
     uint8_t* st_dev = nullptr;
     uint8_t* st_host = nullptr;
     size_t st_off_r = 0, st_off_l = 0, st_bytes = 0;
-    // cross-CTA waits of the MXFP4 decode layer (moe_debug_set_wait)
+    // cross-CTA waits of the decode kernels (moe_debug_set_wait)
     int spin_limit = moe::kSpinLimit;
     int skip_cta = -1;
-    // stack graphs
-    cudaStream_t capture_stream = nullptr;
-    std::vector<StackGraph> graphs;
-    int last_layers = 0;       // layers touched by the last forward call
-    int last_first_layer = 0;
+    int last_steps = 0;        // layer calls of the last forward call: layers
+    int last_first_layer = 0;  // last_first_layer, + 1, ... (mod L)
     int last_launches = 0;
 };
 
@@ -166,26 +151,12 @@ void free_handle(moe_handle* h)
 {
     if (!h)
         return;
-    for (auto& g : h->graphs)
-        if (g.exec)
-            cudaGraphExecDestroy(g.exec);
-    if (h->capture_stream)
-        cudaStreamDestroy(h->capture_stream);
     cudaFree(h->arena);
-    cudaFree(h->special);
-    cudaFree(h->h);
-    cudaFree(h->ypart);
-    cudaFree(h->counters);
-    cudaFree(h->stats);
-    cudaFree(h->status);
-    cudaFree(h->st_dev);
-    cudaFreeHost(h->st_host);
-    cudaFree(h->tarena);
-    cudaFree(h->tc_part);
-    cudaFree(h->tc_gpart);
-    cudaFree(h->tc_flags);
-    cudaFree(h->tc_xt);
-    cudaFree(h->tc_cnt);
+    cudaFree(h->part);
+    cudaFree(h->cnt);
+    cudaFree(h->gpart);
+    cudaFree(h->pflag);
+    cudaFree(h->xt);
     cudaFree(h->b_int);
     cudaFree(h->b_wt);
     cudaFree(h->b_tiles);
@@ -194,6 +165,10 @@ void free_handle(moe_handle* h)
     cudaFree(h->b_hq);
     cudaFree(h->b_hsf);
     cudaFree(h->b_y);
+    cudaFree(h->stats);
+    cudaFree(h->status);
+    cudaFree(h->st_dev);
+    cudaFreeHost(h->st_host);
     delete h;
 }
 
@@ -210,139 +185,155 @@ int dev_alloc(T** p, size_t bytes, const char* what)
     return MOE_OK;
 }
 
-// Token capacity of the decode kernel's workspace and shared memory.
-int decode_tokens(const moe_config& c)
+const uint16_t* bias0(const moe_handle* h, size_t off)
 {
-    return c.max_tokens < moe::kMaxTokens ? c.max_tokens : moe::kMaxTokens;
+    return h->cfg.has_bias ? reinterpret_cast<const uint16_t*>(h->arena + off) : nullptr;
 }
 
-moe::LayerParams layer_params(const moe_handle* h, int layer)
+// Parameters of the MXFP4 decode kernel for `ncalls` calls from `layer0`
+// (the caller sets the inputs, outputs and strides).
+moe::DecodeTcParams tc_params(const moe_handle* h, int layer0, int ncalls)
 {
     const moe_config& c = h->cfg;
-    const uint8_t* base = h->arena + (size_t)layer * h->layer_stride;
-    moe::LayerParams p{};
-    p.gu = base;
-    p.dn = base + h->off_dn;
-    p.gu_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(base + h->off_gu_bias) : nullptr;
-    p.dn_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(base + h->off_dn_bias) : nullptr;
-    p.special = h->special + (size_t)layer * c.num_experts * 2;
-    p.h = h->h;
-    p.ypart = h->ypart;
-    p.done = h->counters;
-    p.hmax = h->counters + moe::kMaxUnits;
-    p.slab_cnt = p.hmax + moe::kMaxUnits * moe::kMaxTokens;
-    p.exit_cnt = p.slab_cnt + c.hidden / moe::kSlabRows;
-    p.status = h->status;
-    p.nu_out = h->stats + layer;
-    p.gu_expert_bytes = (long long)h->gu_expert;
-    p.dn_expert_bytes = (long long)h->dn_expert;
-    p.gu_slab_bytes = h->gu_slab;
-    p.dn_slab_bytes = h->dn_slab;
-    p.H = c.hidden;
-    p.I = c.intermediate;
-    p.E = c.num_experts;
-    p.kmax = c.max_top_k;
-    p.mmax = decode_tokens(c);
-    p.group = c.group;
-    p.nslots = h->nslots;
-    p.slot_bytes = h->slot_bytes;
-    return p;
-}
-
-// MXFP4: tile-layout weights and the workspace of the tensor-core decode kernel.
-int create_tiles(moe_handle* h)
-{
-    const moe_config& c = h->cfg;
-    const int H = c.hidden, I = c.intermediate, E = c.num_experts;
-    h->tiles = true;
-    h->t_gu_expert = (size_t)moe::tile_proj_bytes(2 * I, H);   // interleaved gate_up
-    h->t_dn_expert = (size_t)moe::tile_proj_bytes(H, I);
-    h->t_off_dn = align_up(E * h->t_gu_expert, 256);
-    h->t_layer_stride = align_up(h->t_off_dn + E * h->t_dn_expert, 256);
-    const int G = h->num_sms;
-    int rc;
-    if ((rc = dev_alloc(&h->tarena, h->t_layer_stride * c.num_layers, "tile-layout weights")) ||
-        (rc = dev_alloc(&h->tc_part, moe::tc_part_bytes(G, H), "per-CTA outputs")) ||
-        (rc = dev_alloc(&h->tc_gpart, (size_t)G * moe::kRowTile * 4 * sizeof(float), "split-unit partials")) ||
-        (rc = dev_alloc(&h->tc_flags, (size_t)G * sizeof(unsigned), "split-unit flags")) ||
-        (rc = dev_alloc(&h->tc_xt, moe::tc_terms_bytes(H), "x terms")) ||
-        (rc = dev_alloc(&h->tc_cnt, moe::kTcCounterWords * sizeof(unsigned long long), "counters")))
-        return rc;
-    cudaError_t e = cudaMemset(h->tc_cnt, 0, moe::kTcCounterWords * sizeof(unsigned long long));
-    // x-term rows past M * 8 are never written and feed MMA columns nobody reads:
-    // keep them zero (valid E2M1 codes, E8M0 byte 0) instead of leftover bytes
-    if (e == cudaSuccess)
-        e = cudaMemset(h->tc_xt, 0, moe::tc_terms_bytes(H));
-    if (e == cudaSuccess)
-        e = cudaMemset(h->tc_flags, 0, (size_t)G * sizeof(unsigned));
-    if (e != cudaSuccess)
-        return cuda_fail(e, "counters");
-    // all the shared memory a block may have: the kernel's own plus the stage ring
-    int dev = 0, optin = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
-        (e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
-        return cuda_fail(e, "shared memory limit");
-    h->tc_smem = (size_t)optin - moe::decode_tc_static_smem();
-    if ((e = moe::prepare_decode_tc(h->tc_smem)) != cudaSuccess)
-        return cuda_fail(e, "tensor-core decode kernel set-up");
-    return MOE_OK;
-}
-
-moe::DecodeTcParams tc_params(const moe_handle* h, int layer)
-{
-    const moe_config& c = h->cfg;
-    const uint8_t* tb = h->tarena + (size_t)layer * h->t_layer_stride;
-    const uint8_t* sb = h->arena + (size_t)layer * h->layer_stride;
     moe::DecodeTcParams p{};
-    p.gu = tb;
-    p.dn = tb + h->t_off_dn;
-    p.gu_expert = (long long)h->t_gu_expert;
-    p.dn_expert = (long long)h->t_dn_expert;
-    p.gu_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(sb + h->off_gu_bias) : nullptr;
-    p.dn_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(sb + h->off_dn_bias) : nullptr;
-    p.part = h->tc_part;
-    p.gpart = h->tc_gpart;
-    p.pflag = h->tc_flags;
-    p.xt = h->tc_xt;
-    p.xcnt = h->tc_cnt;
-    p.done = h->tc_cnt + 1;
+    p.gu = h->arena;
+    p.dn = h->arena + h->off_dn;
+    p.layer_stride = (long long)h->layer_stride;
+    p.gu_expert = (long long)h->gu_expert;
+    p.dn_expert = (long long)h->dn_expert;
+    p.gu_bias = bias0(h, h->off_gu_bias);
+    p.dn_bias = bias0(h, h->off_dn_bias);
+    p.bias_stride = (long long)h->layer_stride;
+    p.ncalls = ncalls;
+    p.layer0 = layer0;
+    p.nlayers = c.num_layers;
+    p.part = h->part;
+    p.gpart = h->gpart;
+    p.pflag = h->pflag;
+    p.xt = h->xt;
+    p.xcnt = h->cnt;
+    p.done = h->cnt + 1;
     p.status = h->status;
-    p.nu_out = h->stats + layer;
+    p.nu_out = h->stats;
     p.H = c.hidden;
     p.I = c.intermediate;
     p.E = c.num_experts;
-    p.smem_bytes = (int)h->tc_smem;
+    p.smem_bytes = (int)h->dec_smem;
     p.spin_limit = h->spin_limit;
     p.skip_cta = h->skip_cta;
     return p;
 }
 
-// Kernel launches of one decode layer: the layer kernel (tensor-core MXFP4 or int4).
-int decode_launches(const moe_handle*) { return 1; }
-
-// The decode layer on the current kernel of this handle's format; out_f32
-// (debug, nullable) also receives the result before its bf16 rounding.
-cudaError_t launch_decode(const moe_handle* h, int layer, const float* logits, const void* x, void* resid,
-                          int M, int k, cudaStream_t s, float* out_f32 = nullptr)
+moe::DecodeI4Params i4_params(const moe_handle* h, int layer0, int ncalls)
 {
-    if (h->tiles) {
-        moe::DecodeTcParams p = tc_params(h, layer);
+    const moe_config& c = h->cfg;
+    moe::DecodeI4Params p{};
+    p.gu = h->arena;
+    p.dn = h->arena + h->off_dn;
+    p.layer_stride = (long long)h->layer_stride;
+    p.gu_expert = (long long)h->gu_expert;
+    p.dn_expert = (long long)h->dn_expert;
+    p.gu_bias = bias0(h, h->off_gu_bias);
+    p.dn_bias = bias0(h, h->off_dn_bias);
+    p.bias_stride = (long long)h->layer_stride;
+    p.ncalls = ncalls;
+    p.layer0 = layer0;
+    p.nlayers = c.num_layers;
+    p.part = h->part;
+    p.done = h->cnt + 1;
+    p.status = h->status;
+    p.nu_out = h->stats;
+    p.H = c.hidden;
+    p.I = c.intermediate;
+    p.E = c.num_experts;
+    p.group = c.group;
+    p.smem_bytes = (int)h->dec_smem;
+    p.spin_limit = h->spin_limit;
+    p.skip_cta = h->skip_cta;
+    return p;
+}
+
+// A sequence of `n` decode calls in one launch: call s runs layer (layer0 + s)
+// mod L on logits + s * ls, x + s * xs (x may be NULL: the normalised
+// residual), resid + s * rs and out_f32 + s * fs (bytes).
+cudaError_t launch_seq(const moe_handle* h, int layer0, int n, const float* logits, long long ls, const void* x,
+                       long long xs, void* resid, long long rs, float* out_f32, long long fs, int M, int k,
+                       cudaStream_t s)
+{
+    if (h->mxfp4) {
+        moe::DecodeTcParams p = tc_params(h, layer0, n);
         p.logits = logits;
+        p.logits_stride = ls;
         p.x = static_cast<const uint16_t*>(x);
+        p.x_stride = xs;
         p.resid = static_cast<uint16_t*>(resid);
+        p.resid_stride = rs;
         p.out_f32 = out_f32;
+        p.out_f32_stride = fs;
         p.M = M;
         p.k = k;
-        return moe::launch_decode_tc(p, h->tc_smem, h->num_sms, s);
+        return moe::launch_decode_tc(p, h->dec_smem, h->num_sms, s);
     }
-    moe::LayerParams p = layer_params(h, layer);
+    moe::DecodeI4Params p = i4_params(h, layer0, n);
     p.logits = logits;
+    p.logits_stride = ls;
     p.x = static_cast<const uint16_t*>(x);
+    p.x_stride = xs;
     p.resid = static_cast<uint16_t*>(resid);
+    p.resid_stride = rs;
     p.out_f32 = out_f32;
+    p.out_f32_stride = fs;
     p.M = M;
     p.k = k;
-    return moe::launch_layer(p, h->cfg.format, h->grid, s);
+    return moe::launch_decode_i4(p, h->dec_smem, h->num_sms, s);
+}
+
+// One decode layer call.
+cudaError_t launch_decode(const moe_handle* h, int layer, const float* logits, const void* x, void* resid, int M,
+                          int k, cudaStream_t s, float* out_f32 = nullptr)
+{
+    return launch_seq(h, layer, 1, logits, 0, x, 0, resid, 0, out_f32, 0, M, k, s);
+}
+
+// Decode workspace and kernel set-up (both formats).
+int create_decode(moe_handle* h)
+{
+    const moe_config& c = h->cfg;
+    const int H = c.hidden, G = h->num_sms;
+    int rc;
+    if ((rc = dev_alloc(&h->part, moe::tc_part_bytes(G, H), "per-CTA outputs")) ||
+        (rc = dev_alloc(&h->cnt, moe::kTcCounterWords * sizeof(unsigned long long), "counters")))
+        return rc;
+    cudaError_t e = cudaMemset(h->cnt, 0, moe::kTcCounterWords * sizeof(unsigned long long));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "counters");
+    int dev = 0, optin = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+        return cuda_fail(e, "shared memory limit");
+    if (h->mxfp4) {
+        if ((rc = dev_alloc(&h->gpart, (size_t)G * moe::kRowTile * 4 * sizeof(float), "split-unit partials")) ||
+            (rc = dev_alloc(&h->pflag, (size_t)G * sizeof(unsigned), "split-unit flags")) ||
+            (rc = dev_alloc(&h->xt, moe::tc_terms_bytes(H), "x terms")))
+            return rc;
+        // x-term rows past M * 8 are never written and feed MMA columns nobody reads:
+        // keep them zero (valid E2M1 codes, E8M0 byte 0) instead of leftover bytes
+        if ((e = cudaMemset(h->xt, 0, moe::tc_terms_bytes(H))) != cudaSuccess ||
+            (e = cudaMemset(h->pflag, 0, (size_t)G * sizeof(unsigned))) != cudaSuccess)
+            return cuda_fail(e, "decode workspace");
+        h->dec_smem = (size_t)optin - moe::decode_tc_static_smem();
+        if ((e = moe::prepare_decode_tc(h->dec_smem)) != cudaSuccess)
+            return cuda_fail(e, "tensor-core decode kernel set-up");
+    } else {
+        h->dec_smem = (size_t)optin - moe::decode_i4_static_smem();
+        // the int4 kernel's tail (x as f16, sums, h', the output copy) and at least two stages
+        const size_t tail = (size_t)4 * (H + 8) * 2 + 128 * 16 + 2 * 4 * 64 * 2 + (size_t)H * 16 + 128;
+        if (h->dec_smem < tail + 2 * (size_t)moe::kI4Slot)
+            return fail(MOE_ERR_UNSUPPORTED, "hidden=%d leaves no room for the int4 kernel's stage ring", H);
+        if ((e = moe::prepare_decode_i4(h->dec_smem)) != cudaSuccess)
+            return cuda_fail(e, "int4 decode kernel set-up");
+    }
+    return MOE_OK;
 }
 
 // Workspace of the batched path.
@@ -374,15 +365,14 @@ moe::BatchParams batch_params(const moe_handle* h, int layer)
 {
     const moe_config& c = h->cfg;
     const size_t Mk = (size_t)c.max_tokens * c.max_top_k;
-    const uint8_t* tb = h->tarena + (size_t)layer * h->t_layer_stride;
-    const uint8_t* sb = h->arena + (size_t)layer * h->layer_stride;
+    const uint8_t* base = h->arena + (size_t)layer * h->layer_stride;
     moe::BatchParams p{};
-    p.gu = tb;
-    p.dn = tb + h->t_off_dn;
-    p.gu_expert = (long long)h->t_gu_expert;
-    p.dn_expert = (long long)h->t_dn_expert;
-    p.gu_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(sb + h->off_gu_bias) : nullptr;
-    p.dn_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(sb + h->off_dn_bias) : nullptr;
+    p.gu = base;
+    p.dn = base + h->off_dn;
+    p.gu_expert = (long long)h->gu_expert;
+    p.dn_expert = (long long)h->dn_expert;
+    p.gu_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(base + h->off_gu_bias) : nullptr;
+    p.dn_bias = c.has_bias ? reinterpret_cast<const uint16_t*>(base + h->off_dn_bias) : nullptr;
     p.idx = h->b_int;
     p.slot = h->b_int + Mk;
     p.etile = h->b_int + 2 * Mk;
@@ -424,19 +414,58 @@ int check_forward_args(const moe_handle* h, int M, int top_k)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Caller layout -> tile layout for one layer (gate rows [0, I) and up rows
-// [I, 2I) of gate_up become two projections of I rows each).
-cudaError_t load_tiles(moe_handle* h, int layer, const uint8_t* guc, const uint8_t* gus,
-                       const uint8_t* dnc, const uint8_t* dns, cudaStream_t s)
+int check_all_loaded(const moe_handle* h, const char* who)
 {
-    const moe_config& c = h->cfg;
-    const int H = c.hidden, I = c.intermediate, E = c.num_experts;
-    uint8_t* tb = h->tarena + (size_t)layer * h->t_layer_stride;
-    cudaError_t e;
-    if ((e = moe::launch_repack_tiles(guc, gus, E, 2 * I, 2 * I, H, I, tb, (long long)h->t_gu_expert, s)) !=
-        cudaSuccess)
-        return e;
-    return moe::launch_repack_tiles(dnc, dns, E, H, H, I, 0, tb + h->t_off_dn, (long long)h->t_dn_expert, s);
+    for (int l = 0; l < h->cfg.num_layers; ++l)
+        if (!h->loaded[l])
+            return fail(MOE_ERR_NOT_LOADED, "%s: layer %d has no experts loaded", who, l);
+    return MOE_OK;
+}
+
+int forward_impl(moe_handle* h, int layer, const void* x_bf16, const float* router_logits, int M,
+                 int top_k, void* out_bf16, float* out_f32, void* stream)
+{
+    int rc = check_forward_args(h, M, top_k);
+    if (rc != MOE_OK)
+        return rc;
+    if (layer < 0 || layer >= h->cfg.num_layers)
+        return fail(MOE_ERR_INVALID_ARG, "layer=%d out of range 0..%d", layer, h->cfg.num_layers - 1);
+    if (!x_bf16 || !router_logits || !out_bf16)
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward: x, logits and out must not be NULL");
+    if (!aligned16(x_bf16) || !aligned16(out_bf16) || !aligned16(router_logits))
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward: x, logits and out must be 16-byte aligned");
+    const size_t nb = (size_t)M * h->cfg.hidden * 2;
+    if (overlaps(x_bf16, nb, out_bf16, nb))
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward: x overlaps out");
+    if (!h->loaded[layer])
+        return fail(MOE_ERR_NOT_LOADED, "moe_forward: layer %d has no experts loaded", layer);
+    if (M > moe::kMaxTokens) {
+        moe::BatchParams b = batch_params(h, layer);
+        b.logits = router_logits;
+        b.x = static_cast<const uint16_t*>(x_bf16);
+        b.resid = static_cast<uint16_t*>(out_bf16);
+        b.out_f32 = out_f32;
+        b.M = M;
+        b.k = top_k;
+        int launches = 0;
+        cudaError_t e = moe::launch_batched(b, h->num_sms, (cudaStream_t)stream, &launches);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "moe_forward (batched) launch");
+        h->last_steps = 1;
+        h->last_first_layer = layer;
+        h->last_launches = launches;
+        h->last_bM = M;
+        h->last_bk = top_k;
+        return MOE_OK;
+    }
+    cudaError_t e = launch_decode(h, layer, router_logits, x_bf16, out_bf16, M, top_k, (cudaStream_t)stream,
+                                  out_f32);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "moe_forward launch");
+    h->last_steps = 1;
+    h->last_first_layer = layer;
+    h->last_launches = 1;
+    return MOE_OK;
 }
 
 }  // namespace
@@ -459,21 +488,21 @@ int moe_create(const moe_config* cfg, moe_handle** out)
     h->cfg = *cfg;
     const moe_config& c = h->cfg;
     const size_t H = c.hidden, I = c.intermediate, E = c.num_experts;
-    const size_t sbh = c.format == MOE_FMT_MXFP4 ? H / 32 : 2 * H / c.group;
-    const size_t sbi = c.format == MOE_FMT_MXFP4 ? I / 32 : 2 * I / c.group;
+    h->mxfp4 = c.format == MOE_FMT_MXFP4;
+    const size_t sbh = h->mxfp4 ? H / 32 : 2 * H / c.group;
+    const size_t sbi = h->mxfp4 ? I / 32 : 2 * I / c.group;
     h->gu_codes_b = E * 2 * I * H / 2;
     h->gu_scales_b = E * 2 * I * sbh;
     h->gu_bias_b = c.has_bias ? E * 2 * I * 2 : 0;
     h->dn_codes_b = E * H * I / 2;
     h->dn_scales_b = E * H * sbi;
     h->dn_bias_b = c.has_bias ? E * H * 2 : 0;
-    const bool slabs = c.format == MOE_FMT_INT4;   // MXFP4 weights live in the tile layout only
-    h->sb = moe::scale_entry_bytes(c.format, c.group);
-    if (slabs) {
-        h->gu_slab = moe::slab_bytes((int)H, h->sb);
-        h->dn_slab = moe::slab_bytes((int)I, h->sb);
-        h->gu_expert = (2 * I / moe::kSlabRows) * (size_t)h->gu_slab;
-        h->dn_expert = (H / moe::kSlabRows) * (size_t)h->dn_slab;
+    if (h->mxfp4) {
+        h->gu_expert = (size_t)moe::tile_proj_bytes(2 * (int)I, (int)H);   // interleaved gate_up
+        h->dn_expert = (size_t)moe::tile_proj_bytes((int)H, (int)I);
+    } else {
+        h->gu_expert = (I / 64) * (size_t)moe::i4_unit_bytes((int)H, c.group, 0);
+        h->dn_expert = (I / 64) * (size_t)moe::i4_unit_bytes((int)H, c.group, 1);
     }
     size_t off = align_up(E * h->gu_expert, 256);
     h->off_dn = off;
@@ -481,59 +510,20 @@ int moe_create(const moe_config* cfg, moe_handle** out)
     h->off_gu_bias = off;
     off = align_up(off + h->gu_bias_b, 256);
     h->off_dn_bias = off;
-    off = align_up(off + h->dn_bias_b, 256);
-    h->layer_stride = off > 256 ? off : 256;
-    if (slabs) {
-        h->slot_bytes = (int)align_up((size_t)(h->gu_slab > h->dn_slab ? h->gu_slab : h->dn_slab), 128);
-        h->nslots = (int)((moe::kSmemBudget - moe::kRedBytes - moe::kXfragBytes -
-                           2 * (size_t)decode_tokens(c) * I * sizeof(float)) / h->slot_bytes);
-        if (h->nslots > moe::kMaxSlots)
-            h->nslots = moe::kMaxSlots;
-        if (h->nslots < 2) {
-            free_handle(h);
-            return fail(MOE_ERR_UNSUPPORTED, "a 16-row weight slab (%d bytes) is too large for the "
-                        "shared-memory ring", h->slot_bytes);
-        }
-    }
+    h->layer_stride = align_up(off + h->dn_bias_b, 256);
 
     cudaError_t e = cudaGetDevice(&h->device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
     if (e != cudaSuccess) {
         free_handle(h);
-        return cuda_fail(e, "cudaGetDevice");
+        return cuda_fail(e, "cudaGetDevice / SM count");
     }
-    e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
-    if (e != cudaSuccess) {
-        free_handle(h);
-        return cuda_fail(e, "cudaDeviceGetAttribute");
-    }
-    h->grid = h->num_sms;   // one CTA per SM: every CTA of a layer is resident at once
-    if (slabs) {
-        int per_sm = 0;
-        moe::LayerParams lp{};
-        lp.nslots = h->nslots;
-        lp.slot_bytes = h->slot_bytes;
-        lp.mmax = decode_tokens(c);
-        lp.I = c.intermediate;
-        e = moe::prepare_layer_kernel(c.format, c.group, moe::layer_smem_bytes(lp), &per_sm);
-        if (e != cudaSuccess) {
-            free_handle(h);
-            return cuda_fail(e, "layer kernel set-up");
-        }
-        if (per_sm < 1) {
-            free_handle(h);
-            return fail(MOE_ERR_UNSUPPORTED, "the layer kernel does not fit on an SM");
-        }
-    }
-    const size_t Mx = c.max_tokens, Kx = c.max_top_k, Md = decode_tokens(c);
-    const size_t ncount = moe::counter_words((int)H);
+    const size_t Mx = c.max_tokens;
     h->st_off_r = align_up(Mx * H * 2, 256);
     h->st_off_l = h->st_off_r + align_up(Mx * H * 2, 256);
     h->st_bytes = h->st_off_l + Mx * E * sizeof(float);
     if ((rc = dev_alloc(&h->arena, h->layer_stride * c.num_layers, "expert weights")) ||
-        (rc = dev_alloc(&h->special, (size_t)c.num_layers * E * 2 * sizeof(uint32_t), "flags")) ||
-        (rc = dev_alloc(&h->h, Md * Kx * I * sizeof(float), "h workspace")) ||
-        (rc = dev_alloc(&h->ypart, Md * Kx * H * sizeof(float), "y workspace")) ||
-        (rc = dev_alloc(&h->counters, ncount * sizeof(unsigned), "counters")) ||
         (rc = dev_alloc(&h->stats, c.num_layers * sizeof(int), "stats")) ||
         (rc = dev_alloc(&h->status, sizeof(int), "status")) ||
         (rc = dev_alloc(&h->st_dev, h->st_bytes, "staging"))) {
@@ -546,19 +536,19 @@ int moe_create(const moe_config* cfg, moe_handle** out)
         free_handle(h);
         return fail(MOE_ERR_OOM, "cudaHostAlloc(%zu bytes) for the host staging failed", h->st_bytes);
     }
-    if ((e = cudaMemset(h->counters, 0, ncount * sizeof(unsigned))) != cudaSuccess ||
-        (e = cudaMemset(h->special, 0, (size_t)c.num_layers * E * 2 * sizeof(uint32_t))) != cudaSuccess ||
-        (e = cudaMemset(h->stats, 0, c.num_layers * sizeof(int))) != cudaSuccess ||
-        (e = cudaMemset(h->status, 0, sizeof(int))) != cudaSuccess ||
-        (e = cudaStreamCreateWithFlags(&h->capture_stream, cudaStreamNonBlocking)) != cudaSuccess ||
-        (e = cudaDeviceSynchronize()) != cudaSuccess) {
+    if ((e = cudaMemset(h->stats, 0, c.num_layers * sizeof(int))) != cudaSuccess ||
+        (e = cudaMemset(h->status, 0, sizeof(int))) != cudaSuccess) {
         free_handle(h);
         return cuda_fail(e, "moe_create setup");
     }
-    if ((c.format == MOE_FMT_MXFP4 && (rc = create_tiles(h)) != MOE_OK) ||
+    if ((rc = create_decode(h)) != MOE_OK ||
         (c.max_tokens > moe::kMaxTokens && (rc = create_batched(h)) != MOE_OK)) {
         free_handle(h);
         return rc;
+    }
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) {
+        free_handle(h);
+        return cuda_fail(e, "moe_create setup");
     }
     h->loaded.assign(c.num_layers, 0);
     *out = h;
@@ -599,7 +589,10 @@ int moe_load_experts(moe_handle* h, int layer, const void* gu_codes, const void*
         return fail(MOE_ERR_INVALID_ARG, "moe_load_experts: has_bias=1 but a bias pointer is NULL");
     cudaStream_t s = (cudaStream_t)stream;
     const moe_config& c = h->cfg;
+    const int H = c.hidden, I = c.intermediate, E = c.num_experts;
     uint8_t* base = h->arena + (size_t)layer * h->layer_stride;
+    // the caller's tensors are copied to a staging area first (they may be host
+    // memory), then reordered into the resident layout by a repack kernel
     uint8_t* staging = nullptr;
     const size_t st_bytes = align_up(h->gu_codes_b, 256) + align_up(h->gu_scales_b, 256) +
                             align_up(h->dn_codes_b, 256) + align_up(h->dn_scales_b, 256);
@@ -610,7 +603,6 @@ int moe_load_experts(moe_handle* h, int layer, const void* gu_codes, const void*
     uint8_t* st_gus = st_guc + align_up(h->gu_codes_b, 256);
     uint8_t* st_dnc = st_gus + align_up(h->gu_scales_b, 256);
     uint8_t* st_dns = st_dnc + align_up(h->dn_codes_b, 256);
-    uint32_t* special = h->special + (size_t)layer * c.num_experts * 2;
     cudaError_t e;
     if ((e = cudaMemcpyAsync(st_guc, gu_codes, h->gu_codes_b, cudaMemcpyDefault, s)) != cudaSuccess ||
         (e = cudaMemcpyAsync(st_gus, gu_scales, h->gu_scales_b, cudaMemcpyDefault, s)) != cudaSuccess ||
@@ -619,78 +611,33 @@ int moe_load_experts(moe_handle* h, int layer, const void* gu_codes, const void*
         (h->gu_bias_b && (e = cudaMemcpyAsync(base + h->off_gu_bias, gu_bias, h->gu_bias_b,
                                               cudaMemcpyDefault, s)) != cudaSuccess) ||
         (h->dn_bias_b && (e = cudaMemcpyAsync(base + h->off_dn_bias, dn_bias, h->dn_bias_b,
-                                              cudaMemcpyDefault, s)) != cudaSuccess) ||
-        (e = cudaMemsetAsync(special, 0, (size_t)c.num_experts * 2 * sizeof(uint32_t), s)) != cudaSuccess ||
-        (!h->tiles && (e = moe::launch_repack(c.format, c.group, st_guc, st_gus, c.num_experts, 2 * c.intermediate,
-                                              c.hidden, base, (long long)h->gu_expert, h->gu_slab, special, 0,
-                                              s)) != cudaSuccess) ||
-        (!h->tiles && (e = moe::launch_repack(c.format, c.group, st_dnc, st_dns, c.num_experts, c.hidden,
-                                              c.intermediate, base + h->off_dn, (long long)h->dn_expert,
-                                              h->dn_slab, special, 1, s)) != cudaSuccess) ||
-        (h->tiles && (e = load_tiles(h, layer, st_guc, st_gus, st_dnc, st_dns, s)) != cudaSuccess) ||
-        (e = cudaStreamSynchronize(s)) != cudaSuccess) {
+                                              cudaMemcpyDefault, s)) != cudaSuccess)) {
         cudaStreamSynchronize(s);
         cudaFree(staging);
-        return cuda_fail(e, "moe_load_experts");
+        return cuda_fail(e, "moe_load_experts copy");
+    }
+    if (h->mxfp4) {
+        // gate rows [0, I) and up rows [I, 2I) interleaved per 64 in 128-row tiles
+        if ((e = moe::launch_repack_tiles(st_guc, st_gus, E, 2 * I, 2 * I, H, I, base, (long long)h->gu_expert, s)) ==
+            cudaSuccess)
+            e = moe::launch_repack_tiles(st_dnc, st_dns, E, H, H, I, 0, base + h->off_dn, (long long)h->dn_expert, s);
+    } else {
+        if ((e = moe::launch_repack_i4(st_guc, reinterpret_cast<const uint16_t*>(st_gus), E, H, I, c.group, 0, base,
+                                       (long long)h->gu_expert, s)) == cudaSuccess)
+            e = moe::launch_repack_i4(st_dnc, reinterpret_cast<const uint16_t*>(st_dns), E, H, I, c.group, 1,
+                                      base + h->off_dn, (long long)h->dn_expert, s);
+    }
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        cudaStreamSynchronize(s);
+        cudaFree(staging);
+        return cuda_fail(e, "moe_load_experts repack");
     }
     cudaFree(staging);
     h->loaded[layer] = 1;
     return MOE_OK;
 }
-
-}  // extern "C"
-
-namespace {
-
-int forward_impl(moe_handle* h, int layer, const void* x_bf16, const float* router_logits, int M,
-                 int top_k, void* out_bf16, float* out_f32, void* stream)
-{
-    int rc = check_forward_args(h, M, top_k);
-    if (rc != MOE_OK)
-        return rc;
-    if (layer < 0 || layer >= h->cfg.num_layers)
-        return fail(MOE_ERR_INVALID_ARG, "layer=%d out of range 0..%d", layer, h->cfg.num_layers - 1);
-    if (!x_bf16 || !router_logits || !out_bf16)
-        return fail(MOE_ERR_INVALID_ARG, "moe_forward: x, logits and out must not be NULL");
-    if (!aligned16(x_bf16) || !aligned16(out_bf16) || !aligned16(router_logits))
-        return fail(MOE_ERR_INVALID_ARG, "moe_forward: x, logits and out must be 16-byte aligned");
-    const size_t nb = (size_t)M * h->cfg.hidden * 2;
-    if (overlaps(x_bf16, nb, out_bf16, nb))
-        return fail(MOE_ERR_INVALID_ARG, "moe_forward: x overlaps out");
-    if (!h->loaded[layer])
-        return fail(MOE_ERR_NOT_LOADED, "moe_forward: layer %d has no experts loaded", layer);
-    if (M > moe::kMaxTokens) {
-        moe::BatchParams b = batch_params(h, layer);
-        b.logits = router_logits;
-        b.x = static_cast<const uint16_t*>(x_bf16);
-        b.resid = static_cast<uint16_t*>(out_bf16);
-        b.out_f32 = out_f32;
-        b.M = M;
-        b.k = top_k;
-        int launches = 0;
-        cudaError_t e = moe::launch_batched(b, h->num_sms, (cudaStream_t)stream, &launches);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "moe_forward (batched) launch");
-        h->last_layers = 1;
-        h->last_first_layer = layer;
-        h->last_launches = launches;
-        h->last_bM = M;
-        h->last_bk = top_k;
-        return MOE_OK;
-    }
-    cudaError_t e = launch_decode(h, layer, router_logits, x_bf16, out_bf16, M, top_k, (cudaStream_t)stream,
-                                  out_f32);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "moe_forward launch");
-    h->last_layers = 1;
-    h->last_first_layer = layer;
-    h->last_launches = decode_launches(h);
-    return MOE_OK;
-}
-
-}  // namespace
-
-extern "C" {
 
 int moe_forward(moe_handle* h, int layer, const void* x_bf16, const float* router_logits, int M,
                 int top_k, void* out_bf16, void* stream)
@@ -768,55 +715,51 @@ int moe_forward_stack(moe_handle* h, void* resid_bf16, const float* router_logit
         return fail(MOE_ERR_INVALID_ARG, "moe_forward_stack: resid and logits must not be NULL");
     if (!aligned16(resid_bf16) || !aligned16(router_logits))
         return fail(MOE_ERR_INVALID_ARG, "moe_forward_stack: resid and logits must be 16-byte aligned");
+    if ((rc = check_all_loaded(h, "moe_forward_stack")) != MOE_OK)
+        return rc;
     const int L = h->cfg.num_layers;
-    for (int l = 0; l < L; ++l)
-        if (!h->loaded[l])
-            return fail(MOE_ERR_NOT_LOADED, "moe_forward_stack: layer %d has no experts loaded", l);
-    StackGraph* g = nullptr;
-    for (auto& c : h->graphs)
-        if (c.M == M && c.k == top_k && c.resid == resid_bf16 && c.logits == router_logits)
-            g = &c;
-    if (!g) {
-        // capture the 2L launches once for this (M, top_k, buffers)
-        cudaStream_t cs = h->capture_stream;
-        cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "moe_forward_stack capture begin");
-        cudaError_t le = cudaSuccess;
-        for (int l = 0; l < L && le == cudaSuccess; ++l)
-            le = launch_decode(h, l, router_logits + (size_t)l * M * h->cfg.num_experts, nullptr, resid_bf16, M,
-                               top_k, cs);
-        cudaGraph_t graph = nullptr;
-        e = cudaStreamEndCapture(cs, &graph);
-        if (le != cudaSuccess || e != cudaSuccess) {
-            if (graph)
-                cudaGraphDestroy(graph);
-            return cuda_fail(le != cudaSuccess ? le : e, "moe_forward_stack capture");
-        }
-        cudaGraphExec_t exec = nullptr;
-        e = cudaGraphInstantiate(&exec, graph, 0);
-        cudaGraphDestroy(graph);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "moe_forward_stack instantiate");
-        if (h->graphs.size() >= 8) {
-            cudaGraphExecDestroy(h->graphs.front().exec);
-            h->graphs.erase(h->graphs.begin());
-        }
-        StackGraph ng;
-        ng.M = M;
-        ng.k = top_k;
-        ng.resid = resid_bf16;
-        ng.logits = router_logits;
-        ng.exec = exec;
-        h->graphs.push_back(ng);
-        g = &h->graphs.back();
-    }
-    cudaError_t e = cudaGraphLaunch(g->exec, (cudaStream_t)stream);
+    // the L layers in one persistent launch (grid barriers between layers); each
+    // layer's input is the normalised residual, which the kernel forms itself
+    cudaError_t e = launch_seq(h, 0, L, router_logits, (long long)M * h->cfg.num_experts * sizeof(float), nullptr,
+                               0, resid_bf16, 0, nullptr, 0, M, top_k, (cudaStream_t)stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "moe_forward_stack launch");
-    h->last_layers = L;
+    h->last_steps = L;
     h->last_first_layer = 0;
-    h->last_launches = L * decode_launches(h);
+    h->last_launches = 1;
+    return MOE_OK;
+}
+
+int moe_forward_steps(moe_handle* h, int n, int layer0, const void* x_bf16, const float* router_logits, int M,
+                      int top_k, void* out_bf16, void* stream)
+{
+    int rc = check_forward_args(h, M, top_k);
+    if (rc != MOE_OK)
+        return rc;
+    if (M > moe::kMaxTokens)
+        return fail(MOE_ERR_UNSUPPORTED, "moe_forward_steps: M=%d > %d; decode sizes only", M, moe::kMaxTokens);
+    const int L = h->cfg.num_layers;
+    if (n < 1 || layer0 < 0 || layer0 >= L)
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_steps: n=%d must be >= 1 and layer0=%d in 0..%d", n, layer0,
+                    L - 1);
+    if (!x_bf16 || !router_logits || !out_bf16)
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_steps: x, logits and out must not be NULL");
+    if (!aligned16(x_bf16) || !aligned16(out_bf16) || !aligned16(router_logits))
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_steps: x, logits and out must be 16-byte aligned");
+    const size_t nb = (size_t)n * M * h->cfg.hidden * 2;
+    if (overlaps(x_bf16, nb, out_bf16, nb))
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_steps: x overlaps out");
+    for (int s = 0; s < n && s < L; ++s)
+        if (!h->loaded[(layer0 + s) % L])
+            return fail(MOE_ERR_NOT_LOADED, "moe_forward_steps: layer %d has no experts loaded", (layer0 + s) % L);
+    const long long xs = (long long)M * h->cfg.hidden * 2, ls = (long long)M * h->cfg.num_experts * sizeof(float);
+    cudaError_t e = launch_seq(h, layer0, n, router_logits, ls, x_bf16, xs, out_bf16, xs, nullptr, 0, M, top_k,
+                               (cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "moe_forward_steps launch");
+    h->last_steps = n;
+    h->last_first_layer = layer0;
+    h->last_launches = 1;
     return MOE_OK;
 }
 
@@ -833,10 +776,9 @@ int moe_debug_stack_trace(moe_handle* h, void* resid_bf16, const float* router_l
         return fail(MOE_ERR_INVALID_ARG, "moe_debug_stack_trace: NULL argument");
     if (!aligned16(resid_bf16) || !aligned16(router_logits))
         return fail(MOE_ERR_INVALID_ARG, "moe_debug_stack_trace: resid and logits must be 16-byte aligned");
+    if ((rc = check_all_loaded(h, "moe_debug_stack_trace")) != MOE_OK)
+        return rc;
     const int L = h->cfg.num_layers;
-    for (int l = 0; l < L; ++l)
-        if (!h->loaded[l])
-            return fail(MOE_ERR_NOT_LOADED, "moe_debug_stack_trace: layer %d has no experts loaded", l);
     cudaStream_t s = (cudaStream_t)stream;
     const size_t nb = (size_t)M * h->cfg.hidden * 2;
     uint8_t* tr = static_cast<uint8_t*>(trace_bf16);
@@ -849,9 +791,9 @@ int moe_debug_stack_trace(moe_handle* h, void* resid_bf16, const float* router_l
     }
     if (e != cudaSuccess)
         return cuda_fail(e, "moe_debug_stack_trace");
-    h->last_layers = L;
+    h->last_steps = L;
     h->last_first_layer = 0;
-    h->last_launches = L * decode_launches(h);
+    h->last_launches = L;
     return MOE_OK;
 }
 
@@ -867,12 +809,10 @@ int moe_get_status(moe_handle* h, void* stream)
         (e = cudaMemset(h->status, 0, sizeof(int))) != cudaSuccess)
         return cuda_fail(e, "moe_get_status");
     if (st != MOE_OK) {
-        // a call gave up waiting: its cross-CTA counters may be left part-way; clear them
-        const size_t ncount = moe::counter_words(h->cfg.hidden);
-        // (the call tags restart with the counters, so the flags are cleared too)
-        if ((h->tc_cnt && (e = cudaMemset(h->tc_cnt, 0, moe::kTcCounterWords * sizeof(unsigned long long))) != cudaSuccess) ||
-            (h->tc_flags && (e = cudaMemset(h->tc_flags, 0, (size_t)h->num_sms * sizeof(unsigned))) != cudaSuccess) ||
-            (e = cudaMemset(h->counters, 0, ncount * sizeof(unsigned))) != cudaSuccess ||
+        // a call gave up waiting: its cross-CTA counters may be left part-way; clear
+        // them (the call tags restart with the counters, so the flags are cleared too)
+        if ((e = cudaMemset(h->cnt, 0, moe::kTcCounterWords * sizeof(unsigned long long))) != cudaSuccess ||
+            (h->pflag && (e = cudaMemset(h->pflag, 0, (size_t)h->num_sms * sizeof(unsigned))) != cudaSuccess) ||
             (e = cudaDeviceSynchronize()) != cudaSuccess)
             return cuda_fail(e, "moe_get_status reset");
     }
@@ -886,16 +826,16 @@ int moe_last_bytes(moe_handle* h, void* stream, long long* bytes)
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "moe_last_bytes sync");
-    std::vector<int> nu(h->last_layers > 0 ? h->last_layers : 1, 0);
-    if (h->last_layers > 0) {
-        e = cudaMemcpy(nu.data(), h->stats + h->last_first_layer, h->last_layers * sizeof(int),
-                       cudaMemcpyDeviceToHost);
+    const int L = h->cfg.num_layers;
+    std::vector<int> nu(L, 0);
+    if (h->last_steps > 0) {
+        e = cudaMemcpy(nu.data(), h->stats, L * sizeof(int), cudaMemcpyDeviceToHost);
         if (e != cudaSuccess)
             return cuda_fail(e, "moe_last_bytes read");
     }
     long long total = 0;
-    for (int l = 0; l < h->last_layers; ++l)
-        total += (long long)nu[l] * moe_expert_bytes(h);
+    for (int s2 = 0; s2 < h->last_steps; ++s2)
+        total += (long long)nu[(h->last_first_layer + s2) % L] * moe_expert_bytes(h);
     *bytes = total;
     return MOE_OK;
 }
@@ -912,23 +852,14 @@ int moe_debug_dequant(moe_handle* h, int layer, int expert, int proj, float* out
         return fail(MOE_ERR_NOT_LOADED, "moe_debug_dequant: layer %d has no experts loaded", layer);
     const int N = proj == 0 ? 2 * c.intermediate : c.hidden;
     const int K = proj == 0 ? c.hidden : c.intermediate;
-    if (h->tiles) {
-        // the bytes the tensor-core kernels stream (interleaved gate/up tiles,
-        // scale chunks in tensor-memory order), decoded back to caller order
-        const uint8_t* tb = h->tarena + (size_t)layer * h->t_layer_stride;
-        const uint8_t* src = proj == 0 ? tb + (size_t)expert * h->t_gu_expert
-                                       : tb + h->t_off_dn + (size_t)expert * h->t_dn_expert;
-        cudaError_t e = moe::launch_dequant_tiles(src, N, K, proj == 0 ? c.intermediate : 0, out_dev,
-                                                  (cudaStream_t)stream);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "moe_debug_dequant launch");
-        return MOE_OK;
-    }
-    moe::LayerParams p = layer_params(h, layer);
-    const uint8_t* slabs = proj == 0 ? p.gu + (size_t)expert * h->gu_expert
-                                     : p.dn + (size_t)expert * h->dn_expert;
-    cudaError_t e = moe::launch_dequant(c.format, c.group, slabs, N, K, proj == 0 ? h->gu_slab : h->dn_slab,
-                                        out_dev, (cudaStream_t)stream);
+    // the very bytes the forward kernels stream, decoded back to caller order
+    const uint8_t* base = h->arena + (size_t)layer * h->layer_stride;
+    const uint8_t* src = proj == 0 ? base + (size_t)expert * h->gu_expert
+                                   : base + h->off_dn + (size_t)expert * h->dn_expert;
+    cudaError_t e = h->mxfp4 ? moe::launch_dequant_tiles(src, N, K, proj == 0 ? c.intermediate : 0, out_dev,
+                                                         (cudaStream_t)stream)
+                             : moe::launch_dequant_i4(src, c.hidden, c.intermediate, c.group, proj, out_dev,
+                                                      (cudaStream_t)stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "moe_debug_dequant launch");
     return MOE_OK;

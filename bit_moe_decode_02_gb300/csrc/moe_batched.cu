@@ -13,7 +13,7 @@
 // tensor memory.
 //
 // Kernels, in stream order:
-//   route_kernel (moe_decode.cu)  top-k + softmax per token
+//   route_kernel                  top-k + softmax per token
 //   plan_kernel                   per-expert stable permutation, token tiles
 //   quant_x_kernel                MX(x) into the token tiles
 //   gemm_kernel<true>             gate and up tiles, + bias, SwiGLU, MX(h) into
@@ -26,6 +26,7 @@
 
 #include "../../include/moe.h"
 #include "moe_internal.h"
+#include "route.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -692,6 +693,15 @@ __global__ void dequant_tiles_kernel(const uint8_t* __restrict__ tiles, int N, i
     }
 }
 
+// Top-k and the softmax over it, one warp per token (the debug router and the
+// first step of the batched layer).
+__global__ void route_kernel(const float* __restrict__ logits, int M, int E, int k, int* idx, float* w)
+{
+    const int tok = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (tok < M)
+        rt::warp_topk(logits + (size_t)tok * E, E, k, idx + (size_t)tok * k, w + (size_t)tok * k);
+}
+
 template <bool DUAL>
 cudaError_t launch_gemm(const GemmParams& g, int grid, cudaStream_t s)
 {
@@ -767,6 +777,14 @@ cudaError_t launch_repack_tiles(const uint8_t* codes, const uint8_t* scales, int
     const long long blocks = (work + 255) / 256 < 65536 ? (work + 255) / 256 : 65536;
     repack_tiles_kernel<<<(unsigned)blocks, 256, 0, stream>>>(codes, scales, E, src_rows, N, K, interleave, out,
                                                               expert_bytes);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_route(const float* logits, int M, int E, int k, int* idx, float* w,
+                         cudaStream_t stream)
+{
+    const int warps = 8;
+    route_kernel<<<(M + warps - 1) / warps, warps * 32, 0, stream>>>(logits, M, E, k, idx, w);
     return cudaGetLastError();
 }
 

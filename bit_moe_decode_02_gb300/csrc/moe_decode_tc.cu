@@ -223,9 +223,9 @@ struct GuStage {
 // still has a 4 KB slot, so the MMA's 128-row read stays inside the stage.
 __device__ __forceinline__ uint32_t dn_stage_size(int n) { return (uint32_t)n * (kTileA + kSfChunk); }
 
-struct RingTc {
-    unsigned long long head = 0;
-    uint32_t phys = 0;
+struct RingTc {   // (value-initialise: RingTc{} starts at 0)
+    unsigned long long head;
+    uint32_t phys;
     __device__ uint32_t place(uint32_t size, uint32_t cap, unsigned long long* end)
     {
         if (phys + size > cap) {
@@ -270,6 +270,20 @@ __device__ __forceinline__ unsigned long long atom_add_release_u64(unsigned long
 __device__ __forceinline__ unsigned long long count_target(unsigned long long old, int G)
 {
     return (old / (unsigned long long)G + 1ull) * (unsigned long long)G;
+}
+// Grid barrier between calls (one thread of each CTA): arrive, then wait for
+// the count of this barrier to complete; gives up after `limit` polls.
+__device__ __forceinline__ void grid_sync(unsigned long long* cnt, int G, int limit, int* status)
+{
+    const unsigned long long tgt = count_target(atom_add_release_u64(cnt, 1ull), G);
+    int spins = 0;
+#pragma unroll 1
+    while (ld_acquire_u64(cnt) < tgt) {
+        if (++spins > limit) {
+            atomicExch(status, MOE_ERR_DEVICE_TIMEOUT);
+            break;
+        }
+    }
 }
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
@@ -522,6 +536,19 @@ __device__ __forceinline__ void drain_region(uint32_t taddr, int n, int nrows, i
 
 constexpr int kFinSlots = 64;   // output float4s of a CTA's slice whose final terms are prefetched
 
+// The running state of a role across the calls of a launch: every mbarrier
+// phase and ring position follows it.  Kept in shared memory between calls (a
+// role's threads load it when a call starts, its owner stores it back), so no
+// register holds it across the loop over calls.
+struct RoleState {
+    RingTc rs;                    // producer / MMA issuers: the stage ring
+    uint32_t sc;                  // producer / MMA issuers: stages so far
+    uint32_t rel;                 // producer: stages released
+    unsigned long long rel_end;   // producer: ring position released
+    uint32_t kk;                  // MMA issuers / epilogue: down region groups
+    uint32_t sfn;                 // MMA issuers: scale-factor sets used
+};
+
 struct TcSmem {
     uint64_t full[kSlots], empty[kSlots];
     uint64_t accf[2], acce[2];   // gate/up accumulator buffers: full / drained
@@ -540,14 +567,27 @@ struct TcSmem {
     float wslot[kMaxUnits][kMaxTokens];   // routing weight of token m for expert slot s (0 if not chosen)
     float fin[kFinSlots][4];              // r + sum_s w_s b_s of the slice's elements (loaded before the grid barrier)
     PackedPlan plan_tab[kPlanTab];        // plan of nu = k + i distinct experts
+    unsigned long long ends[kSlots];      // producer: ring position after each stage in flight
+    RoleState role[4];                    // producer, MMA issuer A, MMA issuer B, epilogue
+    int gbase, ubase, npc;                // gate/up items, whole units and split-unit calls so far
 };
 
-__global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTcParams p)
+// The launch's shared state: the stage ring (dynamic), the control block and a
+// copy of the parameters (read by every call).
+extern __shared__ __align__(1024) uint8_t ring[];
+__shared__ __align__(8) TcSmem sh;
+__shared__ DecodeTcParams g_p;
+
+// One layer call of a launch for one role group: `group` 0 = the routing,
+// producer and MMA-issuer warps (0, 1, 6), 1 = the x-term / epilogue warps
+// (2..5), 2 = the combiner warp (7).  Each group runs its own loop over the
+// calls, so that only its own values are live across the loop; the end of a
+// call (bias / residual prefetch, the grid barriers and the reduction) is
+// executed by every thread in each group's loop.
+template <int GROUP>
+__device__ __forceinline__ void decode_call(const int call)
 {
-    extern __shared__ __align__(1024) uint8_t ring[];
-    __shared__ __align__(8) TcSmem sh;
-    // the next layer's CTAs may take each SM as soon as this CTA leaves it
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const DecodeTcParams& p = g_p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, b = blockIdx.x, M = p.M;
     const int nrows = rows_for(M), atom = nrows * 32;
@@ -562,67 +602,40 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
     uint8_t* hterm = xs + ((xterm_bytes(p.H, atom) + 127) & ~127u);   // [3][kHTerm]
     float4* xch = reinterpret_cast<float4*>(hterm + 3 * kHTerm);       // [2][32]
     float* oacc = reinterpret_cast<float*>(hterm + 3 * kHTerm + 2 * 32 * 16);   // [H][M]
-
-    // warm L2 and the TLB for what the first steps read once the previous grid
-    // is complete (a prefetch returns no data, so it cannot see a stale value)
-    if (warp == 2 && lane < M)
-        prefetch_l2(p.logits + (size_t)lane * p.E);
-    if (warp >= 3 && warp <= 5 && b < nitems) {
-        const int it = b + G * (warp - 3);
-        if (it < nitems) {
-            const int m = it / nblk, kb = it - m * nblk;
-            if (lane == 0)
-                prefetch_l2((p.x ? p.x : p.resid) + (size_t)m * p.H + 32 * kb);
-        }
-    }
-    if (tid == 0) {
-        for (int i = 0; i < kSlots; ++i) {
-            mbar_init(&sh.full[i], 1);
-            mbar_init(&sh.empty[i], 2);   // both MMA issuers release every stage
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&sh.accf[i], 2);
-            mbar_init(&sh.acce[i], 4);
-            mbar_init(&sh.dnf[i], 2);
-            mbar_init(&sh.dne[i], 4);
-            mbar_init(&sh.hbar[i], 1);
-        }
-        mbar_init(&sh.routed, 1);
-        mbar_init(&sh.xfull, 1);
-        mbar_init(&sh.hsfull, 1);
-        mbar_init(&sh.planbar, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(su32(&sh.tmem_base)), "r"(kTmemCols));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
-    // the plan of every distinct-expert count the call can have (lane i: nu =
-    // k + i), from the shapes alone, so before the previous grid is waited for
     const int nu_hi = (M * p.k < p.E ? M * p.k : p.E) < kMaxUnits ? (M * p.k < p.E ? M * p.k : p.E) : kMaxUnits;
-    if (warp == kCombineWarp) {
-        const int nu = p.k + lane;
-        if (lane < kPlanTab && nu <= nu_hi)
-            sh.plan_tab[lane] = pack_plan(make_plan(b, G, nu * T1, KSH, CHH, T2));
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&sh.planbar);
-    }
-    // everything below reads what the previous grid in the stream wrote (the
-    // logits, x, the residual) or shares its workspace
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // this thread's role state (0 producer, 1 / 2 MMA issuers, 3 epilogue)
+    const int ri = warp == 0 ? 0 : (warp == 1 ? 1 : (warp == kMmaWarpB ? 2 : 3));
+    RoleState st = sh.role[ri];
+    int gbase = sh.gbase, ubase = sh.ubase, npc = sh.npc;
+    RingTc& rs = st.rs;
+    uint32_t& sc = st.sc;
+    uint32_t& rel = st.rel;
+    unsigned long long& rel_end = st.rel_end;
+    uint32_t& kk = st.kk;
+    uint32_t& sfn = st.sfn;
+    const int layer = (p.layer0 + call) % p.nlayers;
+    // this call's tensors (recomputed where used rather than held in registers)
+#define cl_gu (p.gu + (long long)layer * p.layer_stride)
+#define cl_dn (p.dn + (long long)layer * p.layer_stride)
+#define cl_gub (p.gu_bias ? reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(p.gu_bias) + \
+                                                            (long long)layer * p.bias_stride) : nullptr)
+#define cl_dnb (p.dn_bias ? reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(p.dn_bias) + \
+                                                            (long long)layer * p.bias_stride) : nullptr)
+#define cl_logits reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(p.logits) + \
+                                                 (long long)call * p.logits_stride)
+#define cl_x (p.x ? reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(p.x) + \
+                                                      (long long)call * p.x_stride) : nullptr)
+#define cl_resid reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(p.resid) + (long long)call * p.resid_stride)
+#define cl_f32 (p.out_f32 ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(p.out_f32) + \
+                                                     (long long)call * p.out_f32_stride) : nullptr)
 
-    if (warp < 2 || warp == kMmaWarpB) {
+    if (GROUP == 0) {
         // ---- routing (warps 0, 1, 6): token m on the (m % 3)-th of them, then the
         // distinct experts in ascending order
 #pragma unroll 1
         for (int m = warp == kMmaWarpB ? 2 : warp; m < M; m += 3)
-            rt::warp_topk_fit(p.logits + (size_t)m * p.E, p.E, p.k, sh.sel[m], sh.wt[m]);
+            rt::warp_topk_fit(cl_logits + (size_t)m * p.E, p.E, p.k, sh.sel[m], sh.wt[m]);
         route_barrier();
         if (warp == 0) {
             uint32_t bits = 0;
@@ -670,7 +683,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
             if (lane == 0)
                 mbar_arrive(&sh.routed);   // hands the routing to the epilogue warps
         }
-    } else if (warp <= 5) {
+    } else if (GROUP == 1) {
         // ---- x terms (warps 2..5): items b + G q + 4 G i, token-major (q = warp - 2)
         const int q = warp - 2, te = tid - 64;
         if (b < nitems) {
@@ -682,11 +695,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                 if (m != cm) {
                     // the token's row once; its shift S from its largest |x| (for
                     // x = bf16(r inv), the rounding is monotone, so that is bf16(max|r| inv))
-                    load_row((p.x ? p.x : p.resid) + (size_t)m * p.H, p.H, lane, rowv);
+                    load_row((cl_x ? cl_x : cl_resid) + (size_t)m * p.H, p.H, lane, rowv);
                     uint32_t ab;
-                    inv = row_stats(rowv, p.H, p.x == nullptr, ab);
+                    inv = row_stats(rowv, p.H, cl_x == nullptr, ab);
                     float amax = bf16f((uint16_t)ab);
-                    if (!p.x)
+                    if (!cl_x)
                         amax = bf16f(f2bf16_rne(amax * inv));
                     const int S = token_shift(amax);
                     sx = __uint_as_float((uint32_t)(127 + S) << 23);
@@ -696,7 +709,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                     cm = m;
                 }
                 const uint16_t raw = row_elem(rowv, kb, lane);
-                const float v = (p.x ? bf16f(raw) : bf16f(f2bf16_rne(bf16f(raw) * inv))) * sx;
+                const float v = (cl_x ? bf16f(raw) : bf16f(f2bf16_rne(bf16f(raw) * inv))) * sx;
                 float r4[kMaxTokens] = {v, 0.f, 0.f, 0.f};
                 warp_terms_rows<1>(r4, m, kb, p.xt, p.xt + (long long)KSH * atom, atom, lane);
             }
@@ -731,9 +744,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
         // codes and unit-range scales rather than whatever shared memory held
         for (int i = te; i < 3 * kHTerm / 4; i += kEpi)
             reinterpret_cast<uint32_t*>(hterm)[i] = 0u;
-        mbar_wait(&sh.routed, 0, p.status);
+        mbar_wait(&sh.routed, call & 1, p.status);
     } else {
-        mbar_wait(&sh.routed, 0, p.status);
+        mbar_wait(&sh.routed, call & 1, p.status);
     }
 
     const int nu = sh.nu;
@@ -745,28 +758,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
     const int u0 = pl.u0, nun = pl.nun, nitem = pl.nitem;
     const int nact = U < G ? U : G;   // CTAs with units
     if (b == 0 && tid == 0 && p.nu_out)
-        *p.nu_out = nu;
+        p.nu_out[layer] = nu;
 
-    if (warp == 0) {
+    if (GROUP == 0 && warp == 0) {
         // ================================================================ producer
         // Weights stream in item order: every stage is weights only (the x terms
         // and the h' terms are in shared memory), so nothing but ring space is
         // ever waited for.
-        RingTc ring_alloc;
-        unsigned long long ends[kSlots];
-        unsigned long long rel_end = 0;
-        uint32_t c = 0, rel = 0;
         const uint64_t wpol = l2_evict_first();
         // the whole warp: claim ring bytes and a slot for a stage (stages retire in order)
         auto claim = [&](uint32_t size, uint32_t& off) -> uint32_t {
             unsigned long long end;
-            off = ring_alloc.place(size, ring_cap, &end);
+            off = rs.place(size, ring_cap, &end);
             int spins = 0;
 #pragma unroll 1
-            while (rel < c && (end - rel_end > (unsigned long long)ring_cap || rel + kSlots <= c)) {
+            while (rel < sc && (end - rel_end > (unsigned long long)ring_cap || rel + kSlots <= sc)) {
                 const uint32_t sl = rel % kSlots;
                 if (__shfl_sync(0xffffffffu, mbar_test_wait(&sh.empty[sl], (rel / kSlots) & 1) ? 1 : 0, 0)) {
-                    rel_end = ends[sl];
+                    rel_end = sh.ends[sl];
                     ++rel;
                 } else {
                     if (++spins > (1 << 24)) {
@@ -776,8 +785,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                     }
                 }
             }
-            const uint32_t slot = c % kSlots;
-            ends[slot] = end;
+            const uint32_t slot = sc % kSlots;
+            __syncwarp();
+            if (lane == 0)
+                sh.ends[slot] = end;
+            __syncwarp();
             return slot;
         };
         for (int k = 0; k < nitem; ++k) {
@@ -788,10 +800,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
             const int e = sh.unit_expert[s];
             if (kind == kGu || kind == kGuPiece) {
                 const int kA = piece ? pl.ks0 : 0, kB = piece ? pl.ks1 : KSH;
-                const uint8_t* a0 = p.gu + (long long)e * p.gu_expert + (long long)t * kRowTile * (p.H / 2);
-                const uint8_t* s0 = p.gu + (long long)e * p.gu_expert + (long long)(2 * p.I) * (p.H / 2) +
+                const uint8_t* a0 = cl_gu + (long long)e * p.gu_expert + (long long)t * kRowTile * (p.H / 2);
+                const uint8_t* s0 = cl_gu + (long long)e * p.gu_expert + (long long)(2 * p.I) * (p.H / 2) +
                                     (long long)t * CHH * kSfChunk;
-                for (int ks = kA; ks < kB; ks += kGuSteps, ++c) {
+                for (int ks = kA; ks < kB; ks += kGuSteps, ++sc) {
                     const int steps = kB - ks < kGuSteps ? kB - ks : kGuSteps;
                     const GuStage sg(steps);
                     uint32_t off;
@@ -808,11 +820,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
             } else {
                 // down rows of tiles [tA, tB), k-step t of K = I (h rows 64t .. 64t+63)
                 const int tA = piece ? pl.ta : 0, tB = piece ? pl.tb : T2;
-                const uint8_t* d0 = p.dn + (long long)e * p.dn_expert;
+                const uint8_t* d0 = cl_dn + (long long)e * p.dn_expert;
                 const uint8_t* sd0 = d0 + (long long)p.H * (p.I / 2) + (long long)(t >> 1) * kSfChunk;
                 for (int ga = tA; ga < tB; ga += TG) {
                     const int gb = ga + TG < tB ? ga + TG : tB;
-                    for (int t2 = ga; t2 < gb; t2 += kDnStageTiles, ++c) {
+                    for (int t2 = ga; t2 < gb; t2 += kDnStageTiles, ++sc) {
                         const int n = gb - t2 < kDnStageTiles ? gb - t2 : kDnStageTiles;
                         uint32_t off;
                         const uint32_t slot = claim(dn_stage_size(n), off);
@@ -842,7 +854,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                 }
             }
         }
-    } else if (warp == 1 || warp == kMmaWarpB) {
+    } else if (GROUP == 0) {
         // ================================================================ MMA issuers
         // Issuing a tcgen05 instruction holds its thread ~75-95 cycles (a scale
         // copy as long as an MMA), while the pipe takes one every ~40 cycles from
@@ -854,41 +866,40 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
         // weight stream sooner.
         const int role = warp == 1 ? 0 : 1;
         if (lane == 0) {
-            RingTc ring_alloc;
             const uint32_t idesc = (1u << 7) | (1u << 10) | ((uint32_t)(nrows >> 3) << 17) | (1u << 23) |
                                    ((uint32_t)(kRowTile >> 4) << 24);
             const uint32_t myset = tmem + kSfCol + role * 2 * kSfSet;
-            uint32_t c = 0, kk = 0, mine = 0;
             for (int k = 0; k < nitem; ++k) {
                 int kind, i;
                 item_of(pl, k, kind, i);
                 const bool piece = kind >= kGuPiece;
                 const int t = (piece ? pl.su : u0 + i) % T1;
                 if (kind == kGu || kind == kGuPiece) {
-                    const int gi = piece ? 0 : i + pl.piece;   // gate/up accumulator use
+                    const int gl = piece ? 0 : i + pl.piece;   // gate/up accumulator use in this call
+                    const int gi = gbase + gl;                  // ... and since the launch
                     const int kA = piece ? pl.ks0 : 0, kB = piece ? pl.ks1 : KSH;
                     // each issuer adds its half of every stage into its own accumulator half
                     const uint32_t buf = gi & 1;
-                    if (gi == 0)
-                        mbar_wait(&sh.xfull, 0, p.status);   // the layer's x terms are in
+                    if (gl == 0)
+                        mbar_wait(&sh.xfull, call & 1, p.status);   // the call's x terms are in
                     if (gi >= 2)
                         mbar_wait(&sh.acce[buf], ((gi >> 1) - 1) & 1, p.status);
                     tc_fence_after();
                     const uint32_t d = tmem + kGuCol + buf * kGuBuf + role * 32;
                     bool first = true;
-                    for (int ks = kA; ks < kB; ks += kGuSteps, ++c) {
+                    for (int ks = kA; ks < kB; ks += kGuSteps, ++sc) {
                         const int steps = kB - ks < kGuSteps ? kB - ks : kGuSteps;
                         const GuStage sg(steps);
                         unsigned long long end;
-                        const uint32_t st = su32(ring) + ring_alloc.place(sg.size, ring_cap, &end);
+                        const uint32_t st = su32(ring) + rs.place(sg.size, ring_cap, &end);
                         // this issuer's scale chunks [c0, c1) = k-steps [2 c0, min(2 c1, steps))
                         const int chunks = (steps + 1) >> 1, half = (chunks + 1) >> 1;
                         const int c0 = role ? half : 0, c1 = role ? chunks : half;
-                        const uint32_t slot = c % kSlots;
+                        const uint32_t slot = sc % kSlots;
                         if (c0 < c1) {
-                            mbar_wait(&sh.full[slot], (c / kSlots) & 1, p.status);
+                            mbar_wait(&sh.full[slot], (sc / kSlots) & 1, p.status);
                             tc_fence_after();
-                            const uint32_t set = myset + (mine++ & 1) * kSfSet;
+                            const uint32_t set = myset + (sfn++ & 1) * kSfSet;
                             const uint32_t xsf = su32(xs) + KSH * atom + (ks >> 1) * kSfChunk;   // x-term scales
                             // (the hot loop: unrolled, descriptors stepped by adding the byte
                             // offset / 16 to the start-address field)
@@ -918,10 +929,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                     uint32_t hb;
                     if (piece) {
                         hb = su32(hterm + 2 * kHTerm);
-                        mbar_wait(&sh.hsfull, 0, p.status);
+                        mbar_wait(&sh.hsfull, npc & 1, p.status);
                     } else {
-                        hb = su32(hterm + (i & 1) * kHTerm);
-                        mbar_wait(&sh.hbar[i & 1], (i >> 1) & 1, p.status);
+                        const int ui = ubase + i;
+                        hb = su32(hterm + (ui & 1) * kHTerm);
+                        mbar_wait(&sh.hbar[ui & 1], (ui >> 1) & 1, p.status);
                     }
                     tc_fence_after();
                     const uint32_t aid = (uint32_t)(2 * (t & 1));   // A scale bytes of k-step t in its chunk
@@ -932,17 +944,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                             mbar_wait(&sh.dne[kk & 1], ((kk >> 1) - 1) & 1, p.status);
                         tc_fence_after();
                         const uint32_t dreg = tmem + kDnCol + (kk & 1) * kDnRegion;
-                        for (int t2 = ga; t2 < gb; t2 += kDnStageTiles, ++c) {
+                        for (int t2 = ga; t2 < gb; t2 += kDnStageTiles, ++sc) {
                             const int n = gb - t2 < kDnStageTiles ? gb - t2 : kDnStageTiles;
                             unsigned long long end;
-                            const uint32_t st = su32(ring) + ring_alloc.place(dn_stage_size(n), ring_cap, &end);
+                            const uint32_t st = su32(ring) + rs.place(dn_stage_size(n), ring_cap, &end);
                             // this issuer's tiles [j0, j1) of the stage
                             const int hn = (n + 1) >> 1, j0 = role ? hn : 0, j1 = role ? n : hn;
-                            const uint32_t slot = c % kSlots;
+                            const uint32_t slot = sc % kSlots;
                             if (j0 < j1) {
-                                mbar_wait(&sh.full[slot], (c / kSlots) & 1, p.status);
+                                mbar_wait(&sh.full[slot], (sc / kSlots) & 1, p.status);
                                 tc_fence_after();
-                                const uint32_t set = myset + (mine++ & 1) * kSfSet;
+                                const uint32_t set = myset + (sfn++ & 1) * kSfSet;
                                 tc_cp_sf(set, hb + 1024);
 #pragma unroll
                                 for (int j = 0; j < (kDnStageTiles + 1) / 2; ++j)
@@ -963,7 +975,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                 }
             }
         }
-    } else if (warp == kCombineWarp) {
+    } else if (GROUP == 2) {
         // ================================================================ combiner
         if (pl.piece) {
             // the split unit's h' for this CTA's down tiles: wait for every piece's
@@ -973,14 +985,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
             // the biases first: HBM is busy with the weight stream, so their
             // latency overlaps the wait for the other pieces
             float bg[2] = {0.f, 0.f}, bu[2] = {0.f, 0.f};
-            if (p.gu_bias)
+            if (cl_gub)
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
                     const int hrow = 64 * t + 32 * kb + lane;
-                    bg[kb] = bf16f(__ldg(p.gu_bias + (size_t)e * 2 * p.I + hrow));
-                    bu[kb] = bf16f(__ldg(p.gu_bias + (size_t)e * 2 * p.I + p.I + hrow));
+                    bg[kb] = bf16f(__ldg(cl_gub + (size_t)e * 2 * p.I + hrow));
+                    bu[kb] = bf16f(__ldg(cl_gub + (size_t)e * 2 * p.I + p.I + hrow));
                 }
-            mbar_wait(&sh.xfull, 0, p.status);   // (orders the call tag written before it)
+            mbar_wait(&sh.xfull, call & 1, p.status);   // (orders the call tag written before it)
             const unsigned tag = sh.epoch;
             const int b0 = pl.sj * pl.S;   // the CTA of piece 0
             int spins = 0;
@@ -1068,11 +1080,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                 }
             }
         };
-        uint32_t kk = 0;
         // 2^-S_m of each token: the gate/up sums carry the x terms' shift
         float ush[kMaxTokens] = {1.f, 1.f, 1.f, 1.f};
         if (nitem > 0) {
-            mbar_wait(&sh.xfull, 0, p.status);
+            mbar_wait(&sh.xfull, call & 1, p.status);
 #pragma unroll
             for (int m = 0; m < kMaxTokens; ++m)
                 if (m < M)
@@ -1086,14 +1097,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
             if (kind == kGu || kind == kGuPiece) {
                 // ---- gate (rows 0..63) and up (rows 64..127) sums of 64 h rows; the
                 // biases are loaded before the accumulator is waited for
-                const int gi = piece ? 0 : i + pl.piece;
+                const int gi = gbase + (piece ? 0 : i + pl.piece);   // gate/up accumulator use since the launch
                 const uint32_t buf = gi & 1;
                 const int hrow = 64 * t + 32 * (q & 1) + lane;
                 const int e = sh.unit_expert[s];
                 float bg = 0.f, bu = 0.f;
-                if (q < 2 && p.gu_bias) {
-                    bg = bf16f(__ldg(p.gu_bias + (size_t)e * 2 * p.I + hrow));
-                    bu = bf16f(__ldg(p.gu_bias + (size_t)e * 2 * p.I + p.I + hrow));
+                if (q < 2 && cl_gub) {
+                    bg = bf16f(__ldg(cl_gub + (size_t)e * 2 * p.I + hrow));
+                    bu = bf16f(__ldg(cl_gub + (size_t)e * 2 * p.I + p.I + hrow));
                 }
                 mbar_wait(&sh.accf[buf], (gi >> 1) & 1, p.status);
                 tc_fence_after();
@@ -1130,13 +1141,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                 if (lane == 0)
                     mbar_arrive(&sh.acce[buf]);
                 if (!piece) {
-                    uint8_t* hb = hterm + (i & 1) * kHTerm;
+                    const int ui = ubase + i;
+                    uint8_t* hb = hterm + (ui & 1) * kHTerm;
                     swiglu_terms(sm, s, bg, bu, hb);
                     if (q < 2)
                         fence_proxy_async_smem();
                     epi_barrier();
                     if (te == 0)
-                        mbar_arrive(&sh.hbar[i & 1]);
+                        mbar_arrive(&sh.hbar[ui & 1]);
                     continue;
                 }
                 // ---- a piece of a split unit: publish its partial sums (warp 7
@@ -1206,21 +1218,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
         const int el = (f0 + j) * 4 + z, row = el / V, m = el - row * V;
         float v = 0.f;
         if (m < M) {
-            if (p.dn_bias)
+            if (cl_dnb)
                 for (int s2 = 0; s2 < nu; ++s2)
-                    v = fmaf(sh.wslot[s2][m], bf16f(__ldg(p.dn_bias + (size_t)sh.unit_expert[s2] * p.H + row)), v);
-            v += bf16f(__ldcg(p.resid + (size_t)m * p.H + row));
+                    v = fmaf(sh.wslot[s2][m], bf16f(__ldg(cl_dnb + (size_t)sh.unit_expert[s2] * p.H + row)), v);
+            v += bf16f(__ldcg(cl_resid + (size_t)m * p.H + row));
         }
         return v;
     };
     if (tid < nf && tid < kFinSlots) {
-        mbar_wait(&sh.routed, 0, p.status);   // the weight slots (warp 1 writes them)
+        mbar_wait(&sh.routed, call & 1, p.status);   // the weight slots (warp 1 writes them)
 #pragma unroll
         for (int z = 0; z < 4; ++z)
             sh.fin[tid][z] = fin_term(tid, z);
     }
 
-    // ---- grid barrier: every CTA's output copy is stored (every CTA counts itself in)
+    // ---- grid barrier: every CTA's output copy is stored (every CTA counts itself in).
+    // The CTA's copy of the x terms has landed before it arrives (a CTA without
+    // units never waits for it otherwise, and the next call rewrites them).
+    if (tid == 64)
+        mbar_wait(&sh.xfull, call & 1, p.status);
     tc_fence_before();
     __syncthreads();
     if (tid == 0) {
@@ -1277,14 +1293,130 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
                 const int el = (f0 + j) * 4 + lane, row = el / V, m = el - row * V;
                 if (m < M) {
                     const float v = (j < kFinSlots ? sh.fin[j][lane] : fin_term(j, lane)) + mine;
-                    p.resid[(size_t)m * p.H + row] = f2bf16_rne(v);
-                    if (p.out_f32)
-                        p.out_f32[(size_t)m * p.H + row] = v;
+                    cl_resid[(size_t)m * p.H + row] = f2bf16_rne(v);
+                    if (cl_f32)
+                        cl_f32[(size_t)m * p.H + row] = v;
                 }
             }
         }
     }
 
+    // ---- end of the call: the role states go back to shared memory, and the next
+    // call reads its routing and inputs only after every CTA's slice of this
+    // output is written
+    if (call + 1 < p.ncalls) {
+        if ((ri == 0 && lane == 0) || ((ri == 1 || ri == 2) && lane == 0) || (ri == 3 && tid == 64))
+            sh.role[ri] = st;
+        if (tid == 0) {
+            sh.gbase = gbase + nun + pl.piece;
+            sh.ubase = ubase + nun;
+            sh.npc = npc + pl.piece;
+        }
+        __syncthreads();
+        if (tid == 0)
+            grid_sync(p.done, G, p.spin_limit, p.status);
+        __syncthreads();
+    }
+#undef cl_gu
+#undef cl_dn
+#undef cl_gub
+#undef cl_dnb
+#undef cl_logits
+#undef cl_x
+#undef cl_resid
+#undef cl_f32
+}
+
+__global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTcParams p)
+{
+    // the next layer's CTAs may take each SM as soon as this CTA leaves it
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = gridDim.x, b = blockIdx.x, M = p.M;
+    const int nrows = rows_for(M), atom = nrows * 32;
+    const int KSH = p.H / 64, CHH = ceil_div(p.H, 128), CHI = ceil_div(p.I, 128);
+    const int T1 = p.I / 64, T2 = ceil_div(p.H, kRowTile);   // units per expert, down row tiles
+    const int TG = kDnRegion / nrows;                           // down tiles per accumulator region
+    const int nblk = p.H / 32, nitems = M * nblk;               // x-term items: (token, 32-element block)
+    const int V = M == 1 ? 1 : (M == 2 ? 2 : 4);                // floats per row of a CTA's output copy
+    const uint32_t tail_off = ((uint32_t)p.smem_bytes - tail_bytes(p.H, M, atom)) & ~127u;
+    const uint32_t ring_cap = tail_off;
+    uint8_t* xs = ring + tail_off;                              // x terms of the layer
+    uint8_t* hterm = xs + ((xterm_bytes(p.H, atom) + 127) & ~127u);   // [3][kHTerm]
+    float4* xch = reinterpret_cast<float4*>(hterm + 3 * kHTerm);       // [2][32]
+    float* oacc = reinterpret_cast<float*>(hterm + 3 * kHTerm + 2 * 32 * 16);   // [H][M]
+
+    // warm L2 and the TLB for what the first steps read once the previous grid
+    // is complete (a prefetch returns no data, so it cannot see a stale value)
+    if (warp == 2 && lane < M)
+        prefetch_l2(p.logits + (size_t)lane * p.E);
+    if (warp >= 3 && warp <= 5 && b < nitems) {
+        const int it = b + G * (warp - 3);
+        if (it < nitems) {
+            const int m = it / nblk, kb = it - m * nblk;
+            if (lane == 0)
+                prefetch_l2((p.x ? p.x : p.resid) + (size_t)m * p.H + 32 * kb);
+        }
+    }
+    if (tid == 0) {
+        g_p = p;   // the calls read the parameters from shared memory
+        for (int r = 0; r < 4; ++r)
+            sh.role[r] = RoleState{};
+        sh.gbase = sh.ubase = sh.npc = 0;
+        for (int i = 0; i < kSlots; ++i) {
+            mbar_init(&sh.full[i], 1);
+            mbar_init(&sh.empty[i], 2);   // both MMA issuers release every stage
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sh.accf[i], 2);
+            mbar_init(&sh.acce[i], 4);
+            mbar_init(&sh.dnf[i], 2);
+            mbar_init(&sh.dne[i], 4);
+            mbar_init(&sh.hbar[i], 1);
+        }
+        mbar_init(&sh.routed, 1);
+        mbar_init(&sh.xfull, 1);
+        mbar_init(&sh.hsfull, 1);
+        mbar_init(&sh.planbar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(su32(&sh.tmem_base)), "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+    // the plan of every distinct-expert count the call can have (lane i: nu =
+    // k + i), from the shapes alone, so before the previous grid is waited for
+    const int nu_hi = (M * p.k < p.E ? M * p.k : p.E) < kMaxUnits ? (M * p.k < p.E ? M * p.k : p.E) : kMaxUnits;
+    if (warp == kCombineWarp) {
+        const int nu = p.k + lane;
+        if (lane < kPlanTab && nu <= nu_hi)
+            sh.plan_tab[lane] = pack_plan(make_plan(b, G, nu * T1, KSH, CHH, T2));
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&sh.planbar);
+    }
+    // everything below reads what the previous grid in the stream wrote (the
+    // logits, x, the residual) or shares its workspace
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    if (warp < 2 || warp == kMmaWarpB) {
+#pragma unroll 1
+        for (int call = 0; call < p.ncalls; ++call)
+            decode_call<0>(call);
+    } else if (warp <= 5) {
+#pragma unroll 1
+        for (int call = 0; call < p.ncalls; ++call)
+            decode_call<1>(call);
+    } else {
+#pragma unroll 1
+        for (int call = 0; call < p.ncalls; ++call)
+            decode_call<2>(call);
+    }
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));

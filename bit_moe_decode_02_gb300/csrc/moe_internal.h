@@ -1,14 +1,5 @@
 // moe_internal.h -- declarations shared by the C-ABI layer (moe_api.cu) and
-// the kernels (moe_decode.cu).  Not part of the public interface.
-//
-// Resident weight layout ("slabs").  Every expert projection W [N][K] is
-// stored as N/16 slabs of 16 consecutive rows.  A slab is
-//     [codes: K/64 segments x 32 lanes x 16 bytes][scales: K/64 x 8 x SB bytes]
-// where the 16 code bytes of (segment q, lane l) are exactly the A operands of
-// lane l for the four m16n8k16 MMAs that cover K = 64q .. 64q+63 (g = l/4,
-// t = l%4; word j holds rows g and g+8, elements 16j + {2t, 2t+1, 2t+8, 2t+9}),
-// and the SB scale bytes of (segment q, g) are the scales of rows g and g+8
-// for that segment.  A slab is contiguous, so one bulk copy moves it.
+// the kernels.  Not part of the public interface.
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -19,67 +10,7 @@ constexpr int kMaxTokens = 4;      // decode M
 constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 256;
 constexpr int kMaxUnits = kMaxTokens * kMaxTopK;   // distinct experts of one layer call
-constexpr int kMaxK = 3072;        // largest H or I (12 warps x 4 segments x 64)
-constexpr int kComputeWarps = 12;  // MMA warps of the layer kernel
-constexpr int kThreads = (kComputeWarps + 2) * 32;   // + a producer and a signalling warp
-constexpr int kMaxSegPerWarp = kMaxK / 64 / kComputeWarps;
-constexpr int kSlabRows = 16;
-constexpr int kMaxSlots = 8;       // depth of the shared-memory slab ring
-constexpr int kSmemBudget = 220 * 1024;    // dynamic shared memory of the layer kernel
-constexpr int kRedBytes = 2 * kComputeWarps * 32 * kMaxTokens * 4;
-constexpr int kXfragBytes = kComputeWarps * kMaxSegPerWarp * 4 * 32 * 8;   // x MMA fragments
-
-enum { FMT_MXFP4 = 1, FMT_INT4 = 2 };
-
-// Scale bytes per (segment, g) entry: MXFP4 4 (two E8M0 blocks x two rows),
-// int4 with one group per segment or more 4 (one fp16 x two rows), int4 with
-// 32-element groups 8 (two fp16 x two rows).
-inline __host__ __device__ int scale_entry_bytes(int fmt, int group)
-{
-    return fmt == FMT_MXFP4 ? 4 : (group == 32 ? 8 : 4);
-}
-inline __host__ __device__ int slab_bytes(int K, int sb) { return 8 * K + (K / 64) * 8 * sb; }
-
-struct LayerParams {
-    const uint8_t* gu;          // gate_up slabs of expert 0; expert e at + e * gu_expert_bytes
-    const uint8_t* dn;          // down slabs
-    const uint16_t* gu_bias;    // [E][2I] bf16, or nullptr
-    const uint16_t* dn_bias;    // [E][H] bf16, or nullptr
-    const uint32_t* special;    // [E][2]: 1 if a projection holds an E8M0 byte 0 or 255
-    const float* logits;        // [M][E]
-    const uint16_t* x;          // [M][H] bf16 layer input, or nullptr: normalise resid
-    uint16_t* resid;            // [M][H] bf16 residual in, result out
-    float* h;                   // workspace [M][kmax][I]
-    float* ypart;               // workspace [M][kmax][H]
-    unsigned* done;             // [kMaxUnits] gate_up slab-pairs finished per unit (zero between calls)
-    unsigned* hmax;             // [kMaxUnits][kMaxTokens] bits of max |h| (zero between calls)
-    unsigned* slab_cnt;         // [H/16] units finished per down slab (zero between calls)
-    unsigned* exit_cnt;         // [1] CTAs finished (zero between calls)
-    int* status;                // device status word
-    int* nu_out;                // distinct experts of this call (written by CTA 0)
-    float* out_f32;             // [M][H] fp32 result before the bf16 rounding, or nullptr
-    long long gu_expert_bytes, dn_expert_bytes;
-    int gu_slab_bytes, dn_slab_bytes;
-    int H, I, E, M, k, kmax, mmax, group;
-    int nslots, slot_bytes;
-};
-
-// Counters of one handle: done | hmax | slab_cnt | exit.
-inline size_t counter_words(int H) { return kMaxUnits + kMaxUnits * kMaxTokens + H / kSlabRows + 1; }
-
-// Launch the layer kernel on `stream` (programmatic dependent launch towards
-// the preceding kernel).  grid = one CTA per SM.
-cudaError_t launch_layer(const LayerParams& p, int fmt, int grid, cudaStream_t stream);
-// Dynamic shared memory the layer kernel needs, and its one-time set-up.
-size_t layer_smem_bytes(const LayerParams& p);
-cudaError_t prepare_layer_kernel(int fmt, int group, size_t smem, int* blocks_per_sm);
-
-// Caller layout -> slabs for E experts of one projection ([E][N][K/2] codes,
-// [E][N][K/32] u8 or [E][N][K/group] fp16 scales).  special[e * 2 + proj]
-// gets 1 if an E8M0 byte is 0 or 255.
-cudaError_t launch_repack(int fmt, int group, const uint8_t* codes, const uint8_t* scales, int E,
-                          int N, int K, uint8_t* out, long long expert_bytes, int slab_bytes,
-                          uint32_t* special, int proj, cudaStream_t stream);
+constexpr int kMaxK = 3072;        // largest H or I
 
 // Record the calling thread's error message (read by moe_last_error) and
 // return `code`.
@@ -181,23 +112,32 @@ cudaError_t launch_untile_h(const BatchParams& p, uint8_t* codes, uint8_t* scale
 // to the previous grid with programmatic dependent launch.
 
 struct DecodeTcParams {
-    const uint8_t* gu;          // interleaved tile layout: expert e at + e*gu_expert
-    const uint8_t* dn;          // tile layout: expert e at + e*dn_expert
+    // One launch runs `ncalls` layer calls in sequence: call c uses resident layer
+    // (layer0 + c) mod nlayers and its own inputs and outputs (base + c * stride,
+    // strides in bytes; a stride of 0 reuses the same buffer, as the stack does
+    // with its residual).  Call c + 1 reads nothing before call c's output is
+    // complete (a grid barrier separates them).
+    const uint8_t* gu;          // layer 0's interleaved tile layout: expert e at + e*gu_expert
+    const uint8_t* dn;          // layer 0's down tiles: expert e at + e*dn_expert
+    long long layer_stride;     // bytes from one layer's tiles to the next
     long long gu_expert, dn_expert;
-    const uint16_t* gu_bias;    // [E][2I] bf16 (gate | up), or nullptr
-    const uint16_t* dn_bias;    // [E][H] bf16, or nullptr
-    const float* logits;        // [M][E]
-    const uint16_t* x;          // [M][H] bf16, or nullptr: RMS-normalise resid
-    uint16_t* resid;            // [M][H] bf16 in/out
+    const uint16_t* gu_bias;    // layer 0's [E][2I] bf16 (gate | up), or nullptr
+    const uint16_t* dn_bias;    // layer 0's [E][H] bf16, or nullptr
+    long long bias_stride;      // bytes from one layer's biases to the next
+    const float* logits;        // [M][E] per call
+    const uint16_t* x;          // [M][H] bf16 per call, or nullptr: RMS-normalise resid
+    uint16_t* resid;            // [M][H] bf16 in/out per call
+    float* out_f32;             // [M][H] fp32 result before the bf16 rounding per call, or nullptr
+    long long logits_stride, x_stride, resid_stride, out_f32_stride;
+    int ncalls, layer0, nlayers;
     float* part;                // [G][H][4] each CTA's fp32 copy of the expert output
     uint8_t* xt;                // x terms of the layer: [H/64][N rows x 32 B][ceil(H/128)][512]
     float* gpart;               // [G][128][4] gate/up partial sums of split-unit pieces
     unsigned* pflag;            // [G] piece partial published: the call's tag
     unsigned long long* xcnt;   // [1] x-term publications, G per call (only grows)
-    unsigned long long* done;   // [1] output copies stored, G per call (only grows)
+    unsigned long long* done;   // [1] grid-barrier arrivals, G per barrier (only grows)
     int* status;
-    int* nu_out;
-    float* out_f32;             // [M][H] fp32 result before the bf16 rounding, or nullptr
+    int* nu_out;                // [nlayers] distinct experts of the last call on each layer
     int H, I, E, M, k;
     int smem_bytes;             // dynamic shared memory of the layer kernel
     int spin_limit;             // polls before a cross-CTA wait gives up (kSpinLimit by default)
@@ -217,6 +157,42 @@ constexpr int kTcCounterWords = 2;   // xcnt, done (64-bit)
 cudaError_t prepare_decode_tc(size_t smem);
 size_t decode_tc_static_smem();
 cudaError_t launch_decode_tc(const DecodeTcParams& p, size_t smem, int grid, cudaStream_t stream);
+
+// ------------------------------------------------------------ int4 decode
+// The packed-int4 decode layer (M <= 4) on m16n8k16 f16 MMAs (moe_decode_i4.cu),
+// weights in the unit layout described there; calls and strides as for
+// DecodeTcParams.
+struct DecodeI4Params {
+    const uint8_t* gu;          // layer 0's gate/up units: expert e at + e*gu_expert
+    const uint8_t* dn;          // layer 0's down units: expert e at + e*dn_expert
+    long long layer_stride, gu_expert, dn_expert;
+    const uint16_t* gu_bias;    // layer 0's [E][2I] bf16, or nullptr
+    const uint16_t* dn_bias;    // layer 0's [E][H] bf16, or nullptr
+    long long bias_stride;
+    const float* logits;
+    const uint16_t* x;          // or nullptr: RMS-normalise resid
+    uint16_t* resid;
+    float* out_f32;
+    long long logits_stride, x_stride, resid_stride, out_f32_stride;
+    int ncalls, layer0, nlayers;
+    float* part;                // [G][H][4] each CTA's fp32 copy of the expert output
+    unsigned long long* done;   // [1] grid-barrier arrivals (only grows)
+    int* status;
+    int* nu_out;                // [nlayers]
+    int H, I, E, M, k, group;
+    int smem_bytes;
+    int spin_limit, skip_cta;
+};
+constexpr int kI4Slot = 18432;    // one stage: up to 16 KB of codes, then up to 2 KB of scales
+constexpr int kI4Codes = 16384;
+// bytes of one unit (64 rows of h) of gate/up (proj 0) or down (proj 1)
+long long i4_unit_bytes(int H, int group, int proj);
+size_t decode_i4_static_smem();
+cudaError_t prepare_decode_i4(size_t smem);
+cudaError_t launch_decode_i4(const DecodeI4Params& p, size_t smem, int grid, cudaStream_t stream);
+cudaError_t launch_repack_i4(const uint8_t* codes, const uint16_t* scales, int E, int H, int I, int group, int proj,
+                             uint8_t* out, long long expert_bytes, cudaStream_t stream);
+cudaError_t launch_dequant_i4(const uint8_t* w, int H, int I, int group, int proj, float* out, cudaStream_t stream);
 
 // Debug kernels.
 // One expert projection of the tile layout back to fp32 in caller row order

@@ -166,11 +166,26 @@ int moe_forward_host(moe_handle* h, int layer, const void* x_bf16, const float* 
  * overflows within a few layers on these value distributions).
  * resid bf16 [M][H] holds r_0 on entry and r_L on return; logits fp32
  * [L][M][E].  Layer l+1 reads its logits only after layer l's output is
- * complete.  Device pointers.  Launched as a cached CUDA graph of L
+ * complete.  Device pointers.  MXFP4: one persistent launch for all L layers
+ * (grid barriers between them); int4: a cached CUDA graph of L
  * programmatically chained layer kernels per (M, top_k, resid, logits).
  * Decode sizes only: M <= 4 (else MOE_ERR_UNSUPPORTED). */
 int moe_forward_stack(moe_handle* h, void* resid_bf16, const float* router_logits,
                       int M, int top_k, void* stream);
+
+/* n single-layer decode steps in sequence: step s runs resident layer
+ * (layer0 + s) mod L on x[s], logits[s] and out[s] (x bf16 [n][M][H],
+ * router_logits fp32 [n][M][E], out bf16 [n][M][H]: the residual of each step
+ * on entry, r + MoE(x) on return), exactly as n moe_forward calls in that order
+ * would (bit-identical results).  Step s + 1 reads its routing and inputs only
+ * after step s's output is complete.  MXFP4: one persistent launch for all n
+ * steps ("all decode tokens in a single command buffer", "Single-stream int4
+ * decode of a 30B MoE", section 1); int4: one launch per step.  Decode sizes
+ * only (M <= 4); x must not overlap out; device pointers, 16-byte aligned.
+ * moe_last_bytes then counts each step's distinct experts (a layer run by
+ * several steps counts its last step's, n times over). */
+int moe_forward_steps(moe_handle* h, int n, int layer0, const void* x_bf16, const float* router_logits,
+                      int M, int top_k, void* out_bf16, void* stream);
 
 /* Synchronise `stream` and return (and clear) the handle's device status:
  * MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_FAULT.  After a non-OK

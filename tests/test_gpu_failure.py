@@ -75,3 +75,34 @@ def test_set_wait_rejects_bad_arguments(moe):
             assert ei.value.status == moe.MOE_ERR_INVALID_ARG
     finally:
         moe.moe_destroy(h)
+
+
+def test_timeout_inside_a_multi_step_launch(moe):
+    """The same inside one persistent launch of several steps: every call's
+    barrier gives up in bounded time, the launch ends, the status reports it,
+    and afterwards the steps match single calls again."""
+    shape = synth.Shape("tiny steps L=2", 256, 256, 8, 2, layers=2, bias_sigma=0.02, seed=35)
+    layers = [synth.layer_tensors(shape, l) for l in range(2)]
+    h = create_handle(shape, layers=2, max_tokens=1)
+    try:
+        for l, t in enumerate(layers):
+            load_layer(h, l, t)
+        ins = [synth.step_inputs(shape, 20 + s, M=1, layers=1) for s in range(3)]
+        x = np.stack([a for a, _, _ in ins])
+        r = np.stack([b for _, b, _ in ins])
+        lg = np.ascontiguousarray(np.stack([c[0] for _, _, c in ins]))
+        moe.moe_debug_set_wait(h, 20000, 3)
+        t0 = time.perf_counter()
+        moe.moe_forward_steps(h, 3, 0, to_dev_bf16(x), torch.from_numpy(lg).cuda(), 1, 2, to_dev_bf16(r))
+        assert moe.moe_get_status(h) == moe.MOE_ERR_DEVICE_TIMEOUT
+        assert time.perf_counter() - t0 < 10.0
+        moe.moe_debug_set_wait(h, 0, -1)
+        od = to_dev_bf16(r)
+        moe.moe_forward_steps(h, 3, 0, to_dev_bf16(x), torch.from_numpy(lg).cuda(), 1, 2, od)
+        assert moe.moe_get_status(h) == moe.MOE_OK
+        got = dev_to_bits(od)
+        for s in range(3):
+            ref, _, _ = oracle_layer(shape, layers[s % 2], x[s], lg[s], r[s])
+            assert_parity(bf16_bits_to_f64(got[s]), ref, what=f"after the timeout, step {s}")
+    finally:
+        moe.moe_destroy(h)

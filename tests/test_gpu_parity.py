@@ -331,6 +331,88 @@ def test_forward_argument_errors(moe):
         moe.moe_destroy(h)
 
 
+# ------------------------------------------------------------------ steps
+
+@pytest.mark.parametrize("shape,L,n,layer0", [
+    (synth.Shape("tiny steps L=3", 256, 256, 8, 2, layers=3, bias_sigma=0.02, seed=31), 3, 7, 1),
+    (synth.Shape("ragged steps H=192 I=320 E=5 top-3", 192, 320, 5, 3, layers=2, bias_sigma=0.5, seed=32), 2, 5, 0),
+    (synth.Shape("int4 steps", 128, 64, 6, 2, fmt=synth.FMT_INT4, group=64, has_bias=False, layers=2, seed=33),
+     2, 3, 1),
+], ids=lambda v: getattr(v, "name", str(v)))
+@pytest.mark.parametrize("M", [1, 2, 4])
+def test_forward_steps_equal_single_calls(moe, shape, L, n, layer0, M):
+    """n decode steps in one call (the MXFP4 kernel runs them in one persistent
+    launch, layer (layer0 + s) mod L for step s, wrapping around) give the same
+    bits as n moe_forward calls, and match the oracle."""
+    layers = [synth.layer_tensors(shape, l) for l in range(L)]
+    h = create_handle(shape, layers=L)
+    try:
+        for l, t in enumerate(layers):
+            load_layer(h, l, t)
+        ins = [synth.step_inputs(shape, 200 + s, M=M, layers=1) for s in range(n)]
+        x = np.stack([a for a, _, _ in ins])
+        r = np.stack([b for _, b, _ in ins])
+        lg = np.stack([c[0] for _, _, c in ins])
+        xd, od = to_dev_bf16(x), to_dev_bf16(r)
+        ld = torch.from_numpy(np.ascontiguousarray(lg)).cuda()
+        moe.moe_forward_steps(h, n, layer0, xd, ld, M, shape.top_k, od)
+        torch.cuda.synchronize()
+        assert moe.moe_get_status(h) == 0
+        got = dev_to_bits(od)
+        for s in range(n):
+            single = _run_layer(moe, h, (layer0 + s) % L, x[s], r[s], lg[s], shape.top_k)
+            assert np.array_equal(bf16_bits_to_f64(got[s]), single), f"step {s}"
+            ref, _, _ = oracle_layer(shape, layers[(layer0 + s) % L], x[s], lg[s], r[s])
+            assert_parity(bf16_bits_to_f64(got[s]), ref, what=f"{shape.name} M={M} step {s}")
+    finally:
+        moe.moe_destroy(h)
+
+
+def test_forward_steps_full_size_match_single_calls(moe):
+    """The gpt-oss layer shape: 30 steps over 4 resident layers in one launch,
+    bit-identical to the single calls, with the algorithmic bytes of every step."""
+    shape = synth.Shape("gpt-oss steps", 2880, 2880, 32, 4, layers=4, e8m0_lo=117, e8m0_hi=124, seed=34)
+    L, n = 4, 30
+    h = create_handle(shape, layers=L, max_tokens=1)
+    try:
+        for l in range(L):
+            load_layer(h, l, synth.layer_tensors(shape, l))
+        ins = [synth.step_inputs(shape, 300 + s, M=1, layers=1) for s in range(n)]
+        x = np.stack([a for a, _, _ in ins])
+        r = np.stack([b for _, b, _ in ins])
+        lg = np.stack([c[0] for _, _, c in ins])
+        xd, od = to_dev_bf16(x), to_dev_bf16(r)
+        ld = torch.from_numpy(np.ascontiguousarray(lg)).cuda()
+        moe.moe_forward_steps(h, n, 0, xd, ld, 1, 4, od)
+        torch.cuda.synchronize()
+        assert moe.moe_get_status(h) == 0
+        got = dev_to_bits(od)
+        for s in range(n):
+            single = _run_layer(moe, h, s % L, x[s], r[s], lg[s], 4)
+            assert np.array_equal(bf16_bits_to_f64(got[s]), single), f"step {s}"
+        t = sparse_layer(shape, (n - 1) % L, oracle.route(lg[n - 1], 4)[0].ravel())
+        ref, _, _ = oracle_layer(shape, t, x[n - 1], lg[n - 1], r[n - 1])
+        assert_parity(bf16_bits_to_f64(got[n - 1]), ref, what="last step vs oracle")
+    finally:
+        moe.moe_destroy(h)
+
+
+def test_forward_steps_argument_errors(moe):
+    shape = synth.TINY
+    h = create_handle(shape)
+    try:
+        load_layer(h, 0, synth.layer_tensors(shape))
+        x, r, lg = synth.step_inputs(shape, 0, M=1, layers=1)
+        xd, od = to_dev_bf16(x), to_dev_bf16(r)
+        ld = torch.from_numpy(lg[0]).cuda()
+        for n, layer0 in [(0, 0), (1, 1), (1, -1)]:
+            with pytest.raises(moe.MoeError) as ei:
+                moe.moe_forward_steps(h, n, layer0, xd, ld, 1, shape.top_k, od)
+            assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+    finally:
+        moe.moe_destroy(h)
+
+
 # ------------------------------------------------------------------ stack
 
 def _run_stack(moe, h, r, logits, k):
