@@ -91,8 +91,10 @@ struct moe_handle {
     int last_bM = 0, last_bk = 0;             // M and top_k of the last batched call
     int* stats = nullptr;                     // distinct experts of the last call on each layer
     int* status = nullptr;
-    // staging for moe_forward_host: [x][residual / out][logits], on the device
-    // and in pinned host memory, so one copy each way moves a call's data
+    // staging for moe_forward_host: [x][residual / out][logits] in pinned host
+    // memory mapped into the device's address space (st_dev is its device
+    // address): the layer kernel reads the call's inputs from it and writes the
+    // result into it directly, over the host-device link
     uint8_t* st_dev = nullptr;
     uint8_t* st_host = nullptr;
     size_t st_off_r = 0, st_off_l = 0, st_bytes = 0;
@@ -167,7 +169,6 @@ void free_handle(moe_handle* h)
     cudaFree(h->b_y);
     cudaFree(h->stats);
     cudaFree(h->status);
-    cudaFree(h->st_dev);
     cudaFreeHost(h->st_host);
     delete h;
 }
@@ -525,16 +526,16 @@ int moe_create(const moe_config* cfg, moe_handle** out)
     h->st_bytes = h->st_off_l + Mx * E * sizeof(float);
     if ((rc = dev_alloc(&h->arena, h->layer_stride * c.num_layers, "expert weights")) ||
         (rc = dev_alloc(&h->stats, c.num_layers * sizeof(int), "stats")) ||
-        (rc = dev_alloc(&h->status, sizeof(int), "status")) ||
-        (rc = dev_alloc(&h->st_dev, h->st_bytes, "staging"))) {
+        (rc = dev_alloc(&h->status, sizeof(int), "status"))) {
         free_handle(h);
         return rc;
     }
-    if ((e = cudaHostAlloc((void**)&h->st_host, h->st_bytes, cudaHostAllocDefault)) != cudaSuccess) {
+    if ((e = cudaHostAlloc((void**)&h->st_host, h->st_bytes, cudaHostAllocMapped)) != cudaSuccess ||
+        (e = cudaHostGetDevicePointer((void**)&h->st_dev, h->st_host, 0)) != cudaSuccess) {
         cudaGetLastError();
-        h->st_host = nullptr;
         free_handle(h);
-        return fail(MOE_ERR_OOM, "cudaHostAlloc(%zu bytes) for the host staging failed", h->st_bytes);
+        return fail(MOE_ERR_OOM, "mapped pinned host staging (%zu bytes) failed: %s", h->st_bytes,
+                    cudaGetErrorString(e));
     }
     if ((e = cudaMemset(h->stats, 0, c.num_layers * sizeof(int))) != cudaSuccess ||
         (e = cudaMemset(h->status, 0, sizeof(int))) != cudaSuccess) {
@@ -680,24 +681,21 @@ int moe_forward_host(moe_handle* h, int layer, const void* x_bf16, const float* 
         return fail(MOE_ERR_NOT_LOADED, "moe_forward_host: layer %d has no experts loaded", layer);
     cudaStream_t s = (cudaStream_t)stream;
     const size_t nb = (size_t)M * h->cfg.hidden * 2, nl = (size_t)M * h->cfg.num_experts * 4;
-    // x, the residual and the logits packed into the handle's pinned staging
-    // buffer by the host, so that one copy moves them; one copy brings the
-    // result back (the pages' lesson on per-token host work: keep it to a
-    // fixed, small amount)
+    // x, the residual and the logits packed into the handle's mapped pinned
+    // buffer by the host; the layer kernel reads them from there and writes the
+    // result back there itself (no copy engine round trips: the pages' lesson
+    // on per-token host work, keep it to a fixed, small amount).  The previous
+    // call on this handle has completed (it synchronised before returning).
     std::memcpy(h->st_host, x_bf16, nb);
     std::memcpy(h->st_host + h->st_off_r, out_bf16, nb);
     std::memcpy(h->st_host + h->st_off_l, router_logits, nl);
-    cudaError_t e;
-    if ((e = cudaMemcpyAsync(h->st_dev, h->st_host, h->st_off_l + nl, cudaMemcpyHostToDevice, s)) != cudaSuccess)
-        return cuda_fail(e, "moe_forward_host upload");
     rc = moe_forward(h, layer, h->st_dev, reinterpret_cast<const float*>(h->st_dev + h->st_off_l), M, top_k,
                      h->st_dev + h->st_off_r, stream);
     if (rc != MOE_OK)
         return rc;
-    if ((e = cudaMemcpyAsync(h->st_host + h->st_off_r, h->st_dev + h->st_off_r, nb, cudaMemcpyDeviceToHost, s)) !=
-            cudaSuccess ||
-        (e = cudaStreamSynchronize(s)) != cudaSuccess)
-        return cuda_fail(e, "moe_forward_host download");
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "moe_forward_host");
     std::memcpy(out_bf16, h->st_host + h->st_off_r, nb);
     return MOE_OK;
 }

@@ -271,11 +271,16 @@ __device__ __forceinline__ unsigned long long count_target(unsigned long long ol
 {
     return (old / (unsigned long long)G + 1ull) * (unsigned long long)G;
 }
-// Grid barrier between calls (one thread of each CTA): arrive, then wait for
-// the count of this barrier to complete; gives up after `limit` polls.
-__device__ __forceinline__ void grid_sync(unsigned long long* cnt, int G, int limit, int* status)
+// Add without waiting for the old value (the arrival at a grid barrier whose
+// target is already known), with release semantics.
+__device__ __forceinline__ void red_add_release_u64(unsigned long long* p, unsigned long long v)
 {
-    const unsigned long long tgt = count_target(atom_add_release_u64(cnt, 1ull), G);
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+// Wait (one thread) until a grid counter reaches `tgt`; gives up after `limit`
+// polls and records a timeout.
+__device__ __forceinline__ void wait_count(const unsigned long long* cnt, unsigned long long tgt, int limit, int* status)
+{
     int spins = 0;
 #pragma unroll 1
     while (ld_acquire_u64(cnt) < tgt) {
@@ -570,6 +575,7 @@ struct TcSmem {
     unsigned long long ends[kSlots];      // producer: ring position after each stage in flight
     RoleState role[4];                    // producer, MMA issuer A, MMA issuer B, epilogue
     int gbase, ubase, npc;                // gate/up items, whole units and split-unit calls so far
+    unsigned long long dtgt, xtgt;        // targets of the last grid barrier and x-term count
 };
 
 // The launch's shared state: the stage ring (dynamic), the control block and a
@@ -688,28 +694,39 @@ __device__ __forceinline__ void decode_call(const int call)
         const int q = warp - 2, te = tid - 64;
         if (b < nitems) {
             int cm = -1;
-            float inv = 1.f, sx = 1.f;
+            float inv = 1.f, tmax = 0.f;
             uint4 rowv[kRowVec];
             for (int it = b + G * q; it < nitems; it += 4 * G) {
                 const int m = it / nblk, kb = it - m * nblk;
-                if (m != cm) {
-                    // the token's row once; its shift S from its largest |x| (for
-                    // x = bf16(r inv), the rounding is monotone, so that is bf16(max|r| inv))
-                    load_row((cl_x ? cl_x : cl_resid) + (size_t)m * p.H, p.H, lane, rowv);
+                const uint16_t* row = (cl_x ? cl_x : cl_resid) + (size_t)m * p.H;
+                if (!cl_x && m != cm) {
+                    // the normalised residual: the token's whole row for its rms (and
+                    // its largest |x|: the rounding is monotone, so bf16(max|r| inv))
+                    load_row(row, p.H, lane, rowv);
                     uint32_t ab;
-                    inv = row_stats(rowv, p.H, cl_x == nullptr, ab);
-                    float amax = bf16f((uint16_t)ab);
-                    if (!cl_x)
-                        amax = bf16f(f2bf16_rne(amax * inv));
-                    const int S = token_shift(amax);
-                    sx = __uint_as_float((uint32_t)(127 + S) << 23);
-                    if (lane == 0)   // every builder of token m writes the same 2^-S
-                        reinterpret_cast<float*>(p.xt + (long long)KSH * atom + CHH * kSfChunk)[m] =
-                            __uint_as_float((uint32_t)(127 - S) << 23);
+                    inv = row_stats(rowv, p.H, true, ab);
+                    tmax = bf16f(f2bf16_rne(bf16f((uint16_t)ab) * inv));
                     cm = m;
                 }
-                const uint16_t raw = row_elem(rowv, kb, lane);
-                const float v = (cl_x ? bf16f(raw) : bf16f(f2bf16_rne(bf16f(raw) * inv))) * sx;
+                const uint16_t raw = cl_x ? __ldcg(row + 32 * kb + lane) : row_elem(rowv, kb, lane);
+                float v = cl_x ? bf16f(raw) : bf16f(f2bf16_rne(bf16f(raw) * inv));
+                // the token's shift S: 0 when this block's largest |x| is at least
+                // 2^-98 (then so is the token's), else from the token's largest |x|
+                // (the whole row); every builder of token m finds the same S
+                int S = 0;
+                if (__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v))) < (29u << 23)) {
+                    if (cl_x) {
+                        uint32_t ab;
+                        load_row(row, p.H, lane, rowv);
+                        row_stats(rowv, p.H, false, ab);
+                        tmax = bf16f((uint16_t)ab);
+                    }
+                    S = token_shift(tmax);
+                }
+                if (lane == 0)   // 2^-S of token m
+                    reinterpret_cast<float*>(p.xt + (long long)KSH * atom + CHH * kSfChunk)[m] =
+                        __uint_as_float((uint32_t)(127 - S) << 23);
+                v *= __uint_as_float((uint32_t)(127 + S) << 23);
                 float r4[kMaxTokens] = {v, 0.f, 0.f, 0.f};
                 warp_terms_rows<1>(r4, m, kb, p.xt, p.xt + (long long)KSH * atom, atom, lane);
             }
@@ -719,9 +736,19 @@ __device__ __forceinline__ void decode_call(const int call)
             // publish this CTA's x terms (every CTA counts itself in), then wait for
             // the whole count and hand it to the producer through an mbarrier, so the
             // producer never waits on a load
-            const unsigned long long old = atom_add_release_u64(p.xcnt, 1ull);
-            const unsigned long long tgt = count_target(old, G);
-            sh.epoch = (unsigned)(old / (unsigned long long)G) + 1u;
+            // (the first call of the launch learns where the count stands; later
+            // calls add without waiting for the old value)
+            unsigned long long tgt;
+            if (call == 0) {
+                const unsigned long long old = atom_add_release_u64(p.xcnt, 1ull);
+                tgt = count_target(old, G);
+                sh.epoch = (unsigned)(old / (unsigned long long)G) + 1u;
+            } else {
+                red_add_release_u64(p.xcnt, 1ull);
+                tgt = sh.xtgt + (unsigned long long)G;
+                sh.epoch += 1u;
+            }
+            sh.xtgt = tgt;
             int spins = 0;
 #pragma unroll 1
             while (ld_acquire_u64(p.xcnt) < tgt) {
@@ -1241,8 +1268,15 @@ __device__ __forceinline__ void decode_call(const int call)
     __syncthreads();
     if (tid == 0) {
         // (a debug run may have one CTA skip its arrival, to test that the others give up)
-        const unsigned long long tgt =
-            count_target(b == p.skip_cta ? ld_acquire_u64(p.done) : atom_add_release_u64(p.done, 1ull), G);
+        unsigned long long tgt;
+        if (call == 0) {
+            tgt = count_target(b == p.skip_cta ? ld_acquire_u64(p.done) : atom_add_release_u64(p.done, 1ull), G);
+        } else {
+            if (b != p.skip_cta)
+                red_add_release_u64(p.done, 1ull);
+            tgt = sh.dtgt + (unsigned long long)G;
+        }
+        sh.dtgt = tgt;
         int spins = 0;
 #pragma unroll 1
         while (ld_acquire_u64(p.done) < tgt) {
@@ -1313,8 +1347,11 @@ __device__ __forceinline__ void decode_call(const int call)
             sh.npc = npc + pl.piece;
         }
         __syncthreads();
-        if (tid == 0)
-            grid_sync(p.done, G, p.spin_limit, p.status);
+        if (tid == 0) {
+            red_add_release_u64(p.done, 1ull);
+            sh.dtgt += (unsigned long long)G;
+            wait_count(p.done, sh.dtgt, p.spin_limit, p.status);
+        }
         __syncthreads();
     }
 #undef cl_gu

@@ -149,10 +149,11 @@ int moe_forward(moe_handle* h, int layer, const void* x_bf16, const float* route
                 int M, int top_k, void* out_bf16, void* stream);
 
 /* The same layer with host buffers (any host memory, pinned or not): packs x,
- * the residual and the logits into the handle's pinned staging buffer, moves
- * them with one host-to-device copy, runs moe_forward on `stream`, moves the
- * result back with one device-to-host copy, synchronises the stream and copies
- * the result into out_bf16.  Argument checks as for moe_forward. */
+ * the residual and the logits into the handle's pinned staging buffer, which
+ * is mapped into the device's address space; the layer kernel reads its
+ * inputs from it and writes its result into it directly over the host-device
+ * link (no separate copies).  Synchronises `stream`, then copies the result
+ * into out_bf16.  Argument checks as for moe_forward. */
 int moe_forward_host(moe_handle* h, int layer, const void* x_bf16, const float* router_logits,
                      int M, int top_k, void* out_bf16, void* stream);
 
