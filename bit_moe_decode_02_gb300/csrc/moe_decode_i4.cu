@@ -52,7 +52,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kCw = 8;                     // compute warps
+constexpr int kCw = 16;                    // compute warps (4 per SM sub-partition)
 constexpr int kThreadsI4 = (kCw + 1) * 32; // + the producer warp
 constexpr int kProdWarp = kCw;
 constexpr int kGuSeg = 4;                  // segments per gate/up stage
@@ -71,14 +71,17 @@ __device__ __forceinline__ __half2 u2h(uint32_t u)
 }
 
 // The four f16x2 A registers of one m16n8k16 MMA from one code word: register
-// i holds nibbles i and i + 4, each q - 8 = (1024 + q) - 1032 exactly.
+// i holds nibbles i and i + 4.  A nibble q placed in the low bits of an f16
+// 0x6400 is 1024 + q, and q - 8 = (1024 + q) - 1032; placed 4 bits up it is
+// 1024 + 16 q, and q - 8 = (1024 + 16 q) / 16 - 72 (one fma).  All exact.
 __device__ __forceinline__ void decode_i4(uint32_t w, uint32_t (&a)[4])
 {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t t = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
-        a[i] = h2u(__hsub2(u2h(t), u2h(0x64086408u)));
-    }
+    const uint32_t w8 = w >> 8;
+    const __half2 k1032 = u2h(0x64086408u), k16 = u2h(0x2C002C00u), k72 = u2h(0xD480D480u);
+    a[0] = h2u(__hsub2(u2h((w & 0x000F000Fu) | 0x64006400u), k1032));
+    a[1] = h2u(__hfma2(u2h((w & 0x00F000F0u) | 0x64006400u), k16, k72));
+    a[2] = h2u(__hsub2(u2h((w8 & 0x000F000Fu) | 0x64006400u), k1032));
+    a[3] = h2u(__hfma2(u2h((w8 & 0x00F000F0u) | 0x64006400u), k16, k72));
 }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
@@ -149,11 +152,12 @@ struct I4Smem {
     uint32_t stages;                      // stages streamed so far (producer) / consumed (compute)
 };
 
-// Shared memory past the ring: x as f16 [M][H + 8], the unit's gate/up sums
-// [128][4], h' as f16 hi and lo [2][4][64], the CTA's output copy [H][V].
+// Shared memory past the ring: x as f16 [M][H + 8], the unit's gate/up sums of
+// both K halves [2][128][4], h' as f16 hi and lo [2][4][64], the CTA's output
+// copy [H][V].
 __device__ __forceinline__ uint32_t i4_tail_bytes(int H, int M)
 {
-    return (uint32_t)M * (H + 8) * 2 + 128 * 4 * 4 + 2 * 4 * 64 * 2 + (uint32_t)H * 4 * 4;
+    return (uint32_t)M * (H + 8) * 2 + 2 * 128 * 4 * 4 + 2 * 4 * 64 * 2 + (uint32_t)H * 4 * 4;
 }
 __device__ __forceinline__ int sb_of(int group) { return group == 32 ? 8 : 4; }
 
@@ -174,8 +178,8 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
     const int nslots = min(kMaxSlotsI4, (int)(((uint32_t)p.smem_bytes - tail) / kI4Slot));
     uint8_t* tailp = i4ring + (uint32_t)nslots * kI4Slot;
     __half* xh = reinterpret_cast<__half*>(tailp);                                       // [M][H + 8]
-    float* gsum = reinterpret_cast<float*>(tailp + (uint32_t)M * (H + 8) * 2);           // [128][4]
-    __half* hs16 = reinterpret_cast<__half*>(gsum + 128 * 4);                             // [2][4][64]
+    float* gsum = reinterpret_cast<float*>(tailp + (uint32_t)M * (H + 8) * 2);           // [2][128][4]
+    __half* hs16 = reinterpret_cast<__half*>(gsum + 2 * 128 * 4);                         // [2][4][64]
     float* oacc = reinterpret_cast<float*>(hs16 + 2 * 4 * 64);                            // [H][V]
 
     if (tid == 0) {
@@ -363,7 +367,9 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
             // ================================================================ compute warps
             for (int u = u0; u < u1; ++u) {
                 const int s = u / T1, t = u % T1, e = si.unit_expert[s];
-                // ---- gate / up: warp w = slab w (rows: gate 64t + 16w, or up 64t + 16(w - 4))
+                // ---- gate / up: warp w takes slab w & 7 (rows: gate 64t + 16 (w & 7), or up
+                // 64t + 16 ((w & 7) - 4)) and the even (w < 8) or odd segments of each stage
+                const int slab = warp & 7, half = warp >> 3;
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
                 const int ngu = (KS + kGuSeg - 1) / kGuSeg;
                 for (int st = 0; st < ngu; ++st, ++st_count) {
@@ -371,10 +377,10 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                     mbar_wait(&si.full[slot], (st_count / nslots) & 1, p.status);
                     const uint8_t* sp = i4ring + slot * kI4Slot;
                     const int q0 = st * kGuSeg, n = min(kGuSeg, KS - q0);
-                    for (int qi = 0; qi < n; ++qi) {
+                    for (int qi = half; qi < n; qi += 2) {
                         const int q = q0 + qi;
-                        const uint4 cw = *reinterpret_cast<const uint4*>(sp + qi * 4096 + warp * 512 + lane * 16);
-                        const uint8_t* ent = sp + kI4Codes + (qi * 8 + warp) * 8 * SB + g * SB;
+                        const uint4 cw = *reinterpret_cast<const uint4*>(sp + qi * 4096 + slab * 512 + lane * 16);
+                        const uint8_t* ent = sp + kI4Codes + (qi * 8 + slab) * 8 * SB + g * SB;
                         float sg0, sh0, sg1, sh1;
                         {
                             const uint32_t e0 = *reinterpret_cast<const uint32_t*>(ent);
@@ -420,23 +426,27 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                     if (lane == 0)
                         mbar_arrive(&si.empty[slot]);
                 }
-                // rows 16 w + g and + 8 of the unit's 128 (gate 0..63, up 64..127), tokens 2 t4, 2 t4 + 1
+                // rows 16 slab + g and + 8 of the unit's 128 (gate 0..63, up 64..127), tokens
+                // 2 t4, 2 t4 + 1, for this warp's K half
                 if (t4 < 2) {
-                    gsum[(16 * warp + g) * 4 + 2 * t4] = acc[0];
-                    gsum[(16 * warp + g) * 4 + 2 * t4 + 1] = acc[1];
-                    gsum[(16 * warp + g + 8) * 4 + 2 * t4] = acc[2];
-                    gsum[(16 * warp + g + 8) * 4 + 2 * t4 + 1] = acc[3];
+                    float* gs = gsum + half * 128 * 4;
+                    gs[(16 * slab + g) * 4 + 2 * t4] = acc[0];
+                    gs[(16 * slab + g) * 4 + 2 * t4 + 1] = acc[1];
+                    gs[(16 * slab + g + 8) * 4 + 2 * t4] = acc[2];
+                    gs[(16 * slab + g + 8) * 4 + 2 * t4 + 1] = acc[3];
                 }
                 cw_barrier();
-                // ---- SwiGLU: thread (row r = tid / 4, token m = tid % 4), h' = w h
+                // ---- SwiGLU: thread (row r = tid / 4, token m = tid % 4) of the first 256,
+                // h' = w h; the two K halves added in a fixed order
                 const int hb = (ubase + u - u0) & 1;
                 float hv = 0.f;
-                {
+                if (tid < 256) {
                     const int r = tid >> 2, m = tid & 3;
                     if (m < M) {
                         const float wt = si.wslot[s][m];
                         const float xs = pow2_mul(1.f, -si.xsh[m]);
-                        float gg = gsum[r * 4 + m] * xs, uu = gsum[(64 + r) * 4 + m] * xs;
+                        float gg = (gsum[r * 4 + m] + gsum[128 * 4 + r * 4 + m]) * xs;
+                        float uu = (gsum[(64 + r) * 4 + m] + gsum[128 * 4 + (64 + r) * 4 + m]) * xs;
                         if (gub) {
                             gg += bf16f(__ldg(gub + (size_t)e * 2 * I + 64 * t + r));
                             uu += bf16f(__ldg(gub + (size_t)e * 2 * I + I + 64 * t + r));
@@ -451,7 +461,7 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                         atomicMax(&si.hmax[hb][lane], mx);
                 }
                 cw_barrier();
-                {
+                if (tid < 256) {
                     const int r = tid >> 2, m = tid & 3;
                     const float hm = __uint_as_float(si.hmax[hb][m]);
                     const int sh = hm > 0.f ? 14 - ilog2f(hm) : 0;

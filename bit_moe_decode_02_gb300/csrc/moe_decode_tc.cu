@@ -849,12 +849,26 @@ __device__ __forceinline__ void decode_call(const int call)
                 const int tA = piece ? pl.ta : 0, tB = piece ? pl.tb : T2;
                 const uint8_t* d0 = cl_dn + (long long)e * p.dn_expert;
                 const uint8_t* sd0 = d0 + (long long)p.H * (p.I / 2) + (long long)(t >> 1) * kSfChunk;
+                const void* map_c = p.dn_maps ? static_cast<const uint8_t*>(p.dn_maps) + (size_t)layer * 256 : nullptr;
                 for (int ga = tA; ga < tB; ga += TG) {
                     const int gb = ga + TG < tB ? ga + TG : tB;
                     for (int t2 = ga; t2 < gb; t2 += kDnStageTiles, ++sc) {
                         const int n = gb - t2 < kDnStageTiles ? gb - t2 : kDnStageTiles;
                         uint32_t off;
                         const uint32_t slot = claim(dn_stage_size(n), off);
+                        if (map_c && n == kDnStageTiles && t2 + n <= p.t2full) {
+                            // four full tiles: k-step t of each (4 KB) and their scale chunks,
+                            // one tensor copy each, in the same shared layout as below
+                            if (lane == 0) {
+                                uint8_t* st = ring + off;
+                                mbar_expect_tx(&sh.full[slot], (uint32_t)n * (kTileA + kSfChunk));
+                                tma_load_4d(st, map_c, 0, 2 * t, t2, e, &sh.full[slot], wpol);
+                                tma_load_4d(st + n * kTileA, static_cast<const uint8_t*>(map_c) + 128, 0, t >> 1, t2, e,
+                                            &sh.full[slot], wpol);
+                            }
+                            __syncwarp();
+                            continue;
+                        }
                         uint32_t bytes = 0;
 #pragma unroll 1
                         for (int j = 0; j < n; ++j) {
@@ -1339,6 +1353,12 @@ __device__ __forceinline__ void decode_call(const int call)
     // call reads its routing and inputs only after every CTA's slice of this
     // output is written
     if (call + 1 < p.ncalls) {
+        if (ri == 0) {
+            // every stage of this call has been consumed (its MMAs completed before
+            // the epilogue's last drain): the producer need not poll their releases
+            st.rel = st.sc;
+            st.rel_end = st.rs.head;
+        }
         if ((ri == 0 && lane == 0) || ((ri == 1 || ri == 2) && lane == 0) || (ri == 3 && tid == 64))
             sh.role[ri] = st;
         if (tid == 0) {

@@ -130,6 +130,11 @@ struct DecodeTcParams {
     float* out_f32;             // [M][H] fp32 result before the bf16 rounding per call, or nullptr
     long long logits_stride, x_stride, resid_stride, out_f32_stride;
     int ncalls, layer0, nlayers;
+    // Tensor maps of the down projections, two per layer (codes, then scale
+    // chunks; 128 bytes each, in global memory), or nullptr: with them a down
+    // stage of 4 full 128-row tiles is two tensor copies instead of eight
+    const void* dn_maps;
+    int t2full;                 // full 128-row tiles of the down projection (H / 128)
     float* part;                // [G][H][4] each CTA's fp32 copy of the expert output
     uint8_t* xt;                // x terms of the layer: [H/64][N rows x 32 B][ceil(H/128)][512]
     float* gpart;               // [G][128][4] gate/up partial sums of split-unit pieces
