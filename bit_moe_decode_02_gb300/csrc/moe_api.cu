@@ -13,7 +13,6 @@
 // MXFP4 experts are in the 128-row tile layout of the tensor-core kernels,
 // int4 experts in the 64-row unit layout of the int4 kernel (each described
 // with its kernel); both hold exactly the caller's bytes, reordered.
-#include <cuda.h>   // tensor-map types only: the encoder is looked up through the runtime
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -76,7 +75,6 @@ struct moe_handle {
     unsigned long long* cnt = nullptr;        // xcnt, done (only grow)
     // MXFP4 decode: tensor maps of the down projections ([L][2], 128 bytes each),
     // split-unit partials and flags, the layer's x terms
-    uint8_t* dn_maps = nullptr;
     float* gpart = nullptr;
     unsigned* pflag = nullptr;
     uint8_t* xt = nullptr;
@@ -159,7 +157,6 @@ void free_handle(moe_handle* h)
     cudaFree(h->arena);
     cudaFree(h->part);
     cudaFree(h->cnt);
-    cudaFree(h->dn_maps);
     cudaFree(h->gpart);
     cudaFree(h->pflag);
     cudaFree(h->xt);
@@ -212,8 +209,6 @@ moe::DecodeTcParams tc_params(const moe_handle* h, int layer0, int ncalls)
     p.ncalls = ncalls;
     p.layer0 = layer0;
     p.nlayers = c.num_layers;
-    p.dn_maps = h->dn_maps;
-    p.t2full = c.hidden / moe::kRowTile;
     p.part = h->part;
     p.gpart = h->gpart;
     p.pflag = h->pflag;
@@ -302,57 +297,6 @@ cudaError_t launch_decode(const moe_handle* h, int layer, const float* logits, c
     return launch_seq(h, layer, 1, logits, 0, x, 0, resid, 0, out_f32, 0, M, k, s);
 }
 
-// Tensor maps of every layer's down projections (MXFP4 tile layout), so that a
-// decode down stage of four full 128-row tiles is one tensor copy for their
-// codes and one for their scale chunks.  Codes: 8-byte elements, dims (256
-// elements = 2 KB, half-k-steps of a tile, full tiles, experts), box (256, 2,
-// 4, 1) = k-step t of 4 tiles; scales: dims (64 elements = one 512-byte chunk,
-// chunks of a tile, tiles, experts), box (64, 1, 4, 1).  Skipped (dn_maps stays
-// NULL: plain bulk copies) when there are fewer than 4 full tiles.
-int encode_dn_maps(moe_handle* h)
-{
-    const moe_config& c = h->cfg;
-    const int H = c.hidden, I = c.intermediate, E = c.num_experts, L = c.num_layers;
-    const int T2full = H / moe::kRowTile, T2 = moe::ceil_div(H, moe::kRowTile), CH = moe::ceil_div(I, moe::kRowTile);
-    if (T2full < 4)
-        return MOE_OK;
-    typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess || !fn || q != cudaDriverEntryPointSuccess)
-        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    EncodeFn encode = reinterpret_cast<EncodeFn>(fn);
-    std::vector<CUtensorMap> maps((size_t)2 * L);
-    for (int l = 0; l < L; ++l) {
-        uint8_t* dn = h->arena + (size_t)l * h->layer_stride + h->off_dn;
-        const cuuint64_t cdim[4] = {256, (cuuint64_t)I / 32, (cuuint64_t)T2full, (cuuint64_t)E};
-        const cuuint64_t cstr[3] = {2048, (cuuint64_t)64 * I, (cuuint64_t)h->dn_expert};
-        const cuuint32_t cbox[4] = {256, 2, 4, 1}, one[4] = {1, 1, 1, 1};
-        CUresult r = encode(&maps[2 * l], CU_TENSOR_MAP_DATA_TYPE_INT64, 4, dn, cdim, cstr, cbox, one,
-                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        const cuuint64_t sdim[4] = {64, (cuuint64_t)CH, (cuuint64_t)T2, (cuuint64_t)E};
-        const cuuint64_t sstr[3] = {(cuuint64_t)moe::kSfChunk, (cuuint64_t)CH * moe::kSfChunk, (cuuint64_t)h->dn_expert};
-        const cuuint32_t sbox[4] = {64, 1, 4, 1};
-        if (r == CUDA_SUCCESS)
-            r = encode(&maps[2 * l + 1], CU_TENSOR_MAP_DATA_TYPE_INT64, 4, dn + (size_t)H * (I / 2), sdim, sstr, sbox,
-                       one, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS)
-            return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for layer %d", (int)r, l);
-    }
-    int rc = dev_alloc(&h->dn_maps, maps.size() * sizeof(CUtensorMap), "tensor maps");
-    if (rc != MOE_OK)
-        return rc;
-    if ((e = cudaMemcpy(h->dn_maps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice)) !=
-        cudaSuccess)
-        return cuda_fail(e, "tensor maps");
-    return MOE_OK;
-}
-
 // Decode workspace and kernel set-up (both formats).
 int create_decode(moe_handle* h)
 {
@@ -382,8 +326,6 @@ int create_decode(moe_handle* h)
         h->dec_smem = (size_t)optin - moe::decode_tc_static_smem();
         if ((e = moe::prepare_decode_tc(h->dec_smem)) != cudaSuccess)
             return cuda_fail(e, "tensor-core decode kernel set-up");
-        if ((rc = encode_dn_maps(h)) != MOE_OK)
-            return rc;
     } else {
         h->dec_smem = (size_t)optin - moe::decode_i4_static_smem();
         // the int4 kernel's tail (x as f16, sums, h', the output copy) and at least two stages
@@ -678,9 +620,9 @@ int moe_load_experts(moe_handle* h, int layer, const void* gu_codes, const void*
     }
     if (h->mxfp4) {
         // gate rows [0, I) and up rows [I, 2I) interleaved per 64 in 128-row tiles
-        if ((e = moe::launch_repack_tiles(st_guc, st_gus, E, 2 * I, 2 * I, H, I, base, (long long)h->gu_expert, s)) ==
+        if ((e = moe::launch_repack_tiles(st_guc, st_gus, E, 2 * I, 2 * I, H, I, 0, base, (long long)h->gu_expert, s)) ==
             cudaSuccess)
-            e = moe::launch_repack_tiles(st_dnc, st_dns, E, H, H, I, 0, base + h->off_dn, (long long)h->dn_expert, s);
+            e = moe::launch_repack_tiles(st_dnc, st_dns, E, H, H, I, 0, 1, base + h->off_dn, (long long)h->dn_expert, s);
     } else {
         if ((e = moe::launch_repack_i4(st_guc, reinterpret_cast<const uint16_t*>(st_gus), E, H, I, c.group, 0, base,
                                        (long long)h->gu_expert, s)) == cudaSuccess)
@@ -913,7 +855,7 @@ int moe_debug_dequant(moe_handle* h, int layer, int expert, int proj, float* out
     const uint8_t* base = h->arena + (size_t)layer * h->layer_stride;
     const uint8_t* src = proj == 0 ? base + (size_t)expert * h->gu_expert
                                    : base + h->off_dn + (size_t)expert * h->dn_expert;
-    cudaError_t e = h->mxfp4 ? moe::launch_dequant_tiles(src, N, K, proj == 0 ? c.intermediate : 0, out_dev,
+    cudaError_t e = h->mxfp4 ? moe::launch_dequant_tiles(src, N, K, proj == 0 ? c.intermediate : 0, proj, out_dev,
                                                          (cudaStream_t)stream)
                              : moe::launch_dequant_i4(src, c.hidden, c.intermediate, c.group, proj, out_dev,
                                                       (cudaStream_t)stream);

@@ -263,6 +263,7 @@ __global__ void untile_h_kernel(BatchParams p, uint8_t* codes, uint8_t* scales)
 struct GemmParams {
     const uint8_t* w;       // tile-layout weights; expert e at + e * w_expert (DUAL: interleaved gate_up)
     long long w_expert;
+    int kmajor;             // the weights are in the k-step-major tile order (the down projection)
     int rows, K;            // output rows (DUAL: rows of h, the projection has 2 * rows), reduction length
     const uint8_t* bq;      // activation codes (tile order)
     const uint8_t* bsf;     // activation scale chunks
@@ -389,9 +390,7 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(GemmParams p)
             const int wn = w + gridDim.x;
             const TokTile next = wn < items ? p.tiles[wn / T] : tile;
             const int R = prow - t * kRowTile < kRowTile ? prow - t * kRowTile : kRowTile;
-            const uint8_t* a0 = p.w + tile.e * p.w_expert + (long long)t * kRowTile * (p.K / 2);
-            const uint8_t* s0 = p.w + tile.e * p.w_expert + (long long)prow * (p.K / 2) +
-                                (long long)t * CH * kSfChunk;
+            const uint8_t* we = p.w + tile.e * p.w_expert;
             const uint8_t* b0 = p.bq + tile.boff * KS;
             const uint8_t* sb0 = p.bsf + (long long)tt * CH * kSfChunk;
             for (int j = 0; j < NSTG; ++j, ++c) {
@@ -411,18 +410,35 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(GemmParams p)
                 if (lane == 0)
                     mbar_expect_tx(&full[slot], sg.abytes + sg.sfbytes + sg.bbytes + sg.sfbytes);
                 __syncwarp();
-                const long long aoff = (long long)j * kStageSteps * R * 32;
                 const long long soff = (long long)j * (kStageSteps / 2) * kSfChunk;
+                const int s0 = j * kStageSteps, ch0 = j * (kStageSteps / 2);
                 uint8_t* st = smem + off;
                 uint8_t* dst = nullptr;
                 const uint8_t* src = nullptr;
                 uint32_t n = 0;
-                switch (lane) {
-                case 0: dst = st; src = a0 + aoff; n = sg.abytes; break;
-                case 1: dst = st + sg.sfa0(); src = s0 + soff; n = sg.sfbytes; break;
-                case 2: dst = st + sg.b(); src = b0 + (long long)j * kStageSteps * tile.npad * 32; n = sg.bbytes; break;
-                case 3: dst = st + sg.sfb(); src = sb0 + soff; n = sg.sfbytes; break;
-                default: break;
+                if (!p.kmajor) {
+                    // row-tile-major: the stage's k-steps and scale chunks are two runs
+                    switch (lane) {
+                    case 0: dst = st; src = we + tile_block_off(prow, p.K, t, s0, 0); n = sg.abytes; break;
+                    case 1: dst = st + sg.sfa0(); src = we + tile_sf_off(prow, p.K, t, ch0, 0); n = sg.sfbytes; break;
+                    default: break;
+                    }
+                } else if (lane < steps) {
+                    // k-step-major: one block per k-step (lanes 0..7), one chunk per
+                    // column chunk (lanes 8..11)
+                    dst = st + lane * R * 32;
+                    src = we + tile_block_off(prow, p.K, t, s0 + lane, 1);
+                    n = (uint32_t)R * 32;
+                } else if (lane >= kStageSteps && lane < kStageSteps + (steps + 1) / 2) {
+                    const int c = lane - kStageSteps;
+                    dst = st + sg.sfa0() + c * kSfChunk;
+                    src = we + tile_sf_off(prow, p.K, t, ch0 + c, 1);
+                    n = kSfChunk;
+                }
+                if (lane == 16) {
+                    dst = st + sg.b(); src = b0 + (long long)j * kStageSteps * tile.npad * 32; n = sg.bbytes;
+                } else if (lane == 17) {
+                    dst = st + sg.sfb(); src = sb0 + soff; n = sg.sfbytes;
                 }
                 if (n)
                     bulk_copy(dst, src, n, &full[slot]);
@@ -624,7 +640,7 @@ __device__ __forceinline__ int src_row(int n, int ilv)
 // [src_rows][K/2] code matrix).  Work item g < E*N*K/32 moves one 16-byte run
 // of codes; g beyond that writes one scale byte.
 __global__ void repack_tiles_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
-                                    int E, int src_rows, int N, int K, int ilv, uint8_t* out,
+                                    int E, int src_rows, int N, int K, int ilv, int kmajor, uint8_t* out,
                                     long long expert_bytes)
 {
     const int c16 = K / 32;                       // 16-byte runs per row
@@ -638,11 +654,10 @@ __global__ void repack_tiles_kernel(const uint8_t* __restrict__ codes, const uin
             const long long rem = g % ((long long)N * c16);
             const int n = (int)(rem / c16), c = (int)(rem % c16);
             const int t = n / kRowTile, r = n % kRowTile;
-            const int R = N - t * kRowTile < kRowTile ? N - t * kRowTile : kRowTile;
             const uint4 v = *reinterpret_cast<const uint4*>(
                 codes + ((size_t)e * src_rows + src_row(n, ilv)) * (K / 2) + 16 * c);
-            const long long dst = (long long)e * expert_bytes + (long long)t * kRowTile * (K / 2) +
-                                  (long long)(c >> 1) * R * 32 + (r >> 3) * 256 + (c & 1) * 128 + (r & 7) * 16;
+            const long long dst = (long long)e * expert_bytes + tile_block_off(N, K, t, c >> 1, kmajor) +
+                                  (r >> 3) * 256 + (c & 1) * 128 + (r & 7) * 16;
             *reinterpret_cast<uint4*>(out + dst) = v;
         } else {
             const long long h = g - ncode;
@@ -655,7 +670,7 @@ __global__ void repack_tiles_kernel(const uint8_t* __restrict__ codes, const uin
             uint8_t v = 0;
             if (n < N && blk < K / 32)
                 v = scales[((size_t)e * src_rows + src_row(n, ilv)) * (K / 32) + blk];
-            out[(long long)e * expert_bytes + (long long)N * (K / 2) + rem] = v;
+            out[(long long)e * expert_bytes + tile_sf_off(N, K, t, ch, kmajor) + b] = v;
         }
     }
 }
@@ -664,10 +679,9 @@ __global__ void repack_tiles_kernel(const uint8_t* __restrict__ codes, const uin
 // tile layout the tensor-core kernels stream: its E2M1 code times its E8M0
 // scale 2^(s - 127), in fp32 (exact; byte 0 gives 2^-127, byte 255 NaN, and a
 // product past the fp32 range overflows to infinity).
-__global__ void dequant_tiles_kernel(const uint8_t* __restrict__ tiles, int N, int K, int ilv,
+__global__ void dequant_tiles_kernel(const uint8_t* __restrict__ tiles, int N, int K, int ilv, int kmajor,
                                      float* __restrict__ out)
 {
-    const int CH = ceil_div(K, 128);
     const long long total = (long long)N * K;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {
@@ -678,14 +692,12 @@ __global__ void dequant_tiles_kernel(const uint8_t* __restrict__ tiles, int N, i
             n = (rr / 64) * kRowTile + (up ? 64 : 0) + rr % 64;
         }
         const int t = n / kRowTile, r = n % kRowTile;
-        const int R = N - t * kRowTile < kRowTile ? N - t * kRowTile : kRowTile;
         const int s = k / 64, b = (k % 64) / 2;
-        const uint8_t byte = tiles[(long long)t * kRowTile * (K / 2) + (long long)s * R * 32 + (r >> 3) * 256 +
-                                   (b >> 4) * 128 + (r & 7) * 16 + (b & 15)];
+        const uint8_t byte = tiles[tile_block_off(N, K, t, s, kmajor) + (r >> 3) * 256 + (b >> 4) * 128 +
+                                   (r & 7) * 16 + (b & 15)];
         const uint32_t code = (k & 1) ? byte >> 4 : byte & 0xfu;
         const int blk = k / 32;
-        const uint32_t sbyte = tiles[(long long)N * (K / 2) + (long long)(t * CH + blk / 4) * kSfChunk +
-                                     (r & 31) * 16 + (r >> 5) * 4 + (blk & 3)];
+        const uint32_t sbyte = tiles[tile_sf_off(N, K, t, blk / 4, kmajor) + (r & 31) * 16 + (r >> 5) * 4 + (blk & 3)];
         const float mag[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
         const float v = (code & 8u) ? -mag[code & 7u] : mag[code & 7u];
         const float sc = __uint_as_float(sbyte == 0u ? 0x00400000u : (sbyte == 255u ? 0x7fc00000u : sbyte << 23));
@@ -739,6 +751,7 @@ cudaError_t launch_batched(const BatchParams& p, int grid, cudaStream_t s, int* 
     GemmParams g{};
     g.w = p.gu;
     g.w_expert = p.gu_expert;
+    g.kmajor = 0;
     g.rows = p.I;
     g.K = p.H;
     g.bq = p.xq;
@@ -754,6 +767,7 @@ cudaError_t launch_batched(const BatchParams& p, int grid, cudaStream_t s, int* 
         return e;
     g.w = p.dn;
     g.w_expert = p.dn_expert;
+    g.kmajor = 1;
     g.rows = p.H;
     g.K = p.I;
     g.bq = p.hq;
@@ -769,14 +783,14 @@ cudaError_t launch_batched(const BatchParams& p, int grid, cudaStream_t s, int* 
 }
 
 cudaError_t launch_repack_tiles(const uint8_t* codes, const uint8_t* scales, int E, int src_rows,
-                                int N, int K, int interleave, uint8_t* out, long long expert_bytes,
+                                int N, int K, int interleave, int kmajor, uint8_t* out, long long expert_bytes,
                                 cudaStream_t stream)
 {
     const long long work = (long long)E * N * (K / 32) +
                            (long long)E * ceil_div(N, kRowTile) * ceil_div(K, 128) * kSfChunk;
     const long long blocks = (work + 255) / 256 < 65536 ? (work + 255) / 256 : 65536;
-    repack_tiles_kernel<<<(unsigned)blocks, 256, 0, stream>>>(codes, scales, E, src_rows, N, K, interleave, out,
-                                                              expert_bytes);
+    repack_tiles_kernel<<<(unsigned)blocks, 256, 0, stream>>>(codes, scales, E, src_rows, N, K, interleave, kmajor,
+                                                              out, expert_bytes);
     return cudaGetLastError();
 }
 
@@ -788,11 +802,11 @@ cudaError_t launch_route(const float* logits, int M, int E, int k, int* idx, flo
     return cudaGetLastError();
 }
 
-cudaError_t launch_dequant_tiles(const uint8_t* tiles, int N, int K, int interleave, float* out,
+cudaError_t launch_dequant_tiles(const uint8_t* tiles, int N, int K, int interleave, int kmajor, float* out,
                                  cudaStream_t stream)
 {
     const long long total = (long long)N * K;
-    dequant_tiles_kernel<<<blocks_for(total, 256), 256, 0, stream>>>(tiles, N, K, interleave, out);
+    dequant_tiles_kernel<<<blocks_for(total, 256), 256, 0, stream>>>(tiles, N, K, interleave, kmajor, out);
     return cudaGetLastError();
 }
 

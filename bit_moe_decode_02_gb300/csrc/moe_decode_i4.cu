@@ -581,13 +581,24 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
         {
             const float4* part = reinterpret_cast<const float4*>(p.part);
             for (int j = warp; j < nf; j += kThreadsI4 / 32) {
+                // lane l takes CTAs l, l + 32, ... (all its loads in flight at once),
+                // then a fixed shuffle tree: the order never depends on timing
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int c0 = lane; c0 < G; c0 += 32) {
-                    const bool has = (long long)(c0 + 1) * U / G > (long long)c0 * U / G;
-                    if (has) {
-                        const float4 a = __ldcg(part + (size_t)c0 * U4 + f0 + j);
-                        acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
+                for (int c0 = lane; c0 < G; c0 += 8 * 32) {
+                    float4 a[8];
+                    bool has[8];
+#pragma unroll
+                    for (int z = 0; z < 8; ++z) {
+                        const int c = c0 + 32 * z;
+                        has[z] = c < G && (long long)(c + 1) * U / G > (long long)c * U / G;
+                        if (has[z])
+                            a[z] = __ldcg(part + (size_t)c * U4 + f0 + j);
                     }
+#pragma unroll
+                    for (int z = 0; z < 8; ++z)
+                        if (has[z]) {
+                            acc.x += a[z].x; acc.y += a[z].y; acc.z += a[z].z; acc.w += a[z].w;
+                        }
                 }
 #pragma unroll
                 for (int off = 16; off >= 1; off >>= 1) {

@@ -845,52 +845,30 @@ __device__ __forceinline__ void decode_call(const int call)
                         bulk_copy_hint(st + sg.sfa, s0 + (ks >> 1) * kSfChunk, sg.sfbytes, &sh.full[slot], wpol);
                 }
             } else {
-                // down rows of tiles [tA, tB), k-step t of K = I (h rows 64t .. 64t+63)
+                // down rows of tiles [tA, tB), k-step t of K = I (h rows 64t .. 64t+63):
+                // in the k-step-major order the tiles of a stage are one run of
+                // codes and one run of scale chunks
                 const int tA = piece ? pl.ta : 0, tB = piece ? pl.tb : T2;
-                const uint8_t* d0 = cl_dn + (long long)e * p.dn_expert;
-                const uint8_t* sd0 = d0 + (long long)p.H * (p.I / 2) + (long long)(t >> 1) * kSfChunk;
-                const void* map_c = p.dn_maps ? static_cast<const uint8_t*>(p.dn_maps) + (size_t)layer * 256 : nullptr;
+                const uint8_t* c0 = cl_dn + (long long)e * p.dn_expert + (long long)t * p.H * 32;
+                const uint8_t* sc0 = cl_dn + (long long)e * p.dn_expert + (long long)p.H * (p.I / 2) +
+                                     (long long)(t >> 1) * T2 * kSfChunk;
                 for (int ga = tA; ga < tB; ga += TG) {
                     const int gb = ga + TG < tB ? ga + TG : tB;
                     for (int t2 = ga; t2 < gb; t2 += kDnStageTiles, ++sc) {
                         const int n = gb - t2 < kDnStageTiles ? gb - t2 : kDnStageTiles;
+                        const int rows = p.H - t2 * kRowTile < n * kRowTile ? p.H - t2 * kRowTile : n * kRowTile;
                         uint32_t off;
                         const uint32_t slot = claim(dn_stage_size(n), off);
-                        if (map_c && n == kDnStageTiles && t2 + n <= p.t2full) {
-                            // four full tiles: k-step t of each (4 KB) and their scale chunks,
-                            // one tensor copy each, in the same shared layout as below
-                            if (lane == 0) {
-                                uint8_t* st = ring + off;
-                                mbar_expect_tx(&sh.full[slot], (uint32_t)n * (kTileA + kSfChunk));
-                                tma_load_4d(st, map_c, 0, 2 * t, t2, e, &sh.full[slot], wpol);
-                                tma_load_4d(st + n * kTileA, static_cast<const uint8_t*>(map_c) + 128, 0, t >> 1, t2, e,
-                                            &sh.full[slot], wpol);
-                            }
-                            __syncwarp();
-                            continue;
-                        }
-                        uint32_t bytes = 0;
-#pragma unroll 1
-                        for (int j = 0; j < n; ++j) {
-                            const int R2 = p.H - (t2 + j) * kRowTile < kRowTile ? p.H - (t2 + j) * kRowTile : kRowTile;
-                            bytes += (uint32_t)R2 * 32 + kSfChunk;
-                        }
                         if (lane == 0)
-                            mbar_expect_tx(&sh.full[slot], bytes);
+                            mbar_expect_tx(&sh.full[slot], (uint32_t)rows * 32 + (uint32_t)n * kSfChunk);
                         __syncwarp();
                         uint8_t* st = ring + off;
-                        const int j = lane & 15;
-                        if (j < n) {
-                            const int tt = t2 + j;
-                            const int R2 = p.H - tt * kRowTile < kRowTile ? p.H - tt * kRowTile : kRowTile;
-                            if (lane < 16)
-                                bulk_copy_hint(st + j * kTileA,
-                                               d0 + (long long)tt * kRowTile * (p.I / 2) + (long long)t * R2 * 32,
-                                               (uint32_t)R2 * 32, &sh.full[slot], wpol);
-                            else
-                                bulk_copy_hint(st + n * kTileA + j * kSfChunk, sd0 + (long long)tt * CHI * kSfChunk,
-                                               kSfChunk, &sh.full[slot], wpol);
-                        }
+                        if (lane == 0)
+                            bulk_copy_hint(st, c0 + (long long)t2 * kRowTile * 32, (uint32_t)rows * 32, &sh.full[slot],
+                                           wpol);
+                        else if (lane == 1)
+                            bulk_copy_hint(st + n * kTileA, sc0 + (long long)t2 * kSfChunk, (uint32_t)n * kSfChunk,
+                                           &sh.full[slot], wpol);
                     }
                 }
             }

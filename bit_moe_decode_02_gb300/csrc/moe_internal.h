@@ -19,20 +19,25 @@ int set_error(int code, const char* fmt, ...);
 // ------------------------------------------------------------------ batched
 // Calls with M > kMaxTokens run per-expert grouped GEMMs on the tensor cores
 // (tcgen05.mma kind::mxf4: MXFP4 weights x MXFP4-quantised activations, fp32
-// accumulators in tensor memory).  Weights are kept a second time in a "tile"
-// layout made for that instruction.
+// accumulators in tensor memory).  Weights are kept once, in a "tile" layout
+// made for that instruction, which the decode kernels stream as well.
 //
 // Tile layout of one projection W [N][K] (N, K multiples of 64).  Row tile t
 // covers rows 128t .. 128t + R_t - 1 (R_t = 128, or N % 128 for the last one),
 // k-step s covers K = 64s .. 64s + 63.
-//   codes  at t*128*K/2 + s*R_t*32: an R_t x 32-byte block in the canonical
-//          no-swizzle K-major order -- row r, byte b at
-//          (r/8)*256 + (b/16)*128 + (r%8)*16 + b%16 (8x16-byte core matrices;
-//          K-direction stride 128, row-group stride 256).
-//   scales at N*K/2 + (t*C + c)*512, C = ceil(K/128): chunk c holds the E8M0
-//          bytes of K-blocks 4c..4c+3 of the tile's 128 rows, row r = i + 32j
-//          and block kb at i*16 + j*4 + kb (the order a 32x128-bit tensor-memory
-//          copy replicated to the four lane quarters expects).
+//   codes  an R_t x 32-byte block per (t, s) in the canonical no-swizzle
+//          K-major order -- row r, byte b at (r/8)*256 + (b/16)*128 + (r%8)*16
+//          + b%16 (8x16-byte core matrices; K-direction stride 128, row-group
+//          stride 256) -- at t*128*K/2 + s*R_t*32 (row-tile-major: gate_up)
+//          or at s*N*32 + t*128*32 (k-step-major: down).
+//   scales at N*K/2 + (t*C + c)*512 (row-tile-major) or N*K/2 + (c*T + t)*512
+//          (k-step-major), C = ceil(K/128), T = ceil(N/128): chunk c of tile t
+//          holds the E8M0 bytes of K-blocks 4c..4c+3 of the tile's 128 rows,
+//          row r = i + 32j and block kb at i*16 + j*4 + kb (the order a
+//          32x128-bit tensor-memory copy replicated to the four lane quarters
+//          expects).
+// A decode unit of gate_up is one row tile over all of K, and of down one
+// k-step over all rows: each order makes a unit's bytes one contiguous run.
 // The gate_up matrix [2I][K] (gate rows 0..I-1, up rows I..2I-1) is stored as
 // one projection of 2I rows in the interleaved row order: tile t holds gate rows
 // 64t .. 64t+63 as its rows 0..63 and up rows 64t .. 64t+63 as its rows
@@ -49,6 +54,26 @@ inline __host__ __device__ long long tile_proj_bytes(int N, int K)
 {
     return (long long)N * K / 2 + (long long)ceil_div(N, kRowTile) * ceil_div(K, 128) * kSfChunk;
 }
+// Byte offsets, within one expert's projection, of the R_t x 32-byte
+// block (row tile t, k-step s) and of scale chunk (row tile t, 128-column
+// chunk ch).  Row-tile-major (kmajor = 0): a tile's k-steps follow one
+// another, so one row tile over all of K is contiguous (gate_up: a decode unit
+// is one row tile).  K-step-major (kmajor = 1): the tiles of one k-step follow
+// one another (rows 0 .. N-1 of k-step s are contiguous, and so are the scale
+// chunks of one column chunk), so one k-step over all rows is contiguous
+// (down: a decode unit is one k-step of every row).
+inline __host__ __device__ long long tile_block_off(int N, int K, int t, int s, int kmajor)
+{
+    const int R = N - t * kRowTile < kRowTile ? N - t * kRowTile : kRowTile;
+    return kmajor ? (long long)s * N * 32 + (long long)t * kRowTile * 32
+                  : (long long)t * kRowTile * (K / 2) + (long long)s * R * 32;
+}
+inline __host__ __device__ long long tile_sf_off(int N, int K, int t, int ch, int kmajor)
+{
+    const int T = ceil_div(N, kRowTile), CH = ceil_div(K, 128);
+    return (long long)N * (K / 2) + (long long)(kmajor ? ch * T + t : t * CH + ch) * kSfChunk;
+}
+
 inline int max_tok_tiles(int Mk, int E) { return E + ceil_div(Mk, kTokTile); }
 
 struct TokTile {
@@ -95,9 +120,10 @@ cudaError_t prepare_batched_kernels();
 // Caller layout [E][N][K/2] codes + [E][N][K/32] E8M0 -> tile layout (one projection
 // per expert of N rows of a caller matrix with `src_rows` rows).  Tile row n comes
 // from caller row n, or with `interleave` = I > 0 (N = 2I) from the interleaved
-// gate_up order: row 64t + r (r < 64) or I + 64t + r - 64 of tile t.
+// gate_up order: row 64t + r (r < 64) or I + 64t + r - 64 of tile t; `kmajor`
+// picks the k-step-major order.
 cudaError_t launch_repack_tiles(const uint8_t* codes, const uint8_t* scales, int E, int src_rows,
-                                int N, int K, int interleave, uint8_t* out, long long expert_bytes,
+                                int N, int K, int interleave, int kmajor, uint8_t* out, long long expert_bytes,
                                 cudaStream_t stream);
 // MX quantisation of n fp32 values (n % 32 == 0) into natural order codes/scales.
 cudaError_t launch_mx_quantize(const float* in, long long n, uint8_t* codes, uint8_t* scales,
@@ -130,11 +156,6 @@ struct DecodeTcParams {
     float* out_f32;             // [M][H] fp32 result before the bf16 rounding per call, or nullptr
     long long logits_stride, x_stride, resid_stride, out_f32_stride;
     int ncalls, layer0, nlayers;
-    // Tensor maps of the down projections, two per layer (codes, then scale
-    // chunks; 128 bytes each, in global memory), or nullptr: with them a down
-    // stage of 4 full 128-row tiles is two tensor copies instead of eight
-    const void* dn_maps;
-    int t2full;                 // full 128-row tiles of the down projection (H / 128)
     float* part;                // [G][H][4] each CTA's fp32 copy of the expert output
     uint8_t* xt;                // x terms of the layer: [H/64][N rows x 32 B][ceil(H/128)][512]
     float* gpart;               // [G][128][4] gate/up partial sums of split-unit pieces
@@ -202,7 +223,7 @@ cudaError_t launch_dequant_i4(const uint8_t* w, int H, int I, int group, int pro
 // Debug kernels.
 // One expert projection of the tile layout back to fp32 in caller row order
 // (gate_up: interleave = I, rows [0, I) gate and [I, 2I) up; down: 0).
-cudaError_t launch_dequant_tiles(const uint8_t* tiles, int N, int K, int interleave, float* out,
+cudaError_t launch_dequant_tiles(const uint8_t* tiles, int N, int K, int interleave, int kmajor, float* out,
                                  cudaStream_t stream);
 cudaError_t launch_dequant(int fmt, int group, const uint8_t* slabs, int N, int K, int slab_bytes,
                            float* out, cudaStream_t stream);

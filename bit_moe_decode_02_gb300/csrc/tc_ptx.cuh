@@ -93,18 +93,6 @@ __device__ __forceinline__ void bulk_copy_hint(void* dst, const void* src, uint3
                  ::"r"(su32(dst)), "l"(src), "r"(bytes), "r"(su32(bar)), "l"(pol) : "memory");
 }
 
-// Tiled 4-D tensor copy global -> shared (the box described by the tensor map
-// at `tmap`, a global address) completing on `bar`, with an L2 cache policy.
-// Coordinates are in elements; the destination is 128-byte aligned.
-__device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int c0, int c1, int c2, int c3, uint64_t* bar,
-                                            uint64_t pol)
-{
-    asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
-                 "[%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
-                 ::"r"(su32(dst)), "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(su32(bar)), "l"(pol)
-                 : "memory");
-}
-
 // Shared-memory matrix descriptor, no swizzle, K-major canonical layout:
 // 8-row x 16-byte core matrices, `lbo` bytes between core matrices along K,
 // `sbo` bytes between 8-row groups; bits 46..48 = 0b001 (tcgen05 descriptor).
