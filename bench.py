@@ -249,8 +249,9 @@ def run_ours(args):
     shape = SHAPE
     L = args.layers or shape.layers
     H, E, k = shape.hidden, shape.experts, shape.top_k
-    # max_tokens 4: the same resident layers also serve the M = 4 stack of "extra"
-    h = moe.moe_create(H, shape.intermediate, E, L, 4, k, moe.MOE_FMT_MXFP4, 32, 1)
+    # max_tokens 16: the same resident layers also serve the stacks and the M
+    # sweep of "extra" (M <= 4 on the decode kernel, 8 and 16 on the batched path)
+    h = moe.moe_create(H, shape.intermediate, E, L, 16, k, moe.MOE_FMT_MXFP4, 32, 1)
     _load_all(moe, h, shape, L)
     W, K = args.warmup, args.steps
     n_in = W + K
@@ -312,22 +313,33 @@ def run_ours(args):
         moe.moe_forward(h, s % L, xp[s], lp[s], 1, k, rp[s], stream)
         bytes_per_step.append(moe.moe_last_bytes(h, stream))
 
-    # end to end through the public API with host buffers (pinned): every step
-    # copies x, logits and the residual in and the result out.
+    # end to end through the public API with host buffers: the same K steps with
+    # their inputs and results in page-locked host memory, which the kernel reads
+    # and writes over the host-device link step by step (every step's x, logits
+    # and residual come in from the host, its result goes out to it); the host
+    # clock runs from the call to the end of the stream synchronisation.
     xh = torch.from_numpy(xs.view(np.int16)).pin_memory()
     lh = torch.from_numpy(ls).pin_memory()
     oh = torch.from_numpy(rs.view(np.int16)).pin_memory()
-    xhp = [xh[s].data_ptr() for s in range(n_in)]
-    lhp = [lh[s].data_ptr() for s in range(n_in)]
-    ohp = [oh[s].data_ptr() for s in range(n_in)]
     sp = stream.cuda_stream
-    for s in range(W):
-        moe.moe_forward_host(h, s % L, xhp[s], lhp[s], 1, k, ohp[s], sp)
+    moe.moe_forward_steps(h, W, 0, xh[0].data_ptr(), lh[0].data_ptr(), 1, k, oh[0].data_ptr(), sp)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for s in range(W, n_in):
-        moe.moe_forward_host(h, s % L, xhp[s], lhp[s], 1, k, ohp[s], sp)
+    moe.moe_forward_steps(h, K, W % L, xh[W].data_ptr(), lh[W].data_ptr(), 1, k, oh[W].data_ptr(), sp)
+    stream.synchronize()
     e2e_s = _max_over_ranks(time.perf_counter() - t0, world)
+    assert moe.moe_get_status(h) == 0
+    # one moe_forward_host call per step instead (a host memcpy into the handle's
+    # mapped staging, one launch and one synchronisation each)
+    ohp = [oh[s].data_ptr() for s in range(n_in)]
+    nh = min(K, 200)
+    for s in range(W):
+        moe.moe_forward_host(h, s % L, xh[s].data_ptr(), lh[s].data_ptr(), 1, k, ohp[s], sp)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s in range(W, W + nh):
+        moe.moe_forward_host(h, s % L, xh[s].data_ptr(), lh[s].data_ptr(), 1, k, ohp[s], sp)
+    e2e_call_us = 1e6 * (time.perf_counter() - t0) / nh
 
     us_per_layer = 1e3 * ms / (K * world)
     avg_bytes = float(np.mean(bytes_per_step))
@@ -339,9 +351,16 @@ def run_ours(args):
             "workload": WORKLOAD, "metric": METRIC, "value": 1e3 * ms_graph / (K * world), "unit": UNIT,
             "gbs": float(np.mean(bytes_per_step)) / (ms_graph / 1e3 / K) / 1e9,
             "launch": "the same K steps as K moe_forward launches (PDL-chained) in one CUDA graph",
-            "gpu_launches": K, "clocks": clk_g.summary()}}
+            "gpu_launches": K, "clocks": clk_g.summary()},
+            "e2e_per_call": {"value": e2e_call_us, "unit": UNIT, "calls": nh,
+                             "api": "moe_forward_host per step (host memcpy into mapped staging, one launch, "
+                                    "one stream synchronisation)"}}
         for M in (1, 4):
             extra[f"stack24_m{M}"] = measure_stack(moe, h, synth.GPTOSS_STACK, L, M, args.extra_steps, 8)
+        for M in (1, 4):
+            extra[f"stack24_steps_m{M}"] = measure_stack_steps(moe, h, synth.GPTOSS_STACK, L, M,
+                                                               args.extra_steps, 4)
+        extra["m_sweep"] = measure_m_sweep(moe, h, shape, L, max(args.extra_steps, 64))
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -373,7 +392,10 @@ def run_ours(args):
                      "kernel": "decode_tc_kernel (persistent, one CTA per SM, K layer calls per launch)",
                      "bytes_per_launch": avg_bytes, "traffic": stored_traffic()},
         "e2e": {"value": 1e6 * e2e_s / (K * world), "unit": UNIT,
-                "h2d_bytes_per_step": H * 2 * 2 + E * 4, "d2h_bytes_per_step": H * 2},
+                "h2d_bytes_per_step": H * 2 * 2 + E * 4, "d2h_bytes_per_step": H * 2,
+                "api": "moe_forward_steps on page-locked host buffers (the kernel reads each step's "
+                       "inputs and writes its result over the host-device link); host clock around the "
+                       "call and the stream synchronisation"},
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
@@ -382,6 +404,97 @@ def run_ours(args):
         line["extra"] = extra
     print(json.dumps(line), flush=True)
     return 0
+
+
+def measure_stack_steps(moe, h, shape, L, M, steps, warmup):
+    """Tokens/s of the expert stack with every step of the timed run in ONE
+    launch (moe_forward_stack_steps: steps x L layer calls, each step on its own
+    fresh residual and logits, each layer reading its logits only after the
+    previous layer's output is complete)."""
+    import torch
+    k = shape.top_k
+    n = warmup + steps
+    ins = [synth.step_inputs(shape, 6000 + s, M=M, layers=L) for s in range(n)]
+    rd = torch.from_numpy(np.stack([r for _, r, _ in ins]).view(np.int16)).cuda()
+    ld = torch.from_numpy(np.ascontiguousarray(np.stack([lg for _, _, lg in ins]))).cuda()
+    stream = torch.cuda.current_stream()
+    moe.moe_forward_stack_steps(h, warmup, rd[0], ld[0], M, k, stream)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ev0.record(stream)
+        moe.moe_forward_stack_steps(h, steps, rd[warmup], ld[warmup], M, k, stream)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    assert moe.moe_get_status(h) == 0
+    launches = moe.moe_last_launches(h)
+    nbytes = moe.moe_last_bytes(h, stream) / steps   # per step (the last step's layers)
+    us = 1e3 * ms / steps
+    peak, kind = measured_peaks()
+    gbs = nbytes / (us / 1e6) / 1e9
+    return {"workload": f"{shape.name}, M={M}, {steps} steps x {L} layers in one launch",
+            "metric": "tokens/s of the expert stack", "value": M * 1e6 / us, "unit": "tok/s",
+            "us_per_step": us, "us_per_layer": us / L, "steps": steps, "warmup": warmup,
+            "bytes_per_step": nbytes, "gbs": gbs, "frac_of_peak": gbs / peak, "peak": peak, "peak_kind": kind,
+            "clocks": clk.summary(), "gpu_launches": launches,
+            "launch": "one persistent launch for all steps x layers (moe_forward_stack_steps)"}
+
+
+def measure_m_sweep(moe, h, shape, L, steps):
+    """Per-layer time and throughput of the gpt-oss layer against the number of
+    tokens M: M <= 4 on the decode kernel (moe_forward_steps, one launch),
+    M = 8 and 16 on the batched tensor-core path (moe_forward per step in a
+    CUDA graph).  Step s runs resident layer s mod L (inputs larger than L2)."""
+    import torch
+    k, H, E = shape.top_k, shape.hidden, shape.experts
+    stream = torch.cuda.current_stream()
+    peak, kind = measured_peaks()
+    out = {}
+    for M in (1, 2, 3, 4, 8, 16):
+        ins = [synth.step_inputs(shape, 8000 + 97 * M + s, M=M, layers=1) for s in range(steps)]
+        xd = torch.from_numpy(np.stack([x for x, _, _ in ins]).view(np.int16)).cuda()
+        rd = torch.from_numpy(np.stack([r for _, r, _ in ins]).view(np.int16)).cuda()
+        ld = torch.from_numpy(np.ascontiguousarray(np.stack([lg[0] for _, _, lg in ins]))).cuda()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if M <= 4:
+            moe.moe_forward_steps(h, 8, 0, xd[0], ld[0], M, k, rd[0], stream)
+            torch.cuda.synchronize()
+            ev0.record(stream)
+            moe.moe_forward_steps(h, steps, 0, xd[0], ld[0], M, k, rd[0], stream)
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            nbytes = moe.moe_last_bytes(h, stream) / steps
+            path, launches = "decode kernel, one launch for all steps", 1
+        else:
+            cap = torch.cuda.Stream()
+            g = torch.cuda.CUDAGraph()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=cap):
+                for s in range(steps):
+                    moe.moe_forward(h, s % L, xd[s], ld[s], M, k, rd[s], cap)
+            launches = moe.moe_last_launches(h) * steps
+            g.replay()
+            torch.cuda.synchronize()
+            ev0.record(stream)
+            g.replay()
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            nb = []
+            for s in range(min(steps, 16)):
+                moe.moe_forward(h, s % L, xd[s], ld[s], M, k, rd[s], stream)
+                nb.append(moe.moe_last_bytes(h, stream))
+            nbytes = float(np.mean(nb))
+            path = "batched tensor-core path, moe_forward per step in one CUDA graph"
+        assert moe.moe_get_status(h) == 0
+        us = 1e3 * ev0.elapsed_time(ev1) / steps
+        gbs = nbytes / (us / 1e6) / 1e9
+        out[f"m{M}"] = {"us_per_layer": us, "tok_per_s_per_layer": M * 1e6 / us, "bytes_per_layer": nbytes,
+                        "gbs": gbs, "frac_of_peak": gbs / peak, "path": path, "steps": steps,
+                        "gpu_launches": launches}
+    out["peak"], out["peak_kind"] = peak, kind
+    out["workload"] = f"{shape.name} layer, step s on resident layer s mod {L}"
+    return out
 
 
 def measure_stack(moe, h, shape, L, M, steps, warmup):

@@ -6,8 +6,8 @@ status.  There is no CPU fallback: if libmoe.so is missing the import of the
 library fails loudly (build it with ``python -m bit_moe_decode_02_gb300.build_ext``).
 
 The function names are the C names: moe_create, moe_load_experts, moe_forward,
-moe_forward_host, moe_forward_stack, moe_forward_steps, moe_get_status, moe_debug_dequant,
-moe_debug_route, moe_debug_stack_trace, moe_debug_forward_f32, moe_debug_set_wait,
+moe_forward_host, moe_forward_stack, moe_forward_stack_steps, moe_forward_steps,
+moe_get_status, moe_debug_dequant, moe_debug_route, moe_debug_stack_trace, moe_debug_forward_f32, moe_debug_set_wait,
 moe_last_bytes, moe_expert_bytes, moe_last_launches, moe_last_error, moe_forward_noalloc,
 moe_destroy.
 """
@@ -32,7 +32,7 @@ MOE_FMT_INT4 = 2
 
 # every symbol include/moe.h declares
 EXPORTS = ("moe_create", "moe_load_experts", "moe_forward", "moe_forward_host",
-           "moe_forward_stack", "moe_forward_steps", "moe_get_status", "moe_debug_dequant", "moe_debug_route",
+           "moe_forward_stack", "moe_forward_stack_steps", "moe_forward_steps", "moe_get_status", "moe_debug_dequant", "moe_debug_route",
            "moe_debug_stack_trace", "moe_debug_mx_quantize", "moe_debug_batched_h",
            "moe_debug_forward_f32", "moe_debug_set_wait",
            "moe_last_bytes", "moe_expert_bytes", "moe_last_launches", "moe_last_error",
@@ -73,6 +73,8 @@ def lib() -> ctypes.CDLL:
         L.moe_forward_host.restype = i
         L.moe_forward_stack.argtypes = [p, p, p, i, i, p]
         L.moe_forward_stack.restype = i
+        L.moe_forward_stack_steps.argtypes = [p, i, p, p, i, i, p]
+        L.moe_forward_stack_steps.restype = i
         L.moe_forward_steps.argtypes = [p, i, i, p, p, i, i, p, p]
         L.moe_forward_steps.restype = i
         L.moe_get_status.argtypes = [p, p]
@@ -166,6 +168,10 @@ def moe_forward_host(h, layer, x, logits, M, top_k, out, stream=None):
 
 def moe_forward_stack(h, resid, logits, M, top_k, stream=None):
     return _check(lib().moe_forward_stack(h, _ptr(resid), _ptr(logits), M, top_k, _stream(stream)))
+
+
+def moe_forward_stack_steps(h, n, resid, logits, M, top_k, stream=None):
+    return _check(lib().moe_forward_stack_steps(h, n, _ptr(resid), _ptr(logits), M, top_k, _stream(stream)))
 
 
 def moe_forward_steps(h, n, layer0, x, logits, M, top_k, out, stream=None):

@@ -198,6 +198,7 @@ moe::DecodeTcParams tc_params(const moe_handle* h, int layer0, int ncalls)
 {
     const moe_config& c = h->cfg;
     moe::DecodeTcParams p{};
+    p.resid_every = 1;
     p.gu = h->arena;
     p.dn = h->arena + h->off_dn;
     p.layer_stride = (long long)h->layer_stride;
@@ -230,6 +231,7 @@ moe::DecodeI4Params i4_params(const moe_handle* h, int layer0, int ncalls)
 {
     const moe_config& c = h->cfg;
     moe::DecodeI4Params p{};
+    p.resid_every = 1;
     p.gu = h->arena;
     p.dn = h->arena + h->off_dn;
     p.layer_stride = (long long)h->layer_stride;
@@ -260,7 +262,7 @@ moe::DecodeI4Params i4_params(const moe_handle* h, int layer0, int ncalls)
 // residual), resid + s * rs and out_f32 + s * fs (bytes).
 cudaError_t launch_seq(const moe_handle* h, int layer0, int n, const float* logits, long long ls, const void* x,
                        long long xs, void* resid, long long rs, float* out_f32, long long fs, int M, int k,
-                       cudaStream_t s)
+                       cudaStream_t s, int resid_every = 1)
 {
     if (h->mxfp4) {
         moe::DecodeTcParams p = tc_params(h, layer0, n);
@@ -270,6 +272,7 @@ cudaError_t launch_seq(const moe_handle* h, int layer0, int n, const float* logi
         p.x_stride = xs;
         p.resid = static_cast<uint16_t*>(resid);
         p.resid_stride = rs;
+        p.resid_every = resid_every;
         p.out_f32 = out_f32;
         p.out_f32_stride = fs;
         p.M = M;
@@ -283,6 +286,7 @@ cudaError_t launch_seq(const moe_handle* h, int layer0, int n, const float* logi
     p.x_stride = xs;
     p.resid = static_cast<uint16_t*>(resid);
     p.resid_stride = rs;
+    p.resid_every = resid_every;
     p.out_f32 = out_f32;
     p.out_f32_stride = fs;
     p.M = M;
@@ -415,6 +419,21 @@ int check_forward_args(const moe_handle* h, int M, int top_k)
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// False only for host memory the device cannot read at the same address
+// (pageable, or page-locked but not mapped there).  A query that fails (for
+// instance inside a stream capture that forbids it) proves nothing and passes.
+bool device_accessible(const void* p)
+{
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return true;
+    }
+    if (a.type == cudaMemoryTypeUnregistered)
+        return false;
+    return a.type != cudaMemoryTypeHost || a.devicePointer == p;
+}
 
 int check_all_loaded(const moe_handle* h, const char* who)
 {
@@ -701,8 +720,8 @@ int moe_forward_host(moe_handle* h, int layer, const void* x_bf16, const float* 
     return MOE_OK;
 }
 
-int moe_forward_stack(moe_handle* h, void* resid_bf16, const float* router_logits, int M, int top_k,
-                      void* stream)
+int moe_forward_stack_steps(moe_handle* h, int n, void* resid_bf16, const float* router_logits, int M, int top_k,
+                            void* stream)
 {
     int rc = check_forward_args(h, M, top_k);
     if (rc != MOE_OK)
@@ -710,6 +729,8 @@ int moe_forward_stack(moe_handle* h, void* resid_bf16, const float* router_logit
     if (M > moe::kMaxTokens)
         return fail(MOE_ERR_UNSUPPORTED, "moe_forward_stack: M=%d > %d; the stack runs the decode kernel only", M,
                     moe::kMaxTokens);
+    if (n < 1)
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_stack_steps: n=%d must be >= 1", n);
     if (!resid_bf16 || !router_logits)
         return fail(MOE_ERR_INVALID_ARG, "moe_forward_stack: resid and logits must not be NULL");
     if (!aligned16(resid_bf16) || !aligned16(router_logits))
@@ -717,16 +738,27 @@ int moe_forward_stack(moe_handle* h, void* resid_bf16, const float* router_logit
     if ((rc = check_all_loaded(h, "moe_forward_stack")) != MOE_OK)
         return rc;
     const int L = h->cfg.num_layers;
-    // the L layers in one persistent launch (grid barriers between layers); each
-    // layer's input is the normalised residual, which the kernel forms itself
-    cudaError_t e = launch_seq(h, 0, L, router_logits, (long long)M * h->cfg.num_experts * sizeof(float), nullptr,
-                               0, resid_bf16, 0, nullptr, 0, M, top_k, (cudaStream_t)stream);
+    if ((long long)n * L > (1ll << 30))
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_stack_steps: n * L = %lld layer calls is too many",
+                    (long long)n * L);
+    // the n x L layer calls in one persistent launch (grid barriers between them):
+    // call c runs layer c mod L on step c / L's residual; each layer's input is the
+    // normalised residual, which the kernel forms itself
+    cudaError_t e = launch_seq(h, 0, n * L, router_logits, (long long)M * h->cfg.num_experts * sizeof(float),
+                               nullptr, 0, resid_bf16, (long long)M * h->cfg.hidden * 2, nullptr, 0, M, top_k,
+                               (cudaStream_t)stream, L);
     if (e != cudaSuccess)
         return cuda_fail(e, "moe_forward_stack launch");
-    h->last_steps = L;
+    h->last_steps = n * L;
     h->last_first_layer = 0;
     h->last_launches = 1;
     return MOE_OK;
+}
+
+int moe_forward_stack(moe_handle* h, void* resid_bf16, const float* router_logits, int M, int top_k,
+                      void* stream)
+{
+    return moe_forward_stack_steps(h, 1, resid_bf16, router_logits, M, top_k, stream);
 }
 
 int moe_forward_steps(moe_handle* h, int n, int layer0, const void* x_bf16, const float* router_logits, int M,
@@ -745,6 +777,9 @@ int moe_forward_steps(moe_handle* h, int n, int layer0, const void* x_bf16, cons
         return fail(MOE_ERR_INVALID_ARG, "moe_forward_steps: x, logits and out must not be NULL");
     if (!aligned16(x_bf16) || !aligned16(out_bf16) || !aligned16(router_logits))
         return fail(MOE_ERR_INVALID_ARG, "moe_forward_steps: x, logits and out must be 16-byte aligned");
+    if (!device_accessible(x_bf16) || !device_accessible(router_logits) || !device_accessible(out_bf16))
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_steps: x, logits and out must be device memory or "
+                                         "page-locked host memory mapped at the same address");
     const size_t nb = (size_t)n * M * h->cfg.hidden * 2;
     if (overlaps(x_bf16, nb, out_bf16, nb))
         return fail(MOE_ERR_INVALID_ARG, "moe_forward_steps: x overlaps out");

@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
         const uint16_t* xin = p.x ? reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(p.x) +
                                                                      (long long)call * p.x_stride) : nullptr;
         uint16_t* resid = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(p.resid) +
-                                                      (long long)call * p.resid_stride);
+                                                      (long long)(call / p.resid_every) * p.resid_stride);
         float* of32 = p.out_f32 ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(p.out_f32) +
                                                           (long long)call * p.out_f32_stride) : nullptr;
         const uint16_t* gub = p.gu_bias ? reinterpret_cast<const uint16_t*>(

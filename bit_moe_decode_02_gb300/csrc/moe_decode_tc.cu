@@ -632,7 +632,8 @@ __device__ __forceinline__ void decode_call(const int call)
                                                  (long long)call * p.logits_stride)
 #define cl_x (p.x ? reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(p.x) + \
                                                       (long long)call * p.x_stride) : nullptr)
-#define cl_resid reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(p.resid) + (long long)call * p.resid_stride)
+#define cl_resid reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(p.resid) + \
+                                             (long long)(call / p.resid_every) * p.resid_stride)
 #define cl_f32 (p.out_f32 ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(p.out_f32) + \
                                                      (long long)call * p.out_f32_stride) : nullptr)
 

@@ -155,6 +155,7 @@ struct DecodeTcParams {
     uint16_t* resid;            // [M][H] bf16 in/out per call
     float* out_f32;             // [M][H] fp32 result before the bf16 rounding per call, or nullptr
     long long logits_stride, x_stride, resid_stride, out_f32_stride;
+    int resid_every;            // calls per residual buffer: call c uses resid + (c / resid_every) * resid_stride
     int ncalls, layer0, nlayers;
     float* part;                // [G][H][4] each CTA's fp32 copy of the expert output
     uint8_t* xt;                // x terms of the layer: [H/64][N rows x 32 B][ceil(H/128)][512]
@@ -200,6 +201,7 @@ struct DecodeI4Params {
     uint16_t* resid;
     float* out_f32;
     long long logits_stride, x_stride, resid_stride, out_f32_stride;
+    int resid_every;            // calls per residual buffer: call c uses resid + (c / resid_every) * resid_stride
     int ncalls, layer0, nlayers;
     float* part;                // [G][H][4] each CTA's fp32 copy of the expert output
     unsigned long long* done;   // [1] grid-barrier arrivals (only grows)

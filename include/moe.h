@@ -167,24 +167,42 @@ int moe_forward_host(moe_handle* h, int layer, const void* x_bf16, const float* 
  * overflows within a few layers on these value distributions).
  * resid bf16 [M][H] holds r_0 on entry and r_L on return; logits fp32
  * [L][M][E].  Layer l+1 reads its logits only after layer l's output is
- * complete.  Device pointers.  MXFP4: one persistent launch for all L layers
- * (grid barriers between them); int4: a cached CUDA graph of L
- * programmatically chained layer kernels per (M, top_k, resid, logits).
- * Decode sizes only: M <= 4 (else MOE_ERR_UNSUPPORTED). */
+ * complete.  Device pointers.  One persistent launch for all L layers (grid
+ * barriers between them), both formats.  Decode sizes only: M <= 4 (else
+ * MOE_ERR_UNSUPPORTED). */
 int moe_forward_stack(moe_handle* h, void* resid_bf16, const float* router_logits,
                       int M, int top_k, void* stream);
+
+/* n decode steps of the whole stack in one persistent launch (n tokens, each
+ * through all L layers; P2's "all decode tokens into a single command
+ * buffer"): step t runs the L layers of moe_forward_stack on its own residual
+ * resid[t] (bf16 [n][M][H]: r_0 of step t on entry, its r_L on return) with
+ * logits[t] (fp32 [n][L][M][E]), steps one after another, exactly as n
+ * moe_forward_stack calls in that order would (bit-identical results).  Each
+ * layer call reads its logits only after the previous call's output is
+ * complete.  Device pointers, 16-byte aligned; decode sizes only (M <= 4);
+ * n * L <= 2^30. */
+int moe_forward_stack_steps(moe_handle* h, int n, void* resid_bf16, const float* router_logits,
+                            int M, int top_k, void* stream);
 
 /* n single-layer decode steps in sequence: step s runs resident layer
  * (layer0 + s) mod L on x[s], logits[s] and out[s] (x bf16 [n][M][H],
  * router_logits fp32 [n][M][E], out bf16 [n][M][H]: the residual of each step
  * on entry, r + MoE(x) on return), exactly as n moe_forward calls in that order
  * would (bit-identical results).  Step s + 1 reads its routing and inputs only
- * after step s's output is complete.  MXFP4: one persistent launch for all n
- * steps ("all decode tokens in a single command buffer", "Single-stream int4
- * decode of a 30B MoE", section 1); int4: one launch per step.  Decode sizes
- * only (M <= 4); x must not overlap out; device pointers, 16-byte aligned.
- * moe_last_bytes then counts each step's distinct experts (a layer run by
- * several steps counts its last step's, n times over). */
+ * after step s's output is complete.  One persistent launch for all n steps,
+ * both formats ("all decode tokens in a single command buffer", "Single-stream
+ * int4 decode of a 30B MoE", section 1).  Decode sizes only (M <= 4); x must
+ * not overlap out; 16-byte aligned.  x, logits and out may be device memory
+ * or page-locked host memory mapped into the device's address space at the
+ * same address (cudaHostAlloc / cudaMallocHost, or cudaHostRegister with
+ * cudaHostRegisterMapped, on a system with unified addressing): the kernel
+ * then reads each step's inputs and writes each step's result over the
+ * host-device link itself, and the host sees every step's result once
+ * `stream` has been synchronised.  Host memory that is not mapped so is
+ * rejected (MOE_ERR_INVALID_ARG).  moe_last_bytes then counts each step's
+ * distinct experts (a layer run by several steps counts its last step's, n
+ * times over). */
 int moe_forward_steps(moe_handle* h, int n, int layer0, const void* x_bf16, const float* router_logits,
                       int M, int top_k, void* out_bf16, void* stream);
 

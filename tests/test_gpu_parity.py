@@ -447,6 +447,55 @@ def test_stack_parity_small(moe, shape, L, M):
         moe.moe_destroy(h)
 
 
+@pytest.mark.parametrize("shape,L", [
+    (synth.Shape("tiny stack L=4", 256, 256, 8, 2, layers=4, bias_sigma=0.02, seed=21), 4),
+    (synth.Shape("int4 stack L=3", 128, 64, 6, 2, fmt=synth.FMT_INT4, group=64, has_bias=False,
+                 layers=3, seed=22), 3)], ids=lambda v: getattr(v, "name", str(v)))
+@pytest.mark.parametrize("M", [1, 3])
+def test_stack_steps_equal_single_stacks(moe, shape, L, M):
+    """n stack steps in one launch (n tokens x L layers) give the same bits as
+    n moe_forward_stack calls, and every layer transition of every step matches
+    the oracle's layer applied to the GPU's residual (the stack is an iterated
+    map that amplifies a one-ulp rounding-boundary difference from layer to
+    layer, so whole-stack trajectories are compared transition by transition)."""
+    n = 3
+    layers = [synth.layer_tensors(shape, l) for l in range(L)]
+    h = create_handle(shape, layers=L)
+    try:
+        for l, t in enumerate(layers):
+            load_layer(h, l, t)
+        ins = [synth.step_inputs(shape, 700 + s, M=M) for s in range(n)]
+        r = np.stack([b for _, b, _ in ins])
+        lg = np.stack([c for _, _, c in ins])
+        assert lg.shape == (n, L, M, shape.experts)
+        rd = to_dev_bf16(r)
+        ld = torch.from_numpy(np.ascontiguousarray(lg, np.float32)).cuda()
+        moe.moe_forward_stack_steps(h, n, rd, ld, M, shape.top_k)
+        torch.cuda.synchronize()
+        assert moe.moe_get_status(h) == 0
+        got = dev_to_bits(rd)
+        for s in range(n):
+            single = _run_stack(moe, h, r[s], lg[s], shape.top_k)
+            assert np.array_equal(got[s], single), f"step {s}"
+            trace = torch.empty((L + 1, M, shape.hidden), dtype=torch.int16, device="cuda")
+            moe.moe_debug_stack_trace(h, to_dev_bf16(r[s]), torch.from_numpy(np.ascontiguousarray(lg[s])).cuda(),
+                                      M, shape.top_k, trace)
+            torch.cuda.synchronize()
+            tr = trace.cpu().numpy().view(np.uint16)
+            assert np.array_equal(tr[L], got[s])
+            for l in range(L):
+                ref = oracle.stack(shape.fmt, shape.hidden, shape.intermediate, shape.experts, shape.top_k,
+                                   [layers[l]], lg[s][l:l + 1], tr[l], group=shape.group,
+                                   nthreads=oracle.max_threads())
+                assert_parity(bf16_bits_to_f64(tr[l + 1]), bf16_bits_to_f64(ref), ulps=1.0,
+                              what=f"{shape.name} M={M} step {s} layer {l}")
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_forward_stack_steps(h, 0, rd, ld, M, shape.top_k)
+        assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+    finally:
+        moe.moe_destroy(h)
+
+
 @pytest.mark.parametrize("shape", [synth.GPTOSS_STACK, synth.INT4_STACK], ids=lambda s: s.name)
 def test_stack_parity_full_size(moe, shape):
     """The full stacks (10 GB / 15 GB resident) at M=1 and M=4.
