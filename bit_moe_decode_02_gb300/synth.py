@@ -29,6 +29,7 @@ FMT_INT4 = 2
 _T_GU_CODES, _T_GU_SCALES, _T_GU_BIAS, _T_DN_CODES, _T_DN_SCALES, _T_DN_BIAS = range(6)
 # tensor ids of per-step streams
 _T_X, _T_R, _T_LOGITS = 100, 101, 102
+_T_ROUTER_W, _T_ROUTER_B = 200, 201
 
 
 @dataclass(frozen=True)
@@ -165,6 +166,16 @@ def layer_tensors(shape: Shape, layer: int = 0, experts=None) -> LayerTensors:
             if part is not None:
                 getattr(t, name)[e] = part
     return t
+
+
+def router_tensors(shape: Shape, layer: int = 0):
+    """Router weights of one layer: W bf16 bits [E][H] ~N(0, 1/H) (so that a
+    normalised input gives logits of unit spread, as the given-logits inputs
+    have) and bias bf16 bits [E] ~N(0, 0.1)."""
+    H, E, s = shape.hidden, shape.experts, shape.seed
+    w = _rng(s, layer, _T_ROUTER_W).normal(0.0, 1.0 / np.sqrt(H), (E, H)).astype(np.float32)
+    b = _rng(s, layer, _T_ROUTER_B).normal(0.0, 0.1, E).astype(np.float32)
+    return bf16_bits_from_f32(w), bf16_bits_from_f32(b)
 
 
 def step_inputs(shape: Shape, step: int, M: int | None = None, layers: int | None = None):

@@ -69,7 +69,9 @@ def lib():
             L.moe_oracle_layer.restype = i
             L.moe_oracle_layer.argtypes = [i, i, i, i, i, i, i, p, p, p, p, p, p, p, p, p, p, p, p, i]
             L.moe_oracle_stack.restype = i
-            L.moe_oracle_stack.argtypes = [i, i, i, i, i, i, i, i, p, p, p, p, p, p, p, p, i]
+            L.moe_oracle_stack.argtypes = [i, i, i, i, i, i, i, i, p, p, p, p, p, p, p, p, p, p, i]
+            L.moe_oracle_router.restype = None
+            L.moe_oracle_router.argtypes = [i, i, i, p, p, p, p]
             L.moe_oracle_mx_quantize.restype = None
             L.moe_oracle_mx_quantize.argtypes = [p, i64, p, p]
             L.moe_oracle_layer_batched.restype = i
@@ -179,12 +181,28 @@ def layer(fmt: int, H: int, I: int, E: int, k: int, t, x: np.ndarray, logits: np
     return out, idx, w
 
 
-def stack(fmt: int, H: int, I: int, E: int, k: int, layers, logits: np.ndarray,
-          resid: np.ndarray, group: int = 32, nthreads: int = 1) -> np.ndarray:
-    """Expert stack with the weightless RMSNorm coupling; returns r_L (bf16 bits)."""
+def router(x: np.ndarray, w: np.ndarray, b: np.ndarray | None = None) -> np.ndarray:
+    """Router GEMV in fp64: logits [M][E] = b + x W^T for bf16 bit patterns
+    x [M][H], w [E][H], b [E] (or None)."""
+    x = _c(x, np.uint16)
+    w = _c(w, np.uint16)
+    b = _c(b, np.uint16)
+    M, H = x.shape
+    E = w.shape[0]
+    out = np.empty((M, E), dtype=np.float64)
+    lib().moe_oracle_router(H, E, M, _ptr(x), _ptr(w), _ptr(b), _ptr(out))
+    return out
+
+
+def stack(fmt: int, H: int, I: int, E: int, k: int, layers, logits: np.ndarray | None,
+          resid: np.ndarray, group: int = 32, nthreads: int = 1, routers=None) -> np.ndarray:
+    """Expert stack with the weightless RMSNorm coupling; returns r_L (bf16 bits).
+    With ``routers`` (one (W bf16 [E][H], b bf16 [E] or None) per layer) each
+    layer's logits are the router GEMV of its input, rounded to fp32, and
+    ``logits`` is not read (it may be None)."""
     L = len(layers)
-    logits = _c(logits, np.float32)
-    M = logits.shape[1]
+    M = np.asarray(resid).shape[0]
+    logits = _c(np.zeros((L, M, E), np.float32) if logits is None else logits, np.float32)
     resid = np.array(resid, dtype=np.uint16, copy=True, order="C")
     sd = _scale_dtype(fmt)
     keep = []
@@ -202,10 +220,21 @@ def stack(fmt: int, H: int, I: int, E: int, k: int, layers, logits: np.ndarray,
 
     ptrs = [parr("gu_codes", np.uint8), parr("gu_scales", sd), parr("gu_bias", np.uint16),
             parr("dn_codes", np.uint8), parr("dn_scales", sd), parr("dn_bias", np.uint16)]
+    rw = rb = None
+    if routers is not None:
+        assert len(routers) == L
+        ws = [_c(w_, np.uint16) for w_, _ in routers]
+        bs = [_c(b_, np.uint16) for _, b_ in routers]
+        keep.extend(ws + bs)
+        rw = (ctypes.c_void_p * L)(*[a.ctypes.data for a in ws])
+        if any(a is not None for a in bs):
+            rb = (ctypes.c_void_p * L)(*[0 if a is None else a.ctypes.data for a in bs])
     rc = lib().moe_oracle_stack(fmt, H, I, E, group, L, M, k,
                                 *[ctypes.cast(p, ctypes.c_void_p) if p is not None else None
                                   for p in ptrs],
-                                _ptr(logits), _ptr(resid), nthreads)
+                                _ptr(logits), _ptr(resid),
+                                ctypes.cast(rw, ctypes.c_void_p) if rw is not None else None,
+                                ctypes.cast(rb, ctypes.c_void_p) if rb is not None else None, nthreads)
     if rc != 0:
         raise ValueError("oracle stack: bad arguments")
     return resid

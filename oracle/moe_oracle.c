@@ -332,17 +332,41 @@ int moe_oracle_layer(int fmt, int H, int I, int E, int group, int M, int k,
     return 0;
 }
 
+/* Router GEMV, the plain definition in fp64:
+ *   logits[m][e] = b[e] + sum_h x[m][h] * W[e][h]
+ * x bf16 [M][H] (the layer input the experts see), W bf16 [E][H], b bf16 [E]
+ * or NULL.  The router is the MoE block's gate: a linear map of the
+ * normalised hidden state to one logit per expert, whose top-k picks the
+ * experts ("Sovereign gpt-oss-20B (MXFP4) on Apple Silicon", section 1, top-4
+ * of 32; "Amortizing the per-token host-sync setup tax in fused all-layer q4
+ * decode on Apple M1 Ultra", section 3, the top-k on the GPU). */
+void moe_oracle_router(int H, int E, int M, const uint16_t* x, const uint16_t* w, const uint16_t* b,
+                       double* out)
+{
+    for (int m = 0; m < M; ++m)
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int j = 0; j < H; ++j)
+                acc += moe_oracle_bf16(x[(int64_t)m * H + j]) * moe_oracle_bf16(w[(int64_t)e * H + j]);
+            out[(int64_t)m * E + e] = (b ? moe_oracle_bf16(b[e]) : 0.0) + acc;
+        }
+}
+
 /* Expert stack: for l = 0..L-1, per token
  *   x_l     = bf16( r_l / sqrt(mean(r_l^2) + 1e-6) )
  *   r_{l+1} = bf16( r_l + MoE_l(x_l) )
  * layer l's tensors are passed as arrays of L pointers; logits fp32 [L][M][E];
- * resid bf16 [M][H] is read as r_0 and overwritten with r_L. */
+ * resid bf16 [M][H] is read as r_0 and overwritten with r_L.
+ * With router weights rw (L pointers to bf16 [E][H]; rb: L pointers to bf16
+ * [E] or NULL), layer l's logits are instead the router GEMV of x_l, rounded
+ * to fp32 (the precision the top-k is taken in), and `logits` is not read. */
 int moe_oracle_stack(int fmt, int H, int I, int E, int group, int L, int M, int k,
                      const uint8_t* const* gu_codes, const void* const* gu_scales,
                      const uint16_t* const* gu_bias,
                      const uint8_t* const* dn_codes, const void* const* dn_scales,
                      const uint16_t* const* dn_bias,
-                     const float* logits, uint16_t* resid, int nthreads)
+                     const float* logits, uint16_t* resid,
+                     const uint16_t* const* rw, const uint16_t* const* rb, int nthreads)
 {
     if (k < 1 || k > E || M < 0 || L < 0)
         return -1;
@@ -351,8 +375,12 @@ int moe_oracle_stack(int fmt, int H, int I, int E, int group, int L, int M, int 
     double* xv = (double*)malloc(sizeof(double) * (size_t)H);
     double* rv = (double*)malloc(sizeof(double) * (size_t)H);
     double* delta = (double*)malloc(sizeof(double) * (size_t)H);
+    uint16_t* xb = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)H);
+    double* lg64 = (double*)malloc(sizeof(double) * (size_t)E);
+    float* lg32 = (float*)malloc(sizeof(float) * (size_t)E);
     for (int l = 0; l < L; ++l) {
-        moe_oracle_route(logits + (int64_t)l * M * E, M, E, k, idx, w);
+        if (!rw)
+            moe_oracle_route(logits + (int64_t)l * M * E, M, E, k, idx, w);
         for (int m = 0; m < M; ++m) {
             uint16_t* rm = resid + (int64_t)m * H;
             double ss = 0.0;
@@ -361,8 +389,16 @@ int moe_oracle_stack(int fmt, int H, int I, int E, int group, int L, int M, int 
                 ss += rv[j] * rv[j];
             }
             double inv = 1.0 / sqrt(ss / H + 1e-6);
-            for (int j = 0; j < H; ++j)
-                xv[j] = moe_oracle_bf16(moe_oracle_to_bf16(rv[j] * inv));
+            for (int j = 0; j < H; ++j) {
+                xb[j] = moe_oracle_to_bf16(rv[j] * inv);
+                xv[j] = moe_oracle_bf16(xb[j]);
+            }
+            if (rw) {
+                moe_oracle_router(H, E, 1, xb, rw[l], rb ? rb[l] : NULL, lg64);
+                for (int e = 0; e < E; ++e)
+                    lg32[e] = (float)lg64[e];
+                moe_oracle_route(lg32, 1, E, k, idx + m * k, w + m * k);
+            }
             expert_mix(fmt, H, I, group, k, gu_codes[l], gu_scales[l],
                        gu_bias ? gu_bias[l] : NULL, dn_codes[l], dn_scales[l],
                        dn_bias ? dn_bias[l] : NULL, idx + m * k, w + m * k, xv, delta,
@@ -376,6 +412,9 @@ int moe_oracle_stack(int fmt, int H, int I, int E, int group, int L, int M, int 
     free(xv);
     free(rv);
     free(delta);
+    free(xb);
+    free(lg64);
+    free(lg32);
     return 0;
 }
 

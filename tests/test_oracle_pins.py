@@ -19,6 +19,7 @@ from scipy.special import expit, softmax
 
 import oracle
 from oracle import FMT_INT4, FMT_MXFP4
+from bit_moe_decode_02_gb300 import synth
 
 import os
 
@@ -493,3 +494,67 @@ def test_batched_equals_decode_when_x_on_grid_and_h_given():
     # and the decode oracle with the same x differs from it only through h
     out_dec, _, _ = oracle.layer(FMT_MXFP4, H, I, E, k, t, x, logits, None)
     assert out_dec.shape == out.shape
+
+
+# ------------------------------------------------------------- router GEMV
+
+def _bf(v):
+    return synth.bf16_bits_from_f32(np.asarray(v, np.float32))
+
+
+def test_router_matches_numpy_matmul():
+    """The oracle's fp64 loops against numpy's matmul (another implementation
+    of the same contraction) on bf16 inputs."""
+    rng = np.random.default_rng(11)
+    x, w, b = _bf(rng.standard_normal((3, 96))), _bf(rng.standard_normal((7, 96))), _bf(rng.standard_normal(7))
+    got = oracle.router(x, w, b)
+    ref = oracle.bf16_array(x) @ oracle.bf16_array(w).T + oracle.bf16_array(b)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(oracle.router(x, w), ref - oracle.bf16_array(b), rtol=1e-12, atol=1e-12)
+
+
+def test_router_one_hot_rows_pick_elements():
+    """W[e] = unit vector at h_e: logit e is x[h_e] + b[e], exactly."""
+    rng = np.random.default_rng(12)
+    H, E = 64, 5
+    x = _bf(rng.standard_normal((2, H)))
+    b = _bf(rng.standard_normal(E))
+    hs = [3, 17, 17, 40, 63]
+    w = np.zeros((E, H), np.uint16)
+    for e, hh in enumerate(hs):
+        w[e, hh] = 0x3F80   # 1.0
+    got = oracle.router(x, w, b)
+    xv, bv = oracle.bf16_array(x), oracle.bf16_array(b)
+    for m in range(2):
+        for e, hh in enumerate(hs):
+            assert got[m, e] == xv[m, hh] + bv[e]
+
+
+def test_stack_router_bias_only_equals_given_logits():
+    """Zero router weights and a bias holding the layer's logits (each exactly a
+    bf16 value) route exactly as those logits given directly."""
+    shape = synth.Shape("router pin", 64, 64, 6, 2, layers=3, bias_sigma=0.02, seed=71)
+    layers = [synth.layer_tensors(shape, l) for l in range(3)]
+    _, r, _ = synth.step_inputs(shape, 0, M=1)
+    lg_bits = _bf(np.random.default_rng(13).standard_normal((3, 6)))
+    lg = oracle.bf16_array(lg_bits).astype(np.float32)[:, None, :]
+    ref = oracle.stack(oracle.FMT_MXFP4, 64, 64, 6, 2, layers, lg, r)
+    routers = [(np.zeros((6, 64), np.uint16), lg_bits[l]) for l in range(3)]
+    got = oracle.stack(oracle.FMT_MXFP4, 64, 64, 6, 2, layers, None, r, routers=routers)
+    assert np.array_equal(got, ref)
+
+
+def test_stack_router_routes_on_the_normalised_input():
+    """With router weights, one stack layer equals the layer on x = RMSNorm(r)
+    with the logits taken from x through the (pinned) router GEMV."""
+    shape = synth.Shape("router pin 2", 128, 64, 8, 2, bias_sigma=0.02, seed=72)
+    t = synth.layer_tensors(shape, 0)
+    _, r, _ = synth.step_inputs(shape, 1, M=2)
+    w, b = synth.router_tensors(shape, 0)
+    got = oracle.stack(oracle.FMT_MXFP4, 128, 64, 8, 2, [t], None, r, routers=[(w, b)])
+    rv = oracle.bf16_array(r)
+    inv = 1.0 / np.sqrt((rv * rv).mean(axis=1, keepdims=True) + 1e-6)
+    x = oracle.to_bf16_array(rv * inv)
+    lg = oracle.router(x, w, b).astype(np.float32)
+    out, _, _ = oracle.layer(oracle.FMT_MXFP4, 128, 64, 8, 2, t, x, lg, r)
+    assert np.array_equal(got, oracle.to_bf16_array(out))
