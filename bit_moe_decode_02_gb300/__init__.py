@@ -7,7 +7,7 @@ library fails loudly (build it with ``python -m bit_moe_decode_02_gb300.build_ex
 
 The function names are the C names: moe_create, moe_load_experts, moe_forward,
 moe_forward_host, moe_forward_stack, moe_forward_stack_steps, moe_forward_steps,
-moe_get_status, moe_debug_dequant, moe_debug_route, moe_debug_stack_trace, moe_debug_forward_f32, moe_debug_set_wait,
+moe_load_router, moe_debug_router_logits, moe_get_status, moe_debug_dequant, moe_debug_route, moe_debug_stack_trace, moe_debug_forward_f32, moe_debug_set_wait,
 moe_last_bytes, moe_expert_bytes, moe_last_launches, moe_last_error, moe_forward_noalloc,
 moe_destroy.
 """
@@ -32,7 +32,8 @@ MOE_FMT_INT4 = 2
 
 # every symbol include/moe.h declares
 EXPORTS = ("moe_create", "moe_load_experts", "moe_forward", "moe_forward_host",
-           "moe_forward_stack", "moe_forward_stack_steps", "moe_forward_steps", "moe_get_status", "moe_debug_dequant", "moe_debug_route",
+           "moe_forward_stack", "moe_forward_stack_steps", "moe_forward_steps", "moe_load_router",
+           "moe_debug_router_logits", "moe_get_status", "moe_debug_dequant", "moe_debug_route",
            "moe_debug_stack_trace", "moe_debug_mx_quantize", "moe_debug_batched_h",
            "moe_debug_forward_f32", "moe_debug_set_wait",
            "moe_last_bytes", "moe_expert_bytes", "moe_last_launches", "moe_last_error",
@@ -75,6 +76,10 @@ def lib() -> ctypes.CDLL:
         L.moe_forward_stack.restype = i
         L.moe_forward_stack_steps.argtypes = [p, i, p, p, i, i, p]
         L.moe_forward_stack_steps.restype = i
+        L.moe_load_router.argtypes = [p, i, p, p]
+        L.moe_load_router.restype = i
+        L.moe_debug_router_logits.argtypes = [p, p, i, p]
+        L.moe_debug_router_logits.restype = i
         L.moe_forward_steps.argtypes = [p, i, i, p, p, i, i, p, p]
         L.moe_forward_steps.restype = i
         L.moe_get_status.argtypes = [p, p]
@@ -172,6 +177,15 @@ def moe_forward_stack(h, resid, logits, M, top_k, stream=None):
 
 def moe_forward_stack_steps(h, n, resid, logits, M, top_k, stream=None):
     return _check(lib().moe_forward_stack_steps(h, n, _ptr(resid), _ptr(logits), M, top_k, _stream(stream)))
+
+
+def moe_load_router(h, layer, w, bias=None):
+    """Router weights w bf16 bits [E][H] and bias [E] (numpy uint16 arrays or tensors)."""
+    return _check(lib().moe_load_router(h, layer, _ptr(w), _ptr(bias)))
+
+
+def moe_debug_router_logits(h, out, M, stream=None):
+    return _check(lib().moe_debug_router_logits(h, _ptr(out), M, _stream(stream)))
 
 
 def moe_forward_steps(h, n, layer0, x, logits, M, top_k, out, stream=None):

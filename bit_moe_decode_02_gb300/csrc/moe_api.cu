@@ -15,6 +15,7 @@
 // with its kernel); both hold exactly the caller's bytes, reordered.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -73,8 +74,7 @@ struct moe_handle {
     size_t dec_smem = 0;                      // dynamic shared memory of the decode kernel
     float* part = nullptr;                    // [G][H][4]
     unsigned long long* cnt = nullptr;        // xcnt, done (only grow)
-    // MXFP4 decode: tensor maps of the down projections ([L][2], 128 bytes each),
-    // split-unit partials and flags, the layer's x terms
+    // MXFP4 decode: split-unit partials and flags, the layer's x terms
     float* gpart = nullptr;
     unsigned* pflag = nullptr;
     uint8_t* xt = nullptr;
@@ -90,6 +90,13 @@ struct moe_handle {
     uint8_t* b_hsf = nullptr;
     float* b_y = nullptr;
     int last_bM = 0, last_bk = 0;             // M and top_k of the last batched call
+    // in-kernel router: per layer W bf16 [E][H] then the bias bf16 [E]
+    // (rw_stride bytes a layer; allocated by the first moe_load_router), and
+    // the logits of the last call [max(max_tokens, 4)][E]
+    uint8_t* rw = nullptr;
+    size_t rw_stride = 0;
+    std::vector<char> rloaded;
+    float* rlog = nullptr;
     int* stats = nullptr;                     // distinct experts of the last call on each layer
     int* status = nullptr;
     // staging for moe_forward_host: [x][residual / out][logits] in pinned host
@@ -170,6 +177,8 @@ void free_handle(moe_handle* h)
     cudaFree(h->b_y);
     cudaFree(h->stats);
     cudaFree(h->status);
+    cudaFree(h->rw);
+    cudaFree(h->rlog);
     cudaFreeHost(h->st_host);
     delete h;
 }
@@ -267,6 +276,9 @@ cudaError_t launch_seq(const moe_handle* h, int layer0, int n, const float* logi
     if (h->mxfp4) {
         moe::DecodeTcParams p = tc_params(h, layer0, n);
         p.logits = logits;
+        p.router = logits ? nullptr : reinterpret_cast<const uint16_t*>(h->rw);
+        p.router_stride = (long long)h->rw_stride;
+        p.rlog = h->rlog;
         p.logits_stride = ls;
         p.x = static_cast<const uint16_t*>(x);
         p.x_stride = xs;
@@ -281,6 +293,9 @@ cudaError_t launch_seq(const moe_handle* h, int layer0, int n, const float* logi
     }
     moe::DecodeI4Params p = i4_params(h, layer0, n);
     p.logits = logits;
+    p.router = logits ? nullptr : reinterpret_cast<const uint16_t*>(h->rw);
+    p.router_stride = (long long)h->rw_stride;
+    p.rlog = h->rlog;
     p.logits_stride = ls;
     p.x = static_cast<const uint16_t*>(x);
     p.x_stride = xs;
@@ -435,6 +450,18 @@ bool device_accessible(const void* p)
     return a.type != cudaMemoryTypeHost || a.devicePointer == p;
 }
 
+// Router weights for the layers (layer0 + s) mod L, s < n, when the logits are
+// to be computed in the kernel (the caller passed none).
+int check_router(const moe_handle* h, int layer0, int n, const char* who)
+{
+    const int L = h->cfg.num_layers;
+    for (int s = 0; s < n && s < L; ++s)
+        if (!h->rloaded[(layer0 + s) % L])
+            return fail(MOE_ERR_NOT_LOADED, "%s: no router logits given and layer %d has no router weights "
+                        "(moe_load_router)", who, (layer0 + s) % L);
+    return MOE_OK;
+}
+
 int check_all_loaded(const moe_handle* h, const char* who)
 {
     for (int l = 0; l < h->cfg.num_layers; ++l)
@@ -451,8 +478,8 @@ int forward_impl(moe_handle* h, int layer, const void* x_bf16, const float* rout
         return rc;
     if (layer < 0 || layer >= h->cfg.num_layers)
         return fail(MOE_ERR_INVALID_ARG, "layer=%d out of range 0..%d", layer, h->cfg.num_layers - 1);
-    if (!x_bf16 || !router_logits || !out_bf16)
-        return fail(MOE_ERR_INVALID_ARG, "moe_forward: x, logits and out must not be NULL");
+    if (!x_bf16 || !out_bf16)
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward: x and out must not be NULL");
     if (!aligned16(x_bf16) || !aligned16(out_bf16) || !aligned16(router_logits))
         return fail(MOE_ERR_INVALID_ARG, "moe_forward: x, logits and out must be 16-byte aligned");
     const size_t nb = (size_t)M * h->cfg.hidden * 2;
@@ -460,8 +487,20 @@ int forward_impl(moe_handle* h, int layer, const void* x_bf16, const float* rout
         return fail(MOE_ERR_INVALID_ARG, "moe_forward: x overlaps out");
     if (!h->loaded[layer])
         return fail(MOE_ERR_NOT_LOADED, "moe_forward: layer %d has no experts loaded", layer);
+    if (!router_logits && (rc = check_router(h, layer, 1, "moe_forward")) != MOE_OK)
+        return rc;
     if (M > moe::kMaxTokens) {
         moe::BatchParams b = batch_params(h, layer);
+        if (!router_logits) {
+            // the router GEMV first, into the handle's logits buffer
+            cudaError_t e = moe::launch_router_gemv(static_cast<const uint16_t*>(x_bf16),
+                                                    reinterpret_cast<const uint16_t*>(h->rw + layer * h->rw_stride),
+                                                    M, h->cfg.hidden, h->cfg.num_experts, h->rlog,
+                                                    (cudaStream_t)stream);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "moe_forward (router) launch");
+            router_logits = h->rlog;
+        }
         b.logits = router_logits;
         b.x = static_cast<const uint16_t*>(x_bf16);
         b.resid = static_cast<uint16_t*>(out_bf16);
@@ -474,7 +513,7 @@ int forward_impl(moe_handle* h, int layer, const void* x_bf16, const float* rout
             return cuda_fail(e, "moe_forward (batched) launch");
         h->last_steps = 1;
         h->last_first_layer = layer;
-        h->last_launches = launches;
+        h->last_launches = launches + (router_logits == h->rlog ? 1 : 0);
         h->last_bM = M;
         h->last_bk = top_k;
         return MOE_OK;
@@ -546,6 +585,8 @@ int moe_create(const moe_config* cfg, moe_handle** out)
     h->st_bytes = h->st_off_l + Mx * E * sizeof(float);
     if ((rc = dev_alloc(&h->arena, h->layer_stride * c.num_layers, "expert weights")) ||
         (rc = dev_alloc(&h->stats, c.num_layers * sizeof(int), "stats")) ||
+        (rc = dev_alloc(&h->rlog, (size_t)std::max(c.max_tokens, moe::kMaxTokens) * E * sizeof(float),
+                        "router logits")) ||
         (rc = dev_alloc(&h->status, sizeof(int), "status"))) {
         free_handle(h);
         return rc;
@@ -572,6 +613,7 @@ int moe_create(const moe_config* cfg, moe_handle** out)
         return cuda_fail(e, "moe_create setup");
     }
     h->loaded.assign(c.num_layers, 0);
+    h->rloaded.assign(c.num_layers, 0);
     *out = h;
     g_err[0] = 0;
     return MOE_OK;
@@ -693,8 +735,8 @@ int moe_forward_host(moe_handle* h, int layer, const void* x_bf16, const float* 
     int rc = check_forward_args(h, M, top_k);
     if (rc != MOE_OK)
         return rc;
-    if (!x_bf16 || !router_logits || !out_bf16)
-        return fail(MOE_ERR_INVALID_ARG, "moe_forward_host: x, logits and out must not be NULL");
+    if (!x_bf16 || !out_bf16)
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_host: x and out must not be NULL");
     if (layer < 0 || layer >= h->cfg.num_layers)
         return fail(MOE_ERR_INVALID_ARG, "layer=%d out of range 0..%d", layer, h->cfg.num_layers - 1);
     if (!h->loaded[layer])
@@ -708,8 +750,10 @@ int moe_forward_host(moe_handle* h, int layer, const void* x_bf16, const float* 
     // call on this handle has completed (it synchronised before returning).
     std::memcpy(h->st_host, x_bf16, nb);
     std::memcpy(h->st_host + h->st_off_r, out_bf16, nb);
-    std::memcpy(h->st_host + h->st_off_l, router_logits, nl);
-    rc = moe_forward(h, layer, h->st_dev, reinterpret_cast<const float*>(h->st_dev + h->st_off_l), M, top_k,
+    if (router_logits)
+        std::memcpy(h->st_host + h->st_off_l, router_logits, nl);
+    rc = moe_forward(h, layer, h->st_dev,
+                     router_logits ? reinterpret_cast<const float*>(h->st_dev + h->st_off_l) : nullptr, M, top_k,
                      h->st_dev + h->st_off_r, stream);
     if (rc != MOE_OK)
         return rc;
@@ -731,13 +775,15 @@ int moe_forward_stack_steps(moe_handle* h, int n, void* resid_bf16, const float*
                     moe::kMaxTokens);
     if (n < 1)
         return fail(MOE_ERR_INVALID_ARG, "moe_forward_stack_steps: n=%d must be >= 1", n);
-    if (!resid_bf16 || !router_logits)
-        return fail(MOE_ERR_INVALID_ARG, "moe_forward_stack: resid and logits must not be NULL");
+    if (!resid_bf16)
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_stack: resid must not be NULL");
     if (!aligned16(resid_bf16) || !aligned16(router_logits))
         return fail(MOE_ERR_INVALID_ARG, "moe_forward_stack: resid and logits must be 16-byte aligned");
     if ((rc = check_all_loaded(h, "moe_forward_stack")) != MOE_OK)
         return rc;
     const int L = h->cfg.num_layers;
+    if (!router_logits && (rc = check_router(h, 0, L, "moe_forward_stack")) != MOE_OK)
+        return rc;
     if ((long long)n * L > (1ll << 30))
         return fail(MOE_ERR_INVALID_ARG, "moe_forward_stack_steps: n * L = %lld layer calls is too many",
                     (long long)n * L);
@@ -773,11 +819,12 @@ int moe_forward_steps(moe_handle* h, int n, int layer0, const void* x_bf16, cons
     if (n < 1 || layer0 < 0 || layer0 >= L)
         return fail(MOE_ERR_INVALID_ARG, "moe_forward_steps: n=%d must be >= 1 and layer0=%d in 0..%d", n, layer0,
                     L - 1);
-    if (!x_bf16 || !router_logits || !out_bf16)
-        return fail(MOE_ERR_INVALID_ARG, "moe_forward_steps: x, logits and out must not be NULL");
+    if (!x_bf16 || !out_bf16)
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_steps: x and out must not be NULL");
     if (!aligned16(x_bf16) || !aligned16(out_bf16) || !aligned16(router_logits))
         return fail(MOE_ERR_INVALID_ARG, "moe_forward_steps: x, logits and out must be 16-byte aligned");
-    if (!device_accessible(x_bf16) || !device_accessible(router_logits) || !device_accessible(out_bf16))
+    if (!device_accessible(x_bf16) || (router_logits && !device_accessible(router_logits)) ||
+        !device_accessible(out_bf16))
         return fail(MOE_ERR_INVALID_ARG, "moe_forward_steps: x, logits and out must be device memory or "
                                          "page-locked host memory mapped at the same address");
     const size_t nb = (size_t)n * M * h->cfg.hidden * 2;
@@ -786,6 +833,8 @@ int moe_forward_steps(moe_handle* h, int n, int layer0, const void* x_bf16, cons
     for (int s = 0; s < n && s < L; ++s)
         if (!h->loaded[(layer0 + s) % L])
             return fail(MOE_ERR_NOT_LOADED, "moe_forward_steps: layer %d has no experts loaded", (layer0 + s) % L);
+    if (!router_logits && (rc = check_router(h, layer0, n, "moe_forward_steps")) != MOE_OK)
+        return rc;
     const long long xs = (long long)M * h->cfg.hidden * 2, ls = (long long)M * h->cfg.num_experts * sizeof(float);
     cudaError_t e = launch_seq(h, layer0, n, router_logits, ls, x_bf16, xs, out_bf16, xs, nullptr, 0, M, top_k,
                                (cudaStream_t)stream);
@@ -806,11 +855,13 @@ int moe_debug_stack_trace(moe_handle* h, void* resid_bf16, const float* router_l
     if (M > moe::kMaxTokens)
         return fail(MOE_ERR_UNSUPPORTED, "moe_debug_stack_trace: M=%d > %d; the stack runs the decode kernel only", M,
                     moe::kMaxTokens);
-    if (!resid_bf16 || !router_logits || !trace_bf16)
+    if (!resid_bf16 || !trace_bf16)
         return fail(MOE_ERR_INVALID_ARG, "moe_debug_stack_trace: NULL argument");
     if (!aligned16(resid_bf16) || !aligned16(router_logits))
         return fail(MOE_ERR_INVALID_ARG, "moe_debug_stack_trace: resid and logits must be 16-byte aligned");
     if ((rc = check_all_loaded(h, "moe_debug_stack_trace")) != MOE_OK)
+        return rc;
+    if (!router_logits && (rc = check_router(h, 0, h->cfg.num_layers, "moe_debug_stack_trace")) != MOE_OK)
         return rc;
     const int L = h->cfg.num_layers;
     cudaStream_t s = (cudaStream_t)stream;
@@ -818,8 +869,8 @@ int moe_debug_stack_trace(moe_handle* h, void* resid_bf16, const float* router_l
     uint8_t* tr = static_cast<uint8_t*>(trace_bf16);
     cudaError_t e = cudaMemcpyAsync(tr, resid_bf16, nb, cudaMemcpyDeviceToDevice, s);
     for (int l = 0; l < L && e == cudaSuccess; ++l) {
-        e = launch_decode(h, l, router_logits + (size_t)l * M * h->cfg.num_experts, nullptr, resid_bf16, M, top_k,
-                          s);
+        e = launch_decode(h, l, router_logits ? router_logits + (size_t)l * M * h->cfg.num_experts : nullptr,
+                          nullptr, resid_bf16, M, top_k, s);
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(tr + (size_t)(l + 1) * nb, resid_bf16, nb, cudaMemcpyDeviceToDevice, s);
     }
@@ -828,6 +879,43 @@ int moe_debug_stack_trace(moe_handle* h, void* resid_bf16, const float* router_l
     h->last_steps = L;
     h->last_first_layer = 0;
     h->last_launches = L;
+    return MOE_OK;
+}
+
+int moe_load_router(moe_handle* h, int layer, const void* w_bf16, const void* bias_bf16)
+{
+    if (!h || !w_bf16)
+        return fail(MOE_ERR_INVALID_ARG, "moe_load_router: handle and weights must not be NULL");
+    const moe_config& c = h->cfg;
+    if (layer < 0 || layer >= c.num_layers)
+        return fail(MOE_ERR_INVALID_ARG, "moe_load_router: layer=%d out of range 0..%d", layer, c.num_layers - 1);
+    const size_t wb = (size_t)c.num_experts * c.hidden * 2, bb = (size_t)c.num_experts * 2;
+    cudaError_t e;
+    if (!h->rw) {
+        h->rw_stride = align_up(wb + bb, 256);
+        int rc = dev_alloc(&h->rw, h->rw_stride * c.num_layers, "router weights");
+        if (rc != MOE_OK)
+            return rc;
+    }
+    uint8_t* dst = h->rw + (size_t)layer * h->rw_stride;
+    if ((e = cudaMemcpy(dst, w_bf16, wb, cudaMemcpyDefault)) != cudaSuccess ||
+        (e = bias_bf16 ? cudaMemcpy(dst + wb, bias_bf16, bb, cudaMemcpyDefault) : cudaMemset(dst + wb, 0, bb)) !=
+            cudaSuccess)
+        return cuda_fail(e, "moe_load_router copy");
+    h->rloaded[layer] = 1;
+    return MOE_OK;
+}
+
+int moe_debug_router_logits(moe_handle* h, float* out_dev, int M, void* stream)
+{
+    if (!h || !out_dev)
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_router_logits: NULL argument");
+    if (M < 1 || M > std::max(h->cfg.max_tokens, moe::kMaxTokens))
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_router_logits: M=%d out of range", M);
+    cudaError_t e = cudaMemcpyAsync(out_dev, h->rlog, (size_t)M * h->cfg.num_experts * sizeof(float),
+                                    cudaMemcpyDeviceToDevice, (cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "moe_debug_router_logits");
     return MOE_OK;
 }
 

@@ -794,6 +794,46 @@ cudaError_t launch_repack_tiles(const uint8_t* codes, const uint8_t* scales, int
     return cudaGetLastError();
 }
 
+// Router GEMV of the batched path: logits [M][E] fp32 from x [M][H] bf16 and
+// the router rows w [E][H] bf16 followed by the bias [E], one warp per logit.
+// The arithmetic is the decode kernel's: a lane-strided fp32 FMA chain over
+// 8-element vectors (lo half before hi), a fixed butterfly, then the bias, so
+// both paths give the same bits for the same x.
+__global__ void router_gemv_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w, int M, int H,
+                                   int E, float* __restrict__ out)
+{
+    const long long g = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (g >= (long long)M * E)
+        return;
+    const int m = (int)(g / E), e = (int)(g % E);
+    const uint4* xv = reinterpret_cast<const uint4*>(x + (size_t)m * H);
+    const uint4* wv = reinterpret_cast<const uint4*>(w + (size_t)e * H);
+    float acc = 0.f;
+    for (int i = lane; i < H / 8; i += 32) {
+        const uint4 x4 = __ldg(xv + i), w4 = __ldg(wv + i);
+        const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w}, ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            acc = fmaf(__uint_as_float(xw[c] << 16), __uint_as_float(ww[c] << 16), acc);
+            acc = fmaf(__uint_as_float(xw[c] & 0xffff0000u), __uint_as_float(ww[c] & 0xffff0000u), acc);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+        acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0)
+        out[(size_t)m * E + e] = acc + bf16f(w[(size_t)E * H + e]);
+}
+
+cudaError_t launch_router_gemv(const uint16_t* x, const uint16_t* w, int M, int H, int E, float* out,
+                               cudaStream_t stream)
+{
+    const long long warps = (long long)M * E;
+    router_gemv_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(x, w, M, H, E, out);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_route(const float* logits, int M, int E, int k, int* idx, float* w,
                          cudaStream_t stream)
 {

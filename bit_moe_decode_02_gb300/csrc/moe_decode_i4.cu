@@ -217,10 +217,8 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
             reinterpret_cast<const uint8_t*>(p.dn_bias) + (long long)layer * p.bias_stride) : nullptr;
 
         if (warp < kCw) {
-            // ---- routing (warp m: token m), the distinct experts, the weight table
-            if (warp < M)
-                rt::warp_topk_fit(logits + (size_t)warp * p.E, p.E, p.k, si.sel[warp], si.wt[warp]);
-            // token statistics (warp 4 + m: token m): largest |x|, and 1 / rms for the normalised input
+            // ---- token statistics (warp 4 + m: token m): largest |x|, and 1 / rms for
+            // the normalised input
             if (warp >= 4 && warp - 4 < M) {
                 const int m = warp - 4;
                 const uint16_t* row = (xin ? xin : resid) + (size_t)m * H;
@@ -250,6 +248,51 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                     si.xsh[m] = amax > 0.f ? 14 - ilog2f(amax) : 0;
                 }
             }
+            const float* lgp = logits;
+            if (p.router) {
+                // ---- router GEMV: this CTA's logits (experts e = b, b + G, ..., one
+                // (token, expert) pair a warp) from the layer input (x, or the
+                // normalised residual rounded to bf16 as below), with the decode and
+                // batched paths' summation order; then a grid barrier publishes them
+                cw_barrier();
+                const uint16_t* rw = reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(p.router) +
+                                                                       (long long)layer * p.router_stride);
+                const int nre = b < p.E ? (p.E - 1 - b) / G + 1 : 0;
+                if (warp < M * nre) {
+                    const int m = warp % M, e = b + (warp / M) * G;
+                    const uint4* xv = reinterpret_cast<const uint4*>((xin ? xin : resid) + (size_t)m * H);
+                    const uint4* wv = reinterpret_cast<const uint4*>(rw + (size_t)e * H);
+                    const float inv = si.xinv[m];
+                    float acc = 0.f;
+                    for (int i = lane; i < H / 8; i += 32) {
+                        const uint4 x4 = __ldcg(xv + i), w4 = __ldg(wv + i);
+                        const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w}, ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            float lo = __uint_as_float(xw[c] << 16), hi = __uint_as_float(xw[c] & 0xffff0000u);
+                            if (!xin) {
+                                lo = bf16f(f2bf16_rne(lo * inv));
+                                hi = bf16f(f2bf16_rne(hi * inv));
+                            }
+                            acc = fmaf(lo, __uint_as_float(ww[c] << 16), acc);
+                            acc = fmaf(hi, __uint_as_float(ww[c] & 0xffff0000u), acc);
+                        }
+                    }
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1)
+                        acc += __shfl_xor_sync(0xffffffffu, acc, off);
+                    if (lane == 0)
+                        p.rlog[m * p.E + e] = acc + bf16f(__ldg(rw + (size_t)p.E * H + e));
+                }
+                cw_barrier();
+                if (tid == 0)
+                    grid_sync_i4(p.done, G, p.spin_limit, p.status, false);
+                cw_barrier();
+                lgp = p.rlog;
+            }
+            // ---- routing (warp m: token m), the distinct experts, the weight table
+            if (warp < M)
+                rt::warp_topk_fit(lgp + (size_t)warp * p.E, p.E, p.k, si.sel[warp], si.wt[warp]);
             cw_barrier();
             if (warp == 0) {
                 uint32_t bits = 0;

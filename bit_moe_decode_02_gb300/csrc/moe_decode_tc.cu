@@ -562,6 +562,8 @@ struct TcSmem {
     uint64_t routed, xfull;      // routing done; the layer's x terms copied in
     uint64_t hsfull;             // the split unit's h' terms copied in
     uint64_t planbar;            // the plan table is written
+    uint64_t rlogw, xready;      // in-kernel router: this CTA's logits stored; every CTA's published
+    uint64_t rbar;               // in-kernel router: this CTA's router rows copied in
     unsigned epoch;              // this call's tag for the exchange flags (call index + 1)
     uint32_t tmem_base;
     int sel[kMaxTokens][kMaxTopK];
@@ -583,6 +585,71 @@ struct TcSmem {
 extern __shared__ __align__(1024) uint8_t ring[];
 __shared__ __align__(8) TcSmem sh;
 __shared__ DecodeTcParams g_p;
+
+// The router GEMV of one CTA: logits of experts e = b, b + G, ... (their
+// router rows already in shared memory at wsm, H bf16 each) for tokens m = m0,
+// m0 + 3, ... (one warp), written to rlog [M][E].  The input is the layer
+// input the x terms are cut from: x, or the normalised residual rounded to
+// bf16 exactly as the x terms round it; the warp stages it in shared memory at
+// xsm, so that the product loop keeps few registers.  Each logit is a
+// lane-strided fp32 FMA chain and a fixed butterfly (the same bits on every
+// run), plus the bias.
+__device__ __forceinline__ void router_logits(const uint8_t* wsm, uint16_t* xsm, const uint16_t* bias,
+                                              const uint16_t* x, const uint16_t* resid, int H, int E, int M, int b,
+                                              int G, int m0, int lane, float* rlog)
+{
+#pragma unroll 1
+    for (int m = m0; m < M; m += 3) {
+        {
+            uint4 rowv[kRowVec];
+            load_row((x ? x : resid) + (size_t)m * H, H, lane, rowv);
+            float inv = 1.f;
+            if (!x) {
+                uint32_t ab;
+                inv = row_stats(rowv, H, true, ab);
+            }
+#pragma unroll
+            for (int z = 0; z < kRowVec; ++z) {
+                const int i = lane + 32 * z;
+                if (i < H / 8) {
+                    uint4 u = rowv[z];
+                    if (!x) {
+                        uint32_t* w = &u.x;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint32_t lo = f2bf16_rne(__uint_as_float(w[c] << 16) * inv);
+                            const uint32_t hi = f2bf16_rne(__uint_as_float(w[c] & 0xffff0000u) * inv);
+                            w[c] = lo | (hi << 16);
+                        }
+                    }
+                    reinterpret_cast<uint4*>(xsm)[i] = u;
+                }
+            }
+        }
+        __syncwarp();
+#pragma unroll 1
+        for (int e = b, r = 0; e < E; e += G, ++r) {
+            const uint4* wv = reinterpret_cast<const uint4*>(wsm + (size_t)r * H * 2);
+            float acc = 0.f;
+#pragma unroll 1
+            for (int i = lane; i < H / 8; i += 32) {
+                const uint4 x4 = reinterpret_cast<const uint4*>(xsm)[i], w4 = wv[i];
+                const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w}, ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    acc = fmaf(__uint_as_float(xw[c] << 16), __uint_as_float(ww[c] << 16), acc);
+                    acc = fmaf(__uint_as_float(xw[c] & 0xffff0000u), __uint_as_float(ww[c] & 0xffff0000u), acc);
+                }
+            }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1)
+                acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (lane == 0)
+                rlog[m * E + e] = acc + bf16f(__ldg(bias + e));
+        }
+        __syncwarp();
+    }
+}
 
 // One layer call of a launch for one role group: `group` 0 = the routing,
 // producer and MMA-issuer warps (0, 1, 6), 1 = the x-term / epilogue warps
@@ -638,11 +705,41 @@ __device__ __forceinline__ void decode_call(const int call)
                                                      (long long)call * p.out_f32_stride) : nullptr)
 
     if (GROUP == 0) {
+        const float* lgp = cl_logits;
+        if (p.router) {
+            // ---- router GEMV: logits of this CTA's experts e = b, b + G, ... for
+            // every token (token m on the (m % 3)-th of warps 0, 1, 6), from the
+            // layer input the x terms are cut from; the x-term publication carries
+            // them to every CTA, and the routing waits for it
+            const uint16_t* rw = reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(p.router) +
+                                                                   (long long)layer * p.router_stride);
+            // the ring is idle until the routing is done: its start holds this CTA's
+            // router rows (one bulk copy each), then one x row per warp
+            const int nre = b < p.E ? (p.E - 1 - b) / G + 1 : 0;
+            if (nre > 0) {
+                if (warp == 0 && lane == 0) {
+                    mbar_expect_tx(&sh.rbar, (uint32_t)(nre * p.H * 2));
+                    for (int r = 0; r < nre; ++r)
+                        bulk_copy(ring + (size_t)r * p.H * 2, rw + (size_t)(b + r * G) * p.H, (uint32_t)p.H * 2,
+                                  &sh.rbar);
+                }
+                const int wi = warp == kMmaWarpB ? 2 : warp;
+                uint16_t* xsm = reinterpret_cast<uint16_t*>(ring + (size_t)(nre + wi) * p.H * 2);
+                mbar_wait(&sh.rbar, call & 1, p.status);
+                router_logits(ring, xsm, rw + (size_t)p.E * p.H, cl_x, cl_resid, p.H, p.E, M, b, G, wi, lane, p.rlog);
+                fence_proxy_async_smem();   // the ring's next writers are bulk copies
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sh.rlogw);
+            mbar_wait(&sh.xready, call & 1, p.status);
+            lgp = p.rlog;
+        }
         // ---- routing (warps 0, 1, 6): token m on the (m % 3)-th of them, then the
         // distinct experts in ascending order
 #pragma unroll 1
         for (int m = warp == kMmaWarpB ? 2 : warp; m < M; m += 3)
-            rt::warp_topk_fit(cl_logits + (size_t)m * p.E, p.E, p.k, sh.sel[m], sh.wt[m]);
+            rt::warp_topk_fit(lgp + (size_t)m * p.E, p.E, p.k, sh.sel[m], sh.wt[m]);
         route_barrier();
         if (warp == 0) {
             uint32_t bits = 0;
@@ -740,6 +837,8 @@ __device__ __forceinline__ void decode_call(const int call)
             // (the first call of the launch learns where the count stands; later
             // calls add without waiting for the old value)
             unsigned long long tgt;
+            if (p.router)
+                mbar_wait(&sh.rlogw, call & 1, p.status);   // this CTA's logits are stored
             if (call == 0) {
                 const unsigned long long old = atom_add_release_u64(p.xcnt, 1ull);
                 tgt = count_target(old, G);
@@ -758,6 +857,8 @@ __device__ __forceinline__ void decode_call(const int call)
                     break;
                 }
             }
+            if (p.router)
+                mbar_arrive(&sh.xready);   // every CTA's logits are visible: the routing may read them
             // the whole layer's x terms into shared memory, once
             asm volatile("fence.proxy.async.global;" ::: "memory");   // published x terms -> bulk reads
             const uint32_t ab = (uint32_t)KSH * atom, sb = (uint32_t)CHH * kSfChunk;
@@ -1414,6 +1515,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
         mbar_init(&sh.xfull, 1);
         mbar_init(&sh.hsfull, 1);
         mbar_init(&sh.planbar, 1);
+        mbar_init(&sh.rlogw, 3);   // warps 0, 1 and 6
+        mbar_init(&sh.xready, 1);
+        mbar_init(&sh.rbar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {

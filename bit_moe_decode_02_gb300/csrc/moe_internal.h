@@ -169,6 +169,13 @@ struct DecodeTcParams {
     int smem_bytes;             // dynamic shared memory of the layer kernel
     int spin_limit;             // polls before a cross-CTA wait gives up (kSpinLimit by default)
     int skip_cta;               // debug: this CTA skips its grid-barrier arrival (-1: none)
+    // In-kernel router: layer 0's router weights bf16 [E][H] followed by the
+    // bias bf16 [E] (router_stride bytes from one layer's to the next), or
+    // nullptr when the caller gives the logits.  The call's logits go to rlog
+    // [kMaxTokens][E] (the last call's stay there).
+    const uint16_t* router;
+    long long router_stride;
+    float* rlog;
 };
 constexpr int kSpinLimit = 1 << 24;
 
@@ -210,6 +217,9 @@ struct DecodeI4Params {
     int H, I, E, M, k, group;
     int smem_bytes;
     int spin_limit, skip_cta;
+    const uint16_t* router;     // in-kernel router (as for the MXFP4 decode), or nullptr
+    long long router_stride;
+    float* rlog;
 };
 constexpr int kI4Slot = 18432;    // one stage: up to 16 KB of codes, then up to 2 KB of scales
 constexpr int kI4Codes = 16384;
@@ -225,6 +235,10 @@ cudaError_t launch_dequant_i4(const uint8_t* w, int H, int I, int group, int pro
 // Debug kernels.
 // One expert projection of the tile layout back to fp32 in caller row order
 // (gate_up: interleave = I, rows [0, I) gate and [I, 2I) up; down: 0).
+// Router GEMV logits [M][E] = x [M][H] . W^T + b (w: W bf16 [E][H] then b [E]),
+// fp32 with the decode kernel's summation order.
+cudaError_t launch_router_gemv(const uint16_t* x, const uint16_t* w, int M, int H, int E, float* out,
+                               cudaStream_t stream);
 cudaError_t launch_dequant_tiles(const uint8_t* tiles, int N, int K, int interleave, int kmajor, float* out,
                                  cudaStream_t stream);
 cudaError_t launch_dequant(int fmt, int group, const uint8_t* slabs, int N, int K, int slab_bytes,

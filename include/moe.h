@@ -133,10 +133,31 @@ int moe_load_experts(moe_handle* h, int layer,
                      const void* dn_codes, const void* dn_scales, const void* dn_bias,
                      void* stream);
 
+/* Router weights of one layer, for calls that leave the logits to the
+ * library (router_logits == NULL): logits[m][e] = b[e] + sum_h x[m][h] W[e][h]
+ * over the layer's input x (the same bf16 values the experts see; in the
+ * stack, the normalised residual), accumulated in fp32 -- the MoE block's
+ * gate, whose top-k the pages keep on the GPU ("Amortizing the per-token
+ * host-sync setup tax in fused all-layer q4 decode on Apple M1 Ultra",
+ * section 3; "Sovereign gpt-oss-20B (MXFP4) on Apple Silicon", section 1,
+ * top-4 of 32 experts).  w_bf16 [E][H], bias_bf16 [E] or NULL (zero); host or
+ * device memory, copied before the call returns.  Summation order, the same
+ * in every kernel (so the decode, int4 and batched paths give the same bits):
+ * for each 8-element vector i = lane, lane + 32, ... of the row (lane =
+ * 0..31), its elements in order, fused multiply-adds into the lane's sum;
+ * then a butterfly over the 32 lanes; then + b[e].  The decode kernels
+ * compute the logits inside the layer launch (each CTA a few experts, shared
+ * through the grid-wide exchange that publishes the layer's input), so a
+ * whole decode step with data-dependent routing stays one launch; the batched
+ * path runs one more small kernel first.  A layer may be reloaded. */
+int moe_load_router(moe_handle* h, int layer, const void* w_bf16, const void* bias_bf16);
+
 /* One layer.  x bf16 [M][H] (the layer input, already normalised),
- * router_logits fp32 [M][E], out bf16 [M][H]: the residual r on entry and
- * r + MoE(x) on return.  1 <= M <= max_tokens, 1 <= top_k <= max_top_k.
- * x must not overlap out (checked).  All three are device pointers.
+ * router_logits fp32 [M][E] -- or NULL: computed from x by the layer's
+ * router weights (moe_load_router; MOE_ERR_NOT_LOADED without them) --,
+ * out bf16 [M][H]: the residual r on entry and r + MoE(x) on return.
+ * 1 <= M <= max_tokens, 1 <= top_k <= max_top_k.  x must not overlap out
+ * (checked).  All three are device pointers.
  * M <= 4 runs the decode kernel (one persistent launch).  M > 4 runs the
  * batched path: per-expert grouped GEMMs on the tensor cores
  * (tcgen05.mma kind::mxf4) with x and h quantised to MXFP4 per 32 along K by
@@ -148,12 +169,18 @@ int moe_load_experts(moe_handle* h, int layer,
 int moe_forward(moe_handle* h, int layer, const void* x_bf16, const float* router_logits,
                 int M, int top_k, void* out_bf16, void* stream);
 
+/* Debug: the router logits of the last call that computed them (the last
+ * layer call of a decode launch, or the batched call), fp32 [M][E], copied to
+ * the device buffer out_dev on `stream`. */
+int moe_debug_router_logits(moe_handle* h, float* out_dev, int M, void* stream);
+
 /* The same layer with host buffers (any host memory, pinned or not): packs x,
  * the residual and the logits into the handle's pinned staging buffer, which
  * is mapped into the device's address space; the layer kernel reads its
  * inputs from it and writes its result into it directly over the host-device
  * link (no separate copies).  Synchronises `stream`, then copies the result
- * into out_bf16.  Argument checks as for moe_forward. */
+ * into out_bf16.  Argument checks as for moe_forward; router_logits may be
+ * NULL (the in-kernel router). */
 int moe_forward_host(moe_handle* h, int layer, const void* x_bf16, const float* router_logits,
                      int M, int top_k, void* out_bf16, void* stream);
 
@@ -166,8 +193,10 @@ int moe_forward_host(moe_handle* h, int layer, const void* x_bf16, const float* 
  * normalised input is this library's reading (a literal x + MoE(x) chain
  * overflows within a few layers on these value distributions).
  * resid bf16 [M][H] holds r_0 on entry and r_L on return; logits fp32
- * [L][M][E].  Layer l+1 reads its logits only after layer l's output is
- * complete.  Device pointers.  One persistent launch for all L layers (grid
+ * [L][M][E], or NULL: each layer's logits from its router weights applied to
+ * x_l (moe_load_router, every layer), so that the routing of layer l+1
+ * depends on the output of layer l inside the one launch.  Layer l+1 reads
+ * its logits only after layer l's output is complete.  Device pointers.  One persistent launch for all L layers (grid
  * barriers between them), both formats.  Decode sizes only: M <= 4 (else
  * MOE_ERR_UNSUPPORTED). */
 int moe_forward_stack(moe_handle* h, void* resid_bf16, const float* router_logits,
@@ -177,7 +206,8 @@ int moe_forward_stack(moe_handle* h, void* resid_bf16, const float* router_logit
  * through all L layers; P2's "all decode tokens into a single command
  * buffer"): step t runs the L layers of moe_forward_stack on its own residual
  * resid[t] (bf16 [n][M][H]: r_0 of step t on entry, its r_L on return) with
- * logits[t] (fp32 [n][L][M][E]), steps one after another, exactly as n
+ * logits[t] (fp32 [n][L][M][E], or NULL: the in-kernel router, as for
+ * moe_forward_stack), steps one after another, exactly as n
  * moe_forward_stack calls in that order would (bit-identical results).  Each
  * layer call reads its logits only after the previous call's output is
  * complete.  Device pointers, 16-byte aligned; decode sizes only (M <= 4);
@@ -187,7 +217,8 @@ int moe_forward_stack_steps(moe_handle* h, int n, void* resid_bf16, const float*
 
 /* n single-layer decode steps in sequence: step s runs resident layer
  * (layer0 + s) mod L on x[s], logits[s] and out[s] (x bf16 [n][M][H],
- * router_logits fp32 [n][M][E], out bf16 [n][M][H]: the residual of each step
+ * router_logits fp32 [n][M][E] or NULL for the in-kernel router, out bf16
+ * [n][M][H]: the residual of each step
  * on entry, r + MoE(x) on return), exactly as n moe_forward calls in that order
  * would (bit-identical results).  Step s + 1 reads its routing and inputs only
  * after step s's output is complete.  One persistent launch for all n steps,
@@ -242,9 +273,10 @@ int moe_debug_mx_quantize(const float* in, long long n, unsigned char* codes,
 int moe_debug_batched_h(moe_handle* h, unsigned char* codes, unsigned char* scales, void* stream);
 
 /* Debug: the expert stack run layer by layer with the same kernels as
- * moe_forward_stack (no graph), recording the residual after every layer.
- * resid bf16 [M][H] is updated in place as in moe_forward_stack; trace bf16
- * [L+1][M][H] device buffer receives r_0 .. r_L. */
+ * moe_forward_stack (one launch per layer), recording the residual after
+ * every layer.  resid bf16 [M][H] is updated in place as in
+ * moe_forward_stack; trace bf16 [L+1][M][H] device buffer receives r_0 ..
+ * r_L.  router_logits NULL: the in-kernel router, as in moe_forward_stack. */
 int moe_debug_stack_trace(moe_handle* h, void* resid_bf16, const float* router_logits, int M,
                           int top_k, void* trace_bf16, void* stream);
 
