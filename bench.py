@@ -360,6 +360,11 @@ def run_ours(args):
         for M in (1, 4):
             extra[f"stack24_steps_m{M}"] = measure_stack_steps(moe, h, synth.GPTOSS_STACK, L, M,
                                                                args.extra_steps, 4)
+        for l in range(L):
+            moe.moe_load_router(h, l, *synth.router_tensors(synth.GPTOSS_STACK, l))
+        for M in (1, 4):
+            extra[f"stack24_router_m{M}"] = measure_stack_steps(moe, h, synth.GPTOSS_STACK, L, M,
+                                                                args.extra_steps, 4, router=True)
         extra["m_sweep"] = measure_m_sweep(moe, h, shape, L, max(args.extra_steps, 64))
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -406,11 +411,12 @@ def run_ours(args):
     return 0
 
 
-def measure_stack_steps(moe, h, shape, L, M, steps, warmup):
+def measure_stack_steps(moe, h, shape, L, M, steps, warmup, router=False):
     """Tokens/s of the expert stack with every step of the timed run in ONE
     launch (moe_forward_stack_steps: steps x L layer calls, each step on its own
     fresh residual and logits, each layer reading its logits only after the
-    previous layer's output is complete)."""
+    previous layer's output is complete).  With ``router`` the logits are not
+    given: every layer computes them from its own input inside the launch."""
     import torch
     k = shape.top_k
     n = warmup + steps
@@ -418,12 +424,12 @@ def measure_stack_steps(moe, h, shape, L, M, steps, warmup):
     rd = torch.from_numpy(np.stack([r for _, r, _ in ins]).view(np.int16)).cuda()
     ld = torch.from_numpy(np.ascontiguousarray(np.stack([lg for _, _, lg in ins]))).cuda()
     stream = torch.cuda.current_stream()
-    moe.moe_forward_stack_steps(h, warmup, rd[0], ld[0], M, k, stream)
+    moe.moe_forward_stack_steps(h, warmup, rd[0], None if router else ld[0], M, k, stream)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
         ev0.record(stream)
-        moe.moe_forward_stack_steps(h, steps, rd[warmup], ld[warmup], M, k, stream)
+        moe.moe_forward_stack_steps(h, steps, rd[warmup], None if router else ld[warmup], M, k, stream)
         ev1.record(stream)
         torch.cuda.synchronize()
     ms = ev0.elapsed_time(ev1)
@@ -433,7 +439,8 @@ def measure_stack_steps(moe, h, shape, L, M, steps, warmup):
     us = 1e3 * ms / steps
     peak, kind = measured_peaks()
     gbs = nbytes / (us / 1e6) / 1e9
-    return {"workload": f"{shape.name}, M={M}, {steps} steps x {L} layers in one launch",
+    rt = ", router GEMV in the launch (logits from each layer's input)" if router else ""
+    return {"workload": f"{shape.name}, M={M}, {steps} steps x {L} layers in one launch{rt}",
             "metric": "tokens/s of the expert stack", "value": M * 1e6 / us, "unit": "tok/s",
             "us_per_step": us, "us_per_layer": us / L, "steps": steps, "warmup": warmup,
             "bytes_per_step": nbytes, "gbs": gbs, "frac_of_peak": gbs / peak, "peak": peak, "peak_kind": kind,

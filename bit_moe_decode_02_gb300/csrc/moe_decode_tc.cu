@@ -577,6 +577,7 @@ struct TcSmem {
     unsigned long long ends[kSlots];      // producer: ring position after each stage in flight
     RoleState role[4];                    // producer, MMA issuer A, MMA issuer B, epilogue
     int gbase, ubase, npc;                // gate/up items, whole units and split-unit calls so far
+    uint16_t* cresid;                     // the call's residual buffer
     unsigned long long dtgt, xtgt;        // targets of the last grid barrier and x-term count
 };
 
@@ -651,6 +652,14 @@ __device__ __forceinline__ void router_logits(const uint8_t* wsm, uint16_t* xsm,
     }
 }
 
+// The residual buffer of call c: resid + (c / resid_every) * resid_stride
+// (kept in shared memory for the call, so the per-use path has no division).
+__device__ __forceinline__ uint16_t* call_resid(const DecodeTcParams& p, int c)
+{
+    return reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(p.resid) +
+                                       (long long)(c / p.resid_every) * p.resid_stride);
+}
+
 // One layer call of a launch for one role group: `group` 0 = the routing,
 // producer and MMA-issuer warps (0, 1, 6), 1 = the x-term / epilogue warps
 // (2..5), 2 = the combiner warp (7).  Each group runs its own loop over the
@@ -699,8 +708,7 @@ __device__ __forceinline__ void decode_call(const int call)
                                                  (long long)call * p.logits_stride)
 #define cl_x (p.x ? reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(p.x) + \
                                                       (long long)call * p.x_stride) : nullptr)
-#define cl_resid reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(p.resid) + \
-                                             (long long)(call / p.resid_every) * p.resid_stride)
+#define cl_resid sh.cresid
 #define cl_f32 (p.out_f32 ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(p.out_f32) + \
                                                      (long long)call * p.out_f32_stride) : nullptr)
 
@@ -1448,6 +1456,7 @@ __device__ __forceinline__ void decode_call(const int call)
         }
         __syncthreads();
         if (tid == 0) {
+            sh.cresid = call_resid(p, call + 1);   // every thread is past this call's last use
             red_add_release_u64(p.done, 1ull);
             sh.dtgt += (unsigned long long)G;
             wait_count(p.done, sh.dtgt, p.spin_limit, p.status);
@@ -1500,6 +1509,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
         for (int r = 0; r < 4; ++r)
             sh.role[r] = RoleState{};
         sh.gbase = sh.ubase = sh.npc = 0;
+        sh.cresid = call_resid(p, 0);
         for (int i = 0; i < kSlots; ++i) {
             mbar_init(&sh.full[i], 1);
             mbar_init(&sh.empty[i], 2);   // both MMA issuers release every stage
