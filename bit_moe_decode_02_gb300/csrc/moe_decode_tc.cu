@@ -73,7 +73,8 @@ constexpr int kTmemCols = 512;
 static_assert(kDnCol + 2 * kDnRegion <= kSfCol && kSfCol + 4 * kSfSet <= kTmemCols, "tensor memory");
 static_assert(kDnRegion % (kDnStageTiles * 32) == 0, "a region holds whole down stages");
 static_assert(kSfSet >= 8 * ((kGuSteps + 1) / 2), "a gate/up stage's A and B scale chunks fit a set");
-static_assert(kSfSet >= 4 * (kDnStageTiles + 1), "a down stage's scale chunks fit a set");
+static_assert(kSfSet == 32 && 4 * ((kDnStageTiles + 1) / 2) <= 24 && kSfSet / 2 + 4 * ((kGuSteps + 3) / 4) <= 24,
+              "an issuer's stage scale chunks use columns 0..23 of a set; 24..31 hold the h' scales");
 constexpr int kThreadsTc = 256;      // producer, MMA issuer A, 4 epilogue warps, MMA issuer B, combiner
 constexpr int kMmaWarpB = 6;
 constexpr int kCombineWarp = 7;
@@ -1065,6 +1066,11 @@ __device__ __forceinline__ void decode_call(const int call)
                         mbar_wait(&sh.hbar[ui & 1], (ui >> 1) & 1, p.status);
                     }
                     tc_fence_after();
+                    // the unit's h' scale chunk, copied once for all its down tiles into
+                    // columns no stage set uses (24..31 of set 0: the two h' buffers,
+                    // 24..27 of set 1: the split unit's)
+                    const uint32_t hsf = myset + (piece ? (uint32_t)kSfSet + 24u : 24u + 4u * ((ubase + i) & 1));
+                    tc_cp_sf(hsf, hb + 1024);
                     const uint32_t aid = (uint32_t)(2 * (t & 1));   // A scale bytes of k-step t in its chunk
                     const int tA = piece ? pl.ta : 0, tB = piece ? pl.tb : T2;
                     for (int ga = tA; ga < tB; ga += TG, ++kk) {
@@ -1084,18 +1090,17 @@ __device__ __forceinline__ void decode_call(const int call)
                                 mbar_wait(&sh.full[slot], (sc / kSlots) & 1, p.status);
                                 tc_fence_after();
                                 const uint32_t set = myset + (sfn++ & 1) * kSfSet;
-                                tc_cp_sf(set, hb + 1024);
 #pragma unroll
                                 for (int j = 0; j < (kDnStageTiles + 1) / 2; ++j)
                                     if (j0 + j < j1)
-                                        tc_cp_sf(set + 4 + 4 * j, st + n * kTileA + (j0 + j) * kSfChunk);
+                                        tc_cp_sf(set + 4 * j, st + n * kTileA + (j0 + j) * kSfChunk);
                                 const uint64_t da = smem_desc(st + j0 * kTileA, 128, 256), db = smem_desc(hb, 128, 256);
                                 const uint32_t dcol = dreg + (t2 - ga + j0) * nrows;
 #pragma unroll
                                 for (int j = 0; j < (kDnStageTiles + 1) / 2; ++j)
                                     if (j0 + j < j1)
                                         tc_mma_mxf4(dcol + j * nrows, da + (uint64_t)(j * (kTileA >> 4)), db,
-                                                    idesc | (aid << 29), set + 4 + 4 * j, set, 0u);
+                                                    idesc | (aid << 29), set + 4 * j, hsf, 0u);
                             }
                             tc_commit(&sh.empty[slot]);
                         }
