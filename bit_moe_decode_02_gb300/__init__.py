@@ -5,11 +5,11 @@ module turns torch tensors into pointers and streams and raises on a non-zero
 status.  There is no CPU fallback: if libmoe.so is missing the import of the
 library fails loudly (build it with ``python -m bit_moe_decode_02_gb300.build_ext``).
 
-The function names are the C names: moe_create, moe_load_experts, moe_forward,
-moe_forward_host, moe_forward_stack, moe_forward_stack_steps, moe_forward_steps,
-moe_load_router, moe_debug_router_logits, moe_get_status, moe_debug_dequant, moe_debug_route, moe_debug_stack_trace, moe_debug_forward_f32, moe_debug_set_wait,
-moe_last_bytes, moe_expert_bytes, moe_last_launches, moe_last_error, moe_forward_noalloc,
-moe_destroy.
+The function names are the C names: moe_create, moe_load_experts, moe_load_experts_ex,
+moe_forward, moe_forward_host, moe_forward_stack, moe_forward_stack_steps, moe_forward_steps,
+moe_load_router, moe_debug_router_logits, moe_get_status, moe_debug_dequant, moe_debug_route,
+moe_debug_stack_trace, moe_debug_forward_f32, moe_debug_set_wait, moe_last_bytes,
+moe_expert_bytes, moe_last_launches, moe_last_error, moe_forward_noalloc, moe_destroy.
 """
 from __future__ import annotations
 
@@ -29,9 +29,11 @@ MOE_ERR_DEVICE_TIMEOUT = -6
 MOE_ERR_DEVICE_FAULT = -7
 MOE_FMT_MXFP4 = 1
 MOE_FMT_INT4 = 2
+MOE_LOAD_GATE_UP_INTERLEAVED = 1
+MOE_LOAD_TRANSPOSED = 2
 
 # every symbol include/moe.h declares
-EXPORTS = ("moe_create", "moe_load_experts", "moe_forward", "moe_forward_host",
+EXPORTS = ("moe_create", "moe_load_experts", "moe_load_experts_ex", "moe_forward", "moe_forward_host",
            "moe_forward_stack", "moe_forward_stack_steps", "moe_forward_steps", "moe_load_router",
            "moe_debug_router_logits", "moe_get_status", "moe_debug_dequant", "moe_debug_route",
            "moe_debug_stack_trace", "moe_debug_mx_quantize", "moe_debug_batched_h",
@@ -68,6 +70,8 @@ def lib() -> ctypes.CDLL:
         L.moe_create.restype = i
         L.moe_load_experts.argtypes = [p, i, p, p, p, p, p, p, p]
         L.moe_load_experts.restype = i
+        L.moe_load_experts_ex.argtypes = [p, i, p, p, p, p, p, p, i, p]
+        L.moe_load_experts_ex.restype = i
         L.moe_forward.argtypes = [p, i, p, p, i, i, p, p]
         L.moe_forward.restype = i
         L.moe_forward_host.argtypes = [p, i, p, p, i, i, p, p]
@@ -159,6 +163,13 @@ def moe_load_experts(h, layer, gu_codes, gu_scales, gu_bias, dn_codes, dn_scales
     return _check(lib().moe_load_experts(h, layer, _ptr(gu_codes), _ptr(gu_scales), _ptr(gu_bias),
                                          _ptr(dn_codes), _ptr(dn_scales), _ptr(dn_bias),
                                          _stream(stream)))
+
+
+def moe_load_experts_ex(h, layer, gu_codes, gu_scales, gu_bias, dn_codes, dn_scales, dn_bias, flags,
+                        stream=None):
+    return _check(lib().moe_load_experts_ex(h, layer, _ptr(gu_codes), _ptr(gu_scales), _ptr(gu_bias),
+                                            _ptr(dn_codes), _ptr(dn_scales), _ptr(dn_bias), flags,
+                                            _stream(stream)))
 
 
 def moe_forward(h, layer, x, logits, M, top_k, out, stream=None):

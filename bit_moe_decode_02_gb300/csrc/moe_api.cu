@@ -638,9 +638,9 @@ long long moe_expert_bytes(const moe_handle* h)
 
 int moe_last_launches(const moe_handle* h) { return h ? h->last_launches : 0; }
 
-int moe_load_experts(moe_handle* h, int layer, const void* gu_codes, const void* gu_scales,
-                     const void* gu_bias, const void* dn_codes, const void* dn_scales,
-                     const void* dn_bias, void* stream)
+int moe_load_experts_ex(moe_handle* h, int layer, const void* gu_codes, const void* gu_scales,
+                        const void* gu_bias, const void* dn_codes, const void* dn_scales,
+                        const void* dn_bias, int flags, void* stream)
 {
     if (!h)
         return fail(MOE_ERR_INVALID_ARG, "moe_load_experts: handle is NULL");
@@ -650,28 +650,36 @@ int moe_load_experts(moe_handle* h, int layer, const void* gu_codes, const void*
         return fail(MOE_ERR_INVALID_ARG, "moe_load_experts: codes and scales must not be NULL");
     if (h->cfg.has_bias && (!gu_bias || !dn_bias))
         return fail(MOE_ERR_INVALID_ARG, "moe_load_experts: has_bias=1 but a bias pointer is NULL");
+    if (flags & ~(MOE_LOAD_GATE_UP_INTERLEAVED | MOE_LOAD_TRANSPOSED))
+        return fail(MOE_ERR_INVALID_ARG, "moe_load_experts_ex: unknown flags 0x%x", flags);
     cudaStream_t s = (cudaStream_t)stream;
     const moe_config& c = h->cfg;
     const int H = c.hidden, I = c.intermediate, E = c.num_experts;
+    const int blk = h->mxfp4 ? 32 : c.group, esz = h->mxfp4 ? 1 : 2;
+    const bool ilv = (flags & MOE_LOAD_GATE_UP_INTERLEAVED) != 0, tr = (flags & MOE_LOAD_TRANSPOSED) != 0;
     uint8_t* base = h->arena + (size_t)layer * h->layer_stride;
     // the caller's tensors are copied to a staging area first (they may be host
-    // memory), then reordered into the resident layout by a repack kernel
+    // memory), converted to the caller layout [N][K] with gate rows first if
+    // the flags say they are in another one (a second area takes each
+    // conversion's output), then reordered into the resident layout by a
+    // repack kernel
+    const size_t a_guc = align_up(h->gu_codes_b, 256), a_gus = align_up(h->gu_scales_b, 256);
+    const size_t a_dnc = align_up(h->dn_codes_b, 256), a_dns = align_up(h->dn_scales_b, 256);
+    const size_t a_gub = ilv && h->gu_bias_b ? align_up(h->gu_bias_b, 256) : 0;
+    const size_t st_bytes = a_guc + a_gus + a_dnc + a_dns + a_gub;
     uint8_t* staging = nullptr;
-    const size_t st_bytes = align_up(h->gu_codes_b, 256) + align_up(h->gu_scales_b, 256) +
-                            align_up(h->dn_codes_b, 256) + align_up(h->dn_scales_b, 256);
-    int rc = dev_alloc(&staging, st_bytes, "load staging");
+    int rc = dev_alloc(&staging, flags ? 2 * st_bytes : st_bytes, "load staging");
     if (rc != MOE_OK)
         return rc;
-    uint8_t* st_guc = staging;
-    uint8_t* st_gus = st_guc + align_up(h->gu_codes_b, 256);
-    uint8_t* st_dnc = st_gus + align_up(h->gu_scales_b, 256);
-    uint8_t* st_dns = st_dnc + align_up(h->dn_codes_b, 256);
+    uint8_t* cur[4] = {staging, staging + a_guc, staging + a_guc + a_gus, staging + a_guc + a_gus + a_dnc};
+    uint8_t* oth[4] = {cur[0] + st_bytes, cur[1] + st_bytes, cur[2] + st_bytes, cur[3] + st_bytes};
+    uint8_t* st_gub = staging + a_guc + a_gus + a_dnc + a_dns;
     cudaError_t e;
-    if ((e = cudaMemcpyAsync(st_guc, gu_codes, h->gu_codes_b, cudaMemcpyDefault, s)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(st_gus, gu_scales, h->gu_scales_b, cudaMemcpyDefault, s)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(st_dnc, dn_codes, h->dn_codes_b, cudaMemcpyDefault, s)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(st_dns, dn_scales, h->dn_scales_b, cudaMemcpyDefault, s)) != cudaSuccess ||
-        (h->gu_bias_b && (e = cudaMemcpyAsync(base + h->off_gu_bias, gu_bias, h->gu_bias_b,
+    if ((e = cudaMemcpyAsync(cur[0], gu_codes, h->gu_codes_b, cudaMemcpyDefault, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(cur[1], gu_scales, h->gu_scales_b, cudaMemcpyDefault, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(cur[2], dn_codes, h->dn_codes_b, cudaMemcpyDefault, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(cur[3], dn_scales, h->dn_scales_b, cudaMemcpyDefault, s)) != cudaSuccess ||
+        (h->gu_bias_b && (e = cudaMemcpyAsync(a_gub ? st_gub : base + h->off_gu_bias, gu_bias, h->gu_bias_b,
                                               cudaMemcpyDefault, s)) != cudaSuccess) ||
         (h->dn_bias_b && (e = cudaMemcpyAsync(base + h->off_dn_bias, dn_bias, h->dn_bias_b,
                                               cudaMemcpyDefault, s)) != cudaSuccess)) {
@@ -679,16 +687,39 @@ int moe_load_experts(moe_handle* h, int layer, const void* gu_codes, const void*
         cudaFree(staging);
         return cuda_fail(e, "moe_load_experts copy");
     }
-    if (h->mxfp4) {
-        // gate rows [0, I) and up rows [I, 2I) interleaved per 64 in 128-row tiles
-        if ((e = moe::launch_repack_tiles(st_guc, st_gus, E, 2 * I, 2 * I, H, I, 0, base, (long long)h->gu_expert, s)) ==
-            cudaSuccess)
-            e = moe::launch_repack_tiles(st_dnc, st_dns, E, H, H, I, 0, 1, base + h->off_dn, (long long)h->dn_expert, s);
-    } else {
-        if ((e = moe::launch_repack_i4(st_guc, reinterpret_cast<const uint16_t*>(st_gus), E, H, I, c.group, 0, base,
-                                       (long long)h->gu_expert, s)) == cudaSuccess)
-            e = moe::launch_repack_i4(st_dnc, reinterpret_cast<const uint16_t*>(st_dns), E, H, I, c.group, 1,
-                                      base + h->off_dn, (long long)h->dn_expert, s);
+    auto flip = [&](int i) { uint8_t* t = cur[i]; cur[i] = oth[i]; oth[i] = t; };
+    if (tr) {
+        // [K][N] orientation: codes [E][K][N/2], scales [E][K/blk][N]
+        if ((e = moe::launch_transpose_nibbles(cur[0], oth[0], E, 2 * I, H, s)) == cudaSuccess &&
+            (e = moe::launch_transpose_elems(cur[1], oth[1], E, H / blk, 2 * I, esz, s)) == cudaSuccess &&
+            (e = moe::launch_transpose_nibbles(cur[2], oth[2], E, H, I, s)) == cudaSuccess)
+            e = moe::launch_transpose_elems(cur[3], oth[3], E, I / blk, H, esz, s);
+        for (int i = 0; i < 4; ++i)
+            flip(i);
+    }
+    if (e == cudaSuccess && ilv) {
+        // gate row j at 2j, up row j at 2j + 1 (codes, scales and the gate/up bias)
+        if ((e = moe::launch_deinterleave_rows(cur[0], oth[0], E, 2 * I, H / 2, s)) == cudaSuccess &&
+            (e = moe::launch_deinterleave_rows(cur[1], oth[1], E, 2 * I, (long long)(H / blk) * esz, s)) ==
+                cudaSuccess &&
+            a_gub)
+            e = moe::launch_deinterleave_rows(st_gub, base + h->off_gu_bias, E, 2 * I, 2, s);
+        flip(0);
+        flip(1);
+    }
+    if (e == cudaSuccess) {
+        if (h->mxfp4) {
+            // gate rows [0, I) and up rows [I, 2I) interleaved per 64 in 128-row tiles
+            if ((e = moe::launch_repack_tiles(cur[0], cur[1], E, 2 * I, 2 * I, H, I, 0, base,
+                                              (long long)h->gu_expert, s)) == cudaSuccess)
+                e = moe::launch_repack_tiles(cur[2], cur[3], E, H, H, I, 0, 1, base + h->off_dn,
+                                             (long long)h->dn_expert, s);
+        } else {
+            if ((e = moe::launch_repack_i4(cur[0], reinterpret_cast<const uint16_t*>(cur[1]), E, H, I, c.group, 0,
+                                           base, (long long)h->gu_expert, s)) == cudaSuccess)
+                e = moe::launch_repack_i4(cur[2], reinterpret_cast<const uint16_t*>(cur[3]), E, H, I, c.group, 1,
+                                          base + h->off_dn, (long long)h->dn_expert, s);
+        }
     }
     if (e == cudaSuccess)
         e = cudaStreamSynchronize(s);
@@ -700,6 +731,13 @@ int moe_load_experts(moe_handle* h, int layer, const void* gu_codes, const void*
     cudaFree(staging);
     h->loaded[layer] = 1;
     return MOE_OK;
+}
+
+int moe_load_experts(moe_handle* h, int layer, const void* gu_codes, const void* gu_scales,
+                     const void* gu_bias, const void* dn_codes, const void* dn_scales,
+                     const void* dn_bias, void* stream)
+{
+    return moe_load_experts_ex(h, layer, gu_codes, gu_scales, gu_bias, dn_codes, dn_scales, dn_bias, 0, stream);
 }
 
 int moe_forward(moe_handle* h, int layer, const void* x_bf16, const float* router_logits, int M,

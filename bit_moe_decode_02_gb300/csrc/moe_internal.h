@@ -235,6 +235,13 @@ cudaError_t launch_dequant_i4(const uint8_t* w, int H, int I, int group, int pro
 // Debug kernels.
 // One expert projection of the tile layout back to fp32 in caller row order
 // (gate_up: interleave = I, rows [0, I) gate and [I, 2I) up; down: 0).
+// Load-time layout conversions (moe_loader.cu): [E][K][N] 4-bit codes ->
+// [E][N][K]; [E][R][C] elements of esz bytes -> [E][C][R]; gate/up rows
+// alternating -> gate rows then up rows (rows of row_bytes bytes, R rows).
+cudaError_t launch_transpose_nibbles(const uint8_t* src, uint8_t* dst, int E, int N, int K, cudaStream_t s);
+cudaError_t launch_transpose_elems(const uint8_t* src, uint8_t* dst, int E, int R, int C, int esz, cudaStream_t s);
+cudaError_t launch_deinterleave_rows(const uint8_t* src, uint8_t* dst, int E, int R, long long row_bytes,
+                                     cudaStream_t s);
 // Router GEMV logits [M][E] = x [M][H] . W^T + b (w: W bf16 [E][H] then b [E]),
 // fp32 with the decode kernel's summation order.
 cudaError_t launch_router_gemv(const uint16_t* x, const uint16_t* w, int M, int H, int E, float* out,

@@ -133,6 +133,27 @@ int moe_load_experts(moe_handle* h, int layer,
                      const void* dn_codes, const void* dn_scales, const void* dn_bias,
                      void* stream);
 
+/* Checkpoint-layout flags of moe_load_experts_ex.  The pages verify the
+ * MXFP4 reader's orientation against the reference checkpoint ("Sovereign
+ * gpt-oss-20B (MXFP4) on Apple Silicon", section 3, "transpose orientation
+ * verified"); these accept the layouts a checkpoint may use instead of the
+ * caller layout above:
+ *   MOE_LOAD_GATE_UP_INTERLEAVED: gate_up rows alternate, row 2j gate row j and
+ *     row 2j+1 up row j (codes, scales and gu_bias alike);
+ *   MOE_LOAD_TRANSPOSED: both projections stored [K][N] rather than [N][K]:
+ *     codes u8 [E][K][N/2] (the element with the even index along N in the low
+ *     nibble), scales [E][K/blk][N] (blk = 32 for MXFP4, group for int4); the
+ *     biases are vectors and unchanged.  With both flags the transposed
+ *     gate_up's N index is the alternating row order.
+ * The conversion runs on the device at load time (one extra staging copy of
+ * the layer); the resident layout and every forward are those of
+ * moe_load_experts. */
+typedef enum { MOE_LOAD_GATE_UP_INTERLEAVED = 1, MOE_LOAD_TRANSPOSED = 2 } moe_load_flags;
+int moe_load_experts_ex(moe_handle* h, int layer,
+                        const void* gu_codes, const void* gu_scales, const void* gu_bias,
+                        const void* dn_codes, const void* dn_scales, const void* dn_bias,
+                        int flags, void* stream);
+
 /* Router weights of one layer, for calls that leave the logits to the
  * library (router_logits == NULL): logits[m][e] = b[e] + sum_h x[m][h] W[e][h]
  * over the layer's input x (the same bf16 values the experts see; in the
