@@ -308,6 +308,12 @@ def run_ours(args):
     ms_graph = _max_over_ranks(e0.elapsed_time(e1), world)
     assert moe.moe_get_status(h) == 0
 
+    # the streaming floor of the same bytes: each resident layer's first
+    # avg-bytes read with the decode kernels' copy engine and stage sizes and
+    # nothing else, the layers one after another with a grid barrier between
+    # them (moe_debug_stream_weights)
+    fl_bytes = None
+
     bytes_per_step = []
     for s in range(W, min(n_in, W + 256)):
         moe.moe_forward(h, s % L, xp[s], lp[s], 1, k, rp[s], stream)
@@ -343,6 +349,17 @@ def run_ours(args):
 
     us_per_layer = 1e3 * ms / (K * world)
     avg_bytes = float(np.mean(bytes_per_step))
+    fl_bytes = int(avg_bytes) // 16 * 16
+    moe.moe_debug_stream_weights(h, 0, L, fl_bytes, stream)
+    torch.cuda.synchronize()
+    reps = 8
+    ev0.record(stream)
+    for _ in range(reps):
+        moe.moe_debug_stream_weights(h, 0, L, fl_bytes, stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    assert moe.moe_get_status(h) == 0
+    floor_us = 1e3 * ev0.elapsed_time(ev1) / (reps * L)
     peak, peak_kind = measured_peaks()
     achieved = avg_bytes / (ms / 1e3 / K) / 1e9
     extra = None
@@ -352,6 +369,12 @@ def run_ours(args):
             "gbs": float(np.mean(bytes_per_step)) / (ms_graph / 1e3 / K) / 1e9,
             "launch": "the same K steps as K moe_forward launches (PDL-chained) in one CUDA graph",
             "gpu_launches": K, "clocks": clk_g.summary()},
+            "stream_floor": {"us_per_layer": floor_us, "bytes_per_layer": fl_bytes,
+                             "gbs": fl_bytes / floor_us / 1e3, "layer_over_floor": us_per_layer / floor_us,
+                             "what": "the same bytes per layer read with the decode kernels' bulk copies "
+                                     "(32 KB stages, 128 KB in flight per SM, one CTA per SM) and no compute, "
+                                     f"{L} layers one after another with a grid barrier between them, "
+                                     f"{reps} launches"},
             "e2e_per_call": {"value": e2e_call_us, "unit": UNIT, "calls": nh,
                              "api": "moe_forward_host per step (host memcpy into mapped staging, one launch, "
                                     "one stream synchronisation)"}}

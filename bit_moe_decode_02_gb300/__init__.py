@@ -9,7 +9,8 @@ The function names are the C names: moe_create, moe_load_experts, moe_load_exper
 moe_forward, moe_forward_host, moe_forward_stack, moe_forward_stack_steps, moe_forward_steps,
 moe_load_router, moe_debug_router_logits, moe_get_status, moe_debug_dequant, moe_debug_route,
 moe_debug_stack_trace, moe_debug_forward_f32, moe_debug_set_wait, moe_last_bytes,
-moe_expert_bytes, moe_last_launches, moe_last_error, moe_forward_noalloc, moe_destroy.
+moe_expert_bytes, moe_last_launches, moe_last_error, moe_forward_noalloc, moe_debug_stream_weights,
+moe_destroy.
 """
 from __future__ import annotations
 
@@ -39,7 +40,7 @@ EXPORTS = ("moe_create", "moe_load_experts", "moe_load_experts_ex", "moe_forward
            "moe_debug_stack_trace", "moe_debug_mx_quantize", "moe_debug_batched_h",
            "moe_debug_forward_f32", "moe_debug_set_wait",
            "moe_last_bytes", "moe_expert_bytes", "moe_last_launches", "moe_last_error",
-           "moe_forward_noalloc", "moe_destroy")
+           "moe_forward_noalloc", "moe_debug_stream_weights", "moe_destroy")
 
 
 class MoeError(RuntimeError):
@@ -72,6 +73,8 @@ def lib() -> ctypes.CDLL:
         L.moe_load_experts.restype = i
         L.moe_load_experts_ex.argtypes = [p, i, p, p, p, p, p, p, i, p]
         L.moe_load_experts_ex.restype = i
+        L.moe_debug_stream_weights.argtypes = [p, i, i, ll, p]
+        L.moe_debug_stream_weights.restype = i
         L.moe_forward.argtypes = [p, i, p, p, i, i, p, p]
         L.moe_forward.restype = i
         L.moe_forward_host.argtypes = [p, i, p, p, i, i, p, p]
@@ -193,6 +196,10 @@ def moe_forward_stack_steps(h, n, resid, logits, M, top_k, stream=None):
 def moe_load_router(h, layer, w, bias=None):
     """Router weights w bf16 bits [E][H] and bias [E] (numpy uint16 arrays or tensors)."""
     return _check(lib().moe_load_router(h, layer, _ptr(w), _ptr(bias)))
+
+
+def moe_debug_stream_weights(h, layer0, n, nbytes, stream=None):
+    return _check(lib().moe_debug_stream_weights(h, layer0, n, nbytes, _stream(stream)))
 
 
 def moe_debug_router_logits(h, out, M, stream=None):

@@ -957,6 +957,23 @@ int moe_debug_router_logits(moe_handle* h, float* out_dev, int M, void* stream)
     return MOE_OK;
 }
 
+int moe_debug_stream_weights(moe_handle* h, int layer0, int n, long long bytes, void* stream)
+{
+    if (!h)
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_stream_weights: handle is NULL");
+    const int L = h->cfg.num_layers;
+    if (layer0 < 0 || layer0 >= L || n < 1 || layer0 + n > L || bytes < 16 || bytes % 16 ||
+        bytes > (long long)h->layer_stride)
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_stream_weights: need layers [layer0, layer0 + n) within 0..%d "
+                    "and 16 <= bytes <= %zu, a multiple of 16", L - 1, h->layer_stride);
+    cudaError_t e = moe::launch_stream_read(h->arena + (size_t)layer0 * h->layer_stride, (long long)h->layer_stride,
+                                            bytes, n, h->cnt + 2, h->spin_limit, h->status, h->num_sms,
+                                            (cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "moe_debug_stream_weights launch");
+    return MOE_OK;
+}
+
 int moe_get_status(moe_handle* h, void* stream)
 {
     if (!h)

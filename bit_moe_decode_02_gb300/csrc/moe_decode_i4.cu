@@ -92,19 +92,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p)
-{
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ unsigned long long atom_add_release_u64(unsigned long long* p, unsigned long long v)
-{
-    unsigned long long old;
-    asm volatile("atom.add.release.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
-    return old;
-}
-
 // Grid barrier (one thread of each CTA): the counter only grows, G per
 // barrier; `skip` arrives without adding (debug: the others' waits run out).
 __device__ __forceinline__ void grid_sync_i4(unsigned long long* cnt, int G, int limit, int* status, bool skip)

@@ -244,53 +244,6 @@ struct RingTc {   // (value-initialise: RingTc{} starts at 0)
 __device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, %0;" ::"r"(kEpi) : "memory"); }
 __device__ __forceinline__ void route_barrier() { asm volatile("bar.sync 2, 96;" ::: "memory"); }
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p)
-{
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v)
-{
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p)
-{
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ unsigned long long atom_add_release_u64(unsigned long long* p, unsigned long long v)
-{
-    unsigned long long old;
-    asm volatile("atom.add.release.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
-    return old;
-}
-// The counters only grow: every CTA adds 1 per call, so a call's count is
-// complete at the next multiple of G above what this CTA's own add saw.
-__device__ __forceinline__ unsigned long long count_target(unsigned long long old, int G)
-{
-    return (old / (unsigned long long)G + 1ull) * (unsigned long long)G;
-}
-// Add without waiting for the old value (the arrival at a grid barrier whose
-// target is already known), with release semantics.
-__device__ __forceinline__ void red_add_release_u64(unsigned long long* p, unsigned long long v)
-{
-    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-// Wait (one thread) until a grid counter reaches `tgt`; gives up after `limit`
-// polls and records a timeout.
-__device__ __forceinline__ void wait_count(const unsigned long long* cnt, unsigned long long tgt, int limit, int* status)
-{
-    int spins = 0;
-#pragma unroll 1
-    while (ld_acquire_u64(cnt) < tgt) {
-        if (++spins > limit) {
-            atomicExch(status, MOE_ERR_DEVICE_TIMEOUT);
-            break;
-        }
-    }
-}
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
 // Nearest-even E2M1 value of |x| (x already divided by the block scale, so

@@ -187,7 +187,7 @@ inline size_t tc_terms_bytes(int K)
     return (size_t)(K / 64) * 1024 + (size_t)ceil_div(K, 128) * kSfChunk + 16;
 }
 inline size_t tc_part_bytes(int G, int H) { return (size_t)G * H * 4 * sizeof(float); }
-constexpr int kTcCounterWords = 2;   // xcnt, done (64-bit)
+constexpr int kTcCounterWords = 3;   // xcnt, done, the streaming probe's barrier (64-bit)
 cudaError_t prepare_decode_tc(size_t smem);
 size_t decode_tc_static_smem();
 cudaError_t launch_decode_tc(const DecodeTcParams& p, size_t smem, int grid, cudaStream_t stream);
@@ -242,6 +242,11 @@ cudaError_t launch_transpose_nibbles(const uint8_t* src, uint8_t* dst, int E, in
 cudaError_t launch_transpose_elems(const uint8_t* src, uint8_t* dst, int E, int R, int C, int esz, cudaStream_t s);
 cudaError_t launch_deinterleave_rows(const uint8_t* src, uint8_t* dst, int E, int R, long long row_bytes,
                                      cudaStream_t s);
+// The streaming floor probe (moe_probe.cu): n regions of `bytes` bytes, region r
+// at base + r * region_stride, read one after another by `grid` CTAs with bulk
+// copies and a grid barrier (counter cnt) between regions.
+cudaError_t launch_stream_read(const uint8_t* base, long long region_stride, long long bytes, int nregions,
+                               unsigned long long* cnt, int spin_limit, int* status, int grid, cudaStream_t s);
 // Router GEMV logits [M][E] = x [M][H] . W^T + b (w: W bf16 [E][H] then b [E]),
 // fp32 with the decode kernel's summation order.
 cudaError_t launch_router_gemv(const uint16_t* x, const uint16_t* w, int M, int H, int E, float* out,

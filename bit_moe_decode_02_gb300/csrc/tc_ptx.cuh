@@ -157,6 +157,55 @@ __device__ __forceinline__ void tc_ld8(uint32_t taddr, float (&v)[8])
 
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Grid-wide signalling through global counters and flags (gpu scope).
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned long long atom_add_release_u64(unsigned long long* p, unsigned long long v)
+{
+    unsigned long long old;
+    asm volatile("atom.add.release.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+    return old;
+}
+// The counters only grow: every CTA adds 1 per call, so a call's count is
+// complete at the next multiple of G above what this CTA's own add saw.
+__device__ __forceinline__ unsigned long long count_target(unsigned long long old, int G)
+{
+    return (old / (unsigned long long)G + 1ull) * (unsigned long long)G;
+}
+// Add without waiting for the old value (the arrival at a grid barrier whose
+// target is already known), with release semantics.
+__device__ __forceinline__ void red_add_release_u64(unsigned long long* p, unsigned long long v)
+{
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+// Wait (one thread) until a grid counter reaches `tgt`; gives up after `limit`
+// polls and records a timeout.
+__device__ __forceinline__ void wait_count(const unsigned long long* cnt, unsigned long long tgt, int limit, int* status)
+{
+    int spins = 0;
+#pragma unroll 1
+    while (ld_acquire_u64(cnt) < tgt) {
+        if (++spins > limit) {
+            atomicExch(status, MOE_ERR_DEVICE_TIMEOUT);
+            break;
+        }
+    }
+}
+
 __device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
 __device__ __forceinline__ uint16_t f2bf16_rne(float f)

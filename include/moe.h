@@ -258,6 +258,15 @@ int moe_forward_stack_steps(moe_handle* h, int n, void* resid_bf16, const float*
 int moe_forward_steps(moe_handle* h, int n, int layer0, const void* x_bf16, const float* router_logits,
                       int M, int top_k, void* out_bf16, void* stream);
 
+/* Measurement: the streaming floor of this GPU for decode-sized weight reads.
+ * Reads the first `bytes` bytes of resident layers layer0 .. layer0 + n - 1,
+ * one layer after another with a grid barrier between them (as dependent
+ * decode layers are), with the copy engine and stage sizes of the decode
+ * kernels (one CTA per SM, bulk copies of 32 KB, 128 KB in flight per SM) and
+ * no compute.  bytes: a multiple of 16, at most one layer's arena.  Device
+ * work on `stream`; errors as MOE_ERR_INVALID_ARG. */
+int moe_debug_stream_weights(moe_handle* h, int layer0, int n, long long bytes, void* stream);
+
 /* Synchronise `stream` and return (and clear) the handle's device status:
  * MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_FAULT.  After a non-OK
  * status the handle's cross-CTA counters are reset, so it can be used again.
