@@ -28,8 +28,9 @@
 // (SB = 8 when group is 32: both 32-element blocks of the segment).  One bulk
 // copy moves a stage of a unit: up to 4 gate/up segments or 32 down slabs.
 //
-// Warps 0..7 compute: on a gate/up stage warp w takes slab w (all of the
-// stage's segments), on a down stage slabs w, w + 8, ...; warp 8 streams the
+// Warps 0..15 compute: on a gate/up stage warp w takes slab w mod 8 and every
+// other segment of the stage (w / 8 picks which; the two halves' sums are added
+// in a fixed order), on a down stage slabs w, w + 16, ...; warp 16 streams the
 // stages.  x enters as f16 after an exact power-of-two rescale per token (its
 // largest magnitude to [2^14, 2^15)); h' = w h as f16 hi + lo after a
 // power-of-two rescale per (unit, token).  Products and sums are fp32.
