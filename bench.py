@@ -573,7 +573,7 @@ def measure_stack(moe, h, shape, L, M, steps, warmup):
             "launch": f"one cached CUDA graph of {launches} PDL-chained layer kernels per step"}
 
 
-def measure_batched(moe, shape, steps, warmup):
+def measure_batched(moe, shape, steps, warmup, bf16=False):
     """The batched MXFP4 layer (H = I = 2880, 128 experts, top-4, M = 512)
     through moe_forward's tensor-core path.  One layer is resident (1.7 GB of
     expert weights, 13x L2); P = 4 input sets are cycled, so a step's weights
@@ -581,6 +581,8 @@ def measure_batched(moe, shape, steps, warmup):
     import torch
     H, I, E, k, M = shape.hidden, shape.intermediate, shape.experts, shape.top_k, shape.tokens
     h = moe.moe_create(H, I, E, 1, M, k, moe.MOE_FMT_MXFP4, 32, 1)
+    if bf16:
+        moe.moe_set_batched_numerics(h, moe.MOE_BATCHED_BF16)
     _load_all(moe, h, shape, 1)
     P = 4
     ins = [synth.step_inputs(shape, 7000 + i) for i in range(P)]
@@ -619,7 +621,10 @@ def measure_batched(moe, shape, steps, warmup):
     fp4_peak, fp4_src = _fp4_peak()
     gbs = float(np.mean(nbytes)) / (us / 1e6) / 1e9
     tflops = flops / (us / 1e6) / 1e12
-    return {"workload": shape.name, "metric": "us per batched MoE layer; TFLOP/s and expert-weight GB/s",
+    numerics = ("bf16: tcgen05 kind::f16 on weights dequantised to bf16, x as given, h as bf16 hi + lo" if bf16
+                else "MXFP4 activations: tcgen05 kind::mxf4")
+    return {"workload": shape.name, "numerics": numerics,
+            "metric": "us per batched MoE layer; TFLOP/s and expert-weight GB/s",
             "value": us, "unit": "us/layer", "steps": steps, "warmup": warmup, "tokens": M,
             "tflops": tflops, "tflops_peak_fp4": fp4_peak, "tflops_peak_source": fp4_src,
             "tflops_frac": tflops / fp4_peak, "bytes_per_step": float(np.mean(nbytes)), "gbs": gbs,
@@ -643,6 +648,7 @@ def extra_workloads(moe, args):
     moe.moe_destroy(h)
     out["batched"] = measure_batched(moe, synth.BATCHED, max(args.extra_steps // 4, 8), 3)
     out["batched_skewed"] = measure_batched(moe, synth.BATCHED_SKEWED, max(args.extra_steps // 4, 8), 3)
+    out["batched_bf16"] = measure_batched(moe, synth.BATCHED, max(args.extra_steps // 4, 8), 3, bf16=True)
     return out
 
 

@@ -89,6 +89,8 @@ struct moe_handle {
     uint8_t* b_hq = nullptr;
     uint8_t* b_hsf = nullptr;
     float* b_y = nullptr;
+    int b_f16 = 0;                            // batched numerics: 0 MXFP4 activations, 1 bf16
+    uint8_t* b_a16 = nullptr;                 // bf16 variant: x tiles, then h tiles (allocated on selection)
     int last_bM = 0, last_bk = 0;             // M and top_k of the last batched call
     // in-kernel router: per layer W bf16 [E][H] then the bias bf16 [E]
     // (rw_stride bytes a layer; allocated by the first moe_load_router), and
@@ -175,6 +177,7 @@ void free_handle(moe_handle* h)
     cudaFree(h->b_hq);
     cudaFree(h->b_hsf);
     cudaFree(h->b_y);
+    cudaFree(h->b_a16);
     cudaFree(h->stats);
     cudaFree(h->status);
     cudaFree(h->rw);
@@ -406,6 +409,12 @@ moe::BatchParams batch_params(const moe_handle* h, int layer)
     p.hq = h->b_hq;
     p.hsf = h->b_hsf;
     p.y = h->b_y;
+    if (h->b_f16) {
+        const size_t rows = Mk + 16 * (size_t)h->max_tiles;
+        p.f16 = 1;
+        p.x16 = h->b_a16;
+        p.h16 = h->b_a16 + rows * c.hidden * 2;
+    }
     p.status = h->status;
     p.nu_out = h->stats + layer;
     p.H = c.hidden;
@@ -971,6 +980,30 @@ int moe_debug_stream_weights(moe_handle* h, int layer0, int n, long long bytes, 
                                             (cudaStream_t)stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "moe_debug_stream_weights launch");
+    return MOE_OK;
+}
+
+int moe_set_batched_numerics(moe_handle* h, int numerics)
+{
+    if (!h)
+        return fail(MOE_ERR_INVALID_ARG, "moe_set_batched_numerics: handle is NULL");
+    if (numerics != MOE_BATCHED_MXFP4 && numerics != MOE_BATCHED_BF16)
+        return fail(MOE_ERR_INVALID_ARG, "moe_set_batched_numerics: unknown numerics %d", numerics);
+    if (!h->batched)
+        return fail(MOE_ERR_UNSUPPORTED, "moe_set_batched_numerics: the handle has no batched path (max_tokens <= %d)",
+                    moe::kMaxTokens);
+    if (numerics == MOE_BATCHED_BF16 && !h->b_a16) {
+        const moe_config& c = h->cfg;
+        const size_t rows = (size_t)c.max_tokens * c.max_top_k + 16 * (size_t)h->max_tiles;
+        int rc = dev_alloc(&h->b_a16, moe::batched_f16_act_bytes((long long)rows, c.hidden, c.intermediate),
+                           "bf16 activation tiles");
+        if (rc != MOE_OK)
+            return rc;
+        cudaError_t e = moe::prepare_batched_f16_kernels();
+        if (e != cudaSuccess)
+            return cuda_fail(e, "bf16 batched kernel set-up");
+    }
+    h->b_f16 = numerics == MOE_BATCHED_BF16 ? 1 : 0;
     return MOE_OK;
 }
 

@@ -745,6 +745,15 @@ cudaError_t launch_batched(const BatchParams& p, int grid, cudaStream_t s, int* 
     if ((e = launch_route(p.logits, p.M, p.E, p.k, p.idx, p.wt, s)) != cudaSuccess)
         return e;
     plan_kernel<<<1, 1024, 0, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+    if (p.f16) {
+        if ((e = launch_batched_f16_gemms(p, grid, s)) != cudaSuccess)
+            return e;
+        combine_kernel<<<blocks_for((long long)p.M * (p.H / 8), 256), 256, 0, s>>>(p);
+        *launches = 6;
+        return cudaGetLastError();
+    }
     quant_x_kernel<<<blocks_for((long long)p.M * (p.H / 32), 256), 256, 0, s>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;

@@ -366,31 +366,47 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                 const uint8_t* gsrc = gu + (long long)e * p.gu_expert + (long long)t * gu_unit;
                 const uint8_t* dsrc = dn + (long long)e * p.dn_expert + (long long)t * dn_unit;
                 const int ngu = (KS + kGuSeg - 1) / kGuSeg, ndn = (NSL + kDnSlabs - 1) / kDnSlabs;
-                for (int st = 0; st < ngu + ndn; ++st, ++st_count) {
-                    const uint32_t slot = st_count % nslots;
-                    if (st_count >= (uint32_t)nslots)
-                        mbar_wait(&si.empty[slot], ((st_count / nslots) - 1) & 1, p.status);
-                    uint32_t cb, sb2;
-                    const uint8_t *csrc, *ssrc;
-                    if (st < ngu) {
-                        const int q0 = st * kGuSeg, n = min(kGuSeg, KS - q0);
-                        cb = (uint32_t)n * 4096;
-                        sb2 = (uint32_t)n * 64 * SB;
-                        csrc = gsrc + (long long)q0 * 4096;
-                        ssrc = gsrc + (long long)KS * 4096 + (long long)q0 * 64 * SB;
-                    } else {
-                        const int s0 = (st - ngu) * kDnSlabs, n = min(kDnSlabs, NSL - s0);
-                        cb = (uint32_t)n * 512;
-                        sb2 = (uint32_t)n * 8 * SB;
-                        csrc = dsrc + (long long)s0 * 512;
-                        ssrc = dsrc + (long long)NSL * 512 + (long long)s0 * 8 * SB;
-                    }
-                    uint8_t* dst = i4ring + slot * kI4Slot;
-                    if (lane == 0) {
+                // Stages go out in batches, one lane each: lane 0 waits until stage st's
+                // slot is free, then every stage of the next nslots whose slot is
+                // already free (a non-blocking test; a slot is tested only against its
+                // previous use, which is at most one phase behind) is issued at once.
+                // At a call's start the whole ring is free, so the first batch fills it.
+                const int ntot = ngu + ndn;
+                for (int st = 0; st < ntot;) {
+                    if (lane == 0 && st_count >= (uint32_t)nslots)
+                        mbar_wait(&si.empty[st_count % nslots], ((st_count / nslots) - 1) & 1, p.status);
+                    __syncwarp();
+                    const uint32_t k = st_count + (uint32_t)lane;
+                    bool ready = lane < nslots && st + lane < ntot;
+                    if (ready && lane > 0 && k >= (uint32_t)nslots)
+                        ready = mbar_test_wait(&si.empty[k % nslots], ((k / nslots) - 1) & 1);
+                    const uint32_t rb = __ballot_sync(0xffffffffu, ready);
+                    const int nb = __ffs(~rb) - 1;   // the ready prefix (lane 0 is ready)
+                    if (lane < nb) {
+                        const int sl = st + lane;
+                        const uint32_t slot = k % nslots;
+                        uint32_t cb, sb2;
+                        const uint8_t *csrc, *ssrc;
+                        if (sl < ngu) {
+                            const int q0 = sl * kGuSeg, n = min(kGuSeg, KS - q0);
+                            cb = (uint32_t)n * 4096;
+                            sb2 = (uint32_t)n * 64 * SB;
+                            csrc = gsrc + (long long)q0 * 4096;
+                            ssrc = gsrc + (long long)KS * 4096 + (long long)q0 * 64 * SB;
+                        } else {
+                            const int s0 = (sl - ngu) * kDnSlabs, n = min(kDnSlabs, NSL - s0);
+                            cb = (uint32_t)n * 512;
+                            sb2 = (uint32_t)n * 8 * SB;
+                            csrc = dsrc + (long long)s0 * 512;
+                            ssrc = dsrc + (long long)NSL * 512 + (long long)s0 * 8 * SB;
+                        }
+                        uint8_t* dst = i4ring + slot * kI4Slot;
                         mbar_expect_tx(&si.full[slot], cb + sb2);
                         bulk_copy_hint(dst, csrc, cb, &si.full[slot], wpol);
                         bulk_copy_hint(dst + kI4Codes, ssrc, sb2, &si.full[slot], wpol);
                     }
+                    st += nb;
+                    st_count += (uint32_t)nb;
                     __syncwarp();
                 }
             }
@@ -405,7 +421,9 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                 const int ngu = (KS + kGuSeg - 1) / kGuSeg;
                 for (int st = 0; st < ngu; ++st, ++st_count) {
                     const uint32_t slot = st_count % nslots;
-                    mbar_wait(&si.full[slot], (st_count / nslots) & 1, p.status);
+                    if (lane == 0)   // one poller a warp; the warp's other lanes follow its acquire
+                        mbar_wait(&si.full[slot], (st_count / nslots) & 1, p.status);
+                    __syncwarp();
                     const uint8_t* sp = i4ring + slot * kI4Slot;
                     const int q0 = st * kGuSeg, n = min(kGuSeg, KS - q0);
                     for (int qi = half; qi < n; qi += 2) {
@@ -527,7 +545,9 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                 const int ndn = (NSL + kDnSlabs - 1) / kDnSlabs;
                 for (int st = 0; st < ndn; ++st, ++st_count) {
                     const uint32_t slot = st_count % nslots;
-                    mbar_wait(&si.full[slot], (st_count / nslots) & 1, p.status);
+                    if (lane == 0)   // one poller a warp; the warp's other lanes follow its acquire
+                        mbar_wait(&si.full[slot], (st_count / nslots) & 1, p.status);
+                    __syncwarp();
                     const uint8_t* sp = i4ring + slot * kI4Slot;
                     const int s0 = st * kDnSlabs, n = min(kDnSlabs, NSL - s0);
                     for (int si2 = warp; si2 < n; si2 += kCw) {

@@ -111,12 +111,23 @@ struct BatchParams {
     float* out_f32;             // [M][H] fp32 result before the bf16 rounding, or nullptr
     int H, I, E, M, k;
     int max_tiles;
+    // bf16 numerics (moe_batched_f16.cu): bf16 activation tiles of x and of h
+    // (hi and lo rows), or f16 = 0 for the MXFP4 activations above
+    int f16;
+    uint8_t* x16;
+    uint8_t* h16;
 };
 
 // Enqueue the batched layer (route, plan, quantise x, gate_up GEMM + SwiGLU +
 // quantise h, down GEMM, combine) on `stream`; `grid` = SM count.
 cudaError_t launch_batched(const BatchParams& p, int grid, cudaStream_t stream, int* launches);
 cudaError_t prepare_batched_kernels();
+// The bf16 variant's two GEMMs and the x packing that feeds them (after route
+// and plan, before combine); the bytes of its activation tiles for `rows`
+// padded rows.
+cudaError_t launch_batched_f16_gemms(const BatchParams& p, int grid, cudaStream_t stream);
+cudaError_t prepare_batched_f16_kernels();
+size_t batched_f16_act_bytes(long long rows, int H, int I);
 // Caller layout [E][N][K/2] codes + [E][N][K/32] E8M0 -> tile layout (one projection
 // per expert of N rows of a caller matrix with `src_rows` rows).  Tile row n comes
 // from caller row n, or with `interleave` = I > 0 (N = 2I) from the interleaved

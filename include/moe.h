@@ -190,6 +190,21 @@ int moe_load_router(moe_handle* h, int layer, const void* w_bf16, const void* bi
 int moe_forward(moe_handle* h, int layer, const void* x_bf16, const float* router_logits,
                 int M, int top_k, void* out_bf16, void* stream);
 
+/* Numerics of the batched path (M > 4) on this handle:
+ *   MOE_BATCHED_MXFP4 (default): tcgen05.mma kind::mxf4 -- x and h quantised
+ *     to MXFP4 per 32 along K (the OCP MX rule), as that instruction needs;
+ *   MOE_BATCHED_BF16: tcgen05.mma kind::f16 -- every weight dequantised to
+ *     bf16 in shared memory (exactly: e2m1 * 2^(s-127) is a bf16 value), x as
+ *     given and h as bf16 hi + lo (hi = bf16(h), lo = bf16(h - hi)), fp32
+ *     accumulation: no activation quantisation, at the cost of the
+ *     dequantisation on the CUDA cores.
+ * The grouped-expert GEMM is the lever "Sovereign gpt-oss-20B (MXFP4) on
+ * Apple Silicon", section 5, names as untried; the two numerics are this
+ * library's.  The first switch to bf16 allocates its activation tiles.
+ * MOE_ERR_UNSUPPORTED on a handle with max_tokens <= 4. */
+typedef enum { MOE_BATCHED_MXFP4 = 0, MOE_BATCHED_BF16 = 1 } moe_batched_numerics;
+int moe_set_batched_numerics(moe_handle* h, int numerics);
+
 /* Debug: the router logits of the last call that computed them (the last
  * layer call of a decode launch, or the batched call), fp32 [M][E], copied to
  * the device buffer out_dev on `stream`. */
