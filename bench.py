@@ -673,8 +673,8 @@ def run_batched(args):
     """One batched workload alone (--workload batched / batched_skewed)."""
     rank, world = _setup(args)
     import bit_moe_decode_02_gb300 as moe
-    shape = synth.BATCHED if args.workload == "batched" else synth.BATCHED_SKEWED
-    line = measure_batched(moe, shape, args.steps, args.warmup)
+    shape = synth.BATCHED_SKEWED if args.workload == "batched_skewed" else synth.BATCHED
+    line = measure_batched(moe, shape, args.steps, args.warmup, bf16=args.workload == "batched_bf16")
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -701,7 +701,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None,
                     help="resident layers (default: 24 for the layer workload, all for the "
                          "stacks; smaller for profiling)")
-    ap.add_argument("--workload", choices=["layer", "stack24", "int4stack48", "batched", "batched_skewed"],
+    ap.add_argument("--workload", choices=["layer", "stack24", "int4stack48", "batched", "batched_skewed",
+                                           "batched_bf16"],
                     default="layer")
     ap.add_argument("--tokens", type=int, default=1, help="M for the stack workloads")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")

@@ -11,10 +11,13 @@
 // 96 tokens) and combine; only the activation packing and the two GEMMs
 // differ.  Each GEMM is persistent (one CTA per SM walking (token tile, row
 // tile) items, as gemm_kernel does), with four roles:
-//   warp 0      streams one k-step per stage: the 128-row tile's E2M1 codes
-//               (4 KB), its 128-column scale chunk and the activation block;
-//   warps 6..9  dequantise the codes into a bf16 copy of the k-step (one row
-//               per thread, each element e2m1 * 2^(s - 127) exactly, then
+//   warp 0      streams the weights, one k-step a stage (the 128-row tile's
+//               E2M1 codes, 4 KB, and its 128-column scale chunk), 10 stages
+//               in flight;
+//   warp 14     streams the activation blocks (a ring of their own: they are
+//               mostly L2 hits, re-read by every row tile);
+//   warps 6..13 dequantise the codes into a bf16 copy of the k-step (half a
+//               row per thread, each element e2m1 * 2^(s - 127) exactly, then
 //               RNE to bf16 -- exact: a 2-bit significand, and bf16 has
 //               fp32's exponent range);
 //   warp 1      issues 4 MMAs of K = 16 per k-step (M = 128, N = the token
@@ -37,17 +40,19 @@ namespace {
 
 using namespace tc;
 
-constexpr int kF16Slots = 4;                      // stage ring slots, one k-step each
 constexpr int kTileA16 = kRowTile * 32;           // one k-step of a 128-row tile of E2M1 codes: 4 KB
 constexpr int kF16RawA = kTileA16 + kSfChunk;     // ... and its 128-column scale chunk
+constexpr int kASlots = 10;                       // weight ring: k-steps in flight (the HBM stream)
+constexpr int kBSlots = 5;                        // activation ring (mostly L2 hits)
 constexpr int kF16B = 2 * kTokTile * 128;         // an activation block: up to 2 x 96 rows x 64 bf16
-constexpr int kF16Slot = kF16RawA + kF16B;
 constexpr int kA16 = kRowTile * 64 * 2;           // a dequantised k-step: 128 rows x 64 bf16
-constexpr int kF16Smem = kF16Slots * kF16Slot + 2 * kA16;
-constexpr int kThreadsF16 = 320;                  // producer, MMA, 4 epilogue warps, 4 converter warps
+constexpr int kF16Smem = kASlots * kF16RawA + kBSlots * kF16B + 2 * kA16;
+constexpr int kConvWarps = 8;                     // converter warps: two threads a tile row
+constexpr int kThreadsF16 = 480;                  // 2 producers, MMA, 4 epilogue and 8 converter warps
 constexpr int kAccF16 = 2 * kTokTile;             // accumulator columns per buffer (down: hi + lo)
 static_assert(2 * kAccF16 <= 512, "tensor memory: two accumulator buffers");
-static_assert(kF16Slot % 128 == 0 && kA16 % 1024 == 0, "shared-memory alignment of the operands");
+static_assert(kF16RawA % 128 == 0 && kF16B % 128 == 0, "shared-memory alignment of the operands");
+static_assert(kF16Smem <= 227 * 1024, "shared memory");
 
 struct F16Params {
     const uint8_t* w;       // tile-layout weights; expert e at + e * w_expert
@@ -103,32 +108,50 @@ __global__ void pack_x16_kernel(const uint16_t* __restrict__ x, int M, int H, in
     }
 }
 
-// e2m1 codes of one row's k-step (32 bytes: element 2b in the low nibble of
-// byte b) times its two block scales -> 64 bf16 in the canonical layout.
-__device__ __forceinline__ void dequant_row(const uint8_t* raw, const uint8_t* chunk, int r, int kpair,
-                                            uint8_t* a16)
+// Half a row of a k-step (half hf: elements 32 hf .. 32 hf + 31 = bytes 16 hf
+// .. 16 hf + 15, element 2b in the low nibble of byte b) times its block scale
+// -> 32 bf16 in the canonical layout (e2m1 * 2^(s-127) in fp32 is exact, and
+// so is its RNE conversion to bf16).
+__device__ __forceinline__ void dequant_half_row(const uint8_t* raw, const uint8_t* chunk, int r, int hf, int kpair,
+                                                 uint8_t* a16)
 {
-    const uint4 c0 = *reinterpret_cast<const uint4*>(raw + (r >> 3) * 256 + (r & 7) * 16);
-    const uint4 c1 = *reinterpret_cast<const uint4*>(raw + (r >> 3) * 256 + 128 + (r & 7) * 16);
-    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    const uint8_t* sp = chunk + (r & 31) * 16 + (r >> 5) * 4 + 2 * kpair;
-    float sc[2];
+    const uint4 cw = *reinterpret_cast<const uint4*>(raw + (r >> 3) * 256 + hf * 128 + (r & 7) * 16);
+    const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+    const uint32_t sb = chunk[(r & 31) * 16 + (r >> 5) * 4 + 2 * kpair + hf];
+    const float s = __uint_as_float(sb == 0u ? 0x00400000u : (sb == 255u ? 0x7fc00000u : sb << 23));
 #pragma unroll
-    for (int b = 0; b < 2; ++b) {
-        const uint32_t s = sp[b];
-        sc[b] = __uint_as_float(s == 0u ? 0x00400000u : (s == 255u ? 0x7fc00000u : s << 23));
-    }
-#pragma unroll
-    for (int kg = 0; kg < 8; ++kg) {   // elements 8 kg .. 8 kg + 7: word kg
+    for (int kg = 0; kg < 4; ++kg) {   // elements 8 kg .. 8 kg + 7 of the half: word kg
         uint32_t o[4];
-        const float s = sc[kg >> 2];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const float2 f = e2m1x2_to_f32((w[kg] >> (8 * j)) & 0xffu);
-            o[j] = (uint32_t)f2bf16_rne(f.x * s) | ((uint32_t)f2bf16_rne(f.y * s) << 16);
+            const float2 f = e2m1x2_to_f32(w[kg] >> (8 * j));
+            asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o[j]) : "f"(f.y * s), "f"(f.x * s));
         }
-        *reinterpret_cast<uint4*>(a16 + (r >> 3) * 1024 + kg * 128 + (r & 7) * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(a16 + (r >> 3) * 1024 + (4 * hf + kg) * 128 + (r & 7) * 16) =
+            make_uint4(o[0], o[1], o[2], o[3]);
     }
+}
+
+// Issue, one lane each, the stages [c, c + n) of a ring of `slots` stages
+// whose slots are free: lane 0 waits for stage c's slot, the others only test
+// theirs (a slot is tested against its previous use, at most one phase
+// behind), and the ready prefix goes out.  Returns the number issued.
+template <typename Issue>
+__device__ __forceinline__ int issue_batch(uint64_t* empty, int slots, uint32_t c, int n, int lane, int* status,
+                                           Issue&& issue)
+{
+    if (lane == 0 && c >= (uint32_t)slots)
+        mbar_wait(&empty[c % slots], ((c / slots) - 1) & 1, status);
+    __syncwarp();
+    const uint32_t k = c + (uint32_t)lane;
+    bool ready = lane < slots && lane < n;
+    if (ready && lane > 0 && k >= (uint32_t)slots)
+        ready = mbar_test_wait(&empty[k % slots], ((k / slots) - 1) & 1);
+    const int nb = __ffs(~__ballot_sync(0xffffffffu, ready)) - 1;
+    if (lane < nb)
+        issue(k, k % slots);
+    __syncwarp();
+    return nb;
 }
 
 template <bool DUAL>
@@ -136,18 +159,25 @@ __global__ void __launch_bounds__(kThreadsF16, 1) gemm16_kernel(F16Params p)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ float xbuf[DUAL ? 2 * 2 * 2 * 32 * 8 : 1];
-    __shared__ __align__(8) uint64_t full[kF16Slots], empty[kF16Slots], a16f[2], a16e[2], accf[2], acce[2];
+    __shared__ __align__(8) uint64_t fullA[kASlots], emptyA[kASlots], fullB[kBSlots], emptyB[kBSlots];
+    __shared__ __align__(8) uint64_t a16f[2], a16e[2], accf[2], acce[2];
     __shared__ uint32_t tmem_base;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint8_t* a16 = smem + kF16Slots * kF16Slot;
+    uint8_t* ringA = smem;
+    uint8_t* ringB = smem + kASlots * kF16RawA;
+    uint8_t* a16 = ringB + kBSlots * kF16B;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kF16Slots; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+        for (int i = 0; i < kASlots; ++i) {
+            mbar_init(&fullA[i], 1);
+            mbar_init(&emptyA[i], kConvWarps);
+        }
+        for (int i = 0; i < kBSlots; ++i) {
+            mbar_init(&fullB[i], 1);
+            mbar_init(&emptyB[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&a16f[i], 4);
+            mbar_init(&a16f[i], kConvWarps);
             mbar_init(&a16e[i], 1);
             mbar_init(&accf[i], 1);
             mbar_init(&acce[i], 4);
@@ -167,52 +197,56 @@ __global__ void __launch_bounds__(kThreadsF16, 1) gemm16_kernel(F16Params p)
     const int KS = p.K / 64;
     const int prow = DUAL ? 2 * p.rows : p.rows;
     const int items = *p.ntiles * T;
+    // this CTA's items are w = blockIdx.x + i gridDim.x; its k-steps run c = i KS + s
+    const int nitems = blockIdx.x < items ? (items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const uint32_t total = (uint32_t)nitems * (uint32_t)KS;
 
     if (warp == 0) {
-        // ================================================================ producer
-        uint32_t c = 0;
-        for (int w = blockIdx.x; w < items; w += gridDim.x) {
-            const int tt = w / T, t = w % T;
-            const TokTile tile = p.tiles[tt];
-            const int R = prow - t * kRowTile < kRowTile ? prow - t * kRowTile : kRowTile;
-            const int nb = DUAL ? tile.npad : 2 * tile.npad;
-            const uint8_t* we = p.w + tile.e * p.w_expert;
-            const uint8_t* ab = p.act + act16_base(tile, p.K, DUAL ? 1 : 2);
-            for (int s = 0; s < KS; ++s, ++c) {
-                const uint32_t slot = c % kF16Slots;
-                if (c >= (uint32_t)kF16Slots)
-                    mbar_wait(&empty[slot], ((c / kF16Slots) - 1) & 1, p.status);
-                uint8_t* st = smem + slot * kF16Slot;
-                if (lane == 0)
-                    mbar_expect_tx(&full[slot], (uint32_t)R * 32 + kSfChunk + (uint32_t)nb * 128);
-                __syncwarp();
-                if (lane == 0)
-                    bulk_copy(st, we + tile_block_off(prow, p.K, t, s, p.kmajor), (uint32_t)R * 32, &full[slot]);
-                else if (lane == 1)
-                    bulk_copy(st + kTileA16, we + tile_sf_off(prow, p.K, t, s >> 1, p.kmajor), kSfChunk, &full[slot]);
-                else if (lane == 2)
-                    bulk_copy(st + kF16RawA, ab + (long long)s * nb * 128, (uint32_t)nb * 128, &full[slot]);
-            }
+        // ================================================================ weight producer
+        for (uint32_t c = 0; c < total;) {
+            c += issue_batch(emptyA, kASlots, c, (int)(total - c), lane, p.status, [&](uint32_t k, uint32_t slot) {
+                const int w = blockIdx.x + (int)(k / KS) * gridDim.x, s = (int)(k % KS);
+                const int t = w % T;
+                const TokTile tile = p.tiles[w / T];
+                const int R = prow - t * kRowTile < kRowTile ? prow - t * kRowTile : kRowTile;
+                const uint8_t* we = p.w + tile.e * p.w_expert;
+                uint8_t* st = ringA + slot * kF16RawA;
+                mbar_expect_tx(&fullA[slot], (uint32_t)R * 32 + kSfChunk);
+                bulk_copy(st, we + tile_block_off(prow, p.K, t, s, p.kmajor), (uint32_t)R * 32, &fullA[slot]);
+                bulk_copy(st + kTileA16, we + tile_sf_off(prow, p.K, t, s >> 1, p.kmajor), kSfChunk, &fullA[slot]);
+            });
+        }
+    } else if (warp == 6 + kConvWarps) {
+        // ================================================================ activation producer
+        for (uint32_t c = 0; c < total;) {
+            c += issue_batch(emptyB, kBSlots, c, (int)(total - c), lane, p.status, [&](uint32_t k, uint32_t slot) {
+                const int w = blockIdx.x + (int)(k / KS) * gridDim.x, s = (int)(k % KS);
+                const TokTile tile = p.tiles[w / T];
+                const int nb = DUAL ? tile.npad : 2 * tile.npad;
+                const uint8_t* ab = p.act + act16_base(tile, p.K, DUAL ? 1 : 2);
+                mbar_expect_tx(&fullB[slot], (uint32_t)nb * 128);
+                bulk_copy(ringB + slot * kF16B, ab + (long long)s * nb * 128, (uint32_t)nb * 128, &fullB[slot]);
+            });
         }
     } else if (warp >= 6) {
-        // ================================================================ converters
-        const int r = threadIdx.x - 192;   // the tile row this thread dequantises
-        uint32_t c = 0;
-        for (int w = blockIdx.x; w < items; w += gridDim.x) {
+        // ================================================================ converters (warps 6..13)
+        const int r = (threadIdx.x - 192) & 127, hf = (threadIdx.x - 192) >> 7;   // row, half of it
+        for (uint32_t c = 0; c < total; ++c) {
+            const int w = blockIdx.x + (int)(c / KS) * gridDim.x, s = (int)(c % KS);
             const int t = w % T;
             const int R = prow - t * kRowTile < kRowTile ? prow - t * kRowTile : kRowTile;
-            for (int s = 0; s < KS; ++s, ++c) {
-                const uint32_t slot = c % kF16Slots, a = c & 1;
-                mbar_wait(&full[slot], (c / kF16Slots) & 1, p.status);
-                if (c >= 2)
-                    mbar_wait(&a16e[a], ((c >> 1) - 1) & 1, p.status);
-                const uint8_t* st = smem + slot * kF16Slot;
-                if (r < R)   // rows past a partial tile feed MMA rows nobody reads
-                    dequant_row(st, st + kTileA16, r, s & 1, a16 + a * kA16);
-                fence_proxy_async_smem();   // generic writes -> the MMA's reads
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&a16f[a]);
+            const uint32_t slot = c % kASlots, a = c & 1;
+            mbar_wait(&fullA[slot], (c / kASlots) & 1, p.status);
+            if (c >= 2)
+                mbar_wait(&a16e[a], ((c >> 1) - 1) & 1, p.status);
+            const uint8_t* st = ringA + slot * kF16RawA;
+            if (r < R)   // rows past a partial tile feed MMA rows nobody reads
+                dequant_half_row(st, st + kTileA16, r, hf, s & 1, a16 + a * kA16);
+            fence_proxy_async_smem();   // generic writes -> the MMA's reads
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&a16f[a]);
+                mbar_arrive(&emptyA[slot]);
             }
         }
     } else if (warp == 1) {
@@ -232,11 +266,11 @@ __global__ void __launch_bounds__(kThreadsF16, 1) gemm16_kernel(F16Params p)
                 const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(nb >> 3) << 17) |
                                        ((uint32_t)(kRowTile >> 4) << 24);
                 for (int s = 0; s < KS; ++s, ++c) {
-                    const uint32_t slot = c % kF16Slots, a = c & 1;
-                    mbar_wait(&full[slot], (c / kF16Slots) & 1, p.status);
+                    const uint32_t slot = c % kBSlots, a = c & 1;
+                    mbar_wait(&fullB[slot], (c / kBSlots) & 1, p.status);
                     mbar_wait(&a16f[a], (c >> 1) & 1, p.status);
                     tc_fence_after();
-                    const uint32_t sa = su32(a16 + a * kA16), sb = su32(smem + slot * kF16Slot + kF16RawA);
+                    const uint32_t sa = su32(a16 + a * kA16), sb = su32(ringB + slot * kF16B);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const uint64_t da = smem_desc(sa + j * 256, 128, 1024), db = smem_desc(sb + j * 256, 128, 1024);
@@ -245,13 +279,13 @@ __global__ void __launch_bounds__(kThreadsF16, 1) gemm16_kernel(F16Params p)
                                      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, q;\n\t}"
                                      ::"r"(d), "l"(da), "l"(db), "r"(idesc), "r"(acc) : "memory");
                     }
-                    tc_commit(&empty[slot]);
+                    tc_commit(&emptyB[slot]);
                     tc_commit(&a16e[a]);
                 }
                 tc_commit(&accf[buf]);
             }
         }
-    } else {
+    } else if (warp < 6) {
         // ================================================================ epilogue (warps 2..5)
         const int q = warp & 3;   // lane quarter this warp may access
         uint32_t it = 0, xb = 0;
