@@ -70,6 +70,8 @@ def lib():
             L.moe_oracle_layer.argtypes = [i, i, i, i, i, i, i, p, p, p, p, p, p, p, p, p, p, p, p, i]
             L.moe_oracle_stack.restype = i
             L.moe_oracle_stack.argtypes = [i, i, i, i, i, i, i, i, p, p, p, p, p, p, p, p, p, p, i]
+            L.moe_oracle_set_swiglu.restype = None
+            L.moe_oracle_set_swiglu.argtypes = [d, d, d]
             L.moe_oracle_router.restype = None
             L.moe_oracle_router.argtypes = [i, i, i, p, p, p, p]
             L.moe_oracle_mx_quantize.restype = None
@@ -179,6 +181,23 @@ def layer(fmt: int, H: int, I: int, E: int, k: int, t, x: np.ndarray, logits: np
     if rc != 0:
         raise ValueError("oracle layer: bad arguments")
     return out, idx, w
+
+
+class swiglu:
+    """Context manager: the SwiGLU form h = gc sigmoid(alpha gc) (uc + beta),
+    gc = min(g, limit), uc = clamp(u, -limit, limit), for the oracle calls
+    inside it; (1, inf, 0) -- the plain silu(g) u -- outside."""
+
+    def __init__(self, alpha: float = 1.0, limit: float = float("inf"), beta: float = 0.0):
+        self.args = (float(alpha), float(limit), float(beta))
+
+    def __enter__(self):
+        lib().moe_oracle_set_swiglu(*self.args)
+        return self
+
+    def __exit__(self, *exc):
+        lib().moe_oracle_set_swiglu(1.0, float("inf"), 0.0)
+        return False
 
 
 def router(x: np.ndarray, w: np.ndarray, b: np.ndarray | None = None) -> np.ndarray:

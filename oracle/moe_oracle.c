@@ -32,7 +32,9 @@
  *  - Nibble order: the low nibble of byte b holds element 2b, the high nibble
  *    element 2b+1; weights are row-major [N_out][K] with blocks along K.
  *  - gate_up rows [0, I) are gate, rows [I, 2I) are up; SwiGLU is
- *    silu(gate) * up with silu(g) = g / (1 + exp(-g)).
+ *    silu(gate) * up with silu(g) = g / (1 + exp(-g)) by default; the
+ *    clamped, alpha-scaled form of the public gpt-oss model is a setting
+ *    (moe_oracle_set_swiglu, below).
  *  - Stack coupling: x_l = bf16(r_l / sqrt(mean(r_l^2) + 1e-6)),
  *    r_{l+1} = bf16(r_l + MoE_l(x_l)), both roundings to nearest-even.
  *  - Batched path: x and h are quantised to MXFP4 per 32 elements along K
@@ -245,7 +247,30 @@ void moe_oracle_route(const float* logits, int M, int E, int k, int32_t* idx, do
 /* One routed-expert MoE layer                                               */
 /* ------------------------------------------------------------------------ */
 
-static double silu(double g) { return g / (1.0 + exp(-g)); }
+/* SwiGLU form: h = gc * sigmoid(alpha * gc) * (uc + beta), gc = min(g, limit),
+ * uc = clamp(u, -limit, limit) (a NaN stays NaN).  alpha = 1, limit = +inf,
+ * beta = 0 is the plain silu(g) * u.  The gpt-oss model's expert activation
+ * (its public reference implementation) is alpha = 1.702, limit = 7, beta = 1;
+ * the pages name the model but not its activation's constants. */
+static double sw_alpha = 1.0, sw_limit = INFINITY, sw_beta = 0.0;
+
+void moe_oracle_set_swiglu(double alpha, double limit, double beta)
+{
+    sw_alpha = alpha;
+    sw_limit = limit;
+    sw_beta = beta;
+}
+
+static double swiglu(double g, double u)
+{
+    if (g > sw_limit)
+        g = sw_limit;
+    if (u > sw_limit)
+        u = sw_limit;
+    if (u < -sw_limit)
+        u = -sw_limit;
+    return g / (1.0 + exp(-(sw_alpha * g))) * (u + sw_beta);
+}
 
 /* Sizes of one expert's tensors in elements / bytes. */
 static int64_t codes_bytes(int N, int K) { return (int64_t)N * K / 2; }
@@ -282,7 +307,7 @@ static void expert_mix(int fmt, int H, int I, int group, int k,
         const uint16_t* dnb = dn_bias ? dn_bias + e * H : NULL;
         gemv(fmt, guc, gus, gub, 2 * I, H, group, x, a, nthreads);      /* a = W_gu x + b_gu */
         for (int i = 0; i < I; ++i)
-            h[i] = silu(a[i]) * a[I + i];                              /* SwiGLU */
+            h[i] = swiglu(a[i], a[I + i]);                             /* SwiGLU */
         gemv(fmt, dnc, dns, dnb, H, I, group, h, y, nthreads);          /* y = W_d h + b_d */
         for (int j = 0; j < H; ++j)
             delta[j] += w[s] * y[j];                                   /* weighted combine */
@@ -479,7 +504,7 @@ void moe_oracle_mx_quantize(const double* v, int64_t n, uint8_t* codes, uint8_t*
 
 /* Batched MXFP4 layer with MX-quantised activations (the tensor-core path):
  *   x_q = MX(x)                          per token, blocks of 32 along H
- *   a   = W_gu x_q + b_gu;  h = silu(a[0:I]) * a[I:2I]
+ *   a   = W_gu x_q + b_gu;  h = SwiGLU(a[0:I], a[I:2I]) (the form set above)
  *   h_q = MX(h)                          blocks of 32 along I
  *   y   = W_d h_q + b_d;    out = r + sum_s w_s y_s
  * If h_codes_in / h_scales_in are non-NULL they replace the oracle's own h_q
@@ -526,7 +551,7 @@ int moe_oracle_layer_batched(int H, int I, int E, int M, int k,
                  gu_scales + e * scale_bytes(FMT_MXFP4, 2 * I, H, 32),
                  gu_bias ? gu_bias + e * 2 * I : NULL, 2 * I, H, 32, xq, a, nthreads);
             for (int i = 0; i < I; ++i)
-                h[i] = silu(a[i]) * a[I + i];
+                h[i] = swiglu(a[i], a[I + i]);
             int64_t slot = (int64_t)m * k + s;
             const uint8_t* hcu = hc;
             const uint8_t* hsu = hs;

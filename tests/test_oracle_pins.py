@@ -558,3 +558,83 @@ def test_stack_router_routes_on_the_normalised_input():
     lg = oracle.router(x, w, b).astype(np.float32)
     out, _, _ = oracle.layer(oracle.FMT_MXFP4, 128, 64, 8, 2, t, x, lg, r)
     assert np.array_equal(got, oracle.to_bf16_array(out))
+
+
+# ------------------------------------------------------------- SwiGLU forms
+
+def _tiny_layer(seed, bias=True):
+    shape = synth.Shape("swiglu pin", 64, 64, 4, 1, has_bias=bias, bias_sigma=0.5, seed=seed)
+    t = synth.layer_tensors(shape)
+    x, r, lg = synth.step_inputs(shape, 0, M=3, layers=1)
+    return shape, t, x, r, lg[0]
+
+
+def _layer(t, x, lg, r, k=1):
+    return oracle.layer(FMT_MXFP4, 64, 64, 4, k, t, x, lg, r)[0]
+
+
+def test_swiglu_default_is_the_plain_form():
+    _, t, x, r, lg = _tiny_layer(81)
+    plain = _layer(t, x, lg, r)
+    with oracle.swiglu(1.0, float("inf"), 0.0):
+        same = _layer(t, x, lg, r)
+    assert np.array_equal(plain, same)
+    with oracle.swiglu(1.702, 7.0, 1.0):
+        other = _layer(t, x, lg, r)
+    assert not np.allclose(plain, other)
+    assert np.array_equal(_layer(t, x, lg, r), plain)   # the context restores the default
+
+
+def test_swiglu_gate_clamp_makes_the_gate_weights_irrelevant():
+    """With every gate sum above the limit (a large gate bias), gc = limit for
+    every row, so replacing the gate codes changes nothing."""
+    _, t, x, r, lg = _tiny_layer(82)
+    t.gu_bias[:, :64] = synth.bf16_bits_from_f32(np.full((4, 64), 1.0e6, np.float32))
+    t2 = synth.layer_tensors(synth.Shape("swiglu pin", 64, 64, 4, 1, bias_sigma=0.5, seed=83))
+    u = t.gu_codes.copy()
+    u[:, :64] = t2.gu_codes[:, :64]   # other gate rows, the same up rows
+    tb = SimpleNamespace(**{**vars(t), "gu_codes": u})
+    with oracle.swiglu(1.702, 7.0, 1.0):
+        a = _layer(t, x, lg, r)
+        b = _layer(tb, x, lg, r)
+    assert np.array_equal(a, b)
+    # without the clamp the gate rows matter
+    assert not np.array_equal(_layer(t, x, lg, r), _layer(tb, x, lg, r))
+
+
+def test_swiglu_up_offset_is_linear():
+    """h(beta) = s(g) (u + beta) = s(g) u + beta s(g): the output moves by beta
+    times the layer whose up sums are zero and whose offset is 1."""
+    _, t, x, r, lg = _tiny_layer(84)
+    r0 = np.zeros_like(r)
+    t.dn_bias[:] = 0
+    t0 = SimpleNamespace(**vars(t))
+    t0.gu_codes = t.gu_codes.copy()
+    t0.gu_codes[:, 64:] = 0      # up rows: code 0 = +0
+    t0.gu_bias = t.gu_bias.copy()
+    t0.gu_bias[:, 64:] = 0
+    with oracle.swiglu(1.702, float("inf"), 0.0):
+        base = _layer(t, x, lg, r0)
+    with oracle.swiglu(1.702, float("inf"), 2.5):
+        shifted = _layer(t, x, lg, r0)
+    with oracle.swiglu(1.702, float("inf"), 1.0):
+        unit = _layer(t0, x, lg, r0)
+    np.testing.assert_allclose(shifted - base, 2.5 * unit, rtol=1e-9, atol=1e-12 * np.abs(base).max())
+
+
+def test_swiglu_up_clamp_is_symmetric():
+    """uc = clamp(u, -L, L): flipping the sign of every up weight and bias flips
+    the clamped up sums, so with beta = 0 the output flips sign."""
+    _, t, x, r, lg = _tiny_layer(85)
+    r0 = np.zeros_like(r)
+    t.dn_bias[:] = 0
+    tn = SimpleNamespace(**vars(t))
+    tn.gu_codes = t.gu_codes.copy()
+    up = tn.gu_codes[:, 64:]
+    tn.gu_codes[:, 64:] = up ^ 0x88        # both nibbles' sign bits
+    tn.gu_bias = t.gu_bias.copy()
+    tn.gu_bias[:, 64:] ^= 0x8000
+    with oracle.swiglu(1.702, 0.3, 0.0):   # a limit the up sums cross
+        a = _layer(t, x, lg, r0)
+        b = _layer(tn, x, lg, r0)
+    np.testing.assert_array_equal(a, -b)
