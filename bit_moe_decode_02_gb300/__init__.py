@@ -7,7 +7,7 @@ library fails loudly (build it with ``python -m bit_moe_decode_02_gb300.build_ex
 
 The function names are the C names: moe_create, moe_load_experts, moe_load_experts_ex,
 moe_forward, moe_forward_host, moe_forward_stack, moe_forward_stack_steps, moe_forward_steps,
-moe_load_router, moe_debug_router_logits, moe_set_batched_numerics, moe_get_status,
+moe_load_router, moe_debug_router_logits, moe_set_batched_numerics, moe_set_swiglu, moe_get_status,
 moe_debug_dequant, moe_debug_route, moe_debug_stack_trace, moe_debug_forward_f32,
 moe_debug_set_wait, moe_last_bytes, moe_expert_bytes, moe_last_launches, moe_last_error,
 moe_forward_noalloc, moe_debug_stream_weights, moe_destroy.
@@ -38,7 +38,7 @@ MOE_BATCHED_BF16 = 1
 # every symbol include/moe.h declares
 EXPORTS = ("moe_create", "moe_load_experts", "moe_load_experts_ex", "moe_forward", "moe_forward_host",
            "moe_forward_stack", "moe_forward_stack_steps", "moe_forward_steps", "moe_load_router",
-           "moe_debug_router_logits", "moe_set_batched_numerics", "moe_get_status", "moe_debug_dequant",
+           "moe_debug_router_logits", "moe_set_batched_numerics", "moe_set_swiglu", "moe_get_status", "moe_debug_dequant",
            "moe_debug_route",
            "moe_debug_stack_trace", "moe_debug_mx_quantize", "moe_debug_batched_h",
            "moe_debug_forward_f32", "moe_debug_set_wait",
@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
         L.moe_debug_stream_weights.restype = i
         L.moe_set_batched_numerics.argtypes = [p, i]
         L.moe_set_batched_numerics.restype = i
+        L.moe_set_swiglu.argtypes = [p, ctypes.c_float, ctypes.c_float, ctypes.c_float]
+        L.moe_set_swiglu.restype = i
         L.moe_forward.argtypes = [p, i, p, p, i, i, p, p]
         L.moe_forward.restype = i
         L.moe_forward_host.argtypes = [p, i, p, p, i, i, p, p]
@@ -205,6 +207,10 @@ def moe_load_router(h, layer, w, bias=None):
 
 def moe_debug_stream_weights(h, layer0, n, nbytes, stream=None):
     return _check(lib().moe_debug_stream_weights(h, layer0, n, nbytes, _stream(stream)))
+
+
+def moe_set_swiglu(h, alpha, limit, beta):
+    return _check(lib().moe_set_swiglu(h, alpha, limit, beta))
 
 
 def moe_set_batched_numerics(h, numerics):

@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -111,6 +112,7 @@ struct moe_handle {
     // cross-CTA waits of the decode kernels (moe_debug_set_wait)
     int spin_limit = moe::kSpinLimit;
     int skip_cta = -1;
+    float sw_alpha = 1.0f, sw_limit = INFINITY, sw_beta = 0.0f;   // the SwiGLU form (moe_set_swiglu)
     int last_steps = 0;        // layer calls of the last forward call: layers
     int last_first_layer = 0;  // last_first_layer, + 1, ... (mod L)
     int last_launches = 0;
@@ -211,6 +213,9 @@ moe::DecodeTcParams tc_params(const moe_handle* h, int layer0, int ncalls)
     const moe_config& c = h->cfg;
     moe::DecodeTcParams p{};
     p.resid_every = 1;
+    p.sw_alpha = h->sw_alpha;
+    p.sw_limit = h->sw_limit;
+    p.sw_beta = h->sw_beta;
     p.gu = h->arena;
     p.dn = h->arena + h->off_dn;
     p.layer_stride = (long long)h->layer_stride;
@@ -244,6 +249,9 @@ moe::DecodeI4Params i4_params(const moe_handle* h, int layer0, int ncalls)
     const moe_config& c = h->cfg;
     moe::DecodeI4Params p{};
     p.resid_every = 1;
+    p.sw_alpha = h->sw_alpha;
+    p.sw_limit = h->sw_limit;
+    p.sw_beta = h->sw_beta;
     p.gu = h->arena;
     p.dn = h->arena + h->off_dn;
     p.layer_stride = (long long)h->layer_stride;
@@ -421,6 +429,9 @@ moe::BatchParams batch_params(const moe_handle* h, int layer)
     p.I = c.intermediate;
     p.E = c.num_experts;
     p.max_tiles = h->max_tiles;
+    p.sw_alpha = h->sw_alpha;
+    p.sw_limit = h->sw_limit;
+    p.sw_beta = h->sw_beta;
     return p;
 }
 
@@ -1004,6 +1015,18 @@ int moe_set_batched_numerics(moe_handle* h, int numerics)
             return cuda_fail(e, "bf16 batched kernel set-up");
     }
     h->b_f16 = numerics == MOE_BATCHED_BF16 ? 1 : 0;
+    return MOE_OK;
+}
+
+int moe_set_swiglu(moe_handle* h, float alpha, float limit, float beta)
+{
+    if (!h)
+        return fail(MOE_ERR_INVALID_ARG, "moe_set_swiglu: handle is NULL");
+    if (!std::isfinite(alpha) || !(limit > 0.0f) || std::isnan(limit) || !std::isfinite(beta))
+        return fail(MOE_ERR_INVALID_ARG, "moe_set_swiglu: alpha and beta must be finite and limit > 0 (or +inf)");
+    h->sw_alpha = alpha;
+    h->sw_limit = limit;
+    h->sw_beta = beta;
     return MOE_OK;
 }
 

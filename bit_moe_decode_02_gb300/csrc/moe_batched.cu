@@ -275,6 +275,7 @@ struct GemmParams {
     uint8_t* hq;            // DUAL: MX(h) codes in the down GEMM's activation tile order
     uint8_t* hsf;           // DUAL: MX(h) scale chunks
     int* status;
+    float sw_alpha, sw_limit, sw_beta;   // DUAL: the SwiGLU form
 };
 
 constexpr int kStageSteps = 8;           // k-steps (64 of K) per pipeline stage
@@ -532,7 +533,7 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(GemmParams p)
                             break;
                         const float gg = (gate ? v16[jj] : theirs[jj]) + bg;
                         const float uu = (gate ? theirs[jj] : v16[8 + jj]) + bu;
-                        const float v = gg / (1.0f + expf(-gg)) * uu;
+                        const float v = swiglu(gg, uu, p.sw_alpha, p.sw_limit, p.sw_beta);
                         const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
                         const int ef = (int)(amax >> 23);
                         const uint32_t sbyte = ef > 2 ? (uint32_t)(ef - 2) : 0u;
@@ -772,6 +773,9 @@ cudaError_t launch_batched(const BatchParams& p, int grid, cudaStream_t s, int* 
     g.hq = p.hq;
     g.hsf = p.hsf;
     g.status = p.status;
+    g.sw_alpha = p.sw_alpha;
+    g.sw_limit = p.sw_limit;
+    g.sw_beta = p.sw_beta;
     if ((e = launch_gemm<true>(g, grid, s)) != cudaSuccess)
         return e;
     g.w = p.dn;

@@ -67,6 +67,7 @@ struct F16Params {
     float* out;             // single: y [slots][rows] fp32
     uint8_t* h16;           // DUAL: h as hi/lo rows of the down GEMM's activation tiles
     int* status;
+    float sw_alpha, sw_limit, sw_beta;   // DUAL: the SwiGLU form
 };
 
 // Byte offset of element (row r, column k) of a bf16 activation tile whose
@@ -326,7 +327,7 @@ __global__ void __launch_bounds__(kThreadsF16, 1) gemm16_kernel(F16Params p)
                             break;
                         const float gg = (gate ? v16[jj] : theirs[jj]) + bg;
                         const float uu = (gate ? theirs[jj] : v16[8 + jj]) + bu;
-                        const float v = gg / (1.0f + expf(-gg)) * uu;
+                        const float v = swiglu(gg, uu, p.sw_alpha, p.sw_limit, p.sw_beta);
                         const uint16_t hi = f2bf16_rne(v);
                         const uint16_t lo = f2bf16_rne(v - bf16f(hi));
                         *reinterpret_cast<uint16_t*>(hb + act16_off(2 * tile.npad, n, hrow)) = hi;
@@ -403,6 +404,9 @@ cudaError_t launch_batched_f16_gemms(const BatchParams& b, int grid, cudaStream_
     g.bias_stride = 2 * b.I;
     g.h16 = b.h16;
     g.status = b.status;
+    g.sw_alpha = b.sw_alpha;
+    g.sw_limit = b.sw_limit;
+    g.sw_beta = b.sw_beta;
     gemm16_kernel<true><<<grid, kThreadsF16, kF16Smem, s>>>(g);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;

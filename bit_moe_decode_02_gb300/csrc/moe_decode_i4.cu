@@ -500,7 +500,7 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                             gg += bf16f(__ldg(gub + (size_t)e * 2 * I + 64 * t + r));
                             uu += bf16f(__ldg(gub + (size_t)e * 2 * I + I + 64 * t + r));
                         }
-                        hv = wt != 0.f ? wt * (gg / (1.0f + expf(-gg))) * uu : 0.f;
+                        hv = wt != 0.f ? wt * swiglu(gg, uu, p.sw_alpha, p.sw_limit, p.sw_beta) : 0.f;
                     }
                     uint32_t mx = __float_as_uint(fabsf(hv));
                     mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 4));

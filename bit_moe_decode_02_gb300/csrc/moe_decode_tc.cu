@@ -1123,7 +1123,8 @@ __device__ __forceinline__ void decode_call(const int call)
                     // a token that did not choose this expert gets exactly 0 (its sums may
                     // even be infinite: the expert's weights were applied to every column)
                     const float gg = g[kb][m] + bg[kb], wt = sh.wslot[s][m];
-                    hv[m] = m < M && wt != 0.f ? wt * (gg / (1.0f + expf(-gg))) * (u[kb][m] + bu[kb]) : 0.f;
+                    hv[m] = m < M && wt != 0.f ? wt * swiglu(gg, u[kb][m] + bu[kb], p.sw_alpha, p.sw_limit, p.sw_beta)
+                                               : 0.f;
                 }
                 switch (M) {
                 case 1: warp_terms_rows<1>(hv, 0, kb, hb, hb + 1024, atom, lane); break;
@@ -1157,7 +1158,7 @@ __device__ __forceinline__ void decode_call(const int call)
                 for (int m = 0; m < kMaxTokens; ++m) {
                     // 0 for a token that did not choose this expert, whatever its sums
                     const float g = sm[m] + bg, wt = sh.wslot[s][m];
-                    hv[m] = m < M && wt != 0.f ? wt * (g / (1.0f + expf(-g))) * (us[m] + bu) : 0.f;
+                    hv[m] = m < M && wt != 0.f ? wt * swiglu(g, us[m] + bu, p.sw_alpha, p.sw_limit, p.sw_beta) : 0.f;
                 }
                 switch (M) {   // one copy of the code runs
                 case 1: warp_terms_rows<1>(hv, 0, q, dst, dst + 1024, atom, lane); break;

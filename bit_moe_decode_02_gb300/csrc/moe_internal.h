@@ -116,6 +116,7 @@ struct BatchParams {
     int f16;
     uint8_t* x16;
     uint8_t* h16;
+    float sw_alpha, sw_limit, sw_beta;   // the SwiGLU form (alpha, limit, offset; 1, +inf, 0: plain)
 };
 
 // Enqueue the batched layer (route, plan, quantise x, gate_up GEMM + SwiGLU +
@@ -167,6 +168,7 @@ struct DecodeTcParams {
     float* out_f32;             // [M][H] fp32 result before the bf16 rounding per call, or nullptr
     long long logits_stride, x_stride, resid_stride, out_f32_stride;
     int resid_every;            // calls per residual buffer: call c uses resid + (c / resid_every) * resid_stride
+    float sw_alpha, sw_limit, sw_beta;   // the SwiGLU form (alpha, limit, offset; 1, +inf, 0: plain)
     int ncalls, layer0, nlayers;
     float* part;                // [G][H][4] each CTA's fp32 copy of the expert output
     uint8_t* xt;                // x terms of the layer: [H/64][N rows x 32 B][ceil(H/128)][512]
@@ -220,6 +222,7 @@ struct DecodeI4Params {
     float* out_f32;
     long long logits_stride, x_stride, resid_stride, out_f32_stride;
     int resid_every;            // calls per residual buffer: call c uses resid + (c / resid_every) * resid_stride
+    float sw_alpha, sw_limit, sw_beta;   // the SwiGLU form (alpha, limit, offset; 1, +inf, 0: plain)
     int ncalls, layer0, nlayers;
     float* part;                // [G][H][4] each CTA's fp32 copy of the expert output
     unsigned long long* done;   // [1] grid-barrier arrivals (only grows)

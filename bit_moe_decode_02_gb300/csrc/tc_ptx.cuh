@@ -157,6 +157,21 @@ __device__ __forceinline__ void tc_ld8(uint32_t taddr, float (&v)[8])
 
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// The SwiGLU form h = gc sigmoid(alpha gc) (uc + beta), gc = min(g, limit),
+// uc = clamp(u, -limit, limit) (a NaN passes through).  alpha = 1, limit =
+// +inf, beta = 0 is the plain silu(g) u, and gives its bits: -(1 g) = -g,
+// u + 0 = u.
+__device__ __forceinline__ float swiglu(float g, float u, float alpha, float limit, float beta)
+{
+    if (g > limit)
+        g = limit;
+    if (u > limit)
+        u = limit;
+    if (u < -limit)
+        u = -limit;
+    return g / (1.0f + expf(-(alpha * g))) * (u + beta);
+}
+
 // Grid-wide signalling through global counters and flags (gpu scope).
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p)
 {

@@ -190,6 +190,18 @@ int moe_load_router(moe_handle* h, int layer, const void* w_bf16, const void* bi
 int moe_forward(moe_handle* h, int layer, const void* x_bf16, const float* router_logits,
                 int M, int top_k, void* out_bf16, void* stream);
 
+/* The SwiGLU form of every forward on this handle (decode, int4, batched, the
+ * stack), from the next call on:
+ *   h = gc * sigmoid(alpha * gc) * (uc + beta),
+ *   gc = min(g, limit), uc = clamp(u, -limit, limit),
+ * with g, u the gate and up sums (bias included).  The default (1, +inf, 0)
+ * is the plain silu(g) * u of the pages' layer; the expert activation of the
+ * gpt-oss model in its public reference implementation is (1.702, 7, 1) --
+ * the pages name the model, not these constants.  alpha and beta finite,
+ * limit > 0 (+inf for no clamp); else MOE_ERR_INVALID_ARG.
+ * moe_forward_noalloc always takes the plain form. */
+int moe_set_swiglu(moe_handle* h, float alpha, float limit, float beta);
+
 /* Numerics of the batched path (M > 4) on this handle:
  *   MOE_BATCHED_MXFP4 (default): tcgen05.mma kind::mxf4 -- x and h quantised
  *     to MXFP4 per 32 along K (the OCP MX rule), as that instruction needs;
