@@ -1092,7 +1092,32 @@ __device__ __forceinline__ void decode_call(const int call)
             // gate (rows r) and up (rows 64 + r) sums of both 32-row blocks, every
             // piece's loads in flight together, added in piece order
             float g[2][kMaxTokens] = {}, u[2][kMaxTokens] = {};
-            for (int p0 = 0; p0 < pl.S; p0 += 4) {
+            if (M == 1) {
+                // token 0 only: one scalar per (piece, block, gate / up), eight pieces'
+                // loads in flight together (one round trip for the usual S <= 8)
+                for (int p0 = 0; p0 < pl.S; p0 += 8) {
+                    float v[8][4];
+#pragma unroll
+                    for (int z = 0; z < 8; ++z)
+                        if (p0 + z < pl.S) {
+                            const float* src = p.gpart + (size_t)(b0 + p0 + z) * kRowTile * 4;
+#pragma unroll
+                            for (int kb = 0; kb < 2; ++kb) {
+                                v[z][2 * kb] = __ldcg(src + (32 * kb + lane) * 4);
+                                v[z][2 * kb + 1] = __ldcg(src + (64 + 32 * kb + lane) * 4);
+                            }
+                        }
+#pragma unroll
+                    for (int z = 0; z < 8; ++z)
+                        if (p0 + z < pl.S)
+#pragma unroll
+                            for (int kb = 0; kb < 2; ++kb) {
+                                g[kb][0] += v[z][2 * kb];
+                                u[kb][0] += v[z][2 * kb + 1];
+                            }
+                }
+            }
+            for (int p0 = 0; M > 1 && p0 < pl.S; p0 += 4) {
                 float4 v[4][4];
 #pragma unroll
                 for (int z = 0; z < 4; ++z)
