@@ -421,9 +421,7 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                 const int ngu = (KS + kGuSeg - 1) / kGuSeg;
                 for (int st = 0; st < ngu; ++st, ++st_count) {
                     const uint32_t slot = st_count % nslots;
-                    if (lane == 0)   // one poller a warp; the warp's other lanes follow its acquire
-                        mbar_wait(&si.full[slot], (st_count / nslots) & 1, p.status);
-                    __syncwarp();
+                    mbar_wait(&si.full[slot], (st_count / nslots) & 1, p.status);
                     const uint8_t* sp = i4ring + slot * kI4Slot;
                     const int q0 = st * kGuSeg, n = min(kGuSeg, KS - q0);
                     for (int qi = half; qi < n; qi += 2) {
@@ -545,9 +543,7 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                 const int ndn = (NSL + kDnSlabs - 1) / kDnSlabs;
                 for (int st = 0; st < ndn; ++st, ++st_count) {
                     const uint32_t slot = st_count % nslots;
-                    if (lane == 0)   // one poller a warp; the warp's other lanes follow its acquire
-                        mbar_wait(&si.full[slot], (st_count / nslots) & 1, p.status);
-                    __syncwarp();
+                    mbar_wait(&si.full[slot], (st_count / nslots) & 1, p.status);
                     const uint8_t* sp = i4ring + slot * kI4Slot;
                     const int s0 = st * kDnSlabs, n = min(kDnSlabs, NSL - s0);
                     for (int si2 = warp; si2 < n; si2 += kCw) {
