@@ -235,8 +235,8 @@ struct DecodeI4Params {
     long long router_stride;
     float* rlog;
 };
-constexpr int kI4Slot = 18432;    // one stage: up to 16 KB of codes, then up to 2 KB of scales
-constexpr int kI4Codes = 16384;
+constexpr int kI4Slot = 36864;    // one stage: up to 32 KB of codes, then up to 4 KB of scales
+constexpr int kI4Codes = 32768;
 // bytes of one unit (64 rows of h) of gate/up (proj 0) or down (proj 1)
 long long i4_unit_bytes(int H, int group, int proj);
 size_t decode_i4_static_smem();
