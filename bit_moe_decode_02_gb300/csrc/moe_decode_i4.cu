@@ -26,7 +26,7 @@
 // of one 64-column segment (word j: k16 step j; register i of it = nibbles i
 // and i + 4), and an SB-byte entry holds the fp16 scales of rows g and g + 8
 // (SB = 8 when group is 32: both 32-element blocks of the segment).  One bulk
-// copy moves a stage of a unit: up to 8 gate/up segments or 64 down slabs (32 KB:
+// copy moves a stage of a unit: up to 16 gate/up segments or 128 down slabs (64 KB:
 // smaller bulk copies stream markedly slower per SM).
 //
 // Warps 0..15 compute: on a gate/up stage warp w takes slab w mod 8 and every
@@ -57,8 +57,8 @@ using namespace tc;
 constexpr int kCw = 16;                    // compute warps (4 per SM sub-partition)
 constexpr int kThreadsI4 = (kCw + 1) * 32; // + the producer warp
 constexpr int kProdWarp = kCw;
-constexpr int kGuSeg = 8;                  // segments per gate/up stage (32 KB of codes)
-constexpr int kDnSlabs = 64;               // slabs per down stage (32 KB of codes)
+constexpr int kGuSeg = 16;                 // segments per gate/up stage (64 KB of codes)
+constexpr int kDnSlabs = 128;              // slabs per down stage (64 KB of codes)
 static_assert(kGuSeg * 4096 <= kI4Codes && kDnSlabs * 512 <= kI4Codes, "a stage's codes fit a slot");
 static_assert(kGuSeg * 64 * 8 <= kI4Slot - kI4Codes && kDnSlabs * 8 * 8 <= kI4Slot - kI4Codes,
               "a stage's scale entries fit a slot");

@@ -235,8 +235,8 @@ struct DecodeI4Params {
     long long router_stride;
     float* rlog;
 };
-constexpr int kI4Slot = 36864;    // one stage: up to 32 KB of codes, then up to 4 KB of scales
-constexpr int kI4Codes = 32768;
+constexpr int kI4Slot = 73728;    // one stage: up to 64 KB of codes, then up to 8 KB of scales
+constexpr int kI4Codes = 65536;
 // bytes of one unit (64 rows of h) of gate/up (proj 0) or down (proj 1)
 long long i4_unit_bytes(int H, int group, int proj);
 size_t decode_i4_static_smem();
