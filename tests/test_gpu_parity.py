@@ -279,6 +279,31 @@ def test_layer_parity_full_size(moe, shape, M):
         moe.moe_destroy(h)
 
 
+MAX_HIDDEN = [
+    synth.Shape("max hidden MXFP4 H=3072 I=192 E=6 top-2", 3072, 192, 6, 2, e8m0_lo=118, e8m0_hi=124,
+                bias_sigma=0.3, seed=43),
+    synth.Shape("max hidden int4 H=3072 I=192 E=6 top-2 g32 bias", 3072, 192, 6, 2, fmt=synth.FMT_INT4,
+                group=32, has_bias=True, bias_sigma=0.1, seed=44),
+]
+
+
+@pytest.mark.parametrize("shape", MAX_HIDDEN, ids=lambda s: s.name)
+@pytest.mark.parametrize("M", [1, 4])
+def test_layer_parity_max_hidden(moe, shape, M):
+    """The largest hidden size a handle takes (3072): the decode kernels' shared
+    memory then holds the fewest stages next to the largest x / output tail, and
+    the int4 gate/up stream ends in a partial 64 KB stage (48 segments)."""
+    t = synth.layer_tensors(shape)
+    h = create_handle(shape)
+    try:
+        load_layer(h, 0, t)
+        for step in range(2):
+            x, r, logits = synth.step_inputs(shape, 70 + step, M=M, layers=1)
+            _check_both(moe, h, shape, t, x, r, logits[0], shape.top_k, f"{shape.name} M={M} step={step}")
+    finally:
+        moe.moe_destroy(h)
+
+
 def test_forward_host_equals_forward_and_is_deterministic(moe):
     shape = synth.GPTOSS_LAYER
     t = synth.layer_tensors(shape)
