@@ -29,10 +29,12 @@
 // copy moves a stage of a unit: up to 16 gate/up segments or 128 down slabs (64 KB:
 // smaller bulk copies stream markedly slower per SM).
 //
-// Warps 0..15 compute: on a gate/up stage warp w takes slab w mod 8 and every
+// 16 warps compute: on a gate/up stage warp w takes slab w mod 8 and every
 // other segment of the stage (w / 8 picks which; the two halves' sums are added
-// in a fixed order), on a down stage slabs w, w + 16, ...; warp 16 streams the
-// stages.  x enters as f16 after an exact power-of-two rescale per token (its
+// in a fixed order), on a down stage slabs w, w + 16, ...  No warp is kept for
+// the stream: thread 0 fills the stage ring when a call starts, and the last
+// warp to finish with a stage refills its slot (a 17th warp would cap the
+// registers at 96: one scheduler would hold five warps).  x enters as f16 after an exact power-of-two rescale per token (its
 // largest magnitude to [2^14, 2^15)); h' = w h as f16 hi + lo after a
 // power-of-two rescale per (unit, token).  Products and sums are fp32.
 //
@@ -54,9 +56,8 @@ namespace {
 
 using namespace tc;
 
-constexpr int kCw = 16;                    // compute warps (4 per SM sub-partition)
-constexpr int kThreadsI4 = (kCw + 1) * 32; // + the producer warp
-constexpr int kProdWarp = kCw;
+constexpr int kCw = 16;                    // compute warps (4 per SM sub-partition); no producer
+constexpr int kThreadsI4 = kCw * 32;       // warp: the last warp out of a stage issues the next
 constexpr int kGuSeg = 16;                 // segments per gate/up stage (64 KB of codes)
 constexpr int kDnSlabs = 128;              // slabs per down stage (64 KB of codes)
 static_assert(kGuSeg * 4096 <= kI4Codes && kDnSlabs * 512 <= kI4Codes, "a stage's codes fit a slot");
@@ -128,8 +129,8 @@ __device__ __forceinline__ int ilog2f(float v)
 }
 
 struct I4Smem {
-    uint64_t full[kMaxSlotsI4], empty[kMaxSlotsI4];
-    uint64_t routed;
+    uint64_t full[kMaxSlotsI4];
+    unsigned done[kMaxSlotsI4];           // warps finished with each slot's stages (only grows)
     int sel[kMaxTokens][kMaxTopK];
     float wt[kMaxTokens][kMaxTopK];
     int nu;
@@ -177,9 +178,8 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
     if (tid == 0) {
         for (int i = 0; i < nslots; ++i) {
             mbar_init(&si.full[i], 1);
-            mbar_init(&si.empty[i], kCw);
+            si.done[i] = 0u;
         }
-        mbar_init(&si.routed, 1);
         si.stages = 0;
         for (int m = 0; m < kMaxTokens; ++m)
             si.hmax[0][m] = si.hmax[1][m] = 0u;
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
         const uint16_t* dnb = p.dn_bias ? reinterpret_cast<const uint16_t*>(
             reinterpret_cast<const uint8_t*>(p.dn_bias) + (long long)layer * p.bias_stride) : nullptr;
 
-        if (warp < kCw) {
+        {
             // ---- token statistics (warp 4 + m: token m): largest |x|, and 1 / rms for
             // the normalised input
             if (warp >= 4 && warp - 4 < M) {
@@ -315,7 +315,6 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                 __syncwarp();
                 if (lane == 0) {
                     si.nu = nu;
-                    mbar_arrive(&si.routed);   // the producer may start
                 }
             }
             // x as f16: x 2^S per token (S from the largest |x|), exact for every
@@ -353,8 +352,6 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                 }
             }
             cw_barrier();
-        } else {
-            mbar_wait(&si.routed, call & 1, p.status);
         }
 
         const int nu = si.nu, U = nu * T1;
@@ -362,59 +359,56 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
         if (b == 0 && tid == 0 && p.nu_out)
             p.nu_out[layer] = nu;
 
-        if (warp == kProdWarp) {
-            // ================================================================ producer
-            const uint64_t wpol = l2_evict_first();
-            for (int u = u0; u < u1; ++u) {
-                const int e = si.unit_expert[u / T1], t = u % T1;
-                const uint8_t* gsrc = gu + (long long)e * p.gu_expert + (long long)t * gu_unit;
-                const uint8_t* dsrc = dn + (long long)e * p.dn_expert + (long long)t * dn_unit;
-                const int ngu = (KS + kGuSeg - 1) / kGuSeg, ndn = (NSL + kDnSlabs - 1) / kDnSlabs;
-                // Stages go out in batches, one lane each: lane 0 waits until stage st's
-                // slot is free, then every stage of the next nslots whose slot is
-                // already free (a non-blocking test; a slot is tested only against its
-                // previous use, which is at most one phase behind) is issued at once.
-                // At a call's start the whole ring is free, so the first batch fills it.
-                const int ntot = ngu + ndn;
-                for (int st = 0; st < ntot;) {
-                    if (lane == 0 && st_count >= (uint32_t)nslots)
-                        mbar_wait(&si.empty[st_count % nslots], ((st_count / nslots) - 1) & 1, p.status);
-                    __syncwarp();
-                    const uint32_t k = st_count + (uint32_t)lane;
-                    bool ready = lane < nslots && st + lane < ntot;
-                    if (ready && lane > 0 && k >= (uint32_t)nslots)
-                        ready = mbar_test_wait(&si.empty[k % nslots], ((k / nslots) - 1) & 1);
-                    const uint32_t rb = __ballot_sync(0xffffffffu, ready);
-                    const int nb = __ffs(~rb) - 1;   // the ready prefix (lane 0 is ready)
-                    if (lane < nb) {
-                        const int sl = st + lane;
-                        const uint32_t slot = k % nslots;
-                        uint32_t cb, sb2;
-                        const uint8_t *csrc, *ssrc;
-                        if (sl < ngu) {
-                            const int q0 = sl * kGuSeg, n = min(kGuSeg, KS - q0);
-                            cb = (uint32_t)n * 4096;
-                            sb2 = (uint32_t)n * 64 * SB;
-                            csrc = gsrc + (long long)q0 * 4096;
-                            ssrc = gsrc + (long long)KS * 4096 + (long long)q0 * 64 * SB;
-                        } else {
-                            const int s0 = (sl - ngu) * kDnSlabs, n = min(kDnSlabs, NSL - s0);
-                            cb = (uint32_t)n * 512;
-                            sb2 = (uint32_t)n * 8 * SB;
-                            csrc = dsrc + (long long)s0 * 512;
-                            ssrc = dsrc + (long long)NSL * 512 + (long long)s0 * 8 * SB;
-                        }
-                        uint8_t* dst = i4ring + slot * kI4Slot;
-                        mbar_expect_tx(&si.full[slot], cb + sb2);
-                        bulk_copy_hint(dst, csrc, cb, &si.full[slot], wpol);
-                        bulk_copy_hint(dst + kI4Codes, ssrc, sb2, &si.full[slot], wpol);
-                    }
-                    st += nb;
-                    st_count += (uint32_t)nb;
-                    __syncwarp();
-                }
+        // ---- the stage stream: stage j of this call (unit u0 + j / nsu, its gate/up
+        // stages then its down stages) goes into slot (call_base + j) mod nslots.
+        // Thread 0 fills the ring at the call's start; after that, the last warp to
+        // finish with a slot's stage issues the stage nslots further on into it.
+        const int ngu = (KS + kGuSeg - 1) / kGuSeg, ndn = (NSL + kDnSlabs - 1) / kDnSlabs, nsu = ngu + ndn;
+        const int ntot = (u1 - u0) * nsu;
+        const uint32_t call_base = st_count;
+        auto issue = [&](int j) {
+            const int u = u0 + j / nsu, sl = j % nsu;
+            const int e = si.unit_expert[u / T1], t = u % T1;
+            const uint8_t* gsrc = gu + (long long)e * p.gu_expert + (long long)t * gu_unit;
+            const uint8_t* dsrc = dn + (long long)e * p.dn_expert + (long long)t * dn_unit;
+            uint32_t cb, sb2;
+            const uint8_t *csrc, *ssrc;
+            if (sl < ngu) {
+                const int q0 = sl * kGuSeg, n = min(kGuSeg, KS - q0);
+                cb = (uint32_t)n * 4096;
+                sb2 = (uint32_t)n * 64 * SB;
+                csrc = gsrc + (long long)q0 * 4096;
+                ssrc = gsrc + (long long)KS * 4096 + (long long)q0 * 64 * SB;
+            } else {
+                const int s0 = (sl - ngu) * kDnSlabs, n = min(kDnSlabs, NSL - s0);
+                cb = (uint32_t)n * 512;
+                sb2 = (uint32_t)n * 8 * SB;
+                csrc = dsrc + (long long)s0 * 512;
+                ssrc = dsrc + (long long)NSL * 512 + (long long)s0 * 8 * SB;
             }
-        } else {
+            const uint32_t slot = (call_base + (uint32_t)j) % nslots;
+            uint8_t* dst = i4ring + slot * kI4Slot;
+            const uint64_t wpol = l2_evict_first();
+            mbar_expect_tx(&si.full[slot], cb + sb2);
+            bulk_copy_hint(dst, csrc, cb, &si.full[slot], wpol);
+            bulk_copy_hint(dst + kI4Codes, ssrc, sb2, &si.full[slot], wpol);
+        };
+        // a warp is through with the stage in `slot`: the last of the kCw refills it
+        auto release = [&](uint32_t slot) {
+            __syncwarp();
+            if (lane == 0) {
+                unsigned prev;
+                asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
+                             : "=r"(prev) : "r"(su32(&si.done[slot])) : "memory");
+                const int j = (int)(st_count - call_base) + nslots;
+                if ((prev + 1u) % kCw == 0u && j < ntot)
+                    issue(j);
+            }
+        };
+        if (tid == 0)
+            for (int j = 0; j < ntot && j < nslots; ++j)
+                issue(j);
+        {
             // ================================================================ compute warps
             for (int u = u0; u < u1; ++u) {
                 const int s = u / T1, t = u % T1, e = si.unit_expert[s];
@@ -422,7 +416,6 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                 // 64t + 16 ((w & 7) - 4)) and the even (w < 8) or odd segments of each stage
                 const int slab = warp & 7, half = warp >> 3;
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                const int ngu = (KS + kGuSeg - 1) / kGuSeg;
                 for (int st = 0; st < ngu; ++st, ++st_count) {
                     const uint32_t slot = st_count % nslots;
                     mbar_wait(&si.full[slot], (st_count / nslots) & 1, p.status);
@@ -474,9 +467,7 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                         acc[2] = fmaf(d1[2], sh1, acc[2]);
                         acc[3] = fmaf(d1[3], sh1, acc[3]);
                     }
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&si.empty[slot]);
+                    release(slot);
                 }
                 // rows 16 slab + g and + 8 of the unit's 128 (gate 0..63, up 64..127), tokens
                 // 2 t4, 2 t4 + 1, for this warp's K half
@@ -545,7 +536,6 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                     const float hm = m < kMaxTokens ? __uint_as_float(si.hmax[hb][m]) : 0.f;
                     hinv[c] = hm > 0.f ? pow2_mul(1.f, ilog2f(hm) - 14) : 0.f;
                 }
-                const int ndn = (NSL + kDnSlabs - 1) / kDnSlabs;
                 for (int st = 0; st < ndn; ++st, ++st_count) {
                     const uint32_t slot = st_count % nslots;
                     mbar_wait(&si.full[slot], (st_count / nslots) & 1, p.status);
@@ -591,9 +581,7 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                             }
                         }
                     }
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&si.empty[slot]);
+                    release(slot);
                 }
             }
             cw_barrier();
