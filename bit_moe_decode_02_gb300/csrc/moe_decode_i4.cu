@@ -208,6 +208,40 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
         const uint16_t* dnb = p.dn_bias ? reinterpret_cast<const uint16_t*>(
             reinterpret_cast<const uint8_t*>(p.dn_bias) + (long long)layer * p.bias_stride) : nullptr;
 
+        // ---- the stage stream: stage j of this call (unit u0 + j / nsu, its gate/up
+        // stages then its down stages) goes into slot (call_base + j) mod nslots.
+        // Lane 0 of warp 0 fills the ring as soon as the routing is known; after
+        // that, the last warp to finish with a slot's stage issues the stage nslots
+        // further on into it.
+        const int ngu = (KS + kGuSeg - 1) / kGuSeg, ndn = (NSL + kDnSlabs - 1) / kDnSlabs, nsu = ngu + ndn;
+        const uint32_t call_base = st_count;
+        auto issue = [&](int j, int ufirst) {
+            const int u = ufirst + j / nsu, sl = j % nsu;
+            const int e = si.unit_expert[u / T1], t = u % T1;
+            const uint8_t* gsrc = gu + (long long)e * p.gu_expert + (long long)t * gu_unit;
+            const uint8_t* dsrc = dn + (long long)e * p.dn_expert + (long long)t * dn_unit;
+            uint32_t cb, sb2;
+            const uint8_t *csrc, *ssrc;
+            if (sl < ngu) {
+                const int q0 = sl * kGuSeg, n = min(kGuSeg, KS - q0);
+                cb = (uint32_t)n * 4096;
+                sb2 = (uint32_t)n * 64 * SB;
+                csrc = gsrc + (long long)q0 * 4096;
+                ssrc = gsrc + (long long)KS * 4096 + (long long)q0 * 64 * SB;
+            } else {
+                const int s0 = (sl - ngu) * kDnSlabs, n = min(kDnSlabs, NSL - s0);
+                cb = (uint32_t)n * 512;
+                sb2 = (uint32_t)n * 8 * SB;
+                csrc = dsrc + (long long)s0 * 512;
+                ssrc = dsrc + (long long)NSL * 512 + (long long)s0 * 8 * SB;
+            }
+            const uint32_t slot = (call_base + (uint32_t)j) % nslots;
+            uint8_t* dst = i4ring + slot * kI4Slot;
+            const uint64_t wpol = l2_evict_first();
+            mbar_expect_tx(&si.full[slot], cb + sb2);
+            bulk_copy_hint(dst, csrc, cb, &si.full[slot], wpol);
+            bulk_copy_hint(dst + kI4Codes, ssrc, sb2, &si.full[slot], wpol);
+        };
         {
             // ---- token statistics (warp 4 + m: token m): largest |x|, and 1 / rms for
             // the normalised input
@@ -315,6 +349,11 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                 __syncwarp();
                 if (lane == 0) {
                     si.nu = nu;
+                    // the ring's first stages go out now, ahead of the x conversion
+                    const int Uq = nu * T1;
+                    const int uf = (int)((long long)b * Uq / G), ul = (int)((long long)(b + 1) * Uq / G);
+                    for (int j = 0; j < (ul - uf) * nsu && j < nslots; ++j)
+                        issue(j, uf);
                 }
             }
             // x as f16: x 2^S per token (S from the largest |x|), exact for every
@@ -359,40 +398,7 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
         if (b == 0 && tid == 0 && p.nu_out)
             p.nu_out[layer] = nu;
 
-        // ---- the stage stream: stage j of this call (unit u0 + j / nsu, its gate/up
-        // stages then its down stages) goes into slot (call_base + j) mod nslots.
-        // Thread 0 fills the ring at the call's start; after that, the last warp to
-        // finish with a slot's stage issues the stage nslots further on into it.
-        const int ngu = (KS + kGuSeg - 1) / kGuSeg, ndn = (NSL + kDnSlabs - 1) / kDnSlabs, nsu = ngu + ndn;
         const int ntot = (u1 - u0) * nsu;
-        const uint32_t call_base = st_count;
-        auto issue = [&](int j) {
-            const int u = u0 + j / nsu, sl = j % nsu;
-            const int e = si.unit_expert[u / T1], t = u % T1;
-            const uint8_t* gsrc = gu + (long long)e * p.gu_expert + (long long)t * gu_unit;
-            const uint8_t* dsrc = dn + (long long)e * p.dn_expert + (long long)t * dn_unit;
-            uint32_t cb, sb2;
-            const uint8_t *csrc, *ssrc;
-            if (sl < ngu) {
-                const int q0 = sl * kGuSeg, n = min(kGuSeg, KS - q0);
-                cb = (uint32_t)n * 4096;
-                sb2 = (uint32_t)n * 64 * SB;
-                csrc = gsrc + (long long)q0 * 4096;
-                ssrc = gsrc + (long long)KS * 4096 + (long long)q0 * 64 * SB;
-            } else {
-                const int s0 = (sl - ngu) * kDnSlabs, n = min(kDnSlabs, NSL - s0);
-                cb = (uint32_t)n * 512;
-                sb2 = (uint32_t)n * 8 * SB;
-                csrc = dsrc + (long long)s0 * 512;
-                ssrc = dsrc + (long long)NSL * 512 + (long long)s0 * 8 * SB;
-            }
-            const uint32_t slot = (call_base + (uint32_t)j) % nslots;
-            uint8_t* dst = i4ring + slot * kI4Slot;
-            const uint64_t wpol = l2_evict_first();
-            mbar_expect_tx(&si.full[slot], cb + sb2);
-            bulk_copy_hint(dst, csrc, cb, &si.full[slot], wpol);
-            bulk_copy_hint(dst + kI4Codes, ssrc, sb2, &si.full[slot], wpol);
-        };
         // a warp is through with the stage in `slot`: the last of the kCw refills it
         auto release = [&](uint32_t slot) {
             __syncwarp();
@@ -402,12 +408,9 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                              : "=r"(prev) : "r"(su32(&si.done[slot])) : "memory");
                 const int j = (int)(st_count - call_base) + nslots;
                 if ((prev + 1u) % kCw == 0u && j < ntot)
-                    issue(j);
+                    issue(j, u0);
             }
         };
-        if (tid == 0)
-            for (int j = 0; j < ntot && j < nslots; ++j)
-                issue(j);
         {
             // ================================================================ compute warps
             for (int u = u0; u < u1; ++u) {
