@@ -183,10 +183,13 @@ int moe_load_router(moe_handle* h, int layer, const void* w_bf16, const void* bi
  * batched path: per-expert grouped GEMMs on the tensor cores
  * (tcgen05.mma kind::mxf4) with x and h quantised to MXFP4 per 32 along K by
  * the OCP MX v1.0 rule (shared exponent floor(log2 amax) - 2, E2M1 nearest-
- * even with saturation); seven launches.  Grouped-expert GEMM batching is
- * the lever "Sovereign gpt-oss-20B (MXFP4) on Apple Silicon", section 5,
- * names as untried; the activation quantisation is this library's reading
- * (the tensor-core instruction needs FP4 on both sides). */
+ * even with saturation); six launches (route, plan, quantise x, the gate_up
+ * and down GEMMs, combine), seven when the router weights compute the
+ * logits.  moe_set_batched_numerics(MOE_BATCHED_BF16) swaps the quantised
+ * GEMMs for kind::f16 ones on weights dequantised to bf16.  Grouped-expert
+ * GEMM batching is the lever "Sovereign gpt-oss-20B (MXFP4) on Apple
+ * Silicon", section 5, names as untried; the activation quantisation is this
+ * library's reading (the tensor-core instruction needs FP4 on both sides). */
 int moe_forward(moe_handle* h, int layer, const void* x_bf16, const float* router_logits,
                 int M, int top_k, void* out_bf16, void* stream);
 
