@@ -32,7 +32,7 @@
 // 16 warps compute: on a gate/up stage warp w takes slab w mod 8 and every
 // other segment of the stage (w / 8 picks which; the two halves' sums are added
 // in a fixed order), on a down stage slabs w, w + 16, ...  No warp is kept for
-// the stream: thread 0 fills the stage ring when a call starts, and the last
+// the stream: thread 0 fills the stage ring once a call is routed, and the last
 // warp to finish with a stage refills its slot (a 17th warp would cap the
 // registers at 96: one scheduler would hold five warps).  x enters as f16 after an exact power-of-two rescale per token (its
 // largest magnitude to [2^14, 2^15)); h' = w h as f16 hi + lo after a
