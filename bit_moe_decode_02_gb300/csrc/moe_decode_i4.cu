@@ -210,9 +210,9 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
 
         // ---- the stage stream: stage j of this call (unit u0 + j / nsu, its gate/up
         // stages then its down stages) goes into slot (call_base + j) mod nslots.
-        // Lane 0 of warp 0 fills the ring as soon as the routing is known; after
-        // that, the last warp to finish with a slot's stage issues the stage nslots
-        // further on into it.
+        // Lane 0 of warp 0 issues the first stage as soon as the routing is known
+        // and fills the ring once x is converted; after that, the last warp to
+        // finish with a slot's stage issues the stage nslots further on into it.
         const int ngu = (KS + kGuSeg - 1) / kGuSeg, ndn = (NSL + kDnSlabs - 1) / kDnSlabs, nsu = ngu + ndn;
         const uint32_t call_base = st_count;
         auto issue = [&](int j, int ufirst) {
@@ -349,11 +349,12 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                 __syncwarp();
                 if (lane == 0) {
                     si.nu = nu;
-                    // the ring's first stages go out now, ahead of the x conversion
+                    // the ring's first stage goes out now, ahead of the x conversion; the
+                    // others wait until its reads of x are done (they would queue behind)
                     const int Uq = nu * T1;
                     const int uf = (int)((long long)b * Uq / G), ul = (int)((long long)(b + 1) * Uq / G);
-                    for (int j = 0; j < (ul - uf) * nsu && j < nslots; ++j)
-                        issue(j, uf);
+                    if ((ul - uf) * nsu > 0)
+                        issue(0, uf);   // the rest once the x conversion's reads are done
                 }
             }
             // x as f16: x 2^S per token (S from the largest |x|), exact for every
@@ -379,6 +380,12 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
             for (int i = tid; i < H * V; i += kCw * 32)
                 oacc[i] = 0.f;
             cw_barrier();
+            if (tid == 0) {
+                const int Uq = si.nu * T1;
+                const int uf = (int)((long long)b * Uq / G), ul = (int)((long long)(b + 1) * Uq / G);
+                for (int j = 1; j < (ul - uf) * nsu && j < nslots; ++j)
+                    issue(j, uf);
+            }
             if (warp == 1) {
                 const int nu = si.nu;
                 for (int x = lane; x < nu * kMaxTokens; x += 32)
