@@ -1490,7 +1490,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(const DecodeTc
 
     // warm L2 and the TLB for what the first steps read once the previous grid
     // is complete (a prefetch returns no data, so it cannot see a stale value)
-    if (warp == 2 && lane < M)
+    if (warp == 2 && lane < M && p.logits)   // (the in-kernel router has no given logits)
         prefetch_l2(p.logits + (size_t)lane * p.E);
     if (warp >= 3 && warp <= 5 && b < nitems) {
         const int it = b + G * (warp - 3);
