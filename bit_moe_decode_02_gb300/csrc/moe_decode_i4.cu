@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                     mbar_wait(&si.full[slot], (st_count / nslots) & 1, p.status);
                     const uint8_t* sp = i4ring + slot * kI4Slot;
                     const int q0 = st * kGuSeg, n = min(kGuSeg, KS - q0);
-#pragma unroll 4
+#pragma unroll 8
                     for (int qi = half; qi < n; qi += 2) {
                         const int q = q0 + qi;
                         const uint4 cw = *reinterpret_cast<const uint4*>(sp + qi * 4096 + slab * 512 + lane * 16);
@@ -551,7 +551,7 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
                     mbar_wait(&si.full[slot], (st_count / nslots) & 1, p.status);
                     const uint8_t* sp = i4ring + slot * kI4Slot;
                     const int s0 = st * kDnSlabs, n = min(kDnSlabs, NSL - s0);
-#pragma unroll 4
+#pragma unroll 8
                     for (int si2 = warp; si2 < n; si2 += kCw) {
                         const int sl = s0 + si2;
                         const uint4 cw = *reinterpret_cast<const uint4*>(sp + si2 * 512 + lane * 16);
