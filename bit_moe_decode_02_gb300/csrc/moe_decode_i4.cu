@@ -142,7 +142,6 @@ struct I4Smem {
     int xsh[kMaxTokens];                  // power-of-two shift of x per token
     unsigned hmax[2][kMaxTokens];         // largest |h'| per token of a unit (two units alternate)
     float fin[kFinI4][4];
-    uint32_t stages;                      // stages streamed so far (producer) / consumed (compute)
 };
 
 // Shared memory past the ring: x as f16 [M][H + 8], the unit's gate/up sums of
@@ -180,7 +179,6 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
             mbar_init(&si.full[i], 1);
             si.done[i] = 0u;
         }
-        si.stages = 0;
         for (int m = 0; m < kMaxTokens; ++m)
             si.hmax[0][m] = si.hmax[1][m] = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -188,7 +186,7 @@ __global__ void __launch_bounds__(kThreadsI4, 1) decode_i4_kernel(const DecodeI4
     __syncthreads();
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    uint32_t st_count = 0;   // ring position (producer: stages issued; compute warps: consumed)
+    uint32_t st_count = 0;   // stages of the launch consumed so far: the ring position (same on every thread)
     int ubase = 0;           // whole units done by this CTA in earlier calls (h' buffers alternate)
 #pragma unroll 1
     for (int call = 0; call < p.ncalls; ++call) {
