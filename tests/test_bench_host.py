@@ -77,3 +77,21 @@ def test_stored_traffic_only_for_the_hashed_kernel(tmp_path, monkeypatch):
     fresh = dict(rec, kernel_hash="f" * 16)
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(fresh))
     assert bench.stored_traffic() == rec["dram_bytes_per_forward"]
+
+
+def test_tensor_peaks_follow_the_measured_bf16_figure(tmp_path, monkeypatch):
+    """The batched figures' tensor peaks: the measured cuBLAS bf16 burst figure
+    (MEASURED_PEAKS.json) for the bf16 numerics, and it times 13.5 / 2.25 (the
+    dense FP4 to bf16 ratio of the nominal GB300 rates) for the MXFP4 one; the
+    stated fallback without a measurement."""
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    bf, src = bench._bf16_peak()
+    fp, src4 = bench._fp4_peak()
+    assert bf == 1900.0 and "fallback" in src
+    assert fp == pytest.approx(1900.0 * 6.0) and "fallback" in src4
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6700.0, "bf16_tflops": 2000.0}))
+    bf, src = bench._bf16_peak()
+    fp, src4 = bench._fp4_peak()
+    assert bf == 2000.0 and "measured" in src
+    assert fp == pytest.approx(12000.0) and "measured" in src4
+    assert bench.measured_peaks() == (6700.0, "measured")
