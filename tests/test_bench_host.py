@@ -1,6 +1,6 @@
 """Host logic of bench.py, no GPU: the max-over-ranks timing reduction on two
-gloo ranks, the reference arm's rank rule, and the kernel hash that keys the
-stored ncu traffic."""
+gloo ranks, the reference arm's rank rule, the kernel hash that keys the
+stored ncu traffic, and the peaks the figures are reported against."""
 import json
 import os
 import socket
